@@ -1,0 +1,208 @@
+"""CPU oracle for the FP32 row reductions: TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline may import this package.  The product path (the CUDA library and its
+Python binding) never imports it and shares no code with it.
+
+Wraps ``oracle.c`` (plain serial C): the FP64 definitions of softmax, RMSNorm,
+LayerNorm and cross-entropy, and the bit-exact FP32 emulation of the ordered
+fixed-tree policy (OT-1024) with its own exp/log.  Arrays are numpy; inputs
+are float32 (labels int64) row-major, FP64 outputs are returned as float64 and
+emulated outputs as float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+# -ffp-contract=off: no a*b+c fusion (the emulation must round every op);
+# no -ffast-math; -O2 keeps IEEE semantics.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+          "-fno-fast-math", "-fno-finite-math-only", "-Wall"]
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so next to its source (gcc, a second or so)."""
+    stale = (not os.path.exists(_LIB) or
+             os.path.getmtime(_LIB) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        i64 = ctypes.c_int64
+        sig = {
+            "oracle_softmax_f64": [f32p, f64p, i64, i64],
+            "oracle_rmsnorm_f64": [f32p, f32p, f64p, i64, i64, ctypes.c_float],
+            "oracle_layernorm_f64": [f32p, f32p, f32p, f64p, i64, i64, ctypes.c_float],
+            "oracle_cross_entropy_f64": [f32p, i64p, f64p, i64, i64],
+            "ot_softmax_f32": [f32p, f32p, i64, i64],
+            "ot_rmsnorm_f32": [f32p, f32p, f32p, i64, i64, ctypes.c_float],
+            "ot_layernorm_f32": [f32p, f32p, f32p, f32p, i64, i64, ctypes.c_float],
+            "ot_cross_entropy_f32": [f32p, i64p, f32p, i64, i64],
+            "ot_sum_f32": [f32p, i64],
+            "ot_max_f32": [f32p, i64],
+        }
+        for name, args in sig.items():
+            fn = getattr(_lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_float if name in ("ot_sum_f32", "ot_max_f32") else ctypes.c_int
+        for name in ("ot_expf", "ot_logf"):
+            fn = getattr(_lib, name)
+            fn.argtypes = [ctypes.c_float]
+            fn.restype = ctypes.c_float
+        for name in ("ot_expf_n", "ot_logf_n"):
+            fn = getattr(_lib, name)
+            fn.argtypes = [f32p, f32p, i64]
+            fn.restype = None
+    return _lib
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _rc(code):
+    if code != 0:
+        raise ValueError("oracle rejected the sizes")
+
+
+# --- FP64 definitions ------------------------------------------------------
+
+def softmax(x):
+    x = _f32(x)
+    r, c = x.shape
+    y = np.empty((r, c), np.float64)
+    _rc(lib().oracle_softmax_f64(_ptr(x, ctypes.c_float), _ptr(y, ctypes.c_double), r, c))
+    return y
+
+
+def rmsnorm(x, w=None, eps=1e-5):
+    x = _f32(x)
+    w = None if w is None else _f32(w)
+    r, c = x.shape
+    y = np.empty((r, c), np.float64)
+    _rc(lib().oracle_rmsnorm_f64(_ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float),
+                                 _ptr(y, ctypes.c_double), r, c, eps))
+    return y
+
+
+def layernorm(x, gamma=None, beta=None, eps=1e-5):
+    x = _f32(x)
+    gamma = None if gamma is None else _f32(gamma)
+    beta = None if beta is None else _f32(beta)
+    r, c = x.shape
+    y = np.empty((r, c), np.float64)
+    _rc(lib().oracle_layernorm_f64(_ptr(x, ctypes.c_float), _ptr(gamma, ctypes.c_float),
+                                   _ptr(beta, ctypes.c_float), _ptr(y, ctypes.c_double),
+                                   r, c, eps))
+    return y
+
+
+def cross_entropy(logits, labels):
+    x = _f32(logits)
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    r, c = x.shape
+    loss = np.empty(r, np.float64)
+    _rc(lib().oracle_cross_entropy_f64(_ptr(x, ctypes.c_float), _ptr(lab, ctypes.c_int64),
+                                       _ptr(loss, ctypes.c_double), r, c))
+    return loss
+
+
+# --- OT-1024 emulation -----------------------------------------------------
+
+def ot_softmax(x):
+    x = _f32(x)
+    r, c = x.shape
+    y = np.empty((r, c), np.float32)
+    _rc(lib().ot_softmax_f32(_ptr(x, ctypes.c_float), _ptr(y, ctypes.c_float), r, c))
+    return y
+
+
+def ot_rmsnorm(x, w=None, eps=1e-5):
+    x = _f32(x)
+    w = None if w is None else _f32(w)
+    r, c = x.shape
+    y = np.empty((r, c), np.float32)
+    _rc(lib().ot_rmsnorm_f32(_ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float),
+                             _ptr(y, ctypes.c_float), r, c, eps))
+    return y
+
+
+def ot_layernorm(x, gamma=None, beta=None, eps=1e-5):
+    x = _f32(x)
+    gamma = None if gamma is None else _f32(gamma)
+    beta = None if beta is None else _f32(beta)
+    r, c = x.shape
+    y = np.empty((r, c), np.float32)
+    _rc(lib().ot_layernorm_f32(_ptr(x, ctypes.c_float), _ptr(gamma, ctypes.c_float),
+                               _ptr(beta, ctypes.c_float), _ptr(y, ctypes.c_float), r, c, eps))
+    return y
+
+
+def ot_cross_entropy(logits, labels):
+    x = _f32(logits)
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    r, c = x.shape
+    loss = np.empty(r, np.float32)
+    _rc(lib().ot_cross_entropy_f32(_ptr(x, ctypes.c_float), _ptr(lab, ctypes.c_int64),
+                                   _ptr(loss, ctypes.c_float), r, c))
+    return loss
+
+
+def ot_sum(v):
+    v = _f32(v).ravel()
+    return np.float32(lib().ot_sum_f32(_ptr(v, ctypes.c_float), v.size))
+
+
+def ot_max(v):
+    v = _f32(v).ravel()
+    return np.float32(lib().ot_max_f32(_ptr(v, ctypes.c_float), v.size))
+
+
+def ot_expf(x):
+    return np.float32(lib().ot_expf(float(x)))
+
+
+def ot_logf(x):
+    return np.float32(lib().ot_logf(float(x)))
+
+
+def ot_expf_array(x):
+    x = _f32(x).ravel()
+    y = np.empty_like(x)
+    lib().ot_expf_n(_ptr(x, ctypes.c_float), _ptr(y, ctypes.c_float), x.size)
+    return y
+
+
+def ot_logf_array(x):
+    x = _f32(x).ravel()
+    y = np.empty_like(x)
+    lib().ot_logf_n(_ptr(x, ctypes.c_float), _ptr(y, ctypes.c_float), x.size)
+    return y
