@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP32 row-reduction hot path on one GB300 (or N replicas).
+
+Metric: achieved HBM GB/s (algorithmic bytes / time) and microseconds per op.
+Default workload: softmax, RMSNorm and LayerNorm at 768 x 6144 (x ~ N(0,1),
+weight ~ U(0.5,1.5), bias ~ N(0,0.1), eps 1e-5, seed 2), each under the
+unordered and the ordered (OT-1024) policy: one step = these 6 launches, each
+on its own input and output buffers. Inputs are resident in HBM when timing
+starts; 2 rotating buffer sets (453 MB) keep every launch's data out of L2.
+
+The timed region replays a CUDA graph of unrolled steps (event-record nodes
+between launches give every kernel's duration inside the timed region).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--suite]
+
+``--impl reference`` times the CPU oracle (serial FP64 definitions and the
+OT-1024 emulation) on a bounded row sample of the same workload.
+``--suite`` prints one line per workload (every configuration) and exits.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "achieved HBM GB/s and µs/op per op×shape on 1 GB300 (fraction of ~8 TB/s)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# workload name -> list of (op, synth workload, order)
+TRIO = [("softmax", "softmax_768x6144"), ("rmsnorm", "rmsnorm_768x6144"), ("layernorm", "layernorm_768x6144")]
+WORKLOADS = {
+    "trio_768x6144": [(op, w, o) for o in ("unordered", "ordered") for op, w in TRIO],
+}
+for _name, _w in synth.WORKLOADS.items():
+    WORKLOADS[_name] = [(_w["op"], _name, "unordered")]
+    if _name.endswith("768x6144"):
+        WORKLOADS[_name + "_ordered"] = [(_w["op"], _name, "ordered")]
+DEFAULT_WORKLOAD = "trio_768x6144"
+
+
+def alg_bytes(op, rows, cols):
+    """Algorithmic bytes of one launch: every input read once, every output written once."""
+    e = rows * cols
+    return {"softmax": 8 * e, "rmsnorm": 8 * e + 4 * cols, "layernorm": 8 * e + 8 * cols,
+            "cross_entropy": 4 * e + 12 * rows}[op]
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "fp32_row_reduction_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        v = float(json.load(open(p))["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(p))
+    except Exception:
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    ent = rec.get("launches", {}).get(key)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [t.strip() for t in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]) if f[3] not in ("[N/A]", "") else 0.0, f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        maxp = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * maxp] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded), "power_w_max": maxp}
+
+
+# ----------------------------------------------------------------- our arm
+
+class Launch:
+    """One launch of the step: op, policy, its input/output buffer sets."""
+
+    def __init__(self, op, workload, order, sets, device):
+        import fp32_row_reduction_gb300 as tr
+        self.tr = tr
+        self.op, self.workload, self.order = op, workload, order
+        w = synth.WORKLOADS[workload]
+        self.rows, self.cols = w["rows"], w["cols"]
+        base = synth.workload_inputs(workload, device=device)
+        self.inputs = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(sets - 1)]
+        if op == "cross_entropy":
+            self.outputs = [torch.empty(self.rows, device=device) for _ in range(sets)]
+        else:
+            self.outputs = [torch.empty_like(base["x"]) for _ in range(sets)]
+        self.bytes = alg_bytes(op, self.rows, self.cols)
+        self.key = f"{op}/{self.order}/{self.rows}x{self.cols}"
+
+    def __call__(self, s, stream=None):
+        self.tr.run_op(self.op, self.inputs[s], out=self.outputs[s], order=self.order, stream=stream)
+
+    def plan(self):
+        return self.tr.plan_for(self.op, self.rows, self.cols, self.order)
+
+
+def pick_sets(launches_bytes, l2=126 << 20):
+    per_set = sum(launches_bytes)
+    return max(2, math.ceil(2 * l2 / per_set))
+
+
+def build_graph(launches, steps, sets, first_set, timing):
+    """Capture `steps` unrolled steps; returns (graph, events[step][k]) with per-launch events."""
+    g = torch.cuda.CUDAGraph()
+    evs = []
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(steps):
+            s = (first_set + i) % sets
+            row = []
+            for ln in launches:
+                if timing:
+                    e = torch.cuda.Event(enable_timing=True, external=True)
+                    e.record()
+                    row.append(e)
+                ln(s)
+            if timing:
+                e = torch.cuda.Event(enable_timing=True, external=True)
+                e.record()
+                row.append(e)
+            evs.append(row)
+    return g, evs
+
+
+def run_ours(args, rank, world):
+    import fp32_row_reduction_gb300 as tr
+    tr.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    specs = WORKLOADS[args.workload]
+    probe = [alg_bytes(op, synth.WORKLOADS[w]["rows"], synth.WORKLOADS[w]["cols"]) for op, w, _ in specs]
+    sets = pick_sets(probe)
+    launches = [Launch(op, w, o, sets, dev) for op, w, o in specs]
+    step_bytes = sum(ln.bytes for ln in launches)
+    torch.cuda.synchronize()
+
+    # warm-up (eager: also fills the plan cache before capture)
+    for i in range(max(args.warmup, 1)):
+        for ln in launches:
+            ln(i % sets)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    U = min(K, args.unroll)
+    rem = K % U
+    g_main, ev_main = build_graph(launches, U, sets, 0, timing=True)
+    g_rem = build_graph(launches, rem, sets, U % sets, timing=False)[0] if rem else None
+    g_main.replay()  # graph warm-up
+    torch.cuda.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(K // U):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t1.record()
+        t1.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    # per-launch durations: the events of the last replay of the unrolled graph
+    per = [[] for _ in launches]
+    for row in ev_main:
+        for k in range(len(launches)):
+            per[k].append(row[k].elapsed_time(row[k + 1]))
+    per_us = [1e3 * statistics.mean(v) for v in per]
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    e2e = measure_e2e(launches, args, dev) if rank == 0 else None
+    cpu = cpu_baseline(launches, args) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank != 0:
+        return None
+
+    peak, peak_kind = measured_peak()
+    dom = max(range(len(launches)), key=lambda k: per_us[k])
+    dl = launches[dom]
+    achieved = dl.bytes / (per_us[dom] * 1e-6) / 1e9
+    per_op = {}
+    for k, ln in enumerate(launches):
+        per_op[ln.key] = {"us": round(per_us[k], 3), "gbs": round(ln.bytes / (per_us[k] * 1e3), 1),
+                          "frac_of_peak": round(ln.bytes / (per_us[k] * 1e3) / peak, 4),
+                          "alg_bytes": ln.bytes, "plan": ln.plan()}
+    value = world * K * step_bytes / (elapsed_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "launches_per_step": len(launches),
+                   "shapes": sorted({f"{ln.rows}x{ln.cols}" for ln in launches}),
+                   "policies": sorted({ln.order for ln in launches}),
+                   "l2": f"inputs larger than L2: {sets} rotating buffer sets of "
+                         f"{sum(ln.bytes for ln in launches) / 1e6:.0f} MB per step",
+                   "timing": "CUDA graph of unrolled steps, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dl.key, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic_record(dl.key), "alg_bytes_per_launch": dl.bytes,
+                     "launch_us": round(per_us[dom], 3)},
+        "per_op": per_op,
+        "e2e": e2e,
+        "gpu_launches": K * len(launches),
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+def measure_e2e(launches, args, dev):
+    """Same metric through the public API with pinned HOST buffers: H2D of each
+    launch's inputs, the launches, D2H of the outputs, all inside the timed region."""
+    host_in = [{k: v.cpu().pin_memory() for k, v in ln.inputs[0].items()} for ln in launches]
+    host_out = [ln.outputs[0].cpu().pin_memory() for ln in launches]
+    h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    steps = max(3, min(args.e2e_steps, args.steps))
+
+    def one(s):
+        for k, ln in enumerate(launches):
+            for name, t in host_in[k].items():
+                ln.inputs[s][name].copy_(t, non_blocking=True)
+            ln(s)
+            host_out[k].copy_(ln.outputs[s], non_blocking=True)
+
+    for i in range(2):
+        one(i % len(launches[0].inputs))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i % len(launches[0].inputs))
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    step_bytes = sum(ln.bytes for ln in launches)
+    return {"value": round(steps * step_bytes / dt / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(1e3 * dt / steps, 4)}
+
+
+# ------------------------------------------------------------ the oracle
+
+def oracle_fn(op, order):
+    import oracle
+    if order == "ordered":
+        return {"softmax": lambda h: oracle.ot_softmax(h["x"]),
+                "rmsnorm": lambda h: oracle.ot_rmsnorm(h["x"], h["w"], 1e-5),
+                "layernorm": lambda h: oracle.ot_layernorm(h["x"], h["w"], h["b"], 1e-5),
+                "cross_entropy": lambda h: oracle.ot_cross_entropy(h["x"], h["labels"])}[op]
+    return {"softmax": lambda h: oracle.softmax(h["x"]),
+            "rmsnorm": lambda h: oracle.rmsnorm(h["x"], h["w"], 1e-5),
+            "layernorm": lambda h: oracle.layernorm(h["x"], h["w"], h["b"], 1e-5),
+            "cross_entropy": lambda h: oracle.cross_entropy(h["x"], h["labels"])}[op]
+
+
+def host_sample(op, workload, rows):
+    w = synth.WORKLOADS[workload]
+    d = synth.make_inputs(op, min(rows, w["rows"]), w["cols"], w["seed"], var=w.get("var"),
+                          row_offset=w.get("row_offset", False))
+    return {k: v.numpy() for k, v in d.items()}
+
+
+def time_oracle(specs, rows_per_launch, budget_s=None, repeats=1):
+    """Run the oracle over `rows_per_launch` rows of every launch of the step."""
+    samples = [(oracle_fn(op, o), host_sample(op, w, rows_per_launch), op, w) for op, w, o in specs]
+    done_bytes, t_total, reps = 0, 0.0, 0
+    while True:
+        t0 = time.perf_counter()
+        for fn, h, op, _ in samples:
+            fn(h)
+        t_total += time.perf_counter() - t0
+        reps += 1
+        done_bytes += sum(alg_bytes(op, h["x"].shape[0], h["x"].shape[1]) for _, h, op, _ in samples)
+        if budget_s is None and reps >= repeats:
+            break
+        if budget_s is not None and t_total >= budget_s:
+            break
+    return done_bytes, t_total, reps
+
+
+def cpu_baseline(launches, args):
+    specs = [(ln.op, ln.workload, ln.order) for ln in launches]
+    rows = min(ln.rows for ln in launches)
+    sample_rows = min(rows, args.cpu_rows)
+    b, t, reps = time_oracle(specs, sample_rows, budget_s=args.cpu_seconds)
+    return {"value": round(b / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{sample_rows} rows of each of the {len(specs)} launches' inputs, {reps} passes, "
+                      f"{t:.1f} s (serial FP64 C oracle / OT-1024 C emulation, one thread)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    specs = WORKLOADS[args.workload]
+    # size each step so the whole --warmup + --steps run stays within ~2 minutes
+    b1, t1, _ = time_oracle(specs, 1, repeats=1)
+    per_row = max(t1, 1e-5)
+    rows = int(max(1, min(768, 120.0 / (args.steps + args.warmup) / per_row)))
+    samples = [(oracle_fn(op, o), host_sample(op, w, rows), op) for op, w, o in specs]
+    step_bytes = sum(alg_bytes(op, h["x"].shape[0], h["x"].shape[1]) for _, h, op in samples)
+    for _ in range(args.warmup):
+        for fn, h, _ in samples:
+            fn(h)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for fn, h, _ in samples:
+            fn(h)
+    dt = time.perf_counter() - t0
+    value = args.steps * step_bytes / dt / 1e9
+    sample = f"{rows} rows of each of the {len(specs)} launches' inputs per step (serial C oracle, one thread)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_suite(args):
+    """One line per workload: µs/op, GB/s and plan (no graph; events around batched launches)."""
+    import fp32_row_reduction_gb300 as tr
+    tr.load()
+    dev = torch.device("cuda", 0)
+    peak, _ = measured_peak()
+    names = [n for n in WORKLOADS if n != DEFAULT_WORKLOAD] if args.workload == DEFAULT_WORKLOAD \
+        else [args.workload]
+    for name in names:
+        specs = WORKLOADS[name]
+        op, w, order = specs[0]
+        b = alg_bytes(op, synth.WORKLOADS[w]["rows"], synth.WORKLOADS[w]["cols"])
+        sets = pick_sets([b])
+        ln = Launch(op, w, order, sets, dev)
+        for i in range(args.warmup):
+            ln(i % sets)
+        torch.cuda.synchronize()
+        n = max(20, min(2000, int(2e9 / max(b, 1))))
+        g, _ = build_graph([ln], n, sets, 0, timing=False)
+        g.replay()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        g.replay()
+        t1.record()
+        t1.synchronize()
+        us = 1e3 * t0.elapsed_time(t1) / n
+        print(json.dumps({"workload": name, "op": op, "order": order, "rows": ln.rows, "cols": ln.cols,
+                          "us_per_op": round(us, 3), "gbs": round(b / (us * 1e3), 1),
+                          "frac_of_peak": round(b / (us * 1e3) / peak, 4), "alg_bytes": b, "launches": n,
+                          "l2": f"{sets} rotating buffer sets", "plan": ln.plan()}), flush=True)
+        del ln, g
+        torch.cuda.empty_cache()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--unroll", type=int, default=100, help="steps per captured graph")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-rows", type=int, default=96)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--suite", action="store_true", help="one line per workload, then exit")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 alone runs it; other ranks exit without work
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    try:
+        if args.suite:
+            run_suite(args)
+            return
+        line = run_ours(args, rank, world)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

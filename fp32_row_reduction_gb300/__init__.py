@@ -1,0 +1,278 @@
+"""GB300-native FP32 row reductions: Python binding of libtr (ctypes).
+
+The binding only marshals arguments: every operator runs in libtr's CUDA
+kernels on the GPU. There is no CPU or PyTorch fallback: if libtr.so is
+missing, importing the library functions raises, and on a machine without a
+GPU the calls return TR_ERR_CUDA.
+
+Two layers:
+
+* the C-ABI, same names and arguments as ``include/tr.h``
+  (``tr_softmax_f32(x_ptr, y_ptr, rows, cols, order, stream)`` ...), taking
+  integer device pointers and returning a ``tr_status`` int;
+* tensor helpers (``softmax``, ``rmsnorm``, ``layernorm``, ``cross_entropy``)
+  that take CUDA float32 tensors, allocate the output with PyTorch (PyTorch is
+  used for device memory and streams only) and raise ``TrError`` on failure.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtr.so")
+
+TR_OK = 0
+TR_ERR_INVALID_ARG = 1
+TR_ERR_UNSUPPORTED = 2
+TR_ERR_CUDA = 3
+TR_ERR_DEVICE_TIMEOUT = 4
+
+TR_ORDER_UNORDERED_TREE = 0
+TR_ORDER_ORDERED_TREE = 1
+
+TR_OP_SOFTMAX = 0
+TR_OP_RMSNORM = 1
+TR_OP_LAYERNORM = 2
+TR_OP_CROSS_ENTROPY = 3
+
+TR_PLAN_ROWS = 0
+TR_PLAN_CLUSTER = 1
+TR_PLAN_STREAM = 2
+TR_PLAN_XENT = 3
+TR_PLAN_ORDERED = 4
+
+OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LAYERNORM,
+       "cross_entropy": TR_OP_CROSS_ENTROPY}
+ORDERS = {"unordered": TR_ORDER_UNORDERED_TREE, "ordered": TR_ORDER_ORDERED_TREE}
+
+
+class tr_plan(ctypes.Structure):
+    _fields_ = [
+        ("op", ctypes.c_int32), ("order", ctypes.c_int32), ("kind", ctypes.c_int32),
+        ("lanes_per_row", ctypes.c_int32), ("warps_per_row", ctypes.c_int32),
+        ("rows_per_cta", ctypes.c_int32), ("cluster_ctas", ctypes.c_int32),
+        ("vec_slots", ctypes.c_int32), ("block_threads", ctypes.c_int32),
+        ("ctas_per_sm", ctypes.c_int32), ("grid_ctas", ctypes.c_int64), ("est_us", ctypes.c_double),
+        ("candidates", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+
+
+class tr_device_desc(ctypes.Structure):
+    _fields_ = [
+        ("sm_count", ctypes.c_int32), ("max_threads_per_sm", ctypes.c_int32),
+        ("max_ctas_per_sm", ctypes.c_int32), ("regs_per_sm", ctypes.c_int32),
+        ("smem_per_sm", ctypes.c_int32), ("max_cluster_ctas", ctypes.c_int32),
+        ("l2_bytes", ctypes.c_int64), ("hbm_gbs", ctypes.c_double),
+    ]
+
+
+def gb300_device_desc() -> tr_device_desc:
+    """The GB300 as the plan selector models it (152 SMs, 2048 threads, 64K registers)."""
+    return tr_device_desc(sm_count=152, max_threads_per_sm=2048, max_ctas_per_sm=32,
+                          regs_per_sm=65536, smem_per_sm=233472, max_cluster_ctas=8,
+                          l2_bytes=126 << 20, hbm_gbs=7000.0)
+
+
+# The exported C-ABI and its argument types.
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_F = ctypes.c_float
+SIGNATURES = {
+    "tr_softmax_f32": ([_P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_rmsnorm_f32": ([_P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
+    "tr_layernorm_f32": ([_P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
+    "tr_cross_entropy_f32": ([_P, _P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_plan_describe": ([_I32, _I64, _I64, _I32, ctypes.POINTER(tr_plan)], _I32),
+    "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
+                            ctypes.POINTER(tr_plan)], _I32),
+    "tr_plan_override": ([ctypes.POINTER(tr_plan)], _I32),
+    "tr_last_device_error": ([], _I32),
+    "tr_status_string": ([_I32], ctypes.c_char_p),
+    "tr_last_error_message": ([], ctypes.c_char_p),
+    "tr_version": ([], _I32),
+}
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libtr.so (built by ``fp32_row_reduction_gb300.build``). Raises if missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"libtr.so not found at {p}: build it with `python -m fp32_row_reduction_gb300.build` "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+class TrError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = load()
+        msg = lib.tr_last_error_message().decode()
+        super().__init__(f"{where}: {lib.tr_status_string(status).decode()} ({msg})")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != TR_OK:
+        raise TrError(status, where)
+
+
+# --------------------------------------------------------------------- C-ABI
+
+def tr_softmax_f32(x, y, rows, cols, order, stream):
+    return load().tr_softmax_f32(x, y, rows, cols, order, stream)
+
+
+def tr_rmsnorm_f32(x, w, y, rows, cols, eps, order, stream):
+    return load().tr_rmsnorm_f32(x, w, y, rows, cols, eps, order, stream)
+
+
+def tr_layernorm_f32(x, gamma, beta, y, rows, cols, eps, order, stream):
+    return load().tr_layernorm_f32(x, gamma, beta, y, rows, cols, eps, order, stream)
+
+
+def tr_cross_entropy_f32(logits, labels, losses, rows, cols, order, stream):
+    return load().tr_cross_entropy_f32(logits, labels, losses, rows, cols, order, stream)
+
+
+def tr_plan_describe(op, rows, cols, order) -> tr_plan:
+    out = tr_plan()
+    _check(load().tr_plan_describe(op, rows, cols, order, ctypes.byref(out)), "tr_plan_describe")
+    return out
+
+
+def tr_plan_select_for(dev: tr_device_desc, op, rows, cols, order, align16=1) -> tr_plan:
+    out = tr_plan()
+    _check(load().tr_plan_select_for(ctypes.byref(dev), op, rows, cols, order, align16, ctypes.byref(out)),
+           "tr_plan_select_for")
+    return out
+
+
+def tr_plan_override(plan: tr_plan | None) -> int:
+    return load().tr_plan_override(None if plan is None else ctypes.byref(plan))
+
+
+def tr_last_device_error() -> int:
+    return load().tr_last_device_error()
+
+
+def tr_status_string(status: int) -> str:
+    return load().tr_status_string(status).decode()
+
+
+def tr_last_error_message() -> str:
+    return load().tr_last_error_message().decode()
+
+
+# ------------------------------------------------------------ tensor helpers
+
+def _stream_handle(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check_matrix(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D (rows x cols) tensor")
+
+
+def _check_vector(t, name, cols):
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if t.numel() != cols or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous vector of {cols} floats")
+    return t.data_ptr()
+
+
+def _order(order):
+    return ORDERS[order] if isinstance(order, str) else int(order)
+
+
+def softmax(x, out=None, order="unordered", stream=None):
+    """Row softmax of a CUDA float32 (rows, cols) tensor."""
+    import torch
+    _check_matrix(x, "x")
+    y = torch.empty_like(x) if out is None else out
+    _check_matrix(y, "out")
+    r, c = x.shape
+    _check(tr_softmax_f32(x.data_ptr(), y.data_ptr(), r, c, _order(order), _stream_handle(stream)), "softmax")
+    return y
+
+
+def rmsnorm(x, weight=None, eps=1e-5, out=None, order="unordered", stream=None):
+    import torch
+    _check_matrix(x, "x")
+    r, c = x.shape
+    wp = _check_vector(weight, "weight", c)
+    y = torch.empty_like(x) if out is None else out
+    _check_matrix(y, "out")
+    _check(tr_rmsnorm_f32(x.data_ptr(), wp, y.data_ptr(), r, c, eps, _order(order), _stream_handle(stream)),
+           "rmsnorm")
+    return y
+
+
+def layernorm(x, weight=None, bias=None, eps=1e-5, out=None, order="unordered", stream=None):
+    import torch
+    _check_matrix(x, "x")
+    r, c = x.shape
+    wp = _check_vector(weight, "weight", c)
+    bp = _check_vector(bias, "bias", c)
+    y = torch.empty_like(x) if out is None else out
+    _check_matrix(y, "out")
+    _check(tr_layernorm_f32(x.data_ptr(), wp, bp, y.data_ptr(), r, c, eps, _order(order),
+                            _stream_handle(stream)), "layernorm")
+    return y
+
+
+def cross_entropy(logits, labels, out=None, order="unordered", stream=None):
+    """Per-row loss log(sum exp(x)) - x[label] (label outside [0, cols) selects 0)."""
+    import torch
+    _check_matrix(logits, "logits")
+    r, c = logits.shape
+    if labels.dtype != torch.int64 or not labels.is_cuda or labels.numel() != r or not labels.is_contiguous():
+        raise TypeError("labels must be a contiguous CUDA int64 tensor with one entry per row")
+    loss = torch.empty(r, dtype=torch.float32, device=logits.device) if out is None else out
+    _check(tr_cross_entropy_f32(logits.data_ptr(), labels.data_ptr(), loss.data_ptr(), r, c, _order(order),
+                                _stream_handle(stream)), "cross_entropy")
+    return loss
+
+
+def plan_for(op, rows, cols, order="unordered") -> dict:
+    """The plan the library would use on the current device, as a dict."""
+    return tr_plan_describe(OPS[op] if isinstance(op, str) else op, rows, cols, _order(order)).as_dict()
+
+
+def run_op(op, inputs, out=None, order="unordered", eps=1e-5, stream=None):
+    """Dispatch one operator on a dict of inputs (keys as produced by ``synth``)."""
+    if op == "softmax":
+        return softmax(inputs["x"], out=out, order=order, stream=stream)
+    if op == "rmsnorm":
+        return rmsnorm(inputs["x"], inputs.get("w"), eps, out=out, order=order, stream=stream)
+    if op == "layernorm":
+        return layernorm(inputs["x"], inputs.get("w"), inputs.get("b"), eps, out=out, order=order, stream=stream)
+    if op == "cross_entropy":
+        return cross_entropy(inputs["x"], inputs["labels"], out=out, order=order, stream=stream)
+    raise ValueError(f"unknown op {op!r}")

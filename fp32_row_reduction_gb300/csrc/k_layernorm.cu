@@ -1,0 +1,6 @@
+// Unordered layernorm kernels: the instantiations of the row kernel family.
+#include "tr_dispatch.cuh"
+
+namespace tr {
+const void* kernel_layernorm(int kind, int lanes, int slots) { return unordered_table<OP_LAYERNORM>(kind, lanes, slots); }
+}  // namespace tr

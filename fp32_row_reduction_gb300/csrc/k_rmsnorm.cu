@@ -1,0 +1,6 @@
+// Unordered rmsnorm kernels: the instantiations of the row kernel family.
+#include "tr_dispatch.cuh"
+
+namespace tr {
+const void* kernel_rmsnorm(int kind, int lanes, int slots) { return unordered_table<OP_RMSNORM>(kind, lanes, slots); }
+}  // namespace tr

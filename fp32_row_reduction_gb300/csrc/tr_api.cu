@@ -1,0 +1,392 @@
+// The C-ABI of libtr: argument validation, plan selection and caching, launch.
+//
+// Contracts ("TIRx Metal reduction lowering"): noalias arguments (§3 "Semantic
+// domain and fail-closed admission"), explicit errors rather than clamping or
+// fallback (§1, §6), guarded out-of-range labels selecting 0 (§5.2). Every
+// step of the hot path runs in this library's kernels; there is no CPU path.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "tr.h"
+#include "tr_internal.h"
+#include "tr_plan.h"
+
+namespace tr {
+
+// Device error word: set by a bounded device-side wait that gives up, read and
+// cleared by tr_last_device_error().
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+tr_status fail(tr_status s, const std::string& msg) {
+    t_last_error = msg;
+    return s;
+}
+tr_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(TR_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DeviceState {
+    bool ready = false;
+    tr_device_desc desc{};
+    std::map<std::tuple<int, int64_t, int64_t, int, int>, tr_plan> plans;  // (op, rows, cols, order, align16)
+    std::map<std::tuple<const void*, int, int>, int> occ;                   // (kernel, threads, cluster) -> CTAs/SM
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+bool g_override_set[4] = {false, false, false, false};
+tr_plan g_override[4];
+
+tr_status device_state(int dev, DeviceState** out) {
+    DeviceState& st = g_devices[dev];
+    if (!st.ready) {
+        tr_device_desc d = gb300_desc();
+        int v = 0;
+        cudaError_t e;
+#define TR_ATTR(attr, field)                                      \
+    e = cudaDeviceGetAttribute(&v, attr, dev);                    \
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute"); \
+    d.field = v;
+        TR_ATTR(cudaDevAttrMultiProcessorCount, sm_count)
+        TR_ATTR(cudaDevAttrMaxThreadsPerMultiProcessor, max_threads_per_sm)
+        TR_ATTR(cudaDevAttrMaxBlocksPerMultiprocessor, max_ctas_per_sm)
+        TR_ATTR(cudaDevAttrMaxRegistersPerMultiprocessor, regs_per_sm)
+        TR_ATTR(cudaDevAttrMaxSharedMemoryPerMultiprocessor, smem_per_sm)
+#undef TR_ATTR
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        d.l2_bytes = v;
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrClusterLaunch, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        d.max_cluster_ctas = v ? 8 : 1;
+        if (const char* bw = std::getenv("TR_HBM_GBS")) d.hbm_gbs = std::atof(bw);
+        st.desc = d;
+        st.ready = true;
+    }
+    *out = &st;
+    return TR_OK;
+}
+
+// Resident CTAs per SM of a plan's kernel (0 = cannot run). Cluster plans:
+// the device's concurrent clusters times C, spread over the SMs.
+int query_occupancy(DeviceState& st, const tr_plan& p) {
+    const void* fn = kernel_for(p);
+    if (!fn) return 0;
+    const int C = (p.kind == TR_PLAN_CLUSTER || p.kind == TR_PLAN_STREAM) ? p.cluster_ctas : 1;
+    const auto key = std::make_tuple(fn, p.block_threads, C);
+    auto it = st.occ.find(key);
+    if (it != st.occ.end()) return it->second;
+    int n = 0;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || fa.maxThreadsPerBlock < p.block_threads) {
+        cudaGetLastError();
+        st.occ[key] = 0;
+        return 0;
+    }
+    if (C == 1) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, p.block_threads, 0) != cudaSuccess) n = 0;
+    } else {
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(static_cast<unsigned>(C) * 64u);
+        cfg.blockDim = dim3(p.block_threads);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = C;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) clusters = 0;
+        n = clusters > 0 ? std::max(1, clusters * C / std::max(1, st.desc.sm_count)) : 0;
+    }
+    cudaGetLastError();
+    st.occ[key] = n;
+    return n;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+bool misaligned(const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+struct Call {
+    int op;
+    RowArgs a;
+    int order;
+};
+
+tr_status validate_common(int64_t rows, int64_t cols, int order) {
+    if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE)
+        return fail(TR_ERR_INVALID_ARG, "order must be TR_ORDER_UNORDERED_TREE or TR_ORDER_ORDERED_TREE");
+    if (rows < 0) return fail(TR_ERR_INVALID_ARG, "rows must be >= 0");
+    if (cols < 1 || cols > 0x7fffffffLL) return fail(TR_ERR_INVALID_ARG, "cols must be in [1, 2^31 - 1]");
+    if (rows > 0 && rows > INT64_MAX / cols / 4) return fail(TR_ERR_INVALID_ARG, "rows * cols too large");
+    return TR_OK;
+}
+
+tr_status validate_eps(float eps) {
+    if (!std::isfinite(eps) || eps < 0.0f) return fail(TR_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    return TR_OK;
+}
+
+tr_status run(Call& c, cudaStream_t stream) {
+    RowArgs& a = c.a;
+    if (a.rows == 0) return TR_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const bool align16 = (a.cols % 4 == 0) && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0);
+    tr_plan plan;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* st = nullptr;
+        tr_status s = device_state(dev, &st);
+        if (s != TR_OK) return s;
+        OccupancyFn occ = [st](const tr_plan& p) { return query_occupancy(*st, p); };
+        if (g_override_set[c.op]) {
+            plan = g_override[c.op];
+            plan.op = c.op;
+            plan.order = c.order;
+            const char* why = "";
+            s = check_plan(st->desc, occ, &plan, a.rows, a.cols, &why);
+            if (s != TR_OK) return fail(TR_ERR_UNSUPPORTED, std::string("plan override rejected: ") + why);
+            plan.est_us = estimate_us(st->desc, plan, a.rows, a.cols, align16);
+        } else {
+            const auto key = std::make_tuple(c.op, a.rows, static_cast<int64_t>(a.cols), c.order, align16 ? 1 : 0);
+            auto it = st->plans.find(key);
+            if (it == st->plans.end()) {
+                s = select_plan(st->desc, occ, c.op, a.rows, a.cols, c.order, align16, &plan);
+                if (s != TR_OK) return fail(s, "no legal plan for this shape on this device");
+                st->plans.emplace(key, plan);
+            } else {
+                plan = it->second;
+            }
+        }
+    }
+    const void* fn = kernel_for(plan);
+    if (!fn) return fail(TR_ERR_UNSUPPORTED, "plan has no kernel in this build");
+    a.S = plan.warps_per_row;
+    a.C = plan.cluster_ctas;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid_ctas));
+    cfg.blockDim = dim3(plan.block_threads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    if (plan.cluster_ctas > 1) {
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = plan.cluster_ctas;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+    }
+    void* args[] = {&a};
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return TR_OK;
+}
+
+RowArgs blank_args(const float* x, int64_t rows, int64_t cols) {
+    RowArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.x = x;
+    a.rows = rows;
+    a.cols = static_cast<int>(cols);
+    a.inv_cols = 1.0f / static_cast<float>(cols);
+    a.S = 1;
+    a.C = 1;
+    return a;
+}
+
+}  // namespace
+}  // namespace tr
+
+using namespace tr;
+
+extern "C" {
+
+tr_status tr_softmax_f32(const float* x, float* y, int64_t rows, int64_t cols, tr_order order,
+                         cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!x || !y) return fail(TR_ERR_INVALID_ARG, "x and y must not be null");
+    if (misaligned(x, 4) || misaligned(y, 4)) return fail(TR_ERR_INVALID_ARG, "x and y must be 4-byte aligned");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    if (overlaps(x, n, y, n)) return fail(TR_ERR_INVALID_ARG, "x and y overlap (in-place is not supported)");
+    Call c{TR_OP_SOFTMAX, blank_args(x, rows, cols), order};
+    c.a.y = y;
+    c.a.y_vec = ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+    return run(c, stream);
+}
+
+tr_status tr_rmsnorm_f32(const float* x, const float* w, float* y, int64_t rows, int64_t cols, float eps,
+                         tr_order order, cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    s = validate_eps(eps);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!x || !y) return fail(TR_ERR_INVALID_ARG, "x and y must not be null");
+    if (misaligned(x, 4) || misaligned(y, 4) || misaligned(w, 4))
+        return fail(TR_ERR_INVALID_ARG, "x, y and w must be 4-byte aligned");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    if (overlaps(x, n, y, n) || overlaps(w, cols * 4, y, n))
+        return fail(TR_ERR_INVALID_ARG, "the output overlaps an input");
+    Call c{TR_OP_RMSNORM, blank_args(x, rows, cols), order};
+    c.a.y = y;
+    c.a.w = w;
+    c.a.has_w = w != nullptr;
+    c.a.eps = eps;
+    c.a.y_vec = ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+    return run(c, stream);
+}
+
+tr_status tr_layernorm_f32(const float* x, const float* gamma, const float* beta, float* y, int64_t rows,
+                           int64_t cols, float eps, tr_order order, cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    s = validate_eps(eps);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!x || !y) return fail(TR_ERR_INVALID_ARG, "x and y must not be null");
+    if (misaligned(x, 4) || misaligned(y, 4) || misaligned(gamma, 4) || misaligned(beta, 4))
+        return fail(TR_ERR_INVALID_ARG, "x, y, gamma and beta must be 4-byte aligned");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    if (overlaps(x, n, y, n) || overlaps(gamma, cols * 4, y, n) || overlaps(beta, cols * 4, y, n))
+        return fail(TR_ERR_INVALID_ARG, "the output overlaps an input");
+    Call c{TR_OP_LAYERNORM, blank_args(x, rows, cols), order};
+    c.a.y = y;
+    c.a.w = gamma;
+    c.a.b = beta;
+    c.a.has_w = gamma != nullptr;
+    c.a.has_b = beta != nullptr;
+    c.a.eps = eps;
+    c.a.y_vec = ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+    return run(c, stream);
+}
+
+tr_status tr_cross_entropy_f32(const float* logits, const int64_t* labels, float* losses, int64_t rows,
+                               int64_t cols, tr_order order, cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!logits || !labels || !losses) return fail(TR_ERR_INVALID_ARG, "logits, labels and losses must not be null");
+    if (misaligned(logits, 4) || misaligned(losses, 4) || misaligned(labels, 8))
+        return fail(TR_ERR_INVALID_ARG, "logits/losses must be 4-byte and labels 8-byte aligned");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    if (overlaps(logits, n, losses, rows * 4) || overlaps(labels, rows * 8, losses, rows * 4))
+        return fail(TR_ERR_INVALID_ARG, "losses overlap an input");
+    Call c{TR_OP_CROSS_ENTROPY, blank_args(logits, rows, cols), order};
+    c.a.labels = labels;
+    c.a.loss = losses;
+    return run(c, stream);
+}
+
+tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order order, tr_plan* out) {
+    if (!out) return fail(TR_ERR_INVALID_ARG, "out must not be null");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1 to describe a plan");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* st = nullptr;
+    s = device_state(dev, &st);
+    if (s != TR_OK) return s;
+    OccupancyFn occ = [st](const tr_plan& p) { return query_occupancy(*st, p); };
+    if (g_override_set[op]) {
+        tr_plan p = g_override[op];
+        p.op = op;
+        p.order = order;
+        const char* why = "";
+        s = check_plan(st->desc, occ, &p, rows, cols, &why);
+        if (s != TR_OK) return fail(TR_ERR_UNSUPPORTED, std::string("plan override rejected: ") + why);
+        p.est_us = estimate_us(st->desc, p, rows, cols, cols % 4 == 0);
+        *out = p;
+        return TR_OK;
+    }
+    s = select_plan(st->desc, occ, op, rows, cols, order, cols % 4 == 0, out);
+    if (s != TR_OK) return fail(s, "no legal plan for this shape on this device");
+    return TR_OK;
+}
+
+tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows, int64_t cols, tr_order order,
+                             int32_t align16, tr_plan* out) {
+    if (!dev || !out) return fail(TR_ERR_INVALID_ARG, "dev and out must not be null");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1 to select a plan");
+    if (dev->sm_count < 1 || dev->max_threads_per_sm < 32 || dev->regs_per_sm < 1 || dev->hbm_gbs <= 0)
+        return fail(TR_ERR_INVALID_ARG, "malformed device description");
+    s = select_plan(*dev, OccupancyFn(), op, rows, cols, order, align16 != 0, out);
+    if (s != TR_OK) return fail(s, "no legal plan for this shape on this device");
+    return TR_OK;
+}
+
+tr_status tr_plan_override(const tr_plan* plan) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!plan) {
+        for (bool& b : g_override_set) b = false;
+        return TR_OK;
+    }
+    if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_ORDERED) return fail(TR_ERR_INVALID_ARG, "bad plan kind");
+    g_override[plan->op] = *plan;
+    g_override_set[plan->op] = true;
+    return TR_OK;
+}
+
+tr_status tr_last_device_error(void) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_device_error, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        return fail(TR_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up");
+    }
+    return TR_OK;
+}
+
+const char* tr_status_string(tr_status status) {
+    switch (status) {
+        case TR_OK: return "TR_OK";
+        case TR_ERR_INVALID_ARG: return "TR_ERR_INVALID_ARG";
+        case TR_ERR_UNSUPPORTED: return "TR_ERR_UNSUPPORTED";
+        case TR_ERR_CUDA: return "TR_ERR_CUDA";
+        case TR_ERR_DEVICE_TIMEOUT: return "TR_ERR_DEVICE_TIMEOUT";
+    }
+    return "unknown tr_status";
+}
+
+const char* tr_last_error_message(void) { return t_last_error.c_str(); }
+
+int32_t tr_version(void) { return 100; }
+
+}  // extern "C"

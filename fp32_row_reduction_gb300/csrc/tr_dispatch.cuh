@@ -1,0 +1,48 @@
+// Kernel tables: the instantiations a plan can name, per operator.
+#pragma once
+
+#include "tr_row_kernels.cuh"
+
+namespace tr {
+
+template <int OP, int G>
+const void* rows_table(int slots) {
+    switch (slots) {
+        case 1: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 1>);
+        case 2: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 2>);
+        case 4: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 4>);
+    }
+    if constexpr (G == 32) {
+        switch (slots) {
+            case 8: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 8>);
+            case 16: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 16>);
+        }
+    }
+    return nullptr;
+}
+
+template <int OP>
+const void* unordered_table(int kind, int lanes, int slots) {
+    switch (kind) {
+        case TR_PLAN_ROWS:
+            switch (lanes) {
+                case 4: return rows_table<OP, 4>(slots);
+                case 8: return rows_table<OP, 8>(slots);
+                case 16: return rows_table<OP, 16>(slots);
+                case 32: return rows_table<OP, 32>(slots);
+            }
+            return nullptr;
+        case TR_PLAN_CLUSTER:
+            switch (slots) {
+                case 4: return reinterpret_cast<const void*>(cluster_cached_kernel<OP, 4>);
+                case 8: return reinterpret_cast<const void*>(cluster_cached_kernel<OP, 8>);
+                case 16: return reinterpret_cast<const void*>(cluster_cached_kernel<OP, 16>);
+            }
+            return nullptr;
+        case TR_PLAN_STREAM:
+            return slots == 0 ? reinterpret_cast<const void*>(stream_kernel<OP>) : nullptr;
+    }
+    return nullptr;
+}
+
+}  // namespace tr

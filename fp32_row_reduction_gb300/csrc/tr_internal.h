@@ -1,0 +1,54 @@
+// Internal host/device interface of the library (not installed).
+#pragma once
+
+#include <stdint.h>
+
+#include "tr.h"
+
+namespace tr {
+
+// Kernel parameter block shared by every row kernel (passed by value).
+struct RowArgs {
+    const float* x;
+    float* y;
+    const float* w;         // weight / gamma (has_w == 0: weight 1)
+    const float* b;         // beta (has_b == 0: bias 0)
+    const int64_t* labels;  // cross-entropy
+    float* loss;            // cross-entropy
+    int64_t rows;
+    int cols;
+    float eps;
+    float inv_cols;  // 1 / cols
+    int S;           // warps per row (lanes_per_row == 32)
+    int C;           // CTAs per row (cluster / stream plans)
+    int y_vec;       // y rows have the same 16-byte phase as x rows
+    int has_w, has_b;
+};
+
+// Kernel entry for a plan, or nullptr when this build has no such
+// instantiation (the plan is then unsupported). One table per operator.
+const void* kernel_softmax(int kind, int lanes, int slots);
+const void* kernel_rmsnorm(int kind, int lanes, int slots);
+const void* kernel_layernorm(int kind, int lanes, int slots);
+const void* kernel_xent(int kind, int lanes, int slots);
+const void* kernel_ordered(int op, int slots);
+
+inline const void* kernel_for(const tr_plan& p) {
+    if (p.kind == TR_PLAN_ORDERED) return kernel_ordered(p.op, p.vec_slots);
+    switch (p.op) {
+        case TR_OP_SOFTMAX: return kernel_softmax(p.kind, p.lanes_per_row, p.vec_slots);
+        case TR_OP_RMSNORM: return kernel_rmsnorm(p.kind, p.lanes_per_row, p.vec_slots);
+        case TR_OP_LAYERNORM: return kernel_layernorm(p.kind, p.lanes_per_row, p.vec_slots);
+        case TR_OP_CROSS_ENTROPY: return kernel_xent(p.kind, p.lanes_per_row, p.vec_slots);
+    }
+    return nullptr;
+}
+
+// Instantiated K values (16-byte slots per worker).
+constexpr int kRowsSlotsSub[] = {1, 2, 4};           // lanes_per_row 4, 8, 16
+constexpr int kRowsSlotsWarp[] = {1, 2, 4, 8, 16};   // lanes_per_row 32
+constexpr int kClusterSlots[] = {4, 8, 16};
+constexpr int kOrderedSlots[] = {0, 1, 2, 4, 8, 16}; // 0: re-read plan
+constexpr int kOrderedThreads = 256;                  // OT-1024: 256 workers x 4 leaves
+
+}  // namespace tr

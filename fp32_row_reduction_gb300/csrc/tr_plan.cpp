@@ -1,0 +1,379 @@
+// Plan selection: legality, then a fixed cost model, over a finite family.
+//
+// Page: "TIRx Metal reduction lowering" §6 "Cost model and finite solver" and
+// the "Whole-launch reduction cost policy" page. The page's bootstrap score
+// counts worker rounds, collectives and setup, and its notes record that the
+// deciding terms are global bytes and waves; on an HBM-bound GB300 the build
+// therefore prices a plan in microseconds from bytes, Little's law and waves:
+//
+//   bw_eff  = min(BW, bytes in flight / LATENCY)           (memory parallelism)
+//   t_mem   = full waves' bytes / bw_eff + last wave's time (tail), the last
+//             wave never shorter than its dependent round trips x LATENCY
+//   t       = LAUNCH + max(t_mem, t_alu) + reductions * barrier cost
+//
+// Constants come from the datasheet and the device attributes, never from
+// timing the shapes being planned (the page's rule: measurement may calibrate
+// priors but never selects a benchmark shape's plan, and never makes an
+// illegal candidate legal).
+#include "tr_plan.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <tuple>
+#include <vector>
+
+#include "tr_internal.h"
+
+namespace tr {
+
+namespace {
+
+// Model constants (microseconds, bytes, instructions). Documented priors.
+constexpr double kLaunchUs = 1.5;        // launch + grid ramp
+constexpr double kLatencyUs = 0.8;       // loaded DRAM round trip
+constexpr double kCtaBarrierUs = 0.05;   // one shared-memory reduction round
+constexpr double kClusterBarrierUs = 0.35;
+constexpr double kL2OverHbm = 2.5;       // L2 re-read bandwidth relative to HBM
+constexpr double kClockGhz = 1.9;
+constexpr int kStreamChunk = 8;          // float4 per thread per streamed chunk (kStreamU)
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool in(const int* arr, int n, int v) {
+    for (int i = 0; i < n; ++i)
+        if (arr[i] == v) return true;
+    return false;
+}
+template <size_t N>
+bool in(const int (&arr)[N], int v) {
+    return in(arr, static_cast<int>(N), v);
+}
+template <size_t N>
+int smallest_covering(const int (&arr)[N], int64_t need) {  // smallest K with K >= need
+    for (size_t i = 0; i < N; ++i)
+        if (arr[i] >= need) return arr[i];
+    return -1;
+}
+
+int max_threads_for_slots(int op, int kind, int k) {
+    if (kind == TR_PLAN_ROWS || kind == TR_PLAN_CLUSTER)
+        return k >= 16 ? 512 : (k >= 8 && op == TR_OP_LAYERNORM) ? 768 : 1024;
+    if (kind == TR_PLAN_ORDERED) return kOrderedThreads;
+    return 1024;
+}
+
+int reductions_of(int op) {
+    switch (op) {
+        case TR_OP_SOFTMAX: return 2;
+        case TR_OP_RMSNORM: return 1;
+        case TR_OP_LAYERNORM: return 2;
+        default: return 1;
+    }
+}
+
+}  // namespace
+
+tr_device_desc gb300_desc() {
+    tr_device_desc d;
+    std::memset(&d, 0, sizeof d);
+    d.sm_count = 152;
+    d.max_threads_per_sm = 2048;
+    d.max_ctas_per_sm = 32;
+    d.regs_per_sm = 65536;
+    d.smem_per_sm = 233472;
+    d.max_cluster_ctas = 8;
+    d.l2_bytes = 126LL << 20;
+    d.hbm_gbs = 7000.0;
+    return d;
+}
+
+int model_occupancy(const tr_device_desc& d, const tr_plan& p) {
+    // register estimate per thread (from -Xptxas -v of this build's kernels,
+    // rounded up): a base plus one register per cached float
+    int regs;
+    const int k = p.vec_slots;
+    switch (p.kind) {
+        case TR_PLAN_ROWS:
+        case TR_PLAN_CLUSTER: regs = 28 + 4 * k + (p.op == TR_OP_LAYERNORM ? 4 : 0); break;
+        case TR_PLAN_STREAM: regs = 64; break;
+        case TR_PLAN_XENT: regs = 24 + 4 * k; break;
+        default: regs = 40 + 5 * k; break;
+    }
+    regs = std::min(255, (regs + 7) / 8 * 8);
+    const int t = p.block_threads;
+    if (t <= 0) return 0;
+    const int warps = (t + 31) / 32;
+    const int regs_cta = warps * ((regs * 32 + 255) / 256 * 256);
+    int occ = std::min(d.max_threads_per_sm / t, d.max_ctas_per_sm);
+    occ = std::min(occ, d.regs_per_sm / std::max(1, regs_cta));
+    return occ;
+}
+
+tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p, int64_t rows, int64_t cols,
+                     const char** why) {
+    auto fail = [&](tr_status s, const char* msg) {
+        if (why) *why = msg;
+        return s;
+    };
+    if (rows < 1 || cols < 1) return fail(TR_ERR_INVALID_ARG, "plans are for rows >= 1, cols >= 1");
+    const int64_t n4 = ceil_div(cols, 4);  // upper bound on 16-byte body slots of any row
+    const bool ordered = p->order == TR_ORDER_ORDERED_TREE;
+    const bool xent = p->op == TR_OP_CROSS_ENTROPY;
+    if (p->order != TR_ORDER_UNORDERED_TREE && !ordered) return fail(TR_ERR_INVALID_ARG, "bad order");
+    if (p->op < TR_OP_SOFTMAX || p->op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (ordered != (p->kind == TR_PLAN_ORDERED))
+        return fail(TR_ERR_UNSUPPORTED, "the ordered policy is realised only by the OT-1024 plan");
+    if (!ordered && xent != (p->kind == TR_PLAN_XENT))
+        return fail(TR_ERR_UNSUPPORTED, "cross-entropy is realised only by the streaming XENT plan");
+    const int T = p->block_threads;
+    if (T < 32 || T > 1024 || T % 32) return fail(TR_ERR_UNSUPPORTED, "block_threads must be a multiple of 32 in [32, 1024]");
+    const int k = p->vec_slots;
+    const int G = p->lanes_per_row;
+    switch (p->kind) {
+        case TR_PLAN_ORDERED: {
+            if (T != kOrderedThreads || G != 32 || p->warps_per_row != 8 || p->rows_per_cta != 1 || p->cluster_ctas != 1)
+                return fail(TR_ERR_UNSUPPORTED, "OT-1024 runs 256 threads (8 warps) per row, one row per CTA");
+            if (!in(kOrderedSlots, k)) return fail(TR_ERR_UNSUPPORTED, "no OT-1024 kernel with that vec_slots");
+            if (k > 0 && static_cast<int64_t>(1024) * k < cols)
+                return fail(TR_ERR_UNSUPPORTED, "cached OT-1024 needs cols <= 1024 * vec_slots");
+            p->grid_ctas = rows;
+            break;
+        }
+        case TR_PLAN_ROWS:
+        case TR_PLAN_XENT: {
+            int W;
+            if (G == 4 || G == 8 || G == 16) {
+                if (p->warps_per_row != 1) return fail(TR_ERR_UNSUPPORTED, "sub-warp rows have warps_per_row 1");
+                W = G;
+                if (p->rows_per_cta != T / G) return fail(TR_ERR_UNSUPPORTED, "rows_per_cta must be block_threads / lanes_per_row");
+            } else if (G == 32) {
+                const int S = p->warps_per_row;
+                if (S < 1 || S > 32) return fail(TR_ERR_UNSUPPORTED, "warps_per_row must be in [1, 32]");
+                W = 32 * S;
+                if (p->rows_per_cta < 1 || W * p->rows_per_cta != T)
+                    return fail(TR_ERR_UNSUPPORTED, "block_threads must equal 32 * warps_per_row * rows_per_cta");
+            } else {
+                return fail(TR_ERR_UNSUPPORTED, "lanes_per_row must be 4, 8, 16 or 32");
+            }
+            if (p->cluster_ctas != 1) return fail(TR_ERR_UNSUPPORTED, "row plans use cluster_ctas 1");
+            if (p->kind == TR_PLAN_ROWS) {
+                if (G < 32 ? !in(kRowsSlotsSub, k) : !in(kRowsSlotsWarp, k))
+                    return fail(TR_ERR_UNSUPPORTED, "no cached row kernel with that vec_slots");
+                if (static_cast<int64_t>(W) * k < n4)
+                    return fail(TR_ERR_UNSUPPORTED, "the row does not fit the workers' register stripes");
+            }
+            p->grid_ctas = ceil_div(rows, p->rows_per_cta);
+            break;
+        }
+        case TR_PLAN_CLUSTER:
+        case TR_PLAN_STREAM: {
+            const int C = p->cluster_ctas;
+            const int cmin = p->kind == TR_PLAN_CLUSTER ? 2 : 1;
+            if (C < cmin || C > d.max_cluster_ctas) return fail(TR_ERR_UNSUPPORTED, "cluster_ctas out of range for this device");
+            if (G != 32 || p->rows_per_cta != 1 || p->warps_per_row != T / 32)
+                return fail(TR_ERR_UNSUPPORTED, "a CTA of a split row works as one group of block_threads / 32 warps");
+            if (p->kind == TR_PLAN_CLUSTER) {
+                if (!in(kClusterSlots, k)) return fail(TR_ERR_UNSUPPORTED, "no cluster kernel with that vec_slots");
+                if (static_cast<int64_t>(T) * k < ceil_div(n4, C))
+                    return fail(TR_ERR_UNSUPPORTED, "the row slice does not fit the CTA's register stripes");
+            } else if (k != 0) {
+                return fail(TR_ERR_UNSUPPORTED, "stream plans cache nothing (vec_slots 0)");
+            }
+            p->grid_ctas = rows * C;
+            break;
+        }
+        default: return fail(TR_ERR_UNSUPPORTED, "unknown plan kind");
+    }
+    if (T > max_threads_for_slots(p->op, p->kind, k)) return fail(TR_ERR_UNSUPPORTED, "too many threads for that vec_slots");
+    if (p->grid_ctas > 0x7fffffffLL) return fail(TR_ERR_UNSUPPORTED, "grid too large");
+    const int o = occ ? occ(*p) : model_occupancy(d, *p);
+    if (o < 1) return fail(TR_ERR_UNSUPPORTED, "the plan cannot be resident on this device");
+    p->ctas_per_sm = o;
+    if (why) *why = "";
+    return TR_OK;
+}
+
+double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int64_t cols, bool align16) {
+    (void)align16;
+    const double E = static_cast<double>(rows) * static_cast<double>(cols);
+    const double bw = d.hbm_gbs * 1e3;  // bytes per microsecond
+    const int op = p.op;
+    double alg;
+    switch (op) {
+        case TR_OP_SOFTMAX: alg = 8.0 * E; break;
+        case TR_OP_RMSNORM: alg = 8.0 * E + 4.0 * cols; break;
+        case TR_OP_LAYERNORM: alg = 8.0 * E + 8.0 * cols; break;
+        default: alg = 4.0 * E + 12.0 * rows; break;
+    }
+    // re-reads: served by L2 when the input fits comfortably, else by HBM
+    double reread = 0.0;
+    if (p.kind == TR_PLAN_STREAM) reread = 4.0 * E;
+    if (p.kind == TR_PLAN_ORDERED && p.vec_slots == 0) reread = 4.0 * E * (op == TR_OP_RMSNORM || op == TR_OP_CROSS_ENTROPY ? 1 : 2);
+    const bool l2_fits = 4.0 * E <= 0.5 * static_cast<double>(d.l2_bytes);
+    const double hbm_bytes = alg + (l2_fits ? 0.0 : reread);
+    const double l2_bytes = l2_fits ? reread : 0.0;
+
+    const double grid = static_cast<double>(p.grid_ctas);
+    const double slots = static_cast<double>(p.ctas_per_sm) * d.sm_count;
+    const double T = p.block_threads;
+    double inflight_thread;  // bytes a thread can have in flight at once
+    int rounds;              // dependent memory round trips in a CTA's life
+    switch (p.kind) {
+        case TR_PLAN_ROWS:
+        case TR_PLAN_CLUSTER: inflight_thread = 16.0 * p.vec_slots; rounds = 1; break;
+        case TR_PLAN_ORDERED:
+            inflight_thread = 16.0 * std::max(1, p.vec_slots);
+            rounds = p.vec_slots > 0 ? 1 : 1 + reductions_of(op);
+            break;
+        case TR_PLAN_STREAM: inflight_thread = 16.0 * kStreamChunk; rounds = 2; break;
+        default: inflight_thread = 16.0 * p.vec_slots; rounds = 1; break;
+    }
+    const double bytes_cta = hbm_bytes / grid;
+    const double read_cta = 4.0 * E / grid;  // one pass over the CTA's inputs
+    const double inflight_cta = std::max(16.0, std::min(T * inflight_thread, read_cta));
+    const double full_waves = std::floor(grid / slots);
+    const double last = grid - full_waves * slots;
+    // full waves run at the steady-state bandwidth; the last (or only) wave is
+    // bounded by its share of bandwidth, its memory parallelism and its round trips
+    const double bw_full = std::min(bw, slots * inflight_cta / kLatencyUs);
+    double t_mem = full_waves * slots * bytes_cta / bw_full;
+    if (last > 0) {
+        const double per_cta_bw = std::min(bw / last, inflight_cta / kLatencyUs);
+        t_mem += std::max(rounds * kLatencyUs, bytes_cta / per_cta_bw);
+    } else {
+        t_mem += rounds * kLatencyUs;
+    }
+    t_mem += l2_bytes / (kL2OverHbm * bw);
+
+    // arithmetic: SFU ex2 (16 per SM per clock) and ALU issue (128 lanes per SM per clock)
+    double sfu_per_elem = 0.0, alu_per_elem = 4.0;
+    if (p.kind == TR_PLAN_ORDERED) {
+        alu_per_elem = op == TR_OP_SOFTMAX ? 48.0 : op == TR_OP_CROSS_ENTROPY ? 24.0 : op == TR_OP_LAYERNORM ? 24.0 : 16.0;
+    } else if (op == TR_OP_SOFTMAX) {
+        sfu_per_elem = p.kind == TR_PLAN_STREAM ? 2.0 : 1.0;
+    } else if (op == TR_OP_CROSS_ENTROPY) {
+        sfu_per_elem = 1.0;
+    }
+    const double per_us = d.sm_count * kClockGhz * 1e3;  // SM-clocks per microsecond
+    const double t_alu = E * (sfu_per_elem / (16.0 * per_us) + alu_per_elem / (128.0 * per_us));
+
+    const double waves = std::ceil(grid / slots);
+    double sync = 0.0;
+    const int red = p.kind == TR_PLAN_ORDERED ? reductions_of(op) : (p.kind == TR_PLAN_STREAM || op == TR_OP_CROSS_ENTROPY ? 1 : reductions_of(op));
+    if (p.lanes_per_row == 32 && (p.warps_per_row > 1 || p.kind == TR_PLAN_ORDERED)) sync += kCtaBarrierUs;
+    if (p.cluster_ctas > 1) sync += kClusterBarrierUs;
+    return kLaunchUs + std::max(t_mem, t_alu) + waves * red * sync;
+}
+
+tr_status select_plan(const tr_device_desc& d, const OccupancyFn& occ, int32_t op, int64_t rows, int64_t cols,
+                      int32_t order, bool align16, tr_plan* out) {
+    std::vector<tr_plan> cands;
+    auto base = [&](int kind) {
+        tr_plan p;
+        std::memset(&p, 0, sizeof p);
+        p.op = op;
+        p.order = order;
+        p.kind = kind;
+        p.cluster_ctas = 1;
+        return p;
+    };
+    const int64_t n4 = ceil_div(cols, 4);
+    if (order == TR_ORDER_ORDERED_TREE) {
+        tr_plan p = base(TR_PLAN_ORDERED);
+        p.lanes_per_row = 32;
+        p.warps_per_row = 8;
+        p.rows_per_cta = 1;
+        p.block_threads = kOrderedThreads;
+        const int k = smallest_covering(kOrderedSlots, ceil_div(cols, 1024));
+        p.vec_slots = k < 0 ? 0 : k;
+        cands.push_back(p);
+    } else {
+        const bool xent = op == TR_OP_CROSS_ENTROPY;
+        const int kind = xent ? TR_PLAN_XENT : TR_PLAN_ROWS;
+        // a row inside a warp: 4, 8 or 16 lanes
+        for (int G : {4, 8, 16}) {
+            const int k = xent ? 2 : smallest_covering(kRowsSlotsSub, ceil_div(n4, G));
+            if (k < 0) continue;
+            for (int T : {64, 128, 256, 512}) {
+                tr_plan p = base(kind);
+                p.lanes_per_row = G;
+                p.warps_per_row = 1;
+                p.rows_per_cta = T / G;
+                p.block_threads = T;
+                p.vec_slots = k;
+                cands.push_back(p);
+            }
+        }
+        // a row per S warps, Q rows per CTA
+        for (int S = 1; S <= 32; ++S) {
+            std::vector<int> ks;
+            if (xent) {
+                ks = {2, 4, 8};
+            } else {
+                const int k = smallest_covering(kRowsSlotsWarp, ceil_div(n4, 32 * S));
+                if (k < 0) continue;
+                ks = {k};
+            }
+            for (int k : ks)
+                for (int Q = 1; 32 * S * Q <= 1024; Q *= 2) {
+                    tr_plan p = base(kind);
+                    p.lanes_per_row = 32;
+                    p.warps_per_row = S;
+                    p.rows_per_cta = Q;
+                    p.block_threads = 32 * S * Q;
+                    p.vec_slots = k;
+                    cands.push_back(p);
+                }
+        }
+        if (!xent) {
+            for (int C = 1; C <= d.max_cluster_ctas; ++C)
+                for (int T : {256, 512, 1024}) {
+                    if (C >= 2) {
+                        const int k = smallest_covering(kClusterSlots, ceil_div(ceil_div(n4, C), T));
+                        if (k > 0) {
+                            tr_plan p = base(TR_PLAN_CLUSTER);
+                            p.lanes_per_row = 32;
+                            p.warps_per_row = T / 32;
+                            p.rows_per_cta = 1;
+                            p.block_threads = T;
+                            p.cluster_ctas = C;
+                            p.vec_slots = k;
+                            cands.push_back(p);
+                        }
+                    }
+                    tr_plan s = base(TR_PLAN_STREAM);
+                    s.lanes_per_row = 32;
+                    s.warps_per_row = T / 32;
+                    s.rows_per_cta = 1;
+                    s.block_threads = T;
+                    s.cluster_ctas = C;
+                    s.vec_slots = 0;
+                    cands.push_back(s);
+                }
+        }
+    }
+    bool found = false;
+    tr_plan best;
+    int legal = 0;
+    for (tr_plan& p : cands) {
+        if (check_plan(d, occ, &p, rows, cols, nullptr) != TR_OK) continue;
+        p.est_us = estimate_us(d, p, rows, cols, align16);
+        ++legal;
+        // cheapest; ties keep fewer cooperating warps/CTAs, then smaller CTAs
+        auto key = [](const tr_plan& q) {
+            return std::make_tuple(std::round(q.est_us * 100.0), q.warps_per_row * q.cluster_ctas, q.block_threads,
+                                   q.vec_slots);
+        };
+        if (!found || key(p) < key(best)) {
+            best = p;
+            found = true;
+        }
+    }
+    if (!found) return TR_ERR_UNSUPPORTED;
+    best.candidates = legal;
+    *out = best;
+    return TR_OK;
+}
+
+}  // namespace tr

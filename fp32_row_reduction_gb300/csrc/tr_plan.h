@@ -1,0 +1,39 @@
+// Plan selection (host only, no CUDA calls): legality first, then a fixed
+// cost model ("TIRx Metal reduction lowering" §6 "Cost model and finite
+// solver": legality is decided before profitability, candidates are few
+// enough to enumerate exhaustively, exact constraints are never clamped).
+#pragma once
+
+#include <functional>
+#include <stdint.h>
+
+#include "tr.h"
+
+namespace tr {
+
+// Resident CTAs per SM for a fully specified plan, or 0 if it cannot run.
+// For cluster launches: resident CTAs per SM implied by the number of
+// clusters the device can hold at once.
+using OccupancyFn = std::function<int(const tr_plan&)>;
+
+// Host-only occupancy model from a register estimate (used without a GPU).
+int model_occupancy(const tr_device_desc& d, const tr_plan& p);
+
+// Fill grid_ctas and check every legality rule of `p` for this shape.
+// Returns TR_OK, TR_ERR_UNSUPPORTED (illegal for the shape or not built) or
+// TR_ERR_INVALID_ARG (malformed fields). `why` receives a reason.
+tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p, int64_t rows, int64_t cols,
+                     const char** why);
+
+// Cost-model estimate in microseconds for a legal plan (grid_ctas and
+// ctas_per_sm filled).
+double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int64_t cols, bool align16);
+
+// Enumerate every legal candidate and return the cheapest.
+tr_status select_plan(const tr_device_desc& d, const OccupancyFn& occ, int32_t op, int64_t rows, int64_t cols,
+                      int32_t order, bool align16, tr_plan* out);
+
+// Default description of a GB300 (used by tests and host-only planning).
+tr_device_desc gb300_desc();
+
+}  // namespace tr

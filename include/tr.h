@@ -1,0 +1,170 @@
+/*
+ * tr.h — FP32 row reductions with fused epilogues for one GB300 (sm_103a).
+ *
+ * Four operators, each a per-row reduction followed by an elementwise
+ * epilogue over the same row ("TIRx Metal reduction lowering", §1 "The
+ * frontend stays execution-first": row softmax and cross-entropy programs;
+ * §5.1: LayerNorm mean/variance; RMSNorm is named on the "Whole-launch
+ * reduction cost policy" page and read here as x / sqrt(mean(x^2) + eps) * w).
+ *
+ * Layout: every matrix is row-major and contiguous, element (r, c) at
+ * ptr[r * cols + c]; weights and biases are vectors of `cols` floats; labels
+ * are `rows` int64 values; losses are `rows` floats.
+ *
+ * Pointers are DEVICE pointers owned by the caller. They must be 4-byte
+ * aligned; 16-byte alignment of the row starts is not required (unaligned
+ * heads and tails are peeled), but is faster. Inputs and outputs must not
+ * overlap (the noalias contract of §3 "Semantic domain and fail-closed
+ * admission"): in-place calls are rejected, not silently serialised.
+ * The library allocates no memory per call. Calls are asynchronous on
+ * `stream` (0 = the legacy default stream) and do not synchronise.
+ *
+ * Reduction order (§1, ReductionPolicy): TR_ORDER_UNORDERED_TREE lets the
+ * library pick any tree and plan (results within a max relative error of
+ * 2e-6 plus an absolute 1e-6 of the exact FP64 values); TR_ORDER_ORDERED_TREE
+ * always uses the canonical fixed tree OT-1024 with IEEE round-to-nearest
+ * arithmetic, IEEE division and square root and the library's own exp/log, so
+ * that results are bit-identical across plans, runs and launch
+ * configurations. Unsupported requests are errors, never a fallback (§1:
+ * "missing support is an explicit compile error, not a tolerance change or
+ * CPU fallback").
+ *
+ * Errors: every entry point returns a tr_status. Argument errors are detected
+ * on the host before anything is launched. TR_ERR_CUDA reports a CUDA launch
+ * error (the message is in tr_last_error_message()). Kernels never trap: a
+ * bounded device-side wait that gives up records TR_ERR_DEVICE_TIMEOUT in a
+ * device error word, which tr_last_device_error() reads and clears.
+ */
+#ifndef TR_H
+#define TR_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tr_status {
+    TR_OK = 0,
+    TR_ERR_INVALID_ARG = 1,    /* null pointer, bad size, overlap, bad eps or enum */
+    TR_ERR_UNSUPPORTED = 2,    /* a legal request this build cannot realise (e.g. an illegal plan override) */
+    TR_ERR_CUDA = 3,           /* a CUDA runtime error (launch, attribute, device query) */
+    TR_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait gave up (reported by tr_last_device_error) */
+} tr_status;
+
+typedef enum tr_order {
+    TR_ORDER_UNORDERED_TREE = 0,  /* default: any reassociation / permutation of the reduction */
+    TR_ORDER_ORDERED_TREE = 1     /* canonical OT-1024 fixed tree, bit-exact */
+} tr_order;
+
+typedef enum tr_op {
+    TR_OP_SOFTMAX = 0,
+    TR_OP_RMSNORM = 1,
+    TR_OP_LAYERNORM = 2,
+    TR_OP_CROSS_ENTROPY = 3
+} tr_op;
+
+/* How a row is mapped onto the GPU (the build's counterpart of the page's
+ * GroupPlan, §2 "Where the optimization lives"). */
+typedef enum tr_plan_kind {
+    TR_PLAN_ROWS = 0,     /* a row per lane group (4/8/16 lanes) or per S warps of a CTA; Q rows per CTA; row cached in registers */
+    TR_PLAN_CLUSTER = 1,  /* a row per cluster of C CTAs; slices cached in registers; partials combined through distributed shared memory */
+    TR_PLAN_STREAM = 2,   /* a row per C CTAs (C >= 1); no cache: statistics pass, then the row is re-read (from L2 when it fits) */
+    TR_PLAN_XENT = 3,     /* cross-entropy: one streaming pass with an online (max, sum of exp) pair */
+    TR_PLAN_ORDERED = 4   /* OT-1024: 256 threads per row; cached (vec_slots > 0) or re-read (vec_slots == 0) */
+} tr_plan_kind;
+
+typedef struct tr_plan {
+    int32_t op;              /* tr_op */
+    int32_t order;           /* tr_order */
+    int32_t kind;            /* tr_plan_kind */
+    int32_t lanes_per_row;   /* 4, 8, 16 (a row inside a warp) or 32 (a row spans warps_per_row warps) */
+    int32_t warps_per_row;   /* S: warps of one CTA cooperating on a row (1 when lanes_per_row < 32) */
+    int32_t rows_per_cta;    /* Q: independent rows packed into one CTA */
+    int32_t cluster_ctas;    /* C: CTAs cooperating on one row (1 = no cluster) */
+    int32_t vec_slots;       /* K: 16-byte row slots cached per thread (0 = not cached) */
+    int32_t block_threads;   /* threads per CTA */
+    int32_t ctas_per_sm;     /* resident CTAs per SM assumed by the cost model */
+    int64_t grid_ctas;       /* CTAs launched for the problem this plan was selected for */
+    double est_us;           /* cost-model estimate in microseconds (a prior, not a measurement) */
+    int32_t candidates;      /* legal candidates the selector ranked */
+    int32_t reserved;
+} tr_plan;
+
+/* A device as the plan selector sees it (for host-only planning and tests). */
+typedef struct tr_device_desc {
+    int32_t sm_count;              /* 152 on GB300 */
+    int32_t max_threads_per_sm;    /* 2048 */
+    int32_t max_ctas_per_sm;       /* 32 */
+    int32_t regs_per_sm;           /* 65536 */
+    int32_t smem_per_sm;           /* bytes */
+    int32_t max_cluster_ctas;      /* 8 portable */
+    int64_t l2_bytes;
+    double hbm_gbs;                /* DRAM bandwidth, GB/s */
+} tr_device_desc;
+
+/* ---- the four operators ------------------------------------------------ */
+
+/* y[r, :] = softmax(x[r, :]): m = max, e = exp(x - m), y = e / sum(e).
+ * x, y: rows x cols. */
+tr_status tr_softmax_f32(const float* x, float* y, int64_t rows, int64_t cols,
+                         tr_order order, cudaStream_t stream);
+
+/* y[r, c] = x[r, c] / sqrt(sum_c x[r, c]^2 / cols + eps) * w[c].
+ * w may be NULL (weight 1). eps must be finite and >= 0. */
+tr_status tr_rmsnorm_f32(const float* x, const float* w, float* y,
+                         int64_t rows, int64_t cols, float eps,
+                         tr_order order, cudaStream_t stream);
+
+/* mean = sum(x)/cols, var = sum((x - mean)^2)/cols (population),
+ * y = (x - mean) / sqrt(var + eps) * gamma + beta.
+ * gamma may be NULL (1), beta may be NULL (0). eps finite and >= 0. */
+tr_status tr_layernorm_f32(const float* x, const float* gamma, const float* beta,
+                           float* y, int64_t rows, int64_t cols, float eps,
+                           tr_order order, cudaStream_t stream);
+
+/* loss[r] = log(sum_c exp(x[r, c] - m)) + m - selected, m = max_c x[r, c],
+ * selected = x[r, labels[r]] if 0 <= labels[r] < cols, else 0 (§5.2 "Guarded
+ * immutable views and dynamic gather": an out-of-range label is not an error).
+ * logits: rows x cols; labels: rows int64; losses: rows floats. */
+tr_status tr_cross_entropy_f32(const float* logits, const int64_t* labels, float* losses,
+                               int64_t rows, int64_t cols, tr_order order, cudaStream_t stream);
+
+/* ---- plans, errors, introspection -------------------------------------- */
+
+/* The plan the next call with these arguments would use on the current
+ * device (16-byte-aligned rows assumed when cols % 4 == 0). */
+tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order order, tr_plan* out);
+
+/* Host-only selection for a described device (no GPU needed). align16 = 1
+ * when every row start is 16-byte aligned. */
+tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows, int64_t cols,
+                             tr_order order, int32_t align16, tr_plan* out);
+
+/* Force the next calls of plan->op to use exactly this plan (kind,
+ * lanes_per_row, warps_per_row, rows_per_cta, cluster_ctas, vec_slots,
+ * block_threads). NULL clears. A plan that is illegal for a later call's
+ * shape makes that call return TR_ERR_UNSUPPORTED: constraints are never
+ * clamped or reinterpreted (§6 "Cost model and finite solver"). The override
+ * is process-wide and meant for tests and offline plan audits. */
+tr_status tr_plan_override(const tr_plan* plan);
+
+/* Synchronises the current device, then reads and clears its device error
+ * word: TR_OK, or TR_ERR_DEVICE_TIMEOUT if a bounded wait gave up. */
+tr_status tr_last_device_error(void);
+
+/* Static text for a status. */
+const char* tr_status_string(tr_status status);
+
+/* Text describing the last error returned on the calling thread ("" if none). */
+const char* tr_last_error_message(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t tr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TR_H */

@@ -1,0 +1,111 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp32_row_reduction_gb300 as trlib
+from fp32_row_reduction_gb300 import build as trbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    trbuild.build()
+    return trlib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tr_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_operators():
+    names = declared_functions()
+    for n in ("tr_softmax_f32", "tr_rmsnorm_f32", "tr_layernorm_f32", "tr_cross_entropy_f32"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in trlib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert trlib.tr_status_string(0) == "TR_OK"
+    assert trlib.tr_status_string(1) == "TR_ERR_INVALID_ARG"
+    assert trlib.tr_status_string(4) == "TR_ERR_DEVICE_TIMEOUT"
+    assert lib.tr_version() >= 100
+
+
+def test_plan_struct_layout_matches_header():
+    # int32 x 10, int64, double, int32 x 2 -> 64 bytes with natural alignment
+    assert ctypes.sizeof(trlib.tr_plan) == 64
+    assert ctypes.sizeof(trlib.tr_device_desc) == 40
+
+
+FAKE = 1 << 20  # host-side fake "device" addresses: validation runs before any CUDA call
+
+
+@pytest.mark.parametrize("args,why", [
+    ((FAKE, FAKE + 4096, 1, 1, 7, None), "bad order"),
+    ((FAKE, FAKE + 4096, -1, 8, 0, None), "rows < 0"),
+    ((FAKE, FAKE + 4096, 4, 0, 0, None), "cols < 1"),
+    ((FAKE, FAKE + 4096, 4, 1 << 31, 0, None), "cols >= 2^31"),
+    ((None, FAKE, 4, 8, 0, None), "null x"),
+    ((FAKE, None, 4, 8, 0, None), "null y"),
+    ((FAKE + 2, FAKE + 4096, 4, 8, 0, None), "x not 4-byte aligned"),
+    ((FAKE, FAKE + 64, 4, 8, 0, None), "x and y overlap"),
+    ((FAKE, FAKE, 4, 8, 0, None), "in place"),
+])
+def test_softmax_rejects(lib, args, why):
+    assert trlib.tr_softmax_f32(*args) == trlib.TR_ERR_INVALID_ARG, why
+    assert trlib.tr_last_error_message() != ""
+
+
+def test_zero_rows_is_a_no_op(lib):
+    assert trlib.tr_softmax_f32(None, None, 0, 5, 0, None) == trlib.TR_OK
+    assert trlib.tr_cross_entropy_f32(None, None, None, 0, 5, 0, None) == trlib.TR_OK
+
+
+@pytest.mark.parametrize("eps", [-1e-5, float("nan"), float("inf")])
+def test_norms_reject_bad_eps(lib, eps):
+    assert trlib.tr_rmsnorm_f32(FAKE, None, FAKE + 4096, 2, 8, eps, 0, None) == trlib.TR_ERR_INVALID_ARG
+    assert trlib.tr_layernorm_f32(FAKE, None, None, FAKE + 4096, 2, 8, eps, 0, None) == trlib.TR_ERR_INVALID_ARG
+
+
+def test_norm_output_must_not_alias_parameters(lib):
+    # y overlaps w / beta
+    assert trlib.tr_rmsnorm_f32(FAKE, FAKE + 4096, FAKE + 4096, 2, 8, 1e-5, 0, None) == trlib.TR_ERR_INVALID_ARG
+    assert trlib.tr_layernorm_f32(FAKE, None, FAKE + 4100, FAKE + 4096, 2, 8, 1e-5, 0, None) \
+        == trlib.TR_ERR_INVALID_ARG
+
+
+def test_cross_entropy_rejects(lib):
+    f = trlib.tr_cross_entropy_f32
+    assert f(FAKE, None, FAKE + 8192, 4, 8, 0, None) == trlib.TR_ERR_INVALID_ARG       # null labels
+    assert f(FAKE, FAKE + 8196, FAKE + 16384, 4, 8, 0, None) == trlib.TR_ERR_INVALID_ARG  # labels misaligned
+    assert f(FAKE, FAKE + 8192, FAKE + 8, 4, 8, 0, None) == trlib.TR_ERR_INVALID_ARG   # losses inside logits
+    assert f(FAKE, FAKE + 8192, FAKE + 8200, 4, 8, 0, None) == trlib.TR_ERR_INVALID_ARG  # losses inside labels
+
+
+def test_calls_without_a_gpu_fail_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments: the library reaches CUDA and reports the missing device
+    assert trlib.tr_softmax_f32(FAKE, FAKE + 4096, 4, 8, 0, None) == trlib.TR_ERR_CUDA
+
+
+def test_override_rejects_malformed(lib):
+    p = trlib.tr_plan(op=9)
+    assert trlib.tr_plan_override(p) == trlib.TR_ERR_INVALID_ARG
+    p = trlib.tr_plan(op=0, kind=17)
+    assert trlib.tr_plan_override(p) == trlib.TR_ERR_INVALID_ARG
+    assert trlib.tr_plan_override(None) == trlib.TR_OK

@@ -1,0 +1,339 @@
+"""GPU parity: the CUDA path against the CPU oracle, through the C-ABI.
+
+Unordered policy: |gpu - oracle| <= 1e-6 + 2e-6 * |oracle| element by element
+(the oracle is FP64). Ordered policy: bit-identical to the OT-1024 emulation
+and within the same tolerance of the FP64 oracle. Shapes follow the page's
+test list ("TIRx Metal reduction lowering" §8: row widths 127/257/1024/4096,
+softmax 3x4096, LayerNorm 3x4096, cross-entropy 7x4096, 7x1024, widths
+96..1024, ragged domains, sentinel guard rows) plus the benchmark workloads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import fp32_row_reduction_gb300 as tr
+
+pytestmark = pytest.mark.gpu
+
+RTOL, ATOL = 2e-6, 1e-6
+DEV = "cuda:0"
+
+SMALL_SHAPES = [(1, 1), (2, 1), (5, 3), (3, 7), (4, 127), (4, 257), (17, 257), (4, 1024), (3, 4096), (7, 4096),
+                (7, 1024), (5, 96), (5, 160), (5, 224), (5, 288), (5, 512), (37, 1537), (1000, 96), (64, 12289),
+                (256, 3072), (9, 20000), (3, 70001)]
+OPS = ["softmax", "rmsnorm", "layernorm", "cross_entropy"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tr.load()
+    yield
+    tr.tr_plan_override(None)
+
+
+def make(op, rows, cols, seed, var=None, row_offset=True):
+    if op == "softmax":
+        return synth.make_inputs(op, rows, cols, seed, var=4.0 if var is None else var, device=DEV)
+    if op == "cross_entropy":
+        d = synth.make_inputs(op, rows, cols, seed, var=9.0 if var is None else var, device=DEV)
+        return d
+    return synth.make_inputs(op, rows, cols, seed, row_offset=row_offset, device=DEV)
+
+
+def host(d):
+    return {k: v.cpu().numpy() for k, v in d.items()}
+
+
+def reference(op, h, eps=1e-5):
+    if op == "softmax":
+        return oracle.softmax(h["x"])
+    if op == "rmsnorm":
+        return oracle.rmsnorm(h["x"], h.get("w"), eps)
+    if op == "layernorm":
+        return oracle.layernorm(h["x"], h.get("w"), h.get("b"), eps)
+    return oracle.cross_entropy(h["x"], h["labels"])
+
+
+def emulated(op, h, eps=1e-5):
+    if op == "softmax":
+        return oracle.ot_softmax(h["x"])
+    if op == "rmsnorm":
+        return oracle.ot_rmsnorm(h["x"], h.get("w"), eps)
+    if op == "layernorm":
+        return oracle.ot_layernorm(h["x"], h.get("w"), h.get("b"), eps)
+    return oracle.ot_cross_entropy(h["x"], h["labels"])
+
+
+def assert_close(got, ref, what=""):
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst at {i}: "
+                             f"gpu={got[i]!r} oracle={ref[i]!r}")
+
+
+def run(op, d, order="unordered", out=None):
+    y = tr.run_op(op, d, out=out, order=order)
+    torch.cuda.synchronize()
+    return y
+
+
+# ------------------------------------------------------------------ unordered
+
+@pytest.mark.parametrize("rows,cols", SMALL_SHAPES)
+@pytest.mark.parametrize("op", OPS)
+def test_unordered_matches_oracle(op, rows, cols):
+    d = make(op, rows, cols, seed=rows * 7919 + cols)
+    assert_close(run(op, d).cpu().numpy(), reference(op, host(d)), f"{op} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("op", ["rmsnorm", "layernorm"])
+def test_norms_without_affine(op):
+    d = make(op, 33, 3001, seed=5)
+    d.pop("w")
+    d.pop("b", None)
+    assert_close(run(op, d).cpu().numpy(), reference(op, host(d)), op)
+
+
+def test_layernorm_gamma_only_and_beta_only():
+    d = make("layernorm", 9, 1030, seed=6)
+    h = host(d)
+    y = tr.layernorm(d["x"], d["w"], None)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), oracle.layernorm(h["x"], h["w"], None), "gamma only")
+    y = tr.layernorm(d["x"], None, d["b"])
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), oracle.layernorm(h["x"], None, h["b"]), "beta only")
+
+
+# ------------------------------------------------------------------- ordered
+
+@pytest.mark.parametrize("rows,cols", SMALL_SHAPES)
+@pytest.mark.parametrize("op", OPS)
+def test_ordered_is_bit_exact(op, rows, cols):
+    d = make(op, rows, cols, seed=rows * 104729 + cols)
+    h = host(d)
+    got = run(op, d, order="ordered").cpu().numpy()
+    emu = emulated(op, h)
+    assert np.array_equal(got.view(np.uint32), emu.view(np.uint32)), \
+        f"{op} {rows}x{cols}: {np.sum(got.view(np.uint32) != emu.view(np.uint32))} differing words"
+    assert_close(got, reference(op, h), f"ordered {op} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_ordered_same_bits_cached_and_reread(op):
+    # OT-1024 is defined on columns: the cached and the re-reading realisations agree bit for bit
+    d = make(op, 6, 5000, seed=17)
+    a = run(op, d, order="ordered").cpu().numpy()
+    p = tr.tr_plan(op=tr.OPS[op], order=1, kind=tr.TR_PLAN_ORDERED, lanes_per_row=32, warps_per_row=8,
+                   rows_per_cta=1, cluster_ctas=1, vec_slots=0, block_threads=256)
+    assert tr.tr_plan_override(p) == tr.TR_OK
+    try:
+        b = run(op, d, order="ordered").cpu().numpy()
+    finally:
+        tr.tr_plan_override(None)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_ordered_shift_invariance_exact():
+    # x on a 2^-10 grid, x + 1 exact: x - max is identical, so softmax bits are identical
+    g = torch.randint(-2048, 2049, (5, 3000), generator=torch.Generator().manual_seed(3)).float() / 1024.0
+    a = tr.softmax(g.to(DEV), order="ordered")
+    b = tr.softmax((g + 1.0).to(DEV), order="ordered")
+    torch.cuda.synchronize()
+    assert torch.equal(a.cpu().view(torch.int32), b.cpu().view(torch.int32))
+
+
+# ----------------------------------------------------- every legal plan
+
+def legal_plans(op, rows, cols):
+    """Every plan of the family that the library accepts for this shape."""
+    code = tr.OPS[op]
+    plans = []
+    kinds = [tr.TR_PLAN_XENT] if op == "cross_entropy" else [tr.TR_PLAN_ROWS, tr.TR_PLAN_CLUSTER, tr.TR_PLAN_STREAM]
+    for kind in kinds:
+        if kind in (tr.TR_PLAN_ROWS, tr.TR_PLAN_XENT):
+            ks = [2, 4, 8] if kind == tr.TR_PLAN_XENT else [1, 2, 4, 8, 16]
+            for g in (4, 8, 16):
+                for t in (64, 256):
+                    for k in ks:
+                        plans.append(dict(kind=kind, lanes_per_row=g, warps_per_row=1, rows_per_cta=t // g,
+                                          cluster_ctas=1, vec_slots=k, block_threads=t))
+            for s in (1, 2, 3, 5, 8, 32):
+                for q in (1, 2):
+                    if 32 * s * q > 1024:
+                        continue
+                    for k in ks:
+                        plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=s, rows_per_cta=q,
+                                          cluster_ctas=1, vec_slots=k, block_threads=32 * s * q))
+        else:
+            for c in ((2, 3, 8) if kind == tr.TR_PLAN_CLUSTER else (1, 2, 5)):
+                for t in (64, 256, 1024):
+                    for k in ((4, 8, 16) if kind == tr.TR_PLAN_CLUSTER else (0,)):
+                        plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=t // 32, rows_per_cta=1,
+                                          cluster_ctas=c, vec_slots=k, block_threads=t))
+    ok = []
+    for p in plans:
+        pl = tr.tr_plan(op=code, order=0, **p)
+        assert tr.tr_plan_override(pl) == tr.TR_OK
+        try:
+            tr.tr_plan_describe(code, rows, cols, 0)
+            ok.append(p)
+        except tr.TrError as e:
+            assert e.status == tr.TR_ERR_UNSUPPORTED
+    tr.tr_plan_override(None)
+    return ok
+
+
+@pytest.mark.parametrize("rows,cols", [(5, 3), (17, 257), (3, 1030), (7, 4096), (2, 20001)])
+@pytest.mark.parametrize("op", OPS)
+def test_every_legal_plan_matches_oracle(op, rows, cols):
+    d = make(op, rows, cols, seed=rows + cols)
+    ref = reference(op, host(d))
+    plans = legal_plans(op, rows, cols)
+    assert plans, "no legal plan"
+    try:
+        for p in plans:
+            assert tr.tr_plan_override(tr.tr_plan(op=tr.OPS[op], order=0, **p)) == tr.TR_OK
+            assert_close(run(op, d).cpu().numpy(), ref, f"{op} {rows}x{cols} plan {p}")
+    finally:
+        tr.tr_plan_override(None)
+
+
+def test_illegal_override_is_rejected_not_clamped():
+    # 8 lanes x 1 slot cannot hold a 4096-wide row: the call fails, nothing is launched
+    d = make("softmax", 2, 4096, seed=1)
+    y = torch.full_like(d["x"], 7.0)
+    p = tr.tr_plan(op=0, order=0, kind=tr.TR_PLAN_ROWS, lanes_per_row=8, warps_per_row=1, rows_per_cta=8,
+                   cluster_ctas=1, vec_slots=1, block_threads=64)
+    assert tr.tr_plan_override(p) == tr.TR_OK
+    try:
+        st = tr.tr_softmax_f32(d["x"].data_ptr(), y.data_ptr(), 2, 4096, 0, torch.cuda.current_stream().cuda_stream)
+        assert st == tr.TR_ERR_UNSUPPORTED
+    finally:
+        tr.tr_plan_override(None)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
+# ------------------------------------------- alignment, guards, labels
+
+@pytest.mark.parametrize("xoff,yoff", [(1, 1), (2, 2), (3, 3), (1, 0), (0, 3), (2, 1)])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "layernorm"])
+@pytest.mark.parametrize("order", ["unordered", "ordered"])
+def test_unaligned_rows_and_outputs(op, xoff, yoff, order):
+    rows, cols = 6, 1029
+    d = make(op, rows, cols, seed=xoff * 10 + yoff)
+    xbig = torch.empty(rows * cols + 8, device=DEV)
+    x = xbig[xoff:xoff + rows * cols].view(rows, cols)
+    x.copy_(d["x"])
+    ybig = torch.full((rows * cols + 8,), float("nan"), device=DEV)
+    y = ybig[yoff:yoff + rows * cols].view(rows, cols)
+    d2 = dict(d, x=x)
+    if "w" in d2:  # weights misaligned too
+        wbig = torch.empty(cols + 4, device=DEV)
+        wbig[1:1 + cols].copy_(d["w"])
+        d2["w"] = wbig[1:1 + cols]
+    tr.run_op(op, d2, out=y, order=order)
+    torch.cuda.synchronize()
+    h = host(d)
+    if order == "ordered":
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), emulated(op, h).view(np.uint32))
+    else:
+        assert_close(y.cpu().numpy(), reference(op, h), f"{op} x+{xoff} y+{yoff}")
+    hb = ybig.cpu().numpy()
+    assert np.isnan(hb[:yoff]).all() and np.isnan(hb[yoff + rows * cols:]).all()
+
+
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "layernorm"])
+def test_sentinel_guard_rows_untouched(op):
+    rows, cols, guard = 23, 777, 2
+    d = make(op, rows, cols, seed=99)
+    big = torch.full((rows + 2 * guard, cols), -12345.0, device=DEV)
+    out = big[guard:guard + rows]
+    tr.run_op(op, d, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(big[:guard] == -12345.0) and torch.all(big[guard + rows:] == -12345.0)
+    assert_close(out.cpu().numpy(), reference(op, host(d)), op)
+
+
+@pytest.mark.parametrize("order", ["unordered", "ordered"])
+def test_cross_entropy_out_of_range_labels_select_zero(order):
+    rows, cols = 8, 5000
+    d = make("cross_entropy", rows, cols, seed=11)
+    lab = torch.tensor([-1, cols, cols + 7, -(2 ** 63), 2 ** 63 - 1, 0, cols - 1, 123], dtype=torch.int64,
+                       device=DEV)
+    d["labels"] = lab
+    got = run("cross_entropy", d, order=order).cpu().numpy()
+    h = host(d)
+    assert_close(got, oracle.cross_entropy(h["x"], h["labels"]), "labels")
+    if order == "ordered":
+        assert np.array_equal(got.view(np.uint32), oracle.ot_cross_entropy(h["x"], h["labels"]).view(np.uint32))
+
+
+def test_special_rows():
+    x = torch.zeros(6, 3000, device=DEV)
+    x[1] = 5.0                      # constant row
+    x[2, 17] = 80.0                 # one dominant logit
+    x[3] = torch.linspace(-30, 30, 3000, device=DEV)
+    x[4, ::2] = -1e30               # huge negative entries
+    x[5] = 1e-30                    # tiny
+    y = tr.softmax(x)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), oracle.softmax(x.cpu().numpy()), "special softmax rows")
+    yl = tr.layernorm(x, None, None)
+    torch.cuda.synchronize()
+    hl = oracle.layernorm(x.cpu().numpy(), None, None)
+    assert_close(yl[[0, 1, 2, 3, 5]].cpu().numpy(), hl[[0, 1, 2, 3, 5]], "special layernorm rows")
+
+
+def test_integer_rows_reduce_exactly():
+    # small integers: every partial sum is exact, so the unordered RMSNorm
+    # statistic equals the exact one and y matches the oracle to rounding
+    g = torch.Generator().manual_seed(5)
+    x = torch.randint(-8, 9, (7, 4099), generator=g).float()
+    y = tr.rmsnorm(x.to(DEV), None, 0.0)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), oracle.rmsnorm(x.numpy(), None, 0.0), "integer rmsnorm")
+
+
+# ------------------------------------------- the workloads at full size
+
+FULL = [
+    ("softmax_37x1537", None), ("rmsnorm_256x3072", None), ("layernorm_256x3072", None),
+    ("rmsnorm_64x12289", None), ("layernorm_64x12289", None), ("softmax_768x6144", None),
+    ("rmsnorm_768x6144", None), ("layernorm_768x6144", None), ("cross_entropy_4096x50257", 96),
+    ("softmax_16x65536", None), ("softmax_16x262144", None), ("softmax_16x1048576", None),
+    ("softmax_65536x128", 4096), ("layernorm_16x65536", None), ("layernorm_16x262144", None),
+    ("layernorm_16x1048576", None), ("layernorm_65536x128", 4096),
+]
+
+
+@pytest.mark.parametrize("name,sample", FULL, ids=[f[0] for f in FULL])
+def test_workload_full_size(name, sample):
+    w = synth.WORKLOADS[name]
+    op = w["op"]
+    d = synth.workload_inputs(name, device=DEV)
+    y = run(op, d)
+    rows = w["rows"]
+    idx = np.arange(rows) if sample is None else np.unique(
+        np.linspace(0, rows - 1, sample).astype(np.int64))
+    it = torch.as_tensor(idx, device=DEV)
+    hs = {k: (v[it].cpu().numpy() if k in ("x", "labels") else v.cpu().numpy()) for k, v in d.items()}
+    assert_close(y[it].cpu().numpy(), reference(op, hs), name)
+
+
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "layernorm"])
+def test_768x6144_ordered_bit_exact(op):
+    d = synth.workload_inputs(f"{op}_768x6144", device=DEV)
+    got = run(op, d, order="ordered").cpu().numpy()
+    h = host(d)
+    assert np.array_equal(got.view(np.uint32), emulated(op, h).view(np.uint32))
+    assert_close(got, reference(op, h), f"ordered {op} 768x6144")
