@@ -33,6 +33,12 @@ __device__ __forceinline__ float ex2(float t) {
     return r;
 }
 
+// m * log2(e) rounded on its own. __fmul_rn is never fused into a following
+// add, so mb_of(a) - mb_of(b) is exactly 0 when a == b; a plain a*L2E - mb
+// may be contracted into fma(a, L2E, -mb), which leaves the rounding residual
+// of mb and lets every rescale of a running sum drift by 2^residual.
+__device__ __forceinline__ float mb_of(float m) { return __fmul_rn(m, kL2E); }
+
 // Read-only 128-bit load of data that is read exactly once (no L1 allocation).
 __device__ __forceinline__ float4 ld_stream4(const float* p) {
     float4 v;

@@ -122,7 +122,7 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
 #pragma unroll
         for (int j = 0; j < K; ++j) m = fmaxf(m, fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w)));
         m = red(m, MaxOp{});
-        const float mb = m * kL2E;
+        const float mb = mb_of(m);
         float s = 0.0f;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
@@ -301,7 +301,6 @@ __global__ void __launch_bounds__(max_threads_for<OP, K>()) cluster_cached_kerne
 struct MaxSum {
     float m, s;
 };
-__device__ __forceinline__ float mb_of(float m) { return m * kL2E; }
 __device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
     const float m = fmaxf(a.m, b.m);
     if (m == MaxOp::id()) return MaxSum{m, 0.0f};
