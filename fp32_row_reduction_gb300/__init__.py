@@ -41,6 +41,8 @@ TR_PLAN_CLUSTER = 1
 TR_PLAN_STREAM = 2
 TR_PLAN_XENT = 3
 TR_PLAN_ORDERED = 4
+TR_PLAN_STAGED = 5
+TR_PLAN_FLAG_PARAMS_IN_REGISTERS = 1
 
 OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LAYERNORM,
        "cross_entropy": TR_OP_CROSS_ENTROPY}
@@ -54,11 +56,11 @@ class tr_plan(ctypes.Structure):
         ("rows_per_cta", ctypes.c_int32), ("cluster_ctas", ctypes.c_int32),
         ("vec_slots", ctypes.c_int32), ("block_threads", ctypes.c_int32),
         ("ctas_per_sm", ctypes.c_int32), ("grid_ctas", ctypes.c_int64), ("est_us", ctypes.c_double),
-        ("candidates", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("candidates", ctypes.c_int32), ("flags", ctypes.c_int32),
     ]
 
     def as_dict(self):
-        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class tr_device_desc(ctypes.Structure):
@@ -92,6 +94,7 @@ SIGNATURES = {
                             ctypes.POINTER(tr_plan)], _I32),
     "tr_plan_override": ([ctypes.POINTER(tr_plan)], _I32),
     "tr_last_device_error": ([], _I32),
+    "tr_debug_force_wait_timeout": ([_I32], _I32),
     "tr_status_string": ([_I32], ctypes.c_char_p),
     "tr_last_error_message": ([], ctypes.c_char_p),
     "tr_version": ([], _I32),
@@ -170,6 +173,10 @@ def tr_plan_override(plan: tr_plan | None) -> int:
 
 def tr_last_device_error() -> int:
     return load().tr_last_device_error()
+
+
+def tr_debug_force_wait_timeout(enable: bool) -> int:
+    return load().tr_debug_force_wait_timeout(1 if enable else 0)
 
 
 def tr_status_string(status: int) -> str:

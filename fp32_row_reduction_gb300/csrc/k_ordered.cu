@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kOrderedThreads) ot_kernel(const RowArgs a) {
     constexpr int KC = kCached ? K : 1;
     float q[KC][4];
     bool ok[KC][4];
+    pdl_enter();
     if constexpr (kCached) {
 #pragma unroll
         for (int j = 0; j < K; ++j) {
@@ -232,10 +233,26 @@ __global__ void __launch_bounds__(kOrderedThreads) ot_kernel(const RowArgs a) {
     if constexpr (OP == OP_SOFTMAX || OP == OP_XENT) {
         fold(ident, mx, __int_as_float(0xff800000), leaf);
         const float m = tree<Max>(leaf, gpart, buf);
-        fold([m](float v, int) { return exp_ot(__fsub_rn(v, m)); }, add, 0.0f, leaf);
-        const float s = tree<Add>(leaf, gpart, buf);
+        float s;
+        if constexpr (kCached) {
+            // exp once per element, kept in place: the sum below folds the same
+            // values in the same leaf order as exp_ot(x - m) would
+#pragma unroll
+            for (int j = 0; j < K; ++j)
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (ok[j][v]) q[j][v] = exp_ot(__fsub_rn(q[j][v], m));
+            fold(ident, add, 0.0f, leaf);
+            s = tree<Add>(leaf, gpart, buf);
+        } else {
+            fold([m](float v, int) { return exp_ot(__fsub_rn(v, m)); }, add, 0.0f, leaf);
+            s = tree<Add>(leaf, gpart, buf);
+        }
         if constexpr (OP == OP_SOFTMAX) {
-            emit([m, s](float v, int) { return __fdiv_rn(exp_ot(__fsub_rn(v, m)), s); });
+            if constexpr (kCached)
+                emit([s](float e, int) { return __fdiv_rn(e, s); });
+            else
+                emit([m, s](float v, int) { return __fdiv_rn(exp_ot(__fsub_rn(v, m)), s); });
         } else {
             if (threadIdx.x == 0) {
                 const int64_t label = a.labels[row];

@@ -2,5 +2,7 @@
 #include "tr_dispatch.cuh"
 
 namespace tr {
-const void* kernel_softmax(int kind, int lanes, int slots) { return unordered_table<OP_SOFTMAX>(kind, lanes, slots); }
+const void* kernel_softmax(int kind, int lanes, int slots, int flags) {
+    return unordered_table<OP_SOFTMAX>(kind, lanes, slots, flags);
+}
 }  // namespace tr

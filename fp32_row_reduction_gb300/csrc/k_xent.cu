@@ -2,8 +2,8 @@
 #include "tr_row_kernels.cuh"
 
 namespace tr {
-const void* kernel_xent(int kind, int lanes, int slots) {
-    if (kind != TR_PLAN_XENT) return nullptr;
+const void* kernel_xent(int kind, int lanes, int slots, int flags) {
+    if (kind != TR_PLAN_XENT || flags) return nullptr;
     switch (lanes) {
         case 4: return slots == 2 ? reinterpret_cast<const void*>(xent_kernel<4, 2>) : nullptr;
         case 8: return slots == 2 ? reinterpret_cast<const void*>(xent_kernel<8, 2>) : nullptr;

@@ -41,14 +41,35 @@ tr_status cuda_fail(cudaError_t e, const char* what) {
 struct DeviceState {
     bool ready = false;
     tr_device_desc desc{};
+    unsigned* err = nullptr;  // device address of g_device_error on this device
     std::map<std::tuple<int, int64_t, int64_t, int, int>, tr_plan> plans;  // (op, rows, cols, order, align16)
-    std::map<std::tuple<const void*, int, int>, int> occ;                   // (kernel, threads, cluster) -> CTAs/SM
+    std::map<std::tuple<const void*, int, int, size_t>, int> occ;  // (kernel, threads, cluster, smem) -> CTAs/SM
+    std::map<const void*, bool> smem_opt_in;                        // kernels allowed large dynamic smem
 };
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
 bool g_override_set[4] = {false, false, false, false};
 tr_plan g_override[4];
+int g_debug_flags = 0;
+// Launch with programmatic stream serialization (dependent launches overlap
+// their launch latency with the previous kernel's tail); TR_DISABLE_PDL=1 turns it off.
+const bool g_pdl = [] {
+    const char* v = std::getenv("TR_DISABLE_PDL");
+    return !(v && v[0] == '1');
+}();
+constexpr long long kWaitNs = 2000000000LL;  // a bounded device wait gives up after 2 s
+
+// Allow a kernel the full dynamic shared memory budget (once per kernel and device).
+bool opt_in_smem(DeviceState& st, const void* fn) {
+    auto it = st.smem_opt_in.find(fn);
+    if (it != st.smem_opt_in.end()) return it->second;
+    const bool ok =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmemBudget) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    st.smem_opt_in[fn] = ok;
+    return ok;
+}
 
 tr_status device_state(int dev, DeviceState** out) {
     DeviceState& st = g_devices[dev];
@@ -73,6 +94,10 @@ tr_status device_state(int dev, DeviceState** out) {
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
         d.max_cluster_ctas = v ? 8 : 1;
         if (const char* bw = std::getenv("TR_HBM_GBS")) d.hbm_gbs = std::atof(bw);
+        void* errp = nullptr;
+        e = cudaGetSymbolAddress(&errp, g_device_error);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+        st.err = static_cast<unsigned*>(errp);
         st.desc = d;
         st.ready = true;
     }
@@ -82,11 +107,11 @@ tr_status device_state(int dev, DeviceState** out) {
 
 // Resident CTAs per SM of a plan's kernel (0 = cannot run). Cluster plans:
 // the device's concurrent clusters times C, spread over the SMs.
-int query_occupancy(DeviceState& st, const tr_plan& p) {
+int query_occupancy(DeviceState& st, const tr_plan& p, size_t smem) {
     const void* fn = kernel_for(p);
     if (!fn) return 0;
     const int C = (p.kind == TR_PLAN_CLUSTER || p.kind == TR_PLAN_STREAM) ? p.cluster_ctas : 1;
-    const auto key = std::make_tuple(fn, p.block_threads, C);
+    const auto key = std::make_tuple(fn, p.block_threads, C, smem);
     auto it = st.occ.find(key);
     if (it != st.occ.end()) return it->second;
     int n = 0;
@@ -96,8 +121,12 @@ int query_occupancy(DeviceState& st, const tr_plan& p) {
         st.occ[key] = 0;
         return 0;
     }
+    if (smem > 0 && !opt_in_smem(st, fn)) {
+        st.occ[key] = 0;
+        return 0;
+    }
     if (C == 1) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, p.block_threads, 0) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, p.block_threads, smem) != cudaSuccess) n = 0;
     } else {
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
@@ -153,20 +182,22 @@ tr_status run(Call& c, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const bool align16 = (a.cols % 4 == 0) && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0);
+    const bool align16 = (a.cols % 4 == 0) && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0) &&
+                         (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.b) % 16 == 0);
     tr_plan plan;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         DeviceState* st = nullptr;
         tr_status s = device_state(dev, &st);
         if (s != TR_OK) return s;
-        OccupancyFn occ = [st](const tr_plan& p) { return query_occupancy(*st, p); };
+        OccupancyFn occ = [st](const tr_plan& p, size_t smem) { return query_occupancy(*st, p, smem); };
+        a.err = st->err;
         if (g_override_set[c.op]) {
             plan = g_override[c.op];
             plan.op = c.op;
             plan.order = c.order;
             const char* why = "";
-            s = check_plan(st->desc, occ, &plan, a.rows, a.cols, &why);
+            s = check_plan(st->desc, occ, &plan, a.rows, a.cols, align16, &why);
             if (s != TR_OK) return fail(TR_ERR_UNSUPPORTED, std::string("plan override rejected: ") + why);
             plan.est_us = estimate_us(st->desc, plan, a.rows, a.cols, align16);
         } else {
@@ -185,20 +216,32 @@ tr_status run(Call& c, cudaStream_t stream) {
     if (!fn) return fail(TR_ERR_UNSUPPORTED, "plan has no kernel in this build");
     a.S = plan.warps_per_row;
     a.C = plan.cluster_ctas;
+    a.wait_ns = kWaitNs;
+    a.debug_flags = g_debug_flags;
+    a.nbuf = plan.kind == TR_PLAN_STAGED ? plan.rows_per_cta : 0;
+    a.slot_floats = staged_slot_floats(a.cols);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid_ctas));
     cfg.blockDim = dim3(plan.block_threads);
+    cfg.dynamicSmemBytes = plan_dynamic_smem(plan, a.cols);
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
+    cudaLaunchAttribute attr[2];
+    unsigned nattr = 0;
     if (plan.cluster_ctas > 1) {
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = plan.cluster_ctas;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = plan.cluster_ctas;
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
     }
+    if (g_pdl) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
     void* args[] = {&a};
     e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -212,6 +255,7 @@ RowArgs blank_args(const float* x, int64_t rows, int64_t cols) {
     a.rows = rows;
     a.cols = static_cast<int>(cols);
     a.inv_cols = 1.0f / static_cast<float>(cols);
+    a.cols_f = static_cast<float>(cols);
     a.S = 1;
     a.C = 1;
     return a;
@@ -315,13 +359,13 @@ tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order orde
     DeviceState* st = nullptr;
     s = device_state(dev, &st);
     if (s != TR_OK) return s;
-    OccupancyFn occ = [st](const tr_plan& p) { return query_occupancy(*st, p); };
+    OccupancyFn occ = [st](const tr_plan& p, size_t smem) { return query_occupancy(*st, p, smem); };
     if (g_override_set[op]) {
         tr_plan p = g_override[op];
         p.op = op;
         p.order = order;
         const char* why = "";
-        s = check_plan(st->desc, occ, &p, rows, cols, &why);
+        s = check_plan(st->desc, occ, &p, rows, cols, cols % 4 == 0, &why);
         if (s != TR_OK) return fail(TR_ERR_UNSUPPORTED, std::string("plan override rejected: ") + why);
         p.est_us = estimate_us(st->desc, p, rows, cols, cols % 4 == 0);
         *out = p;
@@ -353,9 +397,15 @@ tr_status tr_plan_override(const tr_plan* plan) {
         return TR_OK;
     }
     if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
-    if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_ORDERED) return fail(TR_ERR_INVALID_ARG, "bad plan kind");
+    if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_STAGED) return fail(TR_ERR_INVALID_ARG, "bad plan kind");
     g_override[plan->op] = *plan;
     g_override_set[plan->op] = true;
+    return TR_OK;
+}
+
+tr_status tr_debug_force_wait_timeout(int32_t enable) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_debug_flags = enable ? (g_debug_flags | kDebugForceTimeout) : (g_debug_flags & ~kDebugForceTimeout);
     return TR_OK;
 }
 

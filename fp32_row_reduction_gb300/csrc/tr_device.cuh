@@ -33,6 +33,15 @@ __device__ __forceinline__ float ex2(float t) {
     return r;
 }
 
+// Programmatic dependent launch. Every kernel waits for the grids it depends
+// on (their memory operations complete and visible) before its first global
+// read or write, then lets the next launch on the stream start its own
+// prologue; without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // m * log2(e) rounded on its own. __fmul_rn is never fused into a following
 // add, so mb_of(a) - mb_of(b) is exactly 0 when a == b; a plain a*L2E - mb
 // may be contracted into fma(a, L2E, -mb), which leaves the rounding residual
@@ -82,6 +91,72 @@ __device__ __forceinline__ float warp_allreduce(float v) {
     return v;
 }
 
+// ---------------------------------------------------------------------------
+// Statistics merged across workers (one shuffle butterfly / shared exchange each).
+// ---------------------------------------------------------------------------
+// (m, s): m is the max of the elements seen and s = sum of 2^(x*log2e - mb(m))
+// with mb(m) = RN(m * log2e). Rescaling by 2^(mb(m_old) - mb(m_new)) keeps every
+// partial sum relative to the same rounded offset its terms were computed with.
+struct MaxSum {
+    float m, s;
+};
+__device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
+    const float m = fmaxf(a.m, b.m);
+    if (m == MaxOp::id()) return MaxSum{m, 0.0f};
+    const float mb = mb_of(m);
+    return MaxSum{m, a.s * ex2(mb_of(a.m) - mb) + b.s * ex2(mb_of(b.m) - mb)};
+}
+// one element x as a (m, s) pair
+__device__ __forceinline__ MaxSum ms_single(float x) { return MaxSum{x, ex2(fmaf(x, kL2E, -mb_of(x)))}; }
+// (n, mean, M2) merged as in Chan, Golub and LeVeque, "Updating formulae and a
+// pairwise algorithm for computing sample variances" (1979).
+struct Moments {
+    float n, mean, m2;
+};
+__device__ __forceinline__ Moments mo_merge(Moments a, Moments b) {
+    const float n = a.n + b.n;
+    if (n == 0.0f) return Moments{0.0f, 0.0f, 0.0f};
+    const float d = b.mean - a.mean;
+    const float fb = b.n / n;
+    return Moments{n, fmaf(d, fb, a.mean), a.m2 + b.m2 + d * d * a.n * fb};
+}
+
+__device__ __forceinline__ MaxSum shfl_xor(MaxSum v, int o) {
+    return MaxSum{__shfl_xor_sync(kFull, v.m, o), __shfl_xor_sync(kFull, v.s, o)};
+}
+__device__ __forceinline__ Moments shfl_xor(Moments v, int o) {
+    return Moments{__shfl_xor_sync(kFull, v.n, o), __shfl_xor_sync(kFull, v.mean, o),
+                   __shfl_xor_sync(kFull, v.m2, o)};
+}
+// A float merged by max (a float alone merges by addition).
+struct MaxF {
+    float v;
+};
+__device__ __forceinline__ MaxF merge(MaxF a, MaxF b) { return MaxF{fmaxf(a.v, b.v)}; }
+__device__ __forceinline__ MaxF shfl_xor(MaxF a, int o) { return MaxF{__shfl_xor_sync(kFull, a.v, o)}; }
+__device__ __forceinline__ MaxSum merge(MaxSum a, MaxSum b) { return ms_merge(a, b); }
+__device__ __forceinline__ Moments merge(Moments a, Moments b) { return mo_merge(a, b); }
+__device__ __forceinline__ float merge(float a, float b) { return a + b; }
+__device__ __forceinline__ float shfl_xor(float v, int o) { return __shfl_xor_sync(kFull, v, o); }
+
+template <class T>
+__device__ __forceinline__ T identity_of();
+template <>
+__device__ __forceinline__ float identity_of<float>() { return 0.0f; }
+template <>
+__device__ __forceinline__ MaxF identity_of<MaxF>() { return MaxF{MaxOp::id()}; }
+template <>
+__device__ __forceinline__ MaxSum identity_of<MaxSum>() { return MaxSum{MaxOp::id(), 0.0f}; }
+template <>
+__device__ __forceinline__ Moments identity_of<Moments>() { return Moments{0.0f, 0.0f, 0.0f}; }
+
+template <class T, int WIDTH>
+__device__ __forceinline__ T warp_merge(T v) {
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) v = merge(v, shfl_xor(v, o));
+    return v;
+}
+
 // The place of one thread inside the row it works on.
 struct RowPos {
     int w;      // worker index within the row's workers (0 .. W-1)
@@ -92,56 +167,108 @@ struct RowPos {
     int lane;
 };
 
-// Reduce one value over the W workers of a row inside one CTA.
-// G < 32: a sub-warp butterfly. G == 32: warp butterfly, then (S > 1) one
-// shared-memory exchange through `part` (2 x 32 floats; `buf` alternates so
-// that consecutive reductions never race on a slot).
-template <class R, int G>
-__device__ __forceinline__ float cta_row_allreduce(float v, const RowPos& p, float (*part)[32], int& buf) {
+// Merge one statistic over the W workers of a row inside one CTA.
+// G < 32: a sub-warp butterfly. G == 32: warp butterfly, then (S > 1) lane 0
+// of each warp publishes its value in `part` (2 x 32 slots of 16 bytes; `buf`
+// alternates so consecutive merges never race on a slot), one barrier, and
+// every warp merges the S published values (identity-padded).
+template <class T, int G>
+__device__ __forceinline__ T cta_row_merge(T v, const RowPos& p, float4 (*part)[32], int& buf) {
     if constexpr (G < 32) {
-        return warp_allreduce<R, G>(v);
+        return warp_merge<T, G>(v);
     } else {
-        v = warp_allreduce<R, 32>(v);
+        v = warp_merge<T, 32>(v);
         if (p.S == 1) return v;
-        float* slot = part[buf];
+        T* slot = reinterpret_cast<T*>(part[buf]);
         buf ^= 1;
         if (p.lane == 0) slot[p.q * p.S + p.s] = v;
         __syncthreads();
-        float t = (p.lane < p.S) ? slot[p.q * p.S + p.lane] : R::id();
-        return warp_allreduce<R, 32>(t);
+        return warp_merge<T, 32>(p.lane < p.S ? slot[p.q * p.S + p.lane] : identity_of<T>());
     }
 }
 
-// Reduce over all threads of a CTA (one row slice per CTA), result in every thread.
-template <class R>
-__device__ __forceinline__ float cta_allreduce(float v, float (*part)[32], int& buf) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    v = warp_allreduce<R, 32>(v);
-    if (nw == 1) return v;
-    float* slot = part[buf];
-    buf ^= 1;
-    if (lane == 0) slot[warp] = v;
-    __syncthreads();
-    float t = (lane < nw) ? slot[lane] : R::id();
-    return warp_allreduce<R, 32>(t);
-}
-
-// Combine one per-CTA value across the C CTAs of a cluster. `cpart` is a
-// 2-slot shared array; slots alternate between consecutive reductions, and
-// the cluster barrier inside each reduction orders a slot's reads before its
-// next write. The caller ends with cluster.sync() before exiting so that no
-// CTA leaves while a peer may still read its shared memory.
-template <class R>
-__device__ __forceinline__ float cluster_allreduce(float v_cta, float* cpart, int& cbuf, int C) {
+// Merge a per-CTA statistic over the C CTAs of a cluster through distributed
+// shared memory. `cpart` has 2 slots of 16 bytes that alternate between merges;
+// the cluster barrier orders a slot's remote reads before its next write. The
+// kernel ends with a cluster barrier so that no CTA exits while a peer may
+// still read its slot.
+template <class T>
+__device__ __forceinline__ T cluster_merge(T v_cta, float4* cpart, int& cbuf, int C) {
     cg::cluster_group cl = cg::this_cluster();
-    float* slot = cpart + cbuf;
+    T* slot = reinterpret_cast<T*>(cpart + cbuf);
     cbuf ^= 1;
     if (threadIdx.x == 0) *slot = v_cta;
     cl.sync();
     const int lane = threadIdx.x & 31;
-    float t = R::id();
-    if (lane < C) t = *cl.map_shared_rank(slot, lane);
-    return warp_allreduce<R, 32>(t);
+    return warp_merge<T, 32>(lane < C ? *cl.map_shared_rank(slot, lane) : identity_of<T>());
+}
+
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copies (TMA, non-tensor form) and mbarriers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+// make initialised barriers visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// order this thread's earlier generic-proxy shared accesses before later async-proxy ones
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// global -> shared bulk copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned), completing `bytes` transactions on `bar`
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Error codes recorded in the device error word.
+constexpr unsigned kErrWaitTimeout = 1u;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar` for at most `limit_ns` nanoseconds. On
+// timeout the error word gets kErrWaitTimeout and false is returned; the
+// caller then finishes without trapping.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit_ns,
+                                                  unsigned* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (static_cast<long long>(global_ns() - t0) > limit_ns) break;
+    }
+    if (err) atomicOr(err, kErrWaitTimeout);
+    return false;
 }
 
 // Geometry of one row's 16-byte body: `head` scalars up to the first 16-byte

@@ -21,8 +21,27 @@ const void* rows_table(int slots) {
     return nullptr;
 }
 
+// Staged kernels holding the weights in registers (norms, aligned rows).
 template <int OP>
-const void* unordered_table(int kind, int lanes, int slots) {
+const void* staged_pre_table(int slots) {
+    if constexpr (OP == OP_SOFTMAX) {
+        return nullptr;
+    } else {
+        switch (slots) {
+            case 1: return reinterpret_cast<const void*>(staged_kernel<OP, 1, true>);
+            case 2: return reinterpret_cast<const void*>(staged_kernel<OP, 2, true>);
+            case 4: return reinterpret_cast<const void*>(staged_kernel<OP, 4, true>);
+            case 8: return reinterpret_cast<const void*>(staged_kernel<OP, 8, true>);
+        }
+        return nullptr;
+    }
+}
+
+template <int OP>
+const void* unordered_table(int kind, int lanes, int slots, int flags) {
+    if (flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS)
+        return kind == TR_PLAN_STAGED ? staged_pre_table<OP>(slots) : nullptr;
+    if (flags) return nullptr;
     switch (kind) {
         case TR_PLAN_ROWS:
             switch (lanes) {
@@ -41,6 +60,14 @@ const void* unordered_table(int kind, int lanes, int slots) {
             return nullptr;
         case TR_PLAN_STREAM:
             return slots == 0 ? reinterpret_cast<const void*>(stream_kernel<OP>) : nullptr;
+        case TR_PLAN_STAGED:
+            switch (slots) {
+                case 1: return reinterpret_cast<const void*>(staged_kernel<OP, 1, false>);
+                case 2: return reinterpret_cast<const void*>(staged_kernel<OP, 2, false>);
+                case 4: return reinterpret_cast<const void*>(staged_kernel<OP, 4, false>);
+                case 8: return reinterpret_cast<const void*>(staged_kernel<OP, 8, false>);
+            }
+            return nullptr;
     }
     return nullptr;
 }

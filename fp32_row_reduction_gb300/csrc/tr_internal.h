@@ -19,27 +19,43 @@ struct RowArgs {
     int cols;
     float eps;
     float inv_cols;  // 1 / cols
+    float cols_f;    // (float) cols
     int S;           // warps per row (lanes_per_row == 32)
     int C;           // CTAs per row (cluster / stream plans)
     int y_vec;       // y rows have the same 16-byte phase as x rows
     int has_w, has_b;
+    unsigned* err;         // device error word (bounded waits record timeouts here)
+    long long wait_ns;     // a bounded wait gives up after this many nanoseconds
+    int nbuf;              // staged plans: row slots in the shared-memory ring
+    int slot_floats;       // staged plans: floats per ring slot (multiple of 4)
+    int debug_flags;       // testing: kDebugForceTimeout makes one bounded wait expire
 };
+
+constexpr int kDebugForceTimeout = 1;
+constexpr int kMaxRing = 8;                // staged plans: most rows in flight per CTA
+constexpr int kStagedSmemBudget = 225 * 1024;  // dynamic shared memory per CTA (bytes; 2 KB left for static)
+
+// Floats of one ring slot for rows of `cols` floats: the row's 16-byte-aligned
+// body plus one partial 16-byte chunk on each side.
+inline int staged_slot_floats(int64_t cols) { return static_cast<int>((cols + 3) / 4 * 4 + 8); }
 
 // Kernel entry for a plan, or nullptr when this build has no such
 // instantiation (the plan is then unsupported). One table per operator.
-const void* kernel_softmax(int kind, int lanes, int slots);
-const void* kernel_rmsnorm(int kind, int lanes, int slots);
-const void* kernel_layernorm(int kind, int lanes, int slots);
-const void* kernel_xent(int kind, int lanes, int slots);
+const void* kernel_softmax(int kind, int lanes, int slots, int flags);
+const void* kernel_rmsnorm(int kind, int lanes, int slots, int flags);
+const void* kernel_layernorm(int kind, int lanes, int slots, int flags);
+const void* kernel_xent(int kind, int lanes, int slots, int flags);
 const void* kernel_ordered(int op, int slots);
+// Dynamic shared memory a plan's kernel needs (0 for all but staged plans).
+size_t plan_dynamic_smem(const tr_plan& p, int64_t cols);
 
 inline const void* kernel_for(const tr_plan& p) {
-    if (p.kind == TR_PLAN_ORDERED) return kernel_ordered(p.op, p.vec_slots);
+    if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
     switch (p.op) {
-        case TR_OP_SOFTMAX: return kernel_softmax(p.kind, p.lanes_per_row, p.vec_slots);
-        case TR_OP_RMSNORM: return kernel_rmsnorm(p.kind, p.lanes_per_row, p.vec_slots);
-        case TR_OP_LAYERNORM: return kernel_layernorm(p.kind, p.lanes_per_row, p.vec_slots);
-        case TR_OP_CROSS_ENTROPY: return kernel_xent(p.kind, p.lanes_per_row, p.vec_slots);
+        case TR_OP_SOFTMAX: return kernel_softmax(p.kind, p.lanes_per_row, p.vec_slots, p.flags);
+        case TR_OP_RMSNORM: return kernel_rmsnorm(p.kind, p.lanes_per_row, p.vec_slots, p.flags);
+        case TR_OP_LAYERNORM: return kernel_layernorm(p.kind, p.lanes_per_row, p.vec_slots, p.flags);
+        case TR_OP_CROSS_ENTROPY: return kernel_xent(p.kind, p.lanes_per_row, p.vec_slots, p.flags);
     }
     return nullptr;
 }
@@ -48,6 +64,7 @@ inline const void* kernel_for(const tr_plan& p) {
 constexpr int kRowsSlotsSub[] = {1, 2, 4};           // lanes_per_row 4, 8, 16
 constexpr int kRowsSlotsWarp[] = {1, 2, 4, 8, 16};   // lanes_per_row 32
 constexpr int kClusterSlots[] = {4, 8, 16};
+constexpr int kStagedSlots[] = {1, 2, 4, 8};
 constexpr int kOrderedSlots[] = {0, 1, 2, 4, 8, 16}; // 0: re-read plan
 constexpr int kOrderedThreads = 256;                  // OT-1024: 256 workers x 4 leaves
 

@@ -11,19 +11,19 @@
 
 namespace tr {
 
-// Resident CTAs per SM for a fully specified plan, or 0 if it cannot run.
-// For cluster launches: resident CTAs per SM implied by the number of
-// clusters the device can hold at once.
-using OccupancyFn = std::function<int(const tr_plan&)>;
+// Resident CTAs per SM for a fully specified plan using `smem` bytes of
+// dynamic shared memory, or 0 if it cannot run. For cluster launches:
+// resident CTAs per SM implied by the number of clusters the device can hold.
+using OccupancyFn = std::function<int(const tr_plan&, size_t smem)>;
 
 // Host-only occupancy model from a register estimate (used without a GPU).
-int model_occupancy(const tr_device_desc& d, const tr_plan& p);
+int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem);
 
 // Fill grid_ctas and check every legality rule of `p` for this shape.
 // Returns TR_OK, TR_ERR_UNSUPPORTED (illegal for the shape or not built) or
 // TR_ERR_INVALID_ARG (malformed fields). `why` receives a reason.
 tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p, int64_t rows, int64_t cols,
-                     const char** why);
+                     bool align16, const char** why);
 
 // Cost-model estimate in microseconds for a legal plan (grid_ctas and
 // ctas_per_sm filled).

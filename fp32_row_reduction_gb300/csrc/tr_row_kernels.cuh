@@ -30,6 +30,13 @@ constexpr int max_threads_for() {
     return K >= 16 ? 512 : (K >= 8 && OP == OP_LAYERNORM) ? 768 : 1024;
 }
 
+// Staged kernels that also hold K float4 of weights (and of biases) per worker.
+template <int OP, int K, bool PRE>
+constexpr int staged_max_threads() {
+    if (!PRE) return K >= 8 ? 768 : 1024;
+    return K <= 2 ? 1024 : K == 4 ? 768 : (OP == OP_LAYERNORM ? 384 : 512);
+}
+
 template <int OP>
 __device__ __forceinline__ float first_identity() {
     return OP == OP_SOFTMAX ? MaxOp::id() : 0.0f;
@@ -65,29 +72,34 @@ struct SlotMapSeg {  // a CTA's segment [v0, v1) of the row: slot j <-> v0 + j*T
     __device__ __forceinline__ bool ok(int j) const { return idx(j) < v1; }
 };
 
-// Reduce over the workers of one row.
+// Merge a worker statistic over the workers of one row (inside one CTA).
 template <int G>
 struct RowsReducer {
     RowPos p;
-    float (*part)[32];
+    float4 (*part)[32];
     int buf;
-    template <class R>
-    __device__ __forceinline__ float operator()(float v, R) {
-        return cta_row_allreduce<R, G>(v, p, part, buf);
+    template <class T>
+    __device__ __forceinline__ T operator()(T v) {
+        return cta_row_merge<T, G>(v, p, part, buf);
     }
 };
+// ... over the CTA, then over the C CTAs of the cluster (distributed shared memory).
 struct ClusterReducer {
-    float (*part)[32];
+    RowPos p;
+    float4 (*part)[32];
     int buf;
-    float* cpart;
+    float4* cpart;
     int cbuf;
     int C;
-    template <class R>
-    __device__ __forceinline__ float operator()(float v, R) {
-        v = cta_allreduce<R>(v, part, buf);
-        return cluster_allreduce<R>(v, cpart, cbuf, C);
+    template <class T>
+    __device__ __forceinline__ T operator()(T v) {
+        v = cta_row_merge<T, 32>(v, p, part, buf);
+        return cluster_merge<T>(v, cpart, cbuf, C);
     }
 };
+
+__device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
+__device__ __forceinline__ float sum4(float4 v) { return (v.x + v.y) + (v.z + v.w); }
 
 // Load a worker's stripe: K float4 slots plus its head/tail scalar.
 template <int OP, int K, class Map>
@@ -108,20 +120,31 @@ __device__ __forceinline__ void load_stripe(const float* xr, const RowGeom& g, c
 }
 
 // The three cached epilogues. Every worker of the row calls this uniformly
-// (reductions may contain barriers); only stores are predicated on `active`.
-template <int OP, int K, class Map, class Red>
+// (merges may contain a barrier); only the stores are predicated on `active`.
+//   softmax:   m = max (merge 1); e = 2^(x log2e - mb(m)) with one FMA per
+//              element; s = sum e (merge 2); y = e * (1/s)
+//   RMSNorm:   sum of squares (one merge); y = x * rsqrt(ss/N + eps) * w
+//   LayerNorm: mean = sum / N (merge 1, one rounded division); var = sum of
+//              (x - mean)^2 over the cached stripe / N (merge 2: the second pass
+//              runs on registers, no cancellation); y = (x - mean) * rsqrt(var + eps)
+//              * gamma + beta
+// Two cheap float butterflies are shorter on the critical path than one merge
+// of compound statistics, which matters when a CTA reduces rows back to back.
+// PRE: the weight/bias float4s of this worker's slots are already in wr/br
+// (persistent CTAs whose workers see the same columns in every row).
+template <int OP, int K, bool PRE = false, class Map, class Red>
 __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, const RowGeom& g, float4 (&v)[K],
                                                 float hv, float tv, bool own_h, bool own_t, bool active, int wi,
-                                                const Map& map, Red& red) {
+                                                const Map& map, Red& red, const float4 (&wr)[K],
+                                                const float4 (&br)[K]) {
     float* yb = yr + g.head;
     const int ti = g.head + 4 * g.nvec + wi;  // column of this worker's tail scalar
     if constexpr (OP == OP_SOFTMAX) {
-        // m = max; e = exp(x - m) computed as 2^(x*log2e - m*log2e) with one FMA;
-        // y = e * (1/sum e). Missing slots hold -inf, so they contribute e = 0.
+        // missing slots hold -inf: they give e = 0
         float m = fmaxf(hv, tv);
 #pragma unroll
-        for (int j = 0; j < K; ++j) m = fmaxf(m, fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w)));
-        m = red(m, MaxOp{});
+        for (int j = 0; j < K; ++j) m = fmaxf(m, max4(v[j]));
+        m = red(MaxF{m}).v;
         const float mb = mb_of(m);
         float s = 0.0f;
 #pragma unroll
@@ -130,12 +153,12 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
             v[j].y = ex2(fmaf(v[j].y, kL2E, -mb));
             v[j].z = ex2(fmaf(v[j].z, kL2E, -mb));
             v[j].w = ex2(fmaf(v[j].w, kL2E, -mb));
-            s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+            s += sum4(v[j]);
         }
         hv = ex2(fmaf(hv, kL2E, -mb));
         tv = ex2(fmaf(tv, kL2E, -mb));
         s += hv + tv;
-        s = red(s, SumOp{});
+        s = red(s);
         const float inv = 1.0f / s;
         if (!active) return;
 #pragma unroll
@@ -146,12 +169,12 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         if (own_h) yr[wi] = hv * inv;
         if (own_t) yr[ti] = tv * inv;
     } else if constexpr (OP == OP_RMSNORM) {
-        // r = sqrt(sum x^2 / N + eps); y = x * (1/r) * w. Missing slots hold 0.
+        // missing slots hold 0
         float ss = fmaf(hv, hv, tv * tv);
 #pragma unroll
         for (int j = 0; j < K; ++j)
             ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
-        ss = red(ss, SumOp{});
+        ss = red(ss);
         const float rstd = rsqrtf(fmaf(ss, a.inv_cols, a.eps));
         if (!active) return;
         const bool wv = a.has_w && aligned16(a.w + g.head);
@@ -161,7 +184,7 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
                 const int e = 4 * map.idx(j);
                 float4 o = make_float4(v[j].x * rstd, v[j].y * rstd, v[j].z * rstd, v[j].w * rstd);
                 if (a.has_w) {
-                    const float4 wq = ld_param(a.w + g.head + e, wv);
+                    const float4 wq = PRE ? wr[j] : ld_param(a.w + g.head + e, wv);
                     o.x *= wq.x; o.y *= wq.y; o.z *= wq.z; o.w *= wq.w;
                 }
                 st_out(yb + e, o, a.y_vec);
@@ -169,27 +192,25 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         if (own_h) yr[wi] = hv * rstd * (a.has_w ? __ldg(a.w + wi) : 1.0f);
         if (own_t) yr[ti] = tv * rstd * (a.has_w ? __ldg(a.w + ti) : 1.0f);
     } else if constexpr (OP == OP_LAYERNORM) {
-        // mean = sum x / N; c = x - mean; var = sum c^2 / N (second pass over the
-        // cached stripe, no cancellation); y = c * rsqrt(var + eps) * gamma + beta.
+        // missing slots hold 0 for the sum; they are excluded from the second pass
         float sm = hv + tv;
 #pragma unroll
-        for (int j = 0; j < K; ++j) sm += (v[j].x + v[j].y) + (v[j].z + v[j].w);
-        sm = red(sm, SumOp{});
-        const float mean = sm * a.inv_cols;
+        for (int j = 0; j < K; ++j) sm += sum4(v[j]);
+        sm = red(sm);
+        // one rounded division: a product sm * (1/N) could be contracted into
+        // fma(-sm, 1/N, x) below, leaving the mean unrounded (a constant row
+        // would then not centre to exactly 0)
+        const float mean = __fdiv_rn(sm, a.cols_f);
         float sq = 0.0f;
 #pragma unroll
-        for (int j = 0; j < K; ++j) {
+        for (int j = 0; j < K; ++j)
             if (map.ok(j)) {
-                v[j].x -= mean; v[j].y -= mean; v[j].z -= mean; v[j].w -= mean;
-            } else {
-                v[j] = f4(0.0f);
+                const float dx = v[j].x - mean, dy = v[j].y - mean, dz = v[j].z - mean, dw = v[j].w - mean;
+                sq = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, fmaf(dw, dw, sq))));
             }
-            sq = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, sq))));
-        }
-        hv = own_h ? hv - mean : 0.0f;
-        tv = own_t ? tv - mean : 0.0f;
-        sq = fmaf(hv, hv, fmaf(tv, tv, sq));
-        sq = red(sq, SumOp{});
+        if (own_h) sq = fmaf(hv - mean, hv - mean, sq);
+        if (own_t) sq = fmaf(tv - mean, tv - mean, sq);
+        sq = red(sq);
         const float rstd = rsqrtf(fmaf(sq, a.inv_cols, a.eps));
         if (!active) return;
         const bool wv = a.has_w && aligned16(a.w + g.head);
@@ -198,25 +219,26 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         for (int j = 0; j < K; ++j)
             if (map.ok(j)) {
                 const int e = 4 * map.idx(j);
-                float4 o = make_float4(v[j].x * rstd, v[j].y * rstd, v[j].z * rstd, v[j].w * rstd);
+                float4 o = make_float4((v[j].x - mean) * rstd, (v[j].y - mean) * rstd, (v[j].z - mean) * rstd,
+                                       (v[j].w - mean) * rstd);
                 if (a.has_w) {
-                    const float4 wq = ld_param(a.w + g.head + e, wv);
+                    const float4 wq = PRE ? wr[j] : ld_param(a.w + g.head + e, wv);
                     o.x *= wq.x; o.y *= wq.y; o.z *= wq.z; o.w *= wq.w;
                 }
                 if (a.has_b) {
-                    const float4 bq = ld_param(a.b + g.head + e, bv);
+                    const float4 bq = PRE ? br[j] : ld_param(a.b + g.head + e, bv);
                     o.x += bq.x; o.y += bq.y; o.z += bq.z; o.w += bq.w;
                 }
                 st_out(yb + e, o, a.y_vec);
             }
         if (own_h) {
-            float o = hv * rstd;
+            float o = (hv - mean) * rstd;
             if (a.has_w) o *= __ldg(a.w + wi);
             if (a.has_b) o += __ldg(a.b + wi);
             yr[wi] = o;
         }
         if (own_t) {
-            float o = tv * rstd;
+            float o = (tv - mean) * rstd;
             if (a.has_w) o *= __ldg(a.w + ti);
             if (a.has_b) o += __ldg(a.b + ti);
             yr[ti] = o;
@@ -230,7 +252,7 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
 // ---------------------------------------------------------------------------
 template <int OP, int G, int K>
 __global__ void __launch_bounds__(max_threads_for<OP, K>()) rows_cached_kernel(const RowArgs a) {
-    __shared__ float part[2][32];
+    __shared__ float4 part[2][32];
     RowPos p;
     p.lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -258,9 +280,11 @@ __global__ void __launch_bounds__(max_threads_for<OP, K>()) rows_cached_kernel(c
     const bool own_h = p.w < g.head, own_t = p.w < g.tail;
     float4 v[K];
     float hv, tv;
+    pdl_enter();
     load_stripe<OP, K>(xr, g, map, active, p.w, own_h, own_t, v, hv, tv);
     RowsReducer<G> red{p, part, 0};
-    cached_epilogue<OP, K>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red);
+    float4 none[K];
+    cached_epilogue<OP, K>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red, none, none);
 }
 
 // ---------------------------------------------------------------------------
@@ -269,8 +293,8 @@ __global__ void __launch_bounds__(max_threads_for<OP, K>()) rows_cached_kernel(c
 // ---------------------------------------------------------------------------
 template <int OP, int K>
 __global__ void __launch_bounds__(max_threads_for<OP, K>()) cluster_cached_kernel(const RowArgs a) {
-    __shared__ float part[2][32];
-    __shared__ float cpart[2];
+    __shared__ float4 part[2][32];
+    __shared__ float4 cpart[2];
     cg::cluster_group cl = cg::this_cluster();
     const int C = a.C;
     const int rank = static_cast<int>(cl.block_rank());
@@ -283,71 +307,162 @@ __global__ void __launch_bounds__(max_threads_for<OP, K>()) cluster_cached_kerne
     const SlotMapSeg map{static_cast<int>(blockDim.x), t, v0, v1};
     const bool own_h = rank == 0 && t < g.head;
     const bool own_t = rank == C - 1 && t < g.tail;
+    RowPos p;
+    p.w = t;
+    p.W = blockDim.x;
+    p.q = 0;
+    p.s = t >> 5;
+    p.S = blockDim.x >> 5;
+    p.lane = t & 31;
     float4 v[K];
     float hv, tv;
+    pdl_enter();
     load_stripe<OP, K>(xr, g, map, true, t, own_h, own_t, v, hv, tv);
-    ClusterReducer red{part, 0, cpart, 0, C};
-    cached_epilogue<OP, K>(a, a.y + row * a.cols, g, v, hv, tv, own_h, own_t, true, t, map, red);
+    ClusterReducer red{p, part, 0, cpart, 0, C};
+    float4 none[K];
+    cached_epilogue<OP, K>(a, a.y + row * a.cols, g, v, hv, tv, own_h, own_t, true, t, map, red, none, none);
     cl.sync();  // peers may still be reading this CTA's cpart
 }
 
 // ---------------------------------------------------------------------------
-// Merges of partial statistics for the streaming plans.
+// TR_PLAN_STAGED: persistent CTAs over rows blockIdx.x, blockIdx.x + gridDim.x,
+// ...; a ring of nbuf shared-memory slots, each filled by one bulk
+// asynchronous copy (TMA) of a row, so every row of a CTA is requested as soon
+// as a slot is free and reads overlap the writes of earlier rows. One thread
+// issues the copies; the whole CTA reduces each row from registers.
 // ---------------------------------------------------------------------------
 
-// (m, s): m is the max of the elements seen and s = sum of 2^(x*log2e - mb(m))
-// with mb(m) = RN(m * log2e). Rescaling by 2^(mb(m_old) - mb(m_new)) keeps every
-// partial sum relative to the same rounded offset its terms were computed with.
-struct MaxSum {
-    float m, s;
+// The global window copied for a row: its 16-byte-aligned body plus the
+// partial 16-byte chunks holding the head and the tail, when those chunks lie
+// inside the tensor (they may hold neighbouring rows' elements: x is read-only).
+struct StagedWindow {
+    const float* lo;  // first float copied
+    int dst;          // slot float index receiving lo
+    int bytes;        // multiple of 16
+    int off;          // slot float index of body float4 0
+    bool head_global, tail_global;  // head / tail scalars not in the slot
 };
-__device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
-    const float m = fmaxf(a.m, b.m);
-    if (m == MaxOp::id()) return MaxSum{m, 0.0f};
-    const float mb = mb_of(m);
-    return MaxSum{m, a.s * ex2(mb_of(a.m) - mb) + b.s * ex2(mb_of(b.m) - mb)};
-}
-// one element x as a (m, s) pair
-__device__ __forceinline__ MaxSum ms_single(float x) { return MaxSum{x, ex2(fmaf(x, kL2E, -mb_of(x)))}; }
-// (n, mean, M2) merged as in Chan, Golub and LeVeque, "Updating formulae and a
-// pairwise algorithm for computing sample variances" (1979).
-struct Moments {
-    float n, mean, m2;
-};
-__device__ __forceinline__ Moments mo_merge(Moments a, Moments b) {
-    const float n = a.n + b.n;
-    if (n == 0.0f) return Moments{0.0f, 0.0f, 0.0f};
-    const float d = b.mean - a.mean;
-    const float fb = b.n / n;
-    return Moments{n, fmaf(d, fb, a.mean), a.m2 + b.m2 + d * d * a.n * fb};
+__device__ __forceinline__ StagedWindow staged_window(const float* xr, const RowGeom& g, const float* x0,
+                                                      const float* x1) {
+    StagedWindow w;
+    const float* body = xr + g.head;
+    w.off = g.head > 0 ? 4 : 0;
+    const float* lo = body - w.off;
+    const float* hi = body + 4 * g.nvec + (g.tail > 0 ? 4 : 0);
+    w.head_global = lo < x0;
+    w.tail_global = hi > x1;
+    if (w.head_global) lo = body;
+    if (w.tail_global) hi = body + 4 * g.nvec;
+    w.lo = lo;
+    w.dst = lo == body ? w.off : 0;
+    w.bytes = static_cast<int>(hi - lo) * 4;
+    return w;
 }
 
-__device__ __forceinline__ MaxSum shfl_xor(MaxSum v, int o) {
-    return MaxSum{__shfl_xor_sync(kFull, v.m, o), __shfl_xor_sync(kFull, v.s, o)};
-}
-__device__ __forceinline__ Moments shfl_xor(Moments v, int o) {
-    return Moments{__shfl_xor_sync(kFull, v.n, o), __shfl_xor_sync(kFull, v.mean, o),
-                   __shfl_xor_sync(kFull, v.m2, o)};
-}
-__device__ __forceinline__ MaxSum merge(MaxSum a, MaxSum b) { return ms_merge(a, b); }
-__device__ __forceinline__ Moments merge(Moments a, Moments b) { return mo_merge(a, b); }
-__device__ __forceinline__ float merge(float a, float b) { return a + b; }
-__device__ __forceinline__ float shfl_xor(float v, int o) { return __shfl_xor_sync(kFull, v, o); }
+// PRE (norms only): every row starts 16-byte aligned and cols % 4 == 0, so a
+// worker owns the same columns in every row and keeps their weights (and
+// biases) in registers for the whole kernel instead of re-reading them per row.
+template <int OP, int K, bool PRE>
+__global__ void __launch_bounds__(staged_max_threads<OP, K, PRE>()) staged_kernel(const RowArgs a) {
+    extern __shared__ __align__(16) float ring[];
+    __shared__ __align__(8) uint64_t full[kMaxRing];
+    __shared__ __align__(8) uint64_t never;  // testing: a barrier nothing completes
+    __shared__ float4 part[2][32];
+    __shared__ volatile int s_abort;
+    const int T = blockDim.x, t = threadIdx.x;
+    const int nbuf = a.nbuf;
+    const int64_t G = gridDim.x;
+    const int64_t mine = (a.rows - blockIdx.x + G - 1) / G;  // rows blockIdx.x + i*G, i < mine
+    const float* x0 = a.x;
+    const float* x1 = a.x + a.rows * a.cols;
+    if (t == 0) {
+        for (int b = 0; b < nbuf; ++b) mbar_init(&full[b], 1);
+        mbar_init(&never, 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_enter();
+    if ((a.debug_flags & kDebugForceTimeout) && t == 0) mbar_wait_bounded(&never, 0, 1000000LL, a.err);
 
-template <class T>
-__device__ __forceinline__ T identity_of();
-template <>
-__device__ __forceinline__ float identity_of<float>() { return 0.0f; }
-template <>
-__device__ __forceinline__ MaxSum identity_of<MaxSum>() { return MaxSum{MaxOp::id(), 0.0f}; }
-template <>
-__device__ __forceinline__ Moments identity_of<Moments>() { return Moments{0.0f, 0.0f, 0.0f}; }
+    auto issue = [&](int64_t i) {  // thread 0: copy the CTA's i-th row into slot i % nbuf
+        const int64_t row = blockIdx.x + i * G;
+        const float* xr = a.x + row * a.cols;
+        const RowGeom g = row_geom(xr, a.cols);
+        const StagedWindow w = staged_window(xr, g, x0, x1);
+        const int b = static_cast<int>(i % nbuf);
+        float* slot = ring + static_cast<int64_t>(b) * a.slot_floats;
+        if (w.bytes > 0) {
+            mbar_arrive_expect_tx(&full[b], static_cast<uint32_t>(w.bytes));
+            bulk_g2s(slot + w.dst, w.lo, static_cast<uint32_t>(w.bytes), &full[b]);
+        } else {
+            mbar_arrive(&full[b]);
+        }
+    };
+    if (t == 0)
+        for (int64_t i = 0; i < mine && i < nbuf; ++i) issue(i);
 
-template <class T, int WIDTH>
-__device__ __forceinline__ T warp_merge(T v) {
+    RowPos p;
+    p.w = t;
+    p.W = T;
+    p.q = 0;
+    p.s = t >> 5;
+    p.S = T >> 5;
+    p.lane = t & 31;
+    const float id = first_identity<OP>();
+    float4 wr[K], br[K];
+    if constexpr (PRE) {
+        const int nvec = a.cols >> 2;
 #pragma unroll
-    for (int o = WIDTH / 2; o > 0; o >>= 1) v = merge(v, shfl_xor(v, o));
-    return v;
+        for (int j = 0; j < K; ++j) {
+            const int e = 4 * (j * T + t);
+            wr[j] = f4(1.0f);
+            br[j] = f4(0.0f);
+            if (j * T + t < nvec) {
+                if (a.has_w) wr[j] = ld_param4(a.w + e);
+                if (OP == OP_LAYERNORM && a.has_b) br[j] = ld_param4(a.b + e);
+            }
+        }
+    }
+    // one reducer for all rows: its two shared buffers alternate, so a row's
+    // merge never overwrites a slot the previous row's merge may still read
+    RowsReducer<32> red{p, part, 0};
+    for (int64_t i = 0; i < mine; ++i) {
+        const int b = static_cast<int>(i % nbuf);
+        const uint32_t parity = static_cast<uint32_t>((i / nbuf) & 1);
+        const int64_t row = blockIdx.x + i * G;
+        const float* xr = a.x + row * a.cols;
+        const RowGeom g = row_geom(xr, a.cols);
+        const StagedWindow w = staged_window(xr, g, x0, x1);
+        const float* slot = ring + static_cast<int64_t>(b) * a.slot_floats;
+        if (!mbar_wait_bounded(&full[b], parity, a.wait_ns, a.err)) s_abort = 1;
+        const SlotMapRows map{T, t, g.nvec};
+        float4 v[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            v[j] = f4(id);
+            if (map.ok(j)) v[j] = *reinterpret_cast<const float4*>(slot + w.off + 4 * map.idx(j));
+        }
+        const bool own_h = t < g.head, own_t = t < g.tail;
+        float hv = id, tv = id;
+        if (own_h) hv = w.head_global ? ld_stream1(xr + t) : slot[w.off - g.head + t];
+        if (own_t) tv = w.tail_global ? ld_stream1(xr + g.head + 4 * g.nvec + t) : slot[w.off + 4 * g.nvec + t];
+        cached_epilogue<OP, K, PRE>(a, a.y + row * a.cols, g, v, hv, tv, own_h, own_t, true, t, map, red, wr, br);
+        // the merge's barrier (or, for one warp, this __syncwarp) orders every
+        // thread's reads of the slot, and the abort flag, before what follows
+        if (p.S == 1) __syncwarp();
+        if (s_abort) {
+            // give up without trapping: wait for the copies still in flight, then leave
+            if (t == 0)
+                for (int64_t j = i; j < mine && j < i + nbuf; ++j)
+                    mbar_wait_bounded(&full[j % nbuf], static_cast<uint32_t>((j / nbuf) & 1), a.wait_ns, a.err);
+            return;
+        }
+        if (t == 0 && i + nbuf < mine) {
+            fence_proxy_async_smem();
+            issue(i + nbuf);
+        }
+    }
 }
 
 // Merge over the CTA's threads and then over the C CTAs of the cluster.
@@ -402,6 +517,7 @@ __global__ void __launch_bounds__(1024) stream_kernel(const RowArgs a) {
     const float* xb = xr + g.head;
     const int ti = g.head + 4 * g.nvec + t;
 
+    pdl_enter();
     // ---- pass 1: statistics ----
     Stat st = identity_of<Stat>();
     for (int base = v0; base < v1; base += kStreamU * T) {
@@ -565,6 +681,7 @@ __global__ void __launch_bounds__(1024) xent_kernel(const RowArgs a) {
     const RowGeom g = row_geom(xr, a.cols);
     const float* xb = xr + g.head;
     MaxSum st{MaxOp::id(), 0.0f};
+    pdl_enter();
     if (active) {
         for (int base = 0; base < g.nvec; base += K * p.W) {
             float4 c[K];

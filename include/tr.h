@@ -72,7 +72,9 @@ typedef enum tr_plan_kind {
     TR_PLAN_CLUSTER = 1,  /* a row per cluster of C CTAs; slices cached in registers; partials combined through distributed shared memory */
     TR_PLAN_STREAM = 2,   /* a row per C CTAs (C >= 1); no cache: statistics pass, then the row is re-read (from L2 when it fits) */
     TR_PLAN_XENT = 3,     /* cross-entropy: one streaming pass with an online (max, sum of exp) pair */
-    TR_PLAN_ORDERED = 4   /* OT-1024: 256 threads per row; cached (vec_slots > 0) or re-read (vec_slots == 0) */
+    TR_PLAN_ORDERED = 4,  /* OT-1024: 256 threads per row; cached (vec_slots > 0) or re-read (vec_slots == 0) */
+    TR_PLAN_STAGED = 5    /* persistent CTAs; rows_per_cta rows in flight in a shared-memory ring filled by
+                             bulk asynchronous copies (TMA); each row reduced by the whole CTA from registers */
 } tr_plan_kind;
 
 typedef struct tr_plan {
@@ -81,7 +83,7 @@ typedef struct tr_plan {
     int32_t kind;            /* tr_plan_kind */
     int32_t lanes_per_row;   /* 4, 8, 16 (a row inside a warp) or 32 (a row spans warps_per_row warps) */
     int32_t warps_per_row;   /* S: warps of one CTA cooperating on a row (1 when lanes_per_row < 32) */
-    int32_t rows_per_cta;    /* Q: independent rows packed into one CTA */
+    int32_t rows_per_cta;    /* Q: independent rows packed into one CTA (staged plans: ring slots in flight) */
     int32_t cluster_ctas;    /* C: CTAs cooperating on one row (1 = no cluster) */
     int32_t vec_slots;       /* K: 16-byte row slots cached per thread (0 = not cached) */
     int32_t block_threads;   /* threads per CTA */
@@ -89,8 +91,13 @@ typedef struct tr_plan {
     int64_t grid_ctas;       /* CTAs launched for the problem this plan was selected for */
     double est_us;           /* cost-model estimate in microseconds (a prior, not a measurement) */
     int32_t candidates;      /* legal candidates the selector ranked */
-    int32_t reserved;
+    int32_t flags;           /* TR_PLAN_FLAG_* */
 } tr_plan;
+
+/* Staged norm plans: each worker keeps the weight (and bias) values of its
+ * columns in registers for all the rows of its CTA. Requires 16-byte-aligned
+ * rows (cols % 4 == 0, aligned x) and 16-byte-aligned weight/bias vectors. */
+#define TR_PLAN_FLAG_PARAMS_IN_REGISTERS 1
 
 /* A device as the plan selector sees it (for host-only planning and tests). */
 typedef struct tr_device_desc {
@@ -138,7 +145,7 @@ tr_status tr_cross_entropy_f32(const float* logits, const int64_t* labels, float
 tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order order, tr_plan* out);
 
 /* Host-only selection for a described device (no GPU needed). align16 = 1
- * when every row start is 16-byte aligned. */
+ * when every row start and the weight/bias vectors are 16-byte aligned. */
 tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows, int64_t cols,
                              tr_order order, int32_t align16, tr_plan* out);
 
@@ -159,6 +166,13 @@ const char* tr_status_string(tr_status status);
 
 /* Text describing the last error returned on the calling thread ("" if none). */
 const char* tr_last_error_message(void);
+
+/* Testing hook: while enabled (non-zero), every launch of a plan that contains
+ * bounded device-side waits also performs one wait on a barrier that nothing
+ * completes, with a 1 ms limit, so that the timeout path runs and
+ * tr_last_device_error() reports TR_ERR_DEVICE_TIMEOUT. Results stay correct;
+ * no GPU fault or hang is involved. */
+tr_status tr_debug_force_wait_timeout(int32_t enable);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t tr_version(void);

@@ -157,7 +157,8 @@ def legal_plans(op, rows, cols):
     """Every plan of the family that the library accepts for this shape."""
     code = tr.OPS[op]
     plans = []
-    kinds = [tr.TR_PLAN_XENT] if op == "cross_entropy" else [tr.TR_PLAN_ROWS, tr.TR_PLAN_CLUSTER, tr.TR_PLAN_STREAM]
+    kinds = [tr.TR_PLAN_XENT] if op == "cross_entropy" else [tr.TR_PLAN_ROWS, tr.TR_PLAN_CLUSTER, tr.TR_PLAN_STREAM,
+                                                             tr.TR_PLAN_STAGED]
     for kind in kinds:
         if kind in (tr.TR_PLAN_ROWS, tr.TR_PLAN_XENT):
             ks = [2, 4, 8] if kind == tr.TR_PLAN_XENT else [1, 2, 4, 8, 16]
@@ -173,6 +174,13 @@ def legal_plans(op, rows, cols):
                     for k in ks:
                         plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=s, rows_per_cta=q,
                                           cluster_ctas=1, vec_slots=k, block_threads=32 * s * q))
+        elif kind == tr.TR_PLAN_STAGED:
+            for t in (64, 256, 1024):
+                for nb in (1, 2, 5):
+                    for k in (1, 2, 4, 8):
+                        for flags in (0, tr.TR_PLAN_FLAG_PARAMS_IN_REGISTERS):
+                            plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=t // 32, rows_per_cta=nb,
+                                              cluster_ctas=1, vec_slots=k, block_threads=t, flags=flags))
         else:
             for c in ((2, 3, 8) if kind == tr.TR_PLAN_CLUSTER else (1, 2, 5)):
                 for t in (64, 256, 1024):
@@ -192,7 +200,7 @@ def legal_plans(op, rows, cols):
     return ok
 
 
-@pytest.mark.parametrize("rows,cols", [(5, 3), (17, 257), (3, 1030), (7, 4096), (2, 20001)])
+@pytest.mark.parametrize("rows,cols", [(5, 3), (17, 257), (3, 1030), (7, 4096), (2, 20001), (40, 1024)])
 @pytest.mark.parametrize("op", OPS)
 def test_every_legal_plan_matches_oracle(op, rows, cols):
     d = make(op, rows, cols, seed=rows + cols)
@@ -205,6 +213,70 @@ def test_every_legal_plan_matches_oracle(op, rows, cols):
             assert_close(run(op, d).cpu().numpy(), ref, f"{op} {rows}x{cols} plan {p}")
     finally:
         tr.tr_plan_override(None)
+
+
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "layernorm"])
+@pytest.mark.parametrize("xoff", [0, 1, 3])
+def test_staged_plans_on_unaligned_tensors(op, xoff):
+    # the first and last rows' partial 16-byte chunks fall outside the tensor
+    rows, cols = 37, 1029
+    d = make(op, rows, cols, seed=70 + xoff)
+    xbig = torch.empty(rows * cols + 8, device=DEV)
+    x = xbig[xoff:xoff + rows * cols].view(rows, cols)
+    x.copy_(d["x"])
+    ref = reference(op, host(d))
+    d2 = dict(d, x=x)
+    try:
+        for t, nb in ((128, 3), (512, 1), (1024, 8)):
+            p = tr.tr_plan(op=tr.OPS[op], order=0, kind=tr.TR_PLAN_STAGED, lanes_per_row=32, warps_per_row=t // 32,
+                           rows_per_cta=nb, cluster_ctas=1, vec_slots=8 if t == 128 else 1, block_threads=t)
+            assert tr.tr_plan_override(p) == tr.TR_OK
+            assert_close(tr.run_op(op, d2).cpu().numpy(), ref, f"staged {op} x+{xoff} T={t} nb={nb}")
+    finally:
+        tr.tr_plan_override(None)
+
+
+def test_params_in_registers_rejected_when_unaligned():
+    d = make("layernorm", 8, 1024, seed=3)
+    wbig = torch.empty(1024 + 4, device=DEV)
+    wbig[1:1025].copy_(d["w"])
+    p = tr.tr_plan(op=2, order=0, kind=tr.TR_PLAN_STAGED, lanes_per_row=32, warps_per_row=8, rows_per_cta=2,
+                   cluster_ctas=1, vec_slots=1, block_threads=256, flags=tr.TR_PLAN_FLAG_PARAMS_IN_REGISTERS)
+    assert tr.tr_plan_override(p) == tr.TR_OK
+    try:
+        y = torch.empty_like(d["x"])
+        st = tr.tr_layernorm_f32(d["x"].data_ptr(), wbig[1:1025].data_ptr(), d["b"].data_ptr(), y.data_ptr(), 8,
+                                 1024, 1e-5, 0, torch.cuda.current_stream().cuda_stream)
+        assert st == tr.TR_ERR_UNSUPPORTED
+        tr.layernorm(d["x"], d["w"], d["b"], out=y)   # aligned weights: accepted
+        torch.cuda.synchronize()
+        assert_close(y.cpu().numpy(), reference("layernorm", host(d)), "params in registers")
+    finally:
+        tr.tr_plan_override(None)
+
+
+def test_bounded_wait_timeout_is_reported_without_a_fault():
+    # the testing hook adds one wait on a barrier that nothing completes: it must
+    # expire after its 1 ms limit, set the device error word, and leave the
+    # context usable (no trap, no hang); the results are still correct
+    d = make("softmax", 64, 4096, seed=8)
+    ref = reference("softmax", host(d))
+    p = tr.tr_plan(op=0, order=0, kind=tr.TR_PLAN_STAGED, lanes_per_row=32, warps_per_row=8, rows_per_cta=2,
+                   cluster_ctas=1, vec_slots=4, block_threads=256)
+    assert tr.tr_last_device_error() == tr.TR_OK
+    assert tr.tr_plan_override(p) == tr.TR_OK
+    try:
+        assert tr.tr_debug_force_wait_timeout(True) == tr.TR_OK
+        y = tr.softmax(d["x"])
+        assert tr.tr_last_device_error() == tr.TR_ERR_DEVICE_TIMEOUT
+        assert_close(y.cpu().numpy(), ref, "softmax while timing out")
+    finally:
+        tr.tr_debug_force_wait_timeout(False)
+        tr.tr_plan_override(None)
+    assert tr.tr_last_device_error() == tr.TR_OK          # the word was cleared
+    y = tr.softmax(d["x"])
+    assert tr.tr_last_device_error() == tr.TR_OK
+    assert_close(y.cpu().numpy(), ref, "softmax after the timeout")
 
 
 def test_illegal_override_is_rejected_not_clamped():

