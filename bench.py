@@ -8,8 +8,9 @@ unordered and the ordered (OT-1024) policy: one step = these 6 launches, each
 on its own input and output buffers. Inputs are resident in HBM when timing
 starts; 2 rotating buffer sets (453 MB) keep every launch's data out of L2.
 
-The timed region replays a CUDA graph of unrolled steps (event-record nodes
-between launches give every kernel's duration inside the timed region).
+The timed region replays CUDA graphs of unrolled steps with nothing between
+the launches. A second timed region gives every kernel's duration: per kernel,
+a graph of back-to-back launches of that kernel alone, timed with CUDA events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--suite]
@@ -220,34 +221,49 @@ def run_ours(args, rank, world):
     K = args.steps
     U = min(K, args.unroll)
     rem = K % U
-    g_main, ev_main = build_graph(launches, U, sets, 0, timing=True)
+    # timed region 1 (the step throughput): graphs of unrolled steps with no
+    # nodes between the launches, so back-to-back launches overlap as they would
+    # in an application (programmatic dependent launch)
+    g_main = build_graph(launches, U, sets, 0, timing=False)[0]
     g_rem = build_graph(launches, rem, sets, U % sets, timing=False)[0] if rem else None
-    g_main.replay()  # graph warm-up
+    for g in (g_main,) + ((g_rem,) if g_rem is not None else ()):
+        g.replay()  # graph warm-up
     torch.cuda.synchronize()
 
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
+    def timed(replays):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
+        replays()
+        t1.record()
+        t1.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return t0.elapsed_time(t1)
+
+    def main_steps():
         for _ in range(K // U):
             g_main.replay()
         if g_rem is not None:
             g_rem.replay()
-        t1.record()
-        t1.synchronize()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    elapsed_ms = t0.elapsed_time(t1)
-    # per-launch durations: the events of the last replay of the unrolled graph
-    per = [[] for _ in launches]
-    for row in ev_main:
-        for k in range(len(launches)):
-            per[k].append(row[k].elapsed_time(row[k + 1]))
-    per_us = [1e3 * statistics.mean(v) for v in per]
+
+    reps = max(1, K // U)
+    with ClockSampler(dev.index) as clk:
+        elapsed_ms = timed(main_steps)
+        # timed region 2 (per-kernel durations): for each launch of the step, a
+        # graph of U back-to-back launches of that kernel alone (same buffers
+        # rotation), replayed as often as region 1 replays its steps
+        per_us = []
+        for ln in launches:
+            g1 = build_graph([ln], U, sets, 0, timing=False)[0]
+            g1.replay()
+            torch.cuda.synchronize()
+            per_us.append(1e3 * timed(lambda: [g1.replay() for _ in range(reps)]) / (reps * U))
+            del g1
 
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
@@ -288,6 +304,9 @@ def run_ours(args, rank, world):
         "per_op": per_op,
         "e2e": e2e,
         "gpu_launches": K * len(launches),
+        "per_kernel_timing": {"launches_per_kernel": reps * U, "sum_of_kernels_ms_per_step": round(sum(per_us) / 1e3, 6),
+                              "how": "second timed region: per kernel, a CUDA graph of back-to-back launches of that "
+                                     "kernel alone on the step's rotating buffers, CUDA events on the launching stream"},
         "clocks": clk.summary(),
     }
     if cpu is not None:
