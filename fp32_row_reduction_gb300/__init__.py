@@ -42,6 +42,7 @@ TR_PLAN_STREAM = 2
 TR_PLAN_XENT = 3
 TR_PLAN_ORDERED = 4
 TR_PLAN_STAGED = 5
+TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_FLAG_PARAMS_IN_REGISTERS = 1
 
 OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LAYERNORM,

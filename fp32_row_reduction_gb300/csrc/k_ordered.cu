@@ -20,11 +20,15 @@
 // Every floating-point step is an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn, __fmaf_rn): nothing can be
 // contracted, approximated or flushed, so the bits equal the CPU emulation.
+// A row is divided by its normaliser (softmax sum, RMS, sigma) as a product with
+// the correctly rounded reciprocal: one IEEE division per row, one rounded
+// product per element.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "tr_device.cuh"
 #include "tr_internal.h"
+#include "tr_row_kernels.cuh"
 
 namespace tr {
 namespace ordered {
@@ -149,11 +153,106 @@ __device__ __forceinline__ void store_quad(float* yr, int cols, int j, bool vec,
     }
 }
 
-__device__ __forceinline__ float param(const float* p, int col, bool has, float dflt) {
-    return has ? __ldg(p + col) : dflt;
+// The OT-1024 epilogue of one row whose quads are cached in q: q[j][v] holds
+// column 1024j + 4t + v of the row (t = threadIdx.x), valid when that column is
+// < cols. `vec_out`: the row's output may be written with 16-byte stores.
+template <int OP, int K>
+__device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, float (&q)[K][4], bool vec_out,
+                                              float (*gpart)[8], int& buf) {
+    const int cols = a.cols;
+    const int t = static_cast<int>(threadIdx.x);
+    const int nj = (cols + 1023) / 1024;
+    auto col = [t](int j, int v) { return 1024 * j + 4 * t + v; };
+    auto okc = [&](int j, int v) { return j < nj && col(j, v) < cols; };
+    float leaf[4];
+    // fold f(value, column) into the leaves in increasing column order
+    auto fold = [&](auto elem, auto comb, float init) {
+        leaf[0] = leaf[1] = leaf[2] = leaf[3] = init;
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                if (okc(j, v)) leaf[v] = comb(leaf[v], elem(q[j][v], col(j, v)));
+    };
+    float* yr = a.y + row * cols;
+    auto emit = [&](auto out) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (j >= nj) continue;
+            float o[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) o[v] = out(q[j][v], col(j, v));
+            if (vec_out && okc(j, 3)) {
+                st4(yr + col(j, 0), make_float4(o[0], o[1], o[2], o[3]));
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (okc(j, v)) yr[col(j, v)] = o[v];
+            }
+        }
+    };
+    auto add = [](float p, float v) { return __fadd_rn(p, v); };
+    auto mx = [](float p, float v) { return max2(p, v); };
+    auto ident = [](float v, int) { return v; };
+    const float n = static_cast<float>(cols);
+
+    if constexpr (OP == OP_SOFTMAX || OP == OP_XENT) {
+        fold(ident, mx, __int_as_float(0xff800000));
+        const float m = tree<Max>(leaf, gpart, buf);
+        // exp once per element, kept in place: the sum folds the same values in
+        // the same leaf order as exp_ot(x - m) would
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                if (okc(j, v)) q[j][v] = exp_ot(__fsub_rn(q[j][v], m));
+        fold(ident, add, 0.0f);
+        const float s = tree<Add>(leaf, gpart, buf);
+        if constexpr (OP == OP_SOFTMAX) {
+            const float inv = __fdiv_rn(1.0f, s);
+            emit([inv](float e, int) { return __fmul_rn(e, inv); });
+        } else {
+            if (t == 0) {
+                const float* xr = a.x + row * cols;
+                const int64_t label = a.labels[row];
+                const float sel = (label >= 0 && label < cols) ? __ldg(xr + label) : 0.0f;
+                a.loss[row] = __fsub_rn(__fadd_rn(log_ot(s), m), sel);
+            }
+        }
+    } else if constexpr (OP == OP_RMSNORM) {
+        fold([](float v, int) { return __fmul_rn(v, v); }, add, 0.0f);
+        const float ss = tree<Add>(leaf, gpart, buf);
+        const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), a.eps));
+        const float inv = __fdiv_rn(1.0f, r);
+        const bool hw = a.has_w;
+        const float* w = a.w;
+        emit([inv, hw, w](float v, int c) {
+            const float u = __fmul_rn(v, inv);
+            return hw ? __fmul_rn(u, __ldg(w + c)) : u;
+        });
+    } else {  // OP_LAYERNORM
+        fold(ident, add, 0.0f);
+        const float mean = __fdiv_rn(tree<Add>(leaf, gpart, buf), n);
+        fold([mean](float v, int) {
+            const float c = __fsub_rn(v, mean);
+            return __fmul_rn(c, c);
+        }, add, 0.0f);
+        const float var = __fdiv_rn(tree<Add>(leaf, gpart, buf), n);
+        const float d = __fsqrt_rn(__fadd_rn(var, a.eps));
+        const float inv = __fdiv_rn(1.0f, d);
+        const bool hw = a.has_w, hb = a.has_b;
+        const float *w = a.w, *b = a.b;
+        emit([mean, inv, hw, hb, w, b](float v, int c) {
+            float u = __fmul_rn(__fsub_rn(v, mean), inv);
+            if (hw) u = __fmul_rn(u, __ldg(w + c));
+            if (hb) u = __fadd_rn(u, __ldg(b + c));
+            return u;
+        });
+    }
 }
 
-// K > 0: the row (cols <= 1024*K) is cached in registers. K == 0: re-read.
+// One-shot realisation: a CTA per row. K > 0: the row (cols <= 1024*K) is
+// cached in registers. K == 0: the row is read again for each pass.
 template <int OP, int K>
 __global__ void __launch_bounds__(kOrderedThreads) ot_kernel(const RowArgs a) {
     __shared__ float gpart[2][8];
@@ -162,33 +261,24 @@ __global__ void __launch_bounds__(kOrderedThreads) ot_kernel(const RowArgs a) {
     const int cols = a.cols;
     const float* xr = a.x + row * cols;
     const bool aligned = aligned16(xr);
-    const int nj = (cols + 1023) / 1024;  // column blocks of 1024
-    constexpr bool kCached = K > 0;
-    constexpr int KC = kCached ? K : 1;
-    float q[KC][4];
-    bool ok[KC][4];
     pdl_enter();
-    if constexpr (kCached) {
+    if constexpr (K > 0) {
+        const int nj = (cols + 1023) / 1024;
+        float q[K][4];
 #pragma unroll
         for (int j = 0; j < K; ++j) {
+            bool ok[4];
             if (j < nj) {
-                load_quad(xr, cols, j, aligned, q[j], ok[j]);
+                load_quad(xr, cols, j, aligned, q[j], ok);
             } else {
                 q[j][0] = q[j][1] = q[j][2] = q[j][3] = 0.0f;
-                ok[j][0] = ok[j][1] = ok[j][2] = ok[j][3] = false;
             }
         }
-    }
-    // fold f(x) into the four leaves, column blocks in increasing order
-    auto fold = [&](auto elem, auto comb, float init, float (&leaf)[4]) {
-        leaf[0] = leaf[1] = leaf[2] = leaf[3] = init;
-        if constexpr (kCached) {
-#pragma unroll
-            for (int j = 0; j < K; ++j)
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    if (ok[j][v]) leaf[v] = comb(leaf[v], elem(q[j][v], j * 1024 + 4 * static_cast<int>(threadIdx.x) + v));
-        } else {
+        ot_cached_row<OP, K>(a, row, q, aligned && a.y_vec, gpart, buf);
+    } else {
+        const int nj = (cols + 1023) / 1024;
+        auto fold = [&](auto elem, auto comb, float init, float (&leaf)[4]) {
+            leaf[0] = leaf[1] = leaf[2] = leaf[3] = init;
             for (int j = 0; j < nj; ++j) {
                 float qq[4];
                 bool oo[4];
@@ -197,100 +287,187 @@ __global__ void __launch_bounds__(kOrderedThreads) ot_kernel(const RowArgs a) {
                 for (int v = 0; v < 4; ++v)
                     if (oo[v]) leaf[v] = comb(leaf[v], elem(qq[v], j * 1024 + 4 * static_cast<int>(threadIdx.x) + v));
             }
-        }
-    };
-    // apply out(x, col) to every element and store it
-    auto emit = [&](auto out) {
-        float* yr = a.y + row * cols;
-        const bool vec = aligned && a.y_vec;
-        if constexpr (kCached) {
-#pragma unroll
-            for (int j = 0; j < K; ++j) {
-                if (j < nj) {
-                    float o[4];
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) o[v] = out(q[j][v], j * 1024 + 4 * static_cast<int>(threadIdx.x) + v);
-                    store_quad(yr, cols, j, vec, o, ok[j]);
-                }
-            }
-        } else {
+        };
+        auto emit = [&](auto out) {
+            float* yr = a.y + row * cols;
+            const bool vec = aligned && a.y_vec;
             for (int j = 0; j < nj; ++j) {
                 float qq[4], o[4];
                 bool oo[4];
                 load_quad(xr, cols, j, aligned, qq, oo);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) o[v] = oo[v] ? out(qq[v], j * 1024 + 4 * static_cast<int>(threadIdx.x) + v) : 0.0f;
+                for (int v = 0; v < 4; ++v)
+                    o[v] = oo[v] ? out(qq[v], j * 1024 + 4 * static_cast<int>(threadIdx.x) + v) : 0.0f;
                 store_quad(yr, cols, j, vec, o, oo);
             }
+        };
+        auto add = [](float p, float v) { return __fadd_rn(p, v); };
+        auto mx = [](float p, float v) { return max2(p, v); };
+        auto ident = [](float v, int) { return v; };
+        float leaf[4];
+        const float n = static_cast<float>(cols);
+        if constexpr (OP == OP_SOFTMAX || OP == OP_XENT) {
+            fold(ident, mx, __int_as_float(0xff800000), leaf);
+            const float m = tree<Max>(leaf, gpart, buf);
+            fold([m](float v, int) { return exp_ot(__fsub_rn(v, m)); }, add, 0.0f, leaf);
+            const float s = tree<Add>(leaf, gpart, buf);
+            if constexpr (OP == OP_SOFTMAX) {
+                const float inv = __fdiv_rn(1.0f, s);
+                emit([m, inv](float v, int) { return __fmul_rn(exp_ot(__fsub_rn(v, m)), inv); });
+            } else {
+                if (threadIdx.x == 0) {
+                    const int64_t label = a.labels[row];
+                    const float sel = (label >= 0 && label < cols) ? __ldg(xr + label) : 0.0f;
+                    a.loss[row] = __fsub_rn(__fadd_rn(log_ot(s), m), sel);
+                }
+            }
+        } else if constexpr (OP == OP_RMSNORM) {
+            fold([](float v, int) { return __fmul_rn(v, v); }, add, 0.0f, leaf);
+            const float ss = tree<Add>(leaf, gpart, buf);
+            const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), a.eps));
+            const float inv = __fdiv_rn(1.0f, r);
+            const bool hw = a.has_w;
+            const float* w = a.w;
+            emit([inv, hw, w](float v, int c) {
+                const float u = __fmul_rn(v, inv);
+                return hw ? __fmul_rn(u, __ldg(w + c)) : u;
+            });
+        } else {
+            fold(ident, add, 0.0f, leaf);
+            const float mean = __fdiv_rn(tree<Add>(leaf, gpart, buf), n);
+            fold([mean](float v, int) {
+                const float c = __fsub_rn(v, mean);
+                return __fmul_rn(c, c);
+            }, add, 0.0f, leaf);
+            const float var = __fdiv_rn(tree<Add>(leaf, gpart, buf), n);
+            const float d = __fsqrt_rn(__fadd_rn(var, a.eps));
+            const float inv = __fdiv_rn(1.0f, d);
+            const bool hw = a.has_w, hb = a.has_b;
+            const float *w = a.w, *b = a.b;
+            emit([mean, inv, hw, hb, w, b](float v, int c) {
+                float u = __fmul_rn(__fsub_rn(v, mean), inv);
+                if (hw) u = __fmul_rn(u, __ldg(w + c));
+                if (hb) u = __fadd_rn(u, __ldg(b + c));
+                return u;
+            });
+        }
+    }
+}
+
+// Staged realisation: persistent CTAs of 256 threads over rows blockIdx.x,
+// blockIdx.x + gridDim.x, ...; each row arrives in a ring slot by one bulk
+// asynchronous copy (the window of the unordered staged plans), so one row's
+// arithmetic overlaps the loads of the next rows and the stores of the
+// previous ones. The tree and every rounding are those of ot_cached_row.
+template <int OP, int K>
+__global__ void __launch_bounds__(kOrderedThreads) ot_staged_kernel(const RowArgs a) {
+    extern __shared__ __align__(16) float ring[];
+    __shared__ __align__(8) uint64_t full[kMaxRing];
+    __shared__ __align__(8) uint64_t never;
+    __shared__ float gpart[2][8];
+    __shared__ volatile int s_abort;
+    int buf = 0;
+    const int t = threadIdx.x;
+    const int nbuf = a.nbuf;
+    const int64_t G = gridDim.x;
+    const int64_t mine = (a.rows - blockIdx.x + G - 1) / G;
+    const float* x0 = a.x;
+    const float* x1 = a.x + a.rows * a.cols;
+    const int cols = a.cols;
+    const int nj = (cols + 1023) / 1024;
+    if (t == 0) {
+        for (int b = 0; b < nbuf; ++b) mbar_init(&full[b], 1);
+        mbar_init(&never, 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_enter();
+    if ((a.debug_flags & kDebugForceTimeout) && t == 0) mbar_wait_bounded(&never, 0, 1000000LL, a.err);
+    auto issue = [&](int64_t i) {
+        const int64_t row = blockIdx.x + i * G;
+        const float* xr = a.x + row * cols;
+        const RowGeom g = row_geom(xr, cols);
+        const StagedWindow w = staged_window(xr, g, x0, x1);
+        const int b = static_cast<int>(i % nbuf);
+        float* slot = ring + static_cast<int64_t>(b) * a.slot_floats;
+        if (w.bytes > 0) {
+            mbar_arrive_expect_tx(&full[b], static_cast<uint32_t>(w.bytes));
+            bulk_g2s(slot + w.dst, w.lo, static_cast<uint32_t>(w.bytes), &full[b]);
+        } else {
+            mbar_arrive(&full[b]);
         }
     };
-    auto add = [](float p, float v) { return __fadd_rn(p, v); };
-    auto mx = [](float p, float v) { return max2(p, v); };
-    auto ident = [](float v, int) { return v; };
-    float leaf[4];
-    const float n = static_cast<float>(cols);
-
-    if constexpr (OP == OP_SOFTMAX || OP == OP_XENT) {
-        fold(ident, mx, __int_as_float(0xff800000), leaf);
-        const float m = tree<Max>(leaf, gpart, buf);
-        float s;
-        if constexpr (kCached) {
-            // exp once per element, kept in place: the sum below folds the same
-            // values in the same leaf order as exp_ot(x - m) would
+    if (t == 0)
+        for (int64_t i = 0; i < mine && i < nbuf; ++i) issue(i);
+    for (int64_t i = 0; i < mine; ++i) {
+        const int b = static_cast<int>(i % nbuf);
+        const uint32_t parity = static_cast<uint32_t>((i / nbuf) & 1);
+        const int64_t row = blockIdx.x + i * G;
+        const float* xr = a.x + row * cols;
+        const RowGeom g = row_geom(xr, cols);
+        const StagedWindow w = staged_window(xr, g, x0, x1);
+        const float* slot = ring + static_cast<int64_t>(b) * a.slot_floats;
+        if (!mbar_wait_bounded(&full[b], parity, a.wait_ns, a.err)) s_abort = 1;
+        // column c sits at slot[pre + c]; pre = 0 exactly when the row is aligned
+        const int pre = w.off - g.head;
+        const int body_end = g.head + 4 * g.nvec;
+        float q[K][4];
 #pragma unroll
-            for (int j = 0; j < K; ++j)
+        for (int j = 0; j < K; ++j) {
+            const int c0 = 1024 * j + 4 * t;
+            if (j < nj && pre == 0 && c0 + 3 < body_end && !(w.head_global && c0 < g.head)) {
+                const float4 v4 = *reinterpret_cast<const float4*>(slot + c0);
+                q[j][0] = v4.x; q[j][1] = v4.y; q[j][2] = v4.z; q[j][3] = v4.w;
+            } else {
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    if (ok[j][v]) q[j][v] = exp_ot(__fsub_rn(q[j][v], m));
-            fold(ident, add, 0.0f, leaf);
-            s = tree<Add>(leaf, gpart, buf);
-        } else {
-            fold([m](float v, int) { return exp_ot(__fsub_rn(v, m)); }, add, 0.0f, leaf);
-            s = tree<Add>(leaf, gpart, buf);
-        }
-        if constexpr (OP == OP_SOFTMAX) {
-            if constexpr (kCached)
-                emit([s](float e, int) { return __fdiv_rn(e, s); });
-            else
-                emit([m, s](float v, int) { return __fdiv_rn(exp_ot(__fsub_rn(v, m)), s); });
-        } else {
-            if (threadIdx.x == 0) {
-                const int64_t label = a.labels[row];
-                const float sel = (label >= 0 && label < cols) ? __ldg(xr + label) : 0.0f;
-                a.loss[row] = __fsub_rn(__fadd_rn(log_ot(s), m), sel);
+                for (int v = 0; v < 4; ++v) {
+                    const int c = c0 + v;
+                    float x = 0.0f;
+                    if (j < nj && c < cols) {
+                        const bool global = (w.head_global && c < g.head) || (w.tail_global && c >= body_end);
+                        x = global ? ld_stream1(xr + c) : slot[pre + c];
+                    }
+                    q[j][v] = x;
+                }
             }
         }
-    } else if constexpr (OP == OP_RMSNORM) {
-        fold([](float v, int) { return __fmul_rn(v, v); }, add, 0.0f, leaf);
-        const float ss = tree<Add>(leaf, gpart, buf);
-        const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), a.eps));
-        const bool hw = a.has_w;
-        const float* w = a.w;
-        emit([r, hw, w](float v, int c) {
-            const float t = __fdiv_rn(v, r);
-            return hw ? __fmul_rn(t, __ldg(w + c)) : t;
-        });
-    } else {  // OP_LAYERNORM
-        fold(ident, add, 0.0f, leaf);
-        const float mean = __fdiv_rn(tree<Add>(leaf, gpart, buf), n);
-        fold([mean](float v, int) {
-            const float c = __fsub_rn(v, mean);
-            return __fmul_rn(c, c);
-        }, add, 0.0f, leaf);
-        const float var = __fdiv_rn(tree<Add>(leaf, gpart, buf), n);
-        const float d = __fsqrt_rn(__fadd_rn(var, a.eps));
-        const bool hw = a.has_w, hb = a.has_b;
-        const float *w = a.w, *b = a.b;
-        emit([mean, d, hw, hb, w, b](float v, int c) {
-            float t = __fdiv_rn(__fsub_rn(v, mean), d);
-            if (hw) t = __fmul_rn(t, __ldg(w + c));
-            if (hb) t = __fadd_rn(t, __ldg(b + c));
-            return t;
-        });
+        ot_cached_row<OP, K>(a, row, q, pre == 0 && a.y_vec, gpart, buf);
+        // each tree ends in a barrier after every thread loaded its quads, so
+        // the slot is free and the abort flag is visible here
+        if (s_abort) {
+            if (t == 0)
+                for (int64_t j = i; j < mine && j < i + nbuf; ++j)
+                    mbar_wait_bounded(&full[j % nbuf], static_cast<uint32_t>((j / nbuf) & 1), a.wait_ns, a.err);
+            return;
+        }
+        if (t == 0 && i + nbuf < mine) {
+            fence_proxy_async_smem();
+            issue(i + nbuf);
+        }
     }
 }
 
 }  // namespace ordered
+
+const void* kernel_ordered_staged(int op, int slots) {
+#define TR_OTS_CASES(OPV)                                                          \
+    switch (slots) {                                                               \
+        case 1: return reinterpret_cast<const void*>(ordered::ot_staged_kernel<OPV, 1>); \
+        case 2: return reinterpret_cast<const void*>(ordered::ot_staged_kernel<OPV, 2>); \
+        case 4: return reinterpret_cast<const void*>(ordered::ot_staged_kernel<OPV, 4>); \
+        case 8: return reinterpret_cast<const void*>(ordered::ot_staged_kernel<OPV, 8>); \
+    }                                                                              \
+    return nullptr;
+    switch (op) {
+        case TR_OP_SOFTMAX: { TR_OTS_CASES(OP_SOFTMAX) }
+        case TR_OP_RMSNORM: { TR_OTS_CASES(OP_RMSNORM) }
+        case TR_OP_LAYERNORM: { TR_OTS_CASES(OP_LAYERNORM) }
+        case TR_OP_CROSS_ENTROPY: { TR_OTS_CASES(OP_XENT) }
+    }
+#undef TR_OTS_CASES
+    return nullptr;
+}
 
 const void* kernel_ordered(int op, int slots) {
 #define TR_OT_CASES(OPV)                                                    \
@@ -299,7 +476,9 @@ const void* kernel_ordered(int op, int slots) {
         case 1: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 1>);   \
         case 2: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 2>);   \
         case 4: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 4>);   \
+        case 6: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 6>);   \
         case 8: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 8>);   \
+        case 12: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 12>); \
         case 16: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 16>); \
     }                                                                       \
     return nullptr;

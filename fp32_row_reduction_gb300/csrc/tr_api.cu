@@ -218,7 +218,7 @@ tr_status run(Call& c, cudaStream_t stream) {
     a.C = plan.cluster_ctas;
     a.wait_ns = kWaitNs;
     a.debug_flags = g_debug_flags;
-    a.nbuf = plan.kind == TR_PLAN_STAGED ? plan.rows_per_cta : 0;
+    a.nbuf = (plan.kind == TR_PLAN_STAGED || plan.kind == TR_PLAN_ORDERED_STAGED) ? plan.rows_per_cta : 0;
     a.slot_floats = staged_slot_floats(a.cols);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -397,7 +397,8 @@ tr_status tr_plan_override(const tr_plan* plan) {
         return TR_OK;
     }
     if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
-    if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_STAGED) return fail(TR_ERR_INVALID_ARG, "bad plan kind");
+    if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_ORDERED_STAGED)
+        return fail(TR_ERR_INVALID_ARG, "bad plan kind");
     g_override[plan->op] = *plan;
     g_override_set[plan->op] = true;
     return TR_OK;

@@ -46,11 +46,13 @@ const void* kernel_rmsnorm(int kind, int lanes, int slots, int flags);
 const void* kernel_layernorm(int kind, int lanes, int slots, int flags);
 const void* kernel_xent(int kind, int lanes, int slots, int flags);
 const void* kernel_ordered(int op, int slots);
+const void* kernel_ordered_staged(int op, int slots);
 // Dynamic shared memory a plan's kernel needs (0 for all but staged plans).
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols);
 
 inline const void* kernel_for(const tr_plan& p) {
     if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
+    if (p.kind == TR_PLAN_ORDERED_STAGED) return p.flags ? nullptr : kernel_ordered_staged(p.op, p.vec_slots);
     switch (p.op) {
         case TR_OP_SOFTMAX: return kernel_softmax(p.kind, p.lanes_per_row, p.vec_slots, p.flags);
         case TR_OP_RMSNORM: return kernel_rmsnorm(p.kind, p.lanes_per_row, p.vec_slots, p.flags);
@@ -65,7 +67,8 @@ constexpr int kRowsSlotsSub[] = {1, 2, 4};           // lanes_per_row 4, 8, 16
 constexpr int kRowsSlotsWarp[] = {1, 2, 4, 8, 16};   // lanes_per_row 32
 constexpr int kClusterSlots[] = {4, 8, 16};
 constexpr int kStagedSlots[] = {1, 2, 4, 8};
-constexpr int kOrderedSlots[] = {0, 1, 2, 4, 8, 16}; // 0: re-read plan
+constexpr int kOrderedSlots[] = {0, 1, 2, 4, 6, 8, 12, 16}; // 0: re-read plan
+constexpr int kOrderedStagedSlots[] = {1, 2, 4, 8};
 constexpr int kOrderedThreads = 256;                  // OT-1024: 256 workers x 4 leaves
 
 }  // namespace tr

@@ -68,6 +68,7 @@ int smallest_covering(const int (&arr)[N], int64_t need) {  // smallest K with K
 }
 
 int max_threads_for_slots(int op, int kind, int k, int flags) {
+    if (kind == TR_PLAN_ORDERED_STAGED) return kOrderedThreads;
     if (kind == TR_PLAN_STAGED && (flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS))
         return k <= 2 ? 1024 : k == 4 ? 768 : (op == TR_OP_LAYERNORM ? 384 : 512);
     if (kind == TR_PLAN_STAGED) return k >= 8 ? 768 : 1024;
@@ -103,7 +104,7 @@ tr_device_desc gb300_desc() {
 }
 
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols) {
-    if (p.kind != TR_PLAN_STAGED) return 0;
+    if (p.kind != TR_PLAN_STAGED && p.kind != TR_PLAN_ORDERED_STAGED) return 0;
     return static_cast<size_t>(p.rows_per_cta) * staged_slot_floats(cols) * sizeof(float);
 }
 
@@ -116,6 +117,7 @@ int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem) {
         case TR_PLAN_ROWS:
         case TR_PLAN_CLUSTER:
         case TR_PLAN_STAGED: regs = 28 + 4 * k + (p.op == TR_OP_LAYERNORM ? 4 : 0); break;
+        case TR_PLAN_ORDERED_STAGED: regs = 40 + 4 * k; break;
         case TR_PLAN_STREAM: regs = 64; break;
         case TR_PLAN_XENT: regs = 24 + 4 * k; break;
         default: regs = 40 + 5 * k; break;
@@ -143,8 +145,9 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     const bool xent = p->op == TR_OP_CROSS_ENTROPY;
     if (p->order != TR_ORDER_UNORDERED_TREE && !ordered) return fail(TR_ERR_INVALID_ARG, "bad order");
     if (p->op < TR_OP_SOFTMAX || p->op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
-    if (ordered != (p->kind == TR_PLAN_ORDERED))
-        return fail(TR_ERR_UNSUPPORTED, "the ordered policy is realised only by the OT-1024 plan");
+    const bool ot_kind = p->kind == TR_PLAN_ORDERED || p->kind == TR_PLAN_ORDERED_STAGED;
+    if (ordered != ot_kind)
+        return fail(TR_ERR_UNSUPPORTED, "the ordered policy is realised only by the OT-1024 plans");
     if (!ordered && xent != (p->kind == TR_PLAN_XENT))
         return fail(TR_ERR_UNSUPPORTED, "cross-entropy is realised only by the streaming XENT plan");
     const int T = p->block_threads;
@@ -210,6 +213,19 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
             p->grid_ctas = rows * C;
             break;
         }
+        case TR_PLAN_ORDERED_STAGED: {
+            if (T != kOrderedThreads || G != 32 || p->warps_per_row != 8 || p->cluster_ctas != 1)
+                return fail(TR_ERR_UNSUPPORTED, "OT-1024 runs 256 threads (8 warps) per row");
+            if (p->rows_per_cta < 1 || p->rows_per_cta > kMaxRing)
+                return fail(TR_ERR_UNSUPPORTED, "staged plans keep 1..8 rows in flight per CTA");
+            if (!in(kOrderedStagedSlots, k)) return fail(TR_ERR_UNSUPPORTED, "no staged OT-1024 kernel with that vec_slots");
+            if (static_cast<int64_t>(1024) * k < cols)
+                return fail(TR_ERR_UNSUPPORTED, "staged OT-1024 needs cols <= 1024 * vec_slots");
+            if (static_cast<int64_t>(p->rows_per_cta) * staged_slot_floats(cols) * 4 > kStagedSmemBudget)
+                return fail(TR_ERR_UNSUPPORTED, "the ring does not fit in shared memory");
+            p->grid_ctas = 0;
+            break;
+        }
         case TR_PLAN_STAGED: {
             if (G != 32 || p->warps_per_row != T / 32 || p->cluster_ctas != 1)
                 return fail(TR_ERR_UNSUPPORTED, "a staged CTA reduces one row at a time with all its warps");
@@ -231,7 +247,7 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     const int o = occ ? occ(*p, smem) : model_occupancy(d, *p, smem);
     if (o < 1) return fail(TR_ERR_UNSUPPORTED, "the plan cannot be resident on this device");
     p->ctas_per_sm = o;
-    if (p->kind == TR_PLAN_STAGED)
+    if (p->kind == TR_PLAN_STAGED || p->kind == TR_PLAN_ORDERED_STAGED)
         p->grid_ctas = std::min<int64_t>(rows, static_cast<int64_t>(o) * d.sm_count);
     if (why) *why = "";
     return TR_OK;
@@ -267,7 +283,7 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
 
     // arithmetic: SFU ex2 (16 per SM per clock) and ALU issue (128 lanes per SM per clock)
     double sfu_per_elem = 0.0, alu_per_elem = 4.0;
-    if (p.kind == TR_PLAN_ORDERED) {
+    if (p.kind == TR_PLAN_ORDERED || p.kind == TR_PLAN_ORDERED_STAGED) {
         alu_per_elem = op == TR_OP_SOFTMAX ? 48.0 : op == TR_OP_CROSS_ENTROPY ? 24.0 : op == TR_OP_LAYERNORM ? 24.0 : 16.0;
     } else if (op == TR_OP_SOFTMAX) {
         sfu_per_elem = p.kind == TR_PLAN_STREAM ? 2.0 : 1.0;
@@ -279,7 +295,7 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
 
     const int red = p.kind == TR_PLAN_STREAM ? 1 : reductions_of(op);
     double sync = 0.0;  // one merge round of the row's workers
-    if (p.lanes_per_row == 32 && p.warps_per_row > 1) sync += kCtaBarrierUs;
+    if (p.lanes_per_row == 32 && p.warps_per_row > 1) sync += kCtaBarrierUs;  // ordered: 8 warps
     if (p.cluster_ctas > 1) sync += kClusterBarrierUs;
     // serial per-thread work on the cached slots (max, exp/centre, scale/store passes)
     const int passes = op == TR_OP_RMSNORM || op == TR_OP_CROSS_ENTROPY ? 2 : 3;
@@ -294,7 +310,7 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const double write_bytes = std::max(0.0, hbm_bytes - read_bytes);
     const double t_l2 = l2_bytes / (kL2OverHbm * bw);
 
-    if (p.kind == TR_PLAN_STAGED) {
+    if (p.kind == TR_PLAN_STAGED || p.kind == TR_PLAN_ORDERED_STAGED) {
         // persistent CTAs: up to nbuf rows in flight per CTA; reads, arithmetic and
         // writes of different rows overlap; a CTA's rows form a serial chain
         const double rows_cta = std::ceil(static_cast<double>(rows) / grid);
@@ -364,6 +380,20 @@ tr_status select_plan(const tr_device_desc& d, const OccupancyFn& occ, int32_t o
         const int k = smallest_covering(kOrderedSlots, ceil_div(cols, 1024));
         p.vec_slots = k < 0 ? 0 : k;
         cands.push_back(p);
+        // the staged OT-1024 realisation (TR_PLAN_ORDERED_STAGED) stays available by
+        // override; measured plan sweeps found the one-shot realisation at full
+        // occupancy as fast or faster, so it is not an automatic candidate
+        const int ks = -1;
+        if (ks > 0)
+            for (int nb = 1; nb <= kMaxRing; ++nb) {
+                tr_plan q = base(TR_PLAN_ORDERED_STAGED);
+                q.lanes_per_row = 32;
+                q.warps_per_row = 8;
+                q.rows_per_cta = nb;
+                q.block_threads = kOrderedThreads;
+                q.vec_slots = ks;
+                cands.push_back(q);
+            }
     } else {
         const bool xent = op == TR_OP_CROSS_ENTROPY;
         const int kind = xent ? TR_PLAN_XENT : TR_PLAN_ROWS;

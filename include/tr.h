@@ -73,8 +73,9 @@ typedef enum tr_plan_kind {
     TR_PLAN_STREAM = 2,   /* a row per C CTAs (C >= 1); no cache: statistics pass, then the row is re-read (from L2 when it fits) */
     TR_PLAN_XENT = 3,     /* cross-entropy: one streaming pass with an online (max, sum of exp) pair */
     TR_PLAN_ORDERED = 4,  /* OT-1024: 256 threads per row; cached (vec_slots > 0) or re-read (vec_slots == 0) */
-    TR_PLAN_STAGED = 5    /* persistent CTAs; rows_per_cta rows in flight in a shared-memory ring filled by
+    TR_PLAN_STAGED = 5,   /* persistent CTAs; rows_per_cta rows in flight in a shared-memory ring filled by
                              bulk asynchronous copies (TMA); each row reduced by the whole CTA from registers */
+    TR_PLAN_ORDERED_STAGED = 6  /* OT-1024 on persistent 256-thread CTAs fed by the same ring (rows_per_cta slots) */
 } tr_plan_kind;
 
 typedef struct tr_plan {

@@ -36,6 +36,9 @@
  * All arithmetic is IEEE binary32 round-to-nearest-even with no FMA
  * contraction (this file is compiled with -ffp-contract=off), no flush to
  * zero, IEEE division and square root, and the exp/log defined below.
+ * A row is divided by its normaliser (softmax sum, RMS, LayerNorm sigma) as a
+ * multiplication by the correctly rounded reciprocal of that normaliser: one
+ * IEEE division per row, then one rounded product per element.
  */
 #include "oracle.h"
 
@@ -284,7 +287,8 @@ int ot_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols) {
         float *yr = y + r * cols;
         float peak = ot_max_f32(xr, cols);
         float total = ot_sum_of(xr, cols, el_exp_shifted, peak);
-        for (int64_t c = 0; c < cols; ++c) yr[c] = ot_expf(xr[c] - peak) / total;
+        float inv = 1.0f / total;
+        for (int64_t c = 0; c < cols; ++c) yr[c] = ot_expf(xr[c] - peak) * inv;
     }
     return 0;
 }
@@ -297,8 +301,9 @@ int ot_rmsnorm_f32(const float *x, const float *w, float *y,
         float *yr = y + r * cols;
         float sumsq = ot_sum_of(xr, cols, el_square, 0.0f);
         float rms = sqrtf(sumsq / (float)cols + eps);
+        float inv = 1.0f / rms;
         for (int64_t c = 0; c < cols; ++c) {
-            float v = xr[c] / rms;
+            float v = xr[c] * inv;
             yr[c] = w ? v * w[c] : v;
         }
     }
@@ -314,8 +319,9 @@ int ot_layernorm_f32(const float *x, const float *gamma, const float *beta,
         float mean = ot_sum_of(xr, cols, el_identity, 0.0f) / (float)cols;
         float var = ot_sum_of(xr, cols, el_centered_square, mean) / (float)cols;
         float sigma = sqrtf(var + eps);
+        float inv = 1.0f / sigma;
         for (int64_t c = 0; c < cols; ++c) {
-            float v = (xr[c] - mean) / sigma;
+            float v = (xr[c] - mean) * inv;
             if (gamma) v = v * gamma[c];
             if (beta) v = v + beta[c];
             yr[c] = v;

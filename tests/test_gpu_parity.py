@@ -127,19 +127,47 @@ def test_ordered_is_bit_exact(op, rows, cols):
     assert_close(got, reference(op, h), f"ordered {op} {rows}x{cols}")
 
 
+OT_REALISATIONS = [dict(kind=4, rows_per_cta=1, vec_slots=0), dict(kind=4, rows_per_cta=1, vec_slots=8),
+                   dict(kind=6, rows_per_cta=1, vec_slots=8), dict(kind=6, rows_per_cta=3, vec_slots=8),
+                   dict(kind=6, rows_per_cta=8, vec_slots=8)]
+
+
 @pytest.mark.parametrize("op", OPS)
-def test_ordered_same_bits_cached_and_reread(op):
-    # OT-1024 is defined on columns: the cached and the re-reading realisations agree bit for bit
-    d = make(op, 6, 5000, seed=17)
-    a = run(op, d, order="ordered").cpu().numpy()
-    p = tr.tr_plan(op=tr.OPS[op], order=1, kind=tr.TR_PLAN_ORDERED, lanes_per_row=32, warps_per_row=8,
-                   rows_per_cta=1, cluster_ctas=1, vec_slots=0, block_threads=256)
-    assert tr.tr_plan_override(p) == tr.TR_OK
+def test_ordered_same_bits_in_every_realisation(op):
+    # OT-1024 is defined on columns: one-shot cached, one-shot re-read and staged
+    # (persistent, TMA ring) realisations agree bit for bit with the emulation
+    d = make(op, 21, 5000, seed=17)
+    emu = emulated(op, host(d))
     try:
-        b = run(op, d, order="ordered").cpu().numpy()
+        for r in OT_REALISATIONS:
+            p = tr.tr_plan(op=tr.OPS[op], order=1, lanes_per_row=32, warps_per_row=8, cluster_ctas=1,
+                           block_threads=256, **r)
+            assert tr.tr_plan_override(p) == tr.TR_OK
+            got = run(op, d, order="ordered").cpu().numpy()
+            assert np.array_equal(got.view(np.uint32), emu.view(np.uint32)), r
     finally:
         tr.tr_plan_override(None)
-    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("xoff", [0, 1, 2, 3])
+def test_ordered_staged_on_unaligned_tensors(op, xoff):
+    rows, cols = 11, 3001
+    d = make(op, rows, cols, seed=90 + xoff)
+    xbig = torch.empty(rows * cols + 8, device=DEV)
+    x = xbig[xoff:xoff + rows * cols].view(rows, cols)
+    x.copy_(d["x"])
+    emu = emulated(op, host(d))
+    try:
+        for nb in (1, 4):
+            p = tr.tr_plan(op=tr.OPS[op], order=1, kind=6, lanes_per_row=32, warps_per_row=8, rows_per_cta=nb,
+                           cluster_ctas=1, vec_slots=4, block_threads=256)
+            assert tr.tr_plan_override(p) == tr.TR_OK
+            got = tr.run_op(op, dict(d, x=x), order="ordered")
+            torch.cuda.synchronize()
+            assert np.array_equal(got.cpu().numpy().view(np.uint32), emu.view(np.uint32)), (xoff, nb)
+    finally:
+        tr.tr_plan_override(None)
 
 
 def test_ordered_shift_invariance_exact():

@@ -34,6 +34,8 @@ def covers(p, cols):
         return p.block_threads * p.vec_slots >= math.ceil(n4 / p.cluster_ctas)
     if p.kind == trlib.TR_PLAN_ORDERED:
         return p.vec_slots == 0 or 1024 * p.vec_slots >= cols
+    if p.kind == trlib.TR_PLAN_ORDERED_STAGED:
+        return 1024 * p.vec_slots >= cols
     if p.kind == trlib.TR_PLAN_STAGED:
         ring = p.rows_per_cta * (4 * math.ceil(cols / 4) + 8) * 4
         return p.block_threads * p.vec_slots >= n4 and ring <= 225 * 1024
@@ -69,10 +71,13 @@ def test_cross_entropy_uses_the_streaming_plan(rows, cols):
 @pytest.mark.parametrize("op", [0, 1, 2, 3])
 def test_ordered_requests_get_the_fixed_tree(op, rows, cols):
     p = select(op, rows, cols, order=1)
-    assert p.kind == trlib.TR_PLAN_ORDERED
-    assert p.block_threads == 256 and p.rows_per_cta == 1 and p.cluster_ctas == 1
+    assert p.kind in (trlib.TR_PLAN_ORDERED, trlib.TR_PLAN_ORDERED_STAGED)
+    assert p.block_threads == 256 and p.cluster_ctas == 1
     assert covers(p, cols)
-    assert p.grid_ctas == rows
+    if p.kind == trlib.TR_PLAN_ORDERED:
+        assert p.rows_per_cta == 1 and p.grid_ctas == rows
+    else:
+        assert 1 <= p.rows_per_cta <= 8 and p.grid_ctas == min(rows, p.ctas_per_sm * DEV.sm_count)
 
 
 def test_selection_is_deterministic():
