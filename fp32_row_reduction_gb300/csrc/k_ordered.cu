@@ -41,12 +41,14 @@ namespace ordered {
 __device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
 
 __device__ __forceinline__ float exp_ot(float x) {
-    if (x != x) return __fadd_rn(x, x);
-    if (x > 100.0f) return __int_as_float(0x7f800000);
-    if (x < -110.0f) return 0.0f;
-    const float kf = rintf(__fmul_rn(x, 0x1.715476p+0f));
+    // Branch-free form of the same function: clamping to [-110, 100] changes
+    // nothing inside the range and reproduces the out-of-range results by
+    // overflow to +inf (x > 100) and underflow to +0 (x < -110); NaN is
+    // selected at the end. Independent elements can then be interleaved.
+    const float xc = fminf(fmaxf(x, -110.0f), 100.0f);
+    const float kf = rintf(__fmul_rn(xc, 0x1.715476p+0f));
     const int k = static_cast<int>(kf);
-    float r = __fmaf_rn(-kf, 0x1.62e430p-1f, x);
+    float r = __fmaf_rn(-kf, 0x1.62e430p-1f, xc);
     r = __fmaf_rn(-kf, -0x1.05c610p-29f, r);
     float p = 0x1.a01a02p-13f;           // 1/7!
     p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/6!
@@ -57,7 +59,8 @@ __device__ __forceinline__ float exp_ot(float x) {
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
     const int k1 = k >> 1;
-    return __fmul_rn(__fmul_rn(p, pow2i(k1)), pow2i(k - k1));
+    const float e = __fmul_rn(__fmul_rn(p, pow2i(k1)), pow2i(k - k1));
+    return x != x ? __fadd_rn(x, x) : e;
 }
 
 // log on binary32: x = 2^e m, m in (sqrt(1/2), sqrt(2)], f = m - 1,
@@ -97,11 +100,9 @@ __device__ __forceinline__ float log_ot(float x) {
 // Canonical max: NaN in the first operand wins, +0 beats -0; commutative for
 // every non-NaN pair, so the butterfly leaves identical bits in all lanes.
 __device__ __forceinline__ float max2(float a, float b) {
-    if (a != a) return a;
-    if (b != b) return b;
-    if (a > b) return a;
-    if (b > a) return b;
-    return (__float_as_uint(a) >> 31) ? b : a;
+    // selects only: a if a is NaN, else b if b is NaN, else the larger, +0 over -0
+    const bool a_wins = (a != a) || (!(b != b) && (a > b || (a == b && !(__float_as_uint(a) >> 31))));
+    return a_wins ? a : b;
 }
 struct Add {
     static __device__ __forceinline__ float f(float a, float b) { return __fadd_rn(a, b); }
@@ -163,16 +164,24 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
     const int t = static_cast<int>(threadIdx.x);
     const int nj = (cols + 1023) / 1024;
     auto col = [t](int j, int v) { return 1024 * j + 4 * t + v; };
+    // validity, tested once per quad: `full` quads need no per-element test
+    auto full = [&](int j) { return j < nj && col(j, 3) < cols; };
     auto okc = [&](int j, int v) { return j < nj && col(j, v) < cols; };
     float leaf[4];
     // fold f(value, column) into the leaves in increasing column order
     auto fold = [&](auto elem, auto comb, float init) {
         leaf[0] = leaf[1] = leaf[2] = leaf[3] = init;
 #pragma unroll
-        for (int j = 0; j < K; ++j)
+        for (int j = 0; j < K; ++j) {
+            if (full(j)) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                if (okc(j, v)) leaf[v] = comb(leaf[v], elem(q[j][v], col(j, v)));
+                for (int v = 0; v < 4; ++v) leaf[v] = comb(leaf[v], elem(q[j][v], col(j, v)));
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (okc(j, v)) leaf[v] = comb(leaf[v], elem(q[j][v], col(j, v)));
+            }
+        }
     };
     float* yr = a.y + row * cols;
     auto emit = [&](auto out) {
@@ -182,8 +191,13 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
             float o[4];
 #pragma unroll
             for (int v = 0; v < 4; ++v) o[v] = out(q[j][v], col(j, v));
-            if (vec_out && okc(j, 3)) {
-                st4(yr + col(j, 0), make_float4(o[0], o[1], o[2], o[3]));
+            if (full(j)) {
+                if (vec_out) {
+                    st4(yr + col(j, 0), make_float4(o[0], o[1], o[2], o[3]));
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) yr[col(j, v)] = o[v];
+                }
             } else {
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
@@ -202,10 +216,16 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
         // exp once per element, kept in place: the sum folds the same values in
         // the same leaf order as exp_ot(x - m) would
 #pragma unroll
-        for (int j = 0; j < K; ++j)
+        for (int j = 0; j < K; ++j) {
+            if (full(j)) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                if (okc(j, v)) q[j][v] = exp_ot(__fsub_rn(q[j][v], m));
+                for (int v = 0; v < 4; ++v) q[j][v] = exp_ot(__fsub_rn(q[j][v], m));
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (okc(j, v)) q[j][v] = exp_ot(__fsub_rn(q[j][v], m));
+            }
+        }
         fold(ident, add, 0.0f);
         const float s = tree<Add>(leaf, gpart, buf);
         if constexpr (OP == OP_SOFTMAX) {
@@ -253,8 +273,15 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
 
 // One-shot realisation: a CTA per row. K > 0: the row (cols <= 1024*K) is
 // cached in registers. K == 0: the row is read again for each pass.
+// Rows of up to 6144 columns (K <= 6) fit six 256-thread CTAs per SM, so that
+// 768 such rows are resident in one wave on 152 SMs.
+template <int K>
+constexpr int ot_min_blocks() {
+    return K >= 1 && K <= 6 ? 6 : (K == 8 ? 5 : 1);
+}
+
 template <int OP, int K>
-__global__ void __launch_bounds__(kOrderedThreads) ot_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(kOrderedThreads, ot_min_blocks<K>()) ot_kernel(const RowArgs a) {
     __shared__ float gpart[2][8];
     int buf = 0;
     const int64_t row = blockIdx.x;

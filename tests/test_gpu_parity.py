@@ -170,6 +170,21 @@ def test_ordered_staged_on_unaligned_tensors(op, xoff):
         tr.tr_plan_override(None)
 
 
+@pytest.mark.parametrize("op", ["softmax", "cross_entropy"])
+def test_ordered_extreme_logits_bit_exact(op):
+    # x - max far below -110 and up to 0 exercises the clamped range of the
+    # ordered exp; subnormal results included
+    g = torch.Generator().manual_seed(12)
+    x = (torch.rand(6, 4099, generator=g) * 400.0 - 300.0)
+    x[1, ::3] = -1e30
+    x[2] = -87.0 - torch.rand(4099, generator=g) * 20.0  # exp(x - m) subnormal for many
+    x[3, 7] = 1e4
+    d = {"x": x.to(DEV), "labels": torch.arange(6, dtype=torch.int64, device=DEV) * 700}
+    got = run(op, d, order="ordered").cpu().numpy()
+    emu = emulated(op, host(d))
+    assert np.array_equal(got.view(np.uint32), emu.view(np.uint32))
+
+
 def test_ordered_shift_invariance_exact():
     # x on a 2^-10 grid, x + 1 exact: x - max is identical, so softmax bits are identical
     g = torch.randint(-2048, 2049, (5, 3000), generator=torch.Generator().manual_seed(3)).float() / 1024.0
