@@ -76,7 +76,7 @@ class tr_device_desc(ctypes.Structure):
 def gb300_device_desc() -> tr_device_desc:
     """The GB300 as the plan selector models it (152 SMs, 2048 threads, 64K registers)."""
     return tr_device_desc(sm_count=152, max_threads_per_sm=2048, max_ctas_per_sm=32,
-                          regs_per_sm=65536, smem_per_sm=233472, max_cluster_ctas=8,
+                          regs_per_sm=65536, smem_per_sm=233472, max_cluster_ctas=16,
                           l2_bytes=126 << 20, hbm_gbs=7000.0)
 
 

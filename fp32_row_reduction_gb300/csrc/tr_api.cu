@@ -45,6 +45,7 @@ struct DeviceState {
     std::map<std::tuple<int, int64_t, int64_t, int, int>, tr_plan> plans;  // (op, rows, cols, order, align16)
     std::map<std::tuple<const void*, int, int, size_t>, int> occ;  // (kernel, threads, cluster, smem) -> CTAs/SM
     std::map<const void*, bool> smem_opt_in;                        // kernels allowed large dynamic smem
+    std::map<const void*, bool> wide_cluster;                       // kernels allowed clusters above 8 CTAs
 };
 
 std::mutex g_mu;
@@ -92,7 +93,7 @@ tr_status device_state(int dev, DeviceState** out) {
         d.l2_bytes = v;
         e = cudaDeviceGetAttribute(&v, cudaDevAttrClusterLaunch, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-        d.max_cluster_ctas = v ? 8 : 1;
+        d.max_cluster_ctas = v ? 16 : 1;  // sizes above 8 are non-portable: checked per kernel
         if (const char* bw = std::getenv("TR_HBM_GBS")) d.hbm_gbs = std::atof(bw);
         void* errp = nullptr;
         e = cudaGetSymbolAddress(&errp, g_device_error);
@@ -103,6 +104,16 @@ tr_status device_state(int dev, DeviceState** out) {
     }
     *out = &st;
     return TR_OK;
+}
+
+// Allow a kernel clusters of more than 8 CTAs (non-portable sizes, up to 16).
+bool opt_in_wide_cluster(DeviceState& st, const void* fn) {
+    auto it = st.wide_cluster.find(fn);
+    if (it != st.wide_cluster.end()) return it->second;
+    const bool ok = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    st.wide_cluster[fn] = ok;
+    return ok;
 }
 
 // Resident CTAs per SM of a plan's kernel (0 = cannot run). Cluster plans:
@@ -121,7 +132,7 @@ int query_occupancy(DeviceState& st, const tr_plan& p, size_t smem) {
         st.occ[key] = 0;
         return 0;
     }
-    if (smem > 0 && !opt_in_smem(st, fn)) {
+    if ((smem > 0 && !opt_in_smem(st, fn)) || (C > 8 && !opt_in_wide_cluster(st, fn))) {
         st.occ[key] = 0;
         return 0;
     }

@@ -71,9 +71,9 @@ int max_threads_for_slots(int op, int kind, int k, int flags) {
     if (kind == TR_PLAN_ORDERED_STAGED) return kOrderedThreads;
     if (kind == TR_PLAN_STAGED && (flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS))
         return k <= 2 ? 1024 : k == 4 ? 768 : (op == TR_OP_LAYERNORM ? 384 : 512);
-    if (kind == TR_PLAN_STAGED) return k >= 8 ? 768 : 1024;
+    if (kind == TR_PLAN_STAGED) return (k >= 8 || (k >= 4 && op == TR_OP_LAYERNORM)) ? 768 : 1024;
     if (kind == TR_PLAN_ROWS || kind == TR_PLAN_CLUSTER)
-        return k >= 16 ? 512 : (k >= 8 && op == TR_OP_LAYERNORM) ? 768 : 1024;
+        return k >= 16 ? 512 : (k >= 4 && op == TR_OP_LAYERNORM) ? 768 : 1024;
     if (kind == TR_PLAN_ORDERED) return kOrderedThreads;
     return 1024;
 }
@@ -97,7 +97,7 @@ tr_device_desc gb300_desc() {
     d.max_ctas_per_sm = 32;
     d.regs_per_sm = 65536;
     d.smem_per_sm = 233472;
-    d.max_cluster_ctas = 8;
+    d.max_cluster_ctas = 16;
     d.l2_bytes = 126LL << 20;
     d.hbm_gbs = 7000.0;
     return d;

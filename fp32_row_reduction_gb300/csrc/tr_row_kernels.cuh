@@ -23,17 +23,18 @@
 namespace tr {
 
 // Largest CTA a K-slot cached kernel is compiled for: 64 cached floats need
-// about 90 registers (at most 512 threads per CTA); LayerNorm's 32-float
-// stripe needs more than the 64 registers a 1024-thread CTA allows.
+// about 90 registers (at most 512 threads per CTA); a LayerNorm stripe of 16
+// or more floats, with its prefetched weights and biases, needs more than the
+// 64 registers a 1024-thread CTA allows.
 template <int OP, int K>
 constexpr int max_threads_for() {
-    return K >= 16 ? 512 : (K >= 8 && OP == OP_LAYERNORM) ? 768 : 1024;
+    return K >= 16 ? 512 : (K >= 4 && OP == OP_LAYERNORM) ? 768 : 1024;
 }
 
 // Staged kernels that also hold K float4 of weights (and of biases) per worker.
 template <int OP, int K, bool PRE>
 constexpr int staged_max_threads() {
-    if (!PRE) return K >= 8 ? 768 : 1024;
+    if (!PRE) return (K >= 8 || (K >= 4 && OP == OP_LAYERNORM)) ? 768 : 1024;
     return K <= 2 ? 1024 : K == 4 ? 768 : (OP == OP_LAYERNORM ? 384 : 512);
 }
 
@@ -169,6 +170,15 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         if (own_h) yr[wi] = hv * inv;
         if (own_t) yr[ti] = tv * inv;
     } else if constexpr (OP == OP_RMSNORM) {
+        // short stripes fetch their weights now, so the load overlaps the merge
+        constexpr bool kFetchEarly = !PRE && K <= 4;
+        const bool wv = a.has_w && aligned16(a.w + g.head);
+        float4 wq[K];
+        if constexpr (kFetchEarly) {
+#pragma unroll
+            for (int j = 0; j < K; ++j)
+                wq[j] = (a.has_w && active && map.ok(j)) ? ld_param(a.w + g.head + 4 * map.idx(j), wv) : f4(1.0f);
+        }
         // missing slots hold 0
         float ss = fmaf(hv, hv, tv * tv);
 #pragma unroll
@@ -177,21 +187,34 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         ss = red(ss);
         const float rstd = rsqrtf(fmaf(ss, a.inv_cols, a.eps));
         if (!active) return;
-        const bool wv = a.has_w && aligned16(a.w + g.head);
 #pragma unroll
         for (int j = 0; j < K; ++j)
             if (map.ok(j)) {
                 const int e = 4 * map.idx(j);
                 float4 o = make_float4(v[j].x * rstd, v[j].y * rstd, v[j].z * rstd, v[j].w * rstd);
                 if (a.has_w) {
-                    const float4 wq = PRE ? wr[j] : ld_param(a.w + g.head + e, wv);
-                    o.x *= wq.x; o.y *= wq.y; o.z *= wq.z; o.w *= wq.w;
+                    const float4 wj = PRE ? wr[j] : kFetchEarly ? wq[j] : ld_param(a.w + g.head + e, wv);
+                    o.x *= wj.x; o.y *= wj.y; o.z *= wj.z; o.w *= wj.w;
                 }
                 st_out(yb + e, o, a.y_vec);
             }
         if (own_h) yr[wi] = hv * rstd * (a.has_w ? __ldg(a.w + wi) : 1.0f);
         if (own_t) yr[ti] = tv * rstd * (a.has_w ? __ldg(a.w + ti) : 1.0f);
     } else if constexpr (OP == OP_LAYERNORM) {
+        // short stripes fetch their weights and biases now, overlapping the merges
+        constexpr bool kFetchEarly = !PRE && K <= 4;
+        const bool wv = a.has_w && aligned16(a.w + g.head);
+        const bool bv = a.has_b && aligned16(a.b + g.head);
+        float4 wq[K], bq[K];
+        if constexpr (kFetchEarly) {
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const bool here = active && map.ok(j);
+                const int e = 4 * map.idx(j);
+                wq[j] = (a.has_w && here) ? ld_param(a.w + g.head + e, wv) : f4(1.0f);
+                bq[j] = (a.has_b && here) ? ld_param(a.b + g.head + e, bv) : f4(0.0f);
+            }
+        }
         // missing slots hold 0 for the sum; they are excluded from the second pass
         float sm = hv + tv;
 #pragma unroll
@@ -213,8 +236,6 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         sq = red(sq);
         const float rstd = rsqrtf(fmaf(sq, a.inv_cols, a.eps));
         if (!active) return;
-        const bool wv = a.has_w && aligned16(a.w + g.head);
-        const bool bv = a.has_b && aligned16(a.b + g.head);
 #pragma unroll
         for (int j = 0; j < K; ++j)
             if (map.ok(j)) {
@@ -222,12 +243,12 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
                 float4 o = make_float4((v[j].x - mean) * rstd, (v[j].y - mean) * rstd, (v[j].z - mean) * rstd,
                                        (v[j].w - mean) * rstd);
                 if (a.has_w) {
-                    const float4 wq = PRE ? wr[j] : ld_param(a.w + g.head + e, wv);
-                    o.x *= wq.x; o.y *= wq.y; o.z *= wq.z; o.w *= wq.w;
+                    const float4 wj = PRE ? wr[j] : kFetchEarly ? wq[j] : ld_param(a.w + g.head + e, wv);
+                    o.x *= wj.x; o.y *= wj.y; o.z *= wj.z; o.w *= wj.w;
                 }
                 if (a.has_b) {
-                    const float4 bq = PRE ? br[j] : ld_param(a.b + g.head + e, bv);
-                    o.x += bq.x; o.y += bq.y; o.z += bq.z; o.w += bq.w;
+                    const float4 bj = PRE ? br[j] : kFetchEarly ? bq[j] : ld_param(a.b + g.head + e, bv);
+                    o.x += bj.x; o.y += bj.y; o.z += bj.z; o.w += bj.w;
                 }
                 st_out(yb + e, o, a.y_vec);
             }

@@ -107,7 +107,7 @@ typedef struct tr_device_desc {
     int32_t max_ctas_per_sm;       /* 32 */
     int32_t regs_per_sm;           /* 65536 */
     int32_t smem_per_sm;           /* bytes */
-    int32_t max_cluster_ctas;      /* 8 portable */
+    int32_t max_cluster_ctas;      /* 16 on GB300 (sizes above 8 are non-portable) */
     int64_t l2_bytes;
     double hbm_gbs;                /* DRAM bandwidth, GB/s */
 } tr_device_desc;
