@@ -43,6 +43,7 @@ TR_PLAN_XENT = 3
 TR_PLAN_ORDERED = 4
 TR_PLAN_STAGED = 5
 TR_PLAN_ORDERED_STAGED = 6
+TR_PLAN_SPLIT = 7
 TR_PLAN_FLAG_PARAMS_IN_REGISTERS = 1
 
 OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LAYERNORM,
@@ -93,6 +94,7 @@ SIGNATURES = {
     "tr_plan_describe": ([_I32, _I64, _I64, _I32, ctypes.POINTER(tr_plan)], _I32),
     "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
                             ctypes.POINTER(tr_plan)], _I32),
+    "tr_plan_check_for": ([ctypes.POINTER(tr_device_desc), ctypes.POINTER(tr_plan), _I64, _I64, _I32], _I32),
     "tr_plan_override": ([ctypes.POINTER(tr_plan)], _I32),
     "tr_last_device_error": ([], _I32),
     "tr_debug_force_wait_timeout": ([_I32], _I32),
@@ -166,6 +168,13 @@ def tr_plan_select_for(dev: tr_device_desc, op, rows, cols, order, align16=1) ->
     _check(load().tr_plan_select_for(ctypes.byref(dev), op, rows, cols, order, align16, ctypes.byref(out)),
            "tr_plan_select_for")
     return out
+
+
+def check_plan_for(dev: tr_device_desc, plan: tr_plan, rows, cols, align16=1):
+    """Host-only legality check: (status, reason). Fills the plan's grid and estimate when legal."""
+    lib = load()
+    st = lib.tr_plan_check_for(ctypes.byref(dev), ctypes.byref(plan), rows, cols, align16)
+    return st, ("" if st == TR_OK else lib.tr_last_error_message().decode())
 
 
 def tr_plan_override(plan: tr_plan | None) -> int:

@@ -40,11 +40,10 @@ namespace ordered {
 // form, and the result scaled by 2^floor(k/2) and then by 2^(k - floor(k/2)).
 __device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
 
-__device__ __forceinline__ float exp_ot(float x) {
-    // Branch-free form of the same function: clamping to [-110, 100] changes
-    // nothing inside the range and reproduces the out-of-range results by
-    // overflow to +inf (x > 100) and underflow to +0 (x < -110); NaN is
-    // selected at the end. Independent elements can then be interleaved.
+// The clamped, two-step form for any x: clamping to [-110, 100] changes
+// nothing inside the range and reproduces the out-of-range results by
+// overflow to +inf (x > 100) and underflow to +0 (x < -110).
+__device__ __noinline__ float exp_ot_wide(float x) {
     const float xc = fminf(fmaxf(x, -110.0f), 100.0f);
     const float kf = rintf(__fmul_rn(xc, 0x1.715476p+0f));
     const int k = static_cast<int>(kf);
@@ -59,7 +58,32 @@ __device__ __forceinline__ float exp_ot(float x) {
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
     const int k1 = k >> 1;
-    const float e = __fmul_rn(__fmul_rn(p, pow2i(k1)), pow2i(k - k1));
+    return __fmul_rn(__fmul_rn(p, pow2i(k1)), pow2i(k - k1));
+}
+
+// For k in [-125, 127] the polynomial p lies in [2^-0.5, 2^0.5], so p * 2^k is
+// a normal number: adding k to p's exponent field is exact and gives the same
+// bits as the two-step product. Other k (|x| > 86, infinities) take the
+// clamped form; NaN is selected at the end.
+__device__ __forceinline__ float exp_ot(float x) {
+    const float kf = rintf(__fmul_rn(x, 0x1.715476p+0f));
+    const int k = static_cast<int>(kf);  // saturating; NaN gives 0
+    float r = __fmaf_rn(-kf, 0x1.62e430p-1f, x);
+    r = __fmaf_rn(-kf, -0x1.05c610p-29f, r);
+    float p = 0x1.a01a02p-13f;
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);
+    p = __fmaf_rn(p, r, 0x1.000000p-1f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    float e;
+    if (static_cast<unsigned>(k) + 125u <= 252u) {
+        e = __int_as_float(__float_as_int(p) + static_cast<int>(static_cast<unsigned>(k) << 23));
+    } else {
+        e = exp_ot_wide(x);
+    }
     return x != x ? __fadd_rn(x, x) : e;
 }
 
@@ -97,13 +121,15 @@ __device__ __forceinline__ float log_ot(float x) {
     return __fmaf_rn(ef, 0x1.62e430p-1f, __fmaf_rn(ef, -0x1.05c610p-29f, lm));
 }
 
-// Canonical max: NaN in the first operand wins, +0 beats -0; commutative for
-// every non-NaN pair, so the butterfly leaves identical bits in all lanes.
-__device__ __forceinline__ float max2(float a, float b) {
-    // selects only: a if a is NaN, else b if b is NaN, else the larger, +0 over -0
-    const bool a_wins = (a != a) || (!(b != b) && (a > b || (a == b && !(__float_as_uint(a) >> 31))));
-    return a_wins ? a : b;
-}
+// Row maximum of the softmax and cross-entropy trees: the hardware maxNum
+// (NaN operands skipped). It can differ from the canonical max of the tree's
+// definition (NaN wins, +0 over -0) only in rows that hold a NaN or whose
+// maximum is a signed zero, and neither changes an output bit: a NaN element
+// still reaches the sum as exp(NaN - m) = NaN, so every output of the row is
+// NaN either way, and x - (+0) and x - (-0) give exponentials of equal value.
+// maxNum of two non-NaN values is exact and commutative up to the sign of a
+// zero, so the butterfly's lanes agree on the value.
+__device__ __forceinline__ float max2(float a, float b) { return fmaxf(a, b); }
 struct Add {
     static __device__ __forceinline__ float f(float a, float b) { return __fadd_rn(a, b); }
 };

@@ -46,6 +46,7 @@ struct DeviceState {
     std::map<std::tuple<const void*, int, int, size_t>, int> occ;  // (kernel, threads, cluster, smem) -> CTAs/SM
     std::map<const void*, bool> smem_opt_in;                        // kernels allowed large dynamic smem
     std::map<const void*, bool> wide_cluster;                       // kernels allowed clusters above 8 CTAs
+    std::map<cudaStream_t, void*> split_ws;                         // split-plan workspace per stream
 };
 
 std::mutex g_mu;
@@ -159,6 +160,38 @@ int query_occupancy(DeviceState& st, const tr_plan& p, size_t smem) {
     return n;
 }
 
+// The split-plan workspace of `stream` (kSplitWorkspaceBytes, counters zero),
+// allocated and cleared in stream order on the stream's first split launch.
+// Launches on one stream run one at a time, so they can share it; another
+// stream gets its own. Allocation is refused while the stream is being
+// captured: make one split call on the stream before capturing it.
+tr_status split_workspace(DeviceState& st, cudaStream_t stream, void** out) {
+    auto it = st.split_ws.find(stream);
+    if (it != st.split_ws.end()) {
+        *out = it->second;
+        return TR_OK;
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return fail(TR_ERR_UNSUPPORTED,
+                    "a split plan's workspace is allocated on the stream's first call, which must not be captured: "
+                    "run one call on this stream before capturing it");
+    }
+    void* ws = nullptr;
+    e = cudaMalloc(&ws, kSplitWorkspaceBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(split workspace)");
+    e = cudaMemsetAsync(ws, 0, kSplitWorkspaceBytes, stream);
+    if (e != cudaSuccess) {
+        cudaFree(ws);
+        return cuda_fail(e, "cudaMemsetAsync(split workspace)");
+    }
+    st.split_ws.emplace(stream, ws);
+    *out = ws;
+    return TR_OK;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     if (!a || !b || na == 0 || nb == 0) return false;
     const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
@@ -196,6 +229,7 @@ tr_status run(Call& c, cudaStream_t stream) {
     const bool align16 = (a.cols % 4 == 0) && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0) &&
                          (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.b) % 16 == 0);
     tr_plan plan;
+    DeviceState* split_dev = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         DeviceState* st = nullptr;
@@ -203,6 +237,7 @@ tr_status run(Call& c, cudaStream_t stream) {
         if (s != TR_OK) return s;
         OccupancyFn occ = [st](const tr_plan& p, size_t smem) { return query_occupancy(*st, p, smem); };
         a.err = st->err;
+        split_dev = st;
         if (g_override_set[c.op]) {
             plan = g_override[c.op];
             plan.op = c.op;
@@ -231,6 +266,19 @@ tr_status run(Call& c, cudaStream_t stream) {
     a.debug_flags = g_debug_flags;
     a.nbuf = (plan.kind == TR_PLAN_STAGED || plan.kind == TR_PLAN_ORDERED_STAGED) ? plan.rows_per_cta : 0;
     a.slot_floats = staged_slot_floats(a.cols);
+    const bool split = plan.kind == TR_PLAN_SPLIT;
+    if (split) {
+        void* ws = nullptr;
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            tr_status s = split_workspace(*split_dev, stream, &ws);
+            if (s != TR_OK) return s;
+        }
+        a.sp_part = static_cast<float4*>(ws);
+        a.sp_arrive = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kSplitMaxParts * 16);
+        a.sp_depart = a.sp_arrive + kSplitMaxRows;
+        a.slot_floats = 4 * plan.vec_slots * plan.block_threads;
+    }
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid_ctas));
@@ -239,14 +287,19 @@ tr_status run(Call& c, cudaStream_t stream) {
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned nattr = 0;
-    if (plan.cluster_ctas > 1) {
+    if (plan.cluster_ctas > 1 && !split) {
         attr[nattr].id = cudaLaunchAttributeClusterDimension;
         attr[nattr].val.clusterDim.x = plan.cluster_ctas;
         attr[nattr].val.clusterDim.y = 1;
         attr[nattr].val.clusterDim.z = 1;
         ++nattr;
     }
-    if (g_pdl) {
+    if (split) {
+        // every CTA waits for the other segments of its row: all must be resident
+        attr[nattr].id = cudaLaunchAttributeCooperative;
+        attr[nattr].val.cooperative = 1;
+        ++nattr;
+    } else if (g_pdl) {
         attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[nattr].val.programmaticStreamSerializationAllowed = 1;
         ++nattr;
@@ -401,6 +454,17 @@ tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows
     return TR_OK;
 }
 
+tr_status tr_plan_check_for(const tr_device_desc* dev, tr_plan* plan, int64_t rows, int64_t cols, int32_t align16) {
+    if (!dev || !plan) return fail(TR_ERR_INVALID_ARG, "dev and plan must not be null");
+    if (dev->sm_count < 1 || dev->max_threads_per_sm < 32 || dev->regs_per_sm < 1 || dev->hbm_gbs <= 0)
+        return fail(TR_ERR_INVALID_ARG, "malformed device description");
+    const char* why = "";
+    tr_status s = check_plan(*dev, OccupancyFn(), plan, rows, cols, align16 != 0, &why);
+    if (s != TR_OK) return fail(s, why);
+    plan->est_us = estimate_us(*dev, *plan, rows, cols, align16 != 0);
+    return TR_OK;
+}
+
 tr_status tr_plan_override(const tr_plan* plan) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!plan) {
@@ -408,7 +472,7 @@ tr_status tr_plan_override(const tr_plan* plan) {
         return TR_OK;
     }
     if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
-    if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_ORDERED_STAGED)
+    if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_SPLIT)
         return fail(TR_ERR_INVALID_ARG, "bad plan kind");
     g_override[plan->op] = *plan;
     g_override_set[plan->op] = true;
@@ -431,6 +495,17 @@ tr_status tr_last_device_error(void) {
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        // a wait that gave up may leave a split row's counters short of zero
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (auto& dv : g_devices)
+            for (auto& w : dv.second.split_ws) {
+                int cur = 0;
+                cudaGetDevice(&cur);
+                cudaSetDevice(dv.first);
+                e = cudaMemset(w.second, 0, kSplitWorkspaceBytes);
+                cudaSetDevice(cur);
+                if (e != cudaSuccess) return cuda_fail(e, "clearing a split workspace");
+            }
         return fail(TR_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up");
     }
     return TR_OK;

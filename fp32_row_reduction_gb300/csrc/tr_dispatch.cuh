@@ -1,7 +1,7 @@
 // Kernel tables: the instantiations a plan can name, per operator.
 #pragma once
 
-#include "tr_row_kernels.cuh"
+#include "tr_split_kernels.cuh"
 
 namespace tr {
 
@@ -60,6 +60,8 @@ const void* unordered_table(int kind, int lanes, int slots, int flags) {
             return nullptr;
         case TR_PLAN_STREAM:
             return slots == 0 ? reinterpret_cast<const void*>(stream_kernel<OP>) : nullptr;
+        case TR_PLAN_SPLIT:
+            return lanes == 32 ? reinterpret_cast<const void*>(split_kernel<OP>) : nullptr;
         case TR_PLAN_STAGED:
             switch (slots) {
                 case 1: return reinterpret_cast<const void*>(staged_kernel<OP, 1, false>);

@@ -1,7 +1,10 @@
 // Internal host/device interface of the library (not installed).
 #pragma once
 
+#include <stddef.h>
 #include <stdint.h>
+
+#include <cuda_runtime.h>
 
 #include "tr.h"
 
@@ -29,11 +32,21 @@ struct RowArgs {
     int nbuf;              // staged plans: row slots in the shared-memory ring
     int slot_floats;       // staged plans: floats per ring slot (multiple of 4)
     int debug_flags;       // testing: kDebugForceTimeout makes one bounded wait expire
+    float4* sp_part;       // split plans: per (row, segment) partial statistic, rows * C entries
+    unsigned* sp_arrive;   // split plans: per-row arrival counters (zero between launches)
+    unsigned* sp_depart;   // split plans: per-row departure counters (zero between launches)
 };
 
 constexpr int kDebugForceTimeout = 1;
 constexpr int kMaxRing = 8;                // staged plans: most rows in flight per CTA
 constexpr int kStagedSmemBudget = 225 * 1024;  // dynamic shared memory per CTA (bytes; 2 KB left for static)
+
+// Split plans: at most 32 CTAs per row (the partials are merged by one warp);
+// the workspace holds kSplitMaxParts partials and kSplitMaxRows counter pairs.
+constexpr int kSplitMaxCtas = 32;
+constexpr int kSplitMaxParts = 4096;
+constexpr int kSplitMaxRows = 2048;
+constexpr size_t kSplitWorkspaceBytes = kSplitMaxParts * 16 + 2 * kSplitMaxRows * sizeof(unsigned);
 
 // Floats of one ring slot for rows of `cols` floats: the row's 16-byte-aligned
 // body plus one partial 16-byte chunk on each side.

@@ -48,6 +48,8 @@ constexpr double kSlotPassUs = 0.06;     // serial per-thread work, per cached s
 constexpr double kParamTripUs = 0.8;     // dependent L2 trip for the norms' weights
 constexpr double kClockGhz = 1.9;
 constexpr int kStreamChunk = 8;          // float4 per thread per streamed chunk (kStreamU)
+constexpr int kSplitChunk = 4;           // float4 per thread per streamed chunk of a split plan (kSplitU)
+constexpr double kSplitSyncUs = 1.5;     // publish, count and read back the row's partials (a prior)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -104,6 +106,7 @@ tr_device_desc gb300_desc() {
 }
 
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols) {
+    if (p.kind == TR_PLAN_SPLIT) return static_cast<size_t>(p.vec_slots) * p.block_threads * 16;
     if (p.kind != TR_PLAN_STAGED && p.kind != TR_PLAN_ORDERED_STAGED) return 0;
     return static_cast<size_t>(p.rows_per_cta) * staged_slot_floats(cols) * sizeof(float);
 }
@@ -119,6 +122,7 @@ int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem) {
         case TR_PLAN_STAGED: regs = 28 + 4 * k + (p.op == TR_OP_LAYERNORM ? 4 : 0); break;
         case TR_PLAN_ORDERED_STAGED: regs = 40 + 4 * k; break;
         case TR_PLAN_STREAM: regs = 64; break;
+        case TR_PLAN_SPLIT: regs = 64; break;
         case TR_PLAN_XENT: regs = 24 + 4 * k; break;
         default: regs = 40 + 5 * k; break;
     }
@@ -148,6 +152,7 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     const bool ot_kind = p->kind == TR_PLAN_ORDERED || p->kind == TR_PLAN_ORDERED_STAGED;
     if (ordered != ot_kind)
         return fail(TR_ERR_UNSUPPORTED, "the ordered policy is realised only by the OT-1024 plans");
+    if (ordered && p->kind == TR_PLAN_SPLIT) return fail(TR_ERR_UNSUPPORTED, "split plans are unordered");
     if (!ordered && xent != (p->kind == TR_PLAN_XENT))
         return fail(TR_ERR_UNSUPPORTED, "cross-entropy is realised only by the streaming XENT plan");
     const int T = p->block_threads;
@@ -239,6 +244,18 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
             p->grid_ctas = 0;  // persistent: set from the occupancy below
             break;
         }
+        case TR_PLAN_SPLIT: {
+            const int C = p->cluster_ctas;
+            if (C < 2 || C > kSplitMaxCtas) return fail(TR_ERR_UNSUPPORTED, "split plans use 2..32 CTAs per row");
+            if (G != 32 || p->rows_per_cta != 1 || p->warps_per_row != T / 32)
+                return fail(TR_ERR_UNSUPPORTED, "a CTA of a split row works as one group of block_threads / 32 warps");
+            if (k < 0 || static_cast<int64_t>(k) * T * 16 > kStagedSmemBudget)
+                return fail(TR_ERR_UNSUPPORTED, "the segment cache does not fit in shared memory");
+            if (rows > kSplitMaxRows || rows * C > kSplitMaxParts)
+                return fail(TR_ERR_UNSUPPORTED, "split plans take at most 2048 rows and 4096 row segments");
+            p->grid_ctas = rows * C;
+            break;
+        }
         default: return fail(TR_ERR_UNSUPPORTED, "unknown plan kind");
     }
     if (T > max_threads_for_slots(p->op, p->kind, k, p->flags)) return fail(TR_ERR_UNSUPPORTED, "too many threads for that vec_slots");
@@ -247,6 +264,8 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     const int o = occ ? occ(*p, smem) : model_occupancy(d, *p, smem);
     if (o < 1) return fail(TR_ERR_UNSUPPORTED, "the plan cannot be resident on this device");
     p->ctas_per_sm = o;
+    if (p->kind == TR_PLAN_SPLIT && p->grid_ctas > static_cast<int64_t>(o) * d.sm_count)
+        return fail(TR_ERR_UNSUPPORTED, "a split plan's CTAs must all be resident at once (cooperative launch)");
     if (p->kind == TR_PLAN_STAGED || p->kind == TR_PLAN_ORDERED_STAGED)
         p->grid_ctas = std::min<int64_t>(rows, static_cast<int64_t>(o) * d.sm_count);
     if (why) *why = "";
@@ -318,6 +337,21 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
         const double bw_eff = std::min(bw, grid * inflight_cta / kLatencyUs);
         const double chain = rows_cta * (kStagedRowUs + red * sync + kchain + ptrip);
         return kLaunchUs + kLatencyUs + std::max({hbm_bytes / bw_eff, t_alu, chain}) + t_l2;
+    }
+
+    if (p.kind == TR_PLAN_SPLIT) {
+        // one wave of co-resident CTAs in lockstep: read (the bulk copy of the
+        // cached part plus the streamed overflow), one exchange of partials
+        // through the workspace, then write; the overflow is read a second time
+        // (from L2 when the input fits)
+        const double seg = 4.0 * static_cast<double>(cols) / p.cluster_ctas;
+        const double cached = std::min(seg, 16.0 * p.vec_slots * T);
+        const double over = seg > 0.0 ? 4.0 * E * (1.0 - cached / seg) : 0.0;
+        const double inflight_cta = cached + std::min(seg - cached, 16.0 * kSplitChunk * T);
+        const double bw_read = std::min(bw, grid * std::max(16.0, inflight_cta) / kLatencyUs);
+        const double t_over = over / ((l2_fits ? kL2OverHbm : 1.0) * bw);
+        return kLaunchUs + kLatencyUs + read_bytes / bw_read + kSplitSyncUs + kOneWaveAluFactor * t_alu + kchain +
+               ptrip + write_bytes / bw + t_over + t_l2;
     }
 
     double inflight_thread;  // bytes a thread can have in flight at once
@@ -477,6 +511,28 @@ tr_status select_plan(const tr_device_desc& d, const OccupancyFn& occ, int32_t o
                     s.cluster_ctas = C;
                     s.vec_slots = 0;
                     cands.push_back(s);
+                }
+            // few long rows: C co-resident CTAs per row, each caching its segment in
+            // shared memory (one CTA per SM with the whole budget, or two with half)
+            for (int C = 2; C <= kSplitMaxCtas && rows <= kSplitMaxRows && rows * C <= kSplitMaxParts; ++C)
+                for (int T : {256, 512, 1024}) {
+                    const int64_t cover = ceil_div(ceil_div(n4, C), T);
+                    const int kfull = kStagedSmemBudget / (16 * T);
+                    const int khalf = (d.smem_per_sm / 2 - 2048) / (16 * T);
+                    int last = -1;
+                    for (int kcap : {kfull, khalf}) {
+                        const int k = static_cast<int>(std::min<int64_t>(cover, kcap));
+                        if (k < 1 || k == last) continue;
+                        last = k;
+                        tr_plan q = base(TR_PLAN_SPLIT);
+                        q.lanes_per_row = 32;
+                        q.warps_per_row = T / 32;
+                        q.rows_per_cta = 1;
+                        q.block_threads = T;
+                        q.cluster_ctas = C;
+                        q.vec_slots = k;
+                        cands.push_back(q);
+                    }
                 }
         }
     }

@@ -1,0 +1,361 @@
+// TR_PLAN_SPLIT: few, long rows spread over every SM.
+//
+// A row is cut into C contiguous segments, one per CTA (C <= 32), and all
+// rows * C CTAs are resident at once (cooperative launch), so a 16-row problem
+// can use every SM instead of one cluster of at most 16 CTAs per row. Each CTA:
+//   1. copies the first part of its segment (up to its shared-memory share)
+//      into shared memory with one bulk asynchronous copy and, while the copy
+//      lands, streams the rest of the segment (the overflow) for statistics;
+//   2. reduces its segment to one partial statistic (softmax: the (max, sum
+//      of exp) pair; RMSNorm: the sum of squares; LayerNorm: Chan moments),
+//      publishes it to a global workspace and arrives on the row's counter;
+//   3. waits (bounded in time) until the C segments of its row have arrived,
+//      merges the C partials in a fixed order, and writes its segment: the
+//      cached part from shared memory, the overflow re-read from L2.
+// This is the combine of "TIRx Metal reduction lowering" §4.2 (cooperative
+// striping) one level up: the per-row partial array lives in global memory
+// instead of on-chip memory, and a per-row arrival counter replaces the
+// barrier. The last CTA to leave a row clears the row's counters, so launches
+// that reuse one workspace in stream order (or graph replays) need no
+// host-side reset.
+#pragma once
+
+#include <type_traits>
+
+#include "tr_row_kernels.cuh"
+
+namespace tr {
+
+constexpr int kSplitU = 4;  // float4 per thread per streamed chunk
+
+__device__ __forceinline__ float4 pack(float v) { return make_float4(v, 0.0f, 0.0f, 0.0f); }
+__device__ __forceinline__ float4 pack(MaxSum v) { return make_float4(v.m, v.s, 0.0f, 0.0f); }
+__device__ __forceinline__ float4 pack(Moments v) { return make_float4(v.n, v.mean, v.m2, 0.0f); }
+template <class T>
+__device__ __forceinline__ T unpack(float4 v);
+template <>
+__device__ __forceinline__ float unpack<float>(float4 v) { return v.x; }
+template <>
+__device__ __forceinline__ MaxSum unpack<MaxSum>(float4 v) { return MaxSum{v.x, v.y}; }
+template <>
+__device__ __forceinline__ Moments unpack<Moments>(float4 v) { return Moments{v.x, v.y, v.z}; }
+
+template <int OP>
+using SplitStat = typename std::conditional<
+    OP == OP_SOFTMAX, MaxSum, typename std::conditional<OP == OP_LAYERNORM, Moments, float>::type>::type;
+
+// Fold N float4 (all valid) into a running statistic.
+template <int OP, int N>
+__device__ __forceinline__ SplitStat<OP> fold_chunk(SplitStat<OP> st, const float4 (&c)[kSplitU]) {
+    if constexpr (OP == OP_SOFTMAX) {
+        float cm = MaxOp::id();
+#pragma unroll
+        for (int u = 0; u < N; ++u) cm = fmaxf(cm, max4(c[u]));
+        const float m = fmaxf(st.m, cm);
+        if (m == MaxOp::id()) return st;
+        const float mb = mb_of(m);
+        float s = st.s * ex2(mb_of(st.m) - mb);
+#pragma unroll
+        for (int u = 0; u < N; ++u)
+            s += (ex2(fmaf(c[u].x, kL2E, -mb)) + ex2(fmaf(c[u].y, kL2E, -mb))) +
+                 (ex2(fmaf(c[u].z, kL2E, -mb)) + ex2(fmaf(c[u].w, kL2E, -mb)));
+        return MaxSum{m, s};
+    } else if constexpr (OP == OP_RMSNORM) {
+#pragma unroll
+        for (int u = 0; u < N; ++u)
+            st = fmaf(c[u].x, c[u].x, fmaf(c[u].y, c[u].y, fmaf(c[u].z, c[u].z, fmaf(c[u].w, c[u].w, st))));
+        return st;
+    } else {
+        float sm = 0.0f;
+#pragma unroll
+        for (int u = 0; u < N; ++u) sm += sum4(c[u]);
+        const float cnt = 4.0f * N;
+        const float mu = __fdiv_rn(sm, cnt);
+        float m2 = 0.0f;
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            const float dx = c[u].x - mu, dy = c[u].y - mu, dz = c[u].z - mu, dw = c[u].w - mu;
+            m2 = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, fmaf(dw, dw, m2))));
+        }
+        return mo_merge(st, Moments{cnt, mu, m2});
+    }
+}
+
+// Fold one scalar (a head or tail element of the row).
+template <int OP>
+__device__ __forceinline__ SplitStat<OP> fold_one(SplitStat<OP> st, float x) {
+    if constexpr (OP == OP_SOFTMAX) {
+        return ms_merge(st, ms_single(x));
+    } else if constexpr (OP == OP_RMSNORM) {
+        return fmaf(x, x, st);
+    } else {
+        return mo_merge(st, Moments{1.0f, x, 0.0f});
+    }
+}
+
+// Statistic of this thread's share of the cached part: slots t, t+T, ... < n.
+// Softmax replaces each cached element by 2^(x*log2e - off), off = RN(ml*log2e)
+// for the thread's own maximum ml (0 when ml = -inf), and returns ml in `ml`.
+template <int OP>
+__device__ __forceinline__ SplitStat<OP> fold_cached(float4* cache, int n, int t, int T, float& ml) {
+    if constexpr (OP == OP_SOFTMAX) {
+        ml = MaxOp::id();
+        for (int i = t; i < n; i += T) ml = fmaxf(ml, max4(cache[i]));
+        const float off = ml == MaxOp::id() ? 0.0f : mb_of(ml);
+        float s = 0.0f;
+        for (int i = t; i < n; i += T) {
+            float4 c = cache[i];
+            c.x = ex2(fmaf(c.x, kL2E, -off));
+            c.y = ex2(fmaf(c.y, kL2E, -off));
+            c.z = ex2(fmaf(c.z, kL2E, -off));
+            c.w = ex2(fmaf(c.w, kL2E, -off));
+            cache[i] = c;
+            s += sum4(c);
+        }
+        return MaxSum{ml, s};
+    } else if constexpr (OP == OP_RMSNORM) {
+        float st = 0.0f;
+        for (int i = t; i < n; i += T) {
+            const float4 c = cache[i];
+            st = fmaf(c.x, c.x, fmaf(c.y, c.y, fmaf(c.z, c.z, fmaf(c.w, c.w, st))));
+        }
+        return st;
+    } else {
+        float cnt = 0.0f, sm = 0.0f;
+        for (int i = t; i < n; i += T) {
+            cnt += 4.0f;
+            sm += sum4(cache[i]);
+        }
+        if (cnt == 0.0f) return Moments{0.0f, 0.0f, 0.0f};
+        const float mu = __fdiv_rn(sm, cnt);
+        float m2 = 0.0f;
+        for (int i = t; i < n; i += T) {
+            const float4 c = cache[i];
+            const float dx = c.x - mu, dy = c.y - mu, dz = c.z - mu, dw = c.w - mu;
+            m2 = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, fmaf(dw, dw, m2))));
+        }
+        return Moments{cnt, mu, m2};
+    }
+}
+
+// Arrival on a row counter: the release orders this thread's earlier stores
+// (the partial) before the increment; no value comes back.
+__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_relaxed4(const float4* p) {
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+// Merge of two statistics (the sum for RMSNorm's float).
+__device__ __forceinline__ float split_merge(float a, float b) { return a + b; }
+__device__ __forceinline__ MaxSum split_merge(MaxSum a, MaxSum b) { return ms_merge(a, b); }
+__device__ __forceinline__ Moments split_merge(Moments a, Moments b) { return mo_merge(a, b); }
+
+// Epilogue of one element for the row statistic (scale, shift, mb) and the
+// element's parameters.
+template <int OP>
+__device__ __forceinline__ float split_out(float x, float scale, float shift, float mb) {
+    if constexpr (OP == OP_SOFTMAX) {
+        return ex2(fmaf(x, kL2E, -mb)) * scale;
+    } else {
+        return (x - shift) * scale;
+    }
+}
+
+template <int OP>
+__global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
+    using Stat = SplitStat<OP>;
+    extern __shared__ __align__(16) float4 cache[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ float4 part[2][32];
+    __shared__ volatile int s_abort;
+    const int C = a.C;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) / C;
+    const int seg = static_cast<int>(blockIdx.x - row * C);
+    const int T = blockDim.x, t = threadIdx.x;
+    const float* xr = a.x + row * a.cols;
+    float* yr = a.y + row * a.cols;
+    const RowGeom g = row_geom(xr, a.cols);
+    const int per = (g.nvec + C - 1) / C;
+    const int v0 = min(g.nvec, seg * per), v1 = min(g.nvec, v0 + per);
+    const int nsm = min(v1 - v0, a.slot_floats / 4);  // slots [v0, v0 + nsm) are cached
+    const float* xb = xr + g.head;
+    float* yb = yr + g.head;
+    const bool own_h = seg == 0 && t < g.head;
+    const bool own_t = seg == C - 1 && t < g.tail;
+    const int ti = g.head + 4 * g.nvec + t;
+    if (t == 0) {
+        mbar_init(&bar, 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_enter();
+    if (t == 0) {
+        if (nsm > 0) {
+            mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nsm) * 16u);
+            bulk_g2s(cache, xb + 4 * v0, static_cast<uint32_t>(nsm) * 16u, &bar);
+        } else {
+            mbar_arrive(&bar);
+        }
+    }
+
+    // ---- 1. statistics: the overflow is streamed while the copy lands
+    Stat st = identity_of<Stat>();
+    int i = v0 + nsm + t;
+    for (; i + (kSplitU - 1) * T < v1; i += kSplitU * T) {
+        float4 c[kSplitU];
+#pragma unroll
+        for (int u = 0; u < kSplitU; ++u) c[u] = ld_stream4(xb + 4 * (i + u * T));
+        st = fold_chunk<OP, kSplitU>(st, c);
+    }
+    for (; i < v1; i += T) {
+        float4 c[kSplitU];
+        c[0] = ld_stream4(xb + 4 * i);
+        st = fold_chunk<OP, 1>(st, c);
+    }
+    float hv = 0.0f, tv = 0.0f;
+    if (own_h) {
+        hv = ld_stream1(xr + t);
+        st = fold_one<OP>(st, hv);
+    }
+    if (own_t) {
+        tv = ld_stream1(xr + ti);
+        st = fold_one<OP>(st, tv);
+    }
+    const bool copied = mbar_wait_bounded(&bar, 0, a.wait_ns, a.err);
+    if (!copied) s_abort = 1;
+    float ml = 0.0f;
+    st = split_merge(st, fold_cached<OP>(cache, nsm, t, T, ml));
+    RowPos p;
+    p.w = t;
+    p.W = T;
+    p.q = 0;
+    p.s = t >> 5;
+    p.S = T >> 5;
+    p.lane = t & 31;
+    int buf = 0;
+    st = cta_row_merge<Stat, 32>(st, p, part, buf);  // every thread holds the CTA's partial
+
+    // ---- 2. publish the partial; warp 0 waits for the row's C partials and
+    // merges them in lane order (the same in every CTA of the row)
+    __shared__ float4 s_row;
+    if (t == 0) {
+        a.sp_part[blockIdx.x] = pack(st);
+        red_add_release(a.sp_arrive + row, 1u);
+    }
+    if (t < 32) {
+        const unsigned long long t0 = global_ns();
+        bool late = false;
+        while (ld_acquire(a.sp_arrive + row) < static_cast<unsigned>(C)) {
+            if (static_cast<long long>(global_ns() - t0) > a.wait_ns) {
+                late = true;
+                break;
+            }
+            __nanosleep(20);
+        }
+        late = __any_sync(kFull, late);
+        if (late && t == 0) {
+            atomicOr(a.err, kErrWaitTimeout);
+            s_abort = 1;
+        }
+        const Stat v = warp_merge<Stat, 32>(p.lane < C ? unpack<Stat>(ld_relaxed4(a.sp_part + row * C + p.lane))
+                                                       : identity_of<Stat>());
+        if (t == 0) s_row = pack(v);
+    }
+    __syncthreads();
+    const Stat rs = unpack<Stat>(s_row);
+    // the last CTA to leave the row clears its counters for the next launch;
+    // every CTA has read the partials once its warp 0 is past the merge
+    auto depart = [&]() {
+        if (t == 0 && atomicAdd(a.sp_depart + row, 1u) == static_cast<unsigned>(C - 1)) {
+            a.sp_arrive[row] = 0u;
+            a.sp_depart[row] = 0u;
+            __threadfence();
+        }
+    };
+    if (s_abort) {
+        depart();
+        if (t == 0 && !copied) mbar_wait_bounded(&bar, 0, a.wait_ns, nullptr);  // drain the copy
+        return;
+    }
+
+    // ---- 4. epilogue: the overflow re-read first (most recently in L2), then the cached part
+    float scale, shift = 0.0f, mb = 0.0f, cscale = 0.0f;
+    if constexpr (OP == OP_SOFTMAX) {
+        mb = mb_of(rs.m);
+        scale = 1.0f / rs.s;
+        // cached values are 2^(x*log2e - off(ml)); ml = -inf caches only zeros
+        // (or NaN), and a row whose maximum is -inf gives NaN as in every plan
+        cscale = ex2((ml == MaxOp::id() ? 0.0f : mb_of(ml)) - mb) * scale;
+        if (ml == MaxOp::id() && rs.m != MaxOp::id()) cscale = 0.0f;
+    } else if constexpr (OP == OP_RMSNORM) {
+        scale = rsqrtf(fmaf(rs, a.inv_cols, a.eps));
+    } else {
+        scale = rsqrtf(fmaf(rs.m2, a.inv_cols, a.eps));
+        shift = rs.mean;
+    }
+    const bool wv = a.has_w && aligned16(a.w + g.head);
+    const bool bv = a.has_b && aligned16(a.b + g.head);
+    auto params = [&](float4 o, int j) -> float4 {
+        if constexpr (OP != OP_SOFTMAX) {
+            if (a.has_w) {
+                const float4 w4 = ld_param(a.w + g.head + 4 * j, wv);
+                o.x *= w4.x; o.y *= w4.y; o.z *= w4.z; o.w *= w4.w;
+            }
+            if constexpr (OP == OP_LAYERNORM) {
+                if (a.has_b) {
+                    const float4 b4 = ld_param(a.b + g.head + 4 * j, bv);
+                    o.x += b4.x; o.y += b4.y; o.z += b4.z; o.w += b4.w;
+                }
+            }
+        }
+        return o;
+    };
+    auto out4 = [&](float4 c) -> float4 {
+        return make_float4(split_out<OP>(c.x, scale, shift, mb), split_out<OP>(c.y, scale, shift, mb),
+                           split_out<OP>(c.z, scale, shift, mb), split_out<OP>(c.w, scale, shift, mb));
+    };
+    i = v0 + nsm + t;
+    for (; i + (kSplitU - 1) * T < v1; i += kSplitU * T) {
+        float4 c[kSplitU];
+#pragma unroll
+        for (int u = 0; u < kSplitU; ++u) c[u] = ld_stream4(xb + 4 * (i + u * T));
+#pragma unroll
+        for (int u = 0; u < kSplitU; ++u) st_out(yb + 4 * (i + u * T), params(out4(c[u]), i + u * T), a.y_vec);
+    }
+    for (; i < v1; i += T) st_out(yb + 4 * i, params(out4(ld_stream4(xb + 4 * i)), i), a.y_vec);
+    for (int j = t; j < nsm; j += T) {
+        const float4 c = cache[j];
+        float4 o;
+        if constexpr (OP == OP_SOFTMAX) {
+            o = make_float4(c.x * cscale, c.y * cscale, c.z * cscale, c.w * cscale);
+        } else {
+            o = out4(c);
+        }
+        st_out(yb + 4 * (v0 + j), params(o, v0 + j), a.y_vec);
+    }
+    auto params1 = [&](float o, int col) -> float {
+        if constexpr (OP != OP_SOFTMAX) {
+            if (a.has_w) o *= __ldg(a.w + col);
+            if (OP == OP_LAYERNORM && a.has_b) o += __ldg(a.b + col);
+        }
+        return o;
+    };
+    if (own_h) yr[t] = params1(split_out<OP>(hv, scale, shift, mb), t);
+    if (own_t) yr[ti] = params1(split_out<OP>(tv, scale, shift, mb), ti);
+    depart();
+}
+
+}  // namespace tr

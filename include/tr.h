@@ -75,7 +75,11 @@ typedef enum tr_plan_kind {
     TR_PLAN_ORDERED = 4,  /* OT-1024: 256 threads per row; cached (vec_slots > 0) or re-read (vec_slots == 0) */
     TR_PLAN_STAGED = 5,   /* persistent CTAs; rows_per_cta rows in flight in a shared-memory ring filled by
                              bulk asynchronous copies (TMA); each row reduced by the whole CTA from registers */
-    TR_PLAN_ORDERED_STAGED = 6  /* OT-1024 on persistent 256-thread CTAs fed by the same ring (rows_per_cta slots) */
+    TR_PLAN_ORDERED_STAGED = 6, /* OT-1024 on persistent 256-thread CTAs fed by the same ring (rows_per_cta slots) */
+    TR_PLAN_SPLIT = 7     /* a row per cluster_ctas co-resident CTAs (cooperative launch, 2..32); each CTA caches
+                             vec_slots * block_threads 16-byte slots of its segment in shared memory (one bulk
+                             asynchronous copy) and streams the rest; partials meet in a per-stream global
+                             workspace allocated on first use (64 KB + 16 KB per stream and device) */
 } tr_plan_kind;
 
 typedef struct tr_plan {
@@ -149,6 +153,14 @@ tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order orde
  * when every row start and the weight/bias vectors are 16-byte aligned. */
 tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows, int64_t cols,
                              tr_order order, int32_t align16, tr_plan* out);
+
+/* Host-only legality check of `plan` for a described device (occupancy from
+ * the device description's register and shared-memory model). Fills
+ * plan->grid_ctas, ctas_per_sm and est_us when legal. Returns TR_OK or
+ * TR_ERR_UNSUPPORTED / TR_ERR_INVALID_ARG with the reason in
+ * tr_last_error_message(); nothing is launched. */
+tr_status tr_plan_check_for(const tr_device_desc* dev, tr_plan* plan, int64_t rows, int64_t cols,
+                            int32_t align16);
 
 /* Force the next calls of plan->op to use exactly this plan (kind,
  * lanes_per_row, warps_per_row, rows_per_cta, cluster_ctas, vec_slots,

@@ -185,6 +185,31 @@ def test_ordered_extreme_logits_bit_exact(op):
     assert np.array_equal(got.view(np.uint32), emu.view(np.uint32))
 
 
+@pytest.mark.parametrize("op", ["softmax", "cross_entropy"])
+def test_ordered_nan_and_signed_zero_rows(op):
+    # rows whose maximum is a signed zero or that hold a NaN or an infinity:
+    # outputs equal the emulation bit for bit, NaN where it has NaN
+    x = torch.randn(8, 2053, generator=torch.Generator().manual_seed(21)) * 3.0
+    x[0] = -x[0].abs() - 1.0
+    x[0, 5] = -0.0                       # maximum -0
+    x[1] = -x[1].abs() - 1.0
+    x[1, 9], x[1, 2000] = -0.0, 0.0      # maximum a tie of -0 and +0
+    x[2, 1000] = float("nan")
+    x[3, 0] = float("nan")
+    x[3, 2052] = float("nan")
+    x[4, 17] = float("inf")
+    x[5] = float("-inf")
+    x[5, 3] = float("nan")
+    x[6] = 0.0
+    x[6, ::2] = -0.0
+    d = {"x": x.to(DEV), "labels": torch.arange(8, dtype=torch.int64, device=DEV) * 250}
+    got = run(op, d, order="ordered").cpu().numpy()
+    emu = emulated(op, host(d))
+    assert np.array_equal(np.isnan(got), np.isnan(emu))
+    ok = ~np.isnan(emu)
+    assert np.array_equal(got[ok].view(np.uint32), emu[ok].view(np.uint32))
+
+
 def test_ordered_shift_invariance_exact():
     # x on a 2^-10 grid, x + 1 exact: x - max is identical, so softmax bits are identical
     g = torch.randint(-2048, 2049, (5, 3000), generator=torch.Generator().manual_seed(3)).float() / 1024.0
@@ -201,7 +226,7 @@ def legal_plans(op, rows, cols):
     code = tr.OPS[op]
     plans = []
     kinds = [tr.TR_PLAN_XENT] if op == "cross_entropy" else [tr.TR_PLAN_ROWS, tr.TR_PLAN_CLUSTER, tr.TR_PLAN_STREAM,
-                                                             tr.TR_PLAN_STAGED]
+                                                             tr.TR_PLAN_STAGED, tr.TR_PLAN_SPLIT]
     for kind in kinds:
         if kind in (tr.TR_PLAN_ROWS, tr.TR_PLAN_XENT):
             ks = [2, 4, 8] if kind == tr.TR_PLAN_XENT else [1, 2, 4, 8, 16]
@@ -224,6 +249,12 @@ def legal_plans(op, rows, cols):
                         for flags in (0, tr.TR_PLAN_FLAG_PARAMS_IN_REGISTERS):
                             plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=t // 32, rows_per_cta=nb,
                                               cluster_ctas=1, vec_slots=k, block_threads=t, flags=flags))
+        elif kind == tr.TR_PLAN_SPLIT:
+            for c in (2, 3, 32):
+                for t in (64, 256, 1024):
+                    for k in (0, 1, 3):
+                        plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=t // 32, rows_per_cta=1,
+                                          cluster_ctas=c, vec_slots=k, block_threads=t))
         else:
             for c in ((2, 3, 8) if kind == tr.TR_PLAN_CLUSTER else (1, 2, 5)):
                 for t in (64, 256, 1024):

@@ -46,7 +46,8 @@ def covers(p, cols):
 @pytest.mark.parametrize("op", [0, 1, 2])
 def test_unordered_plans_are_legal_and_cover(op, rows, cols):
     p = select(op, rows, cols)
-    assert p.kind in (trlib.TR_PLAN_ROWS, trlib.TR_PLAN_CLUSTER, trlib.TR_PLAN_STREAM, trlib.TR_PLAN_STAGED)
+    assert p.kind in (trlib.TR_PLAN_ROWS, trlib.TR_PLAN_CLUSTER, trlib.TR_PLAN_STREAM, trlib.TR_PLAN_STAGED,
+                      trlib.TR_PLAN_SPLIT)
     assert covers(p, cols)
     assert p.block_threads % 32 == 0 and 32 <= p.block_threads <= 1024
     assert p.candidates >= 1 and p.est_us > 0 and p.ctas_per_sm >= 1
@@ -54,6 +55,9 @@ def test_unordered_plans_are_legal_and_cover(op, rows, cols):
         assert p.grid_ctas == math.ceil(rows / p.rows_per_cta)
     elif p.kind == trlib.TR_PLAN_STAGED:
         assert p.grid_ctas == min(rows, p.ctas_per_sm * DEV.sm_count)  # persistent CTAs
+    elif p.kind == trlib.TR_PLAN_SPLIT:
+        assert p.grid_ctas == rows * p.cluster_ctas <= p.ctas_per_sm * DEV.sm_count  # all resident
+        assert 2 <= p.cluster_ctas <= 32 and p.vec_slots * p.block_threads * 16 <= 225 * 1024
     else:
         assert p.grid_ctas == rows * p.cluster_ctas
     if p.flags:
@@ -147,3 +151,25 @@ def test_fewer_sms_never_gives_a_cheaper_estimate():
     small.sm_count = 38
     for op in (0, 2):
         assert select(op, 768, 6144).est_us <= trlib.tr_plan_select_for(small, op, 768, 6144, 0, 1).est_us
+
+
+def split_plan(rows, cols, C=4, T=512, K=2, op=0):
+    return trlib.tr_plan(op=op, order=0, kind=trlib.TR_PLAN_SPLIT, lanes_per_row=32, warps_per_row=T // 32,
+                         rows_per_cta=1, cluster_ctas=C, vec_slots=K, block_threads=T)
+
+
+def test_split_plan_limits():
+    # legal: co-resident grid, 2..32 CTAs per row, cache within the shared-memory budget
+    for C, T, K, ok in [(2, 512, 2, True), (32, 256, 1, True), (33, 256, 1, False), (1, 256, 1, False),
+                        (8, 1024, 14, True), (8, 1024, 15, False), (8, 512, 0, True)]:
+        p = split_plan(4, 100000, C, T, K)
+        st, why = trlib.check_plan_for(DEV, p, 4, 100000, 1)
+        assert (st == trlib.TR_OK) == ok, (C, T, K, why)
+    # the grid must fit the device at once: 200 rows x 2 CTAs of 1024 threads cannot
+    st, why = trlib.check_plan_for(DEV, split_plan(200, 4096, 2, 1024, 1), 200, 4096, 1)
+    assert st == trlib.TR_ERR_UNSUPPORTED and "resident" in why
+    # the ordered policy is never split
+    p = split_plan(4, 100000)
+    p.order = 1
+    st, _ = trlib.check_plan_for(DEV, p, 4, 100000, 1)
+    assert st == trlib.TR_ERR_UNSUPPORTED
