@@ -94,6 +94,7 @@ SIGNATURES = {
     "tr_plan_describe": ([_I32, _I64, _I64, _I32, ctypes.POINTER(tr_plan)], _I32),
     "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
                             ctypes.POINTER(tr_plan)], _I32),
+    "tr_split_rows_noalloc_f32": ([_I32, _P, _P, _P, _P, _I64, _I64, ctypes.c_float, _P], _I32),
     "tr_plan_check_for": ([ctypes.POINTER(tr_device_desc), ctypes.POINTER(tr_plan), _I64, _I64, _I32], _I32),
     "tr_plan_override": ([ctypes.POINTER(tr_plan)], _I32),
     "tr_last_device_error": ([], _I32),
@@ -143,6 +144,25 @@ def _check(status: int, where: str):
 
 def tr_softmax_f32(x, y, rows, cols, order, stream):
     return load().tr_softmax_f32(x, y, rows, cols, order, stream)
+
+
+def tr_split_rows_noalloc_f32(op, x, w, b, y, rows, cols, eps, stream):
+    return load().tr_split_rows_noalloc_f32(op, x, w, b, y, rows, cols, eps, stream)
+
+
+def split_rows_noalloc(op, x, out, weight=None, bias=None, eps=1e-5, stream=None):
+    """The no-allocation entry point on CUDA float32 tensors. ``out`` is
+    required: this wrapper creates no tensor, and the library allocates no
+    device memory."""
+    code = OPS[op] if isinstance(op, str) else int(op)
+    _check_matrix(x, "x")
+    _check_matrix(out, "out")
+    r, c = x.shape
+    wp = _check_vector(weight, "weight", c)
+    bp = _check_vector(bias, "bias", c)
+    _check(tr_split_rows_noalloc_f32(code, x.data_ptr(), wp, bp, out.data_ptr(), r, c, eps, _stream_handle(stream)),
+           "split_rows_noalloc")
+    return out
 
 
 def tr_rmsnorm_f32(x, w, y, rows, cols, eps, order, stream):

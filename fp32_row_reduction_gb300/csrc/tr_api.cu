@@ -326,6 +326,11 @@ RowArgs blank_args(const float* x, int64_t rows, int64_t cols) {
 }
 
 }  // namespace
+
+void set_last_error(const char* what, const char* detail) { t_last_error = std::string(what) + ": " + detail; }
+
+cudaError_t device_error_symbol(void** out) { return cudaGetSymbolAddress(out, g_device_error); }
+
 }  // namespace tr
 
 using namespace tr;

@@ -52,6 +52,11 @@ constexpr size_t kSplitWorkspaceBytes = kSplitMaxParts * 16 + 2 * kSplitMaxRows 
 // body plus one partial 16-byte chunk on each side.
 inline int staged_slot_floats(int64_t cols) { return static_cast<int>((cols + 3) / 4 * 4 + 8); }
 
+// Set the calling thread's last-error text to "what: detail" (tr_last_error_message).
+void set_last_error(const char* what, const char* detail);
+// Device address of the library's error word on the current device.
+cudaError_t device_error_symbol(void** out);
+
 // Kernel entry for a plan, or nullptr when this build has no such
 // instantiation (the plan is then unsupported). One table per operator.
 const void* kernel_softmax(int kind, int lanes, int slots, int flags);

@@ -143,6 +143,43 @@ tr_status tr_layernorm_f32(const float* x, const float* gamma, const float* beta
 tr_status tr_cross_entropy_f32(const float* logits, const int64_t* labels, float* losses,
                                int64_t rows, int64_t cols, tr_order order, cudaStream_t stream);
 
+/* ---- no-allocation entry point ----------------------------------------- */
+
+/* Softmax, RMSNorm or LayerNorm of few long rows with no device allocation on
+ * any call. The pages have no counterpart: it exists for callers that cannot
+ * allocate device memory at call time, such as code running inside a
+ * pre-sized arena in which every byte is accounted for, or latency-critical
+ * loops in which cudaMalloc (which may synchronise the device and can fail
+ * under memory pressure) is not acceptable. The other entry points allocate a
+ * small workspace on a stream's first split-row launch; this one always runs
+ * the split-row plan (TR_PLAN_SPLIT, unordered policy) over a fixed 18 KB
+ * scratch array compiled into the library.
+ *
+ * op: TR_OP_SOFTMAX (w and b must be NULL), TR_OP_RMSNORM (w optional, b
+ * NULL) or TR_OP_LAYERNORM (w = gamma, b = beta, each optional); x, y:
+ * rows x cols row-major device pointers, 4-byte aligned, y not overlapping an
+ * input; eps finite and >= 0 (ignored by softmax). The library owns nothing
+ * the caller passes.
+ *
+ * Limits: rows <= 256, and each row gets C = min(32, R / rows) CTAs, where R
+ * is the number of CTAs the device holds at once (two per SM at 512 threads),
+ * so rows <= R / 2 (152 rows on a 152-SM device). Larger inputs return
+ * TR_ERR_UNSUPPORTED with the reason in tr_last_error_message(); nothing is
+ * launched. Results are within the unordered tolerance of the other entry
+ * points and run-to-run deterministic.
+ *
+ * Set-up: the first call on each device looks up the scratch and error-word
+ * addresses, sets the kernels' shared-memory limit and queries their
+ * residency. Make that first call before capturing a stream into a graph.
+ *
+ * State and concurrency: the scratch's counters must be zero before a launch.
+ * They are zero when the library loads, and every launch leaves them at zero
+ * (the last CTA to leave a row clears its counters). There is one scratch per
+ * device, shared by all streams and host threads: calls whose kernels may
+ * overlap in time race on it, so order them (for example, one stream). */
+tr_status tr_split_rows_noalloc_f32(int32_t op, const float* x, const float* w, const float* b, float* y,
+                                    int64_t rows, int64_t cols, float eps, cudaStream_t stream);
+
 /* ---- plans, errors, introspection -------------------------------------- */
 
 /* The plan the next call with these arguments would use on the current

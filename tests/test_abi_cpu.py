@@ -109,3 +109,16 @@ def test_override_rejects_malformed(lib):
     p = trlib.tr_plan(op=0, kind=17)
     assert trlib.tr_plan_override(p) == trlib.TR_ERR_INVALID_ARG
     assert trlib.tr_plan_override(None) == trlib.TR_OK
+
+
+def test_noalloc_entry_rejects_bad_arguments_on_the_host(lib):
+    f = trlib.tr_split_rows_noalloc_f32
+    assert f(0, None, None, None, None, 0, 10, 0.0, None) == trlib.TR_OK          # empty: nothing to do
+    assert f(3, None, None, None, None, 4, 10, 0.0, None) == trlib.TR_ERR_INVALID_ARG  # no cross-entropy
+    assert f(0, 0x1000, 0x2000, None, 0x100000, 4, 10, 0.0, None) == trlib.TR_ERR_INVALID_ARG  # softmax + w
+    assert f(1, 0x1000, None, None, 0x100000, 4, 10, float("nan"), None) == trlib.TR_ERR_INVALID_ARG
+    assert f(2, 0x1000, None, None, 0x1010, 4, 10, 1e-5, None) == trlib.TR_ERR_INVALID_ARG  # y overlaps x
+    assert f(2, 0x1002, None, None, 0x100000, 4, 10, 1e-5, None) == trlib.TR_ERR_INVALID_ARG  # misaligned
+    # more rows than the fixed scratch holds: refused before any CUDA call
+    assert f(0, 0x1000, None, None, 0x10000000, 257, 10, 0.0, None) == trlib.TR_ERR_UNSUPPORTED
+    assert "256 rows" in lib.tr_last_error_message().decode()
