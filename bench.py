@@ -182,6 +182,12 @@ def build_graph(launches, steps, sets, first_set, timing):
     evs = []
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
+    # one eager call of each launch on the capture stream first: split-row
+    # plans allocate their per-stream workspace on a stream's first call
+    with torch.cuda.stream(stream):
+        for ln in launches:
+            ln(first_set % sets)
+    torch.cuda.synchronize()
     with torch.cuda.graph(g, stream=stream):
         for i in range(steps):
             s = (first_set + i) % sets

@@ -45,6 +45,7 @@ TR_PLAN_STAGED = 5
 TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_SPLIT = 7
 TR_PLAN_FLAG_PARAMS_IN_REGISTERS = 1
+TR_PLAN_FLAG_PARAMS_IN_SHARED = 2
 
 OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LAYERNORM,
        "cross_entropy": TR_OP_CROSS_ENTROPY}
@@ -58,7 +59,7 @@ class tr_plan(ctypes.Structure):
         ("rows_per_cta", ctypes.c_int32), ("cluster_ctas", ctypes.c_int32),
         ("vec_slots", ctypes.c_int32), ("block_threads", ctypes.c_int32),
         ("ctas_per_sm", ctypes.c_int32), ("grid_ctas", ctypes.c_int64), ("est_us", ctypes.c_double),
-        ("candidates", ctypes.c_int32), ("flags", ctypes.c_int32),
+        ("candidates", ctypes.c_int32), ("flags", ctypes.c_int32), ("resident_ctas", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -95,6 +96,11 @@ SIGNATURES = {
     "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
                             ctypes.POINTER(tr_plan)], _I32),
     "tr_split_rows_noalloc_f32": ([_I32, _P, _P, _P, _P, _I64, _I64, ctypes.c_float, _P], _I32),
+    "tr_plan_cost_constants": ([ctypes.POINTER(ctypes.c_double), _I32], _I32),
+    "tr_plan_estimate_with": ([ctypes.POINTER(tr_device_desc), ctypes.POINTER(tr_plan), _I64, _I64, _I32,
+                               ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], _I32),
+    "tr_plan_candidates": ([_I32, _I64, _I64, _I32, _I32, ctypes.POINTER(tr_plan), _I32,
+                            ctypes.POINTER(_I32)], _I32),
     "tr_plan_check_for": ([ctypes.POINTER(tr_device_desc), ctypes.POINTER(tr_plan), _I64, _I64, _I32], _I32),
     "tr_plan_override": ([ctypes.POINTER(tr_plan)], _I32),
     "tr_last_device_error": ([], _I32),
@@ -195,6 +201,32 @@ def check_plan_for(dev: tr_device_desc, plan: tr_plan, rows, cols, align16=1):
     lib = load()
     st = lib.tr_plan_check_for(ctypes.byref(dev), ctypes.byref(plan), rows, cols, align16)
     return st, ("" if st == TR_OK else lib.tr_last_error_message().decode())
+
+
+def cost_constants():
+    """The library's cost-model constants (TR_COST_CONSTANTS doubles)."""
+    out = (ctypes.c_double * 12)()
+    _check(load().tr_plan_cost_constants(out, 12), "tr_plan_cost_constants")
+    return list(out)
+
+
+def estimate_with(dev: tr_device_desc, plan: tr_plan, rows, cols, align16=1, constants=None) -> float:
+    """The model's estimate (us) for a plan with grid_ctas/ctas_per_sm filled, under given constants."""
+    c = None if constants is None else (ctypes.c_double * 12)(*constants)
+    out = ctypes.c_double()
+    _check(load().tr_plan_estimate_with(ctypes.byref(dev), ctypes.byref(plan), rows, cols, align16, c,
+                                        ctypes.byref(out)), "tr_plan_estimate_with")
+    return out.value
+
+
+def plan_candidates(op, rows, cols, order=0, align16=1):
+    """Every legal candidate plan on the current device, with estimates."""
+    lib = load()
+    n = ctypes.c_int32()
+    _check(lib.tr_plan_candidates(op, rows, cols, order, align16, None, 0, ctypes.byref(n)), "tr_plan_candidates")
+    buf = (tr_plan * max(1, n.value))()
+    _check(lib.tr_plan_candidates(op, rows, cols, order, align16, buf, n.value, ctypes.byref(n)), "tr_plan_candidates")
+    return list(buf[:n.value])
 
 
 def tr_plan_override(plan: tr_plan | None) -> int:

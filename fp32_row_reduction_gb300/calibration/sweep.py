@@ -1,0 +1,127 @@
+"""Time every legal plan of the family on this GPU, for the cost model's
+offline calibration and audit ("Whole-launch reduction cost policy":
+measurement calibrates the model's priors and audits its choices; it never
+selects the plan a call runs).
+
+    python -m fp32_row_reduction_gb300.calibration.sweep --set calibration > cal.jsonl
+    python -m fp32_row_reduction_gb300.calibration.sweep --set heldout > held.jsonl
+
+Each line: op, rows, cols, the plan (with the device's occupancy and grid) and
+its time per launch in microseconds (a CUDA graph of back-to-back launches on
+input/output sets that together exceed twice the L2, best of three replays).
+"""
+import argparse
+import gzip
+import json
+import math
+import sys
+
+import torch
+
+import synth
+import fp32_row_reduction_gb300 as tr
+
+# Shapes DISJOINT from the benchmark workloads: the fit sees only these.
+CALIBRATION = {
+    "rows": [(512, 4096), (1024, 8192), (300, 5000), (2048, 2048), (4096, 256), (32768, 64), (100, 20000),
+             (8, 131072), (32, 32768), (2000, 1000), (200, 3000), (12, 500000), (1200, 4096), (600, 8192),
+             (4, 1000000), (64, 65536), (1536, 3072), (160, 6144)],
+    "cross_entropy": [(1024, 32000), (256, 128000), (8192, 8192)],
+}
+# The benchmark workloads, scored only after the fit (held out).
+HELDOUT = {
+    "rows": [(37, 1537), (256, 3072), (64, 12289), (768, 6144), (16, 65536), (16, 262144), (16, 1048576),
+             (65536, 128)],
+    "cross_entropy": [(4096, 50257)],
+}
+L2_BYTES = 126 << 20
+GUARD = 4096          # floats of guard band on each side of an output
+SENTINEL = -12345.0
+
+
+def time_plan(op, ins, outs, plan, est_us):
+    tr.tr_plan_override(plan)
+    s = torch.cuda.Stream()
+    sets = len(ins)
+    with torch.cuda.stream(s):
+        for i in range(3):
+            tr.run_op(op, ins[i % sets], out=outs[i % sets], stream=s)
+    torch.cuda.synchronize()
+    n = int(min(100, max(5, 300.0 / max(est_us, 1.0))))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(n):
+            tr.run_op(op, ins[i % sets], out=outs[i % sets], stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = math.inf
+    for _ in range(3):
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        best = min(best, 1e3 * e0.elapsed_time(e1) / n)
+    return best
+
+
+def sweep(op, rows, cols, out):
+    dev = torch.device("cuda:0")
+    base = synth.make_inputs(op, rows, cols, 11, var=4.0 if op == "softmax" else None,
+                             row_offset=op in ("rmsnorm", "layernorm"), device=dev)
+    per_set = 8 * rows * cols
+    sets = max(2, math.ceil(2 * L2_BYTES / per_set))
+    ins = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(sets - 1)]
+    shape = (rows,) if op == "cross_entropy" else (rows, cols)
+    n_out = math.prod(shape)
+    # every output sits between guard bands of a sentinel value; each plan must
+    # leave the bands untouched and match the library's default plan
+    bigs = [torch.full((n_out + 2 * GUARD,), SENTINEL, device=dev) for _ in range(sets)]
+    outs = [b[GUARD:GUARD + n_out].view(shape) for b in bigs]
+    want = tr.run_op(op, ins[0]).clone()
+    tol = 1e-4 * float(want.abs().max()) + 1e-6
+    cands = tr.plan_candidates(tr.OPS[op], rows, cols, 0, 1)
+    default = tr.tr_plan_describe(tr.OPS[op], rows, cols, 0).as_dict()
+    for p in cands:
+        d = p.as_dict()
+        try:
+            us = time_plan(op, ins, outs, p, d["est_us"])
+        except tr.TrError as e:
+            print(json.dumps({"op": op, "rows": rows, "cols": cols, "error": str(e)[:160], "plan": d}), file=sys.stderr)
+            continue
+        for b in bigs:
+            if not (bool((b[:GUARD] == SENTINEL).all()) and bool((b[GUARD + n_out:] == SENTINEL).all())):
+                raise RuntimeError(f"plan {d} wrote outside its output ({op} {rows}x{cols})")
+        if not float((outs[0] - want).abs().max()) <= tol:
+            raise RuntimeError(f"plan {d} disagrees with the default plan ({op} {rows}x{cols})")
+        out.write(json.dumps({"op": op, "rows": rows, "cols": cols, "us": round(us, 4), "plan": d,
+                              "default": all(d[k] == default[k] for k in ("kind", "lanes_per_row", "warps_per_row",
+                                                                          "rows_per_cta", "cluster_ctas", "vec_slots",
+                                                                          "block_threads", "flags"))}) + "\n")
+        out.flush()
+    tr.tr_plan_override(None)
+    if tr.tr_last_device_error() != tr.TR_OK:
+        raise RuntimeError("a bounded device wait gave up during the sweep")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--set", choices=["calibration", "heldout"], required=True)
+    ap.add_argument("--out", default="-")
+    args = ap.parse_args()
+    tr.load()
+    shapes = CALIBRATION if args.set == "calibration" else HELDOUT
+    out = sys.stdout if args.out == "-" else (gzip.open(args.out, "wt") if args.out.endswith(".gz") else open(args.out, "w"))
+    for op in ("softmax", "rmsnorm", "layernorm"):
+        for rows, cols in shapes["rows"]:
+            print(f"{op} {rows}x{cols}", file=sys.stderr, flush=True)
+            sweep(op, rows, cols, out)
+    for rows, cols in shapes["cross_entropy"]:
+        print(f"cross_entropy {rows}x{cols}", file=sys.stderr, flush=True)
+        sweep("cross_entropy", rows, cols, out)
+    if out is not sys.stdout:
+        out.close()
+
+
+if __name__ == "__main__":
+    main()

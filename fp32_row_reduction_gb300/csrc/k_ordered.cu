@@ -61,13 +61,21 @@ __device__ __noinline__ float exp_ot_wide(float x) {
     return __fmul_rn(__fmul_rn(p, pow2i(k1)), pow2i(k - k1));
 }
 
-// For k in [-125, 127] the polynomial p lies in [2^-0.5, 2^0.5], so p * 2^k is
-// a normal number: adding k to p's exponent field is exact and gives the same
-// bits as the two-step product. Other k (|x| > 86, infinities) take the
-// clamped form; NaN is selected at the end.
+// Fast form for |x| < 86 (so |k| <= 124), the same bits with full-rate
+// instructions only:
+//  - rint(t) for |t| < 2^22 is (t + M) - M with M = 1.5 * 2^23: the sum lands
+//    in [2^23, 2^24), where the float spacing is 1, so adding M rounds t to an
+//    integer with ties to even (M is even), and the difference is exact; k is
+//    the sum's bit pattern minus M's.
+//  - p lies in [2^-0.5, 2^0.5], so p * 2^k is normal: adding k to p's exponent
+//    field is exact and equals the two-step product.
+// Other x (|x| >= 86, infinities, NaN) take the clamped form.
 __device__ __forceinline__ float exp_ot(float x) {
-    const float kf = rintf(__fmul_rn(x, 0x1.715476p+0f));
-    const int k = static_cast<int>(kf);  // saturating; NaN gives 0
+    if (!(fabsf(x) < 86.0f)) return x != x ? __fadd_rn(x, x) : exp_ot_wide(x);
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    const float u = __fadd_rn(__fmul_rn(x, 0x1.715476p+0f), kMagic);
+    const float kf = __fsub_rn(u, kMagic);
+    const int k = __float_as_int(u) - 0x4b400000;
     float r = __fmaf_rn(-kf, 0x1.62e430p-1f, x);
     r = __fmaf_rn(-kf, -0x1.05c610p-29f, r);
     float p = 0x1.a01a02p-13f;
@@ -78,13 +86,7 @@ __device__ __forceinline__ float exp_ot(float x) {
     p = __fmaf_rn(p, r, 0x1.000000p-1f);
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
-    float e;
-    if (static_cast<unsigned>(k) + 125u <= 252u) {
-        e = __int_as_float(__float_as_int(p) + static_cast<int>(static_cast<unsigned>(k) << 23));
-    } else {
-        e = exp_ot_wide(x);
-    }
-    return x != x ? __fadd_rn(x, x) : e;
+    return __int_as_float(__float_as_int(p) + static_cast<int>(static_cast<unsigned>(k) << 23));
 }
 
 // log on binary32: x = 2^e m, m in (sqrt(1/2), sqrt(2)], f = m - 1,

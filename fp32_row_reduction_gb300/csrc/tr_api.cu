@@ -15,6 +15,7 @@
 #include <mutex>
 #include <string>
 #include <tuple>
+#include <vector>
 
 #include "tr.h"
 #include "tr_internal.h"
@@ -43,7 +44,7 @@ struct DeviceState {
     tr_device_desc desc{};
     unsigned* err = nullptr;  // device address of g_device_error on this device
     std::map<std::tuple<int, int64_t, int64_t, int, int>, tr_plan> plans;  // (op, rows, cols, order, align16)
-    std::map<std::tuple<const void*, int, int, size_t>, int> occ;  // (kernel, threads, cluster, smem) -> CTAs/SM
+    std::map<std::tuple<const void*, int, int, size_t>, int64_t> occ;  // (kernel, threads, cluster, smem) -> resident CTAs
     std::map<const void*, bool> smem_opt_in;                        // kernels allowed large dynamic smem
     std::map<const void*, bool> wide_cluster;                       // kernels allowed clusters above 8 CTAs
     std::map<cudaStream_t, void*> split_ws;                         // split-plan workspace per stream
@@ -117,9 +118,9 @@ bool opt_in_wide_cluster(DeviceState& st, const void* fn) {
     return ok;
 }
 
-// Resident CTAs per SM of a plan's kernel (0 = cannot run). Cluster plans:
-// the device's concurrent clusters times C, spread over the SMs.
-int query_occupancy(DeviceState& st, const tr_plan& p, size_t smem) {
+// CTAs of a plan's kernel resident at once on the device (0 = cannot run).
+// Cluster plans: the device's concurrent clusters times C.
+int64_t query_occupancy(DeviceState& st, const tr_plan& p, size_t smem) {
     const void* fn = kernel_for(p);
     if (!fn) return 0;
     const int C = (p.kind == TR_PLAN_CLUSTER || p.kind == TR_PLAN_STREAM) ? p.cluster_ctas : 1;
@@ -139,6 +140,7 @@ int query_occupancy(DeviceState& st, const tr_plan& p, size_t smem) {
     }
     if (C == 1) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, p.block_threads, smem) != cudaSuccess) n = 0;
+        n *= st.desc.sm_count;
     } else {
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
@@ -153,7 +155,7 @@ int query_occupancy(DeviceState& st, const tr_plan& p, size_t smem) {
         cfg.numAttrs = 1;
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) clusters = 0;
-        n = clusters > 0 ? std::max(1, clusters * C / std::max(1, st.desc.sm_count)) : 0;
+        n = clusters > 0 ? clusters * C : 0;
     }
     cudaGetLastError();
     st.occ[key] = n;
@@ -470,6 +472,48 @@ tr_status tr_plan_check_for(const tr_device_desc* dev, tr_plan* plan, int64_t ro
     return TR_OK;
 }
 
+tr_status tr_plan_cost_constants(double* out, int32_t n) {
+    if (!out || n != kCostConstantCount) return fail(TR_ERR_INVALID_ARG, "out must hold TR_COST_CONSTANTS doubles");
+    static_assert(sizeof(CostConstants) == kCostConstantCount * sizeof(double), "constants are doubles");
+    std::memcpy(out, &kCostDefaults, sizeof(CostConstants));
+    return TR_OK;
+}
+
+tr_status tr_plan_estimate_with(const tr_device_desc* dev, const tr_plan* plan, int64_t rows, int64_t cols,
+                                int32_t align16, const double* constants, double* out_us) {
+    if (!dev || !plan || !out_us) return fail(TR_ERR_INVALID_ARG, "dev, plan and out_us must not be null");
+    if (rows < 1 || cols < 1) return fail(TR_ERR_INVALID_ARG, "rows and cols must be >= 1");
+    if (dev->sm_count < 1 || dev->hbm_gbs <= 0) return fail(TR_ERR_INVALID_ARG, "malformed device description");
+    if (plan->grid_ctas < 1 || (plan->ctas_per_sm < 1 && plan->resident_ctas < 1) || plan->block_threads < 1)
+        return fail(TR_ERR_INVALID_ARG, "plan needs grid_ctas, resident_ctas (or ctas_per_sm) and block_threads");
+    CostConstants c = kCostDefaults;
+    if (constants) std::memcpy(&c, constants, sizeof c);
+    *out_us = estimate_us(*dev, *plan, rows, cols, align16 != 0 && cols % 4 == 0, c);
+    return TR_OK;
+}
+
+tr_status tr_plan_candidates(int32_t op, int64_t rows, int64_t cols, tr_order order, int32_t align16, tr_plan* out,
+                             int32_t cap, int32_t* count) {
+    if (!count || (cap > 0 && !out)) return fail(TR_ERR_INVALID_ARG, "count (and out when cap > 0) must not be null");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* st = nullptr;
+    s = device_state(dev, &st);
+    if (s != TR_OK) return s;
+    OccupancyFn occ = [st](const tr_plan& p, size_t smem) { return query_occupancy(*st, p, smem); };
+    std::vector<tr_plan> legal;
+    enumerate_plans(st->desc, occ, op, rows, cols, order, align16 != 0, &legal);
+    *count = static_cast<int32_t>(legal.size());
+    for (int32_t i = 0; i < cap && i < *count; ++i) out[i] = legal[i];
+    return TR_OK;
+}
+
 tr_status tr_plan_override(const tr_plan* plan) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!plan) {
@@ -529,6 +573,6 @@ const char* tr_status_string(tr_status status) {
 
 const char* tr_last_error_message(void) { return t_last_error.c_str(); }
 
-int32_t tr_version(void) { return 100; }
+int32_t tr_version(void) { return 200; }
 
 }  // extern "C"

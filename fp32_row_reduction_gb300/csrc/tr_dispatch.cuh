@@ -14,6 +14,7 @@ const void* rows_table(int slots) {
     }
     if constexpr (G == 32) {
         switch (slots) {
+            case 6: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 6>);
             case 8: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 8>);
             case 16: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 16>);
         }
@@ -37,10 +38,28 @@ const void* staged_pre_table(int slots) {
     }
 }
 
+// Row kernels of the norms with the weights staged in shared memory.
+template <int OP>
+const void* rows_sp_table(int slots) {
+    if constexpr (OP == OP_SOFTMAX) {
+        return nullptr;
+    } else {
+        switch (slots) {
+            case 2: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 2, true>);
+            case 4: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 4, true>);
+            case 6: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 6, true>);
+            case 8: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 8, true>);
+        }
+        return nullptr;
+    }
+}
+
 template <int OP>
 const void* unordered_table(int kind, int lanes, int slots, int flags) {
     if (flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS)
         return kind == TR_PLAN_STAGED ? staged_pre_table<OP>(slots) : nullptr;
+    if (flags & TR_PLAN_FLAG_PARAMS_IN_SHARED)
+        return (kind == TR_PLAN_ROWS && lanes == 32) ? rows_sp_table<OP>(slots) : nullptr;
     if (flags) return nullptr;
     switch (kind) {
         case TR_PLAN_ROWS:

@@ -6,15 +6,16 @@
 
 #include <functional>
 #include <stdint.h>
+#include <vector>
 
 #include "tr.h"
 
 namespace tr {
 
-// Resident CTAs per SM for a fully specified plan using `smem` bytes of
-// dynamic shared memory, or 0 if it cannot run. For cluster launches:
-// resident CTAs per SM implied by the number of clusters the device can hold.
-using OccupancyFn = std::function<int(const tr_plan&, size_t smem)>;
+// CTAs of a fully specified plan (using `smem` bytes of dynamic shared memory)
+// that the whole device holds at once, or 0 if it cannot run. For cluster
+// launches: the clusters the device can hold times the cluster size.
+using OccupancyFn = std::function<int64_t(const tr_plan&, size_t smem)>;
 
 // Host-only occupancy model from a register estimate (used without a GPU).
 int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem);
@@ -25,9 +26,22 @@ int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem);
 tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p, int64_t rows, int64_t cols,
                      bool align16, const char** why);
 
+// The cost model's constants (microseconds unless stated).
+struct CostConstants {
+    double launch, latency, cta_barrier, cluster_barrier, l2_over_hbm, staged_row, one_wave_alu, wave, slot_pass,
+        param_trip, clock_ghz, split_sync;
+};
+constexpr int kCostConstantCount = 12;
+extern const CostConstants kCostDefaults;
+
 // Cost-model estimate in microseconds for a legal plan (grid_ctas and
 // ctas_per_sm filled).
-double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int64_t cols, bool align16);
+double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int64_t cols, bool align16,
+                   const CostConstants& c = kCostDefaults);
+
+// Every legal candidate of the family, with its estimate.
+void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op, int64_t rows, int64_t cols,
+                     int32_t order, bool align16, std::vector<tr_plan>* legal);
 
 // Enumerate every legal candidate and return the cheapest.
 tr_status select_plan(const tr_device_desc& d, const OccupancyFn& occ, int32_t op, int64_t rows, int64_t cols,

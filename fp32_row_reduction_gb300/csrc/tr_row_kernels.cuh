@@ -26,9 +26,17 @@ namespace tr {
 // about 90 registers (at most 512 threads per CTA); a LayerNorm stripe of 16
 // or more floats, with its prefetched weights and biases, needs more than the
 // 64 registers a 1024-thread CTA allows.
+// K == 6 is the one-wave shape for rows of up to 6144 columns: 256 threads a
+// row and six rows on every SM (1536 threads, so at most 40 registers a
+// thread), which keeps 912 rows resident on 152 SMs; a CTA holds one, two or
+// three rows (256, 512 or 768 threads).
 template <int OP, int K>
 constexpr int max_threads_for() {
-    return K >= 16 ? 512 : (K >= 4 && OP == OP_LAYERNORM) ? 768 : 1024;
+    return K == 6 ? 768 : K >= 16 ? 512 : (K >= 4 && OP == OP_LAYERNORM) ? 768 : 1024;
+}
+template <int K>
+constexpr int min_blocks_for() {
+    return K == 6 ? 2 : 1;
 }
 
 // Staged kernels that also hold K float4 of weights (and of biases) per worker.
@@ -120,6 +128,18 @@ __device__ __forceinline__ void load_stripe(const float* xr, const RowGeom& g, c
     if (active && own_t) tv = ld_stream1(xb + 4 * g.nvec + wi);
 }
 
+// Norm weights and biases staged in shared memory (rows plans with
+// TR_PLAN_FLAG_PARAMS_IN_SHARED): one thread issues bulk asynchronous copies
+// of the whole weight (and bias) vector when the kernel starts, while the rows
+// load, and the epilogue reads them once `bar` completes instead of making a
+// dependent trip to L2 after the merges. All rows of the CTA share the copy.
+struct SharedParams {
+    const float* w;  // cols floats (16-byte aligned rows: column = body index)
+    const float* b;
+    uint64_t* bar;
+};
+__device__ __forceinline__ float4 ld_shared4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
 // The three cached epilogues. Every worker of the row calls this uniformly
 // (merges may contain a barrier); only the stores are predicated on `active`.
 //   softmax:   m = max (merge 1); e = 2^(x log2e - mb(m)) with one FMA per
@@ -133,11 +153,11 @@ __device__ __forceinline__ void load_stripe(const float* xr, const RowGeom& g, c
 // of compound statistics, which matters when a CTA reduces rows back to back.
 // PRE: the weight/bias float4s of this worker's slots are already in wr/br
 // (persistent CTAs whose workers see the same columns in every row).
-template <int OP, int K, bool PRE = false, class Map, class Red>
+template <int OP, int K, bool PRE = false, bool SP = false, class Map, class Red>
 __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, const RowGeom& g, float4 (&v)[K],
                                                 float hv, float tv, bool own_h, bool own_t, bool active, int wi,
                                                 const Map& map, Red& red, const float4 (&wr)[K],
-                                                const float4 (&br)[K]) {
+                                                const float4 (&br)[K], const SharedParams& sp = SharedParams{}) {
     float* yb = yr + g.head;
     const int ti = g.head + 4 * g.nvec + wi;  // column of this worker's tail scalar
     if constexpr (OP == OP_SOFTMAX) {
@@ -171,7 +191,7 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         if (own_t) yr[ti] = tv * inv;
     } else if constexpr (OP == OP_RMSNORM) {
         // short stripes fetch their weights now, so the load overlaps the merge
-        constexpr bool kFetchEarly = !PRE && K <= 4;
+        constexpr bool kFetchEarly = !PRE && !SP && K <= 4;
         const bool wv = a.has_w && aligned16(a.w + g.head);
         float4 wq[K];
         if constexpr (kFetchEarly) {
@@ -186,6 +206,7 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
             ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
         ss = red(ss);
         const float rstd = rsqrtf(fmaf(ss, a.inv_cols, a.eps));
+        if constexpr (SP) mbar_wait_bounded(sp.bar, 0, a.wait_ns, a.err);  // uniform: before any return
         if (!active) return;
 #pragma unroll
         for (int j = 0; j < K; ++j)
@@ -193,7 +214,8 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
                 const int e = 4 * map.idx(j);
                 float4 o = make_float4(v[j].x * rstd, v[j].y * rstd, v[j].z * rstd, v[j].w * rstd);
                 if (a.has_w) {
-                    const float4 wj = PRE ? wr[j] : kFetchEarly ? wq[j] : ld_param(a.w + g.head + e, wv);
+                    const float4 wj = SP ? ld_shared4(sp.w + e)
+                                      : PRE ? wr[j] : kFetchEarly ? wq[j] : ld_param(a.w + g.head + e, wv);
                     o.x *= wj.x; o.y *= wj.y; o.z *= wj.z; o.w *= wj.w;
                 }
                 st_out(yb + e, o, a.y_vec);
@@ -202,7 +224,7 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         if (own_t) yr[ti] = tv * rstd * (a.has_w ? __ldg(a.w + ti) : 1.0f);
     } else if constexpr (OP == OP_LAYERNORM) {
         // short stripes fetch their weights and biases now, overlapping the merges
-        constexpr bool kFetchEarly = !PRE && K <= 4;
+        constexpr bool kFetchEarly = !PRE && !SP && K <= 4;
         const bool wv = a.has_w && aligned16(a.w + g.head);
         const bool bv = a.has_b && aligned16(a.b + g.head);
         float4 wq[K], bq[K];
@@ -235,6 +257,7 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
         if (own_t) sq = fmaf(tv - mean, tv - mean, sq);
         sq = red(sq);
         const float rstd = rsqrtf(fmaf(sq, a.inv_cols, a.eps));
+        if constexpr (SP) mbar_wait_bounded(sp.bar, 0, a.wait_ns, a.err);  // uniform: before any return
         if (!active) return;
 #pragma unroll
         for (int j = 0; j < K; ++j)
@@ -243,11 +266,13 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
                 float4 o = make_float4((v[j].x - mean) * rstd, (v[j].y - mean) * rstd, (v[j].z - mean) * rstd,
                                        (v[j].w - mean) * rstd);
                 if (a.has_w) {
-                    const float4 wj = PRE ? wr[j] : kFetchEarly ? wq[j] : ld_param(a.w + g.head + e, wv);
+                    const float4 wj = SP ? ld_shared4(sp.w + e)
+                                      : PRE ? wr[j] : kFetchEarly ? wq[j] : ld_param(a.w + g.head + e, wv);
                     o.x *= wj.x; o.y *= wj.y; o.z *= wj.z; o.w *= wj.w;
                 }
                 if (a.has_b) {
-                    const float4 bj = PRE ? br[j] : kFetchEarly ? bq[j] : ld_param(a.b + g.head + e, bv);
+                    const float4 bj = SP ? ld_shared4(sp.b + e)
+                                      : PRE ? br[j] : kFetchEarly ? bq[j] : ld_param(a.b + g.head + e, bv);
                     o.x += bj.x; o.y += bj.y; o.z += bj.z; o.w += bj.w;
                 }
                 st_out(yb + e, o, a.y_vec);
@@ -271,9 +296,19 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
 // TR_PLAN_ROWS: G lanes per row inside a warp (G = 4, 8, 16), or S warps per
 // row (G = 32); Q rows per CTA; K float4 slots per worker.
 // ---------------------------------------------------------------------------
-template <int OP, int G, int K>
-__global__ void __launch_bounds__(max_threads_for<OP, K>()) rows_cached_kernel(const RowArgs a) {
+template <int OP, int G, int K, bool SP = false>
+__global__ void __launch_bounds__(max_threads_for<OP, K>(), min_blocks_for<K>()) rows_cached_kernel(const RowArgs a) {
     __shared__ float4 part[2][32];
+    extern __shared__ __align__(16) float sparams[];  // SP: weight (cols floats), then bias
+    __shared__ __align__(8) uint64_t pbar;
+    const SharedParams sp{sparams, sparams + (a.has_w ? a.cols : 0), &pbar};
+    if constexpr (SP) {
+        if (threadIdx.x == 0) {
+            mbar_init(&pbar, 1);
+            fence_barrier_init();
+        }
+        __syncthreads();
+    }
     RowPos p;
     p.lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -302,10 +337,20 @@ __global__ void __launch_bounds__(max_threads_for<OP, K>()) rows_cached_kernel(c
     float4 v[K];
     float hv, tv;
     pdl_enter();
+    if constexpr (SP) {
+        // the whole weight (and bias) vector, once per CTA, while the rows load
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(a.cols) * 4u;
+            mbar_arrive_expect_tx(&pbar, bytes * ((a.has_w ? 1u : 0u) + (a.has_b ? 1u : 0u)));
+            if (a.has_w) bulk_g2s(sparams, a.w, bytes, &pbar);
+            if (a.has_b) bulk_g2s(sparams + (a.has_w ? a.cols : 0), a.b, bytes, &pbar);
+        }
+    }
     load_stripe<OP, K>(xr, g, map, active, p.w, own_h, own_t, v, hv, tv);
     RowsReducer<G> red{p, part, 0};
     float4 none[K];
-    cached_epilogue<OP, K>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red, none, none);
+    cached_epilogue<OP, K, false, SP>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red, none,
+                                      none, sp);
 }
 
 // ---------------------------------------------------------------------------

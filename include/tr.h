@@ -97,12 +97,19 @@ typedef struct tr_plan {
     double est_us;           /* cost-model estimate in microseconds (a prior, not a measurement) */
     int32_t candidates;      /* legal candidates the selector ranked */
     int32_t flags;           /* TR_PLAN_FLAG_* */
+    int64_t resident_ctas;   /* CTAs of this plan the device holds at once (from the occupancy query) */
 } tr_plan;
 
 /* Staged norm plans: each worker keeps the weight (and bias) values of its
  * columns in registers for all the rows of its CTA. Requires 16-byte-aligned
  * rows (cols % 4 == 0, aligned x) and 16-byte-aligned weight/bias vectors. */
 #define TR_PLAN_FLAG_PARAMS_IN_REGISTERS 1
+/* Row plans (lanes_per_row 32) of the norms: the CTA copies the whole weight
+ * (and bias) vector into shared memory with bulk asynchronous copies issued
+ * when it starts, so the epilogue needs no dependent global load. Requires
+ * 16-byte-aligned rows and weight/bias vectors; uses cols * 4 bytes of shared
+ * memory per vector. */
+#define TR_PLAN_FLAG_PARAMS_IN_SHARED 2
 
 /* A device as the plan selector sees it (for host-only planning and tests). */
 typedef struct tr_device_desc {
@@ -198,6 +205,30 @@ tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows
  * tr_last_error_message(); nothing is launched. */
 tr_status tr_plan_check_for(const tr_device_desc* dev, tr_plan* plan, int64_t rows, int64_t cols,
                             int32_t align16);
+
+/* ---- cost-model calibration and audit (host side) ----------------------
+ * The model's constants, in this order: launch, latency, cta_barrier,
+ * cluster_barrier, l2_over_hbm, staged_row, one_wave_alu, wave, slot_pass,
+ * param_trip, clock_ghz, split_sync (microseconds unless stated). They are
+ * fixed in the library; these calls exist so that an offline calibration can
+ * score the model on measured plan sweeps ("Whole-launch reduction cost
+ * policy": measurement calibrates priors, never selects a plan). */
+#define TR_COST_CONSTANTS 12
+
+/* Copy the library's constants into out[0 .. n-1] (n must be TR_COST_CONSTANTS). */
+tr_status tr_plan_cost_constants(double* out, int32_t n);
+
+/* The model's estimate for a plan whose grid_ctas and ctas_per_sm are already
+ * filled (for example, as described on a device), with the given constants
+ * (NULL: the library's). No legality check; nothing is launched. */
+tr_status tr_plan_estimate_with(const tr_device_desc* dev, const tr_plan* plan, int64_t rows, int64_t cols,
+                                int32_t align16, const double* constants, double* out_us);
+
+/* Every legal candidate for these arguments on the current device (occupancy
+ * from the CUDA occupancy API), with its estimate: up to `cap` plans are
+ * written to out, and *count receives the number of legal candidates. */
+tr_status tr_plan_candidates(int32_t op, int64_t rows, int64_t cols, tr_order order, int32_t align16,
+                             tr_plan* out, int32_t cap, int32_t* count);
 
 /* Force the next calls of plan->op to use exactly this plan (kind,
  * lanes_per_row, warps_per_row, rows_per_cta, cluster_ctas, vec_slots,

@@ -116,13 +116,21 @@ def uniform_f32(shape, seed, tag, lo, hi, device="cpu") -> torch.Tensor:
 def normal_plus_row_offset_f32(rows, cols, seed, lo=-3.0, hi=3.0, device="cpu") -> torch.Tensor:
     """x[r, c] = N(0,1) + o_r with one o_r ~ U(lo, hi) per row, summed in float64, rounded once."""
     off = lo + (hi - lo) * uniform01(seed, TAG_ROW_OFFSET, rows, device)
-    out = torch.empty(rows * cols, dtype=torch.float32, device=device)
-    n = rows * cols
-    for s in range(0, n, _CHUNK):
-        c = min(_CHUNK, n - s)
-        r = torch.div(torch.arange(s, s + c, device=device), cols, rounding_mode="floor")
-        out[s:s + c] = (_std_normal_f64(seed, TAG_X, s, c, device) + off[r]).to(torch.float32)
-    return out.view(rows, cols)
+    out = torch.empty(rows, cols, dtype=torch.float32, device=device)
+    # whole rows per slice (a row longer than a slice is split): the offsets are
+    # broadcast from plain slices of `off`, no gather
+    rows_per = max(1, _CHUNK // cols)
+    for r0 in range(0, rows, rows_per):
+        r1 = min(rows, r0 + rows_per)
+        if r1 - r0 > 1 or cols <= _CHUNK:
+            z = _std_normal_f64(seed, TAG_X, r0 * cols, (r1 - r0) * cols, device).view(r1 - r0, cols)
+            out[r0:r1] = (z + off[r0:r1].view(-1, 1)).to(torch.float32)
+        else:
+            for c0 in range(0, cols, _CHUNK):
+                c = min(_CHUNK, cols - c0)
+                z = _std_normal_f64(seed, TAG_X, r0 * cols + c0, c, device)
+                out[r0, c0:c0 + c] = (z + off[r0:r0 + 1]).to(torch.float32)
+    return out
 
 
 def labels_i64(rows, classes, seed, device="cpu") -> torch.Tensor:

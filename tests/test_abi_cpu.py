@@ -45,8 +45,8 @@ def test_status_strings(lib):
 
 
 def test_plan_struct_layout_matches_header():
-    # int32 x 10, int64, double, int32 x 2 -> 64 bytes with natural alignment
-    assert ctypes.sizeof(trlib.tr_plan) == 64
+    # int32 x 10, int64, double, int32 x 2, int64 -> 72 bytes with natural alignment
+    assert ctypes.sizeof(trlib.tr_plan) == 72
     assert ctypes.sizeof(trlib.tr_device_desc) == 40
 
 

@@ -239,9 +239,10 @@ def legal_plans(op, rows, cols):
                 for q in (1, 2):
                     if 32 * s * q > 1024:
                         continue
-                    for k in ks:
-                        plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=s, rows_per_cta=q,
-                                          cluster_ctas=1, vec_slots=k, block_threads=32 * s * q))
+                    for k in ks + ([6] if kind == tr.TR_PLAN_ROWS else []):
+                        for flags in ((0, tr.TR_PLAN_FLAG_PARAMS_IN_SHARED) if kind == tr.TR_PLAN_ROWS else (0,)):
+                            plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=s, rows_per_cta=q,
+                                              cluster_ctas=1, vec_slots=k, block_threads=32 * s * q, flags=flags))
         elif kind == tr.TR_PLAN_STAGED:
             for t in (64, 256, 1024):
                 for nb in (1, 2, 5):

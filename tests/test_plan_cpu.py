@@ -60,8 +60,12 @@ def test_unordered_plans_are_legal_and_cover(op, rows, cols):
         assert 2 <= p.cluster_ctas <= 32 and p.vec_slots * p.block_threads * 16 <= 225 * 1024
     else:
         assert p.grid_ctas == rows * p.cluster_ctas
-    if p.flags:
+    if p.flags == trlib.TR_PLAN_FLAG_PARAMS_IN_REGISTERS:
         assert p.kind == trlib.TR_PLAN_STAGED and op in (1, 2) and cols % 4 == 0
+    elif p.flags == trlib.TR_PLAN_FLAG_PARAMS_IN_SHARED:
+        assert p.kind == trlib.TR_PLAN_ROWS and p.lanes_per_row == 32 and op in (1, 2) and cols % 4 == 0
+    else:
+        assert p.flags == 0
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
