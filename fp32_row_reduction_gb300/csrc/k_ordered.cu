@@ -216,10 +216,11 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             if (j >= nj) continue;
-            float o[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) o[v] = out(q[j][v], col(j, v));
+            // `out` may read the column's weight: evaluate it for columns inside the row only
             if (full(j)) {
+                float o[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) o[v] = out(q[j][v], col(j, v));
                 if (vec_out) {
                     st4(yr + col(j, 0), make_float4(o[0], o[1], o[2], o[3]));
                 } else {
@@ -229,7 +230,7 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
             } else {
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
-                    if (okc(j, v)) yr[col(j, v)] = o[v];
+                    if (okc(j, v)) yr[col(j, v)] = out(q[j][v], col(j, v));
             }
         }
     };
