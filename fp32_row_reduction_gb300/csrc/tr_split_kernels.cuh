@@ -336,15 +336,37 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
         for (int u = 0; u < kSplitU; ++u) st_out(yb + 4 * (i + u * T), params(out4(c[u]), i + u * T), a.y_vec);
     }
     for (; i < v1; i += T) st_out(yb + 4 * i, params(out4(ld_stream4(xb + 4 * i)), i), a.y_vec);
-    for (int j = t; j < nsm; j += T) {
-        const float4 c = cache[j];
-        float4 o;
-        if constexpr (OP == OP_SOFTMAX) {
-            o = make_float4(c.x * cscale, c.y * cscale, c.z * cscale, c.w * cscale);
-        } else {
-            o = out4(c);
+    if constexpr (OP == OP_SOFTMAX) {
+        for (int j = t; j < nsm; j += T) {
+            const float4 c = cache[j];
+            st_out(yb + 4 * (v0 + j), make_float4(c.x * cscale, c.y * cscale, c.z * cscale, c.w * cscale), a.y_vec);
         }
-        st_out(yb + 4 * (v0 + j), params(o, v0 + j), a.y_vec);
+    } else {
+        // kSplitU slots at a time, so that their weight/bias loads are in flight together
+        auto pload = [&](const float* p, int j, bool vec, float dflt) {
+            return p ? ld_param(p + g.head + 4 * j, vec) : f4(dflt);
+        };
+        const float* pw = a.has_w ? a.w : nullptr;
+        const float* pb = (OP == OP_LAYERNORM && a.has_b) ? a.b : nullptr;
+        int j = t;
+        for (; j + (kSplitU - 1) * T < nsm; j += kSplitU * T) {
+            float4 w4[kSplitU], b4[kSplitU];
+#pragma unroll
+            for (int u = 0; u < kSplitU; ++u) {
+                w4[u] = pload(pw, v0 + j + u * T, wv, 1.0f);
+                b4[u] = pload(pb, v0 + j + u * T, bv, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < kSplitU; ++u) {
+                float4 o = out4(cache[j + u * T]);
+                o.x = fmaf(o.x, w4[u].x, b4[u].x);
+                o.y = fmaf(o.y, w4[u].y, b4[u].y);
+                o.z = fmaf(o.z, w4[u].z, b4[u].z);
+                o.w = fmaf(o.w, w4[u].w, b4[u].w);
+                st_out(yb + 4 * (v0 + j + u * T), o, a.y_vec);
+            }
+        }
+        for (; j < nsm; j += T) st_out(yb + 4 * (v0 + j), params(out4(cache[j]), v0 + j), a.y_vec);
     }
     auto params1 = [&](float o, int col) -> float {
         if constexpr (OP != OP_SOFTMAX) {
