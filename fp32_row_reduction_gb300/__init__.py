@@ -46,6 +46,7 @@ TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_SPLIT = 7
 TR_PLAN_FLAG_PARAMS_IN_REGISTERS = 1
 TR_PLAN_FLAG_PARAMS_IN_SHARED = 2
+TR_PLAN_FLAG_TWO_ROWS = 4
 
 OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LAYERNORM,
        "cross_entropy": TR_OP_CROSS_ENTROPY}
@@ -205,14 +206,14 @@ def check_plan_for(dev: tr_device_desc, plan: tr_plan, rows, cols, align16=1):
 
 def cost_constants():
     """The library's cost-model constants (TR_COST_CONSTANTS doubles)."""
-    out = (ctypes.c_double * 12)()
-    _check(load().tr_plan_cost_constants(out, 12), "tr_plan_cost_constants")
+    out = (ctypes.c_double * 13)()
+    _check(load().tr_plan_cost_constants(out, 13), "tr_plan_cost_constants")
     return list(out)
 
 
 def estimate_with(dev: tr_device_desc, plan: tr_plan, rows, cols, align16=1, constants=None) -> float:
     """The model's estimate (us) for a plan with grid_ctas/ctas_per_sm filled, under given constants."""
-    c = None if constants is None else (ctypes.c_double * 12)(*constants)
+    c = None if constants is None else (ctypes.c_double * 13)(*constants)
     out = ctypes.c_double()
     _check(load().tr_plan_estimate_with(ctypes.byref(dev), ctypes.byref(plan), rows, cols, align16, c,
                                         ctypes.byref(out)), "tr_plan_estimate_with")

@@ -54,8 +54,29 @@ const void* rows_sp_table(int slots) {
     }
 }
 
+// Two rows per worker group in sequence (optionally with the weights in shared memory).
+template <int OP, bool SP>
+const void* rows_pair_table(int slots) {
+    if constexpr (SP && OP == OP_SOFTMAX) {
+        return nullptr;
+    } else {
+        switch (slots) {
+            case 2: return reinterpret_cast<const void*>(rows_pair_kernel<OP, 2, SP>);
+            case 4: return reinterpret_cast<const void*>(rows_pair_kernel<OP, 4, SP>);
+            case 6: return reinterpret_cast<const void*>(rows_pair_kernel<OP, 6, SP>);
+        }
+        return nullptr;
+    }
+}
+
 template <int OP>
 const void* unordered_table(int kind, int lanes, int slots, int flags) {
+    if (flags & TR_PLAN_FLAG_TWO_ROWS) {
+        if (kind != TR_PLAN_ROWS || lanes != 32) return nullptr;
+        if (flags == TR_PLAN_FLAG_TWO_ROWS) return rows_pair_table<OP, false>(slots);
+        if (flags == (TR_PLAN_FLAG_TWO_ROWS | TR_PLAN_FLAG_PARAMS_IN_SHARED)) return rows_pair_table<OP, true>(slots);
+        return nullptr;
+    }
     if (flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS)
         return kind == TR_PLAN_STAGED ? staged_pre_table<OP>(slots) : nullptr;
     if (flags & TR_PLAN_FLAG_PARAMS_IN_SHARED)

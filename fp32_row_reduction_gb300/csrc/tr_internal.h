@@ -84,6 +84,7 @@ inline const void* kernel_for(const tr_plan& p) {
 constexpr int kRowsSlotsSub[] = {1, 2, 4};           // lanes_per_row 4, 8, 16
 constexpr int kRowsSlotsWarp[] = {1, 2, 4, 6, 8, 16};  // lanes_per_row 32
 constexpr int kRowsSlotsShared[] = {2, 4, 6, 8};       // lanes_per_row 32, weights in shared memory
+constexpr int kRowsSlotsPair[] = {2, 4, 6};            // lanes_per_row 32, two rows per group
 constexpr int kClusterSlots[] = {4, 8, 16};
 constexpr int kStagedSlots[] = {1, 2, 4, 8};
 constexpr int kOrderedSlots[] = {0, 1, 2, 4, 6, 8, 12, 16}; // 0: re-read plan

@@ -57,6 +57,7 @@ int max_threads_for_slots(int op, int kind, int k, int flags) {
     if (kind == TR_PLAN_STAGED && (flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS))
         return k <= 2 ? 1024 : k == 4 ? 768 : (op == TR_OP_LAYERNORM ? 384 : 512);
     if (kind == TR_PLAN_STAGED) return (k >= 8 || (k >= 4 && op == TR_OP_LAYERNORM)) ? 768 : 1024;
+    if (kind == TR_PLAN_ROWS && (flags & TR_PLAN_FLAG_TWO_ROWS)) return k == 6 ? 256 : 512;
     if (kind == TR_PLAN_ROWS && k == 6) return 768;
     if (kind == TR_PLAN_ROWS || kind == TR_PLAN_CLUSTER)
         return k >= 16 ? 512 : (k >= 4 && op == TR_OP_LAYERNORM) ? 768 : 1024;
@@ -79,24 +80,25 @@ int reductions_of(int op) {
 // Fitted by coordinate descent (calibration/fit_cost_model.py) on GB300 plan
 // sweeps of calibration shapes DISJOINT from the benchmark workloads (the
 // shape lists are in calibration/sweep.py, the sweeps beside it), minimising
-// the mean time regret of the chosen plan (with the tie-break below): 7.0%
-// mean, 29% max over 57 cases. The benchmark shapes were then scored as a
+// the mean time regret of the chosen plan (with the tie-break below): 7.3%
+// mean, 28% max over 57 cases. The benchmark shapes were then scored as a
 // held-out set with the constants frozen (the page's frozen held-out
-// protocol): 6.2% mean, 28% max over 25 cases. The clock is the datasheet
+// protocol): 6.3% mean, 25% max over 25 cases. The clock is the datasheet
 // value.
 const CostConstants kCostDefaults = {
     0.375,  // launch: launch and grid ramp beyond what the other terms cover
     3.3,    // latency: loaded DRAM round trip as seen by a CTA
-    0.4,    // cta_barrier: one shared-memory merge round
+    0.528,  // cta_barrier: one shared-memory merge round
     0.84,   // cluster_barrier: one cluster merge round
     1.32,   // l2_over_hbm: L2 re-read bandwidth relative to HBM
     1.44,   // staged_row: fixed cost of one row of a staged CTA
     0.5,    // one_wave_alu: share of arithmetic exposed in a single wave
-    0.6,    // wave: extra cost of each further wave
+    0.15,   // wave: extra cost of each further wave
     0.06,   // slot_pass: serial per-thread work, per cached slot and pass
     0.8,    // param_trip: dependent L2 trip for the norms' weights (per vector)
     1.9,    // clock_ghz
     1.5,    // split_sync: publish, count and read back a split row's partials
+    0.4,    // pair_overlap: share of the write phase hidden by two rows per group
 };
 
 tr_device_desc gb300_desc() {
@@ -170,15 +172,21 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
         return fail(TR_ERR_UNSUPPORTED, "cross-entropy is realised only by the streaming XENT plan");
     const int T = p->block_threads;
     if (T < 32 || T > 1024 || T % 32) return fail(TR_ERR_UNSUPPORTED, "block_threads must be a multiple of 32 in [32, 1024]");
-    if (p->flags & ~(TR_PLAN_FLAG_PARAMS_IN_REGISTERS | TR_PLAN_FLAG_PARAMS_IN_SHARED))
+    if (p->flags & ~(TR_PLAN_FLAG_PARAMS_IN_REGISTERS | TR_PLAN_FLAG_PARAMS_IN_SHARED | TR_PLAN_FLAG_TWO_ROWS))
         return fail(TR_ERR_INVALID_ARG, "unknown plan flags");
+    if (p->flags & TR_PLAN_FLAG_TWO_ROWS) {
+        if (p->kind != TR_PLAN_ROWS || p->lanes_per_row != 32 || !in(kRowsSlotsPair, p->vec_slots))
+            return fail(TR_ERR_UNSUPPORTED, "two rows per group is a warp-row plan with vec_slots 2, 4 or 6");
+        if (p->block_threads > 512) return fail(TR_ERR_UNSUPPORTED, "two rows per group runs at most 512 threads");
+    }
     if ((p->flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS) && (p->flags & TR_PLAN_FLAG_PARAMS_IN_SHARED))
         return fail(TR_ERR_INVALID_ARG, "weights go to registers or to shared memory, not both");
     if (p->flags & TR_PLAN_FLAG_PARAMS_IN_SHARED) {
         if (p->kind != TR_PLAN_ROWS || p->lanes_per_row != 32 || (p->op != TR_OP_RMSNORM && p->op != TR_OP_LAYERNORM))
             return fail(TR_ERR_UNSUPPORTED, "weights in shared memory is a warp-row plan of the norms");
         if (!align16) return fail(TR_ERR_UNSUPPORTED, "weights in shared memory needs 16-byte-aligned rows and weights");
-        if (!in(kRowsSlotsShared, p->vec_slots)) return fail(TR_ERR_UNSUPPORTED, "no such kernel with that vec_slots");
+        if (!in(kRowsSlotsShared, p->vec_slots) && !(p->flags & TR_PLAN_FLAG_TWO_ROWS))
+            return fail(TR_ERR_UNSUPPORTED, "no such kernel with that vec_slots");
         if (cols * 4 * (p->op == TR_OP_LAYERNORM ? 2 : 1) > kStagedSmemBudget)
             return fail(TR_ERR_UNSUPPORTED, "the weights do not fit in shared memory");
     }
@@ -222,7 +230,7 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
                 if (static_cast<int64_t>(W) * k < n4)
                     return fail(TR_ERR_UNSUPPORTED, "the row does not fit the workers' register stripes");
             }
-            p->grid_ctas = ceil_div(rows, p->rows_per_cta);
+            p->grid_ctas = ceil_div(rows, p->rows_per_cta * ((p->flags & TR_PLAN_FLAG_TWO_ROWS) ? 2 : 1));
             break;
         }
         case TR_PLAN_CLUSTER:
@@ -301,7 +309,8 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const double kLaunchUs = c.launch, kLatencyUs = c.latency, kCtaBarrierUs = c.cta_barrier,
                  kClusterBarrierUs = c.cluster_barrier, kL2OverHbm = c.l2_over_hbm, kStagedRowUs = c.staged_row,
                  kOneWaveAluFactor = c.one_wave_alu, kWaveUs = c.wave, kSlotPassUs = c.slot_pass,
-                 kParamTripUs = c.param_trip, kClockGhz = c.clock_ghz, kSplitSyncUs = c.split_sync;
+                 kParamTripUs = c.param_trip, kClockGhz = c.clock_ghz, kSplitSyncUs = c.split_sync,
+                 kPairOverlap = c.pair_overlap;
     (void)align16;
     const double E = static_cast<double>(rows) * static_cast<double>(cols);
     const double bw = d.hbm_gbs * 1e3;  // bytes per microsecond
@@ -387,11 +396,12 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
                ptrip + write_bytes / bw + t_over + t_l2;
     }
 
+    const int rows_seq = (p.flags & TR_PLAN_FLAG_TWO_ROWS) ? 2 : 1;  // rows a worker group handles in sequence
     double inflight_thread;  // bytes a thread can have in flight at once
     int rounds;              // dependent memory round trips in a CTA's life
     switch (p.kind) {
         case TR_PLAN_ROWS:
-        case TR_PLAN_CLUSTER: inflight_thread = 16.0 * p.vec_slots; rounds = 1; break;
+        case TR_PLAN_CLUSTER: inflight_thread = 16.0 * p.vec_slots * rows_seq; rounds = 1; break;
         case TR_PLAN_ORDERED:
             inflight_thread = 16.0 * std::max(1, p.vec_slots);
             rounds = p.vec_slots > 0 ? 1 : 1 + reductions_of(op);
@@ -401,12 +411,17 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     }
     const double read_cta = read_bytes / grid;
     const double inflight_cta = std::max(16.0, std::min(T * inflight_thread, read_cta));
+    // a group's rows in sequence: their merges and epilogues add up
+    const double serial = rows_seq * (red * sync + kchain + ptrip);
     if (grid <= slots) {
         // a single wave: every CTA reads, then reduces and computes, then
-        // writes, in lockstep, so the phases add up instead of overlapping
+        // writes, in lockstep, so the phases add up instead of overlapping;
+        // with two rows per group, part of the first rows' writes overlaps the
+        // second rows' reads
         const double per_cta_bw = std::min(bw / grid, inflight_cta / kLatencyUs);
         const double t_read = std::max(rounds * kLatencyUs, read_cta / per_cta_bw);
-        return kLaunchUs + t_read + kOneWaveAluFactor * t_alu + red * sync + kchain + ptrip + write_bytes / bw + t_l2;
+        const double t_write = write_bytes / bw * (rows_seq > 1 ? 1.0 - kPairOverlap : 1.0);
+        return kLaunchUs + t_read + kOneWaveAluFactor * t_alu + serial + t_write + t_l2;
     }
     // several waves: CTAs drift out of phase and reads overlap writes and
     // arithmetic. Waves count continuously (the page's service-policy prior): the
@@ -414,7 +429,7 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const double waves = grid / slots;
     const double bw_full = std::min(bw, slots * inflight_cta / kLatencyUs);
     const double t_mem = hbm_bytes / bw_full + rounds * kLatencyUs + t_l2;
-    return kLaunchUs + std::max(t_mem, t_alu) + waves * (red * sync + kchain + ptrip) + (waves - 1.0) * kWaveUs;
+    return kLaunchUs + std::max(t_mem, t_alu) + waves * serial + (waves - 1.0) * kWaveUs;
 }
 
 void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op, int64_t rows, int64_t cols,
@@ -492,9 +507,19 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
                     p.vec_slots = k;
                     cands.push_back(p);
                     // norms on aligned rows: the same plan with the weights staged in shared memory
-                    if (align16 && (op == TR_OP_RMSNORM || op == TR_OP_LAYERNORM) && in(kRowsSlotsShared, k)) {
+                    const bool norm = op == TR_OP_RMSNORM || op == TR_OP_LAYERNORM;
+                    if (align16 && norm && in(kRowsSlotsShared, k)) {
                         p.flags = TR_PLAN_FLAG_PARAMS_IN_SHARED;
                         cands.push_back(p);
+                    }
+                    // two rows per group in sequence (the legality check bounds the threads)
+                    if (!xent && in(kRowsSlotsPair, k)) {
+                        p.flags = TR_PLAN_FLAG_TWO_ROWS;
+                        cands.push_back(p);
+                        if (align16 && norm) {
+                            p.flags = TR_PLAN_FLAG_TWO_ROWS | TR_PLAN_FLAG_PARAMS_IN_SHARED;
+                            cands.push_back(p);
+                        }
                     }
                 }
         }

@@ -353,6 +353,72 @@ __global__ void __launch_bounds__(max_threads_for<OP, K>(), min_blocks_for<K>())
                                       none, sp);
 }
 
+// Two rows per worker group, in sequence (TR_PLAN_FLAG_TWO_ROWS): the stripes of
+// both rows are loaded first, so the second row's loads are still landing while
+// the first row is reduced and written. Across the device, the writes of first
+// rows overlap the reads of second rows, instead of every CTA reading, then
+// merging, then writing in lockstep. Group q of the CTA owns rows 2g and 2g + 1,
+// g = blockIdx.x * (groups per CTA) + q. Warp rows only (G == 32).
+// K = 6 (rows of up to 6144 columns at 256 threads): three CTAs, six rows per SM.
+template <int K>
+constexpr int pair_max_threads() {
+    return K == 6 ? 256 : 512;
+}
+template <int K>
+constexpr int pair_min_blocks() {
+    return K == 6 ? 3 : 2;
+}
+
+template <int OP, int K, bool SP = false>
+__global__ void __launch_bounds__(pair_max_threads<K>(), pair_min_blocks<K>()) rows_pair_kernel(const RowArgs a) {
+    __shared__ float4 part[2][32];
+    extern __shared__ __align__(16) float sparams[];  // SP: weight (cols floats), then bias
+    __shared__ __align__(8) uint64_t pbar;
+    const SharedParams sp{sparams, sparams + (a.has_w ? a.cols : 0), &pbar};
+    if constexpr (SP) {
+        if (threadIdx.x == 0) {
+            mbar_init(&pbar, 1);
+            fence_barrier_init();
+        }
+        __syncthreads();
+    }
+    RowPos p;
+    p.lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    p.S = a.S;
+    p.W = 32 * a.S;
+    p.s = warp % a.S;
+    p.q = warp / a.S;
+    p.w = p.s * 32 + p.lane;
+    const int64_t row0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / p.W) + p.q) * 2;
+    const bool act0 = row0 < a.rows, act1 = row0 + 1 < a.rows;
+    const int64_t r0 = act0 ? row0 : a.rows - 1, r1 = act1 ? row0 + 1 : a.rows - 1;
+    const float* x0 = a.x + r0 * a.cols;
+    const float* x1 = a.x + r1 * a.cols;
+    const RowGeom g0 = row_geom(x0, a.cols), g1 = row_geom(x1, a.cols);
+    const SlotMapRows m0{p.W, p.w, g0.nvec}, m1{p.W, p.w, g1.nvec};
+    const bool h0 = p.w < g0.head, t0 = p.w < g0.tail, h1 = p.w < g1.head, t1 = p.w < g1.tail;
+    float4 v0[K], v1[K];
+    float hv0, tv0, hv1, tv1;
+    pdl_enter();
+    if constexpr (SP) {
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(a.cols) * 4u;
+            mbar_arrive_expect_tx(&pbar, bytes * ((a.has_w ? 1u : 0u) + (a.has_b ? 1u : 0u)));
+            if (a.has_w) bulk_g2s(sparams, a.w, bytes, &pbar);
+            if (a.has_b) bulk_g2s(sparams + (a.has_w ? a.cols : 0), a.b, bytes, &pbar);
+        }
+    }
+    load_stripe<OP, K>(x0, g0, m0, act0, p.w, h0, t0, v0, hv0, tv0);
+    load_stripe<OP, K>(x1, g1, m1, act1, p.w, h1, t1, v1, hv1, tv1);
+    RowsReducer<32> red{p, part, 0};
+    float4 none[K];
+    cached_epilogue<OP, K, false, SP>(a, a.y + r0 * a.cols, g0, v0, hv0, tv0, h0, t0, act0, p.w, m0, red, none,
+                                      none, sp);
+    cached_epilogue<OP, K, false, SP>(a, a.y + r1 * a.cols, g1, v1, hv1, tv1, h1, t1, act1, p.w, m1, red, none,
+                                      none, sp);
+}
+
 // ---------------------------------------------------------------------------
 // TR_PLAN_CLUSTER: a row per cluster of C CTAs (launched with a cluster
 // dimension of C). CTA rank c owns the body slots [c*seg, (c+1)*seg).

@@ -110,6 +110,10 @@ typedef struct tr_plan {
  * 16-byte-aligned rows and weight/bias vectors; uses cols * 4 bytes of shared
  * memory per vector. */
 #define TR_PLAN_FLAG_PARAMS_IN_SHARED 2
+/* Warp-row plans (lanes_per_row 32, vec_slots 2, 4 or 6): each of the CTA's
+ * rows_per_cta worker groups handles two consecutive rows in sequence, loading
+ * both before reducing the first (the CTA covers 2 * rows_per_cta rows). */
+#define TR_PLAN_FLAG_TWO_ROWS 4
 
 /* A device as the plan selector sees it (for host-only planning and tests). */
 typedef struct tr_device_desc {
@@ -209,11 +213,11 @@ tr_status tr_plan_check_for(const tr_device_desc* dev, tr_plan* plan, int64_t ro
 /* ---- cost-model calibration and audit (host side) ----------------------
  * The model's constants, in this order: launch, latency, cta_barrier,
  * cluster_barrier, l2_over_hbm, staged_row, one_wave_alu, wave, slot_pass,
- * param_trip, clock_ghz, split_sync (microseconds unless stated). They are
+ * param_trip, clock_ghz, split_sync, pair_overlap (microseconds unless stated). They are
  * fixed in the library; these calls exist so that an offline calibration can
  * score the model on measured plan sweeps ("Whole-launch reduction cost
  * policy": measurement calibrates priors, never selects a plan). */
-#define TR_COST_CONSTANTS 12
+#define TR_COST_CONSTANTS 13
 
 /* Copy the library's constants into out[0 .. n-1] (n must be TR_COST_CONSTANTS). */
 tr_status tr_plan_cost_constants(double* out, int32_t n);

@@ -240,7 +240,13 @@ def legal_plans(op, rows, cols):
                     if 32 * s * q > 1024:
                         continue
                     for k in ks + ([6] if kind == tr.TR_PLAN_ROWS else []):
-                        for flags in ((0, tr.TR_PLAN_FLAG_PARAMS_IN_SHARED) if kind == tr.TR_PLAN_ROWS else (0,)):
+                        fl = (0,)
+                        if kind == tr.TR_PLAN_ROWS:
+                            fl = (0, tr.TR_PLAN_FLAG_PARAMS_IN_SHARED)
+                            if k in (2, 4, 6):
+                                fl += (tr.TR_PLAN_FLAG_TWO_ROWS,
+                                       tr.TR_PLAN_FLAG_TWO_ROWS | tr.TR_PLAN_FLAG_PARAMS_IN_SHARED)
+                        for flags in fl:
                             plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=s, rows_per_cta=q,
                                               cluster_ctas=1, vec_slots=k, block_threads=32 * s * q, flags=flags))
         elif kind == tr.TR_PLAN_STAGED:

@@ -52,7 +52,8 @@ def test_unordered_plans_are_legal_and_cover(op, rows, cols):
     assert p.block_threads % 32 == 0 and 32 <= p.block_threads <= 1024
     assert p.candidates >= 1 and p.est_us > 0 and p.ctas_per_sm >= 1
     if p.kind == trlib.TR_PLAN_ROWS:
-        assert p.grid_ctas == math.ceil(rows / p.rows_per_cta)
+        pair = 2 if p.flags & trlib.TR_PLAN_FLAG_TWO_ROWS else 1
+        assert p.grid_ctas == math.ceil(rows / (p.rows_per_cta * pair))
     elif p.kind == trlib.TR_PLAN_STAGED:
         assert p.grid_ctas == min(rows, p.ctas_per_sm * DEV.sm_count)  # persistent CTAs
     elif p.kind == trlib.TR_PLAN_SPLIT:
@@ -62,10 +63,12 @@ def test_unordered_plans_are_legal_and_cover(op, rows, cols):
         assert p.grid_ctas == rows * p.cluster_ctas
     if p.flags == trlib.TR_PLAN_FLAG_PARAMS_IN_REGISTERS:
         assert p.kind == trlib.TR_PLAN_STAGED and op in (1, 2) and cols % 4 == 0
-    elif p.flags == trlib.TR_PLAN_FLAG_PARAMS_IN_SHARED:
-        assert p.kind == trlib.TR_PLAN_ROWS and p.lanes_per_row == 32 and op in (1, 2) and cols % 4 == 0
     else:
-        assert p.flags == 0
+        if p.flags & trlib.TR_PLAN_FLAG_PARAMS_IN_SHARED:
+            assert p.kind == trlib.TR_PLAN_ROWS and p.lanes_per_row == 32 and op in (1, 2) and cols % 4 == 0
+        if p.flags & trlib.TR_PLAN_FLAG_TWO_ROWS:
+            assert p.kind == trlib.TR_PLAN_ROWS and p.lanes_per_row == 32 and p.vec_slots in (2, 4, 6)
+        assert p.flags & ~(trlib.TR_PLAN_FLAG_PARAMS_IN_SHARED | trlib.TR_PLAN_FLAG_TWO_ROWS) == 0
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
@@ -115,8 +118,9 @@ def test_short_rows_never_split_or_stage():
 
 
 def test_params_in_registers_only_when_aligned():
+    staged = trlib.TR_PLAN_FLAG_PARAMS_IN_REGISTERS | trlib.TR_PLAN_FLAG_PARAMS_IN_SHARED
     for op in (1, 2):
-        assert select(op, 768, 6144, align=0).flags == 0
+        assert select(op, 768, 6144, align=0).flags & staged == 0
 
 
 def test_long_rows_split_across_ctas():
