@@ -59,7 +59,9 @@ def alg_bytes(op, rows, cols):
     """Algorithmic bytes of one launch: every input read once, every output written once."""
     e = rows * cols
     return {"softmax": 8 * e, "rmsnorm": 8 * e + 4 * cols, "layernorm": 8 * e + 8 * cols,
-            "cross_entropy": 4 * e + 12 * rows}[op]
+            "cross_entropy": 4 * e + 12 * rows,
+            # fused residual norms: x and r read, y and h = x + r written
+            "add_rmsnorm": 16 * e + 4 * cols, "add_layernorm": 16 * e + 8 * cols}[op]
 
 
 def kernel_source_hash():
@@ -161,11 +163,14 @@ class Launch:
             self.outputs = [torch.empty(self.rows, device=device) for _ in range(sets)]
         else:
             self.outputs = [torch.empty_like(base["x"]) for _ in range(sets)]
+        # fused residual norms also write h = x + r
+        self.h = [torch.empty_like(base["x"]) for _ in range(sets)] if op.startswith("add_") else None
         self.bytes = alg_bytes(op, self.rows, self.cols)
         self.key = f"{op}/{self.order}/{self.rows}x{self.cols}"
 
     def __call__(self, s, stream=None):
-        self.tr.run_op(self.op, self.inputs[s], out=self.outputs[s], order=self.order, stream=stream)
+        self.tr.run_op(self.op, self.inputs[s], out=self.outputs[s], order=self.order, stream=stream,
+                       h_out=None if self.h is None else self.h[s])
 
     def plan(self):
         return self.tr.plan_for(self.op, self.rows, self.cols, self.order)
@@ -382,11 +387,15 @@ def oracle_fn(op, order):
         return {"softmax": lambda h: oracle.ot_softmax(h["x"]),
                 "rmsnorm": lambda h: oracle.ot_rmsnorm(h["x"], h["w"], 1e-5),
                 "layernorm": lambda h: oracle.ot_layernorm(h["x"], h["w"], h["b"], 1e-5),
-                "cross_entropy": lambda h: oracle.ot_cross_entropy(h["x"], h["labels"])}[op]
+                "cross_entropy": lambda h: oracle.ot_cross_entropy(h["x"], h["labels"]),
+                "add_rmsnorm": lambda h: oracle.ot_add_rmsnorm(h["x"], h["r"], h["w"], 1e-5),
+                "add_layernorm": lambda h: oracle.ot_add_layernorm(h["x"], h["r"], h["w"], h["b"], 1e-5)}[op]
     return {"softmax": lambda h: oracle.softmax(h["x"]),
             "rmsnorm": lambda h: oracle.rmsnorm(h["x"], h["w"], 1e-5),
             "layernorm": lambda h: oracle.layernorm(h["x"], h["w"], h["b"], 1e-5),
-            "cross_entropy": lambda h: oracle.cross_entropy(h["x"], h["labels"])}[op]
+            "cross_entropy": lambda h: oracle.cross_entropy(h["x"], h["labels"]),
+            "add_rmsnorm": lambda h: oracle.add_rmsnorm(h["x"], h["r"], h["w"], 1e-5),
+            "add_layernorm": lambda h: oracle.add_layernorm(h["x"], h["r"], h["w"], h["b"], 1e-5)}[op]
 
 
 def host_sample(op, workload, rows):

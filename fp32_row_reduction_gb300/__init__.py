@@ -44,12 +44,14 @@ TR_PLAN_ORDERED = 4
 TR_PLAN_STAGED = 5
 TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_SPLIT = 7
+TR_OP_ADD_RMSNORM = 4
+TR_OP_ADD_LAYERNORM = 5
 TR_PLAN_FLAG_PARAMS_IN_REGISTERS = 1
 TR_PLAN_FLAG_PARAMS_IN_SHARED = 2
 TR_PLAN_FLAG_TWO_ROWS = 4
 
 OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LAYERNORM,
-       "cross_entropy": TR_OP_CROSS_ENTROPY}
+       "cross_entropy": TR_OP_CROSS_ENTROPY, "add_rmsnorm": TR_OP_ADD_RMSNORM, "add_layernorm": TR_OP_ADD_LAYERNORM}
 ORDERS = {"unordered": TR_ORDER_UNORDERED_TREE, "ordered": TR_ORDER_ORDERED_TREE}
 
 
@@ -93,6 +95,8 @@ SIGNATURES = {
     "tr_rmsnorm_f32": ([_P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
     "tr_layernorm_f32": ([_P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
     "tr_cross_entropy_f32": ([_P, _P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_add_rmsnorm_f32": ([_P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
+    "tr_add_layernorm_f32": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
     "tr_plan_describe": ([_I32, _I64, _I64, _I32, ctypes.POINTER(tr_plan)], _I32),
     "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
                             ctypes.POINTER(tr_plan)], _I32),
@@ -317,6 +321,52 @@ def layernorm(x, weight=None, bias=None, eps=1e-5, out=None, order="unordered", 
     return y
 
 
+def tr_add_rmsnorm_f32(x, r, w, y, h, rows, cols, eps, order, stream):
+    return load().tr_add_rmsnorm_f32(x, r, w, y, h, rows, cols, eps, order, stream)
+
+
+def tr_add_layernorm_f32(x, r, gamma, beta, y, h, rows, cols, eps, order, stream):
+    return load().tr_add_layernorm_f32(x, r, gamma, beta, y, h, rows, cols, eps, order, stream)
+
+
+def add_rmsnorm(x, residual, weight=None, eps=1e-5, out=None, h_out=None, order="unordered", stream=None):
+    """y = RMSNorm(x + residual); h_out (optional) receives x + residual."""
+    import torch
+    _check_matrix(x, "x")
+    _check_matrix(residual, "residual")
+    r, c = x.shape
+    wp = _check_vector(weight, "weight", c)
+    y = torch.empty_like(x) if out is None else out
+    _check_matrix(y, "out")
+    hp = None
+    if h_out is not None:
+        _check_matrix(h_out, "h_out")
+        hp = h_out.data_ptr()
+    _check(tr_add_rmsnorm_f32(x.data_ptr(), residual.data_ptr(), wp, y.data_ptr(), hp, r, c, eps, _order(order),
+                              _stream_handle(stream)), "add_rmsnorm")
+    return y
+
+
+def add_layernorm(x, residual, weight=None, bias=None, eps=1e-5, out=None, h_out=None, order="unordered",
+                  stream=None):
+    """y = LayerNorm(x + residual); h_out (optional) receives x + residual."""
+    import torch
+    _check_matrix(x, "x")
+    _check_matrix(residual, "residual")
+    r, c = x.shape
+    wp = _check_vector(weight, "weight", c)
+    bp = _check_vector(bias, "bias", c)
+    y = torch.empty_like(x) if out is None else out
+    _check_matrix(y, "out")
+    hp = None
+    if h_out is not None:
+        _check_matrix(h_out, "h_out")
+        hp = h_out.data_ptr()
+    _check(tr_add_layernorm_f32(x.data_ptr(), residual.data_ptr(), wp, bp, y.data_ptr(), hp, r, c, eps,
+                                _order(order), _stream_handle(stream)), "add_layernorm")
+    return y
+
+
 def cross_entropy(logits, labels, out=None, order="unordered", stream=None):
     """Per-row loss log(sum exp(x)) - x[label] (label outside [0, cols) selects 0)."""
     import torch
@@ -335,7 +385,7 @@ def plan_for(op, rows, cols, order="unordered") -> dict:
     return tr_plan_describe(OPS[op] if isinstance(op, str) else op, rows, cols, _order(order)).as_dict()
 
 
-def run_op(op, inputs, out=None, order="unordered", eps=1e-5, stream=None):
+def run_op(op, inputs, out=None, order="unordered", eps=1e-5, stream=None, h_out=None):
     """Dispatch one operator on a dict of inputs (keys as produced by ``synth``)."""
     if op == "softmax":
         return softmax(inputs["x"], out=out, order=order, stream=stream)
@@ -343,6 +393,12 @@ def run_op(op, inputs, out=None, order="unordered", eps=1e-5, stream=None):
         return rmsnorm(inputs["x"], inputs.get("w"), eps, out=out, order=order, stream=stream)
     if op == "layernorm":
         return layernorm(inputs["x"], inputs.get("w"), inputs.get("b"), eps, out=out, order=order, stream=stream)
+    if op == "add_rmsnorm":
+        return add_rmsnorm(inputs["x"], inputs["r"], inputs.get("w"), eps, out=out, h_out=h_out, order=order,
+                           stream=stream)
+    if op == "add_layernorm":
+        return add_layernorm(inputs["x"], inputs["r"], inputs.get("w"), inputs.get("b"), eps, out=out, h_out=h_out,
+                             order=order, stream=stream)
     if op == "cross_entropy":
         return cross_entropy(inputs["x"], inputs["labels"], out=out, order=order, stream=stream)
     raise ValueError(f"unknown op {op!r}")

@@ -29,12 +29,19 @@ PLAN_KEYS = ["op", "order", "kind", "lanes_per_row", "warps_per_row", "rows_per_
 
 
 def load(path):
+    """Sweep records, keeping the plans the library's current legality rules
+    accept (occupancy aside: the sweep recorded the device's own)."""
     cases = collections.defaultdict(list)
+    dev = tr.gb300_device_desc()
     opener = gzip.open if path.endswith(".gz") else open
     with opener(path, "rt") as f:
         for line in f:
             r = json.loads(line)
             p = tr.tr_plan(**{k: r["plan"][k] for k in PLAN_KEYS})
+            q = tr.tr_plan(**{k: r["plan"][k] for k in PLAN_KEYS})
+            st, why = tr.check_plan_for(dev, q, r["rows"], r["cols"], 1)
+            if st != tr.TR_OK and "resident" not in why:
+                continue
             cases[(r["op"], r["rows"], r["cols"])].append((r["us"], p))
     return cases
 

@@ -27,31 +27,34 @@ CALIBRATION = {
              (8, 131072), (32, 32768), (2000, 1000), (200, 3000), (12, 500000), (1200, 4096), (600, 8192),
              (4, 1000000), (64, 65536), (1536, 3072), (160, 6144)],
     "cross_entropy": [(1024, 32000), (256, 128000), (8192, 8192)],
+    "residual": [(512, 4096), (1200, 4096), (300, 5000), (2048, 2048), (100, 20000), (32768, 64)],
 }
 # The benchmark workloads, scored only after the fit (held out).
 HELDOUT = {
     "rows": [(37, 1537), (256, 3072), (64, 12289), (768, 6144), (16, 65536), (16, 262144), (16, 1048576),
              (65536, 128)],
     "cross_entropy": [(4096, 50257)],
+    "residual": [(768, 6144)],
 }
 L2_BYTES = 126 << 20
 GUARD = 4096          # floats of guard band on each side of an output
 SENTINEL = -12345.0
 
 
-def time_plan(op, ins, outs, plan, est_us):
+def time_plan(op, ins, outs, plan, est_us, hs=None):
     tr.tr_plan_override(plan)
     s = torch.cuda.Stream()
     sets = len(ins)
+    h = (lambda i: None) if hs is None else (lambda i: hs[i % sets])
     with torch.cuda.stream(s):
         for i in range(3):
-            tr.run_op(op, ins[i % sets], out=outs[i % sets], stream=s)
+            tr.run_op(op, ins[i % sets], out=outs[i % sets], stream=s, h_out=h(i))
     torch.cuda.synchronize()
     n = int(min(100, max(5, 300.0 / max(est_us, 1.0))))
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for i in range(n):
-            tr.run_op(op, ins[i % sets], out=outs[i % sets], stream=s)
+            tr.run_op(op, ins[i % sets], out=outs[i % sets], stream=s, h_out=h(i))
     g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -69,7 +72,7 @@ def sweep(op, rows, cols, out):
     dev = torch.device("cuda:0")
     base = synth.make_inputs(op, rows, cols, 11, var=4.0 if op == "softmax" else None,
                              row_offset=op in ("rmsnorm", "layernorm"), device=dev)
-    per_set = 8 * rows * cols
+    per_set = (16 if op.startswith("add_") else 8) * rows * cols
     sets = max(2, math.ceil(2 * L2_BYTES / per_set))
     ins = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(sets - 1)]
     shape = (rows,) if op == "cross_entropy" else (rows, cols)
@@ -79,13 +82,14 @@ def sweep(op, rows, cols, out):
     bigs = [torch.full((n_out + 2 * GUARD,), SENTINEL, device=dev) for _ in range(sets)]
     outs = [b[GUARD:GUARD + n_out].view(shape) for b in bigs]
     want = tr.run_op(op, ins[0]).clone()
+    hs = [torch.empty(shape, device=dev) for _ in range(sets)] if op.startswith("add_") else None
     tol = 1e-4 * float(want.abs().max()) + 1e-6
     cands = tr.plan_candidates(tr.OPS[op], rows, cols, 0, 1)
     default = tr.tr_plan_describe(tr.OPS[op], rows, cols, 0).as_dict()
     for p in cands:
         d = p.as_dict()
         try:
-            us = time_plan(op, ins, outs, p, d["est_us"])
+            us = time_plan(op, ins, outs, p, d["est_us"], hs)
         except tr.TrError as e:
             print(json.dumps({"op": op, "rows": rows, "cols": cols, "error": str(e)[:160], "plan": d}), file=sys.stderr)
             continue
@@ -119,6 +123,10 @@ def main():
     for rows, cols in shapes["cross_entropy"]:
         print(f"cross_entropy {rows}x{cols}", file=sys.stderr, flush=True)
         sweep("cross_entropy", rows, cols, out)
+    for op in ("add_rmsnorm", "add_layernorm"):
+        for rows, cols in shapes["residual"]:
+            print(f"{op} {rows}x{cols}", file=sys.stderr, flush=True)
+            sweep(op, rows, cols, out)
     if out is not sys.stdout:
         out.close()
 

@@ -309,7 +309,9 @@ constexpr int ot_min_blocks() {
     return K >= 1 && K <= 6 ? 6 : (K == 8 ? 5 : 1);
 }
 
-template <int OP, int K>
+// RES (fused residual norms, K > 0): h = x + r by one IEEE add per element
+// before the tree; h is written at once when requested.
+template <int OP, int K, bool RES = false>
 __global__ void __launch_bounds__(kOrderedThreads, ot_min_blocks<K>()) ot_kernel(const RowArgs a) {
     __shared__ float gpart[2][8];
     int buf = 0;
@@ -328,6 +330,21 @@ __global__ void __launch_bounds__(kOrderedThreads, ot_min_blocks<K>()) ot_kernel
                 load_quad(xr, cols, j, aligned, q[j], ok);
             } else {
                 q[j][0] = q[j][1] = q[j][2] = q[j][3] = 0.0f;
+            }
+        }
+        if constexpr (RES) {
+            const float* rr = a.r + row * cols;
+            const bool raligned = aligned16(rr);
+            float* hr = a.h ? a.h + row * cols : nullptr;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                if (j >= nj) continue;
+                float rq[4];
+                bool ok[4];
+                load_quad(rr, cols, j, raligned, rq, ok);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) q[j][v] = __fadd_rn(q[j][v], rq[v]);
+                if (hr) store_quad(hr, cols, j, aligned && a.h_vec, q[j], ok);
             }
         }
         ot_cached_row<OP, K>(a, row, q, aligned && a.y_vec, gpart, buf);
@@ -522,6 +539,27 @@ const void* kernel_ordered_staged(int op, int slots) {
         case TR_OP_CROSS_ENTROPY: { TR_OTS_CASES(OP_XENT) }
     }
 #undef TR_OTS_CASES
+    return nullptr;
+}
+
+// Fused residual norms (op TR_OP_ADD_RMSNORM / TR_OP_ADD_LAYERNORM): cached plans only.
+const void* kernel_ordered_residual(int op, int slots) {
+#define TR_OTR_CASES(OPV)                                                            \
+    switch (slots) {                                                                 \
+        case 1: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 1, true>);   \
+        case 2: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 2, true>);   \
+        case 4: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 4, true>);   \
+        case 6: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 6, true>);   \
+        case 8: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 8, true>);   \
+        case 12: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 12, true>); \
+        case 16: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 16, true>); \
+    }                                                                                \
+    return nullptr;
+    switch (op) {
+        case TR_OP_ADD_RMSNORM: { TR_OTR_CASES(OP_RMSNORM) }
+        case TR_OP_ADD_LAYERNORM: { TR_OTR_CASES(OP_LAYERNORM) }
+    }
+#undef TR_OTR_CASES
     return nullptr;
 }
 

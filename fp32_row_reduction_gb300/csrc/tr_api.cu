@@ -52,8 +52,9 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
-bool g_override_set[4] = {false, false, false, false};
-tr_plan g_override[4];
+constexpr int kOps = TR_OP_ADD_LAYERNORM + 1;
+bool g_override_set[kOps] = {};
+tr_plan g_override[kOps];
 int g_debug_flags = 0;
 // Launch with programmatic stream serialization (dependent launches overlap
 // their launch latency with the previous kernel's tail); TR_DISABLE_PDL=1 turns it off.
@@ -417,9 +418,54 @@ tr_status tr_cross_entropy_f32(const float* logits, const int64_t* labels, float
     return run(c, stream);
 }
 
+// Fused residual norms: validation common to both, then the norm's own fields.
+static tr_status residual_call(int op, const float* x, const float* residual, const float* w, const float* b,
+                               float* y, float* h, int64_t rows, int64_t cols, float eps, tr_order order,
+                               cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    s = validate_eps(eps);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!x || !residual || !y) return fail(TR_ERR_INVALID_ARG, "x, residual and y must not be null");
+    if (misaligned(x, 4) || misaligned(residual, 4) || misaligned(y, 4) || misaligned(h, 4) || misaligned(w, 4) ||
+        misaligned(b, 4))
+        return fail(TR_ERR_INVALID_ARG, "x, residual, y, h, w and b must be 4-byte aligned");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    const size_t nv = static_cast<size_t>(cols) * 4;
+    const bool bad = overlaps(x, n, y, n) || overlaps(residual, n, y, n) || overlaps(w, nv, y, n) ||
+                     overlaps(b, nv, y, n) || overlaps(h, n, x, n) || overlaps(h, n, residual, n) ||
+                     overlaps(h, n, y, n) || overlaps(h, n, w, nv) || overlaps(h, n, b, nv);
+    if (bad) return fail(TR_ERR_INVALID_ARG, "an output overlaps an input or the other output");
+    Call c{op, blank_args(x, rows, cols), order};
+    c.a.y = y;
+    c.a.w = w;
+    c.a.b = b;
+    c.a.has_w = w != nullptr;
+    c.a.has_b = b != nullptr;
+    c.a.eps = eps;
+    c.a.r = residual;
+    c.a.h = h;
+    c.a.y_vec = ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+    c.a.r_vec = ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(residual)) & 15u) == 0;
+    c.a.h_vec = h && ((reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(h)) & 15u) == 0;
+    return run(c, stream);
+}
+
+tr_status tr_add_rmsnorm_f32(const float* x, const float* residual, const float* w, float* y, float* h,
+                             int64_t rows, int64_t cols, float eps, tr_order order, cudaStream_t stream) {
+    return residual_call(TR_OP_ADD_RMSNORM, x, residual, w, nullptr, y, h, rows, cols, eps, order, stream);
+}
+
+tr_status tr_add_layernorm_f32(const float* x, const float* residual, const float* gamma, const float* beta,
+                               float* y, float* h, int64_t rows, int64_t cols, float eps, tr_order order,
+                               cudaStream_t stream) {
+    return residual_call(TR_OP_ADD_LAYERNORM, x, residual, gamma, beta, y, h, rows, cols, eps, order, stream);
+}
+
 tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order order, tr_plan* out) {
     if (!out) return fail(TR_ERR_INVALID_ARG, "out must not be null");
-    if (op < TR_OP_SOFTMAX || op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
     if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1 to describe a plan");
@@ -450,7 +496,7 @@ tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order orde
 tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows, int64_t cols, tr_order order,
                              int32_t align16, tr_plan* out) {
     if (!dev || !out) return fail(TR_ERR_INVALID_ARG, "dev and out must not be null");
-    if (op < TR_OP_SOFTMAX || op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
     if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1 to select a plan");
@@ -495,7 +541,7 @@ tr_status tr_plan_estimate_with(const tr_device_desc* dev, const tr_plan* plan, 
 tr_status tr_plan_candidates(int32_t op, int64_t rows, int64_t cols, tr_order order, int32_t align16, tr_plan* out,
                              int32_t cap, int32_t* count) {
     if (!count || (cap > 0 && !out)) return fail(TR_ERR_INVALID_ARG, "count (and out when cap > 0) must not be null");
-    if (op < TR_OP_SOFTMAX || op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
     if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1");
@@ -520,7 +566,7 @@ tr_status tr_plan_override(const tr_plan* plan) {
         for (bool& b : g_override_set) b = false;
         return TR_OK;
     }
-    if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
     if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_SPLIT)
         return fail(TR_ERR_INVALID_ARG, "bad plan kind");
     g_override[plan->op] = *plan;

@@ -5,18 +5,18 @@
 
 namespace tr {
 
-template <int OP, int G>
+template <int OP, int G, bool RES = false>
 const void* rows_table(int slots) {
     switch (slots) {
-        case 1: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 1>);
-        case 2: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 2>);
-        case 4: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 4>);
+        case 1: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 1, false, RES>);
+        case 2: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 2, false, RES>);
+        case 4: return reinterpret_cast<const void*>(rows_cached_kernel<OP, G, 4, false, RES>);
     }
     if constexpr (G == 32) {
         switch (slots) {
-            case 6: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 6>);
-            case 8: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 8>);
-            case 16: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 16>);
+            case 6: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 6, false, RES>);
+            case 8: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 8, false, RES>);
+            case 16: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 16, false, RES>);
         }
     }
     return nullptr;
@@ -62,7 +62,11 @@ const void* rows_pair_table(int slots) {
     } else {
         switch (slots) {
             case 2: return reinterpret_cast<const void*>(rows_pair_kernel<OP, 2, SP>);
-            case 4: return reinterpret_cast<const void*>(rows_pair_kernel<OP, 4, SP>);
+            case 4:
+                // norms with global weights fetch them early for K <= 4: two rows of
+                // that spill, so only the shared-memory-weight form is built
+                if constexpr (OP != OP_SOFTMAX && !SP) return nullptr;
+                else return reinterpret_cast<const void*>(rows_pair_kernel<OP, 4, SP>);
             case 6: return reinterpret_cast<const void*>(rows_pair_kernel<OP, 6, SP>);
         }
         return nullptr;
@@ -108,6 +112,41 @@ const void* unordered_table(int kind, int lanes, int slots, int flags) {
                 case 2: return reinterpret_cast<const void*>(staged_kernel<OP, 2, false>);
                 case 4: return reinterpret_cast<const void*>(staged_kernel<OP, 4, false>);
                 case 8: return reinterpret_cast<const void*>(staged_kernel<OP, 8, false>);
+            }
+            return nullptr;
+    }
+    return nullptr;
+}
+
+// Fused residual norms (y = norm(x + r), h = x + r): the cached row and
+// cluster plans, with the weights in shared memory for aligned warp rows.
+template <int OP>
+const void* residual_table(int kind, int lanes, int slots, int flags) {
+    if (kind == TR_PLAN_ROWS && flags == TR_PLAN_FLAG_PARAMS_IN_SHARED) {
+        if (lanes != 32) return nullptr;
+        switch (slots) {
+            case 2: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 2, true, true>);
+            case 4: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 4, true, true>);
+            case 6: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 6, true, true>);
+            case 8: return reinterpret_cast<const void*>(rows_cached_kernel<OP, 32, 8, true, true>);
+        }
+        return nullptr;
+    }
+    if (flags) return nullptr;
+    switch (kind) {
+        case TR_PLAN_ROWS:
+            switch (lanes) {
+                case 4: return rows_table<OP, 4, true>(slots);
+                case 8: return rows_table<OP, 8, true>(slots);
+                case 16: return rows_table<OP, 16, true>(slots);
+                case 32: return rows_table<OP, 32, true>(slots);
+            }
+            return nullptr;
+        case TR_PLAN_CLUSTER:
+            switch (slots) {
+                case 4: return reinterpret_cast<const void*>(cluster_cached_kernel<OP, 4, true>);
+                case 8: return reinterpret_cast<const void*>(cluster_cached_kernel<OP, 8, true>);
+                case 16: return reinterpret_cast<const void*>(cluster_cached_kernel<OP, 16, true>);
             }
             return nullptr;
     }

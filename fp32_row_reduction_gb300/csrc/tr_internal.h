@@ -35,6 +35,10 @@ struct RowArgs {
     float4* sp_part;       // split plans: per (row, segment) partial statistic, rows * C entries
     unsigned* sp_arrive;   // split plans: per-row arrival counters (zero between launches)
     unsigned* sp_depart;   // split plans: per-row departure counters (zero between launches)
+    const float* r;        // fused residual norms: the residual added to x before the norm
+    float* h;              // fused residual norms: x + r written out (null: not written)
+    int r_vec;             // r rows have the same 16-byte phase as x rows
+    int h_vec;             // h rows have the same 16-byte phase as x rows
 };
 
 constexpr int kDebugForceTimeout = 1;
@@ -64,11 +68,19 @@ const void* kernel_rmsnorm(int kind, int lanes, int slots, int flags);
 const void* kernel_layernorm(int kind, int lanes, int slots, int flags);
 const void* kernel_xent(int kind, int lanes, int slots, int flags);
 const void* kernel_ordered(int op, int slots);
+const void* kernel_ordered_residual(int op, int slots);
+const void* kernel_add_rmsnorm(int kind, int lanes, int slots, int flags);
+const void* kernel_add_layernorm(int kind, int lanes, int slots, int flags);
 const void* kernel_ordered_staged(int op, int slots);
 // Dynamic shared memory a plan's kernel needs (0 for all but staged plans).
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols);
 
 inline const void* kernel_for(const tr_plan& p) {
+    if (p.op == TR_OP_ADD_RMSNORM || p.op == TR_OP_ADD_LAYERNORM) {
+        if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered_residual(p.op, p.vec_slots);
+        return p.op == TR_OP_ADD_RMSNORM ? kernel_add_rmsnorm(p.kind, p.lanes_per_row, p.vec_slots, p.flags)
+                                         : kernel_add_layernorm(p.kind, p.lanes_per_row, p.vec_slots, p.flags);
+    }
     if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
     if (p.kind == TR_PLAN_ORDERED_STAGED) return p.flags ? nullptr : kernel_ordered_staged(p.op, p.vec_slots);
     switch (p.op) {

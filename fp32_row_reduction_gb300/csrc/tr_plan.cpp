@@ -65,6 +65,12 @@ int max_threads_for_slots(int op, int kind, int k, int flags) {
     return 1024;
 }
 
+// The fused residual norms plan like their base norm (on cached plans only).
+int base_op(int op) {
+    return op == TR_OP_ADD_RMSNORM ? TR_OP_RMSNORM : op == TR_OP_ADD_LAYERNORM ? TR_OP_LAYERNORM : op;
+}
+bool residual_op(int op) { return op == TR_OP_ADD_RMSNORM || op == TR_OP_ADD_LAYERNORM; }
+
 int reductions_of(int op) {
     switch (op) {
         case TR_OP_SOFTMAX: return 2;
@@ -80,10 +86,10 @@ int reductions_of(int op) {
 // Fitted by coordinate descent (calibration/fit_cost_model.py) on GB300 plan
 // sweeps of calibration shapes DISJOINT from the benchmark workloads (the
 // shape lists are in calibration/sweep.py, the sweeps beside it), minimising
-// the mean time regret of the chosen plan (with the tie-break below): 7.3%
-// mean, 28% max over 57 cases. The benchmark shapes were then scored as a
+// the mean time regret of the chosen plan (with the tie-break below): 7.1%
+// mean, 30% max over 69 cases. The benchmark shapes were then scored as a
 // held-out set with the constants frozen (the page's frozen held-out
-// protocol): 6.3% mean, 25% max over 25 cases. The clock is the datasheet
+// protocol): 6.5% mean, 24% max over 27 cases. The clock is the datasheet
 // value.
 const CostConstants kCostDefaults = {
     0.375,  // launch: launch and grid ramp beyond what the other terms cover
@@ -118,7 +124,7 @@ tr_device_desc gb300_desc() {
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols) {
     if (p.kind == TR_PLAN_SPLIT) return static_cast<size_t>(p.vec_slots) * p.block_threads * 16;
     if (p.kind == TR_PLAN_ROWS && (p.flags & TR_PLAN_FLAG_PARAMS_IN_SHARED))
-        return static_cast<size_t>(cols) * 4 * (p.op == TR_OP_LAYERNORM ? 2 : 1);
+        return static_cast<size_t>(cols) * 4 * (base_op(p.op) == TR_OP_LAYERNORM ? 2 : 1);
     if (p.kind != TR_PLAN_STAGED && p.kind != TR_PLAN_ORDERED_STAGED) return 0;
     return static_cast<size_t>(p.rows_per_cta) * staged_slot_floats(cols) * sizeof(float);
 }
@@ -132,7 +138,7 @@ int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem) {
         case TR_PLAN_ROWS:
         case TR_PLAN_CLUSTER:
         case TR_PLAN_STAGED:
-            regs = (p.kind == TR_PLAN_ROWS && k == 6) ? 40 : 28 + 4 * k + (p.op == TR_OP_LAYERNORM ? 4 : 0);
+            regs = (p.kind == TR_PLAN_ROWS && k == 6) ? 40 : 28 + 4 * k + (base_op(p.op) == TR_OP_LAYERNORM ? 4 : 0);
             break;
         case TR_PLAN_ORDERED_STAGED: regs = 40 + 4 * k; break;
         case TR_PLAN_STREAM: regs = 64; break;
@@ -163,7 +169,19 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     const bool ordered = p->order == TR_ORDER_ORDERED_TREE;
     const bool xent = p->op == TR_OP_CROSS_ENTROPY;
     if (p->order != TR_ORDER_UNORDERED_TREE && !ordered) return fail(TR_ERR_INVALID_ARG, "bad order");
-    if (p->op < TR_OP_SOFTMAX || p->op > TR_OP_CROSS_ENTROPY) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (p->op < TR_OP_SOFTMAX || p->op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
+    const int bop = base_op(p->op);
+    if (residual_op(p->op)) {
+        const bool ok = (p->kind == TR_PLAN_ROWS && (p->flags & ~TR_PLAN_FLAG_PARAMS_IN_SHARED) == 0) ||
+                        (p->kind == TR_PLAN_CLUSTER && p->flags == 0) ||
+                        (p->kind == TR_PLAN_ORDERED && p->flags == 0 && p->vec_slots > 0);
+        if (!ok) return fail(TR_ERR_UNSUPPORTED, "fused residual norms run on cached row, cluster and cached ordered plans");
+        // two materialized stripes per worker (the combined row x + r and the
+        // row being normalised), 4K scalars each: the page's stripe budget of 64
+        // scalars per worker ("TIRx Metal reduction lowering" §5.1) bounds K by 8
+        if (p->kind != TR_PLAN_ORDERED && p->vec_slots > 8)
+            return fail(TR_ERR_UNSUPPORTED, "fused residual stripes exceed 64 scalars per worker (K > 8)");
+    }
     const bool ot_kind = p->kind == TR_PLAN_ORDERED || p->kind == TR_PLAN_ORDERED_STAGED;
     if (ordered != ot_kind)
         return fail(TR_ERR_UNSUPPORTED, "the ordered policy is realised only by the OT-1024 plans");
@@ -182,16 +200,16 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     if ((p->flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS) && (p->flags & TR_PLAN_FLAG_PARAMS_IN_SHARED))
         return fail(TR_ERR_INVALID_ARG, "weights go to registers or to shared memory, not both");
     if (p->flags & TR_PLAN_FLAG_PARAMS_IN_SHARED) {
-        if (p->kind != TR_PLAN_ROWS || p->lanes_per_row != 32 || (p->op != TR_OP_RMSNORM && p->op != TR_OP_LAYERNORM))
+        if (p->kind != TR_PLAN_ROWS || p->lanes_per_row != 32 || (bop != TR_OP_RMSNORM && bop != TR_OP_LAYERNORM))
             return fail(TR_ERR_UNSUPPORTED, "weights in shared memory is a warp-row plan of the norms");
         if (!align16) return fail(TR_ERR_UNSUPPORTED, "weights in shared memory needs 16-byte-aligned rows and weights");
         if (!in(kRowsSlotsShared, p->vec_slots) && !(p->flags & TR_PLAN_FLAG_TWO_ROWS))
             return fail(TR_ERR_UNSUPPORTED, "no such kernel with that vec_slots");
-        if (cols * 4 * (p->op == TR_OP_LAYERNORM ? 2 : 1) > kStagedSmemBudget)
+        if (cols * 4 * (bop == TR_OP_LAYERNORM ? 2 : 1) > kStagedSmemBudget)
             return fail(TR_ERR_UNSUPPORTED, "the weights do not fit in shared memory");
     }
     if (p->flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS) {
-        if (p->kind != TR_PLAN_STAGED || (p->op != TR_OP_RMSNORM && p->op != TR_OP_LAYERNORM))
+        if (p->kind != TR_PLAN_STAGED || (bop != TR_OP_RMSNORM && bop != TR_OP_LAYERNORM))
             return fail(TR_ERR_UNSUPPORTED, "weights in registers is a staged norm plan");
         if (!align16) return fail(TR_ERR_UNSUPPORTED, "weights in registers needs 16-byte-aligned rows and weights");
     }
@@ -290,7 +308,9 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
         }
         default: return fail(TR_ERR_UNSUPPORTED, "unknown plan kind");
     }
-    if (T > max_threads_for_slots(p->op, p->kind, k, p->flags)) return fail(TR_ERR_UNSUPPORTED, "too many threads for that vec_slots");
+    if (residual_op(p->op) && p->kind != TR_PLAN_ORDERED && T > (k >= 16 ? 256 : k >= 4 ? 512 : 1024))
+        return fail(TR_ERR_UNSUPPORTED, "too many threads for a fused residual kernel with that vec_slots");
+    if (T > max_threads_for_slots(bop, p->kind, k, p->flags)) return fail(TR_ERR_UNSUPPORTED, "too many threads for that vec_slots");
     if (p->grid_ctas > 0x7fffffffLL) return fail(TR_ERR_UNSUPPORTED, "grid too large");
     const size_t smem = plan_dynamic_smem(*p, cols);
     const int64_t res = occ ? occ(*p, smem) : static_cast<int64_t>(model_occupancy(d, *p, smem)) * d.sm_count;
@@ -314,7 +334,7 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     (void)align16;
     const double E = static_cast<double>(rows) * static_cast<double>(cols);
     const double bw = d.hbm_gbs * 1e3;  // bytes per microsecond
-    const int op = p.op;
+    const int op = base_op(p.op);
     double alg;
     switch (op) {
         case TR_OP_SOFTMAX: alg = 8.0 * E; break;
@@ -322,6 +342,7 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
         case TR_OP_LAYERNORM: alg = 8.0 * E + 8.0 * cols; break;
         default: alg = 4.0 * E + 12.0 * rows; break;
     }
+    if (residual_op(p.op)) alg += 8.0 * E;  // the residual read and h written
     // re-reads: served by L2 when the input fits comfortably, else by HBM
     double reread = 0.0;
     if (p.kind == TR_PLAN_STREAM) reread = 4.0 * E;
@@ -409,7 +430,9 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
         case TR_PLAN_STREAM: inflight_thread = 16.0 * kStreamChunk; rounds = 2; break;
         default: inflight_thread = 16.0 * p.vec_slots; rounds = 1; break;
     }
-    const double read_cta = read_bytes / grid;
+    // fused residual norms keep both stripes (x and the residual) in flight
+    if (residual_op(p.op)) inflight_thread *= 2.0;
+    const double read_cta = (residual_op(p.op) ? 2.0 : 1.0) * read_bytes / grid;
     const double inflight_cta = std::max(16.0, std::min(T * inflight_thread, read_cta));
     // a group's rows in sequence: their merges and epilogues add up
     const double serial = rows_seq * (red * sync + kchain + ptrip);
@@ -435,6 +458,8 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
 void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op, int64_t rows, int64_t cols,
                      int32_t order, bool align16, std::vector<tr_plan>* legal) {
     std::vector<tr_plan> cands;
+    const bool res = residual_op(op);  // fused residual norms: cached plans only
+    const int bop = base_op(op);
     auto base = [&](int kind) {
         tr_plan p;
         std::memset(&p, 0, sizeof p);
@@ -454,7 +479,7 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
         p.block_threads = kOrderedThreads;
         const int k = smallest_covering(kOrderedSlots, ceil_div(cols, 1024));
         p.vec_slots = k < 0 ? 0 : k;
-        cands.push_back(p);
+        if (!res || p.vec_slots > 0) cands.push_back(p);
         // the staged OT-1024 realisation (TR_PLAN_ORDERED_STAGED) stays available by
         // override; measured plan sweeps found the one-shot realisation at full
         // occupancy as fast or faster, so it is not an automatic candidate
@@ -507,13 +532,13 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
                     p.vec_slots = k;
                     cands.push_back(p);
                     // norms on aligned rows: the same plan with the weights staged in shared memory
-                    const bool norm = op == TR_OP_RMSNORM || op == TR_OP_LAYERNORM;
+                    const bool norm = bop == TR_OP_RMSNORM || bop == TR_OP_LAYERNORM;
                     if (align16 && norm && in(kRowsSlotsShared, k)) {
                         p.flags = TR_PLAN_FLAG_PARAMS_IN_SHARED;
                         cands.push_back(p);
                     }
                     // two rows per group in sequence (the legality check bounds the threads)
-                    if (!xent && in(kRowsSlotsPair, k)) {
+                    if (!xent && !res && in(kRowsSlotsPair, k)) {
                         p.flags = TR_PLAN_FLAG_TWO_ROWS;
                         cands.push_back(p);
                         if (align16 && norm) {
@@ -534,7 +559,7 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
                 // across its rows (norms, aligned rows); otherwise one-shot plans win
                 for (int nb = 1; nb <= max_ring; ++nb)
                     for (int flags : {TR_PLAN_FLAG_PARAMS_IN_REGISTERS}) {
-                        if (op == TR_OP_SOFTMAX || !align16) continue;
+                        if (bop == TR_OP_SOFTMAX || !align16 || res) continue;
                         tr_plan p = base(TR_PLAN_STAGED);
                         p.lanes_per_row = 32;
                         p.warps_per_row = T / 32;

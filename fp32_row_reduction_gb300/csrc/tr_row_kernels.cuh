@@ -38,6 +38,16 @@ template <int K>
 constexpr int min_blocks_for() {
     return K == 6 ? 2 : 1;
 }
+// Fused residual variants hold the residual's stripe in flight beside x's
+// (2K float4 at the peak): half the threads of a plain kernel for K >= 4.
+template <int OP, int K, bool RES>
+constexpr int max_threads_res() {
+    return !RES ? max_threads_for<OP, K>() : K >= 16 ? 256 : K >= 4 ? 512 : 1024;
+}
+template <int K, bool RES>
+constexpr int min_blocks_res() {
+    return RES ? 1 : min_blocks_for<K>();
+}
 
 // Staged kernels that also hold K float4 of weights (and of biases) per worker.
 template <int OP, int K, bool PRE>
@@ -126,6 +136,51 @@ __device__ __forceinline__ void load_stripe(const float* xr, const RowGeom& g, c
     tv = id;
     if (active && own_h) hv = ld_stream1(xr + wi);
     if (active && own_t) tv = ld_stream1(xb + 4 * g.nvec + wi);
+}
+
+// Fused residual norms: add the residual's stripe to the loaded x stripe
+// (h = x + r, one rounded add per element, the residual read with 16-byte
+// loads when its rows have x's 16-byte phase) and, when h is requested, write
+// h at once: it does not depend on the row statistics, so the stores overlap
+// the merges. Padding slots keep the identity.
+template <int K, class Map>
+__device__ __forceinline__ void add_residual(const RowArgs& a, int64_t row, const RowGeom& g, const Map& map,
+                                             bool active, int wi, bool own_h, bool own_t, float4 (&v)[K],
+                                             float& hv, float& tv) {
+    const float* rr = a.r + row * a.cols;
+    const float* rb = rr + g.head;
+    float4 rq[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        rq[j] = f4(0.0f);
+        if (active && map.ok(j)) {
+            const float* p = rb + 4 * map.idx(j);
+            rq[j] = a.r_vec ? ld_stream4(p) : make_float4(ld_stream1(p), ld_stream1(p + 1), ld_stream1(p + 2),
+                                                          ld_stream1(p + 3));
+        }
+    }
+    float rh = 0.0f, rt = 0.0f;
+    if (active && own_h) rh = ld_stream1(rr + wi);
+    if (active && own_t) rt = ld_stream1(rb + 4 * g.nvec + wi);
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+        if (active && map.ok(j)) {
+            v[j].x += rq[j].x;
+            v[j].y += rq[j].y;
+            v[j].z += rq[j].z;
+            v[j].w += rq[j].w;
+        }
+    if (active && own_h) hv += rh;
+    if (active && own_t) tv += rt;
+    if (a.h && active) {
+        float* hr = a.h + row * a.cols;
+        float* hb = hr + g.head;
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+            if (map.ok(j)) st_out(hb + 4 * map.idx(j), v[j], a.h_vec);
+        if (own_h) hr[wi] = hv;
+        if (own_t) hb[4 * g.nvec + wi] = tv;
+    }
 }
 
 // Norm weights and biases staged in shared memory (rows plans with
@@ -296,8 +351,9 @@ __device__ __forceinline__ void cached_epilogue(const RowArgs& a, float* yr, con
 // TR_PLAN_ROWS: G lanes per row inside a warp (G = 4, 8, 16), or S warps per
 // row (G = 32); Q rows per CTA; K float4 slots per worker.
 // ---------------------------------------------------------------------------
-template <int OP, int G, int K, bool SP = false>
-__global__ void __launch_bounds__(max_threads_for<OP, K>(), min_blocks_for<K>()) rows_cached_kernel(const RowArgs a) {
+template <int OP, int G, int K, bool SP = false, bool RES = false>
+__global__ void __launch_bounds__(max_threads_res<OP, K, RES>(), min_blocks_res<K, RES>())
+    rows_cached_kernel(const RowArgs a) {
     __shared__ float4 part[2][32];
     extern __shared__ __align__(16) float sparams[];  // SP: weight (cols floats), then bias
     __shared__ __align__(8) uint64_t pbar;
@@ -347,6 +403,7 @@ __global__ void __launch_bounds__(max_threads_for<OP, K>(), min_blocks_for<K>())
         }
     }
     load_stripe<OP, K>(xr, g, map, active, p.w, own_h, own_t, v, hv, tv);
+    if constexpr (RES) add_residual<K>(a, rr, g, map, active, p.w, own_h, own_t, v, hv, tv);
     RowsReducer<G> red{p, part, 0};
     float4 none[K];
     cached_epilogue<OP, K, false, SP>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red, none,
@@ -423,8 +480,8 @@ __global__ void __launch_bounds__(pair_max_threads<K>(), pair_min_blocks<K>()) r
 // TR_PLAN_CLUSTER: a row per cluster of C CTAs (launched with a cluster
 // dimension of C). CTA rank c owns the body slots [c*seg, (c+1)*seg).
 // ---------------------------------------------------------------------------
-template <int OP, int K>
-__global__ void __launch_bounds__(max_threads_for<OP, K>()) cluster_cached_kernel(const RowArgs a) {
+template <int OP, int K, bool RES = false>
+__global__ void __launch_bounds__(max_threads_res<OP, K, RES>()) cluster_cached_kernel(const RowArgs a) {
     __shared__ float4 part[2][32];
     __shared__ float4 cpart[2];
     cg::cluster_group cl = cg::this_cluster();
@@ -450,6 +507,7 @@ __global__ void __launch_bounds__(max_threads_for<OP, K>()) cluster_cached_kerne
     float hv, tv;
     pdl_enter();
     load_stripe<OP, K>(xr, g, map, true, t, own_h, own_t, v, hv, tv);
+    if constexpr (RES) add_residual<K>(a, row, g, map, true, t, own_h, own_t, v, hv, tv);
     ClusterReducer red{p, part, 0, cpart, 0, C};
     float4 none[K];
     cached_epilogue<OP, K>(a, a.y + row * a.cols, g, v, hv, tv, own_h, own_t, true, t, map, red, none, none);

@@ -62,7 +62,9 @@ typedef enum tr_op {
     TR_OP_SOFTMAX = 0,
     TR_OP_RMSNORM = 1,
     TR_OP_LAYERNORM = 2,
-    TR_OP_CROSS_ENTROPY = 3
+    TR_OP_CROSS_ENTROPY = 3,
+    TR_OP_ADD_RMSNORM = 4,   /* fused residual: y = RMSNorm(x + r) (tr_add_rmsnorm_f32) */
+    TR_OP_ADD_LAYERNORM = 5  /* fused residual: y = LayerNorm(x + r) (tr_add_layernorm_f32) */
 } tr_op;
 
 /* How a row is mapped onto the GPU (the build's counterpart of the page's
@@ -153,6 +155,25 @@ tr_status tr_layernorm_f32(const float* x, const float* gamma, const float* beta
  * logits: rows x cols; labels: rows int64; losses: rows floats. */
 tr_status tr_cross_entropy_f32(const float* logits, const int64_t* labels, float* losses,
                                int64_t rows, int64_t cols, tr_order order, cudaStream_t stream);
+
+/* ---- fused residual norms ----------------------------------------------
+ * "TIRx Metal reduction lowering" §5.1 (Shared SSA is not a physical
+ * allocation decision): LayerNorm over combined = X + residual, where the
+ * combined row is kept as a worker stripe so that each input element is
+ * loaded once. With gamma = beta = NULL and h = NULL this is the page's
+ * example exactly. h = x + residual (one rounded FP32 add per
+ * element), y = RMSNorm(h) or LayerNorm(h) exactly as tr_rmsnorm_f32 /
+ * tr_layernorm_f32 define them on h, and h is written to `h` unless it is NULL
+ * (the updated residual stream). x, residual, y, h: rows x cols; w / gamma /
+ * beta: cols or NULL. No output may overlap an input or the other output.
+ * Runs on the cached row, cluster and cached ordered plans: rows longer than
+ * a cluster's register stripes (unordered) or 16384 columns (ordered) return
+ * TR_ERR_UNSUPPORTED. */
+tr_status tr_add_rmsnorm_f32(const float* x, const float* residual, const float* w, float* y, float* h,
+                             int64_t rows, int64_t cols, float eps, tr_order order, cudaStream_t stream);
+tr_status tr_add_layernorm_f32(const float* x, const float* residual, const float* gamma, const float* beta,
+                               float* y, float* h, int64_t rows, int64_t cols, float eps, tr_order order,
+                               cudaStream_t stream);
 
 /* ---- no-allocation entry point ----------------------------------------- */
 

@@ -137,6 +137,37 @@ def cross_entropy(logits, labels):
 
 # --- OT-1024 emulation -----------------------------------------------------
 
+def residual_sum(x, r):
+    """h = x + r for the fused residual norms: one IEEE binary32 addition per
+    element ("TIRx Metal reduction lowering" §5.1: combined = X + residual),
+    numpy's float32 add (round to nearest even)."""
+    return (_f32(x) + _f32(r)).astype(np.float32)
+
+
+def add_rmsnorm(x, r, w=None, eps=1e-5):
+    """RMSNorm of the FP32 row h = x + r (FP64 definition applied to h); returns (y, h)."""
+    h = residual_sum(x, r)
+    return rmsnorm(h, w, eps), h
+
+
+def add_layernorm(x, r, gamma=None, beta=None, eps=1e-5):
+    """LayerNorm of the FP32 row h = x + r (FP64 definition applied to h); returns (y, h)."""
+    h = residual_sum(x, r)
+    return layernorm(h, gamma, beta, eps), h
+
+
+def ot_add_rmsnorm(x, r, w=None, eps=1e-5):
+    """Ordered-policy emulation of the fused residual RMSNorm: OT-1024 on h = x + r."""
+    h = residual_sum(x, r)
+    return ot_rmsnorm(h, w, eps), h
+
+
+def ot_add_layernorm(x, r, gamma=None, beta=None, eps=1e-5):
+    """Ordered-policy emulation of the fused residual LayerNorm: OT-1024 on h = x + r."""
+    h = residual_sum(x, r)
+    return ot_layernorm(h, gamma, beta, eps), h
+
+
 def ot_softmax(x):
     x = _f32(x)
     r, c = x.shape

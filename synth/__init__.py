@@ -33,6 +33,7 @@ TAG_W = 2
 TAG_B = 3
 TAG_LABELS = 4
 TAG_ROW_OFFSET = 5
+TAG_RESIDUAL = 6
 
 _CHUNK = 1 << 23  # elements generated per slice (bounds temporary memory)
 
@@ -157,6 +158,13 @@ def norm_inputs(rows, cols, seed, row_offset=False, device="cpu"):
     return {"x": x, "w": w, "b": b}
 
 
+def residual_norm_inputs(rows, cols, seed, row_offset=False, device="cpu"):
+    """Norm inputs plus a residual r ~ N(0, 1), i.i.d. per element."""
+    d = norm_inputs(rows, cols, seed, row_offset, device)
+    d["r"] = normal_f32((rows, cols), seed, TAG_RESIDUAL, 0.0, 1.0, device)
+    return d
+
+
 def xent_inputs(rows, cols, seed, var=9.0, device="cpu"):
     return {"x": normal_f32((rows, cols), seed, TAG_X, 0.0, var, device),
             "labels": labels_i64(rows, cols, seed, device)}
@@ -181,6 +189,9 @@ WORKLOADS = {
     "layernorm_16x262144": dict(op="layernorm", rows=16, cols=262144, seed=4),
     "layernorm_16x1048576": dict(op="layernorm", rows=16, cols=1048576, seed=4),
     "layernorm_65536x128": dict(op="layernorm", rows=65536, cols=128, seed=4),
+    # fused residual norms (x and w, b as the 768x6144 family, residual ~ N(0, 1))
+    "add_rmsnorm_768x6144": dict(op="add_rmsnorm", rows=768, cols=6144, seed=2),
+    "add_layernorm_768x6144": dict(op="add_layernorm", rows=768, cols=6144, seed=2),
 }
 
 
@@ -192,6 +203,8 @@ def make_inputs(op, rows, cols, seed, var=None, row_offset=False, device="cpu"):
         return norm_inputs(rows, cols, seed, row_offset, device)
     if op == "cross_entropy":
         return xent_inputs(rows, cols, seed, 9.0 if var is None else var, device)
+    if op in ("add_rmsnorm", "add_layernorm"):
+        return residual_norm_inputs(rows, cols, seed, row_offset, device)
     raise ValueError(f"unknown op {op!r}")
 
 
