@@ -61,7 +61,10 @@ def alg_bytes(op, rows, cols):
     return {"softmax": 8 * e, "rmsnorm": 8 * e + 4 * cols, "layernorm": 8 * e + 8 * cols,
             "cross_entropy": 4 * e + 12 * rows,
             # fused residual norms: x and r read, y and h = x + r written
-            "add_rmsnorm": 16 * e + 4 * cols, "add_layernorm": 16 * e + 8 * cols}[op]
+            "add_rmsnorm": 16 * e + 4 * cols, "add_layernorm": 16 * e + 8 * cols,
+            # standalone row reductions: x read, one (two) values per row written
+            "row_sum": 4 * e + 4 * rows, "row_max": 4 * e + 4 * rows, "row_min": 4 * e + 4 * rows,
+            "row_minmax": 4 * e + 8 * rows}[op]
 
 
 def kernel_source_hash():
@@ -159,12 +162,14 @@ class Launch:
         self.rows, self.cols = w["rows"], w["cols"]
         base = synth.workload_inputs(workload, device=device)
         self.inputs = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(sets - 1)]
-        if op == "cross_entropy":
+        if op == "cross_entropy" or op.startswith("row_"):
             self.outputs = [torch.empty(self.rows, device=device) for _ in range(sets)]
         else:
             self.outputs = [torch.empty_like(base["x"]) for _ in range(sets)]
         # fused residual norms also write h = x + r
         self.h = [torch.empty_like(base["x"]) for _ in range(sets)] if op.startswith("add_") else None
+        if op == "row_minmax":  # the maxima (the minima go to outputs)
+            self.h = [torch.empty(self.rows, device=device) for _ in range(sets)]
         self.bytes = alg_bytes(op, self.rows, self.cols)
         self.key = f"{op}/{self.order}/{self.rows}x{self.cols}"
 
@@ -389,13 +394,19 @@ def oracle_fn(op, order):
                 "layernorm": lambda h: oracle.ot_layernorm(h["x"], h["w"], h["b"], 1e-5),
                 "cross_entropy": lambda h: oracle.ot_cross_entropy(h["x"], h["labels"]),
                 "add_rmsnorm": lambda h: oracle.ot_add_rmsnorm(h["x"], h["r"], h["w"], 1e-5),
-                "add_layernorm": lambda h: oracle.ot_add_layernorm(h["x"], h["r"], h["w"], h["b"], 1e-5)}[op]
+                "add_layernorm": lambda h: oracle.ot_add_layernorm(h["x"], h["r"], h["w"], h["b"], 1e-5),
+                "row_sum": lambda h: oracle.ot_row_sum(h["x"]), "row_max": lambda h: oracle.ot_row_max(h["x"]),
+                "row_min": lambda h: oracle.ot_row_min(h["x"]),
+                "row_minmax": lambda h: (oracle.ot_row_min(h["x"]), oracle.ot_row_max(h["x"]))}[op]
     return {"softmax": lambda h: oracle.softmax(h["x"]),
             "rmsnorm": lambda h: oracle.rmsnorm(h["x"], h["w"], 1e-5),
             "layernorm": lambda h: oracle.layernorm(h["x"], h["w"], h["b"], 1e-5),
             "cross_entropy": lambda h: oracle.cross_entropy(h["x"], h["labels"]),
             "add_rmsnorm": lambda h: oracle.add_rmsnorm(h["x"], h["r"], h["w"], 1e-5),
-            "add_layernorm": lambda h: oracle.add_layernorm(h["x"], h["r"], h["w"], h["b"], 1e-5)}[op]
+            "add_layernorm": lambda h: oracle.add_layernorm(h["x"], h["r"], h["w"], h["b"], 1e-5),
+            "row_sum": lambda h: oracle.row_sum(h["x"]), "row_max": lambda h: oracle.row_max(h["x"]),
+            "row_min": lambda h: oracle.row_min(h["x"]),
+            "row_minmax": lambda h: (oracle.row_min(h["x"]), oracle.row_max(h["x"]))}[op]
 
 
 def host_sample(op, workload, rows):

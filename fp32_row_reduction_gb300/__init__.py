@@ -46,12 +46,18 @@ TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_SPLIT = 7
 TR_OP_ADD_RMSNORM = 4
 TR_OP_ADD_LAYERNORM = 5
+TR_OP_ROW_SUM = 6
+TR_OP_ROW_MAX = 7
+TR_OP_ROW_MIN = 8
+TR_OP_ROW_MINMAX = 9
 TR_PLAN_FLAG_PARAMS_IN_REGISTERS = 1
 TR_PLAN_FLAG_PARAMS_IN_SHARED = 2
 TR_PLAN_FLAG_TWO_ROWS = 4
 
 OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LAYERNORM,
-       "cross_entropy": TR_OP_CROSS_ENTROPY, "add_rmsnorm": TR_OP_ADD_RMSNORM, "add_layernorm": TR_OP_ADD_LAYERNORM}
+       "cross_entropy": TR_OP_CROSS_ENTROPY, "add_rmsnorm": TR_OP_ADD_RMSNORM, "add_layernorm": TR_OP_ADD_LAYERNORM,
+       "row_sum": TR_OP_ROW_SUM, "row_max": TR_OP_ROW_MAX, "row_min": TR_OP_ROW_MIN, "row_minmax": TR_OP_ROW_MINMAX}
+REDUCE_OPS = ("row_sum", "row_max", "row_min", "row_minmax")
 ORDERS = {"unordered": TR_ORDER_UNORDERED_TREE, "ordered": TR_ORDER_ORDERED_TREE}
 
 
@@ -96,6 +102,10 @@ SIGNATURES = {
     "tr_layernorm_f32": ([_P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
     "tr_cross_entropy_f32": ([_P, _P, _P, _I64, _I64, _I32, _P], _I32),
     "tr_add_rmsnorm_f32": ([_P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
+    "tr_row_sum_f32": ([_P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_row_max_f32": ([_P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_row_min_f32": ([_P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_row_minmax_f32": ([_P, _P, _P, _I64, _I64, _I32, _P], _I32),
     "tr_add_layernorm_f32": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
     "tr_plan_describe": ([_I32, _I64, _I64, _I32, ctypes.POINTER(tr_plan)], _I32),
     "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
@@ -367,6 +377,25 @@ def add_layernorm(x, residual, weight=None, bias=None, eps=1e-5, out=None, h_out
     return y
 
 
+def row_reduce(x, op="row_sum", out=None, out2=None, order="unordered", stream=None):
+    """Per-row sum, max or min of a CUDA float32 (rows, cols) tensor; op
+    "row_minmax" writes the minima to ``out`` and the maxima to ``out2`` and
+    returns both."""
+    import torch
+    _check_matrix(x, "x")
+    r, c = x.shape
+    y = torch.empty(r, device=x.device, dtype=torch.float32) if out is None else out
+    lib = load()
+    if op == "row_minmax":
+        y2 = torch.empty(r, device=x.device, dtype=torch.float32) if out2 is None else out2
+        _check(lib.tr_row_minmax_f32(x.data_ptr(), y.data_ptr(), y2.data_ptr(), r, c, _order(order),
+                                     _stream_handle(stream)), "row_minmax")
+        return y, y2
+    fn = {"row_sum": lib.tr_row_sum_f32, "row_max": lib.tr_row_max_f32, "row_min": lib.tr_row_min_f32}[op]
+    _check(fn(x.data_ptr(), y.data_ptr(), r, c, _order(order), _stream_handle(stream)), op)
+    return y
+
+
 def cross_entropy(logits, labels, out=None, order="unordered", stream=None):
     """Per-row loss log(sum exp(x)) - x[label] (label outside [0, cols) selects 0)."""
     import torch
@@ -393,6 +422,8 @@ def run_op(op, inputs, out=None, order="unordered", eps=1e-5, stream=None, h_out
         return rmsnorm(inputs["x"], inputs.get("w"), eps, out=out, order=order, stream=stream)
     if op == "layernorm":
         return layernorm(inputs["x"], inputs.get("w"), inputs.get("b"), eps, out=out, order=order, stream=stream)
+    if op in REDUCE_OPS:
+        return row_reduce(inputs["x"], op, out=out, out2=h_out, order=order, stream=stream)
     if op == "add_rmsnorm":
         return add_rmsnorm(inputs["x"], inputs["r"], inputs.get("w"), eps, out=out, h_out=h_out, order=order,
                            stream=stream)

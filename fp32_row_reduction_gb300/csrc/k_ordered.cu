@@ -24,6 +24,7 @@
 // the correctly rounded reciprocal: one IEEE division per row, one rounded
 // product per element.
 #include <cuda_runtime.h>
+#include <climits>
 #include <stdint.h>
 
 #include "tr_device.cuh"
@@ -134,6 +135,32 @@ __device__ __forceinline__ float log_ot(float x) {
 __device__ __forceinline__ float max2(float a, float b) { return fmaxf(a, b); }
 struct Add {
     static __device__ __forceinline__ float f(float a, float b) { return __fadd_rn(a, b); }
+};
+// Canonical max / min of the standalone ordered reductions, whose result is the
+// output itself: NaN in the first operand wins, then NaN in the second, then
+// the larger (smaller) value, +0 over -0 for the max and -0 over +0 for the
+// min. Selects only, so a NaN keeps its payload.
+__device__ __forceinline__ float cmax2(float a, float b) {
+    const bool a_wins = (a != a) || (!(b != b) && (a > b || (a == b && !(__float_as_uint(a) >> 31))));
+    return a_wins ? a : b;
+}
+__device__ __forceinline__ float cmin2(float a, float b) {
+    const bool a_wins = (a != a) || (!(b != b) && (a < b || (a == b && (__float_as_uint(a) >> 31))));
+    return a_wins ? a : b;
+}
+// Integer key of a float whose signed order is the total order of the floats
+// with -0 below +0 (negative values have their magnitude bits flipped); NaNs
+// map above key(+inf) or below key(-inf). The map is its own inverse.
+__device__ __forceinline__ int order_key(float x) {
+    const int b = __float_as_int(x);
+    return b ^ ((b >> 31) & 0x7fffffff);
+}
+__device__ __forceinline__ float from_order_key(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7fffffff)); }
+struct CMax {
+    static __device__ __forceinline__ float f(float a, float b) { return cmax2(a, b); }
+};
+struct CMin {
+    static __device__ __forceinline__ float f(float a, float b) { return cmin2(a, b); }
 };
 struct Max {
     static __device__ __forceinline__ float f(float a, float b) { return max2(a, b); }
@@ -350,9 +377,23 @@ __global__ void __launch_bounds__(kOrderedThreads, ot_min_blocks<K>()) ot_kernel
         ot_cached_row<OP, K>(a, row, q, aligned && a.y_vec, gpart, buf);
     } else {
         const int nj = (cols + 1023) / 1024;
+        // four quads in flight at a time; the leaves still fold in increasing column order
         auto fold = [&](auto elem, auto comb, float init, float (&leaf)[4]) {
             leaf[0] = leaf[1] = leaf[2] = leaf[3] = init;
-            for (int j = 0; j < nj; ++j) {
+            int j = 0;
+            for (; j + 3 < nj; j += 4) {
+                float qq[4][4];
+                bool oo[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) load_quad(xr, cols, j + u, aligned, qq[u], oo[u]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (oo[u][v])
+                            leaf[v] = comb(leaf[v], elem(qq[u][v], (j + u) * 1024 + 4 * static_cast<int>(threadIdx.x) + v));
+            }
+            for (; j < nj; ++j) {
                 float qq[4];
                 bool oo[4];
                 load_quad(xr, cols, j, aligned, qq, oo);
@@ -392,6 +433,86 @@ __global__ void __launch_bounds__(kOrderedThreads, ot_min_blocks<K>()) ot_kernel
                     const int64_t label = a.labels[row];
                     const float sel = (label >= 0 && label < cols) ? __ldg(xr + label) : 0.0f;
                     a.loss[row] = __fsub_rn(__fadd_rn(log_ot(s), m), sel);
+                }
+            }
+        } else if constexpr (OP == OP_RSUM) {
+            fold(ident, add, 0.0f, leaf);
+            const float r = tree<Add>(leaf, gpart, buf);
+            if (threadIdx.x == 0) a.loss[row] = r;
+        } else if constexpr (OP == OP_RMAX || OP == OP_RMIN || OP == OP_RMINMAX) {
+            // Without a NaN in the row the canonical max (min) of the tree is the
+            // largest (smallest) element in the total order with -0 below +0, in
+            // any grouping. That order is the signed order of the integer keys, so
+            // one pass folds both key extremes with integer max / min; the keys of
+            // NaNs fall outside [key(-inf), key(+inf)], which flags the rare row
+            // that needs the canonical fold itself.
+            int kmax[4], kmin[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                kmax[v] = INT_MIN;
+                kmin[v] = INT_MAX;
+            }
+            auto take = [&](const float (&qq)[4], const bool (&oo)[4]) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int k = order_key(qq[v]);
+                    kmax[v] = oo[v] ? max(kmax[v], k) : kmax[v];
+                    kmin[v] = oo[v] ? min(kmin[v], k) : kmin[v];
+                }
+            };
+            int j = 0;
+            for (; j + 3 < nj; j += 4) {
+                float qq[4][4];
+                bool oo[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) load_quad(xr, cols, j + u, aligned, qq[u], oo[u]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) take(qq[u], oo[u]);
+            }
+            for (; j < nj; ++j) {
+                float qq[4];
+                bool oo[4];
+                load_quad(xr, cols, j, aligned, qq, oo);
+                take(qq, oo);
+            }
+            int hi = max(max(kmax[0], kmax[1]), max(kmax[2], kmax[3]));
+            int lo = min(min(kmin[0], kmin[1]), min(kmin[2], kmin[3]));
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                hi = max(hi, __shfl_xor_sync(kFull, hi, o));
+                lo = min(lo, __shfl_xor_sync(kFull, lo, o));
+            }
+            if ((threadIdx.x & 31) == 0) {
+                gpart[0][threadIdx.x >> 5] = __int_as_float(hi);
+                gpart[1][threadIdx.x >> 5] = __int_as_float(lo);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                hi = max(hi, __float_as_int(gpart[0][w]));
+                lo = min(lo, __float_as_int(gpart[1][w]));
+            }
+            __syncthreads();   // the canonical trees below reuse both slots
+            if (hi <= order_key(__int_as_float(0x7f800000)) && lo >= order_key(__int_as_float(0xff800000))) {
+                if (threadIdx.x == 0) {
+                    if constexpr (OP == OP_RMAX) a.loss[row] = from_order_key(hi);
+                    if constexpr (OP == OP_RMIN) a.loss[row] = from_order_key(lo);
+                    if constexpr (OP == OP_RMINMAX) {
+                        a.loss[row] = from_order_key(lo);
+                        a.out2[row] = from_order_key(hi);
+                    }
+                }
+            } else {
+                // a NaN in the row: the canonical selects decide which one survives
+                if constexpr (OP == OP_RMAX || OP == OP_RMINMAX) {
+                    fold(ident, [](float p, float v) { return cmax2(p, v); }, __int_as_float(0xff800000), leaf);
+                    const float r = tree<CMax>(leaf, gpart, buf);
+                    if (threadIdx.x == 0) (OP == OP_RMAX ? a.loss : a.out2)[row] = r;
+                }
+                if constexpr (OP == OP_RMIN || OP == OP_RMINMAX) {
+                    fold(ident, [](float p, float v) { return cmin2(p, v); }, __int_as_float(0x7f800000), leaf);
+                    const float r = tree<CMin>(leaf, gpart, buf);
+                    if (threadIdx.x == 0) a.loss[row] = r;
                 }
             }
         } else if constexpr (OP == OP_RMSNORM) {
@@ -564,6 +685,17 @@ const void* kernel_ordered_residual(int op, int slots) {
 }
 
 const void* kernel_ordered(int op, int slots) {
+    if (op >= TR_OP_ROW_SUM && op <= TR_OP_ROW_MINMAX) {
+        // standalone reductions read each element once: the streaming realisation only
+        if (slots != 0) return nullptr;
+        switch (op) {
+            case TR_OP_ROW_SUM: return reinterpret_cast<const void*>(ordered::ot_kernel<OP_RSUM, 0>);
+            case TR_OP_ROW_MAX: return reinterpret_cast<const void*>(ordered::ot_kernel<OP_RMAX, 0>);
+            case TR_OP_ROW_MIN: return reinterpret_cast<const void*>(ordered::ot_kernel<OP_RMIN, 0>);
+            case TR_OP_ROW_MINMAX: return reinterpret_cast<const void*>(ordered::ot_kernel<OP_RMINMAX, 0>);
+        }
+        return nullptr;
+    }
 #define TR_OT_CASES(OPV)                                                    \
     switch (slots) {                                                        \
         case 0: return reinterpret_cast<const void*>(ordered::ot_kernel<OPV, 0>);   \

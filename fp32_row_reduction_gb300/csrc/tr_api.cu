@@ -52,7 +52,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
-constexpr int kOps = TR_OP_ADD_LAYERNORM + 1;
+constexpr int kOps = TR_OP_ROW_MINMAX + 1;
 bool g_override_set[kOps] = {};
 tr_plan g_override[kOps];
 int g_debug_flags = 0;
@@ -452,6 +452,46 @@ static tr_status residual_call(int op, const float* x, const float* residual, co
     return run(c, stream);
 }
 
+// Standalone row reductions: out[r] (and out2[r]) per row.
+static tr_status reduce_call(int op, const float* x, float* out, float* out2, int64_t rows, int64_t cols,
+                             tr_order order, cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!x || !out || (op == TR_OP_ROW_MINMAX && !out2))
+        return fail(TR_ERR_INVALID_ARG, "x and the outputs must not be null");
+    if (misaligned(x, 4) || misaligned(out, 4) || misaligned(out2, 4))
+        return fail(TR_ERR_INVALID_ARG, "x and the outputs must be 4-byte aligned");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    const size_t no = static_cast<size_t>(rows) * 4;
+    if (overlaps(x, n, out, no) || overlaps(x, n, out2, no) || overlaps(out, no, out2, no))
+        return fail(TR_ERR_INVALID_ARG, "an output overlaps the input or the other output");
+    Call c{op, blank_args(x, rows, cols), order};
+    c.a.loss = out;
+    c.a.out2 = out2;
+    return run(c, stream);
+}
+
+tr_status tr_row_sum_f32(const float* x, float* out, int64_t rows, int64_t cols, tr_order order,
+                         cudaStream_t stream) {
+    return reduce_call(TR_OP_ROW_SUM, x, out, nullptr, rows, cols, order, stream);
+}
+
+tr_status tr_row_max_f32(const float* x, float* out, int64_t rows, int64_t cols, tr_order order,
+                         cudaStream_t stream) {
+    return reduce_call(TR_OP_ROW_MAX, x, out, nullptr, rows, cols, order, stream);
+}
+
+tr_status tr_row_min_f32(const float* x, float* out, int64_t rows, int64_t cols, tr_order order,
+                         cudaStream_t stream) {
+    return reduce_call(TR_OP_ROW_MIN, x, out, nullptr, rows, cols, order, stream);
+}
+
+tr_status tr_row_minmax_f32(const float* x, float* out_min, float* out_max, int64_t rows, int64_t cols,
+                            tr_order order, cudaStream_t stream) {
+    return reduce_call(TR_OP_ROW_MINMAX, x, out_min, out_max, rows, cols, order, stream);
+}
+
 tr_status tr_add_rmsnorm_f32(const float* x, const float* residual, const float* w, float* y, float* h,
                              int64_t rows, int64_t cols, float eps, tr_order order, cudaStream_t stream) {
     return residual_call(TR_OP_ADD_RMSNORM, x, residual, w, nullptr, y, h, rows, cols, eps, order, stream);
@@ -465,7 +505,7 @@ tr_status tr_add_layernorm_f32(const float* x, const float* residual, const floa
 
 tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order order, tr_plan* out) {
     if (!out) return fail(TR_ERR_INVALID_ARG, "out must not be null");
-    if (op < TR_OP_SOFTMAX || op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "bad op");
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
     if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1 to describe a plan");
@@ -496,7 +536,7 @@ tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order orde
 tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows, int64_t cols, tr_order order,
                              int32_t align16, tr_plan* out) {
     if (!dev || !out) return fail(TR_ERR_INVALID_ARG, "dev and out must not be null");
-    if (op < TR_OP_SOFTMAX || op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "bad op");
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
     if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1 to select a plan");
@@ -541,7 +581,7 @@ tr_status tr_plan_estimate_with(const tr_device_desc* dev, const tr_plan* plan, 
 tr_status tr_plan_candidates(int32_t op, int64_t rows, int64_t cols, tr_order order, int32_t align16, tr_plan* out,
                              int32_t cap, int32_t* count) {
     if (!count || (cap > 0 && !out)) return fail(TR_ERR_INVALID_ARG, "count (and out when cap > 0) must not be null");
-    if (op < TR_OP_SOFTMAX || op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (op < TR_OP_SOFTMAX || op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "bad op");
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
     if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1");
@@ -566,7 +606,7 @@ tr_status tr_plan_override(const tr_plan* plan) {
         for (bool& b : g_override_set) b = false;
         return TR_OK;
     }
-    if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "bad op");
     if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_SPLIT)
         return fail(TR_ERR_INVALID_ARG, "bad plan kind");
     g_override[plan->op] = *plan;

@@ -23,7 +23,17 @@ constexpr float kL2E = 1.44269504088896340736f;  // log2(e)
 constexpr float kLN2 = 0.69314718055994530942f;  // ln(2)
 constexpr unsigned kFull = 0xffffffffu;
 
-enum Op : int { OP_SOFTMAX = 0, OP_RMSNORM = 1, OP_LAYERNORM = 2, OP_XENT = 3 };
+enum Op : int {
+    OP_SOFTMAX = 0,
+    OP_RMSNORM = 1,
+    OP_LAYERNORM = 2,
+    OP_XENT = 3,
+    // standalone row reductions: one value per row (two for min/max)
+    OP_RSUM = 4,
+    OP_RMAX = 5,
+    OP_RMIN = 6,
+    OP_RMINMAX = 7
+};
 
 // 2^t with the SFU (ex2.approx): max relative error ~2^-22 on [-126, 128];
 // results below 2^-126 flush to zero, which the unordered tolerance absorbs.

@@ -39,6 +39,7 @@ struct RowArgs {
     float* h;              // fused residual norms: x + r written out (null: not written)
     int r_vec;             // r rows have the same 16-byte phase as x rows
     int h_vec;             // h rows have the same 16-byte phase as x rows
+    float* out2;           // row min/max: the maxima (loss receives the minima)
 };
 
 constexpr int kDebugForceTimeout = 1;
@@ -71,6 +72,7 @@ const void* kernel_ordered(int op, int slots);
 const void* kernel_ordered_residual(int op, int slots);
 const void* kernel_add_rmsnorm(int kind, int lanes, int slots, int flags);
 const void* kernel_add_layernorm(int kind, int lanes, int slots, int flags);
+const void* kernel_reduce(int op, int kind, int lanes, int slots, int flags);
 const void* kernel_ordered_staged(int op, int slots);
 // Dynamic shared memory a plan's kernel needs (0 for all but staged plans).
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols);
@@ -80,6 +82,10 @@ inline const void* kernel_for(const tr_plan& p) {
         if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered_residual(p.op, p.vec_slots);
         return p.op == TR_OP_ADD_RMSNORM ? kernel_add_rmsnorm(p.kind, p.lanes_per_row, p.vec_slots, p.flags)
                                          : kernel_add_layernorm(p.kind, p.lanes_per_row, p.vec_slots, p.flags);
+    }
+    if (p.op >= TR_OP_ROW_SUM && p.op <= TR_OP_ROW_MINMAX) {
+        if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
+        return kernel_reduce(p.op, p.kind, p.lanes_per_row, p.vec_slots, p.flags);
     }
     if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
     if (p.kind == TR_PLAN_ORDERED_STAGED) return p.flags ? nullptr : kernel_ordered_staged(p.op, p.vec_slots);

@@ -70,9 +70,15 @@ int base_op(int op) {
     return op == TR_OP_ADD_RMSNORM ? TR_OP_RMSNORM : op == TR_OP_ADD_LAYERNORM ? TR_OP_LAYERNORM : op;
 }
 bool residual_op(int op) { return op == TR_OP_ADD_RMSNORM || op == TR_OP_ADD_LAYERNORM; }
+// Standalone row reductions: streamed once, one (or two) values per row.
+bool reduce_op(int op) { return op >= TR_OP_ROW_SUM && op <= TR_OP_ROW_MINMAX; }
 
 int reductions_of(int op) {
     switch (op) {
+        case TR_OP_ROW_MINMAX: return 2;
+        case TR_OP_ROW_SUM:
+        case TR_OP_ROW_MAX:
+        case TR_OP_ROW_MIN: return 1;
         case TR_OP_SOFTMAX: return 2;
         case TR_OP_RMSNORM: return 1;
         case TR_OP_LAYERNORM: return 2;
@@ -167,9 +173,14 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     align16 = align16 && cols % 4 == 0;  // every row start 16-byte aligned needs cols % 4 == 0
     const int64_t n4 = ceil_div(cols, 4);  // upper bound on 16-byte body slots of any row
     const bool ordered = p->order == TR_ORDER_ORDERED_TREE;
-    const bool xent = p->op == TR_OP_CROSS_ENTROPY;
+    // cross-entropy and the standalone reductions stream each row once
+    const bool xent = p->op == TR_OP_CROSS_ENTROPY || reduce_op(p->op);
     if (p->order != TR_ORDER_UNORDERED_TREE && !ordered) return fail(TR_ERR_INVALID_ARG, "bad order");
-    if (p->op < TR_OP_SOFTMAX || p->op > TR_OP_ADD_LAYERNORM) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (p->op < TR_OP_SOFTMAX || p->op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "bad op");
+    if (reduce_op(p->op) && p->kind == TR_PLAN_ORDERED && p->vec_slots != 0)
+        return fail(TR_ERR_UNSUPPORTED, "ordered standalone reductions use the streaming OT-1024 realisation (vec_slots 0)");
+    if (reduce_op(p->op) && p->kind == TR_PLAN_ORDERED_STAGED)
+        return fail(TR_ERR_UNSUPPORTED, "ordered standalone reductions use the streaming OT-1024 realisation");
     const int bop = base_op(p->op);
     if (residual_op(p->op)) {
         const bool ok = (p->kind == TR_PLAN_ROWS && (p->flags & ~TR_PLAN_FLAG_PARAMS_IN_SHARED) == 0) ||
@@ -187,7 +198,7 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
         return fail(TR_ERR_UNSUPPORTED, "the ordered policy is realised only by the OT-1024 plans");
     if (ordered && p->kind == TR_PLAN_SPLIT) return fail(TR_ERR_UNSUPPORTED, "split plans are unordered");
     if (!ordered && xent != (p->kind == TR_PLAN_XENT))
-        return fail(TR_ERR_UNSUPPORTED, "cross-entropy is realised only by the streaming XENT plan");
+        return fail(TR_ERR_UNSUPPORTED, "cross-entropy and the row reductions are realised only by the streaming XENT plan");
     const int T = p->block_threads;
     if (T < 32 || T > 1024 || T % 32) return fail(TR_ERR_UNSUPPORTED, "block_threads must be a multiple of 32 in [32, 1024]");
     if (p->flags & ~(TR_PLAN_FLAG_PARAMS_IN_REGISTERS | TR_PLAN_FLAG_PARAMS_IN_SHARED | TR_PLAN_FLAG_TWO_ROWS))
@@ -340,6 +351,10 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
         case TR_OP_SOFTMAX: alg = 8.0 * E; break;
         case TR_OP_RMSNORM: alg = 8.0 * E + 4.0 * cols; break;
         case TR_OP_LAYERNORM: alg = 8.0 * E + 8.0 * cols; break;
+        case TR_OP_ROW_SUM:
+        case TR_OP_ROW_MAX:
+        case TR_OP_ROW_MIN: alg = 4.0 * E + 4.0 * rows; break;
+        case TR_OP_ROW_MINMAX: alg = 4.0 * E + 8.0 * rows; break;
         default: alg = 4.0 * E + 12.0 * rows; break;
     }
     if (residual_op(p.op)) alg += 8.0 * E;  // the residual read and h written
@@ -364,7 +379,8 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     // arithmetic: SFU ex2 (16 per SM per clock) and ALU issue (128 lanes per SM per clock)
     double sfu_per_elem = 0.0, alu_per_elem = 4.0;
     if (p.kind == TR_PLAN_ORDERED || p.kind == TR_PLAN_ORDERED_STAGED) {
-        alu_per_elem = op == TR_OP_SOFTMAX ? 48.0 : op == TR_OP_CROSS_ENTROPY ? 24.0 : op == TR_OP_LAYERNORM ? 24.0 : 16.0;
+        alu_per_elem = op == TR_OP_SOFTMAX ? 48.0 : op == TR_OP_CROSS_ENTROPY ? 24.0 : op == TR_OP_LAYERNORM ? 24.0
+                       : reduce_op(op) ? 8.0 : 16.0;
     } else if (op == TR_OP_SOFTMAX) {
         sfu_per_elem = p.kind == TR_PLAN_STREAM ? 2.0 : 1.0;
     } else if (op == TR_OP_CROSS_ENTROPY) {
@@ -478,7 +494,7 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
         p.rows_per_cta = 1;
         p.block_threads = kOrderedThreads;
         const int k = smallest_covering(kOrderedSlots, ceil_div(cols, 1024));
-        p.vec_slots = k < 0 ? 0 : k;
+        p.vec_slots = (k < 0 || reduce_op(op)) ? 0 : k;  // a standalone reduction streams its row
         if (!res || p.vec_slots > 0) cands.push_back(p);
         // the staged OT-1024 realisation (TR_PLAN_ORDERED_STAGED) stays available by
         // override; measured plan sweeps found the one-shot realisation at full
@@ -495,7 +511,7 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
                 cands.push_back(q);
             }
     } else {
-        const bool xent = op == TR_OP_CROSS_ENTROPY;
+        const bool xent = op == TR_OP_CROSS_ENTROPY || reduce_op(op);
         const int kind = xent ? TR_PLAN_XENT : TR_PLAN_ROWS;
         // a row inside a warp: 4, 8 or 16 lanes
         for (int G : {4, 8, 16}) {

@@ -918,4 +918,127 @@ __global__ void __launch_bounds__(1024) xent_kernel(const RowArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Standalone row reductions (sum, max, min, min and max together): one
+// streaming pass per row like the cross-entropy kernel (TR_PLAN_XENT shapes: G
+// lanes per row or S warps per row, Q rows per CTA, chunks of K float4 per
+// worker); one value per row (two for min/max). Max and min are the hardware
+// maxNum/minNum (NaN operands skipped); the sum is a tree in worker order.
+// ---------------------------------------------------------------------------
+// The identity of these folds is NaN: maxNum/minNum skip it, so a row (or a
+// padding lane) contributes nothing, and the result is NaN only when every
+// element of the row is NaN.
+struct MinMax {
+    float lo, hi;
+};
+__device__ __forceinline__ MinMax merge(MinMax a, MinMax b) { return MinMax{fminf(a.lo, b.lo), fmaxf(a.hi, b.hi)}; }
+__device__ __forceinline__ MinMax shfl_xor(MinMax v, int o) {
+    return MinMax{__shfl_xor_sync(kFull, v.lo, o), __shfl_xor_sync(kFull, v.hi, o)};
+}
+struct RMax {
+    float v;
+};
+__device__ __forceinline__ RMax merge(RMax a, RMax b) { return RMax{fmaxf(a.v, b.v)}; }
+__device__ __forceinline__ RMax shfl_xor(RMax v, int o) { return RMax{__shfl_xor_sync(kFull, v.v, o)}; }
+struct RMin {
+    float v;
+};
+__device__ __forceinline__ RMin merge(RMin a, RMin b) { return RMin{fminf(a.v, b.v)}; }
+__device__ __forceinline__ RMin shfl_xor(RMin v, int o) { return RMin{__shfl_xor_sync(kFull, v.v, o)}; }
+template <>
+__device__ __forceinline__ MinMax identity_of<MinMax>() {
+    return MinMax{__int_as_float(0x7fc00000), __int_as_float(0x7fc00000)};
+}
+template <>
+__device__ __forceinline__ RMax identity_of<RMax>() { return RMax{__int_as_float(0x7fc00000)}; }
+template <>
+__device__ __forceinline__ RMin identity_of<RMin>() { return RMin{__int_as_float(0x7fc00000)}; }
+
+template <int OP>
+using ReduceStat = typename std::conditional<
+    OP == OP_RSUM, float,
+    typename std::conditional<OP == OP_RMAX, RMax,
+                              typename std::conditional<OP == OP_RMIN, RMin, MinMax>::type>::type>::type;
+
+template <int OP>
+__device__ __forceinline__ ReduceStat<OP> reduce_elem(ReduceStat<OP> s, float v) {
+    if constexpr (OP == OP_RSUM) {
+        return s + v;
+    } else if constexpr (OP == OP_RMAX) {
+        return RMax{fmaxf(s.v, v)};
+    } else if constexpr (OP == OP_RMIN) {
+        return RMin{fminf(s.v, v)};
+    } else {
+        return MinMax{fminf(s.lo, v), fmaxf(s.hi, v)};
+    }
+}
+
+template <int OP, int G, int K>
+__global__ void __launch_bounds__(1024) reduce_kernel(const RowArgs a) {
+    using Stat = ReduceStat<OP>;
+    __shared__ float4 part[2][32];
+    RowPos p;
+    p.lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    int64_t row;
+    if constexpr (G < 32) {
+        p.W = G;
+        p.w = p.lane & (G - 1);
+        p.S = 1;
+        p.s = 0;
+        p.q = warp * (32 / G) + p.lane / G;
+        row = static_cast<int64_t>(blockIdx.x) * ((blockDim.x >> 5) * (32 / G)) + p.q;
+    } else {
+        p.S = a.S;
+        p.W = 32 * a.S;
+        p.s = warp % a.S;
+        p.q = warp / a.S;
+        p.w = p.s * 32 + p.lane;
+        row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / p.W) + p.q;
+    }
+    const bool active = row < a.rows;
+    const int64_t rr = active ? row : a.rows - 1;
+    const float* xr = a.x + rr * a.cols;
+    const RowGeom g = row_geom(xr, a.cols);
+    const float* xb = xr + g.head;
+    Stat st = identity_of<Stat>();
+    pdl_enter();
+    if (active) {
+        for (int base = 0; base < g.nvec; base += K * p.W) {
+            float4 c[K];
+            bool ok[K];
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int i = base + j * p.W + p.w;
+                ok[j] = i < g.nvec;
+                if (ok[j]) c[j] = ld_stream4(xb + 4 * i);
+            }
+#pragma unroll
+            for (int j = 0; j < K; ++j)
+                if (ok[j]) {
+                    if constexpr (OP == OP_RSUM) {
+                        st += (c[j].x + c[j].y) + (c[j].z + c[j].w);
+                    } else {
+                        st = reduce_elem<OP>(reduce_elem<OP>(st, c[j].x), c[j].y);
+                        st = reduce_elem<OP>(reduce_elem<OP>(st, c[j].z), c[j].w);
+                    }
+                }
+        }
+        if (p.w < g.head) st = reduce_elem<OP>(st, ld_stream1(xr + p.w));
+        if (p.w < g.tail) st = reduce_elem<OP>(st, ld_stream1(xb + 4 * g.nvec + p.w));
+    }
+    int buf = 0;
+    st = cta_row_merge<Stat, G>(st, p, part, buf);
+    if (active && p.w == 0) {
+        if constexpr (OP == OP_RSUM) {
+            a.loss[rr] = st;
+        } else if constexpr (OP == OP_RMINMAX) {
+            a.loss[rr] = st.lo;
+            a.out2[rr] = st.hi;
+        } else {
+            a.loss[rr] = st.v;
+        }
+    }
+}
+
 }  // namespace tr

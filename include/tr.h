@@ -64,7 +64,11 @@ typedef enum tr_op {
     TR_OP_LAYERNORM = 2,
     TR_OP_CROSS_ENTROPY = 3,
     TR_OP_ADD_RMSNORM = 4,   /* fused residual: y = RMSNorm(x + r) (tr_add_rmsnorm_f32) */
-    TR_OP_ADD_LAYERNORM = 5  /* fused residual: y = LayerNorm(x + r) (tr_add_layernorm_f32) */
+    TR_OP_ADD_LAYERNORM = 5, /* fused residual: y = LayerNorm(x + r) (tr_add_layernorm_f32) */
+    TR_OP_ROW_SUM = 6,       /* standalone row reductions (tr_row_sum_f32, ...) */
+    TR_OP_ROW_MAX = 7,
+    TR_OP_ROW_MIN = 8,
+    TR_OP_ROW_MINMAX = 9
 } tr_op;
 
 /* How a row is mapped onto the GPU (the build's counterpart of the page's
@@ -174,6 +178,24 @@ tr_status tr_add_rmsnorm_f32(const float* x, const float* residual, const float*
 tr_status tr_add_layernorm_f32(const float* x, const float* residual, const float* gamma, const float* beta,
                                float* y, float* h, int64_t rows, int64_t cols, float eps, tr_order order,
                                cudaStream_t stream);
+
+/* ---- standalone row reductions -----------------------------------------
+ * "TIRx Metal reduction lowering" §8 (its test list: row sums at widths 127,
+ * 257, 1024 and 4096; minimum and maximum together at 7x1024). x: rows x cols;
+ * out (out_min, out_max): rows floats. Unordered policy: a tree in worker
+ * order for the sum; max and min are exact in any order and skip NaN elements
+ * (NaN only when every element of the row is NaN). Ordered policy: the OT-1024 tree with IEEE
+ * adds, and for max/min the canonical select (a NaN wins, +0 over -0 for the
+ * max, -0 over +0 for the min), bit-identical to its CPU emulation (a sum
+ * that becomes NaN has no portable NaN payload). */
+tr_status tr_row_sum_f32(const float* x, float* out, int64_t rows, int64_t cols, tr_order order,
+                         cudaStream_t stream);
+tr_status tr_row_max_f32(const float* x, float* out, int64_t rows, int64_t cols, tr_order order,
+                         cudaStream_t stream);
+tr_status tr_row_min_f32(const float* x, float* out, int64_t rows, int64_t cols, tr_order order,
+                         cudaStream_t stream);
+tr_status tr_row_minmax_f32(const float* x, float* out_min, float* out_max, int64_t rows, int64_t cols,
+                            tr_order order, cudaStream_t stream);
 
 /* ---- no-allocation entry point ----------------------------------------- */
 

@@ -62,11 +62,12 @@ def lib():
             "ot_cross_entropy_f32": [f32p, i64p, f32p, i64, i64],
             "ot_sum_f32": [f32p, i64],
             "ot_max_f32": [f32p, i64],
+            "ot_min_f32": [f32p, i64],
         }
         for name, args in sig.items():
             fn = getattr(_lib, name)
             fn.argtypes = args
-            fn.restype = ctypes.c_float if name in ("ot_sum_f32", "ot_max_f32") else ctypes.c_int
+            fn.restype = ctypes.c_float if name in ("ot_sum_f32", "ot_max_f32", "ot_min_f32") else ctypes.c_int
         for name in ("ot_expf", "ot_logf"):
             fn = getattr(_lib, name)
             fn.argtypes = [ctypes.c_float]
@@ -215,6 +216,42 @@ def ot_sum(v):
 def ot_max(v):
     v = _f32(v).ravel()
     return np.float32(lib().ot_max_f32(_ptr(v, ctypes.c_float), v.size))
+
+
+def ot_min(v):
+    v = _f32(v).ravel()
+    return np.float32(lib().ot_min_f32(_ptr(v, ctypes.c_float), v.size))
+
+
+# ---- standalone row reductions ("TIRx Metal reduction lowering" §8: row sums at
+# widths 127/257/1024/4096, minimum and maximum together): the plain definitions.
+
+def row_sum(x):
+    """Sum of each row in FP64 (float64 result)."""
+    return _f32(x).astype(np.float64).sum(axis=1)
+
+
+def row_max(x):
+    """Maximum of each row (exact in any order; float32 result)."""
+    return _f32(x).max(axis=1)
+
+
+def row_min(x):
+    """Minimum of each row (exact in any order; float32 result)."""
+    return _f32(x).min(axis=1)
+
+
+def ot_row_sum(x):
+    """Ordered-policy (OT-1024) emulation of the row sums."""
+    return np.array([ot_sum(r) for r in _f32(x)], dtype=np.float32)
+
+
+def ot_row_max(x):
+    return np.array([ot_max(r) for r in _f32(x)], dtype=np.float32)
+
+
+def ot_row_min(x):
+    return np.array([ot_min(r) for r in _f32(x)], dtype=np.float32)
 
 
 def ot_expf(x):

@@ -231,6 +231,15 @@ static float ot_max2(float a, float b) {
     if (b > a) return b;
     return signbit(a) ? b : a;
 }
+/* Canonical min: NaN in the first operand wins, then NaN in the second, then
+ * the smaller value, -0 over +0 (commutative for all non-NaN pairs). */
+static float ot_min2(float a, float b) {
+    if (a != a) return a;
+    if (b != b) return b;
+    if (a < b) return a;
+    if (b < a) return b;
+    return signbit(a) ? a : b;
+}
 static float ot_add2(float a, float b) { return a + b; }
 
 enum { OT_LEAVES = 1024, OT_PARTIALS = 256, OT_GROUPS = 8, OT_LANES = 32 };
@@ -265,6 +274,13 @@ float ot_max_f32(const float *v, int64_t n) {
     for (int k = 0; k < OT_LEAVES; ++k) leaf[k] = -INFINITY;
     for (int64_t e = 0; e < n; ++e) leaf[e % OT_LEAVES] = ot_max2(leaf[e % OT_LEAVES], v[e]);
     return ot_tree(leaf, ot_max2);
+}
+
+float ot_min_f32(const float *v, int64_t n) {
+    float leaf[OT_LEAVES];
+    for (int k = 0; k < OT_LEAVES; ++k) leaf[k] = INFINITY;
+    for (int64_t e = 0; e < n; ++e) leaf[e % OT_LEAVES] = ot_min2(leaf[e % OT_LEAVES], v[e]);
+    return ot_tree(leaf, ot_min2);
 }
 
 /* Sum over the row of a per-element contribution, in OT-1024 order. */

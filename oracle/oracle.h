@@ -38,6 +38,7 @@ void ot_expf_n(const float *x, float *y, int64_t n);
 void ot_logf_n(const float *x, float *y, int64_t n);
 float ot_sum_f32(const float *v, int64_t n);
 float ot_max_f32(const float *v, int64_t n);
+float ot_min_f32(const float *v, int64_t n);
 int ot_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols);
 int ot_rmsnorm_f32(const float *x, const float *w, float *y,
                    int64_t rows, int64_t cols, float eps);

@@ -192,6 +192,9 @@ WORKLOADS = {
     # fused residual norms (x and w, b as the 768x6144 family, residual ~ N(0, 1))
     "add_rmsnorm_768x6144": dict(op="add_rmsnorm", rows=768, cols=6144, seed=2),
     "add_layernorm_768x6144": dict(op="add_layernorm", rows=768, cols=6144, seed=2),
+    # standalone row reductions, x ~ N(0, 1)
+    "row_sum_768x6144": dict(op="row_sum", rows=768, cols=6144, seed=2),
+    "row_minmax_768x6144": dict(op="row_minmax", rows=768, cols=6144, seed=2),
 }
 
 
@@ -205,6 +208,9 @@ def make_inputs(op, rows, cols, seed, var=None, row_offset=False, device="cpu"):
         return xent_inputs(rows, cols, seed, 9.0 if var is None else var, device)
     if op in ("add_rmsnorm", "add_layernorm"):
         return residual_norm_inputs(rows, cols, seed, row_offset, device)
+    if op in ("row_sum", "row_max", "row_min", "row_minmax"):
+        return {"x": normal_plus_row_offset_f32(rows, cols, seed, device=device) if row_offset
+                else normal_f32((rows, cols), seed, TAG_X, 0.0, 1.0 if var is None else var, device)}
     raise ValueError(f"unknown op {op!r}")
 
 

@@ -104,7 +104,7 @@ def test_calls_without_a_gpu_fail_loudly(lib):
 
 
 def test_override_rejects_malformed(lib):
-    p = trlib.tr_plan(op=9)
+    p = trlib.tr_plan(op=10)   # one past the last operator
     assert trlib.tr_plan_override(p) == trlib.TR_ERR_INVALID_ARG
     p = trlib.tr_plan(op=0, kind=17)
     assert trlib.tr_plan_override(p) == trlib.TR_ERR_INVALID_ARG

@@ -151,7 +151,7 @@ def test_host_planner_rejects_malformed_device():
     with pytest.raises(trlib.TrError):
         trlib.tr_plan_select_for(bad, 0, 4, 8, 0, 1)
     with pytest.raises(trlib.TrError):
-        trlib.tr_plan_select_for(DEV, 7, 4, 8, 0, 1)
+        trlib.tr_plan_select_for(DEV, 10, 4, 8, 0, 1)   # one past the last operator
 
 
 def test_fewer_sms_never_gives_a_cheaper_estimate():
@@ -181,3 +181,13 @@ def test_split_plan_limits():
     p.order = 1
     st, _ = trlib.check_plan_for(DEV, p, 4, 100000, 1)
     assert st == trlib.TR_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("op", [trlib.TR_OP_ROW_SUM, trlib.TR_OP_ROW_MAX, trlib.TR_OP_ROW_MIN, trlib.TR_OP_ROW_MINMAX])
+def test_row_reductions_stream_once(op):
+    # standalone reductions: the streaming kind unordered, the streaming OT-1024 ordered
+    for rows, cols in SHAPES:
+        p = select(op, rows, cols)
+        assert p.kind == trlib.TR_PLAN_XENT
+        q = select(op, rows, cols, order=1)
+        assert q.kind == trlib.TR_PLAN_ORDERED and q.vec_slots == 0 and q.grid_ctas == rows
