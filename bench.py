@@ -64,7 +64,10 @@ def alg_bytes(op, rows, cols):
             "add_rmsnorm": 16 * e + 4 * cols, "add_layernorm": 16 * e + 8 * cols,
             # standalone row reductions: x read, one (two) values per row written
             "row_sum": 4 * e + 4 * rows, "row_max": 4 * e + 4 * rows, "row_min": 4 * e + 4 * rows,
-            "row_minmax": 4 * e + 8 * rows}[op]
+            "row_minmax": 4 * e + 8 * rows,
+            # reductions over axis 0: x read, one (two) values per column written
+            "axis_sum": 4 * e + 4 * cols, "axis_max": 4 * e + 4 * cols, "axis_min": 4 * e + 4 * cols,
+            "axis_minmax": 4 * e + 8 * cols}[op]
 
 
 def kernel_source_hash():
@@ -164,12 +167,16 @@ class Launch:
         self.inputs = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(sets - 1)]
         if op == "cross_entropy" or op.startswith("row_"):
             self.outputs = [torch.empty(self.rows, device=device) for _ in range(sets)]
+        elif op.startswith("axis_"):
+            self.outputs = [torch.empty(self.cols, device=device) for _ in range(sets)]
         else:
             self.outputs = [torch.empty_like(base["x"]) for _ in range(sets)]
         # fused residual norms also write h = x + r
         self.h = [torch.empty_like(base["x"]) for _ in range(sets)] if op.startswith("add_") else None
         if op == "row_minmax":  # the maxima (the minima go to outputs)
             self.h = [torch.empty(self.rows, device=device) for _ in range(sets)]
+        if op == "axis_minmax":
+            self.h = [torch.empty(self.cols, device=device) for _ in range(sets)]
         self.bytes = alg_bytes(op, self.rows, self.cols)
         self.key = f"{op}/{self.order}/{self.rows}x{self.cols}"
 
@@ -178,6 +185,11 @@ class Launch:
                        h_out=None if self.h is None else self.h[s])
 
     def plan(self):
+        if self.op.startswith("axis_"):
+            sm = torch.cuda.get_device_properties(0).multi_processor_count
+            splits, tiles = self.tr.axis_launch_shape(self.op[len("axis_"):], 1, self.rows, self.cols, sm)
+            return {"kind": "axis", "splits": splits, "tiles": tiles, "block_threads": 256,
+                    "grid_ctas": splits * tiles}
         return self.tr.plan_for(self.op, self.rows, self.cols, self.order)
 
 
@@ -397,7 +409,9 @@ def oracle_fn(op, order):
                 "add_layernorm": lambda h: oracle.ot_add_layernorm(h["x"], h["r"], h["w"], h["b"], 1e-5),
                 "row_sum": lambda h: oracle.ot_row_sum(h["x"]), "row_max": lambda h: oracle.ot_row_max(h["x"]),
                 "row_min": lambda h: oracle.ot_row_min(h["x"]),
-                "row_minmax": lambda h: (oracle.ot_row_min(h["x"]), oracle.ot_row_max(h["x"]))}[op]
+                "row_minmax": lambda h: (oracle.ot_row_min(h["x"]), oracle.ot_row_max(h["x"])),
+                "axis_sum": lambda h: oracle.ot_axis_sum(h["x"], 0),
+                "axis_minmax": lambda h: (oracle.ot_axis_min(h["x"], 0), oracle.ot_axis_max(h["x"], 0))}[op]
     return {"softmax": lambda h: oracle.softmax(h["x"]),
             "rmsnorm": lambda h: oracle.rmsnorm(h["x"], h["w"], 1e-5),
             "layernorm": lambda h: oracle.layernorm(h["x"], h["w"], h["b"], 1e-5),
@@ -406,7 +420,9 @@ def oracle_fn(op, order):
             "add_layernorm": lambda h: oracle.add_layernorm(h["x"], h["r"], h["w"], h["b"], 1e-5),
             "row_sum": lambda h: oracle.row_sum(h["x"]), "row_max": lambda h: oracle.row_max(h["x"]),
             "row_min": lambda h: oracle.row_min(h["x"]),
-            "row_minmax": lambda h: (oracle.row_min(h["x"]), oracle.row_max(h["x"]))}[op]
+            "row_minmax": lambda h: (oracle.row_min(h["x"]), oracle.row_max(h["x"])),
+            "axis_sum": lambda h: oracle.axis_sum(h["x"], 0),
+            "axis_minmax": lambda h: (oracle.axis_min(h["x"], 0), oracle.axis_max(h["x"], 0))}[op]
 
 
 def host_sample(op, workload, rows):

@@ -58,6 +58,8 @@ OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LA
        "cross_entropy": TR_OP_CROSS_ENTROPY, "add_rmsnorm": TR_OP_ADD_RMSNORM, "add_layernorm": TR_OP_ADD_LAYERNORM,
        "row_sum": TR_OP_ROW_SUM, "row_max": TR_OP_ROW_MAX, "row_min": TR_OP_ROW_MIN, "row_minmax": TR_OP_ROW_MINMAX}
 REDUCE_OPS = ("row_sum", "row_max", "row_min", "row_minmax")
+# reductions over axis 0 of a 2-D tensor (one value per column)
+AXIS_OPS = ("axis_sum", "axis_max", "axis_min", "axis_minmax")
 ORDERS = {"unordered": TR_ORDER_UNORDERED_TREE, "ordered": TR_ORDER_ORDERED_TREE}
 
 
@@ -106,6 +108,11 @@ SIGNATURES = {
     "tr_row_max_f32": ([_P, _P, _I64, _I64, _I32, _P], _I32),
     "tr_row_min_f32": ([_P, _P, _I64, _I64, _I32, _P], _I32),
     "tr_row_minmax_f32": ([_P, _P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_axis_sum_f32": ([_P, _P, _I64, _I64, _I64, _I32, _P], _I32),
+    "tr_axis_max_f32": ([_P, _P, _I64, _I64, _I64, _I32, _P], _I32),
+    "tr_axis_min_f32": ([_P, _P, _I64, _I64, _I64, _I32, _P], _I32),
+    "tr_axis_minmax_f32": ([_P, _P, _P, _I64, _I64, _I64, _I32, _P], _I32),
+    "tr_axis_launch_shape": ([_I32, _I32, _I64, _I64, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I64)], _I32),
     "tr_add_layernorm_f32": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
     "tr_plan_describe": ([_I32, _I64, _I64, _I32, ctypes.POINTER(tr_plan)], _I32),
     "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
@@ -396,6 +403,47 @@ def row_reduce(x, op="row_sum", out=None, out2=None, order="unordered", stream=N
     return y
 
 
+def axis_launch_shape(op, outer, extent, inner, sm_count=152):
+    """(splits, tiles) of an axis reduction on a device with `sm_count` SMs (host only)."""
+    sp, tl = ctypes.c_int32(0), ctypes.c_int64(0)
+    code = OPS["row_" + op] if isinstance(op, str) else op
+    _check(load().tr_axis_launch_shape(sm_count, code, outer, extent, inner, ctypes.byref(sp), ctypes.byref(tl)),
+           "axis_launch_shape")
+    return sp.value, tl.value
+
+
+def axis_reduce(x, dim=0, op="sum", out=None, out2=None, order="unordered", stream=None):
+    """Sum, max, min, or min and max together, of a contiguous CUDA float32
+    tensor over dimension `dim` (any position). The result has x's shape
+    without `dim`; "minmax" returns (minima, maxima)."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous CUDA float32 tensor")
+    if x.dim() < 1:
+        raise ValueError("x needs at least one dimension")
+    d = dim % x.dim()
+    shape = list(x.shape)
+    outer = 1
+    for n in shape[:d]:
+        outer *= n
+    inner = 1
+    for n in shape[d + 1:]:
+        inner *= n
+    extent = shape[d]
+    rshape = shape[:d] + shape[d + 1:]
+    y = torch.empty(rshape, device=x.device, dtype=torch.float32) if out is None else out
+    lib = load()
+    if op == "minmax":
+        y2 = torch.empty(rshape, device=x.device, dtype=torch.float32) if out2 is None else out2
+        _check(lib.tr_axis_minmax_f32(x.data_ptr(), y.data_ptr(), y2.data_ptr(), outer, extent, inner,
+                                      _order(order), _stream_handle(stream)), "axis_minmax")
+        return y, y2
+    fn = {"sum": lib.tr_axis_sum_f32, "max": lib.tr_axis_max_f32, "min": lib.tr_axis_min_f32}[op]
+    _check(fn(x.data_ptr(), y.data_ptr(), outer, extent, inner, _order(order), _stream_handle(stream)),
+           "axis_" + op)
+    return y
+
+
 def cross_entropy(logits, labels, out=None, order="unordered", stream=None):
     """Per-row loss log(sum exp(x)) - x[label] (label outside [0, cols) selects 0)."""
     import torch
@@ -424,6 +472,8 @@ def run_op(op, inputs, out=None, order="unordered", eps=1e-5, stream=None, h_out
         return layernorm(inputs["x"], inputs.get("w"), inputs.get("b"), eps, out=out, order=order, stream=stream)
     if op in REDUCE_OPS:
         return row_reduce(inputs["x"], op, out=out, out2=h_out, order=order, stream=stream)
+    if op in AXIS_OPS:
+        return axis_reduce(inputs["x"], 0, op[len("axis_"):], out=out, out2=h_out, order=order, stream=stream)
     if op == "add_rmsnorm":
         return add_rmsnorm(inputs["x"], inputs["r"], inputs.get("w"), eps, out=out, h_out=h_out, order=order,
                            stream=stream)

@@ -492,6 +492,94 @@ tr_status tr_row_minmax_f32(const float* x, float* out_min, float* out_max, int6
     return reduce_call(TR_OP_ROW_MINMAX, x, out_min, out_max, rows, cols, order, stream);
 }
 
+// Splits of the reduced axis: double them while the column tiles alone give
+// fewer than four CTAs per SM and every split keeps at least 64 rows, within
+// the workspace's partial and ticket capacity.
+int axis_splits(int64_t tiles, int64_t extent, int values, int sm_count) {
+    const int64_t target = 4 * static_cast<int64_t>(sm_count);
+    int S = 1;
+    while (S < kAxisMaxSplits && tiles * S < target && extent >= 128 * static_cast<int64_t>(S)) S *= 2;
+    while (S > 1 && (tiles > kAxisMaxTickets || tiles * S * kAxisCols * values > kAxisMaxPartFloats)) S /= 2;
+    return S;
+}
+
+static tr_status axis_call(int op, const float* x, float* out, float* out2, int64_t outer, int64_t extent,
+                           int64_t inner, tr_order order, cudaStream_t stream) {
+    if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE)
+        return fail(TR_ERR_INVALID_ARG, "order must be TR_ORDER_UNORDERED_TREE or TR_ORDER_ORDERED_TREE");
+    if (outer < 0 || extent < 1 || inner < 1)
+        return fail(TR_ERR_INVALID_ARG, "need outer >= 0, extent >= 1 and inner >= 1");
+    if (outer == 0) return TR_OK;
+    if (extent > INT64_MAX / 4 / inner || outer > INT64_MAX / 4 / inner / extent)
+        return fail(TR_ERR_INVALID_ARG, "outer * extent * inner too large");
+    const int64_t ncols = outer * inner;
+    const int64_t tiles = (ncols + kAxisCols - 1) / kAxisCols;
+    if (tiles > 0x7fffffffLL) return fail(TR_ERR_UNSUPPORTED, "more output columns than one launch covers");
+    if (!x || !out || (op == TR_OP_ROW_MINMAX && !out2))
+        return fail(TR_ERR_INVALID_ARG, "x and the outputs must not be null");
+    if (misaligned(x, 4) || misaligned(out, 4) || misaligned(out2, 4))
+        return fail(TR_ERR_INVALID_ARG, "x and the outputs must be 4-byte aligned");
+    const size_t n = static_cast<size_t>(outer) * static_cast<size_t>(extent) * static_cast<size_t>(inner) * 4;
+    const size_t no = static_cast<size_t>(ncols) * 4;
+    if (overlaps(x, n, out, no) || overlaps(x, n, out2, no) || overlaps(out, no, out2, no))
+        return fail(TR_ERR_INVALID_ARG, "an output overlaps the input or the other output");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const int values = op == TR_OP_ROW_MINMAX ? 2 : 1;
+    AxisArgs a{x, out, out2, extent, inner, ncols, nullptr, nullptr};
+    int S = 1;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* st = nullptr;
+        tr_status s = device_state(dev, &st);
+        if (s != TR_OK) return s;
+        S = axis_splits(tiles, extent, values, st->desc.sm_count);
+        if (S > 1) {
+            void* ws = nullptr;
+            s = split_workspace(*st, stream, &ws);
+            if (s != TR_OK) return s;
+            a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kAxisPartOffset);
+            a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kAxisTicketOffset);
+        }
+    }
+    e = launch_axis(op, order == TR_ORDER_ORDERED_TREE, a, tiles, S, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "axis reduction launch");
+    return TR_OK;
+}
+
+tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, int64_t outer, int64_t extent, int64_t inner,
+                               int32_t* splits, int64_t* tiles) {
+    if (!splits || !tiles) return fail(TR_ERR_INVALID_ARG, "splits and tiles must not be null");
+    if (sm_count < 1) return fail(TR_ERR_INVALID_ARG, "sm_count must be >= 1");
+    if (op < TR_OP_ROW_SUM || op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "op must be a row reduction");
+    if (outer < 0 || extent < 1 || inner < 1) return fail(TR_ERR_INVALID_ARG, "need outer >= 0, extent >= 1, inner >= 1");
+    if (outer > 0 && outer > INT64_MAX / inner) return fail(TR_ERR_INVALID_ARG, "outer * inner too large");
+    *tiles = (outer * inner + kAxisCols - 1) / kAxisCols;
+    *splits = *tiles > 0 ? axis_splits(*tiles, extent, op == TR_OP_ROW_MINMAX ? 2 : 1, sm_count) : 1;
+    return TR_OK;
+}
+
+tr_status tr_axis_sum_f32(const float* x, float* out, int64_t outer, int64_t extent, int64_t inner, tr_order order,
+                          cudaStream_t stream) {
+    return axis_call(TR_OP_ROW_SUM, x, out, nullptr, outer, extent, inner, order, stream);
+}
+
+tr_status tr_axis_max_f32(const float* x, float* out, int64_t outer, int64_t extent, int64_t inner, tr_order order,
+                          cudaStream_t stream) {
+    return axis_call(TR_OP_ROW_MAX, x, out, nullptr, outer, extent, inner, order, stream);
+}
+
+tr_status tr_axis_min_f32(const float* x, float* out, int64_t outer, int64_t extent, int64_t inner, tr_order order,
+                          cudaStream_t stream) {
+    return axis_call(TR_OP_ROW_MIN, x, out, nullptr, outer, extent, inner, order, stream);
+}
+
+tr_status tr_axis_minmax_f32(const float* x, float* out_min, float* out_max, int64_t outer, int64_t extent,
+                             int64_t inner, tr_order order, cudaStream_t stream) {
+    return axis_call(TR_OP_ROW_MINMAX, x, out_min, out_max, outer, extent, inner, order, stream);
+}
+
 tr_status tr_add_rmsnorm_f32(const float* x, const float* residual, const float* w, float* y, float* h,
                              int64_t rows, int64_t cols, float eps, tr_order order, cudaStream_t stream) {
     return residual_call(TR_OP_ADD_RMSNORM, x, residual, w, nullptr, y, h, rows, cols, eps, order, stream);

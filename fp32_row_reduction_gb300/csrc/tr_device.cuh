@@ -35,6 +35,28 @@ enum Op : int {
     OP_RMINMAX = 7
 };
 
+// Canonical max / min of the ordered standalone reductions, whose result is
+// the output itself: NaN in the first operand wins, then NaN in the second,
+// then the larger (smaller) value, +0 over -0 for the max and -0 over +0 for
+// the min. Selects only, so a NaN keeps its payload; the predicates combine
+// with bitwise operators, so no branch is taken per element.
+__device__ __forceinline__ float cmax2(float a, float b) {
+    const bool a_wins = (a != a) | (!(b != b) & ((a > b) | ((a == b) & (__float_as_int(a) >= 0))));
+    return a_wins ? a : b;
+}
+__device__ __forceinline__ float cmin2(float a, float b) {
+    const bool a_wins = (a != a) | (!(b != b) & ((a < b) | ((a == b) & (__float_as_int(a) < 0))));
+    return a_wins ? a : b;
+}
+// Integer key of a float whose signed order is the total order of the floats
+// with -0 below +0 (negative values have their magnitude bits flipped); NaNs
+// map above key(+inf) or below key(-inf). The map is its own inverse.
+__device__ __forceinline__ int order_key(float x) {
+    const int b = __float_as_int(x);
+    return b ^ ((b >> 31) & 0x7fffffff);
+}
+__device__ __forceinline__ float from_order_key(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7fffffff)); }
+
 // 2^t with the SFU (ex2.approx): max relative error ~2^-22 on [-126, 128];
 // results below 2^-126 flush to zero, which the unordered tolerance absorbs.
 __device__ __forceinline__ float ex2(float t) {

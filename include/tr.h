@@ -197,6 +197,34 @@ tr_status tr_row_min_f32(const float* x, float* out, int64_t rows, int64_t cols,
 tr_status tr_row_minmax_f32(const float* x, float* out_min, float* out_max, int64_t rows, int64_t cols,
                             tr_order order, cudaStream_t stream);
 
+/* ---- reductions over a non-last axis --------------------------------------
+ * "TIRx Metal reduction lowering", Reductions inside composed groups: the
+ * reduced axis need not be the last memory dimension. x is a contiguous
+ * [outer, extent, inner] array (device memory, row major); the result has
+ * outer * inner floats, out[o * inner + i] = reduce over r of x[o, r, i]
+ * (min and max together: minima to out_min, maxima to out_max). extent >= 1,
+ * inner >= 1, outer >= 0 (0: nothing to do). Policies as for the row
+ * reductions: unordered sums in any order, max / min skip NaN elements;
+ * ordered applies the OT-1024 tree to each column vector x[o, :, i], giving
+ * the bits tr_row_*_f32 gives for that vector. Outputs may not overlap x or
+ * each other. A launch that splits the reduced axis over several CTAs uses the
+ * stream's library workspace (allocated on the first such call on the stream,
+ * which therefore must not be captured into a graph). */
+tr_status tr_axis_sum_f32(const float* x, float* out, int64_t outer, int64_t extent, int64_t inner, tr_order order,
+                          cudaStream_t stream);
+tr_status tr_axis_max_f32(const float* x, float* out, int64_t outer, int64_t extent, int64_t inner, tr_order order,
+                          cudaStream_t stream);
+tr_status tr_axis_min_f32(const float* x, float* out, int64_t outer, int64_t extent, int64_t inner, tr_order order,
+                          cudaStream_t stream);
+tr_status tr_axis_minmax_f32(const float* x, float* out_min, float* out_max, int64_t outer, int64_t extent,
+                             int64_t inner, tr_order order, cudaStream_t stream);
+/* Host only: the launch an axis reduction gets on a device with `sm_count`
+ * SMs: `tiles` CTAs of 32 output columns, and `splits` CTAs per tile along the
+ * reduced axis (a power of two, at most 32). op is one of TR_OP_ROW_SUM ..
+ * TR_OP_ROW_MINMAX. */
+tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, int64_t outer, int64_t extent, int64_t inner,
+                               int32_t* splits, int64_t* tiles);
+
 /* ---- no-allocation entry point ----------------------------------------- */
 
 /* Softmax, RMSNorm or LayerNorm of few long rows with no device allocation on

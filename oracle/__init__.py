@@ -254,6 +254,45 @@ def ot_row_min(x):
     return np.array([ot_min(r) for r in _f32(x)], dtype=np.float32)
 
 
+# ---- reductions over any axis ("TIRx Metal reduction lowering", Reductions
+# inside composed groups: the reduced axis need not be the last memory
+# dimension): the same definitions applied to the vectors along `dim`.
+
+def _columns(x, dim):
+    """x with `dim` moved last, as a 2-D float32 array of vectors (and the result shape)."""
+    a = np.moveaxis(_f32(x), dim, -1)
+    return np.ascontiguousarray(a.reshape(-1, a.shape[-1])), a.shape[:-1]
+
+
+def axis_sum(x, dim=0):
+    """Sum over `dim` in FP64 (float64 result)."""
+    return _f32(x).astype(np.float64).sum(axis=dim)
+
+
+def axis_max(x, dim=0):
+    return _f32(x).max(axis=dim)
+
+
+def axis_min(x, dim=0):
+    return _f32(x).min(axis=dim)
+
+
+def ot_axis_sum(x, dim=0):
+    """Ordered-policy (OT-1024) sum of every vector along `dim`."""
+    v, shape = _columns(x, dim)
+    return ot_row_sum(v).reshape(shape)
+
+
+def ot_axis_max(x, dim=0):
+    v, shape = _columns(x, dim)
+    return ot_row_max(v).reshape(shape)
+
+
+def ot_axis_min(x, dim=0):
+    v, shape = _columns(x, dim)
+    return ot_row_min(v).reshape(shape)
+
+
 def ot_expf(x):
     return np.float32(lib().ot_expf(float(x)))
 

@@ -195,6 +195,9 @@ WORKLOADS = {
     # standalone row reductions, x ~ N(0, 1)
     "row_sum_768x6144": dict(op="row_sum", rows=768, cols=6144, seed=2),
     "row_minmax_768x6144": dict(op="row_minmax", rows=768, cols=6144, seed=2),
+    # reductions over axis 0 (one value per column), x ~ N(0, 1)
+    "axis_sum_768x6144": dict(op="axis_sum", rows=768, cols=6144, seed=2),
+    "axis_minmax_768x6144": dict(op="axis_minmax", rows=768, cols=6144, seed=2),
 }
 
 
@@ -208,7 +211,7 @@ def make_inputs(op, rows, cols, seed, var=None, row_offset=False, device="cpu"):
         return xent_inputs(rows, cols, seed, 9.0 if var is None else var, device)
     if op in ("add_rmsnorm", "add_layernorm"):
         return residual_norm_inputs(rows, cols, seed, row_offset, device)
-    if op in ("row_sum", "row_max", "row_min", "row_minmax"):
+    if op in ("row_sum", "row_max", "row_min", "row_minmax", "axis_sum", "axis_max", "axis_min", "axis_minmax"):
         return {"x": normal_plus_row_offset_f32(rows, cols, seed, device=device) if row_offset
                 else normal_f32((rows, cols), seed, TAG_X, 0.0, 1.0 if var is None else var, device)}
     raise ValueError(f"unknown op {op!r}")
