@@ -187,7 +187,7 @@ class Launch:
     def plan(self):
         if self.op.startswith("axis_"):
             sm = torch.cuda.get_device_properties(0).multi_processor_count
-            splits, tiles = self.tr.axis_launch_shape(self.op[len("axis_"):], 1, self.rows, self.cols, sm)
+            splits, tiles = self.tr.axis_launch_shape(self.op[len("axis_"):], 1, self.rows, self.cols, sm, self.order)
             return {"kind": "axis", "splits": splits, "tiles": tiles, "block_threads": 256,
                     "grid_ctas": splits * tiles}
         return self.tr.plan_for(self.op, self.rows, self.cols, self.order)

@@ -112,7 +112,8 @@ SIGNATURES = {
     "tr_axis_max_f32": ([_P, _P, _I64, _I64, _I64, _I32, _P], _I32),
     "tr_axis_min_f32": ([_P, _P, _I64, _I64, _I64, _I32, _P], _I32),
     "tr_axis_minmax_f32": ([_P, _P, _P, _I64, _I64, _I64, _I32, _P], _I32),
-    "tr_axis_launch_shape": ([_I32, _I32, _I64, _I64, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I64)], _I32),
+    "tr_axis_launch_shape": ([_I32, _I32, _I32, _I64, _I64, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I64)],
+                             _I32),
     "tr_add_layernorm_f32": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
     "tr_plan_describe": ([_I32, _I64, _I64, _I32, ctypes.POINTER(tr_plan)], _I32),
     "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
@@ -403,12 +404,12 @@ def row_reduce(x, op="row_sum", out=None, out2=None, order="unordered", stream=N
     return y
 
 
-def axis_launch_shape(op, outer, extent, inner, sm_count=152):
-    """(splits, tiles) of an axis reduction on a device with `sm_count` SMs (host only)."""
+def axis_launch_shape(op, outer, extent, inner, sm_count=152, order="unordered"):
+    """(splits, tiles) of an axis reduction of an aligned x on a device with `sm_count` SMs (host only)."""
     sp, tl = ctypes.c_int32(0), ctypes.c_int64(0)
     code = OPS["row_" + op] if isinstance(op, str) else op
-    _check(load().tr_axis_launch_shape(sm_count, code, outer, extent, inner, ctypes.byref(sp), ctypes.byref(tl)),
-           "axis_launch_shape")
+    _check(load().tr_axis_launch_shape(sm_count, code, _order(order), outer, extent, inner, ctypes.byref(sp),
+                                       ctypes.byref(tl)), "axis_launch_shape")
     return sp.value, tl.value
 
 

@@ -492,15 +492,27 @@ tr_status tr_row_minmax_f32(const float* x, float* out_min, float* out_max, int6
     return reduce_call(TR_OP_ROW_MINMAX, x, out_min, out_max, rows, cols, order, stream);
 }
 
-// Splits of the reduced axis: double them while the column tiles alone give
-// fewer than four CTAs per SM and every split keeps at least 64 rows, within
-// the workspace's partial and ticket capacity.
-int axis_splits(int64_t tiles, int64_t extent, int values, int sm_count) {
-    const int64_t target = 4 * static_cast<int64_t>(sm_count);
+// Splits of the reduced axis: the most (a power of two, at most 32) that keep
+// the launch within one wave of the CTAs per SM its kernel is built for, with
+// at least 32 rows per split, within the workspace's partial and ticket
+// capacity.
+int axis_splits(int64_t tiles, int64_t extent, int values, int tile_cols, int ctas_per_sm, int sm_count) {
+    const int64_t wave = static_cast<int64_t>(ctas_per_sm) * sm_count;
     int S = 1;
-    while (S < kAxisMaxSplits && tiles * S < target && extent >= 128 * static_cast<int64_t>(S)) S *= 2;
-    while (S > 1 && (tiles > kAxisMaxTickets || tiles * S * kAxisCols * values > kAxisMaxPartFloats)) S /= 2;
+    while (S < kAxisMaxSplits && tiles * 2 * S <= wave && extent >= 64 * static_cast<int64_t>(S)) S *= 2;
+    while (S > 1 && (tiles > kAxisMaxTickets || tiles * S * tile_cols * values > kAxisMaxPartFloats)) S /= 2;
     return S;
+}
+
+// Columns per thread: four when every column quad is one aligned float4 of a
+// row, except for the ordered sum, whose tree keeps one column per thread.
+int axis_vec(int op, int order, int64_t inner, bool x_aligned16) {
+    if (op == TR_OP_ROW_SUM && order == TR_ORDER_ORDERED_TREE) return 1;
+    return (inner % 4 == 0 && x_aligned16) ? 4 : 1;
+}
+
+int axis_ctas_per_sm(int op, int order) {
+    return (op == TR_OP_ROW_SUM && order == TR_ORDER_ORDERED_TREE) ? kAxisCtasTree : kAxisCtasFree;
 }
 
 static tr_status axis_call(int op, const float* x, float* out, float* out2, int64_t outer, int64_t extent,
@@ -513,7 +525,8 @@ static tr_status axis_call(int op, const float* x, float* out, float* out2, int6
     if (extent > INT64_MAX / 4 / inner || outer > INT64_MAX / 4 / inner / extent)
         return fail(TR_ERR_INVALID_ARG, "outer * extent * inner too large");
     const int64_t ncols = outer * inner;
-    const int64_t tiles = (ncols + kAxisCols - 1) / kAxisCols;
+    const int vec = axis_vec(op, order, inner, !misaligned(x, 16));
+    const int64_t tiles = (ncols + kAxisCols * vec - 1) / (kAxisCols * vec);
     if (tiles > 0x7fffffffLL) return fail(TR_ERR_UNSUPPORTED, "more output columns than one launch covers");
     if (!x || !out || (op == TR_OP_ROW_MINMAX && !out2))
         return fail(TR_ERR_INVALID_ARG, "x and the outputs must not be null");
@@ -526,7 +539,7 @@ static tr_status axis_call(int op, const float* x, float* out, float* out2, int6
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const int values = op == TR_OP_ROW_MINMAX ? 2 : 1;
+    const int values = op == TR_OP_ROW_SUM ? 1 : 2;  // ordered max and min keep two keys per column
     AxisArgs a{x, out, out2, extent, inner, ncols, nullptr, nullptr};
     int S = 1;
     {
@@ -534,7 +547,7 @@ static tr_status axis_call(int op, const float* x, float* out, float* out2, int6
         DeviceState* st = nullptr;
         tr_status s = device_state(dev, &st);
         if (s != TR_OK) return s;
-        S = axis_splits(tiles, extent, values, st->desc.sm_count);
+        S = axis_splits(tiles, extent, values, kAxisCols * vec, axis_ctas_per_sm(op, order), st->desc.sm_count);
         if (S > 1) {
             void* ws = nullptr;
             s = split_workspace(*st, stream, &ws);
@@ -543,20 +556,25 @@ static tr_status axis_call(int op, const float* x, float* out, float* out2, int6
             a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kAxisTicketOffset);
         }
     }
-    e = launch_axis(op, order == TR_ORDER_ORDERED_TREE, a, tiles, S, stream);
+    e = launch_axis(op, order == TR_ORDER_ORDERED_TREE, a, vec, tiles, S, stream);
     if (e != cudaSuccess) return cuda_fail(e, "axis reduction launch");
     return TR_OK;
 }
 
-tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, int64_t outer, int64_t extent, int64_t inner,
-                               int32_t* splits, int64_t* tiles) {
+tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, tr_order order, int64_t outer, int64_t extent,
+                               int64_t inner, int32_t* splits, int64_t* tiles) {
     if (!splits || !tiles) return fail(TR_ERR_INVALID_ARG, "splits and tiles must not be null");
     if (sm_count < 1) return fail(TR_ERR_INVALID_ARG, "sm_count must be >= 1");
     if (op < TR_OP_ROW_SUM || op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "op must be a row reduction");
+    if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE)
+        return fail(TR_ERR_INVALID_ARG, "order must be TR_ORDER_UNORDERED_TREE or TR_ORDER_ORDERED_TREE");
     if (outer < 0 || extent < 1 || inner < 1) return fail(TR_ERR_INVALID_ARG, "need outer >= 0, extent >= 1, inner >= 1");
     if (outer > 0 && outer > INT64_MAX / inner) return fail(TR_ERR_INVALID_ARG, "outer * inner too large");
-    *tiles = (outer * inner + kAxisCols - 1) / kAxisCols;
-    *splits = *tiles > 0 ? axis_splits(*tiles, extent, op == TR_OP_ROW_MINMAX ? 2 : 1, sm_count) : 1;
+    const int vec = axis_vec(op, order, inner, true);
+    *tiles = (outer * inner + kAxisCols * vec - 1) / (kAxisCols * vec);
+    *splits = *tiles > 0 ? axis_splits(*tiles, extent, op == TR_OP_ROW_SUM ? 1 : 2, kAxisCols * vec,
+                                       axis_ctas_per_sm(op, order), sm_count)
+                         : 1;
     return TR_OK;
 }
 

@@ -52,13 +52,16 @@ constexpr int kSplitMaxCtas = 32;
 constexpr int kSplitMaxParts = 4096;
 constexpr int kSplitMaxRows = 2048;
 // Axis reductions (a non-last axis of [outer, extent, inner]): 256 threads
-// per CTA over 32 output columns; a launch with splits > 1 keeps its per-CTA
+// per CTA over 32 output columns (32 column quads when inner is a multiple of
+// 4 and x is 16-byte aligned); a launch with splits > 1 keeps its per-CTA
 // partials and per-tile tickets after the split-plan region of the workspace.
 constexpr int kAxisThreads = 256;
 constexpr int kAxisCols = 32;
 constexpr int kAxisMaxSplits = 32;
-constexpr int kAxisMaxTickets = 1024;
-constexpr int kAxisMaxPartFloats = 131072;
+constexpr int kAxisCtasFree = 4;  // resident CTAs per SM the free and key kernels are built for
+constexpr int kAxisCtasTree = 3;  // the same for the ordered sum
+constexpr int kAxisMaxTickets = 2048;
+constexpr int kAxisMaxPartFloats = 1 << 20;
 constexpr size_t kAxisPartOffset = kSplitMaxParts * 16 + 2 * kSplitMaxRows * sizeof(unsigned);
 constexpr size_t kAxisTicketOffset = kAxisPartOffset + kAxisMaxPartFloats * sizeof(float);
 constexpr size_t kSplitWorkspaceBytes = kAxisTicketOffset + kAxisMaxTickets * sizeof(unsigned);
@@ -70,7 +73,7 @@ struct AxisArgs {
     int64_t extent;   // length of the reduced axis
     int64_t inner;    // elements after the reduced axis
     int64_t ncols;    // outer * inner output columns
-    float* part;      // splits > 1: per-CTA partials (tiles * splits * 32 * values)
+    float* part;      // splits > 1: per-CTA partials (tiles * splits * values * columns of a tile)
     unsigned* ticket; // splits > 1: per-tile arrival tickets (zero between launches)
 };
 
@@ -78,8 +81,10 @@ struct AxisArgs {
 // body plus one partial 16-byte chunk on each side.
 inline int staged_slot_floats(int64_t cols) { return static_cast<int>((cols + 3) / 4 * 4 + 8); }
 
-// Launch the axis reduction `op` (TR_OP_ROW_SUM .. TR_OP_ROW_MINMAX) over (tiles, splits) CTAs.
-cudaError_t launch_axis(int op, bool ordered, const AxisArgs& a, int64_t tiles, int splits, cudaStream_t stream);
+// Launch the axis reduction `op` (TR_OP_ROW_SUM .. TR_OP_ROW_MINMAX) over (tiles, splits) CTAs,
+// each thread on `vec` (1 or 4) adjacent columns.
+cudaError_t launch_axis(int op, bool ordered, const AxisArgs& a, int vec, int64_t tiles, int splits,
+                        cudaStream_t stream);
 
 // Set the calling thread's last-error text to "what: detail" (tr_last_error_message).
 void set_last_error(const char* what, const char* detail);

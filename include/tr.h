@@ -218,12 +218,13 @@ tr_status tr_axis_min_f32(const float* x, float* out, int64_t outer, int64_t ext
                           cudaStream_t stream);
 tr_status tr_axis_minmax_f32(const float* x, float* out_min, float* out_max, int64_t outer, int64_t extent,
                              int64_t inner, tr_order order, cudaStream_t stream);
-/* Host only: the launch an axis reduction gets on a device with `sm_count`
- * SMs: `tiles` CTAs of 32 output columns, and `splits` CTAs per tile along the
- * reduced axis (a power of two, at most 32). op is one of TR_OP_ROW_SUM ..
- * TR_OP_ROW_MINMAX. */
-tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, int64_t outer, int64_t extent, int64_t inner,
-                               int32_t* splits, int64_t* tiles);
+/* Host only: the launch an axis reduction of a 16-byte-aligned x gets on a
+ * device with `sm_count` SMs: `tiles` CTAs of 32 output columns (128 when
+ * inner is a multiple of 4, except for the ordered sum), and `splits` CTAs per
+ * tile along the reduced axis (a power of two, at most 32, sized to one wave).
+ * op is one of TR_OP_ROW_SUM .. TR_OP_ROW_MINMAX. */
+tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, tr_order order, int64_t outer, int64_t extent,
+                               int64_t inner, int32_t* splits, int64_t* tiles);
 
 /* ---- no-allocation entry point ----------------------------------------- */
 

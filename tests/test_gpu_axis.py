@@ -152,3 +152,15 @@ def test_full_size_768x6144_column_sums():
     for op in ("sum", "minmax"):
         for order in ("unordered", "ordered"):
             check(x, op, order, run(x, op, order))
+
+
+@pytest.mark.parametrize("off", [1, 2, 3])
+def test_unaligned_x_takes_the_scalar_columns(off):
+    outer, extent, inner = 3, 1500, 64
+    x0 = make(outer, extent, inner, seed=off)
+    big = torch.empty(x0.numel() + 8, device=DEV)
+    x = big[off:off + x0.numel()].view(outer, extent, inner)
+    x.copy_(x0)
+    for op in ("sum", "minmax"):
+        for order in ("unordered", "ordered"):
+            check(x, op, order, run(x, op, order))
