@@ -70,13 +70,20 @@ def alg_bytes(op, rows, cols):
             "axis_minmax": 4 * e + 8 * cols}[op]
 
 
+# The sources that define, select or launch the default step's kernels (the
+# unordered row kernels and the ordered tree of softmax, RMSNorm, LayerNorm):
+# a committed traffic record counts only while none of them has changed.
+STEP_SOURCES = ["k_softmax.cu", "k_rmsnorm.cu", "k_layernorm.cu", "k_ordered.cu", "tr_dispatch.cuh",
+                "tr_split_kernels.cuh", "tr_row_kernels.cuh", "tr_device.cuh", "tr_internal.h", "tr_api.cu",
+                "tr_plan.cpp", "tr_plan.h"]
+
+
 def kernel_source_hash():
     csrc = os.path.join(ROOT, "fp32_row_reduction_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in sorted(STEP_SOURCES):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
