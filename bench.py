@@ -74,7 +74,7 @@ def alg_bytes(op, rows, cols):
 # unordered row kernels and the ordered tree of softmax, RMSNorm, LayerNorm):
 # a committed traffic record counts only while none of them has changed.
 STEP_SOURCES = ["k_softmax.cu", "k_rmsnorm.cu", "k_layernorm.cu", "k_ordered.cu", "tr_dispatch.cuh",
-                "tr_split_kernels.cuh", "tr_row_kernels.cuh", "tr_device.cuh", "tr_internal.h", "tr_api.cu",
+                "tr_split_kernels.cuh", "tr_row_kernels.cuh", "tr_device.cuh", "tr_internal.h", "tr_api.cu", "tr_ot.cuh",
                 "tr_plan.cpp", "tr_plan.h"]
 
 

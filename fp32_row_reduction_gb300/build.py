@@ -29,7 +29,7 @@ SOURCES = ["tr_api.cu", "tr_plan.cpp", "k_softmax.cu", "k_rmsnorm.cu", "k_layern
            "k_ordered.cu", "tr_noalloc.cu", "k_add_rmsnorm.cu", "k_add_layernorm.cu",
            "k_reduce.cu", "k_axis.cu"]
 HEADERS = ["tr_device.cuh", "tr_row_kernels.cuh", "tr_split_kernels.cuh", "tr_dispatch.cuh", "tr_internal.h",
-           "tr_plan.h"]
+           "tr_plan.h", "tr_ot.cuh"]
 
 
 def _nvcc() -> str:

@@ -5,8 +5,8 @@ baseline may import this package.  The product path (the CUDA library and its
 Python binding) never imports it and shares no code with it.
 
 Wraps ``oracle.c`` (plain serial C): the FP64 definitions of softmax, RMSNorm,
-LayerNorm and cross-entropy, and the bit-exact FP32 emulation of the ordered
-fixed-tree policy (OT-1024) with its own exp/log.  Arrays are numpy; inputs
+LayerNorm and cross-entropy and of their gradients, and the bit-exact FP32
+emulation of the ordered fixed-tree policy (OT-1024) with its own exp/log.  Arrays are numpy; inputs
 are float32 (labels int64) row-major, FP64 outputs are returned as float64 and
 emulated outputs as float32.
 """
@@ -60,6 +60,14 @@ def lib():
             "ot_rmsnorm_f32": [f32p, f32p, f32p, i64, i64, ctypes.c_float],
             "ot_layernorm_f32": [f32p, f32p, f32p, f32p, i64, i64, ctypes.c_float],
             "ot_cross_entropy_f32": [f32p, i64p, f32p, i64, i64],
+            "oracle_softmax_bwd_f64": [f32p, f32p, f64p, i64, i64],
+            "oracle_cross_entropy_bwd_f64": [f32p, i64p, f32p, f64p, i64, i64],
+            "oracle_rmsnorm_bwd_f64": [f32p, f32p, f32p, f64p, f64p, i64, i64, ctypes.c_float],
+            "oracle_layernorm_bwd_f64": [f32p, f32p, f32p, f64p, f64p, f64p, i64, i64, ctypes.c_float],
+            "ot_softmax_bwd_f32": [f32p, f32p, f32p, i64, i64],
+            "ot_cross_entropy_bwd_f32": [f32p, i64p, f32p, f32p, i64, i64],
+            "ot_rmsnorm_bwd_f32": [f32p, f32p, f32p, f32p, f32p, i64, i64, ctypes.c_float],
+            "ot_layernorm_bwd_f32": [f32p, f32p, f32p, f32p, f32p, f32p, i64, i64, ctypes.c_float],
             "ot_sum_f32": [f32p, i64],
             "ot_max_f32": [f32p, i64],
             "ot_min_f32": [f32p, i64],
@@ -291,6 +299,98 @@ def ot_axis_max(x, dim=0):
 def ot_axis_min(x, dim=0):
     v, shape = _columns(x, dim)
     return ot_row_min(v).reshape(shape)
+
+
+# ---- backward passes (the gradients of the four operators; not on the pages,
+# the next rows of the same row-reduction family). FP64 definitions return
+# float64 arrays, the OT-1024 emulations float32.
+
+def softmax_backward(y, dy):
+    y, dy = _f32(y), _f32(dy)
+    r, c = y.shape
+    dx = np.empty((r, c), np.float64)
+    _rc(lib().oracle_softmax_bwd_f64(_ptr(y, ctypes.c_float), _ptr(dy, ctypes.c_float), _ptr(dx, ctypes.c_double), r, c))
+    return dx
+
+
+def cross_entropy_backward(logits, labels, dloss=None):
+    x = _f32(logits)
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    dl = None if dloss is None else _f32(dloss)
+    r, c = x.shape
+    dx = np.empty((r, c), np.float64)
+    _rc(lib().oracle_cross_entropy_bwd_f64(_ptr(x, ctypes.c_float), _ptr(lab, ctypes.c_int64),
+                                           _ptr(dl, ctypes.c_float), _ptr(dx, ctypes.c_double), r, c))
+    return dx
+
+
+def rmsnorm_backward(x, w, dy, eps=1e-5):
+    """(dx, dw) in FP64; dw is the column sum over rows of dy * x / rms."""
+    x, dy = _f32(x), _f32(dy)
+    w = None if w is None else _f32(w)
+    r, c = x.shape
+    dx = np.empty((r, c), np.float64)
+    dw = np.empty(c, np.float64)
+    _rc(lib().oracle_rmsnorm_bwd_f64(_ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float), _ptr(dy, ctypes.c_float),
+                                     _ptr(dx, ctypes.c_double), _ptr(dw, ctypes.c_double), r, c, eps))
+    return dx, dw
+
+
+def layernorm_backward(x, gamma, dy, eps=1e-5):
+    """(dx, dgamma, dbeta) in FP64."""
+    x, dy = _f32(x), _f32(dy)
+    gamma = None if gamma is None else _f32(gamma)
+    r, c = x.shape
+    dx = np.empty((r, c), np.float64)
+    dg = np.empty(c, np.float64)
+    db = np.empty(c, np.float64)
+    _rc(lib().oracle_layernorm_bwd_f64(_ptr(x, ctypes.c_float), _ptr(gamma, ctypes.c_float),
+                                       _ptr(dy, ctypes.c_float), _ptr(dx, ctypes.c_double),
+                                       _ptr(dg, ctypes.c_double), _ptr(db, ctypes.c_double), r, c, eps))
+    return dx, dg, db
+
+
+def ot_softmax_backward(y, dy):
+    y, dy = _f32(y), _f32(dy)
+    r, c = y.shape
+    dx = np.empty((r, c), np.float32)
+    _rc(lib().ot_softmax_bwd_f32(_ptr(y, ctypes.c_float), _ptr(dy, ctypes.c_float), _ptr(dx, ctypes.c_float), r, c))
+    return dx
+
+
+def ot_cross_entropy_backward(logits, labels, dloss=None):
+    x = _f32(logits)
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    dl = None if dloss is None else _f32(dloss)
+    r, c = x.shape
+    dx = np.empty((r, c), np.float32)
+    _rc(lib().ot_cross_entropy_bwd_f32(_ptr(x, ctypes.c_float), _ptr(lab, ctypes.c_int64), _ptr(dl, ctypes.c_float),
+                                       _ptr(dx, ctypes.c_float), r, c))
+    return dx
+
+
+def ot_rmsnorm_backward(x, w, dy, eps=1e-5):
+    x, dy = _f32(x), _f32(dy)
+    w = None if w is None else _f32(w)
+    r, c = x.shape
+    dx = np.empty((r, c), np.float32)
+    dw = np.empty(c, np.float32)
+    _rc(lib().ot_rmsnorm_bwd_f32(_ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float), _ptr(dy, ctypes.c_float),
+                                 _ptr(dx, ctypes.c_float), _ptr(dw, ctypes.c_float), r, c, eps))
+    return dx, dw
+
+
+def ot_layernorm_backward(x, gamma, dy, eps=1e-5):
+    x, dy = _f32(x), _f32(dy)
+    gamma = None if gamma is None else _f32(gamma)
+    r, c = x.shape
+    dx = np.empty((r, c), np.float32)
+    dg = np.empty(c, np.float32)
+    db = np.empty(c, np.float32)
+    _rc(lib().ot_layernorm_bwd_f32(_ptr(x, ctypes.c_float), _ptr(gamma, ctypes.c_float), _ptr(dy, ctypes.c_float),
+                                   _ptr(dx, ctypes.c_float), _ptr(dg, ctypes.c_float), _ptr(db, ctypes.c_float),
+                                   r, c, eps))
+    return dx, dg, db
 
 
 def ot_expf(x):

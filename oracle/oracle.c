@@ -44,6 +44,7 @@
 
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ------------------------------------------------------------------------- */
@@ -358,4 +359,215 @@ int ot_cross_entropy_f32(const float *logits, const int64_t *labels,
         loss[r] = (ot_logf(total) + peak) - selected;
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Part 3: backward passes (the gradients of the four row operators)          */
+/* ------------------------------------------------------------------------- */
+/*
+ * Not on the pages (the next rows of the same row-reduction family). The FP64
+ * functions are the derivatives of the Part 1 definitions, written out:
+ *   softmax        dx_c = y_c (dy_c - sum_j dy_j y_j)
+ *   cross-entropy  dx_c = dloss (p_c - [c == label]), p = softmax(logits); a
+ *                  label outside [0, N) selects nothing, so no one-hot term;
+ *                  dloss = 1 when no per-row upstream gradient is given
+ *   RMSNorm        r = 1 / sqrt(mean(x^2) + eps), g = dy w:
+ *                  dx_c = r (g_c - x_c r^2 mean(g x)), dw_c = sum_rows dy_c x_c r
+ *   LayerNorm      xh = (x - mean) r, r = 1 / sqrt(var + eps), g = dy gamma:
+ *                  dx_c = r (g_c - mean(g) - xh_c mean(g xh)),
+ *                  dgamma_c = sum_rows dy_c xh_c, dbeta_c = sum_rows dy_c
+ * The ot_*_bwd_f32 functions emulate the ordered policy: every row sum is
+ * OT-1024 over the row's terms, every column sum (dw, dgamma, dbeta) is
+ * OT-1024 over that column's per-row terms, and each step is the binary32
+ * operation written below, in that order.
+ */
+
+int oracle_softmax_bwd_f64(const float *y, const float *dy, double *dx, int64_t rows, int64_t cols) {
+    if (bad_sizes(rows, cols)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *yr = y + r * cols, *gr = dy + r * cols;
+        double dot = 0.0;
+        for (int64_t c = 0; c < cols; ++c) dot += (double)gr[c] * (double)yr[c];
+        for (int64_t c = 0; c < cols; ++c) dx[r * cols + c] = (double)yr[c] * ((double)gr[c] - dot);
+    }
+    return 0;
+}
+
+int oracle_cross_entropy_bwd_f64(const float *logits, const int64_t *labels, const float *dloss, double *dx,
+                                 int64_t rows, int64_t cols) {
+    if (bad_sizes(rows, cols)) return -1;
+    double *p = (double *)malloc((size_t)cols * sizeof(double));
+    if (!p) return -2;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = logits + r * cols;
+        double peak = -INFINITY;
+        for (int64_t c = 0; c < cols; ++c) if ((double)xr[c] > peak) peak = (double)xr[c];
+        double total = 0.0;
+        for (int64_t c = 0; c < cols; ++c) { p[c] = exp((double)xr[c] - peak); total += p[c]; }
+        const double scale = dloss ? (double)dloss[r] : 1.0;
+        for (int64_t c = 0; c < cols; ++c) {
+            double d = p[c] / total - (c == labels[r] ? 1.0 : 0.0);
+            dx[r * cols + c] = scale * d;
+        }
+    }
+    free(p);
+    return 0;
+}
+
+int oracle_rmsnorm_bwd_f64(const float *x, const float *w, const float *dy, double *dx, double *dw,
+                           int64_t rows, int64_t cols, float eps) {
+    if (bad_sizes(rows, cols)) return -1;
+    if (dw) for (int64_t c = 0; c < cols; ++c) dw[c] = 0.0;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols, *gr = dy + r * cols;
+        double ss = 0.0, gx = 0.0;
+        for (int64_t c = 0; c < cols; ++c) ss += (double)xr[c] * (double)xr[c];
+        const double inv = 1.0 / sqrt(ss / (double)cols + (double)eps);
+        for (int64_t c = 0; c < cols; ++c) gx += (double)gr[c] * (w ? (double)w[c] : 1.0) * (double)xr[c];
+        const double k = gx / (double)cols * inv * inv;
+        for (int64_t c = 0; c < cols; ++c) {
+            const double g = (double)gr[c] * (w ? (double)w[c] : 1.0);
+            dx[r * cols + c] = inv * (g - (double)xr[c] * k);
+            if (dw) dw[c] += (double)gr[c] * (double)xr[c] * inv;
+        }
+    }
+    return 0;
+}
+
+int oracle_layernorm_bwd_f64(const float *x, const float *gamma, const float *dy, double *dx, double *dgamma,
+                             double *dbeta, int64_t rows, int64_t cols, float eps) {
+    if (bad_sizes(rows, cols)) return -1;
+    if (dgamma) for (int64_t c = 0; c < cols; ++c) dgamma[c] = 0.0;
+    if (dbeta) for (int64_t c = 0; c < cols; ++c) dbeta[c] = 0.0;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols, *gr = dy + r * cols;
+        double sum = 0.0, sq = 0.0, sg = 0.0, sgx = 0.0;
+        for (int64_t c = 0; c < cols; ++c) sum += (double)xr[c];
+        const double mean = sum / (double)cols;
+        for (int64_t c = 0; c < cols; ++c) sq += ((double)xr[c] - mean) * ((double)xr[c] - mean);
+        const double inv = 1.0 / sqrt(sq / (double)cols + (double)eps);
+        for (int64_t c = 0; c < cols; ++c) {
+            const double g = (double)gr[c] * (gamma ? (double)gamma[c] : 1.0);
+            sg += g;
+            sgx += g * ((double)xr[c] - mean) * inv;
+        }
+        const double a = sg / (double)cols, b = sgx / (double)cols;
+        for (int64_t c = 0; c < cols; ++c) {
+            const double g = (double)gr[c] * (gamma ? (double)gamma[c] : 1.0);
+            const double xh = ((double)xr[c] - mean) * inv;
+            dx[r * cols + c] = inv * (g - a - xh * b);
+            if (dgamma) dgamma[c] += (double)gr[c] * xh;
+            if (dbeta) dbeta[c] += (double)gr[c];
+        }
+    }
+    return 0;
+}
+
+/* OT-1024 over the columns of a rows x cols term matrix: out[c] = OT_sum(t[., c]). */
+static int ot_column_sums(const float *t, float *out, int64_t rows, int64_t cols) {
+    float *col = (float *)malloc((size_t)(rows > 0 ? rows : 1) * sizeof(float));
+    if (!col) return -2;
+    for (int64_t c = 0; c < cols; ++c) {
+        for (int64_t r = 0; r < rows; ++r) col[r] = t[r * cols + c];
+        out[c] = ot_sum_f32(col, rows);
+    }
+    free(col);
+    return 0;
+}
+
+int ot_softmax_bwd_f32(const float *y, const float *dy, float *dx, int64_t rows, int64_t cols) {
+    if (bad_sizes(rows, cols)) return -1;
+    float *t = (float *)malloc((size_t)cols * sizeof(float));
+    if (!t) return -2;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *yr = y + r * cols, *gr = dy + r * cols;
+        for (int64_t c = 0; c < cols; ++c) t[c] = gr[c] * yr[c];
+        const float s = ot_sum_f32(t, cols);
+        for (int64_t c = 0; c < cols; ++c) dx[r * cols + c] = yr[c] * (gr[c] - s);
+    }
+    free(t);
+    return 0;
+}
+
+int ot_cross_entropy_bwd_f32(const float *logits, const int64_t *labels, const float *dloss, float *dx,
+                             int64_t rows, int64_t cols) {
+    if (bad_sizes(rows, cols)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = logits + r * cols;
+        const float peak = ot_max_f32(xr, cols);
+        const float total = ot_sum_of(xr, cols, el_exp_shifted, peak);
+        const float inv = 1.0f / total;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float p = ot_expf(xr[c] - peak) * inv;
+            const float d = c == labels[r] ? p - 1.0f : p;
+            dx[r * cols + c] = dloss ? d * dloss[r] : d;
+        }
+    }
+    return 0;
+}
+
+int ot_rmsnorm_bwd_f32(const float *x, const float *w, const float *dy, float *dx, float *dw,
+                       int64_t rows, int64_t cols, float eps) {
+    if (bad_sizes(rows, cols)) return -1;
+    float *t = (float *)malloc((size_t)cols * sizeof(float));
+    float *terms = dw ? (float *)malloc((size_t)(rows > 0 ? rows : 1) * (size_t)cols * sizeof(float)) : NULL;
+    if (!t || (dw && !terms)) { free(t); free(terms); return -2; }
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols, *gr = dy + r * cols;
+        const float ss = ot_sum_of(xr, cols, el_square, 0.0f);
+        const float rms = sqrtf(ss / (float)cols + eps);
+        const float inv = 1.0f / rms;
+        for (int64_t c = 0; c < cols; ++c) t[c] = (w ? gr[c] * w[c] : gr[c]) * xr[c];
+        const float cs = ot_sum_f32(t, cols);
+        const float k = ((cs / (float)cols) * inv) * inv;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float g = w ? gr[c] * w[c] : gr[c];
+            dx[r * cols + c] = inv * (g - xr[c] * k);
+            if (terms) terms[r * cols + c] = (gr[c] * xr[c]) * inv;
+        }
+    }
+    int rc = terms ? ot_column_sums(terms, dw, rows, cols) : 0;
+    free(t);
+    free(terms);
+    return rc;
+}
+
+int ot_layernorm_bwd_f32(const float *x, const float *gamma, const float *dy, float *dx, float *dgamma,
+                         float *dbeta, int64_t rows, int64_t cols, float eps) {
+    if (bad_sizes(rows, cols)) return -1;
+    const size_t n = (size_t)(rows > 0 ? rows : 1) * (size_t)cols;
+    float *t = (float *)malloc((size_t)cols * sizeof(float));
+    float *xh = (float *)malloc((size_t)cols * sizeof(float));
+    float *tg = dgamma ? (float *)malloc(n * sizeof(float)) : NULL;
+    float *tb = dbeta ? (float *)malloc(n * sizeof(float)) : NULL;
+    if (!t || !xh || (dgamma && !tg) || (dbeta && !tb)) { free(t); free(xh); free(tg); free(tb); return -2; }
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols, *gr = dy + r * cols;
+        const float mean = ot_sum_of(xr, cols, el_identity, 0.0f) / (float)cols;
+        const float var = ot_sum_of(xr, cols, el_centered_square, mean) / (float)cols;
+        const float sigma = sqrtf(var + eps);
+        const float inv = 1.0f / sigma;
+        for (int64_t c = 0; c < cols; ++c) {
+            xh[c] = (xr[c] - mean) * inv;
+            t[c] = gamma ? gr[c] * gamma[c] : gr[c];
+        }
+        const float sa = ot_sum_f32(t, cols);
+        for (int64_t c = 0; c < cols; ++c) t[c] = (gamma ? gr[c] * gamma[c] : gr[c]) * xh[c];
+        const float sb = ot_sum_f32(t, cols);
+        const float a = sa / (float)cols, b = sb / (float)cols;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float g = gamma ? gr[c] * gamma[c] : gr[c];
+            dx[r * cols + c] = inv * ((g - a) - xh[c] * b);
+            if (tg) tg[r * cols + c] = gr[c] * xh[c];
+            if (tb) tb[r * cols + c] = gr[c];
+        }
+    }
+    int rc = 0;
+    if (tg) rc = ot_column_sums(tg, dgamma, rows, cols);
+    if (!rc && tb) rc = ot_column_sums(tb, dbeta, rows, cols);
+    free(t);
+    free(xh);
+    free(tg);
+    free(tb);
+    return rc;
 }

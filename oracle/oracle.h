@@ -47,6 +47,21 @@ int ot_layernorm_f32(const float *x, const float *gamma, const float *beta,
 int ot_cross_entropy_f32(const float *logits, const int64_t *labels,
                          float *loss, int64_t rows, int64_t cols);
 
+int oracle_softmax_bwd_f64(const float *y, const float *dy, double *dx, int64_t rows, int64_t cols);
+int oracle_cross_entropy_bwd_f64(const float *logits, const int64_t *labels, const float *dloss, double *dx,
+                                 int64_t rows, int64_t cols);
+int oracle_rmsnorm_bwd_f64(const float *x, const float *w, const float *dy, double *dx, double *dw,
+                           int64_t rows, int64_t cols, float eps);
+int oracle_layernorm_bwd_f64(const float *x, const float *gamma, const float *dy, double *dx, double *dgamma,
+                             double *dbeta, int64_t rows, int64_t cols, float eps);
+int ot_softmax_bwd_f32(const float *y, const float *dy, float *dx, int64_t rows, int64_t cols);
+int ot_cross_entropy_bwd_f32(const float *logits, const int64_t *labels, const float *dloss, float *dx,
+                             int64_t rows, int64_t cols);
+int ot_rmsnorm_bwd_f32(const float *x, const float *w, const float *dy, float *dx, float *dw,
+                       int64_t rows, int64_t cols, float eps);
+int ot_layernorm_bwd_f32(const float *x, const float *gamma, const float *dy, float *dx, float *dgamma,
+                         float *dbeta, int64_t rows, int64_t cols, float eps);
+
 #ifdef __cplusplus
 }
 #endif
