@@ -114,6 +114,11 @@ SIGNATURES = {
     "tr_axis_minmax_f32": ([_P, _P, _P, _I64, _I64, _I64, _I32, _P], _I32),
     "tr_axis_launch_shape": ([_I32, _I32, _I32, _I64, _I64, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I64)],
                              _I32),
+    "tr_softmax_backward_f32": ([_P, _P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_cross_entropy_backward_f32": ([_P, _P, _P, _P, _I64, _I64, _I32, _P], _I32),
+    "tr_rmsnorm_backward_f32": ([_P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P, ctypes.c_size_t, _P], _I32),
+    "tr_layernorm_backward_f32": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P, ctypes.c_size_t, _P], _I32),
+    "tr_norm_backward_workspace_bytes": ([_I64, _I64, ctypes.POINTER(ctypes.c_size_t)], _I32),
     "tr_add_layernorm_f32": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I32, _P], _I32),
     "tr_plan_describe": ([_I32, _I64, _I64, _I32, ctypes.POINTER(tr_plan)], _I32),
     "tr_plan_select_for": ([ctypes.POINTER(tr_device_desc), _I32, _I64, _I64, _I32, _I32,
@@ -443,6 +448,86 @@ def axis_reduce(x, dim=0, op="sum", out=None, out2=None, order="unordered", stre
     _check(fn(x.data_ptr(), y.data_ptr(), outer, extent, inner, _order(order), _stream_handle(stream)),
            "axis_" + op)
     return y
+
+
+# ------------------------------------------------------------ backward passes
+
+def norm_backward_workspace_bytes(rows, cols):
+    n = ctypes.c_size_t(0)
+    _check(load().tr_norm_backward_workspace_bytes(rows, cols, ctypes.byref(n)), "norm_backward_workspace_bytes")
+    return n.value
+
+
+def softmax_backward(y, dy, out=None, order="unordered", stream=None):
+    """dx = y * (dy - sum(dy * y)) per row, from the forward output y."""
+    import torch
+    _check_matrix(y, "y")
+    _check_matrix(dy, "dy")
+    r, c = y.shape
+    dx = torch.empty_like(y) if out is None else out
+    _check(load().tr_softmax_backward_f32(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), r, c, _order(order),
+                                          _stream_handle(stream)), "softmax_backward")
+    return dx
+
+
+def cross_entropy_backward(logits, labels, dloss=None, out=None, order="unordered", stream=None):
+    """dlogits = dloss * (softmax(logits) - onehot(labels)); dloss None means 1."""
+    import torch
+    _check_matrix(logits, "logits")
+    r, c = logits.shape
+    dx = torch.empty_like(logits) if out is None else out
+    _check(load().tr_cross_entropy_backward_f32(logits.data_ptr(), labels.data_ptr(),
+                                                None if dloss is None else dloss.data_ptr(), dx.data_ptr(), r, c,
+                                                _order(order), _stream_handle(stream)), "cross_entropy_backward")
+    return dx
+
+
+def _workspace(x, rows, cols, want):
+    import torch
+    if not want:
+        return None, 0
+    n = norm_backward_workspace_bytes(rows, cols)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=x.device), n
+
+
+def rmsnorm_backward(x, w, dy, eps=1e-5, order="unordered", want_dw=True, dx=None, dw=None, workspace=None,
+                     stream=None):
+    """(dx, dw) of RMSNorm; dw is None when not wanted."""
+    import torch
+    _check_matrix(x, "x")
+    _check_matrix(dy, "dy")
+    r, c = x.shape
+    dx = torch.empty_like(x) if dx is None else dx
+    want = want_dw or dw is not None
+    dw = (torch.empty(c, device=x.device, dtype=torch.float32) if dw is None else dw) if want else None
+    ws, n = (workspace, workspace.numel()) if workspace is not None else _workspace(x, r, c, want)
+    _check(load().tr_rmsnorm_backward_f32(x.data_ptr(), None if w is None else w.data_ptr(), dy.data_ptr(),
+                                          dx.data_ptr(), None if dw is None else dw.data_ptr(), r, c, eps,
+                                          _order(order), None if ws is None else ws.data_ptr(), n,
+                                          _stream_handle(stream)), "rmsnorm_backward")
+    return dx, dw
+
+
+def layernorm_backward(x, gamma, dy, eps=1e-5, order="unordered", want_params=True, dx=None, dgamma=None,
+                       dbeta=None, workspace=None, stream=None):
+    """(dx, dgamma, dbeta) of LayerNorm; the parameter gradients are None when not wanted."""
+    import torch
+    _check_matrix(x, "x")
+    _check_matrix(dy, "dy")
+    r, c = x.shape
+    dx = torch.empty_like(x) if dx is None else dx
+    if want_params:
+        dgamma = torch.empty(c, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+        dbeta = torch.empty(c, device=x.device, dtype=torch.float32) if dbeta is None else dbeta
+    want = dgamma is not None or dbeta is not None
+    ws, n = (workspace, workspace.numel()) if workspace is not None else _workspace(x, r, c, want)
+    _check(load().tr_layernorm_backward_f32(x.data_ptr(), None if gamma is None else gamma.data_ptr(),
+                                            dy.data_ptr(), dx.data_ptr(),
+                                            None if dgamma is None else dgamma.data_ptr(),
+                                            None if dbeta is None else dbeta.data_ptr(), r, c, eps, _order(order),
+                                            None if ws is None else ws.data_ptr(), n, _stream_handle(stream)),
+           "layernorm_backward")
+    return dx, dgamma, dbeta
 
 
 def cross_entropy(logits, labels, out=None, order="unordered", stream=None):

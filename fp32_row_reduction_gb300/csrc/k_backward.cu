@@ -1,0 +1,324 @@
+// Backward passes of the four row operators: the gradients of softmax,
+// cross-entropy, RMSNorm and LayerNorm, the next rows of the same row-reduction
+// family (the pages define the forward operators only).
+//
+//   softmax        dx_c = y_c (dy_c - s),            s = sum_j dy_j y_j
+//   cross-entropy  dx_c = dloss (p_c - [c == label]), p = softmax(logits)
+//   RMSNorm        dx_c = r (g_c - x_c k),           g = dy w, k = (sum g x / N) r r,
+//                  r = 1 / sqrt(sum x^2 / N + eps);  dw_c = sum_rows (dy_c x_c) r
+//   LayerNorm      dx_c = r ((g_c - a) - xh_c b),    xh = (x - mean) r, g = dy gamma,
+//                  a = sum g / N, b = sum g xh / N;  dgamma_c = sum_rows dy_c xh_c,
+//                  dbeta_c = sum_rows dy_c
+//
+// Layout: one CTA of 256 threads per row, thread t owning columns 1024j + 4t
+// .. +3, the OT-1024 layout of the ordered forward kernels, so every row sum is
+// the fixed tree in both policies (the unordered policy uses the same tree
+// with contracted arithmetic and the hardware exp2). Rows of at most 1024 K
+// columns stay in registers; longer rows are read again for each pass.
+//
+// Column gradients (dw, dgamma, dbeta): CTA c of G takes rows c, c + G, ...
+// in increasing order and folds its rows' terms per column, starting from +0,
+// into its own row of a G x cols partial matrix; a column reduction over that
+// matrix finishes them. With G = min(rows, 1024), partial row c is exactly
+// leaf c of OT-1024 over the column's terms, so the ordered column reduction
+// of the partials gives the ordered column gradient bit for bit.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tr_device.cuh"
+#include "tr_internal.h"
+#include "tr_ot.cuh"
+
+namespace tr {
+namespace backward {
+
+using ordered::Add;
+using ordered::Max;
+using ordered::exp_ot;
+using ordered::load_quad;
+using ordered::store_quad;
+using ordered::tree;
+
+// Binary32 steps: rounded one by one under the ordered policy, free to
+// contract under the unordered one.
+template <bool O>
+__device__ __forceinline__ float add(float a, float b) { return O ? __fadd_rn(a, b) : a + b; }
+template <bool O>
+__device__ __forceinline__ float sub(float a, float b) { return O ? __fsub_rn(a, b) : a - b; }
+template <bool O>
+__device__ __forceinline__ float mul(float a, float b) { return O ? __fmul_rn(a, b) : a * b; }
+template <bool O>
+__device__ __forceinline__ float divide(float a, float b) { return O ? __fdiv_rn(a, b) : __fdividef(a, b); }
+template <bool O>
+__device__ __forceinline__ float root(float a) { return O ? __fsqrt_rn(a) : sqrtf(a); }
+// exp(x - m): the library's exp under the ordered policy, the hardware exp2 otherwise
+template <bool O>
+__device__ __forceinline__ float exp_shift(float x, float m) {
+    if constexpr (O) return exp_ot(__fsub_rn(x, m));
+    else return ex2(x * kL2E - m * kL2E);
+}
+
+// Columns 1024j + 4t .. +3 of a parameter vector (cached loads; 0 outside the row).
+__device__ __forceinline__ void load_param_quad(const float* w, int cols, int j, bool aligned, float (&q)[4]) {
+    const int c0 = 1024 * j + 4 * static_cast<int>(threadIdx.x);
+    if (aligned && c0 + 3 < cols) {
+        const float4 v = ld_param4(w + c0);
+        q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+    } else {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) q[v] = c0 + v < cols ? __ldg(w + c0 + v) : 0.0f;
+    }
+}
+
+// Partial column sums: the CTA's own row of the G x cols matrix. The first row
+// of a CTA writes its terms (+0 + t, which is t unless t is -0), later rows add.
+template <bool O>
+__device__ __forceinline__ void fold_partial(float* pr, int cols, int j, bool first, const float (&t)[4],
+                                             const bool (&ok)[4]) {
+    const int c0 = 1024 * j + 4 * static_cast<int>(threadIdx.x);
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+        if (ok[v]) pr[c0 + v] = first ? add<O>(0.0f, t[v]) : add<O>(pr[c0 + v], t[v]);
+}
+
+template <int OP, int K, bool O>
+__global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
+    constexpr int KC = K > 0 ? K : 1;
+    __shared__ float gpart[2][8];
+    int buf = 0;
+    const int cols = a.cols;
+    const int nj = (cols + 1023) / 1024;
+    const float n = static_cast<float>(cols);
+    const int t4 = 4 * static_cast<int>(threadIdx.x);
+    const bool w_al = a.w && aligned16(a.w);
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+        const bool first = row == static_cast<int64_t>(blockIdx.x);
+        const float* xr = a.x + row * cols;
+        const float* dr = OP == BW_XENT ? nullptr : a.dy + row * cols;
+        float* yr = a.dx + row * cols;
+        const bool x_al = aligned16(xr);
+        const bool d_al = dr && aligned16(dr);
+        const bool y_al = aligned16(yr);
+        float cx[KC][4], cd[KC][4];
+        if constexpr (K > 0) {
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                bool ok[4];
+                if (j < nj) {
+                    load_quad(xr, cols, j, x_al, cx[j], ok);
+                    if constexpr (OP != BW_XENT) load_quad(dr, cols, j, d_al, cd[j], ok);
+                }
+            }
+        }
+        // fn(j, x quad, dy quad, valid columns) for every quad of the row, in increasing j
+        auto for_quads = [&](auto&& fn) {
+            if constexpr (K > 0) {
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (j < nj) {
+                        bool ok[4];
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) ok[v] = 1024 * j + t4 + v < cols;
+                        fn(j, cx[j], cd[j], ok);
+                    }
+                }
+            } else {
+                for (int j = 0; j < nj; ++j) {
+                    float qx[4], qd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    bool ok[4];
+                    load_quad(xr, cols, j, x_al, qx, ok);
+                    if constexpr (OP != BW_XENT) load_quad(dr, cols, j, d_al, qd, ok);
+                    fn(j, qx, qd, ok);
+                }
+            }
+        };
+        float leaf[4];
+        auto clear = [&](float v0) { leaf[0] = leaf[1] = leaf[2] = leaf[3] = v0; };
+        if constexpr (OP == BW_SOFTMAX) {
+            clear(0.0f);
+            for_quads([&](int, const float (&y)[4], const float (&d)[4], const bool (&ok)[4]) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (ok[v]) leaf[v] = add<O>(leaf[v], mul<O>(d[v], y[v]));
+            });
+            const float s = tree<Add>(leaf, gpart, buf);
+            for_quads([&](int j, const float (&y)[4], const float (&d)[4], const bool (&ok)[4]) {
+                float o[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) o[v] = mul<O>(y[v], sub<O>(d[v], s));
+                store_quad(yr, cols, j, y_al, o, ok);
+            });
+        } else if constexpr (OP == BW_XENT) {
+            clear(__int_as_float(0xff800000));
+            for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (ok[v]) leaf[v] = fmaxf(leaf[v], x[v]);
+            });
+            const float m = tree<Max>(leaf, gpart, buf);
+            clear(0.0f);
+            for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (ok[v]) leaf[v] = add<O>(leaf[v], exp_shift<O>(x[v], m));
+            });
+            const float inv = divide<O>(1.0f, tree<Add>(leaf, gpart, buf));
+            const int64_t label = a.labels[row];
+            const bool scaled = a.dloss != nullptr;
+            const float dl = scaled ? a.dloss[row] : 1.0f;
+            for_quads([&](int j, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+                float o[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float p = mul<O>(exp_shift<O>(x[v], m), inv);
+                    const float d = (1024 * j + t4 + v == label) ? sub<O>(p, 1.0f) : p;
+                    o[v] = scaled ? mul<O>(d, dl) : d;
+                }
+                store_quad(yr, cols, j, y_al, o, ok);
+            });
+        } else if constexpr (OP == BW_RMSNORM) {
+            clear(0.0f);
+            for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (ok[v]) leaf[v] = add<O>(leaf[v], mul<O>(x[v], x[v]));
+            });
+            const float ss = tree<Add>(leaf, gpart, buf);
+            const float inv = divide<O>(1.0f, root<O>(add<O>(divide<O>(ss, n), a.eps)));
+            // g = dy w, column by column
+            auto grad_in = [&](int j, const float (&d)[4], float (&g)[4]) {
+                if (a.w) {
+                    float wq[4];
+                    load_param_quad(a.w, cols, j, w_al, wq);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) g[v] = mul<O>(d[v], wq[v]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) g[v] = d[v];
+                }
+            };
+            clear(0.0f);
+            for_quads([&](int j, const float (&x)[4], const float (&d)[4], const bool (&ok)[4]) {
+                float g[4];
+                grad_in(j, d, g);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (ok[v]) leaf[v] = add<O>(leaf[v], mul<O>(g[v], x[v]));
+            });
+            const float cs = tree<Add>(leaf, gpart, buf);
+            const float k = mul<O>(mul<O>(divide<O>(cs, n), inv), inv);
+            float* pw = a.part_w ? a.part_w + static_cast<int64_t>(blockIdx.x) * cols : nullptr;
+            for_quads([&](int j, const float (&x)[4], const float (&d)[4], const bool (&ok)[4]) {
+                float g[4], o[4];
+                grad_in(j, d, g);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) o[v] = mul<O>(inv, sub<O>(g[v], mul<O>(x[v], k)));
+                store_quad(yr, cols, j, y_al, o, ok);
+                if (pw) {
+                    float t[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) t[v] = mul<O>(mul<O>(d[v], x[v]), inv);
+                    fold_partial<O>(pw, cols, j, first, t, ok);
+                }
+            });
+        } else {
+            clear(0.0f);
+            for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (ok[v]) leaf[v] = add<O>(leaf[v], x[v]);
+            });
+            const float mean = divide<O>(tree<Add>(leaf, gpart, buf), n);
+            clear(0.0f);
+            for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float c = sub<O>(x[v], mean);
+                    if (ok[v]) leaf[v] = add<O>(leaf[v], mul<O>(c, c));
+                }
+            });
+            const float var = divide<O>(tree<Add>(leaf, gpart, buf), n);
+            const float inv = divide<O>(1.0f, root<O>(add<O>(var, a.eps)));
+            auto grad_in = [&](int j, const float (&d)[4], float (&g)[4]) {
+                if (a.w) {
+                    float wq[4];
+                    load_param_quad(a.w, cols, j, w_al, wq);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) g[v] = mul<O>(d[v], wq[v]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) g[v] = d[v];
+                }
+            };
+            float lb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            clear(0.0f);
+            for_quads([&](int j, const float (&x)[4], const float (&d)[4], const bool (&ok)[4]) {
+                float g[4];
+                grad_in(j, d, g);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float xh = mul<O>(sub<O>(x[v], mean), inv);
+                    if (ok[v]) {
+                        leaf[v] = add<O>(leaf[v], g[v]);
+                        lb[v] = add<O>(lb[v], mul<O>(g[v], xh));
+                    }
+                }
+            });
+            const float ga = divide<O>(tree<Add>(leaf, gpart, buf), n);
+            const float gb = divide<O>(tree<Add>(lb, gpart, buf), n);
+            float* pw = a.part_w ? a.part_w + static_cast<int64_t>(blockIdx.x) * cols : nullptr;
+            float* pb = a.part_b ? a.part_b + static_cast<int64_t>(blockIdx.x) * cols : nullptr;
+            for_quads([&](int j, const float (&x)[4], const float (&d)[4], const bool (&ok)[4]) {
+                float g[4], o[4], xh[4];
+                grad_in(j, d, g);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    xh[v] = mul<O>(sub<O>(x[v], mean), inv);
+                    o[v] = mul<O>(inv, sub<O>(sub<O>(g[v], ga), mul<O>(xh[v], gb)));
+                }
+                store_quad(yr, cols, j, y_al, o, ok);
+                if (pw) {
+                    float t[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) t[v] = mul<O>(d[v], xh[v]);
+                    fold_partial<O>(pw, cols, j, first, t, ok);
+                }
+                if (pb) fold_partial<O>(pb, cols, j, first, d, ok);
+            });
+        }
+    }
+}
+
+template <int OP, bool O>
+cudaError_t launch_op(int slots, const BwArgs& a, int ctas, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(ctas));
+    switch (slots) {
+        case 0: bw_kernel<OP, 0, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
+        case 1: bw_kernel<OP, 1, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
+        case 2: bw_kernel<OP, 2, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
+        case 4: bw_kernel<OP, 4, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
+        case 6: bw_kernel<OP, 6, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
+        case 8: bw_kernel<OP, 8, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+template <int OP>
+cudaError_t launch_policy(bool ordered, int slots, const BwArgs& a, int ctas, cudaStream_t stream) {
+    return ordered ? launch_op<OP, true>(slots, a, ctas, stream) : launch_op<OP, false>(slots, a, ctas, stream);
+}
+
+}  // namespace backward
+
+cudaError_t launch_backward(int op, bool ordered, int slots, const BwArgs& a, int ctas, cudaStream_t stream) {
+    switch (op) {
+        case BW_SOFTMAX: return backward::launch_policy<BW_SOFTMAX>(ordered, slots, a, ctas, stream);
+        case BW_XENT: return backward::launch_policy<BW_XENT>(ordered, slots, a, ctas, stream);
+        case BW_RMSNORM: return backward::launch_policy<BW_RMSNORM>(ordered, slots, a, ctas, stream);
+        case BW_LAYERNORM: return backward::launch_policy<BW_LAYERNORM>(ordered, slots, a, ctas, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tr

@@ -515,6 +515,9 @@ int axis_ctas_per_sm(int op, int order) {
     return (op == TR_OP_ROW_SUM && order == TR_ORDER_ORDERED_TREE) ? kAxisCtasTree : kAxisCtasFree;
 }
 
+static tr_status axis_run(int op, const float* x, float* out, float* out2, int64_t extent, int64_t inner,
+                          int64_t ncols, tr_order order, cudaStream_t stream);
+
 static tr_status axis_call(int op, const float* x, float* out, float* out2, int64_t outer, int64_t extent,
                            int64_t inner, tr_order order, cudaStream_t stream) {
     if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE)
@@ -536,6 +539,15 @@ static tr_status axis_call(int op, const float* x, float* out, float* out2, int6
     const size_t no = static_cast<size_t>(ncols) * 4;
     if (overlaps(x, n, out, no) || overlaps(x, n, out2, no) || overlaps(out, no, out2, no))
         return fail(TR_ERR_INVALID_ARG, "an output overlaps the input or the other output");
+    return axis_run(op, x, out, out2, extent, inner, ncols, order, stream);
+}
+
+// The axis reduction of validated arguments (also the second step of the
+// column gradients of the norm backward passes).
+static tr_status axis_run(int op, const float* x, float* out, float* out2, int64_t extent, int64_t inner,
+                          int64_t ncols, tr_order order, cudaStream_t stream) {
+    const int vec = axis_vec(op, order, inner, !misaligned(x, 16));
+    const int64_t tiles = (ncols + kAxisCols * vec - 1) / (kAxisCols * vec);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -596,6 +608,168 @@ tr_status tr_axis_min_f32(const float* x, float* out, int64_t outer, int64_t ext
 tr_status tr_axis_minmax_f32(const float* x, float* out_min, float* out_max, int64_t outer, int64_t extent,
                              int64_t inner, tr_order order, cudaStream_t stream) {
     return axis_call(TR_OP_ROW_MINMAX, x, out_min, out_max, outer, extent, inner, order, stream);
+}
+
+// ---- backward passes -------------------------------------------------------
+
+// Cached quads per thread: the fewest that hold the row, 0 beyond 8192 columns.
+static int bw_slots(int64_t cols) {
+    for (int k : kBwSlots)
+        if (k > 0 && cols <= 1024LL * k) return k;
+    return 0;
+}
+
+// CTAs of a backward launch. With column gradients: min(rows, 1024) ordered (CTA
+// c's partial row is leaf c of OT-1024 over the rows), two per SM unordered
+// (fewer partial rows to reduce); without: one CTA per row (grid capped, the
+// CTAs loop over the rest).
+static int64_t bw_ctas(int64_t rows, bool col_grads, tr_order order, int sm_count) {
+    if (!col_grads) return rows < (1LL << 20) ? rows : (1LL << 20);
+    const int64_t cap = order == TR_ORDER_ORDERED_TREE ? kBwMaxPartialCtas : 2LL * sm_count;
+    return rows < cap ? rows : cap;
+}
+
+tr_status tr_norm_backward_workspace_bytes(int64_t rows, int64_t cols, size_t* bytes) {
+    if (!bytes) return fail(TR_ERR_INVALID_ARG, "bytes must not be null");
+    tr_status s = validate_common(rows, cols, TR_ORDER_UNORDERED_TREE);
+    if (s != TR_OK) return s;
+    const int64_t g = rows < kBwMaxPartialCtas ? rows : kBwMaxPartialCtas;
+    *bytes = static_cast<size_t>(g) * static_cast<size_t>(cols) * 2 * sizeof(float);
+    return TR_OK;
+}
+
+static tr_status bw_run(int op, BwArgs a, tr_order order, float* dw, float* db, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+    if (a.rows == 0) return TR_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int sm_count = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* st = nullptr;
+        tr_status s = device_state(dev, &st);
+        if (s != TR_OK) return s;
+        sm_count = st->desc.sm_count;
+    }
+    const bool col_grads = dw || db;
+    const int64_t G = bw_ctas(a.rows, col_grads, order, sm_count);
+    if (col_grads) {
+        const size_t need = static_cast<size_t>(G) * static_cast<size_t>(a.cols) * sizeof(float) * ((dw && db) ? 2 : 1);
+        if (!ws || ws_bytes < need)
+            return fail(TR_ERR_INVALID_ARG, "the workspace is missing or smaller than tr_norm_backward_workspace_bytes");
+        float* p = static_cast<float*>(ws);
+        if (dw) {
+            a.part_w = p;
+            p += G * a.cols;
+        }
+        if (db) a.part_b = p;
+    }
+    const bool ordered = order == TR_ORDER_ORDERED_TREE;
+    e = launch_backward(op, ordered, bw_slots(a.cols), a, static_cast<int>(G), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    if (dw) {
+        tr_status s = axis_run(TR_OP_ROW_SUM, a.part_w, dw, nullptr, G, a.cols, a.cols, order, stream);
+        if (s != TR_OK) return s;
+    }
+    if (db) {
+        tr_status s = axis_run(TR_OP_ROW_SUM, a.part_b, db, nullptr, G, a.cols, a.cols, order, stream);
+        if (s != TR_OK) return s;
+    }
+    return TR_OK;
+}
+
+static BwArgs bw_blank(const float* x, float* dx, int64_t rows, int64_t cols) {
+    BwArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.x = x;
+    a.dx = dx;
+    a.rows = rows;
+    a.cols = static_cast<int>(cols);
+    return a;
+}
+
+tr_status tr_softmax_backward_f32(const float* y, const float* dy, float* dx, int64_t rows, int64_t cols,
+                                  tr_order order, cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!y || !dy || !dx) return fail(TR_ERR_INVALID_ARG, "y, dy and dx must not be null");
+    if (misaligned(y, 4) || misaligned(dy, 4) || misaligned(dx, 4))
+        return fail(TR_ERR_INVALID_ARG, "y, dy and dx must be 4-byte aligned");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    if (overlaps(dx, n, y, n) || overlaps(dx, n, dy, n)) return fail(TR_ERR_INVALID_ARG, "dx overlaps an input");
+    BwArgs a = bw_blank(y, dx, rows, cols);
+    a.dy = dy;
+    return bw_run(BW_SOFTMAX, a, order, nullptr, nullptr, nullptr, 0, stream);
+}
+
+tr_status tr_cross_entropy_backward_f32(const float* logits, const int64_t* labels, const float* dloss,
+                                        float* dlogits, int64_t rows, int64_t cols, tr_order order,
+                                        cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!logits || !labels || !dlogits) return fail(TR_ERR_INVALID_ARG, "logits, labels and dlogits must not be null");
+    if (misaligned(logits, 4) || misaligned(dlogits, 4) || misaligned(dloss, 4) || misaligned(labels, 8))
+        return fail(TR_ERR_INVALID_ARG, "misaligned pointer");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    if (overlaps(dlogits, n, logits, n) || overlaps(dlogits, n, labels, static_cast<size_t>(rows) * 8) ||
+        overlaps(dlogits, n, dloss, static_cast<size_t>(rows) * 4))
+        return fail(TR_ERR_INVALID_ARG, "dlogits overlaps an input");
+    BwArgs a = bw_blank(logits, dlogits, rows, cols);
+    a.labels = labels;
+    a.dloss = dloss;
+    return bw_run(BW_XENT, a, order, nullptr, nullptr, nullptr, 0, stream);
+}
+
+static tr_status norm_bw_call(int op, const float* x, const float* w, const float* dy, float* dx, float* dw,
+                              float* db, int64_t rows, int64_t cols, float eps, tr_order order, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+    tr_status s = validate_common(rows, cols, order);
+    if (s != TR_OK) return s;
+    s = validate_eps(eps);
+    if (s != TR_OK) return s;
+    if (rows == 0) return TR_OK;
+    if (!x || !dy || !dx) return fail(TR_ERR_INVALID_ARG, "x, dy and dx must not be null");
+    if (misaligned(x, 4) || misaligned(dy, 4) || misaligned(dx, 4) || misaligned(w, 4) || misaligned(dw, 4) ||
+        misaligned(db, 4) || misaligned(ws, 16))
+        return fail(TR_ERR_INVALID_ARG, "misaligned pointer (the workspace must be 16-byte aligned)");
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) * 4;
+    const size_t nc = static_cast<size_t>(cols) * 4;
+    const void* ins[] = {x, dy, w};
+    const size_t in_n[] = {n, n, nc};
+    float* outs[] = {dx, dw, db};
+    const size_t out_n[] = {n, nc, nc};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 3; ++i)
+            if (overlaps(outs[o], out_n[o], ins[i], in_n[i])) return fail(TR_ERR_INVALID_ARG, "an output overlaps an input");
+        for (int p = o + 1; p < 3; ++p)
+            if (overlaps(outs[o], out_n[o], outs[p], out_n[p])) return fail(TR_ERR_INVALID_ARG, "two outputs overlap");
+        if (overlaps(outs[o], out_n[o], ws, ws_bytes)) return fail(TR_ERR_INVALID_ARG, "an output overlaps the workspace");
+    }
+    for (int i = 0; i < 3; ++i)
+        if ((dw || db) && overlaps(ws, ws_bytes, ins[i], in_n[i]))
+            return fail(TR_ERR_INVALID_ARG, "the workspace overlaps an input");
+    BwArgs a = bw_blank(x, dx, rows, cols);
+    a.dy = dy;
+    a.w = w;
+    a.eps = eps;
+    return bw_run(op, a, order, dw, db, ws, ws_bytes, stream);
+}
+
+tr_status tr_rmsnorm_backward_f32(const float* x, const float* w, const float* dy, float* dx, float* dw,
+                                  int64_t rows, int64_t cols, float eps, tr_order order, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+    return norm_bw_call(BW_RMSNORM, x, w, dy, dx, dw, nullptr, rows, cols, eps, order, workspace, workspace_bytes,
+                        stream);
+}
+
+tr_status tr_layernorm_backward_f32(const float* x, const float* gamma, const float* dy, float* dx, float* dgamma,
+                                    float* dbeta, int64_t rows, int64_t cols, float eps, tr_order order,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return norm_bw_call(BW_LAYERNORM, x, gamma, dy, dx, dgamma, dbeta, rows, cols, eps, order, workspace,
+                        workspace_bytes, stream);
 }
 
 tr_status tr_add_rmsnorm_f32(const float* x, const float* residual, const float* w, float* y, float* h,

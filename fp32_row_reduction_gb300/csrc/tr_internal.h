@@ -138,4 +138,27 @@ constexpr int kOrderedSlots[] = {0, 1, 2, 4, 6, 8, 12, 16}; // 0: re-read plan
 constexpr int kOrderedStagedSlots[] = {1, 2, 4, 8};
 constexpr int kOrderedThreads = 256;                  // OT-1024: 256 workers x 4 leaves
 
+// Backward passes: one CTA of 256 threads per row in the OT-1024 layout (thread
+// t owns columns 1024j + 4t .. +3); CTA c takes rows c, c + G, c + 2G, ...
+enum BwOp : int { BW_SOFTMAX = 0, BW_XENT = 1, BW_RMSNORM = 2, BW_LAYERNORM = 3 };
+constexpr int kBwSlots[] = {0, 1, 2, 4, 6, 8};  // 0: rows longer than 8192 columns, read again per pass
+constexpr int kBwMaxPartialCtas = 1024;        // ordered column gradients: one CTA per OT-1024 leaf of rows
+
+struct BwArgs {
+    const float* x;          // softmax: y (the forward output); cross-entropy: logits; norms: x
+    const float* dy;         // softmax, norms: the upstream gradient (rows x cols)
+    const float* w;          // norms: weight / gamma (null: 1)
+    const int64_t* labels;   // cross-entropy
+    const float* dloss;      // cross-entropy: per-row upstream gradient (null: 1)
+    float* dx;               // rows x cols
+    float* part_w;           // norms: G x cols per-CTA column sums of the weight-gradient terms (null: none)
+    float* part_b;           // LayerNorm: G x cols per-CTA column sums of dy (null: none)
+    int64_t rows;
+    int cols;
+    float eps;
+};
+
+// Launch backward op `op` (BwOp) with K cached quads per thread (0: re-read) on G CTAs.
+cudaError_t launch_backward(int op, bool ordered, int slots, const BwArgs& a, int ctas, cudaStream_t stream);
+
 }  // namespace tr

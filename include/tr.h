@@ -197,6 +197,44 @@ tr_status tr_row_min_f32(const float* x, float* out, int64_t rows, int64_t cols,
 tr_status tr_row_minmax_f32(const float* x, float* out_min, float* out_max, int64_t rows, int64_t cols,
                             tr_order order, cudaStream_t stream);
 
+/* ---- backward passes --------------------------------------------------------
+ * The gradients of the four row operators (the pages define the forward
+ * operators only; these are the next rows of the same row-reduction family).
+ * All tensors are device memory, row major; rows x cols unless stated.
+ *
+ *   softmax        dx = y * (dy - sum_j dy_j y_j), y = the forward output
+ *   cross-entropy  dlogits = dloss_r * (softmax(logits) - onehot(label)); a
+ *                  label outside [0, cols) has no one-hot term; dloss: rows
+ *                  floats, or NULL for 1
+ *   RMSNorm        dx = r (g - x r^2 mean(g x)), g = dy w, r = 1/sqrt(mean(x^2)+eps);
+ *                  dw = sum over rows of dy x r (cols floats, or NULL)
+ *   LayerNorm      dx = r (g - mean(g) - xh mean(g xh)), xh = (x - mean) r,
+ *                  g = dy gamma; dgamma = sum over rows of dy xh, dbeta = sum
+ *                  over rows of dy (each cols floats, or NULL)
+ *
+ * w / gamma may be NULL (weight 1). Outputs may overlap no input, no other
+ * output and not the workspace. Under TR_ORDER_ORDERED_TREE every row sum and
+ * every column sum is OT-1024 with each binary32 step rounded in the order
+ * written above, bit-identical to the CPU emulation; unordered results meet a
+ * rounding bound. The column gradients need a caller-owned, 16-byte-aligned
+ * device workspace of at least tr_norm_backward_workspace_bytes(rows, cols)
+ * bytes (none when dw, dgamma and dbeta are NULL); their final column
+ * reduction may use the stream's library workspace, allocated on the first
+ * such call on the stream, which therefore must not be captured. */
+tr_status tr_softmax_backward_f32(const float* y, const float* dy, float* dx, int64_t rows, int64_t cols,
+                                  tr_order order, cudaStream_t stream);
+tr_status tr_cross_entropy_backward_f32(const float* logits, const int64_t* labels, const float* dloss,
+                                        float* dlogits, int64_t rows, int64_t cols, tr_order order,
+                                        cudaStream_t stream);
+tr_status tr_rmsnorm_backward_f32(const float* x, const float* w, const float* dy, float* dx, float* dw,
+                                  int64_t rows, int64_t cols, float eps, tr_order order, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+tr_status tr_layernorm_backward_f32(const float* x, const float* gamma, const float* dy, float* dx, float* dgamma,
+                                    float* dbeta, int64_t rows, int64_t cols, float eps, tr_order order,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+/* Host only: workspace bytes of a norm backward pass of rows x cols. */
+tr_status tr_norm_backward_workspace_bytes(int64_t rows, int64_t cols, size_t* bytes);
+
 /* ---- reductions over a non-last axis --------------------------------------
  * "TIRx Metal reduction lowering", Reductions inside composed groups: the
  * reduced axis need not be the last memory dimension. x is a contiguous

@@ -34,6 +34,8 @@ TAG_B = 3
 TAG_LABELS = 4
 TAG_ROW_OFFSET = 5
 TAG_RESIDUAL = 6
+TAG_DY = 7
+TAG_DLOSS = 8
 
 _CHUNK = 1 << 23  # elements generated per slice (bounds temporary memory)
 
@@ -199,6 +201,16 @@ WORKLOADS = {
     "axis_sum_768x6144": dict(op="axis_sum", rows=768, cols=6144, seed=2),
     "axis_minmax_768x6144": dict(op="axis_minmax", rows=768, cols=6144, seed=2),
 }
+
+
+def grad_f32(rows, cols, seed, device="cpu"):
+    """An upstream gradient dy ~ N(0, 1), i.i.d. per element."""
+    return normal_f32((rows, cols), seed, TAG_DY, 0.0, 1.0, device)
+
+
+def dloss_f32(rows, seed, device="cpu"):
+    """A per-row upstream loss gradient ~ U(0.5, 1.5)."""
+    return uniform_f32((rows,), seed, TAG_DLOSS, 0.5, 1.5, device)
 
 
 def make_inputs(op, rows, cols, seed, var=None, row_offset=False, device="cpu"):
