@@ -67,7 +67,10 @@ def alg_bytes(op, rows, cols):
             "row_minmax": 4 * e + 8 * rows,
             # reductions over axis 0: x read, one (two) values per column written
             "axis_sum": 4 * e + 4 * cols, "axis_max": 4 * e + 4 * cols, "axis_min": 4 * e + 4 * cols,
-            "axis_minmax": 4 * e + 8 * cols}[op]
+            "axis_minmax": 4 * e + 8 * cols,
+            # backward passes: inputs read once, dx (and the column gradients) written once
+            "softmax_bwd": 12 * e, "cross_entropy_bwd": 8 * e + 12 * rows,
+            "rmsnorm_bwd": 12 * e + 8 * cols, "layernorm_bwd": 12 * e + 12 * cols}[op]
 
 
 # The sources that define, select or launch the default step's kernels (the
@@ -171,27 +174,53 @@ class Launch:
         w = synth.WORKLOADS[workload]
         self.rows, self.cols = w["rows"], w["cols"]
         base = synth.workload_inputs(workload, device=device)
+        if op == "softmax_bwd":  # y = the forward output, by this library's softmax
+            base = {"y": tr.softmax(base["x"]), "dy": base["dy"]}
         self.inputs = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(sets - 1)]
         if op == "cross_entropy" or op.startswith("row_"):
             self.outputs = [torch.empty(self.rows, device=device) for _ in range(sets)]
         elif op.startswith("axis_"):
             self.outputs = [torch.empty(self.cols, device=device) for _ in range(sets)]
         else:
-            self.outputs = [torch.empty_like(base["x"]) for _ in range(sets)]
+            self.outputs = [torch.empty_like(base["x"] if "x" in base else base["y"]) for _ in range(sets)]
         # fused residual norms also write h = x + r
         self.h = [torch.empty_like(base["x"]) for _ in range(sets)] if op.startswith("add_") else None
         if op == "row_minmax":  # the maxima (the minima go to outputs)
             self.h = [torch.empty(self.rows, device=device) for _ in range(sets)]
         if op == "axis_minmax":
             self.h = [torch.empty(self.cols, device=device) for _ in range(sets)]
+        # norm backward passes: the column gradients and one workspace per buffer set
+        self.aux = None
+        if op in ("rmsnorm_bwd", "layernorm_bwd"):
+            nws = tr.norm_backward_workspace_bytes(self.rows, self.cols)
+            self.aux = [{"dw": torch.empty(self.cols, device=device), "db": torch.empty(self.cols, device=device),
+                         "ws": torch.empty(nws, dtype=torch.uint8, device=device)} for _ in range(sets)]
         self.bytes = alg_bytes(op, self.rows, self.cols)
         self.key = f"{op}/{self.order}/{self.rows}x{self.cols}"
 
     def __call__(self, s, stream=None):
-        self.tr.run_op(self.op, self.inputs[s], out=self.outputs[s], order=self.order, stream=stream,
-                       h_out=None if self.h is None else self.h[s])
+        d = self.inputs[s]
+        if self.op == "softmax_bwd":
+            self.tr.softmax_backward(d["y"], d["dy"], out=self.outputs[s], order=self.order, stream=stream)
+        elif self.op == "cross_entropy_bwd":
+            self.tr.cross_entropy_backward(d["x"], d["labels"], d["dloss"], out=self.outputs[s], order=self.order,
+                                           stream=stream)
+        elif self.op == "rmsnorm_bwd":
+            a = self.aux[s]
+            self.tr.rmsnorm_backward(d["x"], d["w"], d["dy"], order=self.order, dx=self.outputs[s], dw=a["dw"],
+                                     workspace=a["ws"], stream=stream)
+        elif self.op == "layernorm_bwd":
+            a = self.aux[s]
+            self.tr.layernorm_backward(d["x"], d["w"], d["dy"], order=self.order, dx=self.outputs[s],
+                                       dgamma=a["dw"], dbeta=a["db"], workspace=a["ws"], stream=stream)
+        else:
+            self.tr.run_op(self.op, d, out=self.outputs[s], order=self.order, stream=stream,
+                           h_out=None if self.h is None else self.h[s])
 
     def plan(self):
+        if self.op.endswith("_bwd"):
+            return {"kind": "backward", "block_threads": 256,
+                    "slots": next((k for k in (1, 2, 4, 6, 8) if self.cols <= 1024 * k), 0)}
         if self.op.startswith("axis_"):
             sm = torch.cuda.get_device_properties(0).multi_processor_count
             splits, tiles = self.tr.axis_launch_shape(self.op[len("axis_"):], 1, self.rows, self.cols, sm, self.order)
@@ -417,6 +446,10 @@ def oracle_fn(op, order):
                 "row_sum": lambda h: oracle.ot_row_sum(h["x"]), "row_max": lambda h: oracle.ot_row_max(h["x"]),
                 "row_min": lambda h: oracle.ot_row_min(h["x"]),
                 "row_minmax": lambda h: (oracle.ot_row_min(h["x"]), oracle.ot_row_max(h["x"])),
+                "softmax_bwd": lambda h: oracle.ot_softmax_backward(h["y"], h["dy"]),
+                "cross_entropy_bwd": lambda h: oracle.ot_cross_entropy_backward(h["x"], h["labels"], h["dloss"]),
+                "rmsnorm_bwd": lambda h: oracle.ot_rmsnorm_backward(h["x"], h["w"], h["dy"], 1e-5),
+                "layernorm_bwd": lambda h: oracle.ot_layernorm_backward(h["x"], h["w"], h["dy"], 1e-5),
                 "axis_sum": lambda h: oracle.ot_axis_sum(h["x"], 0),
                 "axis_minmax": lambda h: (oracle.ot_axis_min(h["x"], 0), oracle.ot_axis_max(h["x"], 0))}[op]
     return {"softmax": lambda h: oracle.softmax(h["x"]),
@@ -428,6 +461,10 @@ def oracle_fn(op, order):
             "row_sum": lambda h: oracle.row_sum(h["x"]), "row_max": lambda h: oracle.row_max(h["x"]),
             "row_min": lambda h: oracle.row_min(h["x"]),
             "row_minmax": lambda h: (oracle.row_min(h["x"]), oracle.row_max(h["x"])),
+            "softmax_bwd": lambda h: oracle.softmax_backward(h["y"], h["dy"]),
+            "cross_entropy_bwd": lambda h: oracle.cross_entropy_backward(h["x"], h["labels"], h["dloss"]),
+            "rmsnorm_bwd": lambda h: oracle.rmsnorm_backward(h["x"], h["w"], h["dy"], 1e-5),
+            "layernorm_bwd": lambda h: oracle.layernorm_backward(h["x"], h["w"], h["dy"], 1e-5),
             "axis_sum": lambda h: oracle.axis_sum(h["x"], 0),
             "axis_minmax": lambda h: (oracle.axis_min(h["x"], 0), oracle.axis_max(h["x"], 0))}[op]
 
@@ -436,7 +473,16 @@ def host_sample(op, workload, rows):
     w = synth.WORKLOADS[workload]
     d = synth.make_inputs(op, min(rows, w["rows"]), w["cols"], w["seed"], var=w.get("var"),
                           row_offset=w.get("row_offset", False))
-    return {k: v.numpy() for k, v in d.items()}
+    h = {k: v.numpy() for k, v in d.items()}
+    if op == "softmax_bwd":
+        import oracle
+        h = {"y": oracle.ot_softmax(h["x"]), "dy": h["dy"]}
+    return h
+
+
+def sample_shape(h):
+    """(rows, cols) of a host sample (the softmax backward's matrix is y)."""
+    return (h["x"] if "x" in h else h["y"]).shape
 
 
 def time_oracle(specs, rows_per_launch, budget_s=None, repeats=1):
@@ -449,7 +495,7 @@ def time_oracle(specs, rows_per_launch, budget_s=None, repeats=1):
             fn(h)
         t_total += time.perf_counter() - t0
         reps += 1
-        done_bytes += sum(alg_bytes(op, h["x"].shape[0], h["x"].shape[1]) for _, h, op, _ in samples)
+        done_bytes += sum(alg_bytes(op, *sample_shape(h)) for _, h, op, _ in samples)
         if budget_s is None and reps >= repeats:
             break
         if budget_s is not None and t_total >= budget_s:
@@ -476,7 +522,7 @@ def run_reference(args, rank, world):
     per_row = max(t1, 1e-5)
     rows = int(max(1, min(768, 120.0 / (args.steps + args.warmup) / per_row)))
     samples = [(oracle_fn(op, o), host_sample(op, w, rows), op) for op, w, o in specs]
-    step_bytes = sum(alg_bytes(op, h["x"].shape[0], h["x"].shape[1]) for _, h, op in samples)
+    step_bytes = sum(alg_bytes(op, *sample_shape(h)) for _, h, op in samples)
     for _ in range(args.warmup):
         for fn, h, _ in samples:
             fn(h)

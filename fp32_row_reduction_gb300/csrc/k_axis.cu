@@ -109,6 +109,35 @@ __device__ __forceinline__ void ld_cols(const float* p, float (&v)[V]) {
     }
 }
 
+// Element (row r) of this thread's V columns: x itself, or a backward term.
+// Ordered (O): each binary32 step rounded in the written order.
+template <int TERM, bool O, int V>
+__device__ __forceinline__ void ld_elem(const AxisArgs& a, const float* p, int64_t r, float (&v)[V]) {
+    if constexpr (TERM == AXIS_PLAIN) {
+        ld_cols<V>(p, v);
+    } else {
+        float d[V];
+        ld_cols<V>(a.dy + (p - a.x), d);
+        if constexpr (TERM == AXIS_LN_BETA) {
+#pragma unroll
+            for (int c = 0; c < V; ++c) v[c] = d[c];
+        } else {
+            float x[V];
+            ld_cols<V>(p, x);
+            const float s0 = __ldg(a.sa + r);
+            if constexpr (TERM == AXIS_RMS_W) {
+#pragma unroll
+                for (int c = 0; c < V; ++c) v[c] = O ? __fmul_rn(__fmul_rn(d[c], x[c]), s0) : d[c] * x[c] * s0;
+            } else {
+                const float s1 = __ldg(a.sb + r);
+#pragma unroll
+                for (int c = 0; c < V; ++c)
+                    v[c] = O ? __fmul_rn(d[c], __fmul_rn(__fsub_rn(x[c], s0), s1)) : d[c] * ((x[c] - s0) * s1);
+            }
+        }
+    }
+}
+
 // Push the subtree value `cur` (the n-th of its block, n from 0) onto a stack
 // of pending left siblings; after the last push of a block of 2^d values,
 // `cur` holds the block's tree. No break: every level index stays a constant,
@@ -131,9 +160,9 @@ __device__ __forceinline__ void push(float (&stk)[5][V], float (&cur)[V], int n)
 
 // The OT-1024 subtree over quad positions p0 .. p0 + P - 1 (P a power of two,
 // at most 32) of this thread's columns; `col` points at row 0 of them.
-template <class F, int V, int B>  // B quads loaded together
-__device__ __forceinline__ void tree_block(const float* col, bool jok, int64_t R, int64_t inner, int p0, int P,
-                                           float (&out)[V]) {
+template <class F, int V, int B, int TERM = AXIS_PLAIN>  // B quads loaded together
+__device__ __forceinline__ void tree_block(const AxisArgs& a, const float* col, bool jok, int64_t R, int64_t inner,
+                                           int p0, int P, float (&out)[V]) {
     float stk[5][V];
     float cur[V];
 #pragma unroll
@@ -148,12 +177,14 @@ __device__ __forceinline__ void tree_block(const float* col, bool jok, int64_t R
         float lf[B][4][V];
         const float* qp[B];
         int64_t left[B];  // rows of the quad's first leaf from this round on
+        int64_t rowb[B];  // the row of the quad's first leaf in this round
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             // first leaf row of position p: 4t, t = 32 * group + bit-reversed lane
             const int p = p0 + n0 + b;
             const int e0 = 4 * (32 * (p >> 5) + static_cast<int>(__brev(p & 31) >> 27));
             qp[b] = col + e0 * inner;
+            rowb[b] = e0;
             left[b] = (jok && b < nb) ? R - e0 : 0;
 #pragma unroll
             for (int v = 0; v < 4; ++v)
@@ -168,7 +199,7 @@ __device__ __forceinline__ void tree_block(const float* col, bool jok, int64_t R
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     if (v < left[b]) {
-                        ld_cols<V>(qp[b] + v * inner, val[b][v]);
+                        ld_elem<TERM, true, V>(a, qp[b] + v * inner, rowb[b] + v, val[b][v]);
                     } else {
 #pragma unroll
                         for (int c = 0; c < V; ++c) val[b][v][c] = 0.0f;
@@ -184,6 +215,7 @@ __device__ __forceinline__ void tree_block(const float* col, bool jok, int64_t R
                     }
                 qp[b] += step;
                 left[b] -= 1024;
+                rowb[b] += 1024;
             }
         }
 #pragma unroll
@@ -214,7 +246,7 @@ __device__ __forceinline__ float cta_tree(const float (*g)[kAxisCols * 4], int i
 template <int MODE>
 constexpr int min_ctas() { return MODE == TREE ? kAxisCtasTree : kAxisCtasFree; }
 
-template <int OP, int MODE, int V>
+template <int OP, int MODE, int V, int TERM = AXIS_PLAIN>
 __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(AxisArgs a) {
     constexpr int N = nvals<OP, MODE>();
     constexpr int W = kAxisCols * V;  // columns of the tile
@@ -236,13 +268,16 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
     if constexpr (MODE == TREE) {
         static_assert(OP == OP_RSUM, "the tree mode folds sums");
         const int P = kQuads / (S * kWarps);
-        tree_block<AddF, V, V == 4 ? 1 : 4>(col, jok, R, inner, s * (kQuads / S) + w * P, P, res[0]);
+        // quads loaded together: fewer when each element is a term of two loads
+        constexpr int B = V == 4 ? 1 : (TERM == AXIS_PLAIN ? 4 : 2);
+        tree_block<AddF, V, B, TERM>(a, col, jok, R, inner, s * (kQuads / S) + w * P, P, res[0]);
     } else {
         // rows [r0, r1) of this split, interleaved over the warps
         const int64_t base = R / S, extra = R % S;
         const int64_t r0 = s * base + (s < extra ? s : extra);
         const int64_t r1 = r0 + base + (s < extra ? 1 : 0);
-        constexpr int U = V == 4 ? 4 : 8;  // loads in flight per thread
+        // loads in flight per thread (a term loads two elements)
+        constexpr int U = (V == 4 ? 4 : 8) / (TERM == AXIS_PLAIN || TERM == AXIS_LN_BETA ? 1 : 2);
         float acc[4][N][V];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -256,7 +291,7 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     if (r + u * kWarps < r1) {
-                        ld_cols<V>(col + (r + u * kWarps) * inner, v[u]);
+                        ld_elem<TERM, false, V>(a, col + (r + u * kWarps) * inner, r + u * kWarps, v[u]);
                     } else {
 #pragma unroll
                         for (int c = 0; c < V; ++c) v[u][c] = 0.0f;
@@ -382,8 +417,8 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
 #pragma unroll 1
                 for (int c = 0; c < V; ++c) {  // one column at a time keeps the registers low
                     float tc[1];
-                    if (k == 0) tree_block<CMinF, 1, 1>(col + c, jok, R, inner, 32 * w, 32, tc);
-                    else tree_block<CMaxF, 1, 1>(col + c, jok, R, inner, 32 * w, 32, tc);
+                    if (k == 0) tree_block<CMinF, 1, 1>(a, col + c, jok, R, inner, 32 * w, 32, tc);
+                    else tree_block<CMaxF, 1, 1>(a, col + c, jok, R, inner, 32 * w, 32, tc);
                     g[0][w][lane * V + c] = tc[0];
                 }
                 __syncthreads();
@@ -440,6 +475,28 @@ cudaError_t launch(bool ordered, const AxisArgs& a, int vec, int64_t tiles, int 
 }
 
 }  // namespace axis
+
+template <int TERM>
+cudaError_t launch_term(bool ordered, const AxisArgs& a, int vec, int64_t tiles, int splits, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(splits));
+    if (ordered)
+        axis::axis_kernel<OP_RSUM, axis::TREE, 1, TERM><<<grid, kAxisThreads, 0, stream>>>(a);
+    else if (vec == 4)
+        axis::axis_kernel<OP_RSUM, axis::FREE, 4, TERM><<<grid, kAxisThreads, 0, stream>>>(a);
+    else
+        axis::axis_kernel<OP_RSUM, axis::FREE, 1, TERM><<<grid, kAxisThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_axis_term(int term, bool ordered, const AxisArgs& a, int vec, int64_t tiles, int splits,
+                             cudaStream_t stream) {
+    switch (term) {
+        case AXIS_RMS_W: return launch_term<AXIS_RMS_W>(ordered, a, vec, tiles, splits, stream);
+        case AXIS_LN_GAMMA: return launch_term<AXIS_LN_GAMMA>(ordered, a, vec, tiles, splits, stream);
+        case AXIS_LN_BETA: return launch_term<AXIS_LN_BETA>(ordered, a, vec, tiles, splits, stream);
+    }
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_axis(int op, bool ordered, const AxisArgs& a, int vec, int64_t tiles, int splits,
                         cudaStream_t stream) {

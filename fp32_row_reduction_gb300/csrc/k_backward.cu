@@ -16,12 +16,10 @@
 // with contracted arithmetic and the hardware exp2). Rows of at most 1024 K
 // columns stay in registers; longer rows are read again for each pass.
 //
-// Column gradients (dw, dgamma, dbeta): CTA c of G takes rows c, c + G, ...
-// in increasing order and folds its rows' terms per column, starting from +0,
-// into its own row of a G x cols partial matrix; a column reduction over that
-// matrix finishes them. With G = min(rows, 1024), partial row c is exactly
-// leaf c of OT-1024 over the column's terms, so the ordered column reduction
-// of the partials gives the ordered column gradient bit for bit.
+// Column gradients (dw, dgamma, dbeta): the row kernel writes each row's
+// statistics (1/rms; mean and 1/sigma), and a column sum over the rows of the
+// per-element terms, recomputed from x, dy and those statistics, finishes them
+// (ordered: OT-1024 over each column's terms, as every ordered column sum).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -70,20 +68,33 @@ __device__ __forceinline__ void load_param_quad(const float* w, int cols, int j,
     }
 }
 
-// Partial column sums: the CTA's own row of the G x cols matrix. The first row
-// of a CTA writes its terms (+0 + t, which is t unless t is -0), later rows add.
-template <bool O>
-__device__ __forceinline__ void fold_partial(float* pr, int cols, int j, bool first, const float (&t)[4],
-                                             const bool (&ok)[4]) {
-    const int c0 = 1024 * j + 4 * static_cast<int>(threadIdx.x);
-#pragma unroll
-    for (int v = 0; v < 4; ++v)
-        if (ok[v]) pr[c0 + v] = first ? add<O>(0.0f, t[v]) : add<O>(pr[c0 + v], t[v]);
+// 16-byte asynchronous copy global -> shared (no registers held while in flight).
+__device__ __forceinline__ void cp_async16(void* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Stage quad j of a row into this thread's shared-memory slot: an async copy
+// when the quad is a whole aligned float4, plain loads otherwise (0 outside).
+__device__ __forceinline__ void stage_quad(float4* slot, const float* r, int cols, int j, bool aligned) {
+    const int c0 = 1024 * j + 4 * static_cast<int>(threadIdx.x);
+    if (aligned && c0 + 3 < cols) {
+        cp_async16(slot, r + c0);
+    } else {
+        float q[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) q[v] = c0 + v < cols ? ld_stream1(r + c0 + v) : 0.0f;
+        *slot = make_float4(q[0], q[1], q[2], q[3]);
+    }
+}
+
+// Shared memory of a launch: x and (but for cross-entropy) dy, K quads per thread.
+template <int OP>
+constexpr size_t bw_smem_per_slot() { return (OP == BW_XENT ? 1 : 2) * kOrderedThreads * sizeof(float4); }
 
 template <int OP, int K, bool O>
 __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
-    constexpr int KC = K > 0 ? K : 1;
+    extern __shared__ float4 smem_raw[];
     __shared__ float gpart[2][8];
     int buf = 0;
     const int cols = a.cols;
@@ -99,16 +110,36 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
         const bool x_al = aligned16(xr);
         const bool d_al = dr && aligned16(dr);
         const bool y_al = aligned16(yr);
-        float cx[KC][4], cd[KC][4];
-        if constexpr (K > 0) {
-#pragma unroll
-            for (int j = 0; j < K; ++j) {
-                bool ok[4];
-                if (j < nj) {
-                    load_quad(xr, cols, j, x_al, cx[j], ok);
-                    if constexpr (OP != BW_XENT) load_quad(dr, cols, j, d_al, cd[j], ok);
+        // the row's quads in shared memory, each thread's own slots (no barrier):
+        // x at cache[j][t], dy at cache[K + j][t]; staged by async copies, the
+        // next row's quad j as soon as the last pass has used this row's
+        float4* cache = reinterpret_cast<float4*>(smem_raw);
+        auto slot_x = [&](int j) { return cache + j * kOrderedThreads + threadIdx.x; };
+        auto slot_d = [&](int j) { return cache + (K + j) * kOrderedThreads + threadIdx.x; };
+        const int64_t next = row + gridDim.x;
+        auto stage_next = [&](int j) {
+            if constexpr (K > 0) {
+                if (next < a.rows) {
+                    const float* nx = a.x + next * cols;
+                    stage_quad(slot_x(j), nx, cols, j, aligned16(nx));
+                    if constexpr (OP != BW_XENT) {
+                        const float* nd = a.dy + next * cols;
+                        stage_quad(slot_d(j), nd, cols, j, aligned16(nd));
+                    }
                 }
             }
+        };
+        if constexpr (K > 0) {
+            if (first) {
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (j < nj) {
+                        stage_quad(slot_x(j), xr, cols, j, x_al);
+                        if constexpr (OP != BW_XENT) stage_quad(slot_d(j), dr, cols, j, d_al);
+                    }
+                }
+            }
+            cp_async_wait_all();
         }
         // fn(j, x quad, dy quad, valid columns) for every quad of the row, in increasing j
         auto for_quads = [&](auto&& fn) {
@@ -119,7 +150,14 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
                         bool ok[4];
 #pragma unroll
                         for (int v = 0; v < 4; ++v) ok[v] = 1024 * j + t4 + v < cols;
-                        fn(j, cx[j], cd[j], ok);
+                        const float4 vx = *slot_x(j);
+                        float qx[4] = {vx.x, vx.y, vx.z, vx.w};
+                        float qd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        if constexpr (OP != BW_XENT) {
+                            const float4 vd = *slot_d(j);
+                            qd[0] = vd.x; qd[1] = vd.y; qd[2] = vd.z; qd[3] = vd.w;
+                        }
+                        fn(j, qx, qd, ok);
                     }
                 }
             } else {
@@ -147,6 +185,7 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
 #pragma unroll
                 for (int v = 0; v < 4; ++v) o[v] = mul<O>(y[v], sub<O>(d[v], s));
                 store_quad(yr, cols, j, y_al, o, ok);
+                stage_next(j);
             });
         } else if constexpr (OP == BW_XENT) {
             clear(__int_as_float(0xff800000));
@@ -175,6 +214,7 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
                     o[v] = scaled ? mul<O>(d, dl) : d;
                 }
                 store_quad(yr, cols, j, y_al, o, ok);
+                stage_next(j);
             });
         } else if constexpr (OP == BW_RMSNORM) {
             clear(0.0f);
@@ -207,19 +247,14 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
             });
             const float cs = tree<Add>(leaf, gpart, buf);
             const float k = mul<O>(mul<O>(divide<O>(cs, n), inv), inv);
-            float* pw = a.part_w ? a.part_w + static_cast<int64_t>(blockIdx.x) * cols : nullptr;
+            if (a.stat_a && threadIdx.x == 0) a.stat_a[row] = inv;
             for_quads([&](int j, const float (&x)[4], const float (&d)[4], const bool (&ok)[4]) {
                 float g[4], o[4];
                 grad_in(j, d, g);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) o[v] = mul<O>(inv, sub<O>(g[v], mul<O>(x[v], k)));
                 store_quad(yr, cols, j, y_al, o, ok);
-                if (pw) {
-                    float t[4];
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) t[v] = mul<O>(mul<O>(d[v], x[v]), inv);
-                    fold_partial<O>(pw, cols, j, first, t, ok);
-                }
+                stage_next(j);
             });
         } else {
             clear(0.0f);
@@ -266,42 +301,48 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
             });
             const float ga = divide<O>(tree<Add>(leaf, gpart, buf), n);
             const float gb = divide<O>(tree<Add>(lb, gpart, buf), n);
-            float* pw = a.part_w ? a.part_w + static_cast<int64_t>(blockIdx.x) * cols : nullptr;
-            float* pb = a.part_b ? a.part_b + static_cast<int64_t>(blockIdx.x) * cols : nullptr;
+            if (a.stat_a && threadIdx.x == 0) {
+                a.stat_a[row] = mean;
+                a.stat_b[row] = inv;
+            }
             for_quads([&](int j, const float (&x)[4], const float (&d)[4], const bool (&ok)[4]) {
-                float g[4], o[4], xh[4];
+                float g[4], o[4];
                 grad_in(j, d, g);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    xh[v] = mul<O>(sub<O>(x[v], mean), inv);
-                    o[v] = mul<O>(inv, sub<O>(sub<O>(g[v], ga), mul<O>(xh[v], gb)));
+                    const float xh = mul<O>(sub<O>(x[v], mean), inv);
+                    o[v] = mul<O>(inv, sub<O>(sub<O>(g[v], ga), mul<O>(xh, gb)));
                 }
                 store_quad(yr, cols, j, y_al, o, ok);
-                if (pw) {
-                    float t[4];
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) t[v] = mul<O>(d[v], xh[v]);
-                    fold_partial<O>(pw, cols, j, first, t, ok);
-                }
-                if (pb) fold_partial<O>(pb, cols, j, first, d, ok);
+                stage_next(j);
             });
         }
     }
 }
 
+template <int OP, int K, bool O>
+cudaError_t launch_k(const BwArgs& a, int ctas, cudaStream_t stream) {
+    const size_t smem = K * bw_smem_per_slot<OP>();
+    if (smem > 40 * 1024) {  // beyond the default 48 KB once the static shared memory is added
+        const cudaError_t e = cudaFuncSetAttribute(bw_kernel<OP, K, O>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    bw_kernel<OP, K, O><<<dim3(static_cast<unsigned>(ctas)), kOrderedThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <int OP, bool O>
 cudaError_t launch_op(int slots, const BwArgs& a, int ctas, cudaStream_t stream) {
-    const dim3 grid(static_cast<unsigned>(ctas));
     switch (slots) {
-        case 0: bw_kernel<OP, 0, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
-        case 1: bw_kernel<OP, 1, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
-        case 2: bw_kernel<OP, 2, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
-        case 4: bw_kernel<OP, 4, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
-        case 6: bw_kernel<OP, 6, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
-        case 8: bw_kernel<OP, 8, O><<<grid, kOrderedThreads, 0, stream>>>(a); break;
-        default: return cudaErrorInvalidValue;
+        case 0: return launch_k<OP, 0, O>(a, ctas, stream);
+        case 1: return launch_k<OP, 1, O>(a, ctas, stream);
+        case 2: return launch_k<OP, 2, O>(a, ctas, stream);
+        case 4: return launch_k<OP, 4, O>(a, ctas, stream);
+        case 6: return launch_k<OP, 6, O>(a, ctas, stream);
+        case 8: return launch_k<OP, 8, O>(a, ctas, stream);
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 template <int OP>

@@ -619,61 +619,66 @@ static int bw_slots(int64_t cols) {
     return 0;
 }
 
-// CTAs of a backward launch. With column gradients: min(rows, 1024) ordered (CTA
-// c's partial row is leaf c of OT-1024 over the rows), two per SM unordered
-// (fewer partial rows to reduce); without: one CTA per row (grid capped, the
-// CTAs loop over the rest).
-static int64_t bw_ctas(int64_t rows, bool col_grads, tr_order order, int sm_count) {
-    if (!col_grads) return rows < (1LL << 20) ? rows : (1LL << 20);
-    const int64_t cap = order == TR_ORDER_ORDERED_TREE ? kBwMaxPartialCtas : 2LL * sm_count;
-    return rows < cap ? rows : cap;
-}
+// CTAs of a backward launch: one per row (capped; the CTAs loop over the rest).
+static int64_t bw_ctas(int64_t rows) { return rows < (1LL << 20) ? rows : (1LL << 20); }
 
 tr_status tr_norm_backward_workspace_bytes(int64_t rows, int64_t cols, size_t* bytes) {
     if (!bytes) return fail(TR_ERR_INVALID_ARG, "bytes must not be null");
     tr_status s = validate_common(rows, cols, TR_ORDER_UNORDERED_TREE);
     if (s != TR_OK) return s;
-    const int64_t g = rows < kBwMaxPartialCtas ? rows : kBwMaxPartialCtas;
-    *bytes = static_cast<size_t>(g) * static_cast<size_t>(cols) * 2 * sizeof(float);
+    *bytes = static_cast<size_t>(rows) * 2 * sizeof(float);  // two statistics per row
+    return TR_OK;
+}
+
+// The column sum over the rows of a norm backward term (see AxisTerm).
+static tr_status term_sum(int term, const BwArgs& b, float* out, tr_order order, cudaStream_t stream) {
+    const int64_t rows = b.rows, cols = b.cols;
+    const bool ordered = order == TR_ORDER_ORDERED_TREE;
+    const int vec = (!ordered && cols % 4 == 0 && !misaligned(b.x, 16) && !misaligned(b.dy, 16)) ? 4 : 1;
+    const int64_t tiles = (cols + kAxisCols * vec - 1) / (kAxisCols * vec);
+    AxisArgs a{b.x, out, nullptr, rows, cols, cols, nullptr, nullptr, b.dy, b.stat_a, b.stat_b};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int S = 1;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* st = nullptr;
+        tr_status s = device_state(dev, &st);
+        if (s != TR_OK) return s;
+        S = axis_splits(tiles, rows, 1, kAxisCols * vec, ordered ? kAxisCtasTree : kAxisCtasFree, st->desc.sm_count);
+        if (S > 1) {
+            void* ws = nullptr;
+            s = split_workspace(*st, stream, &ws);
+            if (s != TR_OK) return s;
+            a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kAxisPartOffset);
+            a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kAxisTicketOffset);
+        }
+    }
+    e = launch_axis_term(term, ordered, a, vec, tiles, S, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "column gradient launch");
     return TR_OK;
 }
 
 static tr_status bw_run(int op, BwArgs a, tr_order order, float* dw, float* db, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
     if (a.rows == 0) return TR_OK;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    int sm_count = 0;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        DeviceState* st = nullptr;
-        tr_status s = device_state(dev, &st);
-        if (s != TR_OK) return s;
-        sm_count = st->desc.sm_count;
-    }
-    const bool col_grads = dw || db;
-    const int64_t G = bw_ctas(a.rows, col_grads, order, sm_count);
-    if (col_grads) {
-        const size_t need = static_cast<size_t>(G) * static_cast<size_t>(a.cols) * sizeof(float) * ((dw && db) ? 2 : 1);
+    if (dw || db) {
+        const size_t need = static_cast<size_t>(a.rows) * 2 * sizeof(float);
         if (!ws || ws_bytes < need)
             return fail(TR_ERR_INVALID_ARG, "the workspace is missing or smaller than tr_norm_backward_workspace_bytes");
-        float* p = static_cast<float*>(ws);
-        if (dw) {
-            a.part_w = p;
-            p += G * a.cols;
-        }
-        if (db) a.part_b = p;
+        a.stat_a = static_cast<float*>(ws);
+        a.stat_b = a.stat_a + a.rows;
     }
     const bool ordered = order == TR_ORDER_ORDERED_TREE;
-    e = launch_backward(op, ordered, bw_slots(a.cols), a, static_cast<int>(G), stream);
+    cudaError_t e = launch_backward(op, ordered, bw_slots(a.cols), a, static_cast<int>(bw_ctas(a.rows)), stream);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     if (dw) {
-        tr_status s = axis_run(TR_OP_ROW_SUM, a.part_w, dw, nullptr, G, a.cols, a.cols, order, stream);
+        tr_status s = term_sum(op == BW_RMSNORM ? AXIS_RMS_W : AXIS_LN_GAMMA, a, dw, order, stream);
         if (s != TR_OK) return s;
     }
     if (db) {
-        tr_status s = axis_run(TR_OP_ROW_SUM, a.part_b, db, nullptr, G, a.cols, a.cols, order, stream);
+        tr_status s = term_sum(AXIS_LN_BETA, a, db, order, stream);
         if (s != TR_OK) return s;
     }
     return TR_OK;

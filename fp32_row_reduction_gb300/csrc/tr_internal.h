@@ -75,7 +75,25 @@ struct AxisArgs {
     int64_t ncols;    // outer * inner output columns
     float* part;      // splits > 1: per-CTA partials (tiles * splits * values * columns of a tile)
     unsigned* ticket; // splits > 1: per-tile arrival tickets (zero between launches)
+    // column gradients of the norm backward passes (term != AXIS_PLAIN): the
+    // reduced element of row r is a term of x, dy (same layout as x) and the
+    // row's statistics sa[r], sb[r]
+    const float* dy;
+    const float* sa;
+    const float* sb;
 };
+
+// The element an axis sum reduces: x itself, or a term of a norm backward pass.
+enum AxisTerm : int {
+    AXIS_PLAIN = 0,
+    AXIS_RMS_W = 1,   // (dy x) r,              sa = r = 1 / rms
+    AXIS_LN_GAMMA = 2,  // dy ((x - mean) r),   sa = mean, sb = r = 1 / sigma
+    AXIS_LN_BETA = 3  // dy
+};
+
+// Launch the column sum of a norm backward term (AXIS_RMS_W .. AXIS_LN_BETA).
+cudaError_t launch_axis_term(int term, bool ordered, const AxisArgs& a, int vec, int64_t tiles, int splits,
+                             cudaStream_t stream);
 
 // Floats of one ring slot for rows of `cols` floats: the row's 16-byte-aligned
 // body plus one partial 16-byte chunk on each side.
@@ -142,7 +160,6 @@ constexpr int kOrderedThreads = 256;                  // OT-1024: 256 workers x 
 // t owns columns 1024j + 4t .. +3); CTA c takes rows c, c + G, c + 2G, ...
 enum BwOp : int { BW_SOFTMAX = 0, BW_XENT = 1, BW_RMSNORM = 2, BW_LAYERNORM = 3 };
 constexpr int kBwSlots[] = {0, 1, 2, 4, 6, 8};  // 0: rows longer than 8192 columns, read again per pass
-constexpr int kBwMaxPartialCtas = 1024;        // ordered column gradients: one CTA per OT-1024 leaf of rows
 
 struct BwArgs {
     const float* x;          // softmax: y (the forward output); cross-entropy: logits; norms: x
@@ -151,8 +168,9 @@ struct BwArgs {
     const int64_t* labels;   // cross-entropy
     const float* dloss;      // cross-entropy: per-row upstream gradient (null: 1)
     float* dx;               // rows x cols
-    float* part_w;           // norms: G x cols per-CTA column sums of the weight-gradient terms (null: none)
-    float* part_b;           // LayerNorm: G x cols per-CTA column sums of dy (null: none)
+    float* stat_a;           // norms: per-row statistic for the column gradients, RMSNorm 1/rms,
+                             // LayerNorm the mean (null: not written)
+    float* stat_b;           // LayerNorm: per-row 1/sigma (null: not written)
     int64_t rows;
     int cols;
     float eps;

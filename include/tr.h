@@ -218,9 +218,10 @@ tr_status tr_row_minmax_f32(const float* x, float* out_min, float* out_max, int6
  * written above, bit-identical to the CPU emulation; unordered results meet a
  * rounding bound. The column gradients need a caller-owned, 16-byte-aligned
  * device workspace of at least tr_norm_backward_workspace_bytes(rows, cols)
- * bytes (none when dw, dgamma and dbeta are NULL); their final column
- * reduction may use the stream's library workspace, allocated on the first
- * such call on the stream, which therefore must not be captured. */
+ * bytes (two statistics per row; none when dw, dgamma and dbeta are NULL);
+ * they are column sums over the rows of their per-element terms, which may
+ * use the stream's library workspace, allocated on the first such call on the
+ * stream, which therefore must not be captured. */
 tr_status tr_softmax_backward_f32(const float* y, const float* dy, float* dx, int64_t rows, int64_t cols,
                                   tr_order order, cudaStream_t stream);
 tr_status tr_cross_entropy_backward_f32(const float* logits, const int64_t* labels, const float* dloss,

@@ -197,6 +197,12 @@ WORKLOADS = {
     # standalone row reductions, x ~ N(0, 1)
     "row_sum_768x6144": dict(op="row_sum", rows=768, cols=6144, seed=2),
     "row_minmax_768x6144": dict(op="row_minmax", rows=768, cols=6144, seed=2),
+    # backward passes: upstream gradients dy ~ N(0, 1), dloss ~ U(0.5, 1.5); the softmax
+    # backward's y is the forward softmax of x ~ N(0, 1), computed by the caller
+    "softmax_bwd_768x6144": dict(op="softmax_bwd", rows=768, cols=6144, seed=2, var=1.0),
+    "rmsnorm_bwd_768x6144": dict(op="rmsnorm_bwd", rows=768, cols=6144, seed=2),
+    "layernorm_bwd_768x6144": dict(op="layernorm_bwd", rows=768, cols=6144, seed=2),
+    "cross_entropy_bwd_4096x50257": dict(op="cross_entropy_bwd", rows=4096, cols=50257, seed=3, var=9.0),
     # reductions over axis 0 (one value per column), x ~ N(0, 1)
     "axis_sum_768x6144": dict(op="axis_sum", rows=768, cols=6144, seed=2),
     "axis_minmax_768x6144": dict(op="axis_minmax", rows=768, cols=6144, seed=2),
@@ -223,6 +229,18 @@ def make_inputs(op, rows, cols, seed, var=None, row_offset=False, device="cpu"):
         return xent_inputs(rows, cols, seed, 9.0 if var is None else var, device)
     if op in ("add_rmsnorm", "add_layernorm"):
         return residual_norm_inputs(rows, cols, seed, row_offset, device)
+    if op == "softmax_bwd":
+        return {"x": normal_f32((rows, cols), seed, TAG_X, 0.0, 1.0 if var is None else var, device),
+                "dy": grad_f32(rows, cols, seed, device)}
+    if op == "cross_entropy_bwd":
+        d = xent_inputs(rows, cols, seed, 9.0 if var is None else var, device)
+        d["dloss"] = dloss_f32(rows, seed, device)
+        return d
+    if op in ("rmsnorm_bwd", "layernorm_bwd"):
+        d = norm_inputs(rows, cols, seed, row_offset, device)
+        d.pop("b")
+        d["dy"] = grad_f32(rows, cols, seed, device)
+        return d
     if op in ("row_sum", "row_max", "row_min", "row_minmax", "axis_sum", "axis_max", "axis_min", "axis_minmax"):
         return {"x": normal_plus_row_offset_f32(rows, cols, seed, device=device) if row_offset
                 else normal_f32((rows, cols), seed, TAG_X, 0.0, 1.0 if var is None else var, device)}

@@ -194,9 +194,11 @@ def test_dx_only_and_workspace_errors():
     X, W, DY = dev(x), dev(w), dev(dy)
     DX, DW = torch.empty_like(X), torch.empty(3000, device=DEV)
     s = torch.cuda.current_stream().cuda_stream
-    small = torch.empty(64, dtype=torch.uint8, device=DEV)
+    need = tr.norm_backward_workspace_bytes(6, 3000)
+    assert need == 6 * 2 * 4                                                        # two statistics per row
+    small = torch.empty(need, dtype=torch.uint8, device=DEV)
     assert lib.tr_rmsnorm_backward_f32(X.data_ptr(), W.data_ptr(), DY.data_ptr(), DX.data_ptr(), DW.data_ptr(), 6, 3000,
-                                       1e-5, 0, small.data_ptr(), 64, s) == tr.TR_ERR_INVALID_ARG
+                                       1e-5, 0, small.data_ptr(), need - 4, s) == tr.TR_ERR_INVALID_ARG
     assert lib.tr_rmsnorm_backward_f32(X.data_ptr(), W.data_ptr(), DY.data_ptr(), X.data_ptr(), None, 6, 3000,
                                        1e-5, 0, None, 0, s) == tr.TR_ERR_INVALID_ARG     # dx aliases x
     assert lib.tr_softmax_backward_f32(X.data_ptr(), DY.data_ptr(), DY.data_ptr(), 6, 3000, 0, s) == tr.TR_ERR_INVALID_ARG
