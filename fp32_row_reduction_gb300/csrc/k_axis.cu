@@ -40,7 +40,10 @@ namespace axis {
 
 constexpr int kWarps = kAxisThreads / 32;
 constexpr int kQuads = 256;  // OT-1024: 1024 leaves, four per quad
-enum Mode : int { FREE = 0, TREE = 1, KEY = 2 };
+// STAGED: the tree mode for a reduced axis of at most 1024 rows (one element
+// per leaf), with the split's rows staged in shared memory first, so that
+// every load of the CTA is in flight at once before the tree is folded.
+enum Mode : int { FREE = 0, TREE = 1, KEY = 2, STAGED = 3 };
 
 template <int OP, int MODE>
 constexpr int nvals() { return MODE == KEY ? 2 : (OP == OP_RMINMAX ? 2 : 1); }
@@ -137,6 +140,12 @@ __device__ __forceinline__ void ld_elem(const AxisArgs& a, const float* p, int64
         }
     }
 }
+
+// 4-byte asynchronous copy global -> shared.
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Push the subtree value `cur` (the n-th of its block, n from 0) onto a stack
 // of pending left siblings; after the last push of a block of 2^d values,
@@ -244,7 +253,7 @@ __device__ __forceinline__ float cta_tree(const float (*g)[kAxisCols * 4], int i
 
 // Resident CTAs per SM each mode is built for (the host sizes its splits to fit one wave).
 template <int MODE>
-constexpr int min_ctas() { return MODE == TREE ? kAxisCtasTree : kAxisCtasFree; }
+constexpr int min_ctas() { return MODE == TREE || MODE == STAGED ? kAxisCtasTree : kAxisCtasFree; }
 
 template <int OP, int MODE, int V, int TERM = AXIS_PLAIN>
 __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(AxisArgs a) {
@@ -265,7 +274,56 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
     const float* col = a.x + (o * R) * inner + (j - o * inner);
 
     float res[N][V];
-    if constexpr (MODE == TREE) {
+    if constexpr (MODE == STAGED) {
+        static_assert(OP == OP_RSUM && V == 1, "the staged tree folds sums of single columns");
+        // rows [rs, re) hold the leaves of this split's quad positions (S <= 8);
+        // their x (and dy) are copied to shared memory asynchronously, all at once
+        constexpr bool two = TERM == AXIS_RMS_W || TERM == AXIS_LN_GAMMA;
+        extern __shared__ float stage[];
+        const int64_t per = 1024 / S;
+        const int64_t rows_cta = R < per ? R : per;
+        float* sx = stage;                 // x, or dy for the dbeta term
+        float* sd = stage + rows_cta * 32;  // dy of the two-input terms
+        const int64_t rs = static_cast<int64_t>(s) * per;
+        const int64_t re = rs + per < R ? rs + per : R;
+        if (jok) {
+            const float* gcol = TERM == AXIS_PLAIN ? col : a.dy + (col - a.x);
+            for (int64_t r = rs + w; r < re; r += kWarps) {
+                const int64_t i = (r - rs) * 32 + lane;
+                cp_async4(sx + i, (TERM == AXIS_LN_BETA ? gcol : col) + r * inner);
+                if constexpr (two) cp_async4(sd + i, gcol + r * inner);
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        auto elem = [&](int64_t r) {
+            const int64_t i = (r - rs) * 32 + lane;
+            if constexpr (TERM == AXIS_PLAIN || TERM == AXIS_LN_BETA) {
+                return sx[i];
+            } else if constexpr (TERM == AXIS_RMS_W) {
+                return __fmul_rn(__fmul_rn(sd[i], sx[i]), __ldg(a.sa + r));
+            } else {
+                return __fmul_rn(sd[i], __fmul_rn(__fsub_rn(sx[i], __ldg(a.sa + r)), __ldg(a.sb + r)));
+            }
+        };
+        const int P = kQuads / (S * kWarps);
+        const int p0 = s * (kQuads / S) + w * P;
+        float stk[5][1];
+        float cur[1] = {0.0f};
+#pragma unroll
+        for (int lv = 0; lv < 5; ++lv) stk[lv][0] = 0.0f;
+        for (int n = 0; n < P; ++n) {
+            const int p = p0 + n;
+            const int64_t e0 = 4 * (32 * (p >> 5) + static_cast<int>(__brev(p & 31) >> 27));
+            float l[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) l[v] = e0 + v < R ? __fadd_rn(0.0f, elem(e0 + v)) : 0.0f;
+            float q[1] = {__fadd_rn(__fadd_rn(l[0], l[1]), __fadd_rn(l[2], l[3]))};
+            push<AddF, 1>(stk, q, n);
+            cur[0] = q[0];
+        }
+        res[0][0] = cur[0];
+    } else if constexpr (MODE == TREE) {
         static_assert(OP == OP_RSUM, "the tree mode folds sums");
         const int P = kQuads / (S * kWarps);
         // quads loaded together: fewer when each element is a term of two loads
@@ -475,6 +533,27 @@ cudaError_t launch(bool ordered, const AxisArgs& a, int vec, int64_t tiles, int 
 }
 
 }  // namespace axis
+
+cudaError_t launch_axis_staged(int term, const AxisArgs& a, int64_t tiles, int splits, size_t smem,
+                               cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(splits));
+    switch (term) {
+        case AXIS_PLAIN:
+            axis::axis_kernel<OP_RSUM, axis::STAGED, 1, AXIS_PLAIN><<<grid, kAxisThreads, smem, stream>>>(a);
+            break;
+        case AXIS_RMS_W:
+            axis::axis_kernel<OP_RSUM, axis::STAGED, 1, AXIS_RMS_W><<<grid, kAxisThreads, smem, stream>>>(a);
+            break;
+        case AXIS_LN_GAMMA:
+            axis::axis_kernel<OP_RSUM, axis::STAGED, 1, AXIS_LN_GAMMA><<<grid, kAxisThreads, smem, stream>>>(a);
+            break;
+        case AXIS_LN_BETA:
+            axis::axis_kernel<OP_RSUM, axis::STAGED, 1, AXIS_LN_BETA><<<grid, kAxisThreads, smem, stream>>>(a);
+            break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
 
 template <int TERM>
 cudaError_t launch_term(bool ordered, const AxisArgs& a, int vec, int64_t tiles, int splits, cudaStream_t stream) {

@@ -518,6 +518,65 @@ int axis_ctas_per_sm(int op, int order) {
 static tr_status axis_run(int op, const float* x, float* out, float* out2, int64_t extent, int64_t inner,
                           int64_t ncols, tr_order order, cudaStream_t stream);
 
+// Splits of the staged ordered column sum (a reduced axis of at most 1024 rows,
+// each CTA staging at most 256 of them), or 0 where it does not apply.
+int axis_staged_splits(int64_t rows, int64_t tiles, int arrays, int sm_count) {
+    if (rows > kAxisStagedMaxRows) return 0;
+    const int64_t per = kAxisStagedRowsPerCta / arrays;  // rows per CTA: 32 KB of shared memory
+    int S = rows <= per ? 1 : static_cast<int>(kAxisStagedMaxRows / per);
+    if (S > 1 && S < 8 && tiles * 2 * S <= 6LL * sm_count) S *= 2;  // few tiles: more CTAs per tile
+    if (S > 1 && (tiles > kAxisMaxTickets || tiles * S * kAxisCols > kAxisMaxPartFloats)) return 0;
+    return S;
+}
+
+// Arrays the staged tree copies per row: x and dy for the two-input terms.
+static int staged_arrays(int term) { return term == AXIS_RMS_W || term == AXIS_LN_GAMMA ? 2 : 1; }
+
+// Launch an axis sum / max / min (term AXIS_PLAIN) or the column sum of a
+// backward term over `tiles` column tiles: the staged tree for ordered sums of
+// at most 1024 rows, otherwise the splits that fill one wave.
+static tr_status axis_dispatch(int op, int term, AxisArgs a, tr_order order, int vec, int64_t tiles,
+                               cudaStream_t stream) {
+    const bool ordered = order == TR_ORDER_ORDERED_TREE;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int S = 1, staged = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* st = nullptr;
+        tr_status s = device_state(dev, &st);
+        if (s != TR_OK) return s;
+        const int sm = st->desc.sm_count;
+        staged = (ordered && op == TR_OP_ROW_SUM) ? axis_staged_splits(a.extent, tiles, staged_arrays(term), sm) : 0;
+        if (staged > 0) {
+            S = staged;
+        } else {
+            const int values = op == TR_OP_ROW_SUM ? 1 : 2;  // ordered max and min keep two keys per column
+            const int ctas = term == AXIS_PLAIN ? axis_ctas_per_sm(op, order) : (ordered ? kAxisCtasTree : kAxisCtasFree);
+            S = axis_splits(tiles, a.extent, values, kAxisCols * vec, ctas, sm);
+        }
+        if (S > 1) {
+            void* ws = nullptr;
+            s = split_workspace(*st, stream, &ws);
+            if (s != TR_OK) return s;
+            a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kAxisPartOffset);
+            a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kAxisTicketOffset);
+        }
+    }
+    if (staged > 0) {
+        const int64_t rows_per = a.extent < kAxisStagedMaxRows / S ? a.extent : kAxisStagedMaxRows / S;
+        e = launch_axis_staged(term, a, tiles, S,
+                               static_cast<size_t>(rows_per) * kAxisCols * sizeof(float) * staged_arrays(term), stream);
+    } else if (term == AXIS_PLAIN) {
+        e = launch_axis(op, ordered, a, vec, tiles, S, stream);
+    } else {
+        e = launch_axis_term(term, ordered, a, vec, tiles, S, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "axis reduction launch");
+    return TR_OK;
+}
+
 static tr_status axis_call(int op, const float* x, float* out, float* out2, int64_t outer, int64_t extent,
                            int64_t inner, tr_order order, cudaStream_t stream) {
     if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE)
@@ -548,29 +607,8 @@ static tr_status axis_run(int op, const float* x, float* out, float* out2, int64
                           int64_t ncols, tr_order order, cudaStream_t stream) {
     const int vec = axis_vec(op, order, inner, !misaligned(x, 16));
     const int64_t tiles = (ncols + kAxisCols * vec - 1) / (kAxisCols * vec);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const int values = op == TR_OP_ROW_SUM ? 1 : 2;  // ordered max and min keep two keys per column
     AxisArgs a{x, out, out2, extent, inner, ncols, nullptr, nullptr};
-    int S = 1;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        DeviceState* st = nullptr;
-        tr_status s = device_state(dev, &st);
-        if (s != TR_OK) return s;
-        S = axis_splits(tiles, extent, values, kAxisCols * vec, axis_ctas_per_sm(op, order), st->desc.sm_count);
-        if (S > 1) {
-            void* ws = nullptr;
-            s = split_workspace(*st, stream, &ws);
-            if (s != TR_OK) return s;
-            a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kAxisPartOffset);
-            a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kAxisTicketOffset);
-        }
-    }
-    e = launch_axis(op, order == TR_ORDER_ORDERED_TREE, a, vec, tiles, S, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "axis reduction launch");
-    return TR_OK;
+    return axis_dispatch(op, AXIS_PLAIN, a, order, vec, tiles, stream);
 }
 
 tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, tr_order order, int64_t outer, int64_t extent,
@@ -584,7 +622,10 @@ tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, tr_order order, int
     if (outer > 0 && outer > INT64_MAX / inner) return fail(TR_ERR_INVALID_ARG, "outer * inner too large");
     const int vec = axis_vec(op, order, inner, true);
     *tiles = (outer * inner + kAxisCols * vec - 1) / (kAxisCols * vec);
-    *splits = *tiles > 0 ? axis_splits(*tiles, extent, op == TR_OP_ROW_SUM ? 1 : 2, kAxisCols * vec,
+    const int staged = (order == TR_ORDER_ORDERED_TREE && op == TR_OP_ROW_SUM && *tiles > 0)
+                           ? axis_staged_splits(extent, *tiles, 1, sm_count) : 0;
+    *splits = staged > 0 ? staged
+            : *tiles > 0 ? axis_splits(*tiles, extent, op == TR_OP_ROW_SUM ? 1 : 2, kAxisCols * vec,
                                        axis_ctas_per_sm(op, order), sm_count)
                          : 1;
     return TR_OK;
@@ -637,27 +678,7 @@ static tr_status term_sum(int term, const BwArgs& b, float* out, tr_order order,
     const int vec = (!ordered && cols % 4 == 0 && !misaligned(b.x, 16) && !misaligned(b.dy, 16)) ? 4 : 1;
     const int64_t tiles = (cols + kAxisCols * vec - 1) / (kAxisCols * vec);
     AxisArgs a{b.x, out, nullptr, rows, cols, cols, nullptr, nullptr, b.dy, b.stat_a, b.stat_b};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    int S = 1;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        DeviceState* st = nullptr;
-        tr_status s = device_state(dev, &st);
-        if (s != TR_OK) return s;
-        S = axis_splits(tiles, rows, 1, kAxisCols * vec, ordered ? kAxisCtasTree : kAxisCtasFree, st->desc.sm_count);
-        if (S > 1) {
-            void* ws = nullptr;
-            s = split_workspace(*st, stream, &ws);
-            if (s != TR_OK) return s;
-            a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kAxisPartOffset);
-            a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kAxisTicketOffset);
-        }
-    }
-    e = launch_axis_term(term, ordered, a, vec, tiles, S, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "column gradient launch");
-    return TR_OK;
+    return axis_dispatch(TR_OP_ROW_SUM, term, a, order, vec, tiles, stream);
 }
 
 static tr_status bw_run(int op, BwArgs a, tr_order order, float* dw, float* db, void* ws, size_t ws_bytes,

@@ -91,6 +91,14 @@ enum AxisTerm : int {
     AXIS_LN_BETA = 3  // dy
 };
 
+// Launch the ordered column sum (plain or of a term) of a reduced axis of at
+// most 1024 rows with the split's rows staged in `smem` bytes of shared memory
+// (splits 1, 2, 4 or 8).
+cudaError_t launch_axis_staged(int term, const AxisArgs& a, int64_t tiles, int splits, size_t smem,
+                               cudaStream_t stream);
+constexpr int kAxisStagedMaxRows = 1024;
+constexpr int kAxisStagedRowsPerCta = 256;  // rows one CTA stages (32 KB for 32 columns)
+
 // Launch the column sum of a norm backward term (AXIS_RMS_W .. AXIS_LN_BETA).
 cudaError_t launch_axis_term(int term, bool ordered, const AxisArgs& a, int vec, int64_t tiles, int splits,
                              cudaStream_t stream);
