@@ -68,6 +68,10 @@ def lib():
             "ot_cross_entropy_bwd_f32": [f32p, i64p, f32p, f32p, i64, i64],
             "ot_rmsnorm_bwd_f32": [f32p, f32p, f32p, f32p, f32p, i64, i64, ctypes.c_float],
             "ot_layernorm_bwd_f32": [f32p, f32p, f32p, f32p, f32p, f32p, i64, i64, ctypes.c_float],
+            "fold_softmax_f32": [f32p, f32p, i64, i64, ctypes.c_int],
+            "fold_rmsnorm_f32": [f32p, f32p, f32p, i64, i64, ctypes.c_float, ctypes.c_int],
+            "fold_layernorm_f32": [f32p, f32p, f32p, f32p, i64, i64, ctypes.c_float, ctypes.c_int],
+            "fold_cross_entropy_f32": [f32p, i64p, f32p, i64, i64, ctypes.c_int],
             "ot_sum_f32": [f32p, i64],
             "ot_max_f32": [f32p, i64],
             "ot_min_f32": [f32p, i64],
@@ -76,6 +80,10 @@ def lib():
             fn = getattr(_lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_float if name in ("ot_sum_f32", "ot_max_f32", "ot_min_f32") else ctypes.c_int
+        for name in ("fold_sum_f32", "fold_max_f32", "fold_min_f32"):
+            fn = getattr(_lib, name)
+            fn.argtypes = [f32p, i64, ctypes.c_int]
+            fn.restype = ctypes.c_float
         for name in ("ot_expf", "ot_logf"):
             fn = getattr(_lib, name)
             fn.argtypes = [ctypes.c_float]
@@ -391,6 +399,83 @@ def ot_layernorm_backward(x, gamma, dy, eps=1e-5):
                                    _ptr(dx, ctypes.c_float), _ptr(dg, ctypes.c_float), _ptr(db, ctypes.c_float),
                                    r, c, eps))
     return dx, dg, db
+
+
+# ---- the fold policies ("TIRx Metal reduction lowering" §1, ReductionPolicy
+# fold_left / fold_right): every reduction a sequential fold over the columns,
+# left to right with the accumulator on the left, or right to left with the
+# accumulator on the right. `direction` is "left" or "right".
+
+def _right(direction):
+    if direction not in ("left", "right"):
+        raise ValueError("direction must be 'left' or 'right'")
+    return 1 if direction == "right" else 0
+
+
+def fold_sum(v, direction="left"):
+    v = _f32(v).ravel()
+    return np.float32(lib().fold_sum_f32(_ptr(v, ctypes.c_float), v.size, _right(direction)))
+
+
+def fold_max(v, direction="left"):
+    v = _f32(v).ravel()
+    return np.float32(lib().fold_max_f32(_ptr(v, ctypes.c_float), v.size, _right(direction)))
+
+
+def fold_min(v, direction="left"):
+    v = _f32(v).ravel()
+    return np.float32(lib().fold_min_f32(_ptr(v, ctypes.c_float), v.size, _right(direction)))
+
+
+def fold_row_sum(x, direction="left"):
+    return np.array([fold_sum(r, direction) for r in _f32(x)], dtype=np.float32)
+
+
+def fold_row_max(x, direction="left"):
+    return np.array([fold_max(r, direction) for r in _f32(x)], dtype=np.float32)
+
+
+def fold_row_min(x, direction="left"):
+    return np.array([fold_min(r, direction) for r in _f32(x)], dtype=np.float32)
+
+
+def fold_softmax(x, direction="left"):
+    x = _f32(x)
+    r, c = x.shape
+    y = np.empty((r, c), np.float32)
+    _rc(lib().fold_softmax_f32(_ptr(x, ctypes.c_float), _ptr(y, ctypes.c_float), r, c, _right(direction)))
+    return y
+
+
+def fold_rmsnorm(x, w=None, eps=1e-5, direction="left"):
+    x = _f32(x)
+    w = None if w is None else _f32(w)
+    r, c = x.shape
+    y = np.empty((r, c), np.float32)
+    _rc(lib().fold_rmsnorm_f32(_ptr(x, ctypes.c_float), _ptr(w, ctypes.c_float), _ptr(y, ctypes.c_float), r, c, eps,
+                               _right(direction)))
+    return y
+
+
+def fold_layernorm(x, gamma=None, beta=None, eps=1e-5, direction="left"):
+    x = _f32(x)
+    gamma = None if gamma is None else _f32(gamma)
+    beta = None if beta is None else _f32(beta)
+    r, c = x.shape
+    y = np.empty((r, c), np.float32)
+    _rc(lib().fold_layernorm_f32(_ptr(x, ctypes.c_float), _ptr(gamma, ctypes.c_float), _ptr(beta, ctypes.c_float),
+                                 _ptr(y, ctypes.c_float), r, c, eps, _right(direction)))
+    return y
+
+
+def fold_cross_entropy(logits, labels, direction="left"):
+    x = _f32(logits)
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    r, c = x.shape
+    loss = np.empty(r, np.float32)
+    _rc(lib().fold_cross_entropy_f32(_ptr(x, ctypes.c_float), _ptr(lab, ctypes.c_int64), _ptr(loss, ctypes.c_float),
+                                     r, c, _right(direction)))
+    return loss
 
 
 def ot_expf(x):

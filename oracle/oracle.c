@@ -571,3 +571,102 @@ int ot_layernorm_bwd_f32(const float *x, const float *gamma, const float *dy, fl
     free(tb);
     return rc;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Part 4: the fold policies                                                  */
+/* ------------------------------------------------------------------------- */
+/*
+ * "TIRx Metal reduction lowering" §1 (ReductionPolicy): besides the trees, a
+ * reduction may be restricted to fold_left or fold_right, and "stays ordered".
+ * Reading: fold_left visits the columns in increasing order with the
+ * accumulator as the left operand, acc = acc (+) t_c, starting from the
+ * identity; fold_right visits them in decreasing order with the accumulator as
+ * the right operand, acc = t_c (+) acc. Max and min are the canonical selects
+ * of Part 2. The operators keep the op sequences of Part 2 with every
+ * OT-1024 reduction replaced by the fold (the same exp/log).
+ */
+static float fold_sum_of(const float *xr, int64_t n, ot_elem_fn f, float a, int right) {
+    float acc = 0.0f;
+    if (!right)
+        for (int64_t e = 0; e < n; ++e) acc = acc + f(xr[e], a);
+    else
+        for (int64_t e = n - 1; e >= 0; --e) acc = f(xr[e], a) + acc;
+    return acc;
+}
+
+float fold_sum_f32(const float *v, int64_t n, int right) { return fold_sum_of(v, n, el_identity, 0.0f, right); }
+
+float fold_max_f32(const float *v, int64_t n, int right) {
+    float acc = -INFINITY;
+    if (!right)
+        for (int64_t e = 0; e < n; ++e) acc = ot_max2(acc, v[e]);
+    else
+        for (int64_t e = n - 1; e >= 0; --e) acc = ot_max2(v[e], acc);
+    return acc;
+}
+
+float fold_min_f32(const float *v, int64_t n, int right) {
+    float acc = INFINITY;
+    if (!right)
+        for (int64_t e = 0; e < n; ++e) acc = ot_min2(acc, v[e]);
+    else
+        for (int64_t e = n - 1; e >= 0; --e) acc = ot_min2(v[e], acc);
+    return acc;
+}
+
+int fold_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols, int right) {
+    if (bad_sizes(rows, cols)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols;
+        const float peak = fold_max_f32(xr, cols, right);
+        const float inv = 1.0f / fold_sum_of(xr, cols, el_exp_shifted, peak, right);
+        for (int64_t c = 0; c < cols; ++c) y[r * cols + c] = ot_expf(xr[c] - peak) * inv;
+    }
+    return 0;
+}
+
+int fold_rmsnorm_f32(const float *x, const float *w, float *y, int64_t rows, int64_t cols, float eps, int right) {
+    if (bad_sizes(rows, cols)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols;
+        const float rms = sqrtf(fold_sum_of(xr, cols, el_square, 0.0f, right) / (float)cols + eps);
+        const float inv = 1.0f / rms;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float v = xr[c] * inv;
+            y[r * cols + c] = w ? v * w[c] : v;
+        }
+    }
+    return 0;
+}
+
+int fold_layernorm_f32(const float *x, const float *gamma, const float *beta, float *y, int64_t rows, int64_t cols,
+                       float eps, int right) {
+    if (bad_sizes(rows, cols)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols;
+        const float mean = fold_sum_of(xr, cols, el_identity, 0.0f, right) / (float)cols;
+        const float var = fold_sum_of(xr, cols, el_centered_square, mean, right) / (float)cols;
+        const float inv = 1.0f / sqrtf(var + eps);
+        for (int64_t c = 0; c < cols; ++c) {
+            float v = (xr[c] - mean) * inv;
+            if (gamma) v = v * gamma[c];
+            if (beta) v = v + beta[c];
+            y[r * cols + c] = v;
+        }
+    }
+    return 0;
+}
+
+int fold_cross_entropy_f32(const float *logits, const int64_t *labels, float *loss, int64_t rows, int64_t cols,
+                           int right) {
+    if (bad_sizes(rows, cols)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = logits + r * cols;
+        const float peak = fold_max_f32(xr, cols, right);
+        const float total = fold_sum_of(xr, cols, el_exp_shifted, peak, right);
+        const int64_t label = labels[r];
+        const float selected = (label >= 0 && label < cols) ? xr[label] : 0.0f;
+        loss[r] = (ot_logf(total) + peak) - selected;
+    }
+    return 0;
+}

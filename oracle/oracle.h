@@ -62,6 +62,16 @@ int ot_rmsnorm_bwd_f32(const float *x, const float *w, const float *dy, float *d
 int ot_layernorm_bwd_f32(const float *x, const float *gamma, const float *dy, float *dx, float *dgamma,
                          float *dbeta, int64_t rows, int64_t cols, float eps);
 
+float fold_sum_f32(const float *v, int64_t n, int right);
+float fold_max_f32(const float *v, int64_t n, int right);
+float fold_min_f32(const float *v, int64_t n, int right);
+int fold_softmax_f32(const float *x, float *y, int64_t rows, int64_t cols, int right);
+int fold_rmsnorm_f32(const float *x, const float *w, float *y, int64_t rows, int64_t cols, float eps, int right);
+int fold_layernorm_f32(const float *x, const float *gamma, const float *beta, float *y, int64_t rows, int64_t cols,
+                       float eps, int right);
+int fold_cross_entropy_f32(const float *logits, const int64_t *labels, float *loss, int64_t rows, int64_t cols,
+                           int right);
+
 #ifdef __cplusplus
 }
 #endif
