@@ -52,6 +52,9 @@ for _name, _w in synth.WORKLOADS.items():
     WORKLOADS[_name] = [(_w["op"], _name, "unordered")]
     if _name.endswith("768x6144"):
         WORKLOADS[_name + "_ordered"] = [(_w["op"], _name, "ordered")]
+        if _w["op"] in ("softmax", "rmsnorm", "layernorm", "row_sum", "row_minmax"):
+            for _f in ("fold_left", "fold_right"):
+                WORKLOADS[f"{_name}_{_f}"] = [(_w["op"], _name, _f)]
 DEFAULT_WORKLOAD = "trio_768x6144"
 
 
@@ -436,6 +439,14 @@ def measure_e2e(launches, args, dev):
 
 def oracle_fn(op, order):
     import oracle
+    if order in ("fold_left", "fold_right"):
+        d = "left" if order == "fold_left" else "right"
+        return {"softmax": lambda h: oracle.fold_softmax(h["x"], d),
+                "rmsnorm": lambda h: oracle.fold_rmsnorm(h["x"], h["w"], 1e-5, d),
+                "layernorm": lambda h: oracle.fold_layernorm(h["x"], h["w"], h["b"], 1e-5, d),
+                "cross_entropy": lambda h: oracle.fold_cross_entropy(h["x"], h["labels"], d),
+                "row_sum": lambda h: oracle.fold_row_sum(h["x"], d),
+                "row_minmax": lambda h: (oracle.fold_row_min(h["x"], d), oracle.fold_row_max(h["x"], d))}[op]
     if order == "ordered":
         return {"softmax": lambda h: oracle.ot_softmax(h["x"]),
                 "rmsnorm": lambda h: oracle.ot_rmsnorm(h["x"], h["w"], 1e-5),

@@ -30,6 +30,8 @@ TR_ERR_DEVICE_TIMEOUT = 4
 
 TR_ORDER_UNORDERED_TREE = 0
 TR_ORDER_ORDERED_TREE = 1
+TR_ORDER_FOLD_LEFT = 2
+TR_ORDER_FOLD_RIGHT = 3
 
 TR_OP_SOFTMAX = 0
 TR_OP_RMSNORM = 1
@@ -44,6 +46,7 @@ TR_PLAN_ORDERED = 4
 TR_PLAN_STAGED = 5
 TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_SPLIT = 7
+TR_PLAN_FOLD = 8
 TR_OP_ADD_RMSNORM = 4
 TR_OP_ADD_LAYERNORM = 5
 TR_OP_ROW_SUM = 6
@@ -60,7 +63,8 @@ OPS = {"softmax": TR_OP_SOFTMAX, "rmsnorm": TR_OP_RMSNORM, "layernorm": TR_OP_LA
 REDUCE_OPS = ("row_sum", "row_max", "row_min", "row_minmax")
 # reductions over axis 0 of a 2-D tensor (one value per column)
 AXIS_OPS = ("axis_sum", "axis_max", "axis_min", "axis_minmax")
-ORDERS = {"unordered": TR_ORDER_UNORDERED_TREE, "ordered": TR_ORDER_ORDERED_TREE}
+ORDERS = {"unordered": TR_ORDER_UNORDERED_TREE, "ordered": TR_ORDER_ORDERED_TREE,
+          "fold_left": TR_ORDER_FOLD_LEFT, "fold_right": TR_ORDER_FOLD_RIGHT}
 
 
 class tr_plan(ctypes.Structure):

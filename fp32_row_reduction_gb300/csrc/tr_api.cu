@@ -210,8 +210,8 @@ struct Call {
 };
 
 tr_status validate_common(int64_t rows, int64_t cols, int order) {
-    if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE)
-        return fail(TR_ERR_INVALID_ARG, "order must be TR_ORDER_UNORDERED_TREE or TR_ORDER_ORDERED_TREE");
+    if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE && !fold_order(order))
+        return fail(TR_ERR_INVALID_ARG, "order must be one of the tr_order values");
     if (rows < 0) return fail(TR_ERR_INVALID_ARG, "rows must be >= 0");
     if (cols < 1 || cols > 0x7fffffffLL) return fail(TR_ERR_INVALID_ARG, "cols must be in [1, 2^31 - 1]");
     if (rows > 0 && rows > INT64_MAX / cols / 4) return fail(TR_ERR_INVALID_ARG, "rows * cols too large");
@@ -223,9 +223,32 @@ tr_status validate_eps(float eps) {
     return TR_OK;
 }
 
+// The fold policies' single realisation (TR_PLAN_FOLD): a warp per row.
+static tr_plan fold_plan(int op, int64_t rows, int order) {
+    tr_plan p;
+    std::memset(&p, 0, sizeof p);
+    p.op = op;
+    p.order = order;
+    p.kind = TR_PLAN_FOLD;
+    p.lanes_per_row = 32;
+    p.warps_per_row = 1;
+    p.rows_per_cta = 8;
+    p.cluster_ctas = 1;
+    p.block_threads = 256;
+    p.grid_ctas = (rows + 7) / 8;
+    p.candidates = 1;
+    return p;
+}
+
 tr_status run(Call& c, cudaStream_t stream) {
     RowArgs& a = c.a;
     if (a.rows == 0) return TR_OK;
+    if (fold_order(c.order)) {
+        if (!fold_supported(c.op)) return fail(TR_ERR_UNSUPPORTED, "the fold policies cover the four operators and the row reductions");
+        const cudaError_t fe = launch_fold(c.op, c.order == TR_ORDER_FOLD_RIGHT, a, stream);
+        if (fe != cudaSuccess) return cuda_fail(fe, "fold launch");
+        return TR_OK;
+    }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -579,8 +602,9 @@ static tr_status axis_dispatch(int op, int term, AxisArgs a, tr_order order, int
 
 static tr_status axis_call(int op, const float* x, float* out, float* out2, int64_t outer, int64_t extent,
                            int64_t inner, tr_order order, cudaStream_t stream) {
+    if (fold_order(order)) return fail(TR_ERR_UNSUPPORTED, "the axis reductions take the tree policies");
     if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE)
-        return fail(TR_ERR_INVALID_ARG, "order must be TR_ORDER_UNORDERED_TREE or TR_ORDER_ORDERED_TREE");
+        return fail(TR_ERR_INVALID_ARG, "order must be one of the tr_order values");
     if (outer < 0 || extent < 1 || inner < 1)
         return fail(TR_ERR_INVALID_ARG, "need outer >= 0, extent >= 1 and inner >= 1");
     if (outer == 0) return TR_OK;
@@ -719,6 +743,7 @@ tr_status tr_softmax_backward_f32(const float* y, const float* dy, float* dx, in
                                   tr_order order, cudaStream_t stream) {
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
+    if (fold_order(order)) return fail(TR_ERR_UNSUPPORTED, "the backward passes take the tree policies");
     if (rows == 0) return TR_OK;
     if (!y || !dy || !dx) return fail(TR_ERR_INVALID_ARG, "y, dy and dx must not be null");
     if (misaligned(y, 4) || misaligned(dy, 4) || misaligned(dx, 4))
@@ -735,6 +760,7 @@ tr_status tr_cross_entropy_backward_f32(const float* logits, const int64_t* labe
                                         cudaStream_t stream) {
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
+    if (fold_order(order)) return fail(TR_ERR_UNSUPPORTED, "the backward passes take the tree policies");
     if (rows == 0) return TR_OK;
     if (!logits || !labels || !dlogits) return fail(TR_ERR_INVALID_ARG, "logits, labels and dlogits must not be null");
     if (misaligned(logits, 4) || misaligned(dlogits, 4) || misaligned(dloss, 4) || misaligned(labels, 8))
@@ -754,6 +780,7 @@ static tr_status norm_bw_call(int op, const float* x, const float* w, const floa
                               size_t ws_bytes, cudaStream_t stream) {
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
+    if (fold_order(order)) return fail(TR_ERR_UNSUPPORTED, "the backward passes take the tree policies");
     s = validate_eps(eps);
     if (s != TR_OK) return s;
     if (rows == 0) return TR_OK;
@@ -815,6 +842,11 @@ tr_status tr_plan_describe(int32_t op, int64_t rows, int64_t cols, tr_order orde
     tr_status s = validate_common(rows, cols, order);
     if (s != TR_OK) return s;
     if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1 to describe a plan");
+    if (fold_order(order)) {
+        if (!fold_supported(op)) return fail(TR_ERR_UNSUPPORTED, "no fold plan for this operator");
+        *out = fold_plan(op, rows, order);
+        return TR_OK;
+    }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -848,6 +880,11 @@ tr_status tr_plan_select_for(const tr_device_desc* dev, int32_t op, int64_t rows
     if (rows < 1) return fail(TR_ERR_INVALID_ARG, "rows must be >= 1 to select a plan");
     if (dev->sm_count < 1 || dev->max_threads_per_sm < 32 || dev->regs_per_sm < 1 || dev->hbm_gbs <= 0)
         return fail(TR_ERR_INVALID_ARG, "malformed device description");
+    if (fold_order(order)) {
+        if (!fold_supported(op)) return fail(TR_ERR_UNSUPPORTED, "no fold plan for this operator");
+        *out = fold_plan(op, rows, order);
+        return TR_OK;
+    }
     s = select_plan(*dev, OccupancyFn(), op, rows, cols, order, align16 != 0, out);
     if (s != TR_OK) return fail(s, "no legal plan for this shape on this device");
     return TR_OK;

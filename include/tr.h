@@ -55,7 +55,16 @@ typedef enum tr_status {
 
 typedef enum tr_order {
     TR_ORDER_UNORDERED_TREE = 0,  /* default: any reassociation / permutation of the reduction */
-    TR_ORDER_ORDERED_TREE = 1     /* canonical OT-1024 fixed tree, bit-exact */
+    TR_ORDER_ORDERED_TREE = 1,    /* canonical OT-1024 fixed tree, bit-exact */
+    /* §1 ReductionPolicy fold_left / fold_right: every row reduction one
+     * sequential fold over the columns, in increasing order with the
+     * accumulator on the left, or in decreasing order with the accumulator on
+     * the right, from the identity; otherwise the ordered tree's op sequences,
+     * bit-identical to the CPU emulation. For the four operators and the row
+     * reductions; other entry points return TR_ERR_UNSUPPORTED. A fold is one
+     * chain of dependent additions per row, so it runs far below bandwidth. */
+    TR_ORDER_FOLD_LEFT = 2,
+    TR_ORDER_FOLD_RIGHT = 3
 } tr_order;
 
 typedef enum tr_op {
@@ -82,10 +91,11 @@ typedef enum tr_plan_kind {
     TR_PLAN_STAGED = 5,   /* persistent CTAs; rows_per_cta rows in flight in a shared-memory ring filled by
                              bulk asynchronous copies (TMA); each row reduced by the whole CTA from registers */
     TR_PLAN_ORDERED_STAGED = 6, /* OT-1024 on persistent 256-thread CTAs fed by the same ring (rows_per_cta slots) */
-    TR_PLAN_SPLIT = 7     /* a row per cluster_ctas co-resident CTAs (cooperative launch, 2..32); each CTA caches
+    TR_PLAN_SPLIT = 7,    /* a row per cluster_ctas co-resident CTAs (cooperative launch, 2..32); each CTA caches
                              vec_slots * block_threads 16-byte slots of its segment in shared memory (one bulk
                              asynchronous copy) and streams the rest; partials meet in a per-stream global
-                             workspace allocated on first use (64 KB + 16 KB per stream and device) */
+                             workspace allocated on first use (per stream and device) */
+    TR_PLAN_FOLD = 8      /* fold policies: a warp per row, 8 rows per 256-thread CTA */
 } tr_plan_kind;
 
 typedef struct tr_plan {
