@@ -10,10 +10,10 @@
 //
 // A fold is one chain of dependent additions per row: the chain is the floor
 // of the run time (4 cycles an add), so each row gets one warp. The 32 lanes
-// load 128 columns at a time (coalesced float4), compute their terms (the
+// load 128 columns at a time (coalesced float4) and compute their terms (the
 // exponentials of softmax and cross-entropy, the squares of the norms) in
-// parallel and stage them in shared memory; lane 0 folds them in order while
-// the lanes' loads of the next 128 columns are in flight. Max and min need no
+// parallel; the warp then runs the chain on terms broadcast by shuffles while
+// the loads of the next 128 columns are in flight. Max and min need no
 // chain: without a NaN in the row the canonical fold's result is the largest
 // (smallest) element in the total order with -0 below +0, whatever the
 // order, so the lanes fold integer keys in any order; a row with a NaN is
@@ -32,7 +32,7 @@ namespace fold {
 using ordered::exp_ot;
 using ordered::log_ot;
 
-constexpr int kWarps = 8;    // rows per CTA
+constexpr int kWarps = 2;    // rows per CTA: few, so the rows spread over every SM (the chains share an SM's shuffle throughput)
 constexpr int kChunk = 128;  // columns per step: 32 lanes x 4
 
 // Columns c0 .. c0 + 3 of a row (0 outside it).
@@ -78,7 +78,6 @@ struct MinC {
 
 template <int OP, bool RIGHT>
 __global__ void __launch_bounds__(kWarps * 32) fold_kernel(const RowArgs a) {
-    __shared__ __align__(16) float buf[kWarps][kChunk];
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + w;
@@ -87,36 +86,76 @@ __global__ void __launch_bounds__(kWarps * 32) fold_kernel(const RowArgs a) {
     const float* xr = a.x + row * cols;
     const bool al = aligned16(xr);
     const int nch = (cols + kChunk - 1) / kChunk;
-    float* bw = buf[w];
     const int64_t lc = 4 * lane;  // this lane's first column within a chunk
 
     // The fold of term(x_c) over the row in the policy's order, starting from
-    // init: the lanes compute 128 terms at a time, lane 0 combines them in
-    // order while the next 128 columns load. The result reaches every lane.
+    // init. Every lane computes the terms of its 4 columns, then the whole
+    // warp runs the chain, each term broadcast by a shuffle (independent of the
+    // chain, so the shuffles issue ahead of the dependent adds) while the next
+    // 128 columns load. Every lane ends with the result.
     auto fold_seq = [&](auto term, auto comb, float init) -> float {
         using C = decltype(comb);
         float acc = init;
-        float nxt[4];
-        load4(xr, cols, static_cast<int64_t>(RIGHT ? nch - 1 : 0) * kChunk + lc, al, nxt);
-        for (int i = 0; i < nch; ++i) {
-            const int ch = RIGHT ? nch - 1 - i : i;
-            float t[4];
+        // the i-th chunk visited and the loads of four of them at a time
+        auto chunk_of = [&](int i) { return RIGHT ? nch - 1 - i : i; };
+        auto load_group = [&](int i0, float (&g)[4][4]) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) t[v] = term(nxt[v]);
-            if (i + 1 < nch) load4(xr, cols, static_cast<int64_t>(RIGHT ? ch - 1 : ch + 1) * kChunk + lc, al, nxt);
-            __syncwarp();  // lane 0 has folded the previous chunk
-            *reinterpret_cast<float4*>(bw + lc) = make_float4(t[0], t[1], t[2], t[3]);
-            __syncwarp();
-            if (lane == 0) {
-                const int n = cols - ch * kChunk < kChunk ? cols - ch * kChunk : kChunk;
-                if (!RIGHT) {
-                    for (int k = 0; k < n; ++k) acc = C::f(acc, bw[k]);
+            for (int u = 0; u < 4; ++u) {
+                if (i0 + u < nch) {
+                    load4(xr, cols, static_cast<int64_t>(chunk_of(i0 + u)) * kChunk + lc, al, g[u]);
                 } else {
-                    for (int k = n - 1; k >= 0; --k) acc = C::f(bw[k], acc);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) g[u][v] = 0.0f;
                 }
             }
+        };
+        float cur[4][4], nxt[4][4];
+        load_group(0, cur);
+        for (int i0 = 0; i0 < nch; i0 += 4) {
+            if (i0 + 4 < nch) load_group(i0 + 4, nxt);  // four chunks of chain time to arrive
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                if (i < nch) {
+                    const int ch = chunk_of(i);
+                    float t[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) t[v] = term(cur[u][v]);
+                    const int n = cols - ch * kChunk < kChunk ? cols - ch * kChunk : kChunk;
+                    if (n == kChunk) {
+                        // the shuffle of element q + 16 issues right after the combine
+                        // of element q, in the shadow of the combine's latency (a warp
+                        // issues in order); visit position q is column RIGHT ? 127 - q : q
+                        float sh[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int k = RIGHT ? kChunk - 1 - e : e;
+                            sh[e] = __shfl_sync(kFull, t[k & 3], k >> 2);
+                        }
+#pragma unroll
+                        for (int q = 0; q < kChunk; ++q) {
+                            acc = RIGHT ? C::f(sh[q & 15], acc) : C::f(acc, sh[q & 15]);
+                            if (q + 16 < kChunk) {
+                                const int k = RIGHT ? kChunk - 1 - (q + 16) : q + 16;
+                                sh[q & 15] = __shfl_sync(kFull, t[k & 3], k >> 2);
+                            }
+                        }
+                    } else {
+                        for (int q = 0; q < n; ++q) {
+                            const int k = RIGHT ? n - 1 - q : q;
+                            const int v = k & 3;
+                            const float tk = __shfl_sync(kFull, v == 0 ? t[0] : v == 1 ? t[1] : v == 2 ? t[2] : t[3], k >> 2);
+                            acc = RIGHT ? C::f(tk, acc) : C::f(acc, tk);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) cur[u][v] = nxt[u][v];
         }
-        return __shfl_sync(kFull, acc, 0);
+        return acc;
     };
     auto ident = [](float v) { return v; };
 
@@ -124,17 +163,19 @@ __global__ void __launch_bounds__(kWarps * 32) fold_kernel(const RowArgs a) {
     // the canonical fold only for a row that holds a NaN
     auto extreme = [&](bool want_max, float& lo, float& hi) {
         int kmax = INT_MIN, kmin = INT_MAX;
-        for (int ch = 0; ch < nch; ++ch) {
-            const int64_t c0 = static_cast<int64_t>(ch) * kChunk + lc;
-            float q[4];
-            load4(xr, cols, c0, al, q);
+        for (int ch0 = 0; ch0 < nch; ch0 += 4) {  // four chunks' loads in flight
+            float q[4][4];
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                if (c0 + v < cols) {
-                    const int k = order_key(q[v]);
-                    kmax = max(kmax, k);
-                    kmin = min(kmin, k);
-                }
+            for (int u = 0; u < 4; ++u) load4(xr, cols, static_cast<int64_t>(ch0 + u) * kChunk + lc, al, q[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (static_cast<int64_t>(ch0 + u) * kChunk + lc + v < cols) {
+                        const int k = order_key(q[u][v]);
+                        kmax = max(kmax, k);
+                        kmin = min(kmin, k);
+                    }
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
@@ -154,12 +195,19 @@ __global__ void __launch_bounds__(kWarps * 32) fold_kernel(const RowArgs a) {
     // y_c = out(x_c, c) for every column (any order)
     auto emit = [&](auto out) {
         float* yr = a.y + row * cols;
-        for (int ch = 0; ch < nch; ++ch) {
-            const int64_t c0 = static_cast<int64_t>(ch) * kChunk + lc;
-            float q[4], o[4];
-            load4(xr, cols, c0, al, q);
-            out(q, c0, o);
-            store4(yr, cols, c0, o);
+        for (int ch0 = 0; ch0 < nch; ch0 += 4) {  // four chunks' loads in flight
+            float q[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) load4(xr, cols, static_cast<int64_t>(ch0 + u) * kChunk + lc, al, q[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c0 = static_cast<int64_t>(ch0 + u) * kChunk + lc;
+                if (c0 < cols) {
+                    float o[4];
+                    out(q[u], c0, o);
+                    store4(yr, cols, c0, o);
+                }
+            }
         }
     };
     const float n = static_cast<float>(cols);

@@ -232,10 +232,10 @@ static tr_plan fold_plan(int op, int64_t rows, int order) {
     p.kind = TR_PLAN_FOLD;
     p.lanes_per_row = 32;
     p.warps_per_row = 1;
-    p.rows_per_cta = 8;
+    p.rows_per_cta = 2;
     p.cluster_ctas = 1;
-    p.block_threads = 256;
-    p.grid_ctas = (rows + 7) / 8;
+    p.block_threads = 64;
+    p.grid_ctas = (rows + 1) / 2;
     p.candidates = 1;
     return p;
 }

@@ -164,7 +164,7 @@ constexpr int kOrderedSlots[] = {0, 1, 2, 4, 6, 8, 12, 16}; // 0: re-read plan
 constexpr int kOrderedStagedSlots[] = {1, 2, 4, 8};
 constexpr int kOrderedThreads = 256;                  // OT-1024: 256 workers x 4 leaves
 
-// The fold policies: one warp per row, 8 rows per CTA (op: TR_OP_SOFTMAX ..
+// The fold policies: one warp per row, 2 rows per CTA (op: TR_OP_SOFTMAX ..
 // TR_OP_CROSS_ENTROPY or TR_OP_ROW_SUM .. TR_OP_ROW_MINMAX; right: fold_right).
 cudaError_t launch_fold(int op, bool right, const RowArgs& a, cudaStream_t stream);
 inline bool fold_order(int order) { return order == TR_ORDER_FOLD_LEFT || order == TR_ORDER_FOLD_RIGHT; }

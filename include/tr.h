@@ -95,7 +95,7 @@ typedef enum tr_plan_kind {
                              vec_slots * block_threads 16-byte slots of its segment in shared memory (one bulk
                              asynchronous copy) and streams the rest; partials meet in a per-stream global
                              workspace allocated on first use (per stream and device) */
-    TR_PLAN_FOLD = 8      /* fold policies: a warp per row, 8 rows per 256-thread CTA */
+    TR_PLAN_FOLD = 8      /* fold policies: a warp per row, 2 rows per 64-thread CTA */
 } tr_plan_kind;
 
 typedef struct tr_plan {

@@ -118,7 +118,7 @@ def test_fold_refusals():
             tr.axis_reduce(d["x"], 0, "sum", order=order)
         assert e.value.status == tr.TR_ERR_UNSUPPORTED
         p = tr.tr_plan_describe(tr.TR_OP_SOFTMAX, 100, 6144, tr.ORDERS[order])
-        assert p.kind == tr.TR_PLAN_FOLD and p.grid_ctas == 13
+        assert p.kind == tr.TR_PLAN_FOLD and p.grid_ctas == 50
 
 
 def test_fold_full_size_768x6144():

@@ -198,8 +198,8 @@ def test_fold_orders_get_the_warp_per_row_plan(order):
     for op in (0, 1, 2, 3, trlib.TR_OP_ROW_SUM, trlib.TR_OP_ROW_MINMAX):
         for rows, cols in [(768, 6144), (5, 3), (4096, 50257)]:
             p = select(op, rows, cols, order=order)
-            assert p.kind == trlib.TR_PLAN_FOLD and p.block_threads == 256 and p.rows_per_cta == 8
-            assert p.grid_ctas == math.ceil(rows / 8)
+            assert p.kind == trlib.TR_PLAN_FOLD and p.block_threads == 64 and p.rows_per_cta == 2
+            assert p.grid_ctas == math.ceil(rows / 2)
     with pytest.raises(trlib.TrError) as e:
         select(trlib.TR_OP_ADD_LAYERNORM, 4, 8, order=order)
     assert e.value.status == trlib.TR_ERR_UNSUPPORTED
