@@ -48,6 +48,17 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
     // validity, tested once per quad: `full` quads need no per-element test
     auto full = [&](int j) { return j < nj && col(j, 3) < cols; };
     auto okc = [&](int j, int v) { return j < nj && col(j, v) < cols; };
+    // the norms' weight and bias quads: into L1 now, so that the epilogue after
+    // the trees finds them there (every CTA on the SM reads the same vectors)
+    if constexpr (OP == OP_RMSNORM || OP == OP_LAYERNORM) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (j < nj && col(j, 0) < cols) {
+                if (a.has_w) prefetch_l1(a.w + col(j, 0));
+                if (OP == OP_LAYERNORM && a.has_b) prefetch_l1(a.b + col(j, 0));
+            }
+        }
+    }
     float leaf[4];
     // fold f(value, column) into the leaves in increasing column order
     auto fold = [&](auto elem, auto comb, float init) {
@@ -84,6 +95,28 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
                     if (okc(j, v)) yr[col(j, v)] = out(q[j][v], col(j, v));
+            }
+        }
+    };
+    // emit with a whole-quad form for full quads (quad(v[4], first column, o[4]))
+    // and the per-element form for the partial last quad
+    auto emit_quads = [&](auto quad, auto elem) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (j >= nj) continue;
+            if (full(j)) {
+                float o[4];
+                quad(q[j], col(j, 0), o);
+                if (vec_out) {
+                    st4(yr + col(j, 0), make_float4(o[0], o[1], o[2], o[3]));
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) yr[col(j, v)] = o[v];
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (okc(j, v)) yr[col(j, v)] = elem(q[j][v], col(j, v));
             }
         }
     };
@@ -128,10 +161,20 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
         const float inv = __fdiv_rn(1.0f, r);
         const bool hw = a.has_w;
         const float* w = a.w;
-        emit([inv, hw, w](float v, int c) {
-            const float u = __fmul_rn(v, inv);
-            return hw ? __fmul_rn(u, __ldg(w + c)) : u;
-        });
+        if (hw && aligned16(w)) {
+            // whole quads: one 16-byte weight load per quad
+            emit_quads([inv, w](const float (&v)[4], int c0, float (&o)[4]) {
+                const float4 wq = ld_param4(w + c0);
+                const float wv[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = __fmul_rn(__fmul_rn(v[e], inv), wv[e]);
+            }, [inv, w](float v, int c) { return __fmul_rn(__fmul_rn(v, inv), __ldg(w + c)); });
+        } else {
+            emit([inv, hw, w](float v, int c) {
+                const float u = __fmul_rn(v, inv);
+                return hw ? __fmul_rn(u, __ldg(w + c)) : u;
+            });
+        }
     } else {  // OP_LAYERNORM
         fold(ident, add, 0.0f);
         const float mean = __fdiv_rn(tree<Add>(leaf, gpart, buf), n);
@@ -144,12 +187,22 @@ __device__ __forceinline__ void ot_cached_row(const RowArgs& a, int64_t row, flo
         const float inv = __fdiv_rn(1.0f, d);
         const bool hw = a.has_w, hb = a.has_b;
         const float *w = a.w, *b = a.b;
-        emit([mean, inv, hw, hb, w, b](float v, int c) {
+        auto scalar = [mean, inv, hw, hb, w, b](float v, int c) {
             float u = __fmul_rn(__fsub_rn(v, mean), inv);
             if (hw) u = __fmul_rn(u, __ldg(w + c));
             if (hb) u = __fadd_rn(u, __ldg(b + c));
             return u;
-        });
+        };
+        if (hw && hb && aligned16(w) && aligned16(b)) {
+            emit_quads([mean, inv, w, b](const float (&v)[4], int c0, float (&o)[4]) {
+                const float4 wq = ld_param4(w + c0), bq = ld_param4(b + c0);
+                const float wv[4] = {wq.x, wq.y, wq.z, wq.w}, bv[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(v[e], mean), inv), wv[e]), bv[e]);
+            }, scalar);
+        } else {
+            emit(scalar);
+        }
     }
 }
 

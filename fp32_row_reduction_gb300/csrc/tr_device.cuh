@@ -98,6 +98,9 @@ __device__ __forceinline__ float4 ld_param4(const float* p) {
     return __ldg(reinterpret_cast<const float4*>(p));
 }
 
+// Bring the line holding p into L1 (no register, no wait).
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+
 __device__ __forceinline__ bool aligned16(const void* p) {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
