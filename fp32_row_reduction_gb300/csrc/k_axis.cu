@@ -45,8 +45,8 @@ constexpr int kQuads = 256;  // OT-1024: 1024 leaves, four per quad
 // every load of the CTA is in flight at once before the tree is folded.
 enum Mode : int { FREE = 0, TREE = 1, KEY = 2, STAGED = 3 };
 
-template <int OP, int MODE>
-constexpr int nvals() { return MODE == KEY ? 2 : (OP == OP_RMINMAX ? 2 : 1); }
+template <int OP, int MODE, int TERM = AXIS_PLAIN>
+constexpr int nvals() { return MODE == KEY ? 2 : (OP == OP_RMINMAX || TERM == AXIS_LN_BOTH ? 2 : 1); }
 
 // Value k of the free / tree reductions (min and max together: 0 = min, 1 = max).
 template <int OP, bool ORD>
@@ -146,6 +146,30 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The N values an element contributes: the LayerNorm's (dy xh, dy) for
+// AXIS_LN_BOTH, otherwise the element (or term) itself for every value.
+template <int TERM, bool O, int V, int N>
+__device__ __forceinline__ void ld_terms(const AxisArgs& a, const float* p, int64_t r, float (&e)[N][V]) {
+    if constexpr (TERM == AXIS_LN_BOTH) {
+        static_assert(N == 2, "two gradients");
+        float d[V], x[V];
+        ld_cols<V>(a.dy + (p - a.x), d);
+        ld_cols<V>(p, x);
+        const float s0 = __ldg(a.sa + r), s1 = __ldg(a.sb + r);
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+            e[0][c] = O ? __fmul_rn(d[c], __fmul_rn(__fsub_rn(x[c], s0), s1)) : d[c] * ((x[c] - s0) * s1);
+            e[1][c] = d[c];
+        }
+    } else {
+        ld_elem<TERM, O, V>(a, p, r, e[0]);
+#pragma unroll
+        for (int k = 1; k < N; ++k)
+#pragma unroll
+            for (int c = 0; c < V; ++c) e[k][c] = e[0][c];
+    }
+}
 
 // Push the subtree value `cur` (the n-th of its block, n from 0) onto a stack
 // of pending left siblings; after the last push of a block of 2^d values,
@@ -257,7 +281,7 @@ constexpr int min_ctas() { return MODE == TREE || MODE == STAGED ? kAxisCtasTree
 
 template <int OP, int MODE, int V, int TERM = AXIS_PLAIN>
 __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(AxisArgs a) {
-    constexpr int N = nvals<OP, MODE>();
+    constexpr int N = nvals<OP, MODE, TERM>();
     constexpr int W = kAxisCols * V;  // columns of the tile
     __shared__ float g[N][kWarps][kAxisCols * 4];
     __shared__ unsigned s_last;
@@ -278,7 +302,7 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
         static_assert(OP == OP_RSUM && V == 1, "the staged tree folds sums of single columns");
         // rows [rs, re) hold the leaves of this split's quad positions (S <= 8);
         // their x (and dy) are copied to shared memory asynchronously, all at once
-        constexpr bool two = TERM == AXIS_RMS_W || TERM == AXIS_LN_GAMMA;
+        constexpr bool two = TERM == AXIS_RMS_W || TERM == AXIS_LN_GAMMA || TERM == AXIS_LN_BOTH;
         extern __shared__ float stage[];
         const int64_t per = 1024 / S;
         const int64_t rows_cta = R < per ? R : per;
@@ -296,33 +320,45 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
         }
         cp_async_wait_all();
         __syncthreads();
-        auto elem = [&](int64_t r) {
+        // value k of row r's element
+        auto elem = [&](int64_t r, int k) {
             const int64_t i = (r - rs) * 32 + lane;
             if constexpr (TERM == AXIS_PLAIN || TERM == AXIS_LN_BETA) {
                 return sx[i];
             } else if constexpr (TERM == AXIS_RMS_W) {
                 return __fmul_rn(__fmul_rn(sd[i], sx[i]), __ldg(a.sa + r));
             } else {
+                if (TERM == AXIS_LN_BOTH && k == 1) return sd[i];
                 return __fmul_rn(sd[i], __fmul_rn(__fsub_rn(sx[i], __ldg(a.sa + r)), __ldg(a.sb + r)));
             }
         };
         const int P = kQuads / (S * kWarps);
         const int p0 = s * (kQuads / S) + w * P;
-        float stk[5][1];
-        float cur[1] = {0.0f};
+        float stk[5][N];
+        float cur[N];
 #pragma unroll
-        for (int lv = 0; lv < 5; ++lv) stk[lv][0] = 0.0f;
+        for (int k = 0; k < N; ++k) {
+            cur[k] = 0.0f;
+#pragma unroll
+            for (int lv = 0; lv < 5; ++lv) stk[lv][k] = 0.0f;
+        }
         for (int n = 0; n < P; ++n) {
             const int p = p0 + n;
             const int64_t e0 = 4 * (32 * (p >> 5) + static_cast<int>(__brev(p & 31) >> 27));
-            float l[4];
+            float q[N];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) l[v] = e0 + v < R ? __fadd_rn(0.0f, elem(e0 + v)) : 0.0f;
-            float q[1] = {__fadd_rn(__fadd_rn(l[0], l[1]), __fadd_rn(l[2], l[3]))};
-            push<AddF, 1>(stk, q, n);
-            cur[0] = q[0];
+            for (int k = 0; k < N; ++k) {
+                float l[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) l[v] = e0 + v < R ? __fadd_rn(0.0f, elem(e0 + v, k)) : 0.0f;
+                q[k] = __fadd_rn(__fadd_rn(l[0], l[1]), __fadd_rn(l[2], l[3]));
+            }
+            push<AddF, N>(stk, q, n);
+#pragma unroll
+            for (int k = 0; k < N; ++k) cur[k] = q[k];
         }
-        res[0][0] = cur[0];
+#pragma unroll
+        for (int k = 0; k < N; ++k) res[k][0] = cur[k];
     } else if constexpr (MODE == TREE) {
         static_assert(OP == OP_RSUM, "the tree mode folds sums");
         const int P = kQuads / (S * kWarps);
@@ -336,6 +372,7 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
         const int64_t r1 = r0 + base + (s < extra ? 1 : 0);
         // loads in flight per thread (a term loads two elements)
         constexpr int U = (V == 4 ? 4 : 8) / (TERM == AXIS_PLAIN || TERM == AXIS_LN_BETA ? 1 : 2);
+        static_assert(MODE != TREE || TERM != AXIS_LN_BOTH, "the register tree takes one term");
         float acc[4][N][V];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -345,14 +382,16 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
                 for (int c = 0; c < V; ++c) acc[u][k][c] = acc_init<OP, MODE>(k);
         if (jok) {
             for (int64_t r = r0 + w; r < r1; r += U * kWarps) {
-                float v[U][V];
+                float v[U][N][V];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     if (r + u * kWarps < r1) {
-                        ld_elem<TERM, false, V>(a, col + (r + u * kWarps) * inner, r + u * kWarps, v[u]);
+                        ld_terms<TERM, false, V, N>(a, col + (r + u * kWarps) * inner, r + u * kWarps, v[u]);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < V; ++c) v[u][c] = 0.0f;
+                        for (int k = 0; k < N; ++k)
+#pragma unroll
+                            for (int c = 0; c < V; ++c) v[u][k][c] = 0.0f;
                     }
                 }
 #pragma unroll
@@ -362,7 +401,7 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
                         for (int k = 0; k < N; ++k)
 #pragma unroll
                             for (int c = 0; c < V; ++c)
-                                acc[u & 3][k][c] = acc_fold<OP, MODE>(k, acc[u & 3][k][c], v[u][c]);
+                                acc[u & 3][k][c] = acc_fold<OP, MODE>(k, acc[u & 3][k][c], v[u][k][c]);
                     }
             }
         }
@@ -550,6 +589,9 @@ cudaError_t launch_axis_staged(int term, const AxisArgs& a, int64_t tiles, int s
         case AXIS_LN_BETA:
             axis::axis_kernel<OP_RSUM, axis::STAGED, 1, AXIS_LN_BETA><<<grid, kAxisThreads, smem, stream>>>(a);
             break;
+        case AXIS_LN_BOTH:
+            axis::axis_kernel<OP_RSUM, axis::STAGED, 1, AXIS_LN_BOTH><<<grid, kAxisThreads, smem, stream>>>(a);
+            break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -558,9 +600,10 @@ cudaError_t launch_axis_staged(int term, const AxisArgs& a, int64_t tiles, int s
 template <int TERM>
 cudaError_t launch_term(bool ordered, const AxisArgs& a, int vec, int64_t tiles, int splits, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(splits));
-    if (ordered)
-        axis::axis_kernel<OP_RSUM, axis::TREE, 1, TERM><<<grid, kAxisThreads, 0, stream>>>(a);
-    else if (vec == 4)
+    if (ordered) {
+        if constexpr (TERM == AXIS_LN_BOTH) return cudaErrorInvalidValue;  // the ordered pair is staged only
+        else axis::axis_kernel<OP_RSUM, axis::TREE, 1, TERM><<<grid, kAxisThreads, 0, stream>>>(a);
+    } else if (vec == 4)
         axis::axis_kernel<OP_RSUM, axis::FREE, 4, TERM><<<grid, kAxisThreads, 0, stream>>>(a);
     else
         axis::axis_kernel<OP_RSUM, axis::FREE, 1, TERM><<<grid, kAxisThreads, 0, stream>>>(a);
@@ -573,6 +616,7 @@ cudaError_t launch_axis_term(int term, bool ordered, const AxisArgs& a, int vec,
         case AXIS_RMS_W: return launch_term<AXIS_RMS_W>(ordered, a, vec, tiles, splits, stream);
         case AXIS_LN_GAMMA: return launch_term<AXIS_LN_GAMMA>(ordered, a, vec, tiles, splits, stream);
         case AXIS_LN_BETA: return launch_term<AXIS_LN_BETA>(ordered, a, vec, tiles, splits, stream);
+        case AXIS_LN_BOTH: return launch_term<AXIS_LN_BOTH>(ordered, a, vec, tiles, splits, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -553,7 +553,9 @@ int axis_staged_splits(int64_t rows, int64_t tiles, int arrays, int sm_count) {
 }
 
 // Arrays the staged tree copies per row: x and dy for the two-input terms.
-static int staged_arrays(int term) { return term == AXIS_RMS_W || term == AXIS_LN_GAMMA ? 2 : 1; }
+static int staged_arrays(int term) {
+    return term == AXIS_RMS_W || term == AXIS_LN_GAMMA || term == AXIS_LN_BOTH ? 2 : 1;
+}
 
 // Launch an axis sum / max / min (term AXIS_PLAIN) or the column sum of a
 // backward term over `tiles` column tiles: the staged tree for ordered sums of
@@ -574,8 +576,11 @@ static tr_status axis_dispatch(int op, int term, AxisArgs a, tr_order order, int
         staged = (ordered && op == TR_OP_ROW_SUM) ? axis_staged_splits(a.extent, tiles, staged_arrays(term), sm) : 0;
         if (staged > 0) {
             S = staged;
+        } else if (term == AXIS_LN_BOTH && ordered) {
+            S = 0;  // the ordered pair runs as two single-term sums (below, outside the lock)
         } else {
-            const int values = op == TR_OP_ROW_SUM ? 1 : 2;  // ordered max and min keep two keys per column
+            // ordered max and min keep two keys per column; the LayerNorm pair two sums
+            const int values = (op == TR_OP_ROW_SUM && term != AXIS_LN_BOTH) ? 1 : 2;
             const int ctas = term == AXIS_PLAIN ? axis_ctas_per_sm(op, order) : (ordered ? kAxisCtasTree : kAxisCtasFree);
             S = axis_splits(tiles, a.extent, values, kAxisCols * vec, ctas, sm);
         }
@@ -586,6 +591,14 @@ static tr_status axis_dispatch(int op, int term, AxisArgs a, tr_order order, int
             a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + kAxisPartOffset);
             a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kAxisTicketOffset);
         }
+    }
+    if (S == 0) {
+        AxisArgs g = a, b = a;
+        g.out2 = nullptr;
+        b.out = a.out2;
+        b.out2 = nullptr;
+        tr_status s = axis_dispatch(op, AXIS_LN_GAMMA, g, order, vec, tiles, stream);
+        return s != TR_OK ? s : axis_dispatch(op, AXIS_LN_BETA, b, order, vec, tiles, stream);
     }
     if (staged > 0) {
         const int64_t rows_per = a.extent < kAxisStagedMaxRows / S ? a.extent : kAxisStagedMaxRows / S;
@@ -696,12 +709,12 @@ tr_status tr_norm_backward_workspace_bytes(int64_t rows, int64_t cols, size_t* b
 }
 
 // The column sum over the rows of a norm backward term (see AxisTerm).
-static tr_status term_sum(int term, const BwArgs& b, float* out, tr_order order, cudaStream_t stream) {
+static tr_status term_sum(int term, const BwArgs& b, float* out, float* out2, tr_order order, cudaStream_t stream) {
     const int64_t rows = b.rows, cols = b.cols;
     const bool ordered = order == TR_ORDER_ORDERED_TREE;
     const int vec = (!ordered && cols % 4 == 0 && !misaligned(b.x, 16) && !misaligned(b.dy, 16)) ? 4 : 1;
     const int64_t tiles = (cols + kAxisCols * vec - 1) / (kAxisCols * vec);
-    AxisArgs a{b.x, out, nullptr, rows, cols, cols, nullptr, nullptr, b.dy, b.stat_a, b.stat_b};
+    AxisArgs a{b.x, out, out2, rows, cols, cols, nullptr, nullptr, b.dy, b.stat_a, b.stat_b};
     return axis_dispatch(TR_OP_ROW_SUM, term, a, order, vec, tiles, stream);
 }
 
@@ -718,14 +731,9 @@ static tr_status bw_run(int op, BwArgs a, tr_order order, float* dw, float* db, 
     const bool ordered = order == TR_ORDER_ORDERED_TREE;
     cudaError_t e = launch_backward(op, ordered, bw_slots(a.cols), a, static_cast<int>(bw_ctas(a.rows)), stream);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    if (dw) {
-        tr_status s = term_sum(op == BW_RMSNORM ? AXIS_RMS_W : AXIS_LN_GAMMA, a, dw, order, stream);
-        if (s != TR_OK) return s;
-    }
-    if (db) {
-        tr_status s = term_sum(AXIS_LN_BETA, a, db, order, stream);
-        if (s != TR_OK) return s;
-    }
+    if (dw && db) return term_sum(AXIS_LN_BOTH, a, dw, db, order, stream);  // one pass over x and dy
+    if (dw) return term_sum(op == BW_RMSNORM ? AXIS_RMS_W : AXIS_LN_GAMMA, a, dw, nullptr, order, stream);
+    if (db) return term_sum(AXIS_LN_BETA, a, db, nullptr, order, stream);
     return TR_OK;
 }
 

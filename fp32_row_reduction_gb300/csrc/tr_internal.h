@@ -88,7 +88,8 @@ enum AxisTerm : int {
     AXIS_PLAIN = 0,
     AXIS_RMS_W = 1,   // (dy x) r,              sa = r = 1 / rms
     AXIS_LN_GAMMA = 2,  // dy ((x - mean) r),   sa = mean, sb = r = 1 / sigma
-    AXIS_LN_BETA = 3  // dy
+    AXIS_LN_BETA = 3,   // dy
+    AXIS_LN_BOTH = 4    // the LayerNorm's two column gradients at once: out = dgamma, out2 = dbeta
 };
 
 // Launch the ordered column sum (plain or of a term) of a reduced axis of at
