@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
                     if (j < nj) {
                         stage_quad(slot_x(j), xr, cols, j, x_al);
                         if constexpr (OP != BW_XENT) stage_quad(slot_d(j), dr, cols, j, d_al);
+                        // the norms' weight quads into L1 while the row lands
+                        if ((OP == BW_RMSNORM || OP == BW_LAYERNORM) && a.w && 1024 * j + t4 < cols)
+                            prefetch_l1(a.w + 1024 * j + t4);
                     }
                 }
             }
