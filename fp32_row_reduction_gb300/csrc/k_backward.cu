@@ -191,20 +191,70 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
                 stage_next(j);
             });
         } else if constexpr (OP == BW_XENT) {
-            clear(__int_as_float(0xff800000));
-            for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+            float m, inv;
+            if constexpr (!O && K == 0) {
+                // a row read from memory per pass: the maximum and the sum of
+                // exponentials in one online pass (a running pair per leaf, the sum
+                // rescaled when the maximum grows), so the row is read twice, not three times
+                float lm[4], ls[4];
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    if (ok[v]) leaf[v] = fmaxf(leaf[v], x[v]);
-            });
-            const float m = tree<Max>(leaf, gpart, buf);
-            clear(0.0f);
-            for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+                for (int v = 0; v < 4; ++v) {
+                    lm[v] = __int_as_float(0xff800000);
+                    ls[v] = 0.0f;
+                }
+                for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    if (ok[v]) leaf[v] = add<O>(leaf[v], exp_shift<O>(x[v], m));
-            });
-            const float inv = divide<O>(1.0f, tree<Add>(leaf, gpart, buf));
+                    for (int v = 0; v < 4; ++v) {
+                        if (!ok[v]) continue;
+                        if (x[v] > lm[v]) {
+                            ls[v] = ls[v] * ex2((lm[v] - x[v]) * kL2E) + 1.0f;
+                            lm[v] = x[v];
+                        } else {
+                            ls[v] += ex2((x[v] - lm[v]) * kL2E);
+                        }
+                    }
+                });
+                auto merge = [](float& ma, float& sa, float mb, float sb) {
+                    const float mm = fmaxf(ma, mb);
+                    if (mm == __int_as_float(0xff800000)) return;  // both empty
+                    sa = sa * ex2((ma - mm) * kL2E) + sb * ex2((mb - mm) * kL2E);
+                    ma = mm;
+                };
+                float pm = lm[0], ps = ls[0];
+#pragma unroll
+                for (int v = 1; v < 4; ++v) merge(pm, ps, lm[v], ls[v]);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    const float om = __shfl_xor_sync(kFull, pm, o), os = __shfl_xor_sync(kFull, ps, o);
+                    merge(pm, ps, om, os);
+                }
+                if ((threadIdx.x & 31) == 0) {
+                    gpart[0][threadIdx.x >> 5] = pm;
+                    gpart[1][threadIdx.x >> 5] = ps;
+                }
+                __syncthreads();
+                float gm = gpart[0][0], gs = gpart[1][0];
+#pragma unroll
+                for (int q = 1; q < 8; ++q) merge(gm, gs, gpart[0][q], gpart[1][q]);
+                __syncthreads();  // the next row writes both slots again
+                m = gm;
+                inv = divide<O>(1.0f, gs);
+            } else {
+                clear(__int_as_float(0xff800000));
+                for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (ok[v]) leaf[v] = fmaxf(leaf[v], x[v]);
+                });
+                m = tree<Max>(leaf, gpart, buf);
+                clear(0.0f);
+                for_quads([&](int, const float (&x)[4], const float (&)[4], const bool (&ok)[4]) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (ok[v]) leaf[v] = add<O>(leaf[v], exp_shift<O>(x[v], m));
+                });
+                inv = divide<O>(1.0f, tree<Add>(leaf, gpart, buf));
+            }
             const int64_t label = a.labels[row];
             const bool scaled = a.dloss != nullptr;
             const float dl = scaled ? a.dloss[row] : 1.0f;

@@ -29,7 +29,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 U = 2.0 ** -24
 SHAPES = [(1, 1), (5, 3), (4, 127), (17, 257), (3, 1024), (7, 1025), (37, 1537), (2, 4096), (9, 6144),
-          (3, 8193), (2, 20000), (1100, 64)]
+          (3, 8193), (2, 20000), (2, 60000), (1100, 64)]
 
 
 @pytest.fixture(scope="module", autouse=True)
