@@ -122,3 +122,37 @@ def test_noalloc_entry_rejects_bad_arguments_on_the_host(lib):
     # more rows than the fixed scratch holds: refused before any CUDA call
     assert f(0, 0x1000, None, None, 0x10000000, 257, 10, 0.0, None) == trlib.TR_ERR_UNSUPPORTED
     assert "256 rows" in lib.tr_last_error_message().decode()
+
+
+def test_next_row_entry_points_validate_on_the_host(lib):
+    L = trlib.load()
+    E, U = trlib.TR_ERR_INVALID_ARG, trlib.TR_ERR_UNSUPPORTED
+    # backward passes: null outputs, aliasing, bad order, fold orders refused
+    assert L.tr_softmax_backward_f32(FAKE, FAKE + 4096, None, 2, 8, 0, None) == E
+    assert L.tr_softmax_backward_f32(FAKE, FAKE + 4096, FAKE, 2, 8, 0, None) == E          # dx aliases y
+    assert L.tr_softmax_backward_f32(FAKE, FAKE + 4096, FAKE + 8192, 2, 8, 9, None) == E
+    assert L.tr_softmax_backward_f32(FAKE, FAKE + 4096, FAKE + 8192, 2, 8, 2, None) == U    # fold_left
+    assert L.tr_cross_entropy_backward_f32(FAKE, None, None, FAKE + 8192, 2, 8, 0, None) == E
+    assert L.tr_rmsnorm_backward_f32(FAKE, None, FAKE + 4096, FAKE + 8192, None, 2, 8, -1.0, 0, None, 0, None) == E
+    assert L.tr_layernorm_backward_f32(FAKE, None, FAKE + 4096, FAKE + 8192, None, None, 2, 8, 1e-5, 3, None, 0,
+                                       None) == U
+    n = ctypes.c_size_t(0)
+    assert L.tr_norm_backward_workspace_bytes(10, 100, ctypes.byref(n)) == trlib.TR_OK and n.value == 80
+    # axis reductions: sizes, aliasing, fold orders refused
+    assert L.tr_axis_sum_f32(FAKE, FAKE + 4096, 2, 0, 4, 0, None) == E
+    assert L.tr_axis_sum_f32(FAKE, FAKE, 2, 3, 4, 0, None) == E
+    assert L.tr_axis_max_f32(FAKE, FAKE + 4096, 2, 3, 4, 3, None) == U
+    assert L.tr_axis_minmax_f32(FAKE, FAKE + 4096, None, 2, 3, 4, 0, None) == E
+    # row reductions and the fused norms under bad arguments
+    assert L.tr_row_minmax_f32(FAKE, FAKE + 4096, None, 2, 8, 0, None) == E
+    assert L.tr_row_sum_f32(FAKE, FAKE + 4096, 2, 8, 4, None) == E
+    assert L.tr_add_rmsnorm_f32(FAKE, None, None, FAKE + 4096, None, 2, 8, 1e-5, 0, None) == E
+
+
+def test_axis_launch_shape_on_the_host(lib):
+    sp, tl = trlib.axis_launch_shape("sum", 1, 768, 6144, 152)
+    assert tl == 48 and 1 <= sp <= 32 and sp & (sp - 1) == 0
+    sp, tl = trlib.axis_launch_shape("sum", 1, 768, 6144, 152, "ordered")
+    assert tl == 192 and sp in (1, 2, 4, 8)
+    sp, tl = trlib.axis_launch_shape("sum", 1, 20000, 7, 152)
+    assert tl == 1 and sp == 32
