@@ -327,13 +327,38 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
         return make_float4(split_out<OP>(c.x, scale, shift, mb), split_out<OP>(c.y, scale, shift, mb),
                            split_out<OP>(c.z, scale, shift, mb), split_out<OP>(c.w, scale, shift, mb));
     };
+    // the weight and bias loads of the norms issue with the row's, not after them
+    auto pload = [&](const float* p, int j, bool vec, float dflt) {
+        return p ? ld_param(p + g.head + 4 * j, vec) : f4(dflt);
+    };
+    const float* pw = a.has_w ? a.w : nullptr;
+    const float* pb = (OP == OP_LAYERNORM && a.has_b) ? a.b : nullptr;
     i = v0 + nsm + t;
     for (; i + (kSplitU - 1) * T < v1; i += kSplitU * T) {
         float4 c[kSplitU];
+        if constexpr (OP == OP_SOFTMAX) {
 #pragma unroll
-        for (int u = 0; u < kSplitU; ++u) c[u] = ld_stream4(xb + 4 * (i + u * T));
+            for (int u = 0; u < kSplitU; ++u) c[u] = ld_stream4(xb + 4 * (i + u * T));
 #pragma unroll
-        for (int u = 0; u < kSplitU; ++u) st_out(yb + 4 * (i + u * T), params(out4(c[u]), i + u * T), a.y_vec);
+            for (int u = 0; u < kSplitU; ++u) st_out(yb + 4 * (i + u * T), out4(c[u]), a.y_vec);
+        } else {
+            float4 w4[kSplitU], b4[kSplitU];
+#pragma unroll
+            for (int u = 0; u < kSplitU; ++u) {
+                c[u] = ld_stream4(xb + 4 * (i + u * T));
+                w4[u] = pload(pw, i + u * T, wv, 1.0f);
+                b4[u] = pload(pb, i + u * T, bv, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < kSplitU; ++u) {
+                float4 o = out4(c[u]);
+                o.x = fmaf(o.x, w4[u].x, b4[u].x);
+                o.y = fmaf(o.y, w4[u].y, b4[u].y);
+                o.z = fmaf(o.z, w4[u].z, b4[u].z);
+                o.w = fmaf(o.w, w4[u].w, b4[u].w);
+                st_out(yb + 4 * (i + u * T), o, a.y_vec);
+            }
+        }
     }
     for (; i < v1; i += T) st_out(yb + 4 * i, params(out4(ld_stream4(xb + 4 * i)), i), a.y_vec);
     if constexpr (OP == OP_SOFTMAX) {
@@ -343,11 +368,6 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
         }
     } else {
         // kSplitU slots at a time, so that their weight/bias loads are in flight together
-        auto pload = [&](const float* p, int j, bool vec, float dflt) {
-            return p ? ld_param(p + g.head + 4 * j, vec) : f4(dflt);
-        };
-        const float* pw = a.has_w ? a.w : nullptr;
-        const float* pb = (OP == OP_LAYERNORM && a.has_b) ? a.b : nullptr;
         int j = t;
         for (; j + (kSplitU - 1) * T < nsm; j += kSplitU * T) {
             float4 w4[kSplitU], b4[kSplitU];
