@@ -29,6 +29,7 @@
 //   folded freely in key space, and a tile with a NaN in any column is
 //   recomputed by its last CTA with the canonical tree.
 #include <climits>
+#include <type_traits>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -311,54 +312,73 @@ __global__ void __launch_bounds__(kAxisThreads, min_ctas<MODE>()) axis_kernel(Ax
         const int64_t rs = static_cast<int64_t>(s) * per;
         const int64_t re = rs + per < R ? rs + per : R;
         if (jok) {
+            // pointers advance by a stride: no 64-bit product per copy
             const float* gcol = TERM == AXIS_PLAIN ? col : a.dy + (col - a.x);
+            const int64_t step = kWarps * inner;
+            const float* src = (TERM == AXIS_LN_BETA ? gcol : col) + (rs + w) * inner;
+            const float* srd = gcol + (rs + w) * inner;
+            float* dx = sx + w * 32 + lane;
+            float* dd = sd + w * 32 + lane;
             for (int64_t r = rs + w; r < re; r += kWarps) {
-                const int64_t i = (r - rs) * 32 + lane;
-                cp_async4(sx + i, (TERM == AXIS_LN_BETA ? gcol : col) + r * inner);
-                if constexpr (two) cp_async4(sd + i, gcol + r * inner);
+                cp_async4(dx, src);
+                if constexpr (two) cp_async4(dd, srd);
+                src += step;
+                srd += step;
+                dx += kWarps * 32;
+                dd += kWarps * 32;
             }
         }
         cp_async_wait_all();
         __syncthreads();
-        // value k of row r's element
-        auto elem = [&](int64_t r, int k) {
-            const int64_t i = (r - rs) * 32 + lane;
+        // value k of the element of row rs + i
+        auto elem = [&](int i, int64_t r, int k) {
+            const int at = i * 32 + lane;
             if constexpr (TERM == AXIS_PLAIN || TERM == AXIS_LN_BETA) {
-                return sx[i];
+                return sx[at];
             } else if constexpr (TERM == AXIS_RMS_W) {
-                return __fmul_rn(__fmul_rn(sd[i], sx[i]), __ldg(a.sa + r));
+                return __fmul_rn(__fmul_rn(sd[at], sx[at]), __ldg(a.sa + r));
             } else {
-                if (TERM == AXIS_LN_BOTH && k == 1) return sd[i];
-                return __fmul_rn(sd[i], __fmul_rn(__fsub_rn(sx[i], __ldg(a.sa + r)), __ldg(a.sb + r)));
+                if (TERM == AXIS_LN_BOTH && k == 1) return sd[at];
+                return __fmul_rn(sd[at], __fmul_rn(__fsub_rn(sx[at], __ldg(a.sa + r)), __ldg(a.sb + r)));
             }
         };
+        // this warp's P (a power of two, at most 32) quad positions, then the
+        // perfect tree over them, adjacent pairs level by level; unrolled for at
+        // most 8 positions (the usual splits) or for 32, so only one short path runs
         const int P = kQuads / (S * kWarps);
         const int p0 = s * (kQuads / S) + w * P;
-        float stk[5][N];
-        float cur[N];
+        auto fold_positions = [&](auto pmax) {
+            constexpr int PM = decltype(pmax)::value;
+            float q[N][PM];
 #pragma unroll
-        for (int k = 0; k < N; ++k) {
-            cur[k] = 0.0f;
+            for (int n = 0; n < PM; ++n) {
+                if (n < P) {
+                    const int p = p0 + n;
+                    const int e0 = 4 * (32 * (p >> 5) + static_cast<int>(__brev(p & 31) >> 27));
 #pragma unroll
-            for (int lv = 0; lv < 5; ++lv) stk[lv][k] = 0.0f;
-        }
-        for (int n = 0; n < P; ++n) {
-            const int p = p0 + n;
-            const int64_t e0 = 4 * (32 * (p >> 5) + static_cast<int>(__brev(p & 31) >> 27));
-            float q[N];
+                    for (int k = 0; k < N; ++k) {
+                        float l[4];
 #pragma unroll
-            for (int k = 0; k < N; ++k) {
-                float l[4];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) l[v] = e0 + v < R ? __fadd_rn(0.0f, elem(e0 + v, k)) : 0.0f;
-                q[k] = __fadd_rn(__fadd_rn(l[0], l[1]), __fadd_rn(l[2], l[3]));
+                        for (int v = 0; v < 4; ++v)
+                            l[v] = e0 + v < R ? __fadd_rn(0.0f, elem(static_cast<int>(e0 + v - rs), e0 + v, k)) : 0.0f;
+                        q[k][n] = __fadd_rn(__fadd_rn(l[0], l[1]), __fadd_rn(l[2], l[3]));
+                    }
+                }
             }
-            push<AddF, N>(stk, q, n);
 #pragma unroll
-            for (int k = 0; k < N; ++k) cur[k] = q[k];
-        }
+            for (int wd = 1; wd < PM; wd *= 2)
 #pragma unroll
-        for (int k = 0; k < N; ++k) res[k][0] = cur[k];
+                for (int n = 0; n + wd < PM; n += 2 * wd)
+                    if (n + wd < P)
+#pragma unroll
+                        for (int k = 0; k < N; ++k) q[k][n] = __fadd_rn(q[k][n], q[k][n + wd]);
+#pragma unroll
+            for (int k = 0; k < N; ++k) res[k][0] = q[k][0];
+        };
+        if (P <= 8)
+            fold_positions(std::integral_constant<int, 8>{});
+        else
+            fold_positions(std::integral_constant<int, 32>{});
     } else if constexpr (MODE == TREE) {
         static_assert(OP == OP_RSUM, "the tree mode folds sums");
         const int P = kQuads / (S * kWarps);
