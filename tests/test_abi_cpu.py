@@ -156,3 +156,20 @@ def test_axis_launch_shape_on_the_host(lib):
     assert tl == 192 and sp in (1, 2, 4, 8)
     sp, tl = trlib.axis_launch_shape("sum", 1, 20000, 7, 152)
     assert tl == 1 and sp == 32
+
+
+def test_empty_inputs_are_a_no_op_on_every_entry_point(lib):
+    L = trlib.load()
+    ok = trlib.TR_OK
+    ws = ctypes.c_size_t(0)
+    assert L.tr_softmax_backward_f32(FAKE, FAKE + 4096, FAKE + 8192, 0, 8, 0, None) == ok
+    assert L.tr_cross_entropy_backward_f32(FAKE, FAKE + 4096, None, FAKE + 8192, 0, 8, 1, None) == ok
+    assert L.tr_rmsnorm_backward_f32(FAKE, None, FAKE + 4096, FAKE + 8192, FAKE + 12288, 0, 8, 1e-5, 0, None, 0,
+                                     None) == ok
+    assert L.tr_layernorm_backward_f32(FAKE, None, FAKE + 4096, FAKE + 8192, None, None, 0, 8, 1e-5, 1, None, 0,
+                                       None) == ok
+    assert L.tr_norm_backward_workspace_bytes(0, 8, ctypes.byref(ws)) == ok and ws.value == 0
+    assert L.tr_axis_sum_f32(FAKE, FAKE + 4096, 0, 5, 3, 1, None) == ok
+    for order in (0, 1, 2, 3):
+        assert L.tr_row_sum_f32(FAKE, FAKE + 4096, 0, 8, order, None) == ok
+        assert L.tr_softmax_f32(FAKE, FAKE + 4096, 0, 8, order, None) == ok
