@@ -164,7 +164,20 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
                     }
                 }
             } else {
-                for (int j = 0; j < nj; ++j) {
+                // four quads' loads in flight, then their folds in increasing j
+                int j = 0;
+                for (; j + 3 < nj; j += 4) {
+                    float qx[4][4], qd[4][4] = {};
+                    bool ok[4][4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        load_quad(xr, cols, j + u, x_al, qx[u], ok[u]);
+                        if constexpr (OP != BW_XENT) load_quad(dr, cols, j + u, d_al, qd[u], ok[u]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) fn(j + u, qx[u], qd[u], ok[u]);
+                }
+                for (; j < nj; ++j) {
                     float qx[4], qd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                     bool ok[4];
                     load_quad(xr, cols, j, x_al, qx, ok);
