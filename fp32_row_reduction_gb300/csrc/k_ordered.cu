@@ -284,14 +284,29 @@ __global__ void __launch_bounds__(kOrderedThreads, ot_min_blocks<K>()) ot_kernel
         auto emit = [&](auto out) {
             float* yr = a.y + row * cols;
             const bool vec = aligned && a.y_vec;
-            for (int j = 0; j < nj; ++j) {
-                float qq[4], o[4];
-                bool oo[4];
-                load_quad(xr, cols, j, aligned, qq, oo);
+            auto one = [&](int jj, const float (&qq)[4], const bool (&oo)[4]) {
+                float o[4];
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
-                    o[v] = oo[v] ? out(qq[v], j * 1024 + 4 * static_cast<int>(threadIdx.x) + v) : 0.0f;
-                store_quad(yr, cols, j, vec, o, oo);
+                    o[v] = oo[v] ? out(qq[v], jj * 1024 + 4 * static_cast<int>(threadIdx.x) + v) : 0.0f;
+                store_quad(yr, cols, jj, vec, o, oo);
+            };
+            int j = 0;
+            // softmax: four quads' loads in flight (the norms' per-element weight loads
+            // measured slower batched)
+            for (; OP == OP_SOFTMAX && j + 3 < nj; j += 4) {
+                float qq[4][4];
+                bool oo[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) load_quad(xr, cols, j + u, aligned, qq[u], oo[u]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) one(j + u, qq[u], oo[u]);
+            }
+            for (; j < nj; ++j) {
+                float qq[4];
+                bool oo[4];
+                load_quad(xr, cols, j, aligned, qq, oo);
+                one(j, qq, oo);
             }
         };
         auto add = [](float p, float v) { return __fadd_rn(p, v); };
