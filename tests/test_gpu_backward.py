@@ -216,3 +216,47 @@ def test_full_size_768x6144():
             want = oracle.layernorm_backward(x, g, dy, 1e-5)
             for a, b, bd, nm in zip(got, want, ln_bounds(x, g, dy, 1e-5), ("dx", "dgamma", "dbeta")):
                 within(a, b, bd, f"ln bwd {nm} 768x6144")
+
+
+def offset_copy(a, off):
+    """A copy of the float32 array a in device memory starting `off` floats past a 16-byte boundary."""
+    big = torch.empty(a.size + 8, device=DEV)
+    v = big[off:off + a.size].view(*a.shape)
+    v.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return v
+
+
+@pytest.mark.parametrize("offs", [(1, 0, 0), (0, 2, 3), (3, 1, 2)])
+def test_unaligned_tensors(offs):
+    rows, cols = 5, 3001
+    x, g, dy = norm_inputs(rows, cols, seed=sum(offs) + 3)
+    X, DY = offset_copy(x, offs[0]), offset_copy(dy, offs[1])
+    for order in ("unordered", "ordered"):
+        big = torch.zeros(rows * cols + 8, device=DEV)
+        DX = big[offs[2]:offs[2] + rows * cols].view(rows, cols)
+        dx, dg, db = tr.layernorm_backward(X, dev(g), DY, 1e-5, order=order, dx=DX)
+        torch.cuda.synchronize()
+        got = [t.cpu().numpy() for t in (dx, dg, db)]
+        if order == "ordered":
+            for a, b, nm in zip(got, oracle.ot_layernorm_backward(x, g, dy, 1e-5), ("dx", "dgamma", "dbeta")):
+                same_bits(a, b, f"ln bwd {nm} offsets {offs}")
+        else:
+            want = oracle.layernorm_backward(x, g, dy, 1e-5)
+            for a, b, bd, nm in zip(got, want, ln_bounds(x, g, dy, 1e-5), ("dx", "dgamma", "dbeta")):
+                within(a, b, bd, f"ln bwd {nm} offsets {offs}")
+        y = oracle.ot_softmax(x)
+        Y = offset_copy(y, offs[0])
+        big2 = torch.zeros(rows * cols + 8, device=DEV)
+        DX2 = big2[offs[2]:offs[2] + rows * cols].view(rows, cols)
+        tr.softmax_backward(Y, DY, out=DX2, order=order)
+        torch.cuda.synchronize()
+        if order == "ordered":
+            same_bits(DX2.cpu().numpy(), oracle.ot_softmax_backward(y, dy), f"softmax bwd offsets {offs}")
+        labels = synth.labels_i64(rows, cols, seed=7)
+        L = offset_copy(x, offs[1])
+        big3 = torch.zeros(rows * cols + 8, device=DEV)
+        DL = big3[offs[2]:offs[2] + rows * cols].view(rows, cols)
+        tr.cross_entropy_backward(L, labels.to(DEV), None, out=DL, order=order)
+        torch.cuda.synchronize()
+        if order == "ordered":
+            same_bits(DL.cpu().numpy(), oracle.ot_cross_entropy_backward(x, labels.numpy()), f"xent bwd offsets {offs}")
