@@ -124,7 +124,7 @@ bool opt_in_wide_cluster(DeviceState& st, const void* fn) {
 int64_t query_occupancy(DeviceState& st, const tr_plan& p, size_t smem) {
     const void* fn = kernel_for(p);
     if (!fn) return 0;
-    const int C = (p.kind == TR_PLAN_CLUSTER || p.kind == TR_PLAN_STREAM) ? p.cluster_ctas : 1;
+    const int C = (p.kind == TR_PLAN_CLUSTER || p.kind == TR_PLAN_STREAM || p.kind == TR_PLAN_ORDERED) ? p.cluster_ctas : 1;
     const auto key = std::make_tuple(fn, p.block_threads, C, smem);
     auto it = st.occ.find(key);
     if (it != st.occ.end()) return it->second;

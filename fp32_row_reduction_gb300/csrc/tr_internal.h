@@ -130,6 +130,11 @@ const void* kernel_add_rmsnorm(int kind, int lanes, int slots, int flags);
 const void* kernel_add_layernorm(int kind, int lanes, int slots, int flags);
 const void* kernel_reduce(int op, int kind, int lanes, int slots, int flags);
 const void* kernel_ordered_staged(int op, int slots);
+// OT-1024 for few long rows: a cluster of kOtClusterCtas CTAs per row, one per group of the tree.
+const void* kernel_ordered_cluster(int op);
+constexpr int kOtClusterCtas = 8;
+constexpr size_t kOtClusterSmemMax = 200 * 1024;  // a group's share of the row staged in shared memory
+inline size_t ot_cluster_smem(int64_t cols) { return static_cast<size_t>((cols + 1023) / 1024) * 32 * 16; }
 // Dynamic shared memory a plan's kernel needs (0 for all but staged plans).
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols);
 
@@ -143,6 +148,8 @@ inline const void* kernel_for(const tr_plan& p) {
         if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
         return kernel_reduce(p.op, p.kind, p.lanes_per_row, p.vec_slots, p.flags);
     }
+    if (p.kind == TR_PLAN_ORDERED && p.cluster_ctas == kOtClusterCtas)
+        return p.flags ? nullptr : kernel_ordered_cluster(p.op);
     if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
     if (p.kind == TR_PLAN_ORDERED_STAGED) return p.flags ? nullptr : kernel_ordered_staged(p.op, p.vec_slots);
     switch (p.op) {

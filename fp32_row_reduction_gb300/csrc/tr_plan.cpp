@@ -129,6 +129,7 @@ tr_device_desc gb300_desc() {
 
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols) {
     if (p.kind == TR_PLAN_SPLIT) return static_cast<size_t>(p.vec_slots) * p.block_threads * 16;
+    if (p.kind == TR_PLAN_ORDERED && p.cluster_ctas == kOtClusterCtas) return ot_cluster_smem(cols);
     if (p.kind == TR_PLAN_ROWS && (p.flags & TR_PLAN_FLAG_PARAMS_IN_SHARED))
         return static_cast<size_t>(cols) * 4 * (base_op(p.op) == TR_OP_LAYERNORM ? 2 : 1);
     if (p.kind != TR_PLAN_STAGED && p.kind != TR_PLAN_ORDERED_STAGED) return 0;
@@ -228,8 +229,19 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     const int G = p->lanes_per_row;
     switch (p->kind) {
         case TR_PLAN_ORDERED: {
-            if (T != kOrderedThreads || G != 32 || p->warps_per_row != 8 || p->rows_per_cta != 1 || p->cluster_ctas != 1)
-                return fail(TR_ERR_UNSUPPORTED, "OT-1024 runs 256 threads (8 warps) per row, one row per CTA");
+            if (T != kOrderedThreads || G != 32 || p->warps_per_row != 8 || p->rows_per_cta != 1)
+                return fail(TR_ERR_UNSUPPORTED, "OT-1024 runs 256 threads (8 warps) per CTA, one row per CTA or cluster");
+            if (p->cluster_ctas == kOtClusterCtas) {
+                // one CTA per group of the tree: a base operator's row whose group shares fit shared memory
+                if (k != 0 || residual_op(p->op) || reduce_op(p->op))
+                    return fail(TR_ERR_UNSUPPORTED, "the group-cluster OT-1024 serves the four operators, vec_slots 0");
+                if (ot_cluster_smem(cols) > kOtClusterSmemMax)
+                    return fail(TR_ERR_UNSUPPORTED, "a group's share of the row does not fit shared memory");
+                p->grid_ctas = rows * kOtClusterCtas;
+                break;
+            }
+            if (p->cluster_ctas != 1)
+                return fail(TR_ERR_UNSUPPORTED, "OT-1024 runs one CTA per row, or one cluster of 8 per row");
             if (!in(kOrderedSlots, k)) return fail(TR_ERR_UNSUPPORTED, "no OT-1024 kernel with that vec_slots");
             if (k > 0 && static_cast<int64_t>(1024) * k < cols)
                 return fail(TR_ERR_UNSUPPORTED, "cached OT-1024 needs cols <= 1024 * vec_slots");
@@ -495,7 +507,17 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
         p.block_threads = kOrderedThreads;
         const int k = smallest_covering(kOrderedSlots, ceil_div(cols, 1024));
         p.vec_slots = (k < 0 || reduce_op(op)) ? 0 : k;  // a standalone reduction streams its row
-        if (!res || p.vec_slots > 0) cands.push_back(p);
+        // few long rows (re-read realisation, fewer rows than two per SM): a cluster of
+        // 8 CTAs per row, one per group of the tree, spreads each row over 8 SMs
+        const bool few_long = p.vec_slots == 0 && !res && !reduce_op(op) && rows < 2LL * d.sm_count &&
+                              ot_cluster_smem(cols) <= kOtClusterSmemMax;
+        if (few_long) {
+            tr_plan q = p;
+            q.cluster_ctas = kOtClusterCtas;
+            cands.push_back(q);
+        } else if (!res || p.vec_slots > 0) {
+            cands.push_back(p);
+        }
         // the staged OT-1024 realisation (TR_PLAN_ORDERED_STAGED) stays available by
         // override; measured plan sweeps found the one-shot realisation at full
         // occupancy as fast or faster, so it is not an automatic candidate

@@ -490,3 +490,30 @@ def test_768x6144_ordered_bit_exact(op):
     h = host(d)
     assert np.array_equal(got.view(np.uint32), emulated(op, h).view(np.uint32))
     assert_close(got, reference(op, h), f"ordered {op} 768x6144")
+
+
+@pytest.mark.parametrize("rows,cols", [(3, 16385), (5, 20001), (16, 65536), (4, 262144), (2, 409600)])
+@pytest.mark.parametrize("op", ["softmax", "rmsnorm", "layernorm", "cross_entropy"])
+def test_ordered_group_cluster_matches_emulation(op, rows, cols):
+    # few long rows: OT-1024 on a cluster of 8 CTAs per row (one per group of the tree)
+    import oracle
+    plan = tr.plan_for(op, rows, cols, "ordered")
+    assert plan["cluster_ctas"] == 8 and plan["grid_ctas"] == 8 * rows
+    d = synth.make_inputs(op, rows, cols, seed=rows + cols, row_offset=op in ("rmsnorm", "layernorm"),
+                          device="cuda:0")
+    h = {k: v.cpu().numpy() for k, v in d.items()}
+    if op == "cross_entropy":
+        got = tr.cross_entropy(d["x"], d["labels"], order="ordered")
+        want = oracle.ot_cross_entropy(h["x"], h["labels"])
+    elif op == "softmax":
+        got = tr.softmax(d["x"], order="ordered")
+        want = oracle.ot_softmax(h["x"])
+    elif op == "rmsnorm":
+        got = tr.rmsnorm(d["x"], d["w"], 1e-5, order="ordered")
+        want = oracle.ot_rmsnorm(h["x"], h["w"], 1e-5)
+    else:
+        got = tr.layernorm(d["x"], d["w"], d["b"], 1e-5, order="ordered")
+        want = oracle.ot_layernorm(h["x"], h["w"], h["b"], 1e-5)
+    torch.cuda.synchronize()
+    g = got.cpu().numpy()
+    assert np.array_equal(g.view(np.uint32), np.asarray(want, np.float32).view(np.uint32))

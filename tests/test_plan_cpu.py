@@ -83,11 +83,16 @@ def test_cross_entropy_uses_the_streaming_plan(rows, cols):
 def test_ordered_requests_get_the_fixed_tree(op, rows, cols):
     p = select(op, rows, cols, order=1)
     assert p.kind in (trlib.TR_PLAN_ORDERED, trlib.TR_PLAN_ORDERED_STAGED)
-    assert p.block_threads == 256 and p.cluster_ctas == 1
+    assert p.block_threads == 256
     assert covers(p, cols)
-    if p.kind == trlib.TR_PLAN_ORDERED:
-        assert p.rows_per_cta == 1 and p.grid_ctas == rows
+    if p.kind == trlib.TR_PLAN_ORDERED and p.cluster_ctas == 8:
+        # few long rows: a cluster per row, one CTA per group of the tree
+        assert p.vec_slots == 0 and cols > 16 * 1024 and rows < 2 * DEV.sm_count
+        assert p.grid_ctas == 8 * rows and math.ceil(cols / 1024) * 512 <= 200 * 1024
+    elif p.kind == trlib.TR_PLAN_ORDERED:
+        assert p.cluster_ctas == 1 and p.rows_per_cta == 1 and p.grid_ctas == rows
     else:
+        assert p.cluster_ctas == 1
         assert 1 <= p.rows_per_cta <= 8 and p.grid_ctas == min(rows, p.ctas_per_sm * DEV.sm_count)
 
 
@@ -203,3 +208,12 @@ def test_fold_orders_get_the_warp_per_row_plan(order):
     with pytest.raises(trlib.TrError) as e:
         select(trlib.TR_OP_ADD_LAYERNORM, 4, 8, order=order)
     assert e.value.status == trlib.TR_ERR_UNSUPPORTED
+
+
+def test_few_long_ordered_rows_spread_over_a_cluster():
+    for op in (0, 1, 2, 3):
+        p = select(op, 16, 262144, order=1)
+        assert p.kind == trlib.TR_PLAN_ORDERED and p.cluster_ctas == 8 and p.grid_ctas == 128
+        assert select(op, 16, 1048576, order=1).cluster_ctas == 1      # a group's share exceeds shared memory
+        assert select(op, 4096, 50257, order=1).cluster_ctas == 1      # enough rows for a CTA each
+    assert select(trlib.TR_OP_ROW_SUM, 16, 262144, order=1).cluster_ctas == 1
