@@ -63,14 +63,22 @@ __global__ void __launch_bounds__(kOrderedThreads) ot_cluster_kernel(const RowAr
     auto fold_group = [&](auto elem, auto R, float init) -> float {
         using F = decltype(R);
         float leaf[4] = {init, init, init, init};
-        for (int m = 0; m < nm; ++m) {
-            const float4 q4 = slab[m * 32 + lane];
+        auto take = [&](const float4& q4, int m) {
             const float q[4] = {q4.x, q4.y, q4.z, q4.w};
             const int c0 = 1024 * m + 128 * W + 4 * lane;
 #pragma unroll
             for (int v = 0; v < 4; ++v)
                 if (c0 + v < cols) leaf[v] = F::f(leaf[v], elem(q[v], c0 + v));
+        };
+        int m = 0;
+        for (; m + 7 < nm; m += 8) {  // eight shared-memory loads ahead of their folds
+            float4 q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) q[u] = slab[(m + u) * 32 + lane];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) take(q[u], m + u);
         }
+        for (; m < nm; ++m) take(slab[m * 32 + lane], m);
         float val = F::f(F::f(leaf[0], leaf[1]), F::f(leaf[2], leaf[3]));
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) val = F::f(val, __shfl_xor_sync(kFull, val, o));
