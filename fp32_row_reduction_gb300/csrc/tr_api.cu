@@ -64,12 +64,19 @@ const bool g_pdl = [] {
 }();
 constexpr long long kWaitNs = 2000000000LL;  // a bounded device wait gives up after 2 s
 
-// Allow a kernel the full dynamic shared memory budget (once per kernel and device).
+// Allow a kernel the full dynamic shared memory budget (once per kernel and
+// device), less what its static shared memory takes of the per-CTA limit.
 bool opt_in_smem(DeviceState& st, const void* fn) {
     auto it = st.smem_opt_in.find(fn);
     if (it != st.smem_opt_in.end()) return it->second;
-    const bool ok =
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmemBudget) == cudaSuccess;
+    cudaFuncAttributes fa;
+    int dev = 0, optin = 0;
+    bool ok = cudaFuncGetAttributes(&fa, fn) == cudaSuccess && cudaGetDevice(&dev) == cudaSuccess &&
+              cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess;
+    if (ok) {
+        const int budget = std::min<int>(kStagedSmemBudget, optin - static_cast<int>(fa.sharedSizeBytes));
+        ok = budget > 0 && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, budget) == cudaSuccess;
+    }
     if (!ok) cudaGetLastError();
     st.smem_opt_in[fn] = ok;
     return ok;

@@ -32,6 +32,7 @@ namespace tr {
 namespace {
 
 constexpr int kStreamChunk = 8;          // float4 per thread per streamed chunk (kStreamU)
+constexpr int kSplitStaticSmem = 1280;    // static shared memory of the split kernel (upper bound)
 constexpr int kSplitChunk = 4;           // float4 per thread per streamed chunk of a split plan (kSplitU)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -160,7 +161,11 @@ int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem) {
     const int regs_cta = warps * ((regs * 32 + 255) / 256 * 256);
     int occ = std::min(d.max_threads_per_sm / t, d.max_ctas_per_sm);
     occ = std::min(occ, d.regs_per_sm / std::max(1, regs_cta));
-    if (smem > 0) occ = std::min(occ, static_cast<int>(d.smem_per_sm / (smem + 1024)));
+    // (1 KB per CTA is reserved by the hardware; a split kernel's static shared
+    // memory comes on top of its segment cache)
+    if (smem > 0)
+        occ = std::min(occ, static_cast<int>(d.smem_per_sm /
+                                             (smem + 1024 + (p.kind == TR_PLAN_SPLIT ? kSplitStaticSmem : 0))));
     return occ;
 }
 
@@ -638,7 +643,7 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
                 for (int T : {256, 512, 1024}) {
                     const int64_t cover = ceil_div(ceil_div(n4, C), T);
                     const int kfull = kStagedSmemBudget / (16 * T);
-                    const int khalf = (d.smem_per_sm / 2 - 2048) / (16 * T);
+                    const int khalf = (d.smem_per_sm / 2 - 1024 - kSplitStaticSmem) / (16 * T);
                     int last = -1;
                     for (int kcap : {kfull, khalf}) {
                         const int k = static_cast<int>(std::min<int64_t>(cover, kcap));
