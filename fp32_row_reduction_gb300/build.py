@@ -27,7 +27,7 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}
 EXTRA = {"k_ordered.cu": ["-fmad=false", "-prec-div=true", "-prec-sqrt=true", "-ftz=false"]}
 SOURCES = ["tr_api.cu", "tr_plan.cpp", "k_softmax.cu", "k_rmsnorm.cu", "k_layernorm.cu", "k_xent.cu",
            "k_ordered.cu", "tr_noalloc.cu", "k_add_rmsnorm.cu", "k_add_layernorm.cu",
-           "k_reduce.cu", "k_axis.cu", "k_backward.cu", "k_fold.cu", "k_ot_cluster.cu"]
+           "k_reduce.cu", "k_axis.cu", "k_backward.cu", "k_fold.cu", "k_ot_cluster.cu", "k_xent_bwd.cu"]
 HEADERS = ["tr_device.cuh", "tr_row_kernels.cuh", "tr_split_kernels.cuh", "tr_dispatch.cuh", "tr_internal.h",
            "tr_plan.h", "tr_ot.cuh"]
 

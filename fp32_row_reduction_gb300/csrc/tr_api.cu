@@ -736,7 +736,20 @@ static tr_status bw_run(int op, BwArgs a, tr_order order, float* dw, float* db, 
         a.stat_b = a.stat_a + a.rows;
     }
     const bool ordered = order == TR_ORDER_ORDERED_TREE;
-    cudaError_t e = launch_backward(op, ordered, bw_slots(a.cols), a, static_cast<int>(bw_ctas(a.rows)), stream);
+    // unordered cross-entropy rows too long for registers: the 1024-thread streaming kernel
+    const bool xent_stream = op == BW_XENT && !ordered && bw_slots(a.cols) == 0;
+    if (xent_stream) {
+        int dev = 0;
+        cudaError_t de = cudaGetDevice(&dev);
+        if (de != cudaSuccess) return cuda_fail(de, "cudaGetDevice");
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* st = nullptr;
+        tr_status ss = device_state(dev, &st);
+        if (ss != TR_OK) return ss;
+        a.err = st->err;
+    }
+    cudaError_t e = xent_stream ? launch_xent_backward_stream(a, stream)
+                                : launch_backward(op, ordered, bw_slots(a.cols), a, static_cast<int>(bw_ctas(a.rows)), stream);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     if (dw && db) return term_sum(AXIS_LN_BOTH, a, dw, db, order, stream);  // one pass over x and dy
     if (dw) return term_sum(op == BW_RMSNORM ? AXIS_RMS_W : AXIS_LN_GAMMA, a, dw, nullptr, order, stream);
@@ -999,6 +1012,8 @@ tr_status tr_last_device_error(void) {
                 cudaSetDevice(cur);
                 if (e != cudaSuccess) return cuda_fail(e, "clearing a split workspace");
             }
+        if (word & kErrAccessCheck)
+            return fail(TR_ERR_CUDA, "a kernel's own access check found an out-of-range or misaligned access and skipped it");
         return fail(TR_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up");
     }
     return TR_OK;

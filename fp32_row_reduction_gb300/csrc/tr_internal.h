@@ -198,9 +198,17 @@ struct BwArgs {
     int64_t rows;
     int cols;
     float eps;
+    unsigned* err;           // device error word (kernels that check their own accesses record here)
 };
+
+// Device error word bit: a kernel's own access check skipped a bad access
+// (bit 1, kErrWaitTimeout, is a bounded wait that gave up).
+constexpr unsigned kErrAccessCheck = 2u;
 
 // Launch backward op `op` (BwOp) with K cached quads per thread (0: re-read) on G CTAs.
 cudaError_t launch_backward(int op, bool ordered, int slots, const BwArgs& a, int ctas, cudaStream_t stream);
+// Unordered cross-entropy backward of rows longer than the cached kernels take
+// (more than 8192 columns): a 1024-thread CTA per row, the row read twice.
+cudaError_t launch_xent_backward_stream(const BwArgs& a, cudaStream_t stream);
 
 }  // namespace tr

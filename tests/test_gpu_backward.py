@@ -260,3 +260,43 @@ def test_unaligned_tensors(offs):
         torch.cuda.synchronize()
         if order == "ordered":
             same_bits(DL.cpu().numpy(), oracle.ot_cross_entropy_backward(x, labels.numpy()), f"xent bwd offsets {offs}")
+
+
+@pytest.mark.parametrize("offs", [(0, 0), (1, 0), (0, 3), (2, 1)])
+@pytest.mark.parametrize("rows,cols", [(3, 8193), (4, 20001), (2, 100003)])
+def test_cross_entropy_backward_long_rows_unaligned(rows, cols, offs):
+    # rows longer than the cached kernels take run the streaming kernel (a
+    # 1024-thread CTA per row): row heads and tails of every phase, dlogits on
+    # the logits' 16-byte phase or off it, labels on the head, the tail, a
+    # quad's last lane and out of range; the guard floats stay untouched
+    x = synth.make_inputs("cross_entropy", rows, cols, seed=cols + 11 * offs[0] + offs[1], var=9.0)["x"].numpy()
+    labels = np.array([0, cols - 1, 7, -3][:rows], dtype=np.int64)
+    dl = synth.dloss_f32(rows, seed=cols).numpy()
+    L = offset_copy(x, offs[0])
+    big = torch.zeros(rows * cols + 8, device=DEV)
+    DL = big[offs[1]:offs[1] + rows * cols].view(rows, cols)
+    tr.cross_entropy_backward(L, torch.from_numpy(labels).to(DEV), dev(dl), out=DL, order="unordered")
+    torch.cuda.synchronize()
+    want = oracle.cross_entropy_backward(x, labels, dl)
+    p = oracle.softmax(x)
+    scale = dl.astype(np.float64)[:, None]
+    within(DL.cpu().numpy(), want, scale * (4e-6 * p + 2 * U * np.abs(want / scale)),
+           f"xent bwd {rows}x{cols} offsets {offs}")
+    assert float(big[:offs[1]].abs().sum()) == 0.0 and float(big[offs[1] + rows * cols:].abs().sum()) == 0.0
+
+
+def test_cross_entropy_backward_full_size_sampled_rows():
+    # the 4096 x 50257 workload through the streaming kernel; sampled rows
+    # against the oracle, and every row of dlogits sums to 0 (in-range labels)
+    rows, cols = 4096, 50257
+    d = synth.make_inputs("cross_entropy", rows, cols, seed=3, var=9.0)
+    dx = tr.cross_entropy_backward(d["x"].to(DEV), d["labels"].to(DEV), None, order="unordered")
+    torch.cuda.synchronize()
+    pick = [0, 1, 777, 2048, 4095]
+    x = d["x"].numpy()[pick]
+    labels = d["labels"].numpy()[pick]
+    want = oracle.cross_entropy_backward(x, labels, None)
+    p = oracle.softmax(x)
+    within(dx[pick].cpu().numpy(), want, 4e-6 * p + 2 * U * np.abs(want), "xent bwd 4096x50257 sampled")
+    sums = dx.double().sum(1).abs().max().item()
+    assert sums < 1e-4, sums
