@@ -33,7 +33,8 @@
  * on the host before anything is launched. TR_ERR_CUDA reports a CUDA launch
  * error (the message is in tr_last_error_message()). Kernels never trap: a
  * bounded device-side wait that gives up records TR_ERR_DEVICE_TIMEOUT in a
- * device error word, which tr_last_device_error() reads and clears.
+ * device error word, which tr_last_device_error() reads and clears (a kernel
+ * that checks its own accesses records a skipped access there too).
  */
 #ifndef TR_H
 #define TR_H
@@ -364,7 +365,10 @@ tr_status tr_plan_candidates(int32_t op, int64_t rows, int64_t cols, tr_order or
 tr_status tr_plan_override(const tr_plan* plan);
 
 /* Synchronises the current device, then reads and clears its device error
- * word: TR_OK, or TR_ERR_DEVICE_TIMEOUT if a bounded wait gave up. */
+ * word: TR_OK; TR_ERR_CUDA if a kernel that checks its own accesses (the
+ * unordered cross-entropy backward of rows over 8192 columns) found one out of
+ * range or misaligned and skipped it; else TR_ERR_DEVICE_TIMEOUT if a bounded
+ * wait gave up. */
 tr_status tr_last_device_error(void);
 
 /* Static text for a status. */
