@@ -133,25 +133,30 @@ __global__ void __launch_bounds__(kXbThreads, 2) xent_bwd_stream_kernel(const Bw
         const int64_t label = a.labels[row];
         const bool scaled = a.dloss != nullptr;
         const float dl = scaled ? a.dloss[row] : 1.0f;
-        auto grad = [&](float x, int64_t col) {
-            float d = ex2(fmaf(x, kL2E, -mb)) * inv;
-            if (col == label) d -= 1.0f;
+        // every element as if it were not the label's; the label's element (one per
+        // row, when in range) is written again after the barrier below
+        auto grad = [&](float x) {
+            const float d = ex2(fmaf(x, kL2E, -mb)) * inv;
             return scaled ? d * dl : d;
         };
-        auto grad4 = [&](float4 c, int64_t col) {
-            return make_float4(grad(c.x, col), grad(c.y, col + 1), grad(c.z, col + 2), grad(c.w, col + 3));
-        };
+        auto grad4 = [&](float4 c) { return make_float4(grad(c.x), grad(c.y), grad(c.z), grad(c.w)); };
         i = t;
         for (; i + (kXbU - 1) * T < g.nvec; i += kXbU * T) {
             float4 c[kXbU];
             for (int u = 0; u < kXbU; ++u) c[u] = io.ld4(xb + 4 * (i + u * T), drop);
-            for (int u = 0; u < kXbU; ++u) io.st(yb + 4 * (i + u * T), grad4(c[u], g.head + 4 * (i + u * T)), yv);
+            for (int u = 0; u < kXbU; ++u) io.st(yb + 4 * (i + u * T), grad4(c[u]), yv);
         }
-        for (; i < g.nvec; i += T) io.st(yb + 4 * i, grad4(io.ld4(xb + 4 * i, drop), g.head + 4 * i), yv);
-        if (t < g.head) io.st1(yr + t, grad(io.ld1(xr + t), t));
+        for (; i < g.nvec; i += T) io.st(yb + 4 * i, grad4(io.ld4(xb + 4 * i, drop)), yv);
+        if (t < g.head) io.st1(yr + t, grad(io.ld1(xr + t)));
         if (t < g.tail) {
             const int c = g.head + 4 * g.nvec + t;
-            io.st1(yr + c, grad(io.ld1(xr + c), c));
+            io.st1(yr + c, grad(io.ld1(xr + c)));
+        }
+        // the barrier orders the CTA's stores of this row before the label's rewrite
+        __syncthreads();
+        if (t == 0 && label >= 0 && label < cols) {
+            const float d = ex2(fmaf(io.ld1(xr + label), kL2E, -mb)) * inv - 1.0f;
+            io.st1(yr + label, scaled ? d * dl : d);
         }
     }
 }
