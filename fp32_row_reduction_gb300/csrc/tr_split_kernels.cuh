@@ -333,7 +333,36 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     };
     const float* pw = a.has_w ? a.w : nullptr;
     const float* pb = (OP == OP_LAYERNORM && a.has_b) ? a.b : nullptr;
-    i = v0 + nsm + t;
+    // the norms sweep their whole blocks of T slots starting at a per-row
+    // rotation, so that the CTAs of the rows sharing a segment read different
+    // weight lines at a time instead of all the same ones
+    const int ob = OP == OP_SOFTMAX ? 0 : (v1 - (v0 + nsm)) / T;  // whole blocks of the overflow
+    const int orot = ob > 0 ? static_cast<int>(row % ob) : 0;
+    auto oslot = [&](int b) { return v0 + nsm + ((b + orot) % ob) * T + t; };
+    if constexpr (OP != OP_SOFTMAX) {
+        int b = 0;
+        for (; b + kSplitU - 1 < ob; b += kSplitU) {
+            float4 c[kSplitU], w4[kSplitU], b4[kSplitU];
+#pragma unroll
+            for (int u = 0; u < kSplitU; ++u) {
+                const int k = oslot(b + u);
+                c[u] = ld_stream4(xb + 4 * k);
+                w4[u] = pload(pw, k, wv, 1.0f);
+                b4[u] = pload(pb, k, bv, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < kSplitU; ++u) {
+                float4 o = out4(c[u]);
+                o.x = fmaf(o.x, w4[u].x, b4[u].x);
+                o.y = fmaf(o.y, w4[u].y, b4[u].y);
+                o.z = fmaf(o.z, w4[u].z, b4[u].z);
+                o.w = fmaf(o.w, w4[u].w, b4[u].w);
+                st_out(yb + 4 * oslot(b + u), o, a.y_vec);
+            }
+        }
+        for (; b < ob; ++b) st_out(yb + 4 * oslot(b), params(out4(ld_stream4(xb + 4 * oslot(b))), oslot(b)), a.y_vec);
+    }
+    i = OP == OP_SOFTMAX ? v0 + nsm + t : v0 + nsm + ob * T + t;  // the norms: the part block
     for (; i + (kSplitU - 1) * T < v1; i += kSplitU * T) {
         float4 c[kSplitU];
         if constexpr (OP == OP_SOFTMAX) {
@@ -367,8 +396,31 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
             st_out(yb + 4 * (v0 + j), make_float4(c.x * cscale, c.y * cscale, c.z * cscale, c.w * cscale), a.y_vec);
         }
     } else {
-        // kSplitU slots at a time, so that their weight/bias loads are in flight together
-        int j = t;
+        // kSplitU slots at a time, so that their weight/bias loads are in flight
+        // together; whole blocks of T slots from the per-row rotation, as above
+        const int cb = nsm / T;
+        const int crot = cb > 0 ? static_cast<int>(row % cb) : 0;
+        auto cslot = [&](int bb) { return ((bb + crot) % cb) * T + t; };
+        int bb = 0;
+        for (; bb + kSplitU - 1 < cb; bb += kSplitU) {
+            float4 w4[kSplitU], b4[kSplitU];
+#pragma unroll
+            for (int u = 0; u < kSplitU; ++u) {
+                w4[u] = pload(pw, v0 + cslot(bb + u), wv, 1.0f);
+                b4[u] = pload(pb, v0 + cslot(bb + u), bv, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < kSplitU; ++u) {
+                float4 o = out4(cache[cslot(bb + u)]);
+                o.x = fmaf(o.x, w4[u].x, b4[u].x);
+                o.y = fmaf(o.y, w4[u].y, b4[u].y);
+                o.z = fmaf(o.z, w4[u].z, b4[u].z);
+                o.w = fmaf(o.w, w4[u].w, b4[u].w);
+                st_out(yb + 4 * (v0 + cslot(bb + u)), o, a.y_vec);
+            }
+        }
+        for (; bb < cb; ++bb) st_out(yb + 4 * (v0 + cslot(bb)), params(out4(cache[cslot(bb)]), v0 + cslot(bb)), a.y_vec);
+        int j = cb * T + t;  // the part block
         for (; j + (kSplitU - 1) * T < nsm; j += kSplitU * T) {
             float4 w4[kSplitU], b4[kSplitU];
 #pragma unroll
