@@ -11,9 +11,10 @@
 // reads the row from DRAM twice. Here a CTA of 1024 threads takes a row, two
 // CTAs per SM, so ~300 rows (60 MB) are in flight, and each thread keeps four
 // 16-byte loads in flight per pass, enough to cover DRAM latency. The first
-// pass loads with an L2 evict-last policy and the second with evict-first, so
-// the rows waiting for their second pass are the lines L2 keeps (without the
-// hints ncu counts 1.62 GB of DRAM reads for 0.82 GB of logits at 4096 x 50257).
+// pass loads with an L2 evict-last policy, the second pass and the dx stores
+// with evict-first, so the rows waiting for their second pass are the lines L2
+// keeps (without the hints ncu counts 1.62 GB of DRAM reads for 0.82 GB of
+// logits at 4096 x 50257).
 //
 // Every global access is checked against its buffer and, for 16-byte
 // accesses, its alignment before it is made; a failed check skips the access
@@ -60,8 +61,9 @@ struct XbIo {
         }
         return ld_stream1(p);
     }
-    // four consecutive outputs: one 16-byte store when p is on the 16-byte grid
-    __device__ __forceinline__ void st(float* p, float4 o, bool vec) const {
+    // four consecutive outputs: one 16-byte store (under the L2 policy `pol`)
+    // when p is on the 16-byte grid
+    __device__ __forceinline__ void st(float* p, float4 o, bool vec, uint64_t pol) const {
         if (p < y0 || p + 4 > y1) {
             bad();
             return;
@@ -71,7 +73,9 @@ struct XbIo {
                 bad();
                 return;
             }
-            st4(p, o);
+            asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(o.x), "f"(o.y),
+                         "f"(o.z), "f"(o.w), "l"(pol)
+                         : "memory");
         } else {
             p[0] = o.x;
             p[1] = o.y;
@@ -144,9 +148,9 @@ __global__ void __launch_bounds__(kXbThreads, 2) xent_bwd_stream_kernel(const Bw
         for (; i + (kXbU - 1) * T < g.nvec; i += kXbU * T) {
             float4 c[kXbU];
             for (int u = 0; u < kXbU; ++u) c[u] = io.ld4(xb + 4 * (i + u * T), drop);
-            for (int u = 0; u < kXbU; ++u) io.st(yb + 4 * (i + u * T), grad4(c[u]), yv);
+            for (int u = 0; u < kXbU; ++u) io.st(yb + 4 * (i + u * T), grad4(c[u]), yv, drop);
         }
-        for (; i < g.nvec; i += T) io.st(yb + 4 * i, grad4(io.ld4(xb + 4 * i, drop)), yv);
+        for (; i < g.nvec; i += T) io.st(yb + 4 * i, grad4(io.ld4(xb + 4 * i, drop)), yv, drop);
         if (t < g.head) io.st1(yr + t, grad(io.ld1(xr + t)));
         if (t < g.tail) {
             const int c = g.head + 4 * g.nvec + t;
