@@ -173,6 +173,27 @@ __device__ __forceinline__ float split_out(float x, float scale, float shift, fl
     }
 }
 
+// 16-byte load and store under an L2 eviction policy (createpolicy).
+__device__ __forceinline__ float4 ld_pol4(const float* p, uint64_t pol) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_out_pol(float* p, float4 o, bool vec, uint64_t pol) {
+    if (vec) {
+        asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(o.x), "f"(o.y),
+                     "f"(o.z), "f"(o.w), "l"(pol)
+                     : "memory");
+    } else {
+        p[0] = o.x;
+        p[1] = o.y;
+        p[2] = o.z;
+        p[3] = o.w;
+    }
+}
+
 template <int OP>
 __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     using Stat = SplitStat<OP>;
@@ -202,6 +223,11 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     }
     __syncthreads();
     pdl_enter();
+    // L2 policies: the streamed overflow is read again after the exchange (keep);
+    // the re-read and the outputs are on their last use (drop)
+    uint64_t keep, drop;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(drop));
     if (t == 0) {
         if (nsm > 0) {
             mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nsm) * 16u);
@@ -217,12 +243,12 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     for (; i + (kSplitU - 1) * T < v1; i += kSplitU * T) {
         float4 c[kSplitU];
 #pragma unroll
-        for (int u = 0; u < kSplitU; ++u) c[u] = ld_stream4(xb + 4 * (i + u * T));
+        for (int u = 0; u < kSplitU; ++u) c[u] = ld_pol4(xb + 4 * (i + u * T), keep);
         st = fold_chunk<OP, kSplitU>(st, c);
     }
     for (; i < v1; i += T) {
         float4 c[kSplitU];
-        c[0] = ld_stream4(xb + 4 * i);
+        c[0] = ld_pol4(xb + 4 * i, keep);
         st = fold_chunk<OP, 1>(st, c);
     }
     float hv = 0.0f, tv = 0.0f;
@@ -346,7 +372,7 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
 #pragma unroll
             for (int u = 0; u < kSplitU; ++u) {
                 const int k = oslot(b + u);
-                c[u] = ld_stream4(xb + 4 * k);
+                c[u] = ld_pol4(xb + 4 * k, drop);
                 w4[u] = pload(pw, k, wv, 1.0f);
                 b4[u] = pload(pb, k, bv, 0.0f);
             }
@@ -357,24 +383,24 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
                 o.y = fmaf(o.y, w4[u].y, b4[u].y);
                 o.z = fmaf(o.z, w4[u].z, b4[u].z);
                 o.w = fmaf(o.w, w4[u].w, b4[u].w);
-                st_out(yb + 4 * oslot(b + u), o, a.y_vec);
+                st_out_pol(yb + 4 * oslot(b + u), o, a.y_vec, drop);
             }
         }
-        for (; b < ob; ++b) st_out(yb + 4 * oslot(b), params(out4(ld_stream4(xb + 4 * oslot(b))), oslot(b)), a.y_vec);
+        for (; b < ob; ++b) st_out_pol(yb + 4 * oslot(b), params(out4(ld_pol4(xb + 4 * oslot(b), drop)), oslot(b)), a.y_vec, drop);
     }
     i = OP == OP_SOFTMAX ? v0 + nsm + t : v0 + nsm + ob * T + t;  // the norms: the part block
     for (; i + (kSplitU - 1) * T < v1; i += kSplitU * T) {
         float4 c[kSplitU];
         if constexpr (OP == OP_SOFTMAX) {
 #pragma unroll
-            for (int u = 0; u < kSplitU; ++u) c[u] = ld_stream4(xb + 4 * (i + u * T));
+            for (int u = 0; u < kSplitU; ++u) c[u] = ld_pol4(xb + 4 * (i + u * T), drop);
 #pragma unroll
-            for (int u = 0; u < kSplitU; ++u) st_out(yb + 4 * (i + u * T), out4(c[u]), a.y_vec);
+            for (int u = 0; u < kSplitU; ++u) st_out_pol(yb + 4 * (i + u * T), out4(c[u]), a.y_vec, drop);
         } else {
             float4 w4[kSplitU], b4[kSplitU];
 #pragma unroll
             for (int u = 0; u < kSplitU; ++u) {
-                c[u] = ld_stream4(xb + 4 * (i + u * T));
+                c[u] = ld_pol4(xb + 4 * (i + u * T), drop);
                 w4[u] = pload(pw, i + u * T, wv, 1.0f);
                 b4[u] = pload(pb, i + u * T, bv, 0.0f);
             }
@@ -385,15 +411,15 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
                 o.y = fmaf(o.y, w4[u].y, b4[u].y);
                 o.z = fmaf(o.z, w4[u].z, b4[u].z);
                 o.w = fmaf(o.w, w4[u].w, b4[u].w);
-                st_out(yb + 4 * (i + u * T), o, a.y_vec);
+                st_out_pol(yb + 4 * (i + u * T), o, a.y_vec, drop);
             }
         }
     }
-    for (; i < v1; i += T) st_out(yb + 4 * i, params(out4(ld_stream4(xb + 4 * i)), i), a.y_vec);
+    for (; i < v1; i += T) st_out_pol(yb + 4 * i, params(out4(ld_pol4(xb + 4 * i, drop)), i), a.y_vec, drop);
     if constexpr (OP == OP_SOFTMAX) {
         for (int j = t; j < nsm; j += T) {
             const float4 c = cache[j];
-            st_out(yb + 4 * (v0 + j), make_float4(c.x * cscale, c.y * cscale, c.z * cscale, c.w * cscale), a.y_vec);
+            st_out_pol(yb + 4 * (v0 + j), make_float4(c.x * cscale, c.y * cscale, c.z * cscale, c.w * cscale), a.y_vec, drop);
         }
     } else {
         // kSplitU slots at a time, so that their weight/bias loads are in flight
@@ -416,10 +442,10 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
                 o.y = fmaf(o.y, w4[u].y, b4[u].y);
                 o.z = fmaf(o.z, w4[u].z, b4[u].z);
                 o.w = fmaf(o.w, w4[u].w, b4[u].w);
-                st_out(yb + 4 * (v0 + cslot(bb + u)), o, a.y_vec);
+                st_out_pol(yb + 4 * (v0 + cslot(bb + u)), o, a.y_vec, drop);
             }
         }
-        for (; bb < cb; ++bb) st_out(yb + 4 * (v0 + cslot(bb)), params(out4(cache[cslot(bb)]), v0 + cslot(bb)), a.y_vec);
+        for (; bb < cb; ++bb) st_out_pol(yb + 4 * (v0 + cslot(bb)), params(out4(cache[cslot(bb)]), v0 + cslot(bb)), a.y_vec, drop);
         int j = cb * T + t;  // the part block
         for (; j + (kSplitU - 1) * T < nsm; j += kSplitU * T) {
             float4 w4[kSplitU], b4[kSplitU];
@@ -435,10 +461,10 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
                 o.y = fmaf(o.y, w4[u].y, b4[u].y);
                 o.z = fmaf(o.z, w4[u].z, b4[u].z);
                 o.w = fmaf(o.w, w4[u].w, b4[u].w);
-                st_out(yb + 4 * (v0 + j + u * T), o, a.y_vec);
+                st_out_pol(yb + 4 * (v0 + j + u * T), o, a.y_vec, drop);
             }
         }
-        for (; j < nsm; j += T) st_out(yb + 4 * (v0 + j), params(out4(cache[j]), v0 + j), a.y_vec);
+        for (; j < nsm; j += T) st_out_pol(yb + 4 * (v0 + j), params(out4(cache[j]), v0 + j), a.y_vec, drop);
     }
     auto params1 = [&](float o, int col) -> float {
         if constexpr (OP != OP_SOFTMAX) {
