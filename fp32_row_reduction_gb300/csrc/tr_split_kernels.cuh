@@ -181,6 +181,14 @@ __device__ __forceinline__ float4 ld_pol4(const float* p, uint64_t pol) {
                  : "l"(p), "l"(pol));
     return v;
 }
+// Bulk copy global -> shared under an L2 eviction policy.
+__device__ __forceinline__ void bulk_g2s_pol(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
 __device__ __forceinline__ void st_out_pol(float* p, float4 o, bool vec, uint64_t pol) {
     if (vec) {
         asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(o.x), "f"(o.y),
@@ -231,7 +239,7 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     if (t == 0) {
         if (nsm > 0) {
             mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nsm) * 16u);
-            bulk_g2s(cache, xb + 4 * v0, static_cast<uint32_t>(nsm) * 16u, &bar);
+            bulk_g2s_pol(cache, xb + 4 * v0, static_cast<uint32_t>(nsm) * 16u, &bar, drop);  // read once, into smem
         } else {
             mbar_arrive(&bar);
         }
