@@ -6,14 +6,20 @@ Default workload: softmax, RMSNorm and LayerNorm at 768 x 6144 (x ~ N(0,1),
 weight ~ U(0.5,1.5), bias ~ N(0,0.1), eps 1e-5, seed 2), each under the
 unordered and the ordered (OT-1024) policy: one step = these 6 launches, each
 on its own input and output buffers. Inputs are resident in HBM when timing
-starts; 2 rotating buffer sets (453 MB) keep every launch's data out of L2.
+starts; rotating buffer sets keep every launch's data out of L2.
 
-The timed region replays CUDA graphs of unrolled steps with nothing between
-the launches. A second timed region gives every kernel's duration: per kernel,
-a graph of back-to-back launches of that kernel alone, timed with CUDA events.
+Timed regions (CUDA events on the launching stream, one nvidia-smi clock
+record around all of them):
+  1. the headline `value`: CUDA graphs of exactly --steps unrolled steps;
+  2. every kernel of the step alone: a graph of 200 back-to-back launches,
+     replayed 9 times, the median replay (the roofline kernel is the slowest);
+  3. `per_op`: the same protocol for every configuration of the workload list
+     (cross-entropy 4096x50257, the long-row sweep, the small shapes);
+  4. synchronized single calls (GPU time between events, and host wall time
+     through the C-ABI including the synchronisation), median of 30.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--suite]
+                  [--workload NAME] [--suite] [--no-per-op]
 
 ``--impl reference`` times the CPU oracle (serial FP64 definitions and the
 OT-1024 emulation) on a bounded row sample of the same workload.
@@ -81,7 +87,23 @@ def alg_bytes(op, rows, cols):
 # a committed traffic record counts only while none of them has changed.
 STEP_SOURCES = ["k_softmax.cu", "k_rmsnorm.cu", "k_layernorm.cu", "k_ordered.cu", "tr_dispatch.cuh",
                 "tr_split_kernels.cuh", "tr_row_kernels.cuh", "tr_device.cuh", "tr_internal.h", "tr_api.cu", "tr_ot.cuh",
-                "tr_plan.cpp", "tr_plan.h"]
+                "tr_plan.cpp", "tr_plan.h", "tr_wave_kernels.cuh", "k_wave.cu", "k_wave_ordered.cu"]
+
+# The configurations whose kernels `per_op` reports beside the step's: every
+# workload of the benchmark's list (op, synthetic workload, policy).
+PER_OP_CONFIGS = [
+    ("softmax", "softmax_37x1537", "unordered"),
+    ("rmsnorm", "rmsnorm_256x3072", "unordered"), ("layernorm", "layernorm_256x3072", "unordered"),
+    ("rmsnorm", "rmsnorm_64x12289", "unordered"), ("layernorm", "layernorm_64x12289", "unordered"),
+    ("cross_entropy", "cross_entropy_4096x50257", "unordered"),
+    ("softmax", "softmax_16x65536", "unordered"), ("softmax", "softmax_16x262144", "unordered"),
+    ("softmax", "softmax_16x1048576", "unordered"), ("softmax", "softmax_65536x128", "unordered"),
+    ("layernorm", "layernorm_16x65536", "unordered"), ("layernorm", "layernorm_16x262144", "unordered"),
+    ("layernorm", "layernorm_16x1048576", "unordered"), ("layernorm", "layernorm_65536x128", "unordered"),
+]
+KERNEL_LAUNCHES = 200   # back-to-back launches per timed graph
+KERNEL_ROUNDS = 9       # replays of that graph; the median is reported
+SINGLE_CALLS = 30       # synchronized single calls per kernel
 
 
 def kernel_source_hash():
@@ -279,6 +301,65 @@ def job_gbs(world, steps, step_bytes, elapsed_ms):
     return world * steps * step_bytes / (elapsed_ms * 1e-3) / 1e9
 
 
+def workload_config(specs, sets=None):
+    """The `config` object of both arms: the workload and what a step launches."""
+    return {"workload": specs["name"], "launches_per_step": len(specs["launches"]),
+            "shapes": sorted({f"{synth.WORKLOADS[w]['rows']}x{synth.WORKLOADS[w]['cols']}"
+                              for _, w, _ in specs["launches"]}),
+            "policies": sorted({o for _, _, o in specs["launches"]}),
+            "l2": "inputs larger than L2: rotating buffer sets, every launch reads data not used since "
+                  "more than twice the L2 size was touched"}
+
+
+def timed_graph_us(ln, sets, n=KERNEL_LAUNCHES, rounds=KERNEL_ROUNDS):
+    """Median microseconds per launch of `rounds` replays of a graph of `n`
+    back-to-back launches of one kernel (its rotating buffer sets)."""
+    g = build_graph([ln], n, sets, 0, timing=False)[0]
+    g.replay()
+    torch.cuda.synchronize()
+    samples = []
+    for _ in range(rounds):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        g.replay()
+        t1.record()
+        t1.synchronize()
+        samples.append(1e3 * t0.elapsed_time(t1) / n)
+    del g
+    return statistics.median(samples), samples
+
+
+def single_call_us(ln, sets, reps=SINGLE_CALLS):
+    """Synchronized single calls: GPU time between events around one call, and
+    host wall time of the call through the C-ABI plus the synchronisation
+    (medians; the buffer sets rotate, so every call reads cold data)."""
+    gpu, host = [], []
+    for i in range(reps):
+        s = i % sets
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record()
+        ln(s)
+        e1.record()
+        e1.synchronize()
+        host.append(1e6 * (time.perf_counter() - t0))
+        gpu.append(1e3 * e0.elapsed_time(e1))
+    return statistics.median(gpu), statistics.median(host)
+
+
+def op_entry(ln, us, samples, peak, single=None):
+    e = {"us": round(us, 3), "gbs": round(ln.bytes / (us * 1e3), 1),
+         "frac_of_peak": round(ln.bytes / (us * 1e3) / peak, 4),
+         "frac_of_8tbs": round(ln.bytes / (us * 1e3) / 8000.0, 4),
+         "us_rounds": [round(v, 3) for v in samples], "alg_bytes": ln.bytes, "plan": ln.plan()}
+    if single is not None:
+        e["single_call_gpu_us"], e["single_call_e2e_us"] = round(single[0], 3), round(single[1], 3)
+    return e
+
+
 def run_ours(args, rank, world):
     import fp32_row_reduction_gb300 as tr
     tr.load()
@@ -332,19 +413,29 @@ def run_ours(args, rank, world):
         if g_rem is not None:
             g_rem.replay()
 
-    reps = max(1, K // U)
+    peak, peak_kind = measured_peak()
     with ClockSampler(dev.index) as clk:
         elapsed_ms = timed(main_steps)
-        # timed region 2 (per-kernel durations): for each launch of the step, a
-        # graph of U back-to-back launches of that kernel alone (same buffers
-        # rotation), replayed as often as region 1 replays its steps
-        per_us = []
-        for ln in launches:
-            g1 = build_graph([ln], U, sets, 0, timing=False)[0]
-            g1.replay()
-            torch.cuda.synchronize()
-            per_us.append(1e3 * timed(lambda: [g1.replay() for _ in range(reps)]) / (reps * U))
-            del g1
+        del g_main, g_rem
+        # timed region 2: each kernel of the step alone (median of 9 graphs of 200)
+        per = [timed_graph_us(ln, sets) for ln in launches]
+        per_us = [p[0] for p in per]
+        # timed region 4 for the step's kernels: synchronized single calls
+        singles = [single_call_us(ln, sets) for ln in launches]
+        per_op = {ln.key: op_entry(ln, per[k][0], per[k][1], peak, singles[k]) for k, ln in enumerate(launches)}
+        # timed region 3: every other configuration of the list, one at a time
+        if rank == 0 and not args.no_per_op and args.workload == DEFAULT_WORKLOAD:
+            for op, w, o in PER_OP_CONFIGS:
+                b = alg_bytes(op, synth.WORKLOADS[w]["rows"], synth.WORKLOADS[w]["cols"])
+                xs = pick_sets([b])
+                ln = Launch(op, w, o, xs, dev)
+                for i in range(3):
+                    ln(i % xs)
+                torch.cuda.synchronize()
+                us, samples = timed_graph_us(ln, xs)
+                per_op[ln.key] = op_entry(ln, us, samples, peak, single_call_us(ln, xs, reps=10))
+                del ln
+                torch.cuda.empty_cache()
 
     if world > 1:
         elapsed_ms = max_over_ranks(elapsed_ms, dev)
@@ -354,39 +445,35 @@ def run_ours(args, rank, world):
     if rank != 0:
         return None
 
-    peak, peak_kind = measured_peak()
     dom = max(range(len(launches)), key=lambda k: per_us[k])
     dl = launches[dom]
     achieved = dl.bytes / (per_us[dom] * 1e-6) / 1e9
-    per_op = {}
-    for k, ln in enumerate(launches):
-        per_op[ln.key] = {"us": round(per_us[k], 3), "gbs": round(ln.bytes / (per_us[k] * 1e3), 1),
-                          "frac_of_peak": round(ln.bytes / (per_us[k] * 1e3) / peak, 4),
-                          "alg_bytes": ln.bytes, "plan": ln.plan()}
     value = job_gbs(world, K, step_bytes, elapsed_ms)
+    config = workload_config({"name": args.workload, "launches": specs})
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "launches_per_step": len(launches),
-                   "shapes": sorted({f"{ln.rows}x{ln.cols}" for ln in launches}),
-                   "policies": sorted({ln.order for ln in launches}),
-                   "l2": f"inputs larger than L2: {sets} rotating buffer sets of "
-                         f"{sum(ln.bytes for ln in launches) / 1e6:.0f} MB per step "
-                         f"(each kernel alone also cycles through > 2x L2)",
-                   "timing": "CUDA graph of unrolled steps, CUDA events on the launching stream",
+        "config": config,
+        "timing": {"value": "CUDA graphs of exactly `steps` unrolled steps, CUDA events on the launching stream",
+                   "per_kernel": f"per kernel, a CUDA graph of {KERNEL_LAUNCHES} back-to-back launches on its "
+                                 f"rotating buffer sets, replayed {KERNEL_ROUNDS} times; median replay "
+                                 f"(us_rounds lists all)",
+                   "single_call": "median of synchronized single calls: GPU time between events around the call, "
+                                  "and host wall time of the call through the C-ABI plus the synchronisation",
+                   "buffer_sets": sets,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dl.key, "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_of_8tbs": round(achieved / 8000.0, 4),
                      "traffic": traffic_record(dl.key), "alg_bytes_per_launch": dl.bytes,
                      "launch_us": round(per_us[dom], 3)},
         "per_op": per_op,
         "e2e": e2e,
         "gpu_launches": K * len(launches),
-        "per_kernel_timing": {"launches_per_kernel": reps * U, "sum_of_kernels_ms_per_step": round(sum(per_us) / 1e3, 6),
-                              "how": "second timed region: per kernel, a CUDA graph of back-to-back launches of that "
-                                     "kernel alone on the step's rotating buffers, CUDA events on the launching stream"},
+        "per_kernel_timing": {"launches_per_kernel": KERNEL_LAUNCHES * KERNEL_ROUNDS,
+                              "sum_of_kernels_ms_per_step": round(sum(per_us) / 1e3, 6)},
         "clocks": clk.summary(),
     }
     if cpu is not None:
@@ -506,65 +593,128 @@ def sample_shape(h):
     return (h["x"] if "x" in h else h["y"]).shape
 
 
-def time_oracle(specs, rows_per_launch, budget_s=None, repeats=1):
-    """Run the oracle over `rows_per_launch` rows of every launch of the step."""
+ROW_KEYS = ("x", "y", "dy", "labels", "dloss", "r")  # per-row inputs; the rest are column vectors
+
+
+def cpu_info():
+    """Host core count and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    import platform
+    return {"cpu_count": os.cpu_count() or 1, "cpu_model": model or platform.machine()}
+
+
+def row_chunks(h, n):
+    """Split a host sample into n contiguous row ranges (column vectors shared)."""
+    rows = sample_shape(h)[0]
+    bounds = [rows * i // n for i in range(n + 1)]
+    return [{k: (v[a:b] if k in ROW_KEYS else v) for k, v in h.items()}
+            for a, b in zip(bounds, bounds[1:]) if b > a]
+
+
+def time_oracle(specs, rows_per_launch, budget_s=None, repeats=1, threads=1):
+    """Run the oracle over `rows_per_launch` rows of every launch of the step,
+    row-parallel on `threads` host threads (the C oracle runs with the
+    interpreter lock released, one contiguous row range per thread)."""
     samples = [(oracle_fn(op, o), host_sample(op, w, rows_per_launch), op, w) for op, w, o in specs]
+    pool = None
+    if threads > 1:
+        import concurrent.futures as cf
+        pool = cf.ThreadPoolExecutor(max_workers=threads)
+        samples = [(fn, h, op, w, row_chunks(h, threads)) for fn, h, op, w in samples]
     done_bytes, t_total, reps = 0, 0.0, 0
-    while True:
-        t0 = time.perf_counter()
-        for fn, h, op, _ in samples:
-            fn(h)
-        t_total += time.perf_counter() - t0
-        reps += 1
-        done_bytes += sum(alg_bytes(op, *sample_shape(h)) for _, h, op, _ in samples)
-        if budget_s is None and reps >= repeats:
-            break
-        if budget_s is not None and t_total >= budget_s:
-            break
+    try:
+        while True:
+            t0 = time.perf_counter()
+            for smp in samples:
+                if pool is None:
+                    smp[0](smp[1])
+                else:
+                    list(pool.map(smp[0], smp[4]))
+            t_total += time.perf_counter() - t0
+            reps += 1
+            done_bytes += sum(alg_bytes(smp[2], *sample_shape(smp[1])) for smp in samples)
+            if budget_s is None and reps >= repeats:
+                break
+            if budget_s is not None and t_total >= budget_s:
+                break
+    finally:
+        if pool is not None:
+            pool.shutdown()
     return done_bytes, t_total, reps
 
 
 def cpu_baseline(launches, args):
     specs = [(ln.op, ln.workload, ln.order) for ln in launches]
     rows = min(ln.rows for ln in launches)
-    sample_rows = min(rows, args.cpu_rows)
-    b, t, reps = time_oracle(specs, sample_rows, budget_s=args.cpu_seconds)
-    return {"value": round(b / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{sample_rows} rows of each of the {len(specs)} launches' inputs, {reps} passes, "
-                      f"{t:.1f} s (serial FP64 C oracle / OT-1024 C emulation, one thread)"}
+    info = cpu_info()
+    cores = info["cpu_count"]
+    serial_rows = min(rows, args.cpu_rows)
+    b1, t1, r1 = time_oracle(specs, serial_rows, budget_s=args.cpu_seconds / 2)
+    par_rows = rows
+    bp, tp, rp = time_oracle(specs, par_rows, budget_s=args.cpu_seconds / 2, threads=cores)
+    return {"value": round(bp / tp / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu_model": info["cpu_model"],
+            "sample": f"{par_rows} rows of each of the {len(specs)} launches' inputs, row-parallel on {cores} "
+                      f"threads, {rp} passes, {tp:.1f} s (serial FP64 C oracle / OT-1024 C emulation per row range)",
+            "serial": {"value": round(b1 / t1 / 1e9, 4), "cores": 1,
+                       "sample": f"{serial_rows} rows of each launch's inputs, {r1} passes, {t1:.1f} s, one thread"}}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
     specs = WORKLOADS[args.workload]
+    info = cpu_info()
+    cores = info["cpu_count"]
     # size each step so the whole --warmup + --steps run stays within ~2 minutes
     b1, t1, _ = time_oracle(specs, 1, repeats=1)
-    per_row = max(t1, 1e-5)
+    per_row = max(t1, 1e-5) / max(1, min(cores, 8))
     rows = int(max(1, min(768, 120.0 / (args.steps + args.warmup) / per_row)))
     samples = [(oracle_fn(op, o), host_sample(op, w, rows), op) for op, w, o in specs]
+    import concurrent.futures as cf
+    chunks = [(fn, row_chunks(h, cores)) for fn, h, _ in samples]
     step_bytes = sum(alg_bytes(op, *sample_shape(h)) for _, h, op in samples)
-    for _ in range(args.warmup):
-        for fn, h, _ in samples:
-            fn(h)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        for fn, h, _ in samples:
-            fn(h)
-    dt = time.perf_counter() - t0
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        def step():
+            for fn, ch in chunks:
+                list(pool.map(fn, ch))
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step()
+        dt = time.perf_counter() - t0
     value = args.steps * step_bytes / dt / 1e9
-    sample = f"{rows} rows of each of the {len(specs)} launches' inputs per step (serial C oracle, one thread)"
+    sample = (f"{rows} rows of each of the {len(specs)} launches' inputs per step, row-parallel on {cores} threads "
+              f"(serial C oracle per row range)")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload, "sample_rows": rows},
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "data": "synthetic", "config": workload_config({"name": args.workload, "launches": specs}),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "cpu_model": info["cpu_model"], "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def run_suite(args):
-    """One line per workload: µs/op, GB/s and plan (no graph; events around batched launches)."""
+    """One line per workload: µs/op (median of 9 graphs of 200 back-to-back
+    launches), GB/s, single-call latency and plan."""
     import fp32_row_reduction_gb300 as tr
     tr.load()
     dev = torch.device("cuda", 0)
@@ -580,21 +730,13 @@ def run_suite(args):
         for i in range(args.warmup):
             ln(i % sets)
         torch.cuda.synchronize()
-        n = max(20, min(2000, int(2e9 / max(b, 1))))
-        g, _ = build_graph([ln], n, sets, 0, timing=False)
-        g.replay()
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record()
-        g.replay()
-        t1.record()
-        t1.synchronize()
-        us = 1e3 * t0.elapsed_time(t1) / n
-        print(json.dumps({"workload": name, "op": op, "order": order, "rows": ln.rows, "cols": ln.cols,
-                          "us_per_op": round(us, 3), "gbs": round(b / (us * 1e3), 1),
-                          "frac_of_peak": round(b / (us * 1e3) / peak, 4), "alg_bytes": b, "launches": n,
-                          "l2": f"{sets} rotating buffer sets", "plan": ln.plan()}), flush=True)
-        del ln, g
+        us, samples = timed_graph_us(ln, sets)
+        e = op_entry(ln, us, samples, peak, single_call_us(ln, sets, reps=10))
+        print(json.dumps(dict(workload=name, op=op, order=order, rows=ln.rows, cols=ln.cols, us_per_op=e["us"],
+                              gbs=e["gbs"], frac_of_peak=e["frac_of_peak"], frac_of_8tbs=e["frac_of_8tbs"],
+                              single_call_gpu_us=e["single_call_gpu_us"], single_call_e2e_us=e["single_call_e2e_us"],
+                              alg_bytes=b, l2=f"{sets} rotating buffer sets", plan=e["plan"])), flush=True)
+        del ln
         torch.cuda.empty_cache()
 
 
@@ -607,10 +749,11 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--unroll", type=int, default=100, help="steps per captured graph")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-rows", type=int, default=96)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--suite", action="store_true", help="one line per workload, then exit")
+    ap.add_argument("--no-per-op", action="store_true", help="report only the step's kernels in per_op")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -47,6 +47,7 @@ TR_PLAN_STAGED = 5
 TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_SPLIT = 7
 TR_PLAN_FOLD = 8
+TR_PLAN_WAVE = 9
 TR_OP_ADD_RMSNORM = 4
 TR_OP_ADD_LAYERNORM = 5
 TR_OP_ROW_SUM = 6
@@ -269,8 +270,10 @@ def tr_last_device_error() -> int:
     return load().tr_last_device_error()
 
 
-def tr_debug_force_wait_timeout(enable: bool) -> int:
-    return load().tr_debug_force_wait_timeout(1 if enable else 0)
+def tr_debug_force_wait_timeout(mode) -> int:
+    """Testing hook (tr.h): True / 1 adds a wait nothing completes; 2 expires the
+    bulk-copy waits; 4 expires the split plan's waits for peer CTAs; 0 / False off."""
+    return load().tr_debug_force_wait_timeout(int(mode))
 
 
 def tr_status_string(status: int) -> str:

@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kOrderedThreads) ot_staged_kernel(const RowArg
         const RowGeom g = row_geom(xr, cols);
         const StagedWindow w = staged_window(xr, g, x0, x1);
         const float* slot = ring + static_cast<int64_t>(b) * a.slot_floats;
-        if (!mbar_wait_bounded(&full[b], parity, a.wait_ns, a.err)) s_abort = 1;
+        if (!mbar_wait_bounded(&full[b], parity, a.wait_ns, a.err, a.debug_flags & kDebugExpireCopies)) s_abort = 1;
         // column c sits at slot[pre + c]; pre = 0 exactly when the row is aligned
         const int pre = w.off - g.head;
         const int body_end = g.head + 4 * g.nvec;

@@ -216,11 +216,20 @@ struct Call {
     int order;
 };
 
-tr_status validate_common(int64_t rows, int64_t cols, int order) {
+// The operators (softmax, the norms, cross-entropy, their fused and backward
+// forms) take rows of fewer than 2^24 columns, so that (float)cols, by which
+// the norms divide, is exact; the standalone row reductions divide by nothing
+// and take rows of up to 2^31 - 1 columns.
+constexpr int64_t kMaxOperatorCols = (1LL << 24) - 1;
+constexpr int64_t kMaxReductionCols = 0x7fffffffLL;
+
+tr_status validate_common(int64_t rows, int64_t cols, int order, int64_t max_cols = kMaxOperatorCols) {
     if (order != TR_ORDER_UNORDERED_TREE && order != TR_ORDER_ORDERED_TREE && !fold_order(order))
         return fail(TR_ERR_INVALID_ARG, "order must be one of the tr_order values");
     if (rows < 0) return fail(TR_ERR_INVALID_ARG, "rows must be >= 0");
-    if (cols < 1 || cols > 0x7fffffffLL) return fail(TR_ERR_INVALID_ARG, "cols must be in [1, 2^31 - 1]");
+    if (cols < 1 || cols > max_cols)
+        return fail(TR_ERR_INVALID_ARG, max_cols == kMaxOperatorCols ? "cols must be in [1, 2^24 - 1]"
+                                                                      : "cols must be in [1, 2^31 - 1]");
     if (rows > 0 && rows > INT64_MAX / cols / 4) return fail(TR_ERR_INVALID_ARG, "rows * cols too large");
     return TR_OK;
 }
@@ -364,6 +373,11 @@ void set_last_error(const char* what, const char* detail) { t_last_error = std::
 
 cudaError_t device_error_symbol(void** out) { return cudaGetSymbolAddress(out, g_device_error); }
 
+int debug_flags_now() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return g_debug_flags;
+}
+
 }  // namespace tr
 
 using namespace tr;
@@ -485,7 +499,7 @@ static tr_status residual_call(int op, const float* x, const float* residual, co
 // Standalone row reductions: out[r] (and out2[r]) per row.
 static tr_status reduce_call(int op, const float* x, float* out, float* out2, int64_t rows, int64_t cols,
                              tr_order order, cudaStream_t stream) {
-    tr_status s = validate_common(rows, cols, order);
+    tr_status s = validate_common(rows, cols, order, kMaxReductionCols);
     if (s != TR_OK) return s;
     if (rows == 0) return TR_OK;
     if (!x || !out || (op == TR_OP_ROW_MINMAX && !out2))
@@ -978,16 +992,17 @@ tr_status tr_plan_override(const tr_plan* plan) {
         return TR_OK;
     }
     if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "bad op");
-    if (plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_SPLIT)
+    if ((plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_SPLIT) && plan->kind != TR_PLAN_WAVE)
         return fail(TR_ERR_INVALID_ARG, "bad plan kind");
     g_override[plan->op] = *plan;
     g_override_set[plan->op] = true;
     return TR_OK;
 }
 
-tr_status tr_debug_force_wait_timeout(int32_t enable) {
+tr_status tr_debug_force_wait_timeout(int32_t mode) {
+    if (mode & ~kDebugModes) return fail(TR_ERR_INVALID_ARG, "mode is a mask of 1, 2 and 4");
     std::lock_guard<std::mutex> lock(g_mu);
-    g_debug_flags = enable ? (g_debug_flags | kDebugForceTimeout) : (g_debug_flags & ~kDebugForceTimeout);
+    g_debug_flags = mode;
     return TR_OK;
 }
 
@@ -1001,17 +1016,10 @@ tr_status tr_last_device_error(void) {
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
-        // a wait that gave up may leave a split row's counters short of zero
-        std::lock_guard<std::mutex> lock(g_mu);
-        for (auto& dv : g_devices)
-            for (auto& w : dv.second.split_ws) {
-                int cur = 0;
-                cudaGetDevice(&cur);
-                cudaSetDevice(dv.first);
-                e = cudaMemset(w.second, 0, kSplitWorkspaceBytes);
-                cudaSetDevice(cur);
-                if (e != cudaSuccess) return cuda_fail(e, "clearing a split workspace");
-            }
+        // Nothing else needs resetting: every CTA of a split launch arrives and
+        // departs exactly once, also when a wait gave up, and the last to depart
+        // zeroes its row's counters, so workspaces and the no-allocation scratch
+        // are left ready for the next launch.
         if (word & kErrAccessCheck)
             return fail(TR_ERR_CUDA, "a kernel's own access check found an out-of-range or misaligned access and skipped it");
         return fail(TR_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up");

@@ -67,12 +67,12 @@ __device__ __forceinline__ float ex2(float t) {
 
 // Programmatic dependent launch. Every kernel waits for the grids it depends
 // on (their memory operations complete and visible) before its first global
-// read or write, then lets the next launch on the stream start its own
-// prologue; without a programmatic predecessor the wait returns at once.
-__device__ __forceinline__ void pdl_enter() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+// read or write; without a programmatic predecessor the wait returns at once.
+// No kernel signals its dependents early: the next launch on the stream is
+// released as this grid's CTAs exit. An early signal lets the next grid's CTAs
+// take free slots and sit in their own wait while this grid still streams,
+// and in back-to-back launches at 768 x 6144 that cost about 1 us a launch.
+__device__ __forceinline__ void pdl_enter() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // m * log2(e) rounded on its own. __fmul_rn is never fused into a following
 // add, so mb_of(a) - mb_of(b) is exactly 0 when a == b; a plain a*L2E - mb
@@ -100,6 +100,8 @@ __device__ __forceinline__ float4 ld_param4(const float* p) {
 
 // Bring the line holding p into L1 (no register, no wait).
 __device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+// Bring the line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ bool aligned16(const void* p) {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -293,9 +295,16 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 // Wait for phase `parity` of `bar` for at most `limit_ns` nanoseconds. On
 // timeout the error word gets kErrWaitTimeout and false is returned; the
-// caller then finishes without trapping.
+// caller then finishes without trapping. `expire` (a testing mode) makes the
+// wait give up at once without looking, as if its limit had passed, so that
+// the caller's give-up path runs; waits that drain copies before a CTA exits
+// never pass it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit_ns,
-                                                  unsigned* err) {
+                                                  unsigned* err, bool expire = false) {
+    if (expire) {
+        if (err) atomicOr(err, kErrWaitTimeout);
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {

@@ -42,7 +42,13 @@ struct RowArgs {
     float* out2;           // row min/max: the maxima (loss receives the minima)
 };
 
-constexpr int kDebugForceTimeout = 1;
+// Testing modes (tr_debug_force_wait_timeout), a bit mask in RowArgs::debug_flags:
+constexpr int kDebugForceTimeout = 1;  // one extra wait on a barrier nothing completes (1 ms limit)
+constexpr int kDebugExpireCopies = 2;  // waits for bulk copies (split segment, staged rings) give up at once
+constexpr int kDebugExpirePeers = 4;   // a split CTA's wait for the other CTAs of its row gives up at once
+constexpr int kDebugModes = kDebugForceTimeout | kDebugExpireCopies | kDebugExpirePeers;
+// The testing modes in force now (for launches that build their own arguments).
+int debug_flags_now();
 constexpr int kMaxRing = 8;                // staged plans: most rows in flight per CTA
 constexpr int kStagedSmemBudget = 225 * 1024;  // dynamic shared memory per CTA (bytes; 2 KB left for static)
 
@@ -135,6 +141,12 @@ const void* kernel_ordered_cluster(int op);
 constexpr int kOtClusterCtas = 8;
 constexpr size_t kOtClusterSmemMax = 200 * 1024;  // a group's share of the row staged in shared memory
 inline size_t ot_cluster_smem(int64_t cols) { return static_cast<size_t>((cols + 1023) / 1024) * 32 * 16; }
+// Wave kernels (TR_PLAN_WAVE): softmax, RMSNorm, LayerNorm; vec_slots 2, 4, 6, 8;
+// rows_per_cta 1 or 2.
+const void* kernel_wave_unordered(int op, int slots, int rows_per_cta);
+const void* kernel_wave_ordered(int op, int slots, int rows_per_cta);
+constexpr int kWaveSlots[] = {2, 4, 6, 8};
+constexpr int kWaveThreads = 256;
 // Dynamic shared memory a plan's kernel needs (0 for all but staged plans).
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols);
 
@@ -147,6 +159,11 @@ inline const void* kernel_for(const tr_plan& p) {
     if (p.op >= TR_OP_ROW_SUM && p.op <= TR_OP_ROW_MINMAX) {
         if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
         return kernel_reduce(p.op, p.kind, p.lanes_per_row, p.vec_slots, p.flags);
+    }
+    if (p.kind == TR_PLAN_WAVE) {
+        if (p.flags) return nullptr;
+        return p.order == TR_ORDER_ORDERED_TREE ? kernel_wave_ordered(p.op, p.vec_slots, p.rows_per_cta)
+                                                : kernel_wave_unordered(p.op, p.vec_slots, p.rows_per_cta);
     }
     if (p.kind == TR_PLAN_ORDERED && p.cluster_ctas == kOtClusterCtas)
         return p.flags ? nullptr : kernel_ordered_cluster(p.op);

@@ -63,8 +63,11 @@ const void* split_fn(int op) {
     return nullptr;
 }
 
+// Report a CUDA error and clear it from the runtime's sticky last-error slot,
+// so that a failed set-up does not surface in the caller's next CUDA call.
 tr_status cuda_err(cudaError_t e, const char* what) {
     set_last_error(what, cudaGetErrorString(e));
+    cudaGetLastError();
     return TR_ERR_CUDA;
 }
 
@@ -87,9 +90,22 @@ tr_status setup(int dev, NoAllocDevice** out) {
         e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_err(e, "cudaDeviceGetAttribute");
         const size_t smem = static_cast<size_t>(kNoAllocMaxSlots) * kNoAllocThreads * 16;
+        int optin = 0;
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return cuda_err(e, "cudaDeviceGetAttribute");
         for (int op = 0; op < 3; ++op) {
             const void* fn = split_fn(op);
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmemBudget);
+            // the dynamic limit is what the per-CTA opt-in maximum leaves beside
+            // the kernel's static shared memory (as for the other entry points)
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, fn);
+            if (e != cudaSuccess) return cuda_err(e, "cudaFuncGetAttributes");
+            const int budget = std::min<int>(kStagedSmemBudget, optin - static_cast<int>(fa.sharedSizeBytes));
+            if (budget < static_cast<int>(smem)) {
+                set_last_error("no-alloc entry point", "the segment cache does not fit this device's shared memory");
+                return TR_ERR_UNSUPPORTED;
+            }
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
             if (e != cudaSuccess) return cuda_err(e, "cudaFuncSetAttribute(shared memory)");
             int n = 0;
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kNoAllocThreads, smem);
@@ -121,8 +137,8 @@ extern "C" tr_status tr_split_rows_noalloc_f32(int32_t op, const float* x, const
         set_last_error("no-alloc entry point", "op must be TR_OP_SOFTMAX, TR_OP_RMSNORM or TR_OP_LAYERNORM");
         return TR_ERR_INVALID_ARG;
     }
-    if (rows < 0 || cols < 1 || cols > 0x7fffffffLL || (rows > 0 && rows > INT64_MAX / cols / 4)) {
-        set_last_error("no-alloc entry point", "rows must be >= 0 and cols in [1, 2^31 - 1]");
+    if (rows < 0 || cols < 1 || cols >= (1LL << 24) || (rows > 0 && rows > INT64_MAX / cols / 4)) {
+        set_last_error("no-alloc entry point", "rows must be >= 0 and cols in [1, 2^24 - 1]");
         return TR_ERR_INVALID_ARG;
     }
     if (op != TR_OP_SOFTMAX && (!std::isfinite(eps) || eps < 0.0f)) {
@@ -191,6 +207,7 @@ extern "C" tr_status tr_split_rows_noalloc_f32(int32_t op, const float* x, const
     a.has_b = b != nullptr;
     a.err = d->err;
     a.wait_ns = 2000000000LL;
+    a.debug_flags = debug_flags_now();
     a.slot_floats = 4 * K * kNoAllocThreads;
     a.sp_part = reinterpret_cast<float4*>(d->scratch);
     a.sp_arrive = reinterpret_cast<unsigned*>(d->scratch + kNoAllocMaxParts * 16);

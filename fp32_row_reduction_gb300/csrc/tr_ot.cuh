@@ -50,8 +50,8 @@ static __device__ __noinline__ float exp_ot_wide(float x) {
 //  - p lies in [2^-0.5, 2^0.5], so p * 2^k is normal: adding k to p's exponent
 //    field is exact and equals the two-step product.
 // Other x (|x| >= 86, infinities, NaN) take the clamped form.
-__device__ __forceinline__ float exp_ot(float x) {
-    if (!(fabsf(x) < 86.0f)) return x != x ? __fadd_rn(x, x) : exp_ot_wide(x);
+__device__ __forceinline__ bool exp_ot_in_fast_range(float x) { return fabsf(x) < 86.0f; }
+__device__ __forceinline__ float exp_ot_fast(float x) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
     const float u = __fadd_rn(__fmul_rn(x, 0x1.715476p+0f), kMagic);
     const float kf = __fsub_rn(u, kMagic);
@@ -67,6 +67,10 @@ __device__ __forceinline__ float exp_ot(float x) {
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
     return __int_as_float(__float_as_int(p) + static_cast<int>(static_cast<unsigned>(k) << 23));
+}
+__device__ __forceinline__ float exp_ot(float x) {
+    if (!exp_ot_in_fast_range(x)) return x != x ? __fadd_rn(x, x) : exp_ot_wide(x);
+    return exp_ot_fast(x);
 }
 
 // log on binary32: x = 2^e m, m in (sqrt(1/2), sqrt(2)], f = m - 1,

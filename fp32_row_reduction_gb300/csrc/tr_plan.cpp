@@ -54,7 +54,7 @@ int smallest_covering(const int (&arr)[N], int64_t need) {  // smallest K with K
 }
 
 int max_threads_for_slots(int op, int kind, int k, int flags) {
-    if (kind == TR_PLAN_ORDERED_STAGED) return kOrderedThreads;
+    if (kind == TR_PLAN_ORDERED_STAGED || kind == TR_PLAN_WAVE) return kOrderedThreads;
     if (kind == TR_PLAN_STAGED && (flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS))
         return k <= 2 ? 1024 : k == 4 ? 768 : (op == TR_OP_LAYERNORM ? 384 : 512);
     if (kind == TR_PLAN_STAGED) return (k >= 8 || (k >= 4 && op == TR_OP_LAYERNORM)) ? 768 : 1024;
@@ -149,6 +149,7 @@ int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem) {
             regs = (p.kind == TR_PLAN_ROWS && k == 6) ? 40 : 28 + 4 * k + (base_op(p.op) == TR_OP_LAYERNORM ? 4 : 0);
             break;
         case TR_PLAN_ORDERED_STAGED: regs = 40 + 4 * k; break;
+        case TR_PLAN_WAVE: regs = p.rows_per_cta == 1 ? std::max(32, 16 + 4 * k) : 30 + 8 * k; break;
         case TR_PLAN_STREAM: regs = 64; break;
         case TR_PLAN_SPLIT: regs = 64; break;
         case TR_PLAN_XENT: regs = 24 + 4 * k; break;
@@ -200,8 +201,14 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
             return fail(TR_ERR_UNSUPPORTED, "fused residual stripes exceed 64 scalars per worker (K > 8)");
     }
     const bool ot_kind = p->kind == TR_PLAN_ORDERED || p->kind == TR_PLAN_ORDERED_STAGED;
-    if (ordered != ot_kind)
-        return fail(TR_ERR_UNSUPPORTED, "the ordered policy is realised only by the OT-1024 plans");
+    if (p->kind == TR_PLAN_WAVE) {
+        // the aligned-row realisation of the 8-warp row plan, in both tree policies
+        if (p->op != TR_OP_SOFTMAX && p->op != TR_OP_RMSNORM && p->op != TR_OP_LAYERNORM)
+            return fail(TR_ERR_UNSUPPORTED, "wave plans serve softmax, RMSNorm and LayerNorm");
+        if (!align16) return fail(TR_ERR_UNSUPPORTED, "wave plans need 16-byte-aligned rows and weights (cols % 4 == 0)");
+    } else if (ordered != ot_kind) {
+        return fail(TR_ERR_UNSUPPORTED, "the ordered policy is realised only by the OT-1024 and wave plans");
+    }
     if (ordered && p->kind == TR_PLAN_SPLIT) return fail(TR_ERR_UNSUPPORTED, "split plans are unordered");
     if (!ordered && xent != (p->kind == TR_PLAN_XENT))
         return fail(TR_ERR_UNSUPPORTED, "cross-entropy and the row reductions are realised only by the streaming XENT plan");
@@ -233,6 +240,20 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     const int k = p->vec_slots;
     const int G = p->lanes_per_row;
     switch (p->kind) {
+        case TR_PLAN_WAVE: {
+            if (T != kWaveThreads || G != 32 || p->warps_per_row != 8 || p->cluster_ctas != 1)
+                return fail(TR_ERR_UNSUPPORTED, "a wave CTA is 256 threads (8 warps) on each of its rows, no cluster");
+            if (p->rows_per_cta != 1 && p->rows_per_cta != 2)
+                return fail(TR_ERR_UNSUPPORTED, "wave plans take 1 or 2 rows per CTA");
+            if (!in(kWaveSlots, k)) return fail(TR_ERR_UNSUPPORTED, "no wave kernel with that vec_slots");
+            if (static_cast<int64_t>(4 * kWaveThreads) * k < cols)
+                return fail(TR_ERR_UNSUPPORTED, "a wave plan needs cols <= 1024 * vec_slots");
+            if (cols < 4 * kWaveThreads) return fail(TR_ERR_UNSUPPORTED, "wave plans take rows of at least 1024 columns");
+            if (k != smallest_covering(kWaveSlots, ceil_div(cols, 4 * kWaveThreads)))
+                return fail(TR_ERR_UNSUPPORTED, "a wave plan's vec_slots is the smallest that covers the row");
+            p->grid_ctas = ceil_div(rows, p->rows_per_cta);
+            break;
+        }
         case TR_PLAN_ORDERED: {
             if (T != kOrderedThreads || G != 32 || p->warps_per_row != 8 || p->rows_per_cta != 1)
                 return fail(TR_ERR_UNSUPPORTED, "OT-1024 runs 256 threads (8 warps) per CTA, one row per CTA or cluster");
@@ -383,9 +404,11 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const double hbm_bytes = alg + (l2_fits ? 0.0 : reread);
     // weights/biases come from L2 once per row (once per CTA when held in registers)
     const double param_bytes = op == TR_OP_RMSNORM ? 4.0 * cols : op == TR_OP_LAYERNORM ? 8.0 * cols : 0.0;
+    // (a wave plan's CTAs find them in their SM's L1 after the first one: one L2 read per SM)
     const double param_reads = (p.flags & (TR_PLAN_FLAG_PARAMS_IN_REGISTERS | TR_PLAN_FLAG_PARAMS_IN_SHARED))
                                    ? static_cast<double>(p.grid_ctas)
-                                                                             : static_cast<double>(rows);
+                               : p.kind == TR_PLAN_WAVE ? std::min<double>(static_cast<double>(p.grid_ctas), d.sm_count)
+                                                        : static_cast<double>(rows);
     const double l2_bytes = (l2_fits ? reread : 0.0) + param_bytes * param_reads;
 
     const double grid = static_cast<double>(p.grid_ctas);
@@ -395,7 +418,12 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
 
     // arithmetic: SFU ex2 (16 per SM per clock) and ALU issue (128 lanes per SM per clock)
     double sfu_per_elem = 0.0, alu_per_elem = 4.0;
-    if (p.kind == TR_PLAN_ORDERED || p.kind == TR_PLAN_ORDERED_STAGED) {
+    const bool wave_ordered = p.kind == TR_PLAN_WAVE && p.order == TR_ORDER_ORDERED_TREE;
+    if (wave_ordered) {
+        // the wave kernel's ordered steps: the library's exp (about 16 full-rate
+        // instructions) for softmax, a few rounded steps per element for the norms
+        alu_per_elem = op == TR_OP_SOFTMAX ? 20.0 : op == TR_OP_LAYERNORM ? 6.0 : 4.0;
+    } else if (p.kind == TR_PLAN_ORDERED || p.kind == TR_PLAN_ORDERED_STAGED) {
         alu_per_elem = op == TR_OP_SOFTMAX ? 48.0 : op == TR_OP_CROSS_ENTROPY ? 24.0 : op == TR_OP_LAYERNORM ? 24.0
                        : reduce_op(op) ? 8.0 : 16.0;
     } else if (op == TR_OP_SOFTMAX) {
@@ -419,7 +447,17 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const bool cached_kind = p.kind == TR_PLAN_ROWS || p.kind == TR_PLAN_CLUSTER || p.kind == TR_PLAN_STAGED;
     const bool late_params = (op == TR_OP_RMSNORM || op == TR_OP_LAYERNORM) && cached_kind && p.vec_slots > 4 &&
                              !(p.flags & (TR_PLAN_FLAG_PARAMS_IN_REGISTERS | TR_PLAN_FLAG_PARAMS_IN_SHARED));
-    const double ptrip = late_params ? kParamTripUs * (op == TR_OP_LAYERNORM ? 2.0 : 1.0) : 0.0;
+    double ptrip = late_params ? kParamTripUs * (op == TR_OP_LAYERNORM ? 2.0 : 1.0) : 0.0;
+    const bool shared_params = p.kind == TR_PLAN_ROWS && (p.flags & TR_PLAN_FLAG_PARAMS_IN_SHARED);
+    if ((p.kind == TR_PLAN_WAVE || shared_params) && (op == TR_OP_RMSNORM || op == TR_OP_LAYERNORM)) {
+        // the epilogue reads every row's weight (and bias) quads from L1 (a wave
+        // plan: the SM's first CTA leaves them there) or from the CTA's shared
+        // copy: no dependent L2 trip per row, but the bytes cross the SM's L1 /
+        // shared-memory data path (128 bytes per SM clock) beside the stores; a
+        // wave CTA applies each quad to its rows_per_cta rows
+        const double l1_bytes = param_bytes * static_cast<double>(rows) / (shared_params ? 1 : p.rows_per_cta);
+        ptrip = l1_bytes / (d.sm_count * 128.0 * kClockGhz * 1e3);
+    }
 
     const double read_bytes = 4.0 * E;  // one pass over the inputs
     const double write_bytes = std::max(0.0, hbm_bytes - read_bytes);
@@ -456,6 +494,7 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     switch (p.kind) {
         case TR_PLAN_ROWS:
         case TR_PLAN_CLUSTER: inflight_thread = 16.0 * p.vec_slots * rows_seq; rounds = 1; break;
+        case TR_PLAN_WAVE: inflight_thread = 16.0 * p.vec_slots * p.rows_per_cta; rounds = 1; break;
         case TR_PLAN_ORDERED:
             inflight_thread = 16.0 * std::max(1, p.vec_slots);
             rounds = p.vec_slots > 0 ? 1 : 1 + reductions_of(op);
@@ -468,7 +507,9 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const double read_cta = (residual_op(p.op) ? 2.0 : 1.0) * read_bytes / grid;
     const double inflight_cta = std::max(16.0, std::min(T * inflight_thread, read_cta));
     // a group's rows in sequence: their merges and epilogues add up
-    const double serial = rows_seq * (red * sync + kchain + ptrip);
+    // a wave CTA's R rows share each merge round; their per-slot work adds up
+    const double serial = p.kind == TR_PLAN_WAVE ? red * sync + p.rows_per_cta * kchain + ptrip
+                                                 : rows_seq * (red * sync + kchain + ptrip);
     if (grid <= slots) {
         // a single wave: every CTA reads, then reduces and computes, then
         // writes, in lockstep, so the phases add up instead of overlapping;
@@ -504,6 +545,21 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
     };
     const int64_t n4 = ceil_div(cols, 4);
     align16 = align16 && cols % 4 == 0;
+    // the wave realisation of the 8-warp row plan on aligned rows (both tree
+    // policies): it takes the place of the plain 8-warp, one-row-per-CTA plan
+    const int kwave = smallest_covering(kWaveSlots, ceil_div(cols, 4 * kWaveThreads));
+    const bool wave_ok = align16 && kwave > 0 && cols >= 4 * kWaveThreads && !res &&
+                         (op == TR_OP_SOFTMAX || op == TR_OP_RMSNORM || op == TR_OP_LAYERNORM);
+    if (wave_ok && (order == TR_ORDER_ORDERED_TREE || order == TR_ORDER_UNORDERED_TREE))
+        for (int R : {1, 2}) {
+            tr_plan p = base(TR_PLAN_WAVE);
+            p.lanes_per_row = 32;
+            p.warps_per_row = 8;
+            p.rows_per_cta = R;
+            p.block_threads = kWaveThreads;
+            p.vec_slots = kwave;
+            cands.push_back(p);
+        }
     if (order == TR_ORDER_ORDERED_TREE) {
         tr_plan p = base(TR_PLAN_ORDERED);
         p.lanes_per_row = 32;
@@ -573,7 +629,7 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
                     p.rows_per_cta = Q;
                     p.block_threads = 32 * S * Q;
                     p.vec_slots = k;
-                    cands.push_back(p);
+                    if (!(wave_ok && S == 8 && Q == 1)) cands.push_back(p);
                     // norms on aligned rows: the same plan with the weights staged in shared memory
                     const bool norm = bop == TR_OP_RMSNORM || bop == TR_OP_LAYERNORM;
                     if (align16 && norm && in(kRowsSlotsShared, k)) {

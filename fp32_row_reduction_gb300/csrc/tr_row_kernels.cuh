@@ -408,6 +408,10 @@ __global__ void __launch_bounds__(max_threads_res<OP, K, RES>(), min_blocks_res<
     float4 none[K];
     cached_epilogue<OP, K, false, SP>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red, none,
                                       none, sp);
+    // the weight copy has landed unless the epilogue's wait gave up: then wait
+    // for it once more before the CTA's shared memory goes away
+    if constexpr (SP)
+        if (threadIdx.x == 0) mbar_wait_bounded(&pbar, 0, a.wait_ns, nullptr);
 }
 
 // Two rows per worker group, in sequence (TR_PLAN_FLAG_TWO_ROWS): the stripes of
@@ -474,6 +478,8 @@ __global__ void __launch_bounds__(pair_max_threads<K>(), pair_min_blocks<K>()) r
                                       none, sp);
     cached_epilogue<OP, K, false, SP>(a, a.y + r1 * a.cols, g1, v1, hv1, tv1, h1, t1, act1, p.w, m1, red, none,
                                       none, sp);
+    if constexpr (SP)
+        if (threadIdx.x == 0) mbar_wait_bounded(&pbar, 0, a.wait_ns, nullptr);  // as in rows_cached_kernel
 }
 
 // ---------------------------------------------------------------------------
@@ -625,7 +631,7 @@ __global__ void __launch_bounds__(staged_max_threads<OP, K, PRE>()) staged_kerne
         const RowGeom g = row_geom(xr, a.cols);
         const StagedWindow w = staged_window(xr, g, x0, x1);
         const float* slot = ring + static_cast<int64_t>(b) * a.slot_floats;
-        if (!mbar_wait_bounded(&full[b], parity, a.wait_ns, a.err)) s_abort = 1;
+        if (!mbar_wait_bounded(&full[b], parity, a.wait_ns, a.err, a.debug_flags & kDebugExpireCopies)) s_abort = 1;
         const SlotMapRows map{T, t, g.nvec};
         float4 v[K];
 #pragma unroll

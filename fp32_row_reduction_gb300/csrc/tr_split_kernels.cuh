@@ -27,6 +27,9 @@
 namespace tr {
 
 constexpr int kSplitU = 4;  // float4 per thread per streamed chunk
+// A segment that aborted (its copy wait gave up) arrives with this weight on
+// its row's arrival word, whose low 16 bits count arrivals (at most 32).
+constexpr unsigned kSplitAbortUnit = 1u << 16;
 
 __device__ __forceinline__ float4 pack(float v) { return make_float4(v, 0.0f, 0.0f, 0.0f); }
 __device__ __forceinline__ float4 pack(MaxSum v) { return make_float4(v.m, v.s, 0.0f, 0.0f); }
@@ -268,10 +271,15 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
         tv = ld_stream1(xr + ti);
         st = fold_one<OP>(st, tv);
     }
-    const bool copied = mbar_wait_bounded(&bar, 0, a.wait_ns, a.err);
+    // (testing: the copy wait of each row's first segment gives up, and the
+    // other segments must learn of it through the arrival word)
+    const bool copied =
+        mbar_wait_bounded(&bar, 0, a.wait_ns, a.err, (a.debug_flags & kDebugExpireCopies) && seg == 0);
     if (!copied) s_abort = 1;
     float ml = 0.0f;
-    st = split_merge(st, fold_cached<OP>(cache, nsm, t, T, ml));
+    // a segment whose copy has not landed is not read: its partial is marked
+    // aborted below and no CTA of the row merges it
+    if (copied) st = split_merge(st, fold_cached<OP>(cache, nsm, t, T, ml));
     RowPos p;
     p.w = t;
     p.W = T;
@@ -283,16 +291,26 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     st = cta_row_merge<Stat, 32>(st, p, part, buf);  // every thread holds the CTA's partial
 
     // ---- 2. publish the partial; warp 0 waits for the row's C partials and
-    // merges them in lane order (the same in every CTA of the row)
+    // merges them in lane order (the same in every CTA of the row). The row's
+    // arrival word counts arrivals in its low 16 bits and aborted segments
+    // (whose copy wait gave up) from bit 16: one aborted segment makes every
+    // CTA of the row stop waiting and skip the epilogue.
     __shared__ float4 s_row;
     if (t == 0) {
         a.sp_part[blockIdx.x] = pack(st);
-        red_add_release(a.sp_arrive + row, 1u);
+        red_add_release(a.sp_arrive + row, s_abort ? 1u + kSplitAbortUnit : 1u);
     }
     if (t < 32) {
         const unsigned long long t0 = global_ns();
-        bool late = false;
-        while (ld_acquire(a.sp_arrive + row) < static_cast<unsigned>(C)) {
+        // (testing: every CTA's wait gives up before it looks)
+        bool late = a.debug_flags & kDebugExpirePeers, aborted = false;
+        while (!late) {
+            const unsigned v = ld_acquire(a.sp_arrive + row);
+            if (v >= kSplitAbortUnit) {
+                aborted = true;
+                break;
+            }
+            if (v >= static_cast<unsigned>(C)) break;
             if (static_cast<long long>(global_ns() - t0) > a.wait_ns) {
                 late = true;
                 break;
@@ -300,10 +318,9 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
             __nanosleep(20);
         }
         late = __any_sync(kFull, late);
-        if (late && t == 0) {
-            atomicOr(a.err, kErrWaitTimeout);
-            s_abort = 1;
-        }
+        aborted = __any_sync(kFull, aborted);
+        if (late && t == 0) atomicOr(a.err, kErrWaitTimeout);
+        if ((late || aborted) && t == 0) s_abort = 1;
         const Stat v = warp_merge<Stat, 32>(p.lane < C ? unpack<Stat>(ld_relaxed4(a.sp_part + row * C + p.lane))
                                                        : identity_of<Stat>());
         if (t == 0) s_row = pack(v);

@@ -11,6 +11,12 @@
  * ptr[r * cols + c]; weights and biases are vectors of `cols` floats; labels
  * are `rows` int64 values; losses are `rows` floats.
  *
+ * Sizes: rows >= 0 (0 does nothing and returns TR_OK). The operators
+ * (softmax, RMSNorm, LayerNorm, cross-entropy, the fused residual norms, the
+ * backward passes and the no-allocation entry point) take 1 <= cols < 2^24,
+ * so that (float)cols, by which the norms divide, is exact; the standalone row
+ * reductions take 1 <= cols < 2^31. Other sizes: TR_ERR_INVALID_ARG.
+ *
  * Pointers are DEVICE pointers owned by the caller. They must be 4-byte
  * aligned; 16-byte alignment of the row starts is not required (unaligned
  * heads and tails are peeled), but is faster. Inputs and outputs must not
@@ -96,7 +102,12 @@ typedef enum tr_plan_kind {
                              vec_slots * block_threads 16-byte slots of its segment in shared memory (one bulk
                              asynchronous copy) and streams the rest; partials meet in a per-stream global
                              workspace allocated on first use (per stream and device) */
-    TR_PLAN_FOLD = 8      /* fold policies: a warp per row, 2 rows per 64-thread CTA */
+    TR_PLAN_FOLD = 8,     /* fold policies: a warp per row, 2 rows per 64-thread CTA */
+    TR_PLAN_WAVE = 9      /* softmax and the norms on 16-byte-aligned rows (cols % 4 == 0) of at most
+                             1024 * vec_slots columns, both tree policies: a 256-thread CTA per
+                             rows_per_cta rows (1 or 2), thread t caching the 16-byte slots t + 256 j
+                             (j < vec_slots, 2/4/6/8) of each of its rows, which is the OT-1024 leaf
+                             layout; meant for grids that are resident in one wave */
 } tr_plan_kind;
 
 typedef struct tr_plan {
@@ -296,20 +307,22 @@ tr_status tr_axis_launch_shape(int32_t sm_count, int32_t op, tr_order order, int
  *
  * Limits: rows <= 256, and each row gets C = min(32, R / rows) CTAs, where R
  * is the number of CTAs the device holds at once (two per SM at 512 threads),
- * so rows <= R / 2 (152 rows on a 152-SM device). Larger inputs return
- * TR_ERR_UNSUPPORTED with the reason in tr_last_error_message(); nothing is
- * launched. Results are within the unordered tolerance of the other entry
- * points and run-to-run deterministic.
+ * capped at the scratch's 1024 row segments, so rows <= R / 2 (152 rows on a
+ * 152-SM device). Larger inputs return TR_ERR_UNSUPPORTED with the reason in
+ * tr_last_error_message(); nothing is launched. Results are within the
+ * unordered tolerance of the FP64 definitions and run-to-run deterministic.
  *
  * Set-up: the first call on each device looks up the scratch and error-word
  * addresses, sets the kernels' shared-memory limit and queries their
  * residency. Make that first call before capturing a stream into a graph.
  *
  * State and concurrency: the scratch's counters must be zero before a launch.
- * They are zero when the library loads, and every launch leaves them at zero
- * (the last CTA to leave a row clears its counters). There is one scratch per
- * device, shared by all streams and host threads: calls whose kernels may
- * overlap in time race on it, so order them (for example, one stream). */
+ * They are zero when the library loads, and every launch leaves them at zero,
+ * also one in which a bounded wait gave up: every CTA of a row arrives and
+ * departs exactly once, and the last to depart clears the row's counters
+ * (nothing is reset on the host). There is one scratch per device, shared by
+ * all streams and host threads: calls whose kernels may overlap in time race
+ * on it, so order them (for example, one stream). */
 tr_status tr_split_rows_noalloc_f32(int32_t op, const float* x, const float* w, const float* b, float* y,
                                     int64_t rows, int64_t cols, float eps, cudaStream_t stream);
 
@@ -377,12 +390,23 @@ const char* tr_status_string(tr_status status);
 /* Text describing the last error returned on the calling thread ("" if none). */
 const char* tr_last_error_message(void);
 
-/* Testing hook: while enabled (non-zero), every launch of a plan that contains
- * bounded device-side waits also performs one wait on a barrier that nothing
- * completes, with a 1 ms limit, so that the timeout path runs and
- * tr_last_device_error() reports TR_ERR_DEVICE_TIMEOUT. Results stay correct;
- * no GPU fault or hang is involved. */
-tr_status tr_debug_force_wait_timeout(int32_t enable);
+/* Testing hook: makes bounded device-side waits give up, so that their
+ * give-up paths run and tr_last_device_error() reports TR_ERR_DEVICE_TIMEOUT,
+ * without a GPU fault or hang. `mode` is a bit mask (0 turns everything off):
+ *   1  every launch of a plan with bounded waits (staged plans) also waits on
+ *      a barrier that nothing completes, with a 1 ms limit; results stay correct;
+ *   2  waits for bulk asynchronous copies give up at once: in the split plan
+ *      the copy of each row's first segment (the row's other CTAs learn of it
+ *      through the row's arrival word, and no CTA of the row writes outputs),
+ *      in the staged plans every ring slot (that row's outputs are undefined);
+ *      a CTA still waits for its copies, with the normal limit, before it exits;
+ *   4  every split CTA's wait for the other CTAs of its row gives up at once:
+ *      no CTA of the row writes outputs.
+ * Applies to the launches made while it is set, including
+ * tr_split_rows_noalloc_f32. A launch that gave up leaves every workspace and
+ * the no-allocation scratch ready for the next launch. Other bits:
+ * TR_ERR_INVALID_ARG. */
+tr_status tr_debug_force_wait_timeout(int32_t mode);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t tr_version(void);

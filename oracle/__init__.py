@@ -75,6 +75,10 @@ def lib():
             "ot_sum_f32": [f32p, i64],
             "ot_max_f32": [f32p, i64],
             "ot_min_f32": [f32p, i64],
+            "skipnan_row_max_f32": [f32p, f32p, i64, i64],
+            "skipnan_row_min_f32": [f32p, f32p, i64, i64],
+            "skipnan_axis_max_f32": [f32p, f32p, i64, i64, i64],
+            "skipnan_axis_min_f32": [f32p, f32p, i64, i64, i64],
         }
         for name, args in sig.items():
             fn = getattr(_lib, name)
@@ -257,6 +261,25 @@ def row_min(x):
     return _f32(x).min(axis=1)
 
 
+def _skipnan_rows(x, name):
+    x = _f32(x)
+    out = np.empty(x.shape[0], np.float32)
+    _rc(getattr(lib(), name)(_ptr(x, ctypes.c_float), _ptr(out, ctypes.c_float), x.shape[0], x.shape[1]))
+    return out
+
+
+def row_max_skipnan(x):
+    """Unordered-policy row maximum (oracle.c Part 5): NaN elements are skipped,
+    so a row gives NaN only when all of it is NaN; a zero maximum that occurs
+    with both signs may come out with either sign."""
+    return _skipnan_rows(x, "skipnan_row_max_f32")
+
+
+def row_min_skipnan(x):
+    """Unordered-policy row minimum (oracle.c Part 5), NaN elements skipped."""
+    return _skipnan_rows(x, "skipnan_row_min_f32")
+
+
 def ot_row_sum(x):
     """Ordered-policy (OT-1024) emulation of the row sums."""
     return np.array([ot_sum(r) for r in _f32(x)], dtype=np.float32)
@@ -291,6 +314,26 @@ def axis_max(x, dim=0):
 
 def axis_min(x, dim=0):
     return _f32(x).min(axis=dim)
+
+
+def _skipnan_axis(x, dim, name):
+    x = _f32(x)
+    dim = dim % x.ndim
+    outer = int(np.prod(x.shape[:dim], dtype=np.int64))
+    inner = int(np.prod(x.shape[dim + 1:], dtype=np.int64))
+    out = np.empty(x.shape[:dim] + x.shape[dim + 1:], np.float32)
+    _rc(getattr(lib(), name)(_ptr(x, ctypes.c_float), _ptr(out, ctypes.c_float), outer, x.shape[dim], inner))
+    return out
+
+
+def axis_max_skipnan(x, dim=0):
+    """Unordered-policy maximum over `dim` (oracle.c Part 5), NaN elements skipped."""
+    return _skipnan_axis(x, dim, "skipnan_axis_max_f32")
+
+
+def axis_min_skipnan(x, dim=0):
+    """Unordered-policy minimum over `dim` (oracle.c Part 5), NaN elements skipped."""
+    return _skipnan_axis(x, dim, "skipnan_axis_min_f32")
 
 
 def ot_axis_sum(x, dim=0):

@@ -670,3 +670,57 @@ int fold_cross_entropy_f32(const float *logits, const int64_t *labels, float *lo
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Part 5: the unordered maximum and minimum                                 */
+/* ------------------------------------------------------------------------- */
+/*
+ * "TIRx Metal reduction lowering" §8 lists minimum and maximum among the row
+ * reductions and fixes only their reducers; the page leaves NaN undefined
+ * (§3). The unordered policy's reading: a NaN element is skipped, so a vector
+ * gives NaN only when every element is NaN; otherwise the result is the
+ * largest (smallest) non-NaN value, infinities included. When the extreme is
+ * a zero that occurs with both signs the sign is not fixed (either zero is a
+ * correct result), and this definition returns the first one met. Written as
+ * the plain serial scan: start from "nothing seen" (NaN) and replace it by
+ * each non-NaN element that is larger (smaller).
+ */
+static float skipnan_extreme(const float *v, int64_t n, int64_t stride, int want_max) {
+    float best = NAN;
+    for (int64_t i = 0; i < n; ++i) {
+        const float e = v[i * stride];
+        if (isnan(e)) continue;
+        if (isnan(best) || (want_max ? e > best : e < best)) best = e;
+    }
+    return best;
+}
+
+int skipnan_row_max_f32(const float *x, float *out, int64_t rows, int64_t cols) {
+    if (bad_sizes(rows, cols)) return -1;
+    for (int64_t r = 0; r < rows; ++r) out[r] = skipnan_extreme(x + r * cols, cols, 1, 1);
+    return 0;
+}
+
+int skipnan_row_min_f32(const float *x, float *out, int64_t rows, int64_t cols) {
+    if (bad_sizes(rows, cols)) return -1;
+    for (int64_t r = 0; r < rows; ++r) out[r] = skipnan_extreme(x + r * cols, cols, 1, 0);
+    return 0;
+}
+
+/* The same over the middle axis of a contiguous [outer, extent, inner] array:
+ * out[o * inner + i] is the extreme of x[o, :, i]. */
+int skipnan_axis_max_f32(const float *x, float *out, int64_t outer, int64_t extent, int64_t inner) {
+    if (outer < 0 || extent < 1 || inner < 1) return -1;
+    for (int64_t o = 0; o < outer; ++o)
+        for (int64_t i = 0; i < inner; ++i)
+            out[o * inner + i] = skipnan_extreme(x + o * extent * inner + i, extent, inner, 1);
+    return 0;
+}
+
+int skipnan_axis_min_f32(const float *x, float *out, int64_t outer, int64_t extent, int64_t inner) {
+    if (outer < 0 || extent < 1 || inner < 1) return -1;
+    for (int64_t o = 0; o < outer; ++o)
+        for (int64_t i = 0; i < inner; ++i)
+            out[o * inner + i] = skipnan_extreme(x + o * extent * inner + i, extent, inner, 0);
+    return 0;
+}

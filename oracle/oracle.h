@@ -72,6 +72,12 @@ int fold_layernorm_f32(const float *x, const float *gamma, const float *beta, fl
 int fold_cross_entropy_f32(const float *logits, const int64_t *labels, float *loss, int64_t rows, int64_t cols,
                            int right);
 
+/* Unordered maximum / minimum: NaN elements skipped (NaN only when all are NaN). */
+int skipnan_row_max_f32(const float *x, float *out, int64_t rows, int64_t cols);
+int skipnan_row_min_f32(const float *x, float *out, int64_t rows, int64_t cols);
+int skipnan_axis_max_f32(const float *x, float *out, int64_t outer, int64_t extent, int64_t inner);
+int skipnan_axis_min_f32(const float *x, float *out, int64_t outer, int64_t extent, int64_t inner);
+
 #ifdef __cplusplus
 }
 #endif

@@ -173,3 +173,30 @@ def test_empty_inputs_are_a_no_op_on_every_entry_point(lib):
     for order in (0, 1, 2, 3):
         assert L.tr_row_sum_f32(FAKE, FAKE + 4096, 0, 8, order, None) == ok
         assert L.tr_softmax_f32(FAKE, FAKE + 4096, 0, 8, order, None) == ok
+
+
+BIG = 1 << 24  # the first width the operators refuse: (float)cols must be exact
+
+
+@pytest.mark.parametrize("call,name", [
+    (lambda: trlib.tr_softmax_f32(FAKE, FAKE + 4 * BIG + 64, 1, BIG, 0, None), "softmax"),
+    (lambda: trlib.tr_rmsnorm_f32(FAKE, None, FAKE + 4 * BIG + 64, 1, BIG, 1e-5, 0, None), "rmsnorm"),
+    (lambda: trlib.tr_layernorm_f32(FAKE, None, None, FAKE + 4 * BIG + 64, 1, BIG, 1e-5, 1, None), "layernorm"),
+    (lambda: trlib.tr_cross_entropy_f32(FAKE, FAKE + 4 * BIG + 64, FAKE + 4 * BIG + 256, 1, BIG, 0, None),
+     "cross-entropy"),
+    (lambda: trlib.tr_add_rmsnorm_f32(FAKE, FAKE + 4 * BIG + 64, None, FAKE + 8 * BIG + 128, None, 1, BIG,
+                                      1e-5, 0, None), "fused residual RMSNorm"),
+    (lambda: trlib.tr_split_rows_noalloc_f32(0, FAKE, None, None, FAKE + 4 * BIG + 64, 1, BIG, 0.0, None),
+     "no-allocation entry point"),
+])
+def test_operators_refuse_cols_of_2_to_the_24(lib, call, name):
+    # the operators take 1 <= cols < 2^24 (validation runs before any CUDA call)
+    assert call() == trlib.TR_ERR_INVALID_ARG, name
+    assert "2^24" in trlib.tr_last_error_message(), name
+
+
+def test_debug_hook_takes_a_mask_of_known_modes(lib):
+    # the hook only sets host state: no GPU is needed to check its arguments
+    assert trlib.tr_debug_force_wait_timeout(8) == trlib.TR_ERR_INVALID_ARG
+    assert trlib.tr_debug_force_wait_timeout(6) == trlib.TR_OK
+    assert trlib.tr_debug_force_wait_timeout(0) == trlib.TR_OK

@@ -49,6 +49,15 @@ def bits(a):
     return np.asarray(a, np.float32).view(np.uint32)
 
 
+def same_extremes(got, want):
+    """Unordered max / min (NaN elements skipped): NaN exactly where the oracle has
+    NaN, every other value equal (a zero extreme of either sign)."""
+    got, want = np.asarray(got, np.float32), np.asarray(want, np.float32)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
 def check(x, op, order, got, dim=1):
     h = x.cpu().numpy()
     if order == "unordered":
@@ -57,11 +66,12 @@ def check(x, op, order, got, dim=1):
             bound = (h.shape[dim] / 32 + 24) * 2.0 ** -24 * np.abs(h.astype(np.float64)).sum(axis=dim)
             assert np.all(np.abs(got.astype(np.float64) - exact) <= bound)
         elif op == "max":
-            assert np.array_equal(got, oracle.axis_max(h, dim))
+            same_extremes(got, oracle.axis_max_skipnan(h, dim))
         elif op == "min":
-            assert np.array_equal(got, oracle.axis_min(h, dim))
+            same_extremes(got, oracle.axis_min_skipnan(h, dim))
         else:
-            assert np.array_equal(got[0], oracle.axis_min(h, dim)) and np.array_equal(got[1], oracle.axis_max(h, dim))
+            same_extremes(got[0], oracle.axis_min_skipnan(h, dim))
+            same_extremes(got[1], oracle.axis_max_skipnan(h, dim))
         return
     if op == "sum":
         want = oracle.ot_axis_sum(h, dim)
@@ -131,8 +141,7 @@ def test_ordered_nan_payloads_and_zeros():
     x = torch.from_numpy(h.copy()).to(DEV)
     for op in ("max", "min", "minmax"):
         check(x, op, "ordered", run(x, op, "ordered"))
-    mx = run(x, "max", "unordered")
-    assert np.isnan(mx[0, 2]) and not np.isnan(mx[1, 2])      # NaN only for an all-NaN column
+        check(x, op, "unordered", run(x, op, "unordered"))
 
 
 def test_axis_argument_errors():
@@ -164,3 +173,30 @@ def test_unaligned_x_takes_the_scalar_columns(off):
     for op in ("sum", "minmax"):
         for order in ("unordered", "ordered"):
             check(x, op, order, run(x, op, order))
+
+
+@pytest.mark.parametrize("shape", [(2, 3000, 40), (1, 20000, 7), (3, 64, 129), (4, 9, 256)])
+def test_unordered_axis_extremes_skip_nan(shape):
+    # NaN at random places of some columns, all-NaN columns, infinities, signed
+    # zeros; with and without splits of the reduced axis, scalar and quad columns
+    outer, extent, inner = shape
+    rng = np.random.default_rng(sum(shape))
+    h = (rng.standard_normal(shape) * 2.0).astype(np.float32)
+    for i in range(inner):
+        kind = i % 6
+        o = i % outer
+        if kind == 1:
+            h[o, rng.choice(extent, min(extent, 3), replace=False), i] = np.nan
+        elif kind == 2:
+            h[o, :, i] = np.nan
+        elif kind == 3:
+            h[o, rng.random(extent) < 0.8, i] = np.nan
+        elif kind == 4:
+            h[o, rng.integers(0, extent), i] = np.inf
+            h[o, rng.integers(0, extent), i] = -np.inf
+        elif kind == 5:
+            h[o, :, i] = -np.abs(h[o, :, i]) - 1.0
+            h[o, 0, i], h[o, extent - 1, i] = -0.0, 0.0
+    x = torch.from_numpy(h).to(DEV)
+    for op in ("max", "min", "minmax"):
+        check(x, op, "unordered", run(x, op, "unordered"))

@@ -136,10 +136,12 @@ OT_REALISATIONS = [dict(kind=4, rows_per_cta=1, vec_slots=0), dict(kind=4, rows_
 def test_ordered_same_bits_in_every_realisation(op):
     # OT-1024 is defined on columns: one-shot cached, one-shot re-read and staged
     # (persistent, TMA ring) realisations agree bit for bit with the emulation
-    d = make(op, 21, 5000, seed=17)
+    d = make(op, 21, 5000, seed=17)  # 5000 % 4 == 0: the wave realisation applies too
     emu = emulated(op, host(d))
     try:
-        for r in OT_REALISATIONS:
+        wave = [dict(kind=tr.TR_PLAN_WAVE, rows_per_cta=q, vec_slots=6) for q in (1, 2)] \
+            if op != "cross_entropy" else []
+        for r in OT_REALISATIONS + wave:
             p = tr.tr_plan(op=tr.OPS[op], order=1, lanes_per_row=32, warps_per_row=8, cluster_ctas=1,
                            block_threads=256, **r)
             assert tr.tr_plan_override(p) == tr.TR_OK
@@ -226,7 +228,7 @@ def legal_plans(op, rows, cols):
     code = tr.OPS[op]
     plans = []
     kinds = [tr.TR_PLAN_XENT] if op == "cross_entropy" else [tr.TR_PLAN_ROWS, tr.TR_PLAN_CLUSTER, tr.TR_PLAN_STREAM,
-                                                             tr.TR_PLAN_STAGED, tr.TR_PLAN_SPLIT]
+                                                             tr.TR_PLAN_STAGED, tr.TR_PLAN_SPLIT, tr.TR_PLAN_WAVE]
     for kind in kinds:
         if kind in (tr.TR_PLAN_ROWS, tr.TR_PLAN_XENT):
             ks = [2, 4, 8] if kind == tr.TR_PLAN_XENT else [1, 2, 4, 8, 16]
@@ -256,6 +258,11 @@ def legal_plans(op, rows, cols):
                         for flags in (0, tr.TR_PLAN_FLAG_PARAMS_IN_REGISTERS):
                             plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=t // 32, rows_per_cta=nb,
                                               cluster_ctas=1, vec_slots=k, block_threads=t, flags=flags))
+        elif kind == tr.TR_PLAN_WAVE:
+            for q in (1, 2):
+                for k in (2, 4, 6, 8):
+                    plans.append(dict(kind=kind, lanes_per_row=32, warps_per_row=8, rows_per_cta=q, cluster_ctas=1,
+                                      vec_slots=k, block_threads=256))
         elif kind == tr.TR_PLAN_SPLIT:
             for c in (2, 3, 32):
                 for t in (64, 256, 1024):
@@ -281,7 +288,7 @@ def legal_plans(op, rows, cols):
     return ok
 
 
-@pytest.mark.parametrize("rows,cols", [(5, 3), (17, 257), (3, 1030), (7, 4096), (2, 20001), (40, 1024)])
+@pytest.mark.parametrize("rows,cols", [(5, 3), (17, 257), (3, 1030), (7, 4096), (2, 20001), (40, 1024), (9, 5000)])
 @pytest.mark.parametrize("op", OPS)
 def test_every_legal_plan_matches_oracle(op, rows, cols):
     d = make(op, rows, cols, seed=rows + cols)

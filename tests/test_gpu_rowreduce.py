@@ -5,8 +5,11 @@ at widths 127, 257, 1024 and 4096; minimum and maximum together at 7x1024).
 Unordered sum: |gpu - FP64 sum| <= (cols/4 + 16) * 2^-24 * sum|x|, the
 rounding bound of a sum in which every element passes through at most
 cols/4 + 16 additions (the longest chain of any plan: a 4-lane worker's
-sequential fold, then the tree). Max and min are exact in any order, so they
-must equal the oracle bit for bit. Ordered: bit-identical to the OT-1024
+sequential fold, then the tree). Max and min are exact in any order; under
+the unordered policy they skip NaN elements (oracle.row_max_skipnan /
+row_min_skipnan), so they must give NaN exactly where the oracle does and the
+oracle's value everywhere else (a zero extreme met with both signs may come
+out with either sign). Ordered: bit-identical to the OT-1024
 emulation; max and min keep NaN payloads (they only select), a sum that
 becomes NaN is only checked to be NaN.
 """
@@ -42,6 +45,14 @@ def run(op, x, order="unordered"):
     return out.cpu().numpy()
 
 
+def same_extremes(got, want):
+    """NaN exactly where `want` has NaN; every other value equal (+0 == -0)."""
+    got, want = np.asarray(got, np.float32), np.asarray(want, np.float32)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
 def check_unordered(op, x, got):
     h = x.cpu().numpy()
     if op == "row_sum":
@@ -50,11 +61,12 @@ def check_unordered(op, x, got):
         bound = (cols / 4 + 16) * 2.0 ** -24 * np.abs(h.astype(np.float64)).sum(axis=1)
         assert np.all(np.abs(got.astype(np.float64) - exact) <= bound)
     elif op == "row_max":
-        assert np.array_equal(got, oracle.row_max(h))
+        same_extremes(got, oracle.row_max_skipnan(h))
     elif op == "row_min":
-        assert np.array_equal(got, oracle.row_min(h))
+        same_extremes(got, oracle.row_min_skipnan(h))
     else:
-        assert np.array_equal(got[0], oracle.row_min(h)) and np.array_equal(got[1], oracle.row_max(h))
+        same_extremes(got[0], oracle.row_min_skipnan(h))
+        same_extremes(got[1], oracle.row_max_skipnan(h))
 
 
 def check_ordered(op, x, got):
@@ -121,11 +133,8 @@ def test_special_rows():
     x = x.to(DEV)
     for op in ("row_max", "row_min", "row_minmax", "row_sum"):
         check_ordered(op, x, run(op, x, "ordered"))
-    mx, mn = run("row_max", x), run("row_min", x)
-    assert np.isnan(mx[0]) and np.isnan(mn[0])                 # a row of NaN only gives NaN
-    h = x.cpu().numpy()
-    assert mx[1] == np.nanmax(h[1]) and mn[1] == np.nanmin(h[1])  # unordered skips NaN operands
-    assert mx[4] == np.inf and mn[5] == -np.inf
+    for op in ("row_max", "row_min", "row_minmax"):
+        check_unordered(op, x, run(op, x))
 
 
 def reduce_plans(op, rows, cols):
@@ -198,3 +207,56 @@ def test_ordered_nan_payloads_and_signed_zeros():
     x = torch.from_numpy(h.copy()).to(DEV)
     for op in ("row_max", "row_min", "row_minmax"):
         check_ordered(op, x, run(op, x, "ordered"))
+
+
+def nan_rows(rows, cols, seed):
+    """Rows with NaN at random places (none, a few, most, all), infinities and signed zeros."""
+    rng = np.random.default_rng(seed)
+    h = (rng.standard_normal((rows, cols)) * 3.0).astype(np.float32)
+    for r in range(rows):
+        kind = r % 8
+        if kind == 1:
+            h[r, rng.choice(cols, min(cols, 3), replace=False)] = np.nan
+        elif kind == 2:
+            h[r, rng.random(cols) < 0.9] = np.nan
+        elif kind == 3:
+            h[r] = np.nan
+        elif kind == 4:
+            h[r, rng.integers(0, cols)] = np.inf
+            h[r, rng.integers(0, cols)] = -np.inf
+            h[r, rng.integers(0, cols)] = np.nan
+        elif kind == 5:
+            h[r] = -np.abs(h[r]) - 1.0
+            h[r, rng.choice(cols, min(cols, 2), replace=False)] = [-0.0, 0.0][:min(cols, 2)]
+            h[r, rng.integers(0, cols)] = np.nan
+        elif kind == 6:
+            h[r] = np.abs(h[r]) + 1.0
+            h[r, rng.integers(0, cols)] = -0.0
+        elif kind == 7:
+            h[r, 0] = np.nan
+            h[r, cols - 1] = np.nan
+    return h
+
+
+@pytest.mark.parametrize("rows,cols", [(8, 1), (16, 5), (24, 257), (16, 1024), (8, 4099), (16, 20000)])
+def test_unordered_extremes_skip_nan(rows, cols):
+    # the unordered max / min against the oracle's NaN-skipping definition
+    h = nan_rows(rows, cols, seed=rows * 31 + cols)
+    x = torch.from_numpy(h).to(DEV)
+    for op in ("row_max", "row_min", "row_minmax"):
+        check_unordered(op, x, run(op, x))
+
+
+def test_unordered_extremes_skip_nan_in_every_plan():
+    h = nan_rows(24, 1031, seed=77)
+    x = torch.from_numpy(h).to(DEV)
+    for op in ("row_max", "row_min", "row_minmax"):
+        plans = reduce_plans(op, 24, 1031)
+        assert plans
+        try:
+            for p in plans:
+                assert tr.tr_plan_override(tr.tr_plan(op=tr.OPS[op], order=0, kind=tr.TR_PLAN_XENT, cluster_ctas=1,
+                                                      **p)) == tr.TR_OK
+                check_unordered(op, x, run(op, x))
+        finally:
+            tr.tr_plan_override(None)

@@ -45,3 +45,58 @@ def test_single_column_rows():
     assert np.array_equal(oracle.ot_row_sum(x), x[:, 0])
     assert np.array_equal(oracle.ot_row_min(x), x[:, 0])
     assert np.array_equal(oracle.row_sum(x), x[:, 0].astype(np.float64))
+
+
+# ---- the unordered maximum and minimum (oracle.c Part 5). The page fixes the
+# reducers and leaves NaN undefined; the reading: NaN elements are skipped, a
+# vector of NaN only gives NaN, the sign of a zero extreme met with both signs
+# is not fixed. Every expected value below is written out by hand.
+
+NAN, INF = np.float32(np.nan), np.float32(np.inf)
+
+
+def test_skipnan_row_extremes_hand_written():
+    x = np.array([
+        [1.0, NAN, 3.0, -2.0],        # NaN in the middle: skipped
+        [NAN, NAN, NAN, NAN],         # only NaN: NaN
+        [NAN, 5.0, 7.0, NAN],         # NaN first and last
+        [-INF, NAN, -INF, -INF],      # infinities are values
+        [INF, 5.0, NAN, -1.5],
+        [2.5, 2.5, 2.5, 2.5],
+    ], np.float32)
+    want_max = np.array([3.0, NAN, 7.0, -INF, INF, 2.5], np.float32)
+    want_min = np.array([-2.0, NAN, 5.0, -INF, -1.5, 2.5], np.float32)
+    got_max, got_min = oracle.row_max_skipnan(x), oracle.row_min_skipnan(x)
+    assert np.array_equal(np.isnan(got_max), np.isnan(want_max))
+    assert np.array_equal(np.isnan(got_min), np.isnan(want_min))
+    ok = ~np.isnan(want_max)
+    assert np.array_equal(got_max[ok], want_max[ok]) and np.array_equal(got_min[ok], want_min[ok])
+
+
+def test_skipnan_zero_extremes_have_value_zero():
+    # a zero maximum met as -0 and +0: either sign is a correct result
+    x = np.array([[-1.0, -0.0, NAN, 0.0], [NAN, 0.0, 1.0, -0.0]], np.float32)
+    assert oracle.row_max_skipnan(x)[0] == 0.0
+    assert oracle.row_min_skipnan(x)[1] == 0.0
+
+
+def test_skipnan_differs_from_propagating_reducers():
+    # the reading is not numpy's NaN-propagating max / min
+    x = np.array([[1.0, NAN, 3.0]], np.float32)
+    assert np.isnan(x.max(axis=1)[0]) and oracle.row_max_skipnan(x)[0] == 3.0
+    assert np.isnan(x.min(axis=1)[0]) and oracle.row_min_skipnan(x)[0] == 1.0
+
+
+def test_skipnan_axis_extremes_hand_written():
+    # x[o, r, i] with outer 2, extent 3, inner 2; the reduction runs over r
+    x = np.array([[[1.0, NAN], [4.0, NAN], [-3.0, NAN]],
+                  [[NAN, 0.5], [NAN, -INF], [2.0, 9.0]]], np.float32)
+    got_max = oracle.axis_max_skipnan(x, 1)
+    got_min = oracle.axis_min_skipnan(x, 1)
+    assert got_max[0, 0] == 4.0 and np.isnan(got_max[0, 1])
+    assert got_max[1, 0] == 2.0 and got_max[1, 1] == 9.0
+    assert got_min[0, 0] == -3.0 and np.isnan(got_min[0, 1])
+    assert got_min[1, 0] == 2.0 and got_min[1, 1] == -INF
+    # the same values reduced over axis 0 (outer) and axis 2 (inner)
+    assert oracle.axis_max_skipnan(x, 0)[0, 0] == 1.0 and oracle.axis_max_skipnan(x, 0)[2, 1] == 9.0
+    assert oracle.axis_min_skipnan(x, 2)[1, 1] == -INF and oracle.axis_max_skipnan(x, 2)[0, 0] == 1.0

@@ -39,7 +39,19 @@ def covers(p, cols):
     if p.kind == trlib.TR_PLAN_STAGED:
         ring = p.rows_per_cta * (4 * math.ceil(cols / 4) + 8) * 4
         return p.block_threads * p.vec_slots >= n4 and ring <= 225 * 1024
+    if p.kind == trlib.TR_PLAN_WAVE:
+        return cols % 4 == 0 and 1024 * p.vec_slots >= cols
     return True  # streaming plans cover any row
+
+
+def check_wave(p, rows, cols, op):
+    """A wave plan: 256 threads (8 warps) per CTA on 1 or 2 aligned rows of >= 1024
+    columns, vec_slots the smallest of 2/4/6/8 that covers the row, one CTA per rows_per_cta rows."""
+    assert op in (0, 1, 2) and cols % 4 == 0 and cols >= 1024
+    assert p.block_threads == 256 and p.warps_per_row == 8 and p.lanes_per_row == 32 and p.cluster_ctas == 1
+    assert p.rows_per_cta in (1, 2) and p.flags == 0
+    assert p.vec_slots == min(k for k in (2, 4, 6, 8) if 1024 * k >= cols)
+    assert p.grid_ctas == math.ceil(rows / p.rows_per_cta)
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
@@ -47,7 +59,7 @@ def covers(p, cols):
 def test_unordered_plans_are_legal_and_cover(op, rows, cols):
     p = select(op, rows, cols)
     assert p.kind in (trlib.TR_PLAN_ROWS, trlib.TR_PLAN_CLUSTER, trlib.TR_PLAN_STREAM, trlib.TR_PLAN_STAGED,
-                      trlib.TR_PLAN_SPLIT)
+                      trlib.TR_PLAN_SPLIT, trlib.TR_PLAN_WAVE)
     assert covers(p, cols)
     assert p.block_threads % 32 == 0 and 32 <= p.block_threads <= 1024
     assert p.candidates >= 1 and p.est_us > 0 and p.ctas_per_sm >= 1
@@ -59,6 +71,8 @@ def test_unordered_plans_are_legal_and_cover(op, rows, cols):
     elif p.kind == trlib.TR_PLAN_SPLIT:
         assert p.grid_ctas == rows * p.cluster_ctas <= p.ctas_per_sm * DEV.sm_count  # all resident
         assert 2 <= p.cluster_ctas <= 32 and p.vec_slots * p.block_threads * 16 <= 225 * 1024
+    elif p.kind == trlib.TR_PLAN_WAVE:
+        check_wave(p, rows, cols, op)
     else:
         assert p.grid_ctas == rows * p.cluster_ctas
     if p.flags == trlib.TR_PLAN_FLAG_PARAMS_IN_REGISTERS:
@@ -82,10 +96,12 @@ def test_cross_entropy_uses_the_streaming_plan(rows, cols):
 @pytest.mark.parametrize("op", [0, 1, 2, 3])
 def test_ordered_requests_get_the_fixed_tree(op, rows, cols):
     p = select(op, rows, cols, order=1)
-    assert p.kind in (trlib.TR_PLAN_ORDERED, trlib.TR_PLAN_ORDERED_STAGED)
+    assert p.kind in (trlib.TR_PLAN_ORDERED, trlib.TR_PLAN_ORDERED_STAGED, trlib.TR_PLAN_WAVE)
     assert p.block_threads == 256
     assert covers(p, cols)
-    if p.kind == trlib.TR_PLAN_ORDERED and p.cluster_ctas == 8:
+    if p.kind == trlib.TR_PLAN_WAVE:
+        check_wave(p, rows, cols, op)
+    elif p.kind == trlib.TR_PLAN_ORDERED and p.cluster_ctas == 8:
         # few long rows: a cluster per row, one CTA per group of the tree
         assert p.vec_slots == 0 and cols > 16 * 1024 and rows < 2 * DEV.sm_count
         assert p.grid_ctas == 8 * rows and math.ceil(cols / 1024) * 512 <= 200 * 1024

@@ -1,9 +1,13 @@
-"""The no-allocation entry point (tr_split_rows_noalloc_f32) against the
-existing entry points.
+"""The no-allocation entry point (tr_split_rows_noalloc_f32) against the CPU oracle.
 
-It runs the split-row plan over a fixed scratch array. Two calls in a row
-must each match the existing entry point's result within the unordered
-tolerance and give identical bits. Oversize inputs are refused before any
+Some callers cannot allocate device memory when they call: code that runs
+inside a pre-sized arena in which every byte is accounted for, or a
+latency-critical loop in which cudaMalloc (which may synchronise the device and
+can fail under memory pressure) is not allowed. This entry point runs the
+split-row plan over a fixed scratch array compiled into the library instead of
+a workspace allocated on first use. Two calls in a row must each match the
+FP64 oracle within the unordered tolerance (|gpu - oracle| <= 1e-6 + 2e-6
+|oracle|) and give identical bits. Oversize inputs are refused before any
 launch. The file is named to be collected last, and it holds no state that
 depends on the tests before it.
 """
@@ -18,9 +22,7 @@ import fp32_row_reduction_gb300 as tr
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-# both results lie within 1e-6 + 2e-6|ref| of the FP64 oracle, so they differ
-# from each other by at most twice that
-RTOL, ATOL = 4e-6, 2e-6
+RTOL, ATOL = 2e-6, 1e-6
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,12 +31,23 @@ def _lib():
         pytest.skip("no CUDA device")
     tr.load()
     tr.tr_plan_override(None)
+    tr.tr_debug_force_wait_timeout(0)
 
 
-def close(got, ref):
-    got = got.double()
-    ref = ref.double()
-    return bool(((got - ref).abs() <= ATOL + RTOL * ref.abs()).all())
+def reference(op, d, eps=1e-5):
+    h = {k: v.cpu().numpy() for k, v in d.items()}
+    if op == "softmax":
+        return oracle.softmax(h["x"])
+    if op == "rmsnorm":
+        return oracle.rmsnorm(h["x"], h.get("w"), eps)
+    return oracle.layernorm(h["x"], h.get("w"), h.get("b"), eps)
+
+
+def assert_close(got, ref, what):
+    got = got.cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    bad = ~(err <= ATOL + RTOL * np.abs(ref))
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} elements outside tolerance"
 
 
 CASES = [("softmax", 16, 65536), ("rmsnorm", 16, 262144), ("layernorm", 16, 65536), ("softmax", 3, 70001),
@@ -42,9 +55,9 @@ CASES = [("softmax", 16, 65536), ("rmsnorm", 16, 262144), ("layernorm", 16, 6553
 
 
 @pytest.mark.parametrize("op,rows,cols", CASES)
-def test_two_calls_match_the_existing_entry_point(op, rows, cols):
+def test_two_calls_match_the_oracle(op, rows, cols):
     d = synth.make_inputs(op, rows, cols, 41 + rows, var=4.0 if op == "softmax" else 1.0, device=DEV)
-    want = tr.run_op(op, d)
+    ref = reference(op, d)
     a = torch.empty_like(d["x"])
     b = torch.empty_like(d["x"])
     w = d.get("w") if op != "softmax" else None
@@ -53,8 +66,8 @@ def test_two_calls_match_the_existing_entry_point(op, rows, cols):
     tr.split_rows_noalloc(op, d["x"], b, weight=w, bias=bias)
     torch.cuda.synchronize()
     assert tr.tr_last_device_error() == tr.TR_OK
-    assert close(a, want), f"{op} {rows}x{cols}: first call"
-    assert close(b, want), f"{op} {rows}x{cols}: second call"
+    assert_close(a, ref, f"{op} {rows}x{cols}: first call")
+    assert_close(b, ref, f"{op} {rows}x{cols}: second call")
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
