@@ -73,6 +73,36 @@ __device__ __forceinline__ float exp_ot(float x) {
     return exp_ot_fast(x);
 }
 
+// exp_ot_fast on two values at once with the packed binary32 FMA
+// (__ffma2_rn: each lane rounds exactly as __fmaf_rn), so every lane gives
+// exp_ot_fast's bits:
+//  - u = RN(RN(x * RN(1/ln2)) + M) stays two scalar steps per lane: the
+//    scalar _rn forms are never fused, and a fused u (one rounding) would
+//    pick another k for rare x; such a difference was seen in a kernel that
+//    formed u with the packed multiply and add;
+//  - -kf = M - u exactly (u - M is an integer of at most 2^22 in magnitude), as
+//    one packed FMA u * -1 + M;
+//  - the scaling adds k << 23 to p's bits, and k << 23 equals u's bits << 23
+//    modulo 2^32 (M's bits, 0x4b400000, vanish under the shift).
+__device__ __forceinline__ float2 exp_ot_fast2(float2 x) {
+    const float2 magic = make_float2(12582912.0f, 12582912.0f);
+    const float2 u = make_float2(__fadd_rn(__fmul_rn(x.x, 0x1.715476p+0f), 12582912.0f),
+                                 __fadd_rn(__fmul_rn(x.y, 0x1.715476p+0f), 12582912.0f));
+    const float2 nkf = __ffma2_rn(u, make_float2(-1.0f, -1.0f), magic);
+    float2 r = __ffma2_rn(nkf, make_float2(0x1.62e430p-1f, 0x1.62e430p-1f), x);
+    r = __ffma2_rn(nkf, make_float2(-0x1.05c610p-29f, -0x1.05c610p-29f), r);
+    float2 p = make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f);
+    p = __ffma2_rn(p, r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+    p = __ffma2_rn(p, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));
+    p = __ffma2_rn(p, r, make_float2(0x1.555556p-5f, 0x1.555556p-5f));
+    p = __ffma2_rn(p, r, make_float2(0x1.555556p-3f, 0x1.555556p-3f));
+    p = __ffma2_rn(p, r, make_float2(0x1.000000p-1f, 0x1.000000p-1f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(u.x) << 23)),
+                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(u.y) << 23)));
+}
+
 // log on binary32: x = 2^e m, m in (sqrt(1/2), sqrt(2)], f = m - 1,
 // s = f / (2 + f), log m = f - s (f - R(s^2)) with
 // R(z) = z (2/3 + z (2/5 + z (2/7 + z 2/9))) (the atanh series written so that

@@ -507,8 +507,10 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const double read_cta = (residual_op(p.op) ? 2.0 : 1.0) * read_bytes / grid;
     const double inflight_cta = std::max(16.0, std::min(T * inflight_thread, read_cta));
     // a group's rows in sequence: their merges and epilogues add up
-    // a wave CTA's R rows share each merge round; their per-slot work adds up
-    const double serial = p.kind == TR_PLAN_WAVE ? red * sync + p.rows_per_cta * kchain + ptrip
+    // a wave CTA's R rows share each merge round, and a thread's R rows are
+    // independent instruction streams that the scheduler interleaves (the SM's
+    // total work does not depend on R), so their per-slot chains overlap
+    const double serial = p.kind == TR_PLAN_WAVE ? red * sync + kchain + ptrip
                                                  : rows_seq * (red * sync + kchain + ptrip);
     if (grid <= slots) {
         // a single wave: every CTA reads, then reduces and computes, then

@@ -101,6 +101,43 @@ __device__ __forceinline__ void store4(float* p, float4 o, bool vec) {
     }
 }
 
+// Quad arithmetic on the packed binary32 instructions: each float4 is two
+// float2 lanes, and every lane rounds exactly like the scalar _rn form, so the
+// ordered policy keeps its bits while issuing half the instructions. One rule
+// for the ordered policy: a product that feeds an addition is formed with the
+// scalar __fmul_rn (prod4_rn), never a packed multiply. The scalar _rn forms
+// are never fused, but a packed multiply whose result fed a packed add was
+// seen fused into one rounding inside these kernels, which changed bits.
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float4 cat2(float2 a, float2 b) { return make_float4(a.x, a.y, b.x, b.y); }
+__device__ __forceinline__ float2 dup2(float s) { return make_float2(s, s); }
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return cat2(__fadd2_rn(lo2(a), lo2(b)), __fadd2_rn(hi2(a), hi2(b)));
+}
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) {
+    return cat2(__fmul2_rn(lo2(a), lo2(b)), __fmul2_rn(hi2(a), hi2(b)));
+}
+__device__ __forceinline__ float4 mul4s(float4 a, float s) {
+    return cat2(__fmul2_rn(lo2(a), dup2(s)), __fmul2_rn(hi2(a), dup2(s)));
+}
+// a - s, exactly a + (-s)
+__device__ __forceinline__ float4 sub4s(float4 a, float s) {
+    return cat2(__fadd2_rn(lo2(a), dup2(-s)), __fadd2_rn(hi2(a), dup2(-s)));
+}
+__device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {
+    return cat2(__ffma2_rn(lo2(a), lo2(b), lo2(c)), __ffma2_rn(hi2(a), hi2(b), hi2(c)));
+}
+// a * b per element with the scalar round-to-nearest multiply (never fused)
+__device__ __forceinline__ float4 prod4_rn(float4 a, float4 b) {
+    return make_float4(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y), __fmul_rn(a.z, b.z), __fmul_rn(a.w, b.w));
+}
+// the packed running sum of squares (unordered: any association)
+__device__ __forceinline__ float2 sq_acc(float2 acc, float4 v) {
+    acc = __ffma2_rn(lo2(v), lo2(v), acc);
+    return __ffma2_rn(hi2(v), hi2(v), acc);
+}
+
 // One group of R rows starting at row0. `part` holds two [R][8] slot blocks;
 // the group's trees use part[tb], part[tb ^ 1], ... alternately, continuing
 // from the previous group (the caller passes the next block index in tb).
@@ -144,19 +181,16 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
         float s[R];
         if constexpr (ORD) {
             // e = exp_ot(x - m) in place. The differences of a finite row lie in
-            // (-86, 0] almost always: then the whole thread takes the branch-free
-            // form; otherwise (a huge spread, infinities, NaN) every element
-            // takes the general form. Padding slots stay 0.
+            // (-86, 0] almost always: then the whole thread takes the packed,
+            // branch-free form; otherwise (a huge spread, infinities, NaN) every
+            // element takes the general form. Padding slots end up 0.
             bool fast = true;
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int j = 0; j < K; ++j)
                     if (okj[j]) {
-                        v[r][j].x = __fsub_rn(v[r][j].x, m[r]);
-                        v[r][j].y = __fsub_rn(v[r][j].y, m[r]);
-                        v[r][j].z = __fsub_rn(v[r][j].z, m[r]);
-                        v[r][j].w = __fsub_rn(v[r][j].w, m[r]);
+                        v[r][j] = sub4s(v[r][j], m[r]);
                         fast &= ordered::exp_ot_in_fast_range(v[r][j].x) & ordered::exp_ot_in_fast_range(v[r][j].y) &
                                 ordered::exp_ot_in_fast_range(v[r][j].z) & ordered::exp_ot_in_fast_range(v[r][j].w);
                     }
@@ -165,12 +199,7 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
                 for (int r = 0; r < R; ++r)
 #pragma unroll
                     for (int j = 0; j < K; ++j)
-                        if (okj[j]) {
-                            v[r][j].x = ordered::exp_ot_fast(v[r][j].x);
-                            v[r][j].y = ordered::exp_ot_fast(v[r][j].y);
-                            v[r][j].z = ordered::exp_ot_fast(v[r][j].z);
-                            v[r][j].w = ordered::exp_ot_fast(v[r][j].w);
-                        }
+                        if (okj[j]) v[r][j] = cat2(ordered::exp_ot_fast2(lo2(v[r][j])), ordered::exp_ot_fast2(hi2(v[r][j])));
             } else {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
@@ -191,13 +220,12 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float mb = mb_of(m[r]);
+                const float4 nmb = make_float4(-mb_of(m[r]), -mb_of(m[r]), -mb_of(m[r]), -mb_of(m[r]));
+                const float4 l2e = make_float4(kL2E, kL2E, kL2E, kL2E);
 #pragma unroll
                 for (int j = 0; j < K; ++j) {  // padding: ex2(-inf) = 0
-                    v[r][j].x = ex2(fmaf(v[r][j].x, kL2E, -mb));
-                    v[r][j].y = ex2(fmaf(v[r][j].y, kL2E, -mb));
-                    v[r][j].z = ex2(fmaf(v[r][j].z, kL2E, -mb));
-                    v[r][j].w = ex2(fmaf(v[r][j].w, kL2E, -mb));
+                    const float4 t4 = fma4(v[r][j], l2e, nmb);
+                    v[r][j] = make_float4(ex2(t4.x), ex2(t4.y), ex2(t4.z), ex2(t4.w));
                 }
             }
         }
@@ -205,12 +233,7 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
         for (int r = 0; r < R; ++r) {
             float4 l = v[r][0];
 #pragma unroll
-            for (int j = 1; j < K; ++j) {
-                l.x = Add::f(l.x, v[r][j].x);
-                l.y = Add::f(l.y, v[r][j].y);
-                l.z = Add::f(l.z, v[r][j].z);
-                l.w = Add::f(l.w, v[r][j].w);
-            }
+            for (int j = 1; j < K; ++j) l = add4(l, v[r][j]);
             s[r] = quad_top<Add>(l);
         }
         tree_rows<Add, R>(s, part[tb]);
@@ -222,12 +245,7 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
             float* yr = a.y + (row0 + r) * a.cols + 4 * t;
 #pragma unroll
             for (int j = 0; j < K; ++j)
-                if (okj[j])
-                    store4(yr + 4 * kThreads * j,
-                        ORD ? make_float4(__fmul_rn(v[r][j].x, inv), __fmul_rn(v[r][j].y, inv),
-                                          __fmul_rn(v[r][j].z, inv), __fmul_rn(v[r][j].w, inv))
-                            : make_float4(v[r][j].x * inv, v[r][j].y * inv, v[r][j].z * inv, v[r][j].w * inv),
-                        a.y_vec);
+                if (okj[j]) store4(yr + 4 * kThreads * j, mul4s(v[r][j], inv), a.y_vec);
         }
     } else if constexpr (OP == OP_RMSNORM) {
         float ss[R];
@@ -236,20 +254,13 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
             if constexpr (ORD) {
                 float4 l = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-                for (int j = 0; j < K; ++j) {
-                    l.x = __fadd_rn(l.x, __fmul_rn(v[r][j].x, v[r][j].x));
-                    l.y = __fadd_rn(l.y, __fmul_rn(v[r][j].y, v[r][j].y));
-                    l.z = __fadd_rn(l.z, __fmul_rn(v[r][j].z, v[r][j].z));
-                    l.w = __fadd_rn(l.w, __fmul_rn(v[r][j].w, v[r][j].w));
-                }
+                for (int j = 0; j < K; ++j) l = add4(l, prod4_rn(v[r][j], v[r][j]));
                 ss[r] = quad_top<AddO>(l);
             } else {
-                float acc = 0.0f;
+                float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int j = 0; j < K; ++j)
-                    acc = fmaf(v[r][j].x, v[r][j].x,
-                               fmaf(v[r][j].y, v[r][j].y, fmaf(v[r][j].z, v[r][j].z, fmaf(v[r][j].w, v[r][j].w, acc))));
-                ss[r] = acc;
+                for (int j = 0; j < K; ++j) acc = sq_acc(acc, v[r][j]);
+                ss[r] = acc.x + acc.y;
             }
         }
         tree_rows<Add, R>(ss, part[tb]);
@@ -268,16 +279,11 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 if (row0 + r >= a.rows) break;
-                const float4 x = v[r][j];
-                float4 o;
-                if constexpr (ORD) {
-                    o = make_float4(__fmul_rn(x.x, sc[r]), __fmul_rn(x.y, sc[r]), __fmul_rn(x.z, sc[r]),
-                                    __fmul_rn(x.w, sc[r]));
-                    if (a.has_w)
-                        o = make_float4(__fmul_rn(o.x, w.x), __fmul_rn(o.y, w.y), __fmul_rn(o.z, w.z),
-                                        __fmul_rn(o.w, w.w));
+                float4 o = mul4s(v[r][j], sc[r]);
+                if (ORD) {
+                    if (a.has_w) o = mul4(o, w);
                 } else {
-                    o = make_float4(x.x * sc[r] * w.x, x.y * sc[r] * w.y, x.z * sc[r] * w.z, x.w * sc[r] * w.w);
+                    o = mul4(o, w);
                 }
                 store4(a.y + (row0 + r) * a.cols + c, o, a.y_vec);
             }
@@ -288,12 +294,7 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
         for (int r = 0; r < R; ++r) {
             float4 l = v[r][0];
 #pragma unroll
-            for (int j = 1; j < K; ++j) {
-                l.x = Add::f(l.x, v[r][j].x);
-                l.y = Add::f(l.y, v[r][j].y);
-                l.z = Add::f(l.z, v[r][j].z);
-                l.w = Add::f(l.w, v[r][j].w);
-            }
+            for (int j = 1; j < K; ++j) l = add4(l, v[r][j]);
             mu[r] = quad_top<Add>(l);
         }
         tree_rows<Add, R>(mu, part[tb]);
@@ -309,24 +310,16 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
                     if (!okj[j]) continue;  // padding is no column of the row
-                    const float cx = __fsub_rn(v[r][j].x, mu[r]), cy = __fsub_rn(v[r][j].y, mu[r]);
-                    const float cz = __fsub_rn(v[r][j].z, mu[r]), cw = __fsub_rn(v[r][j].w, mu[r]);
-                    l.x = __fadd_rn(l.x, __fmul_rn(cx, cx));
-                    l.y = __fadd_rn(l.y, __fmul_rn(cy, cy));
-                    l.z = __fadd_rn(l.z, __fmul_rn(cz, cz));
-                    l.w = __fadd_rn(l.w, __fmul_rn(cw, cw));
+                    const float4 c = sub4s(v[r][j], mu[r]);
+                    l = add4(l, prod4_rn(c, c));
                 }
                 q[r] = quad_top<AddO>(l);
             } else {
-                float acc = 0.0f;
+                float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int j = 0; j < K; ++j) {
-                    if (!okj[j]) continue;
-                    const float cx = v[r][j].x - mu[r], cy = v[r][j].y - mu[r];
-                    const float cz = v[r][j].z - mu[r], cw = v[r][j].w - mu[r];
-                    acc = fmaf(cx, cx, fmaf(cy, cy, fmaf(cz, cz, fmaf(cw, cw, acc))));
-                }
-                q[r] = acc;
+                for (int j = 0; j < K; ++j)
+                    if (okj[j]) acc = sq_acc(acc, sub4s(v[r][j], mu[r]));
+                q[r] = acc.x + acc.y;
             }
         }
         tree_rows<Add, R>(q, part[tb]);
@@ -346,20 +339,12 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 if (row0 + r >= a.rows) break;
-                const float4 x = v[r][j];
-                float4 o;
-                if constexpr (ORD) {
-                    o = make_float4(__fmul_rn(__fsub_rn(x.x, mu[r]), sc[r]), __fmul_rn(__fsub_rn(x.y, mu[r]), sc[r]),
-                                    __fmul_rn(__fsub_rn(x.z, mu[r]), sc[r]), __fmul_rn(__fsub_rn(x.w, mu[r]), sc[r]));
-                    if (a.has_w)
-                        o = make_float4(__fmul_rn(o.x, w.x), __fmul_rn(o.y, w.y), __fmul_rn(o.z, w.z),
-                                        __fmul_rn(o.w, w.w));
-                    if (a.has_b)
-                        o = make_float4(__fadd_rn(o.x, b.x), __fadd_rn(o.y, b.y), __fadd_rn(o.z, b.z),
-                                        __fadd_rn(o.w, b.w));
+                float4 o = mul4s(sub4s(v[r][j], mu[r]), sc[r]);
+                if (ORD) {
+                    if (a.has_w) o = a.has_b ? prod4_rn(o, w) : mul4(o, w);
+                    if (a.has_b) o = add4(o, b);
                 } else {
-                    o = make_float4(fmaf((x.x - mu[r]) * sc[r], w.x, b.x), fmaf((x.y - mu[r]) * sc[r], w.y, b.y),
-                                    fmaf((x.z - mu[r]) * sc[r], w.z, b.z), fmaf((x.w - mu[r]) * sc[r], w.w, b.w));
+                    o = fma4(o, w, b);
                 }
                 store4(a.y + (row0 + r) * a.cols + c, o, a.y_vec);
             }

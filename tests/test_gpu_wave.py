@@ -225,3 +225,20 @@ def test_wave_full_size_768x6144(op, order):
         assert_bits(got, emulated(op, h), f"{op} 768x6144")
     else:
         assert_close(got, reference(op, h), f"{op} 768x6144")
+
+
+@pytest.mark.parametrize("rows_per_cta", [1, 2])
+def test_wave_ordered_softmax_dense_exp_range(rows_per_cta):
+    # every difference x - max in (-86, 0], dense, plus a band where x / ln2 lies
+    # within a few ulps of a half-integer (the rounding that picks the exp's k):
+    # the packed exp must give the emulation's bits for all of them
+    rng = np.random.default_rng(99 + rows_per_cta)
+    rows, cols = 2048, 4096
+    x = -(rng.random((rows, cols)) * 85.99).astype(np.float32)
+    half = (rng.integers(-124, 0, size=(rows // 2, cols)) + 0.5) / np.log2(np.e)
+    band = half.astype(np.float32).view(np.int32) + rng.integers(-3, 4, size=half.shape).astype(np.int32)
+    x[: rows // 2] = np.maximum(band.view(np.float32), np.float32(-85.99))
+    x[:, 0] = 0.0                                   # the row maximum, so x - max = x
+    d = {"x": torch.from_numpy(x).to(DEV)}
+    y = run_with(wave_plan("softmax", "ordered", cols, rows_per_cta), "softmax", d, "ordered").cpu().numpy()
+    assert_bits(y, oracle.ot_softmax(x), "dense exp range")
