@@ -47,7 +47,9 @@ TR_PLAN_STAGED = 5
 TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_SPLIT = 7
 TR_PLAN_FOLD = 8
+COST_CONSTANTS = 15  # TR_COST_CONSTANTS
 TR_PLAN_WAVE = 9
+TR_PLAN_SEGMENTS = 10
 TR_OP_ADD_RMSNORM = 4
 TR_OP_ADD_LAYERNORM = 5
 TR_OP_ROW_SUM = 6
@@ -238,14 +240,14 @@ def check_plan_for(dev: tr_device_desc, plan: tr_plan, rows, cols, align16=1):
 
 def cost_constants():
     """The library's cost-model constants (TR_COST_CONSTANTS doubles)."""
-    out = (ctypes.c_double * 13)()
-    _check(load().tr_plan_cost_constants(out, 13), "tr_plan_cost_constants")
+    out = (ctypes.c_double * COST_CONSTANTS)()
+    _check(load().tr_plan_cost_constants(out, COST_CONSTANTS), "tr_plan_cost_constants")
     return list(out)
 
 
 def estimate_with(dev: tr_device_desc, plan: tr_plan, rows, cols, align16=1, constants=None) -> float:
     """The model's estimate (us) for a plan with grid_ctas/ctas_per_sm filled, under given constants."""
-    c = None if constants is None else (ctypes.c_double * 13)(*constants)
+    c = None if constants is None else (ctypes.c_double * COST_CONSTANTS)(*constants)
     out = ctypes.c_double()
     _check(load().tr_plan_estimate_with(ctypes.byref(dev), ctypes.byref(plan), rows, cols, align16, c,
                                         ctypes.byref(out)), "tr_plan_estimate_with")

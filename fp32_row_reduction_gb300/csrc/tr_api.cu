@@ -309,7 +309,8 @@ tr_status run(Call& c, cudaStream_t stream) {
     a.nbuf = (plan.kind == TR_PLAN_STAGED || plan.kind == TR_PLAN_ORDERED_STAGED) ? plan.rows_per_cta : 0;
     a.slot_floats = staged_slot_floats(a.cols);
     const bool split = plan.kind == TR_PLAN_SPLIT;
-    if (split) {
+    const bool segs = plan.kind == TR_PLAN_SEGMENTS;
+    if (split || segs) {
         void* ws = nullptr;
         {
             std::lock_guard<std::mutex> lock(g_mu);
@@ -320,6 +321,7 @@ tr_status run(Call& c, cudaStream_t stream) {
         a.sp_arrive = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kSplitMaxParts * 16);
         a.sp_depart = a.sp_arrive + kSplitMaxRows;
         a.slot_floats = 4 * plan.vec_slots * plan.block_threads;
+        if (segs) a.nbuf = seg_cached_rows(a.rows, a.cols, plan.grid_ctas);
     }
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -329,15 +331,15 @@ tr_status run(Call& c, cudaStream_t stream) {
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned nattr = 0;
-    if (plan.cluster_ctas > 1 && !split) {
+    if (plan.cluster_ctas > 1 && !split && !segs) {
         attr[nattr].id = cudaLaunchAttributeClusterDimension;
         attr[nattr].val.clusterDim.x = plan.cluster_ctas;
         attr[nattr].val.clusterDim.y = 1;
         attr[nattr].val.clusterDim.z = 1;
         ++nattr;
     }
-    if (split) {
-        // every CTA waits for the other segments of its row: all must be resident
+    if (split || segs) {
+        // every CTA waits for the other segments of its row(s): all must be resident
         attr[nattr].id = cudaLaunchAttributeCooperative;
         attr[nattr].val.cooperative = 1;
         ++nattr;
@@ -992,7 +994,8 @@ tr_status tr_plan_override(const tr_plan* plan) {
         return TR_OK;
     }
     if (plan->op < TR_OP_SOFTMAX || plan->op > TR_OP_ROW_MINMAX) return fail(TR_ERR_INVALID_ARG, "bad op");
-    if ((plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_SPLIT) && plan->kind != TR_PLAN_WAVE)
+    if ((plan->kind < TR_PLAN_ROWS || plan->kind > TR_PLAN_SPLIT) && plan->kind != TR_PLAN_WAVE &&
+        plan->kind != TR_PLAN_SEGMENTS)
         return fail(TR_ERR_INVALID_ARG, "bad plan kind");
     g_override[plan->op] = *plan;
     g_override_set[plan->op] = true;

@@ -147,6 +147,18 @@ const void* kernel_wave_unordered(int op, int slots, int rows_per_cta);
 const void* kernel_wave_ordered(int op, int slots, int rows_per_cta);
 constexpr int kWaveSlots[] = {2, 4, 6, 8};
 constexpr int kWaveThreads = 256;
+// Segments kernels (TR_PLAN_SEGMENTS): softmax, RMSNorm, LayerNorm; vec_slots 1, 2.
+const void* kernel_segments(int op, int slots);
+constexpr int kSegSlots[] = {1, 2};
+constexpr int kSegThreads = 1024;
+constexpr int kSegMaxRows = 32;
+constexpr int kSegSmem = 200 * 1024;  // dynamic shared memory of a segments CTA (one CTA per SM)
+// Rows of a segments launch whose segment is cached in shared memory.
+inline int seg_cached_rows(int64_t rows, int64_t cols, int64_t grid) {
+    const int64_t sq = (cols / 4 + grid - 1) / grid;
+    const int64_t n = sq > 0 ? kSegSmem / (sq * 16) : rows;
+    return static_cast<int>(n < rows ? n : rows);
+}
 // Dynamic shared memory a plan's kernel needs (0 for all but staged plans).
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols);
 
@@ -160,6 +172,8 @@ inline const void* kernel_for(const tr_plan& p) {
         if (p.kind == TR_PLAN_ORDERED) return p.flags ? nullptr : kernel_ordered(p.op, p.vec_slots);
         return kernel_reduce(p.op, p.kind, p.lanes_per_row, p.vec_slots, p.flags);
     }
+    if (p.kind == TR_PLAN_SEGMENTS) return p.flags || p.order != TR_ORDER_UNORDERED_TREE ? nullptr
+                                                                                         : kernel_segments(p.op, p.vec_slots);
     if (p.kind == TR_PLAN_WAVE) {
         if (p.flags) return nullptr;
         return p.order == TR_ORDER_ORDERED_TREE ? kernel_wave_ordered(p.op, p.vec_slots, p.rows_per_cta)

@@ -55,6 +55,7 @@ int smallest_covering(const int (&arr)[N], int64_t need) {  // smallest K with K
 
 int max_threads_for_slots(int op, int kind, int k, int flags) {
     if (kind == TR_PLAN_ORDERED_STAGED || kind == TR_PLAN_WAVE) return kOrderedThreads;
+    if (kind == TR_PLAN_SEGMENTS) return kSegThreads;
     if (kind == TR_PLAN_STAGED && (flags & TR_PLAN_FLAG_PARAMS_IN_REGISTERS))
         return k <= 2 ? 1024 : k == 4 ? 768 : (op == TR_OP_LAYERNORM ? 384 : 512);
     if (kind == TR_PLAN_STAGED) return (k >= 8 || (k >= 4 && op == TR_OP_LAYERNORM)) ? 768 : 1024;
@@ -93,25 +94,27 @@ int reductions_of(int op) {
 // Fitted by coordinate descent (calibration/fit_cost_model.py) on GB300 plan
 // sweeps of calibration shapes DISJOINT from the benchmark workloads (the
 // shape lists are in calibration/sweep.py, the sweeps beside it), minimising
-// the mean time regret of the chosen plan (with the tie-break below): 7.1%
-// mean, 30% max over 69 cases. The benchmark shapes were then scored as a
+// the mean time regret of the chosen plan (with the tie-break below): 6.1%
+// mean, 24.8% max over 69 cases. The benchmark shapes were then scored as a
 // held-out set with the constants frozen (the page's frozen held-out
-// protocol): 6.5% mean, 24% max over 27 cases. The clock is the datasheet
+// protocol): 3.8% mean, 21.5% max over 27 cases. The clock is the datasheet
 // value.
 const CostConstants kCostDefaults = {
-    0.375,  // launch: launch and grid ramp beyond what the other terms cover
-    3.3,    // latency: loaded DRAM round trip as seen by a CTA
-    0.528,  // cta_barrier: one shared-memory merge round
-    0.84,   // cluster_barrier: one cluster merge round
-    1.32,   // l2_over_hbm: L2 re-read bandwidth relative to HBM
-    1.44,   // staged_row: fixed cost of one row of a staged CTA
-    0.5,    // one_wave_alu: share of arithmetic exposed in a single wave
-    0.15,   // wave: extra cost of each further wave
-    0.06,   // slot_pass: serial per-thread work, per cached slot and pass
-    0.8,    // param_trip: dependent L2 trip for the norms' weights (per vector)
-    1.9,    // clock_ghz
-    1.5,    // split_sync: publish, count and read back a split row's partials
-    0.4,    // pair_overlap: share of the write phase hidden by two rows per group
+    0.375,   // launch: launch and grid ramp beyond what the other terms cover
+    3.3,     // latency: loaded DRAM round trip as seen by a CTA
+    0.33,    // cta_barrier: one shared-memory merge round
+    0.56,    // cluster_barrier: one cluster merge round
+    1.32,    // l2_over_hbm: L2 re-read bandwidth relative to HBM
+    1.44,    // staged_row: fixed cost of one row of a staged CTA
+    0.6,     // one_wave_alu: share of arithmetic exposed in a single wave
+    0.15,    // wave: extra cost of each further wave
+    0.063,   // slot_pass: serial per-thread work, per cached slot and pass
+    0.4,     // param_trip: dependent L2 trip for the norms' weights (per vector)
+    1.9,     // clock_ghz
+    0.375,   // split_sync: publish, count and read back a split row's partials
+    0.6,     // pair_overlap: share of the write phase hidden by two rows per group
+    0.015,   // wave_slot_pass: a wave thread's serial work per cached slot and pass
+    4.0,     // wave_row_share: share of that work each further row of a wave thread adds
 };
 
 tr_device_desc gb300_desc() {
@@ -130,6 +133,7 @@ tr_device_desc gb300_desc() {
 
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols) {
     if (p.kind == TR_PLAN_SPLIT) return static_cast<size_t>(p.vec_slots) * p.block_threads * 16;
+    if (p.kind == TR_PLAN_SEGMENTS) return kSegSmem;
     if (p.kind == TR_PLAN_ORDERED && p.cluster_ctas == kOtClusterCtas) return ot_cluster_smem(cols);
     if (p.kind == TR_PLAN_ROWS && (p.flags & TR_PLAN_FLAG_PARAMS_IN_SHARED))
         return static_cast<size_t>(cols) * 4 * (base_op(p.op) == TR_OP_LAYERNORM ? 2 : 1);
@@ -150,6 +154,7 @@ int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem) {
             break;
         case TR_PLAN_ORDERED_STAGED: regs = 40 + 4 * k; break;
         case TR_PLAN_WAVE: regs = p.rows_per_cta == 1 ? std::max(32, 16 + 4 * k) : 30 + 8 * k; break;
+        case TR_PLAN_SEGMENTS: regs = 48 + 8 * k; break;
         case TR_PLAN_STREAM: regs = 64; break;
         case TR_PLAN_SPLIT: regs = 64; break;
         case TR_PLAN_XENT: regs = 24 + 4 * k; break;
@@ -240,6 +245,18 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     const int k = p->vec_slots;
     const int G = p->lanes_per_row;
     switch (p->kind) {
+        case TR_PLAN_SEGMENTS: {
+            if (p->op != TR_OP_SOFTMAX && p->op != TR_OP_RMSNORM && p->op != TR_OP_LAYERNORM)
+                return fail(TR_ERR_UNSUPPORTED, "segments plans serve softmax, RMSNorm and LayerNorm");
+            if (!align16) return fail(TR_ERR_UNSUPPORTED, "segments plans need 16-byte-aligned rows and weights");
+            if (T != kSegThreads || G != 32 || p->warps_per_row != T / 32 || p->cluster_ctas != 1)
+                return fail(TR_ERR_UNSUPPORTED, "a segments CTA is 1024 threads on its segment of every row");
+            if (p->rows_per_cta != rows) return fail(TR_ERR_UNSUPPORTED, "a segments plan serves all rows (rows_per_cta = rows)");
+            if (rows > kSegMaxRows) return fail(TR_ERR_UNSUPPORTED, "segments plans take at most 32 rows");
+            if (!in(kSegSlots, k)) return fail(TR_ERR_UNSUPPORTED, "no segments kernel with that vec_slots");
+            p->grid_ctas = 0;  // every resident CTA (set below)
+            break;
+        }
         case TR_PLAN_WAVE: {
             if (T != kWaveThreads || G != 32 || p->warps_per_row != 8 || p->cluster_ctas != 1)
                 return fail(TR_ERR_UNSUPPORTED, "a wave CTA is 256 threads (8 warps) on each of its rows, no cluster");
@@ -369,6 +386,14 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     if (p->kind == TR_PLAN_SPLIT && p->grid_ctas > res)
         return fail(TR_ERR_UNSUPPORTED, "a split plan's CTAs must all be resident at once (cooperative launch)");
     if (p->kind == TR_PLAN_STAGED || p->kind == TR_PLAN_ORDERED_STAGED) p->grid_ctas = std::min<int64_t>(rows, res);
+    if (p->kind == TR_PLAN_SEGMENTS) {
+        // every resident CTA, at most one per SM; each owns a segment of every row
+        p->grid_ctas = std::min<int64_t>(res, d.sm_count);
+        const int64_t sq = ceil_div(cols / 4, p->grid_ctas);
+        if (sq > static_cast<int64_t>(k) * T) return fail(TR_ERR_UNSUPPORTED, "a segment exceeds vec_slots quads per thread");
+        if (sq < T / 2) return fail(TR_ERR_UNSUPPORTED, "segments plans are for rows of at least 512 quads per CTA");
+        if (rows * p->grid_ctas > kSplitMaxParts) return fail(TR_ERR_UNSUPPORTED, "rows x CTAs partials exceed the workspace");
+    }
     if (why) *why = "";
     return TR_OK;
 }
@@ -379,7 +404,8 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
                  kClusterBarrierUs = c.cluster_barrier, kL2OverHbm = c.l2_over_hbm, kStagedRowUs = c.staged_row,
                  kOneWaveAluFactor = c.one_wave_alu, kWaveUs = c.wave, kSlotPassUs = c.slot_pass,
                  kParamTripUs = c.param_trip, kClockGhz = c.clock_ghz, kSplitSyncUs = c.split_sync,
-                 kPairOverlap = c.pair_overlap;
+                 kPairOverlap = c.pair_overlap, kWaveSlotPass = c.wave_slot_pass,
+                 kWaveRowShare = c.wave_row_share;
     (void)align16;
     const double E = static_cast<double>(rows) * static_cast<double>(cols);
     const double bw = d.hbm_gbs * 1e3;  // bytes per microsecond
@@ -457,6 +483,16 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
         // wave CTA applies each quad to its rows_per_cta rows
         const double l1_bytes = param_bytes * static_cast<double>(rows) / (shared_params ? 1 : p.rows_per_cta);
         ptrip = l1_bytes / (d.sm_count * 128.0 * kClockGhz * 1e3);
+        if (p.kind == TR_PLAN_WAVE) {
+            // a wave thread keeps 4 K R cached floats, and in the epilogue one
+            // quad per parameter vector beside about 12 other values; where that
+            // exceeds the registers of its resident CTAs (40 at six per SM) the
+            // parameter loads serialise behind spills: one dependent trip per vector
+            const int vectors = op == TR_OP_LAYERNORM ? 2 : 1;
+            const int live = 4 * p.vec_slots * p.rows_per_cta + 4 * vectors + 12;
+            const int budget = p.ctas_per_sm > 0 ? d.regs_per_sm / (p.block_threads * p.ctas_per_sm) / 8 * 8 : 255;
+            if (live > budget) ptrip += kParamTripUs * vectors;
+        }
     }
 
     const double read_bytes = 4.0 * E;  // one pass over the inputs
@@ -473,6 +509,20 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
         return kLaunchUs + kLatencyUs + std::max({hbm_bytes / bw_eff, t_alu, chain}) + t_l2;
     }
 
+    if (p.kind == TR_PLAN_SEGMENTS) {
+        // one wave of co-resident CTAs: the cached rows land by bulk copies while
+        // the others stream, one exchange of all rows' partials, then the writes;
+        // the streamed rows are read again (from L2 when the input fits), the
+        // weights and biases cross L2 once
+        const int nbuf = seg_cached_rows(rows, cols, p.grid_ctas);
+        const double cached = static_cast<double>(nbuf) * static_cast<double>(ceil_div(cols / 4, p.grid_ctas)) * 16.0 *
+                              static_cast<double>(p.grid_ctas);
+        const double over = std::max(0.0, read_bytes - cached);
+        const double t_over = over / ((l2_fits ? kL2OverHbm : 1.0) * bw);
+        const double t_par = param_bytes / (kL2OverHbm * bw);
+        return kLaunchUs + kLatencyUs + read_bytes / bw + kSplitSyncUs + kOneWaveAluFactor * t_alu + kchain +
+               write_bytes / bw + t_over + t_par;
+    }
     if (p.kind == TR_PLAN_SPLIT) {
         // one wave of co-resident CTAs in lockstep: read (the bulk copy of the
         // cached part plus the streamed overflow), one exchange of partials
@@ -507,10 +557,13 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const double read_cta = (residual_op(p.op) ? 2.0 : 1.0) * read_bytes / grid;
     const double inflight_cta = std::max(16.0, std::min(T * inflight_thread, read_cta));
     // a group's rows in sequence: their merges and epilogues add up
-    // a wave CTA's R rows share each merge round, and a thread's R rows are
-    // independent instruction streams that the scheduler interleaves (the SM's
-    // total work does not depend on R), so their per-slot chains overlap
-    const double serial = p.kind == TR_PLAN_WAVE ? red * sync + kchain + ptrip
+    // a wave CTA's R rows share each merge round; a thread's R rows are
+    // independent instruction streams, so each further row adds only a share of
+    // the per-slot chain (fitted), and the chain of the lean wave kernel has its
+    // own per-slot constant
+    const double wchain = std::max(1, p.vec_slots) * kWaveSlotPass * passes *
+                          (1.0 + kWaveRowShare * (p.rows_per_cta - 1));
+    const double serial = p.kind == TR_PLAN_WAVE ? red * sync + wchain + ptrip
                                                  : rows_seq * (red * sync + kchain + ptrip);
     if (grid <= slots) {
         // a single wave: every CTA reads, then reduces and computes, then
@@ -695,6 +748,9 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
                     s.vec_slots = 0;
                     cands.push_back(s);
                 }
+            // (the segments plan, TR_PLAN_SEGMENTS, is not enumerated: measured, it
+            // is slower than the split and cluster plans on most long-row shapes;
+            // it runs only when a caller forces it)
             // few long rows: C co-resident CTAs per row, each caching its segment in
             // shared memory (one CTA per SM with the whole budget, or two with half)
             for (int C = 2; C <= kSplitMaxCtas && rows <= kSplitMaxRows && rows * C <= kSplitMaxParts; ++C)

@@ -103,11 +103,19 @@ typedef enum tr_plan_kind {
                              asynchronous copy) and streams the rest; partials meet in a per-stream global
                              workspace allocated on first use (per stream and device) */
     TR_PLAN_FOLD = 8,     /* fold policies: a warp per row, 2 rows per 64-thread CTA */
-    TR_PLAN_WAVE = 9      /* softmax and the norms on 16-byte-aligned rows (cols % 4 == 0) of at most
+    TR_PLAN_WAVE = 9,     /* softmax and the norms on 16-byte-aligned rows (cols % 4 == 0) of at most
                              1024 * vec_slots columns, both tree policies: a 256-thread CTA per
                              rows_per_cta rows (1 or 2), thread t caching the 16-byte slots t + 256 j
                              (j < vec_slots, 2/4/6/8) of each of its rows, which is the OT-1024 leaf
                              layout; meant for grids that are resident in one wave */
+    TR_PLAN_SEGMENTS = 10 /* few long rows, unordered softmax and norms on 16-byte-aligned rows: grid_ctas
+                             co-resident CTAs (cooperative launch, one per SM) of 1024 threads, CTA g owning
+                             one column segment of EVERY row (rows_per_cta = rows, at most 32), vec_slots
+                             16-byte slots per thread per row (1 or 2); a thread keeps its columns' weight and
+                             bias in registers for all rows; the rows' partials meet once in the stream's
+                             workspace (allocated on first use, as for the split plan). The selector never
+                             picks it (it measured slower than the split plan on most long rows): it runs
+                             only under tr_plan_override */
 } tr_plan_kind;
 
 typedef struct tr_plan {
@@ -348,11 +356,12 @@ tr_status tr_plan_check_for(const tr_device_desc* dev, tr_plan* plan, int64_t ro
 /* ---- cost-model calibration and audit (host side) ----------------------
  * The model's constants, in this order: launch, latency, cta_barrier,
  * cluster_barrier, l2_over_hbm, staged_row, one_wave_alu, wave, slot_pass,
- * param_trip, clock_ghz, split_sync, pair_overlap (microseconds unless stated). They are
+ * param_trip, clock_ghz, split_sync, pair_overlap, wave_slot_pass, wave_row_share
+ * (microseconds unless stated). They are
  * fixed in the library; these calls exist so that an offline calibration can
  * score the model on measured plan sweeps ("Whole-launch reduction cost
  * policy": measurement calibrates priors, never selects a plan). */
-#define TR_COST_CONSTANTS 13
+#define TR_COST_CONSTANTS 15
 
 /* Copy the library's constants into out[0 .. n-1] (n must be TR_COST_CONSTANTS). */
 tr_status tr_plan_cost_constants(double* out, int32_t n);

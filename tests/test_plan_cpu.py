@@ -204,6 +204,35 @@ def test_split_plan_limits():
     assert st == trlib.TR_ERR_UNSUPPORTED
 
 
+def seg_plan(op, rows, cols, K=None):
+    sq = math.ceil(cols // 4 / DEV.sm_count)
+    K = K if K is not None else math.ceil(sq / 1024)
+    return trlib.tr_plan(op=op, order=0, kind=trlib.TR_PLAN_SEGMENTS, lanes_per_row=32, warps_per_row=32,
+                         rows_per_cta=rows, cluster_ctas=1, vec_slots=K, block_threads=1024)
+
+
+def test_segments_plan_limits_and_never_selected():
+    # legal when forced: aligned rows, one 1024-thread CTA per SM holding a
+    # segment of every row (rows <= 32, rows x SMs partials), 512..2048 quads per CTA
+    for op, rows, cols, K, ok in [(0, 16, 1048576, 2, True), (1, 4, 1245184, 2, True), (2, 26, 400000, 1, True),
+                                  (2, 27, 400000, 1, False),   # 27 x 152 partials > the workspace
+                                  (0, 16, 1048576, 1, False),  # 1725 quads per CTA > 1 x 1024
+                                  (0, 16, 262144, 1, False),   # 432 quads per CTA: too short
+                                  (0, 4, 1253376, 2, False),   # 2062 quads per CTA > 2 x 1024
+                                  (3, 16, 1048576, 2, False)]:  # cross-entropy is not served
+        st, why = trlib.check_plan_for(DEV, seg_plan(op, rows, cols, K), rows, cols, 1)
+        assert (st == trlib.TR_OK) == ok, (op, rows, cols, K, why)
+    st, _ = trlib.check_plan_for(DEV, seg_plan(0, 16, 1048576), 16, 1048576, 0)  # unaligned
+    assert st == trlib.TR_ERR_UNSUPPORTED
+    p = seg_plan(0, 16, 1048576)
+    p.rows_per_cta = 8                                 # a CTA holds every row
+    assert trlib.check_plan_for(DEV, p, 16, 1048576, 1)[0] == trlib.TR_ERR_UNSUPPORTED
+    # measured slower than the split and cluster plans on most long rows: never chosen
+    for op in (0, 1, 2):
+        for rows, cols in SHAPES + [(4, 1245184), (24, 1048576), (16, 400000)]:
+            assert select(op, rows, cols).kind != trlib.TR_PLAN_SEGMENTS
+
+
 @pytest.mark.parametrize("op", [trlib.TR_OP_ROW_SUM, trlib.TR_OP_ROW_MAX, trlib.TR_OP_ROW_MIN, trlib.TR_OP_ROW_MINMAX])
 def test_row_reductions_stream_once(op):
     # standalone reductions: the streaming kind unordered, the streaming OT-1024 ordered
