@@ -306,6 +306,7 @@ tr_status run(Call& c, cudaStream_t stream) {
     a.C = plan.cluster_ctas;
     a.wait_ns = kWaitNs;
     a.debug_flags = g_debug_flags;
+    a.pf_ctas = split_dev->desc.sm_count;  // about one CTA per SM: the first the block scheduler places there
     a.nbuf = (plan.kind == TR_PLAN_STAGED || plan.kind == TR_PLAN_ORDERED_STAGED) ? plan.rows_per_cta : 0;
     a.slot_floats = staged_slot_floats(a.cols);
     const bool split = plan.kind == TR_PLAN_SPLIT;

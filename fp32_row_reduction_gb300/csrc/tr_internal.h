@@ -40,6 +40,7 @@ struct RowArgs {
     int r_vec;             // r rows have the same 16-byte phase as x rows
     int h_vec;             // h rows have the same 16-byte phase as x rows
     float* out2;           // row min/max: the maxima (loss receives the minima)
+    int pf_ctas;           // wave plans: CTAs below this index prefetch the norm parameters into L1
 };
 
 // Testing modes (tr_debug_force_wait_timeout), a bit mask in RowArgs::debug_flags:

@@ -134,6 +134,9 @@ tr_device_desc gb300_desc() {
 size_t plan_dynamic_smem(const tr_plan& p, int64_t cols) {
     if (p.kind == TR_PLAN_SPLIT) return static_cast<size_t>(p.vec_slots) * p.block_threads * 16;
     if (p.kind == TR_PLAN_SEGMENTS) return kSegSmem;
+    // a LayerNorm wave CTA stages its weight and bias quads: 2 x 256 K x 16 bytes
+    if (p.kind == TR_PLAN_WAVE && base_op(p.op) == TR_OP_LAYERNORM)
+        return static_cast<size_t>(2) * p.vec_slots * kWaveThreads * 16;
     if (p.kind == TR_PLAN_ORDERED && p.cluster_ctas == kOtClusterCtas) return ot_cluster_smem(cols);
     if (p.kind == TR_PLAN_ROWS && (p.flags & TR_PLAN_FLAG_PARAMS_IN_SHARED))
         return static_cast<size_t>(cols) * 4 * (base_op(p.op) == TR_OP_LAYERNORM ? 2 : 1);
@@ -430,8 +433,12 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     const double hbm_bytes = alg + (l2_fits ? 0.0 : reread);
     // weights/biases come from L2 once per row (once per CTA when held in registers)
     const double param_bytes = op == TR_OP_RMSNORM ? 4.0 * cols : op == TR_OP_LAYERNORM ? 8.0 * cols : 0.0;
-    // (a wave plan's CTAs find them in their SM's L1 after the first one: one L2 read per SM)
-    const double param_reads = (p.flags & (TR_PLAN_FLAG_PARAMS_IN_REGISTERS | TR_PLAN_FLAG_PARAMS_IN_SHARED))
+    // (a wave plan's CTAs find them in their SM's L1 after the first one: one L2 read per
+    // SM; a LayerNorm wave CTA copies them into its shared memory as it starts, one copy
+    // per CTA issued ahead of its rows, which the row reads hide: not counted)
+    const bool wave_staged = p.kind == TR_PLAN_WAVE && op == TR_OP_LAYERNORM;
+    const double param_reads = wave_staged ? 0.0
+                               : (p.flags & (TR_PLAN_FLAG_PARAMS_IN_REGISTERS | TR_PLAN_FLAG_PARAMS_IN_SHARED))
                                    ? static_cast<double>(p.grid_ctas)
                                : p.kind == TR_PLAN_WAVE ? std::min<double>(static_cast<double>(p.grid_ctas), d.sm_count)
                                                         : static_cast<double>(rows);

@@ -84,6 +84,32 @@ __device__ __forceinline__ float quad_top(float4 l) {
     return Rd::f(Rd::f(l.x, l.y), Rd::f(l.z, l.w));
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async: no register is held
+// while it is in flight, and the later shared-memory reads do not queue behind
+// the row loads in the SM's global-load path).
+__device__ __forceinline__ void cp_async16(void* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// LayerNorm's parameter staging: the weight quads t + 256 j of the row in
+// psm[t + 256 j], the bias quads in psm[256 K + t + 256 j]; each thread copies
+// exactly the quads its own epilogue reads, so a thread's wait for its own
+// copies is all the synchronisation there is.
+template <int K>
+__device__ __forceinline__ void stage_params(const RowArgs& a, float4* psm) {
+    const int t = threadIdx.x, nvec = a.cols >> 2;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const int q = t + kThreads * j;
+        if (q >= nvec) continue;
+        if (a.has_w) cp_async16(&psm[q], a.w + 4 * q);
+        if (a.has_b) cp_async16(&psm[K * kThreads + q], a.b + 4 * q);
+    }
+    cp_async_commit();
+}
+
 __device__ __forceinline__ float4 param4(const float* p, bool vec) {
     if (vec) return ld_param4(p);
     return make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
@@ -142,7 +168,8 @@ __device__ __forceinline__ float2 sq_acc(float2 acc, float4 v) {
 // the group's trees use part[tb], part[tb ^ 1], ... alternately, continuing
 // from the previous group (the caller passes the next block index in tb).
 template <int OP, bool ORD, int K, int R>
-__device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float (*part)[R][8], int& tb) {
+__device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float (*part)[R][8], const float4* psm,
+                                           int& tb) {
     using Add = typename std::conditional<ORD, AddO, AddU>::type;
     const int t = threadIdx.x;
     const int nvec = a.cols >> 2;
@@ -159,6 +186,21 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
         const float* xr = a.x + row * a.cols + 4 * t;
 #pragma unroll
         for (int j = 0; j < K; ++j) v[r][j] = okj[j] ? ld_stream4(xr + 4 * kThreads * j) : make_float4(kId, kId, kId, kId);
+    }
+    if constexpr (OP == OP_RMSNORM) {
+        // The epilogue's weight quads, into L1 while the rows load: by the
+        // first CTA on each SM (the block scheduler gives CTAs 0 .. SMs - 1 one
+        // SM each); the SM's later CTAs then find them in L1. One prefetch per
+        // 128-byte line: from the thread whose quad starts the line, and from
+        // thread 0 (a vector need not start on a line).
+        if (blockIdx.x < a.pf_ctas) {
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                if (!okj[j]) continue;
+                const int c = 4 * (t + kThreads * j);
+                if (a.has_w && (t == 0 || (reinterpret_cast<uintptr_t>(a.w + c) & 127) < 16)) prefetch_l1(a.w + c);
+            }
+        }
     }
     const float n = a.cols_f;
 
@@ -329,13 +371,13 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
         for (int r = 0; r < R; ++r)
             sc[r] = ORD ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q[r], n), a.eps)))
                         : rsqrtf(fmaf(q[r], a.inv_cols, a.eps));
-        const bool wv = a.has_w && aligned16(a.w), bv = a.has_b && aligned16(a.b);
+        cp_async_wait_all();  // this thread's own parameter quads (copied at entry)
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             if (!okj[j]) continue;
             const int c = 4 * (t + kThreads * j);
-            const float4 w = a.has_w ? param4(a.w + c, wv) : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-            const float4 b = a.has_b ? param4(a.b + c, bv) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            const float4 w = a.has_w ? psm[t + kThreads * j] : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+            const float4 b = a.has_b ? psm[K * kThreads + t + kThreads * j] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 if (row0 + r >= a.rows) break;
@@ -359,8 +401,18 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
 template <int OP, bool ORD, int K, int R>
 __global__ void __launch_bounds__(kThreads, min_blocks<K, R>()) wave_kernel(const RowArgs a) {
     __shared__ __align__(16) float part[2][R][8];
+    // LayerNorm: its weight and bias quads, 2 x 256 K of them (dynamic shared memory)
+    extern __shared__ __align__(16) float4 psm[];
     int tb = 0;
     pdl_enter();
+    if constexpr (OP == OP_LAYERNORM) {
+        // Every CTA copies the weight and bias quads its threads will use into
+        // shared memory before it requests its rows. Read from global memory in
+        // the epilogue, they would wait behind the other CTAs' row loads still
+        // outstanding on the SM, even as L1 or L2 hits; from shared memory they
+        // are there when the statistics are, and the SM's stores start early.
+        stage_params<K>(a, psm);
+    }
     if constexpr (OP != OP_SOFTMAX) {
         // The norms read their weight (and bias) quads only in the epilogue, and
         // in a stream of launches those vectors have usually left L2, so the
@@ -381,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks<K, R>()) wave_kernel(cons
             }
         }
     }
-    for (int64_t g = blockIdx.x; g * R < a.rows; g += gridDim.x) wave_group<OP, ORD, K, R>(a, g * R, part, tb);
+    for (int64_t g = blockIdx.x; g * R < a.rows; g += gridDim.x) wave_group<OP, ORD, K, R>(a, g * R, part, psm, tb);
 }
 
 }  // namespace wave
