@@ -64,6 +64,20 @@ const bool g_pdl = [] {
 }();
 constexpr long long kWaitNs = 2000000000LL;  // a bounded device wait gives up after 2 s
 
+// The start delay per launch rank of a wave plan (see the wave kernel): the
+// time the device's HBM takes to deliver one rank's rows (SMs x rows_per_cta
+// rows), scaled by kWaveStagger (measured at 768 x 6144: 0.8-1.0 of it gave
+// 0.2-0.4 us per launch, 1.3 and more lost), for grids of more than one rank
+// that are resident in one wave; 0 (no delay) otherwise.
+constexpr double kWaveStagger = 0.95;
+int wave_stagger_ns(const tr_device_desc& d, const tr_plan& p, int64_t cols) {
+    if (p.kind != TR_PLAN_WAVE || d.sm_count < 1 || d.hbm_gbs <= 0.0) return 0;
+    const int64_t resident = p.resident_ctas > 0 ? p.resident_ctas : static_cast<int64_t>(p.ctas_per_sm) * d.sm_count;
+    if (p.grid_ctas <= d.sm_count || p.grid_ctas > resident) return 0;
+    const double rank_bytes = static_cast<double>(d.sm_count) * p.rows_per_cta * static_cast<double>(cols) * 4.0;
+    return static_cast<int>(std::min(4000.0, kWaveStagger * rank_bytes / d.hbm_gbs));  // GB/s = bytes per ns
+}
+
 // Allow a kernel the full dynamic shared memory budget (once per kernel and
 // device), less what its static shared memory takes of the per-CTA limit.
 bool opt_in_smem(DeviceState& st, const void* fn) {
@@ -307,6 +321,7 @@ tr_status run(Call& c, cudaStream_t stream) {
     a.wait_ns = kWaitNs;
     a.debug_flags = g_debug_flags;
     a.pf_ctas = split_dev->desc.sm_count;  // about one CTA per SM: the first the block scheduler places there
+    a.stagger_ns = wave_stagger_ns(split_dev->desc, plan, a.cols);
     a.nbuf = (plan.kind == TR_PLAN_STAGED || plan.kind == TR_PLAN_ORDERED_STAGED) ? plan.rows_per_cta : 0;
     a.slot_floats = staged_slot_floats(a.cols);
     const bool split = plan.kind == TR_PLAN_SPLIT;

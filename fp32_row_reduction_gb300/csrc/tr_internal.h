@@ -40,7 +40,8 @@ struct RowArgs {
     int r_vec;             // r rows have the same 16-byte phase as x rows
     int h_vec;             // h rows have the same 16-byte phase as x rows
     float* out2;           // row min/max: the maxima (loss receives the minima)
-    int pf_ctas;           // wave plans: CTAs below this index prefetch the norm parameters into L1
+    int pf_ctas;           // wave plans: the SM count (CTAs below it prefetch the norm parameters into L1)
+    int stagger_ns;        // wave plans: a CTA of launch rank k = blockIdx / pf_ctas starts k x this late
 };
 
 // Testing modes (tr_debug_force_wait_timeout), a bit mask in RowArgs::debug_flags:

@@ -433,6 +433,28 @@ __global__ void __launch_bounds__(kThreads, min_blocks<K, R>()) wave_kernel(cons
             }
         }
     }
+    // Staggered start. The block scheduler gives CTAs 0 .. SMs - 1 one SM each,
+    // the next SMs CTAs one more each, and so on: CTA b is of launch rank
+    // k = b / SMs. Issued all at once, every CTA's loads would be served
+    // interleaved and land together at the end of the read phase, and all
+    // epilogues would follow it at once, each SM storing its five or six rows
+    // while DRAM idles. A CTA of rank k instead requests its rows k x
+    // stagger_ns late, about the time DRAM takes to serve one rank: the ranks'
+    // rows land one after another, and each rank's reductions and stores run
+    // while the next ranks' rows stream in. (Host-set for grids that are
+    // resident in one wave; the wait is one thread's bounded sleep on the
+    // global timer, the others wait at the barrier.)
+    if (a.stagger_ns > 0) {
+        const unsigned rank = blockIdx.x / static_cast<unsigned>(a.pf_ctas);
+        if (rank > 0) {
+            if (threadIdx.x == 0) {
+                const unsigned long long t0 = global_ns();
+                const unsigned long long d = static_cast<unsigned long long>(rank) * a.stagger_ns;
+                while (global_ns() - t0 < d) __nanosleep(64);
+            }
+            __syncthreads();
+        }
+    }
     for (int64_t g = blockIdx.x; g * R < a.rows; g += gridDim.x) wave_group<OP, ORD, K, R>(a, g * R, part, psm, tb);
 }
 
