@@ -3,15 +3,16 @@
 // A row is cut into C contiguous segments, one per CTA (C <= 32), and all
 // rows * C CTAs are resident at once (cooperative launch), so a 16-row problem
 // can use every SM instead of one cluster of at most 16 CTAs per row. Each CTA:
-//   1. copies the first part of its segment (up to its shared-memory share)
-//      into shared memory with one bulk asynchronous copy and, while the copy
-//      lands, streams the rest of the segment (the overflow) for statistics;
+//   1. streams its whole segment through registers once, two chunks in
+//      flight per thread, folding each chunk into its statistic as it lands;
+//      the first part of the segment (up to its shared-memory share) is also
+//      kept, raw, in shared memory;
 //   2. reduces its segment to one partial statistic (softmax: the (max, sum
 //      of exp) pair; RMSNorm: the sum of squares; LayerNorm: Chan moments),
 //      publishes it to a global workspace and arrives on the row's counter;
 //   3. waits (bounded in time) until the C segments of its row have arrived,
 //      merges the C partials in a fixed order, and writes its segment: the
-//      cached part from shared memory, the overflow re-read from L2.
+//      kept part from shared memory, the rest (the overflow) re-read from L2.
 // This is the combine of "TIRx Metal reduction lowering" §4.2 (cooperative
 // striping) one level up: the per-row partial array lives in global memory
 // instead of on-chip memory, and a per-row arrival counter replaces the
@@ -27,8 +28,9 @@
 namespace tr {
 
 constexpr int kSplitU = 4;  // float4 per thread per streamed chunk
-// A segment that aborted (its copy wait gave up) arrives with this weight on
-// its row's arrival word, whose low 16 bits count arrivals (at most 32).
+// A CTA that aborted before it arrived (the segments plan: its copy wait gave
+// up) arrives with this weight on the arrival word, whose low 16 bits count
+// arrivals.
 constexpr unsigned kSplitAbortUnit = 1u << 16;
 
 __device__ __forceinline__ float4 pack(float v) { return make_float4(v, 0.0f, 0.0f, 0.0f); }
@@ -93,51 +95,6 @@ __device__ __forceinline__ SplitStat<OP> fold_one(SplitStat<OP> st, float x) {
         return fmaf(x, x, st);
     } else {
         return mo_merge(st, Moments{1.0f, x, 0.0f});
-    }
-}
-
-// Statistic of this thread's share of the cached part: slots t, t+T, ... < n.
-// Softmax replaces each cached element by 2^(x*log2e - off), off = RN(ml*log2e)
-// for the thread's own maximum ml (0 when ml = -inf), and returns ml in `ml`.
-template <int OP>
-__device__ __forceinline__ SplitStat<OP> fold_cached(float4* cache, int n, int t, int T, float& ml) {
-    if constexpr (OP == OP_SOFTMAX) {
-        ml = MaxOp::id();
-        for (int i = t; i < n; i += T) ml = fmaxf(ml, max4(cache[i]));
-        const float off = ml == MaxOp::id() ? 0.0f : mb_of(ml);
-        float s = 0.0f;
-        for (int i = t; i < n; i += T) {
-            float4 c = cache[i];
-            c.x = ex2(fmaf(c.x, kL2E, -off));
-            c.y = ex2(fmaf(c.y, kL2E, -off));
-            c.z = ex2(fmaf(c.z, kL2E, -off));
-            c.w = ex2(fmaf(c.w, kL2E, -off));
-            cache[i] = c;
-            s += sum4(c);
-        }
-        return MaxSum{ml, s};
-    } else if constexpr (OP == OP_RMSNORM) {
-        float st = 0.0f;
-        for (int i = t; i < n; i += T) {
-            const float4 c = cache[i];
-            st = fmaf(c.x, c.x, fmaf(c.y, c.y, fmaf(c.z, c.z, fmaf(c.w, c.w, st))));
-        }
-        return st;
-    } else {
-        float cnt = 0.0f, sm = 0.0f;
-        for (int i = t; i < n; i += T) {
-            cnt += 4.0f;
-            sm += sum4(cache[i]);
-        }
-        if (cnt == 0.0f) return Moments{0.0f, 0.0f, 0.0f};
-        const float mu = __fdiv_rn(sm, cnt);
-        float m2 = 0.0f;
-        for (int i = t; i < n; i += T) {
-            const float4 c = cache[i];
-            const float dx = c.x - mu, dy = c.y - mu, dz = c.z - mu, dw = c.w - mu;
-            m2 = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, fmaf(dw, dw, m2))));
-        }
-        return Moments{cnt, mu, m2};
     }
 }
 
@@ -209,7 +166,6 @@ template <int OP>
 __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     using Stat = SplitStat<OP>;
     extern __shared__ __align__(16) float4 cache[];
-    __shared__ __align__(8) uint64_t bar;
     __shared__ float4 part[2][32];
     __shared__ volatile int s_abort;
     const int C = a.C;
@@ -221,45 +177,53 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     const RowGeom g = row_geom(xr, a.cols);
     const int per = (g.nvec + C - 1) / C;
     const int v0 = min(g.nvec, seg * per), v1 = min(g.nvec, v0 + per);
-    const int nsm = min(v1 - v0, a.slot_floats / 4);  // slots [v0, v0 + nsm) are cached
+    const int nsm = min(v1 - v0, a.slot_floats / 4);  // slots [v0, v0 + nsm) are kept in shared memory
     const float* xb = xr + g.head;
     float* yb = yr + g.head;
     const bool own_h = seg == 0 && t < g.head;
     const bool own_t = seg == C - 1 && t < g.tail;
     const int ti = g.head + 4 * g.nvec + t;
-    if (t == 0) {
-        mbar_init(&bar, 1);
-        s_abort = 0;
-        fence_barrier_init();
-    }
+    if (t == 0) s_abort = 0;
     __syncthreads();
     pdl_enter();
-    // L2 policies: the streamed overflow is read again after the exchange (keep);
-    // the re-read and the outputs are on their last use (drop)
+    // L2 policies: the overflow is read again after the exchange (keep); the
+    // kept part, the re-read and the outputs are on their last use (drop)
     uint64_t keep, drop;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(drop));
-    if (t == 0) {
-        if (nsm > 0) {
-            mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nsm) * 16u);
-            bulk_g2s_pol(cache, xb + 4 * v0, static_cast<uint32_t>(nsm) * 16u, &bar, drop);  // read once, into smem
-        } else {
-            mbar_arrive(&bar);
-        }
-    }
 
-    // ---- 1. statistics: the overflow is streamed while the copy lands
+    // ---- 1. statistics: every slot streams through registers once, the next
+    // chunk's loads in flight while this one is folded. (A bulk copy of the
+    // kept part landed together with the streamed loads, at the end of the
+    // read phase, and its fold from shared memory then ran after the reads.)
     Stat st = identity_of<Stat>();
-    int i = v0 + nsm + t;
-    for (; i + (kSplitU - 1) * T < v1; i += kSplitU * T) {
-        float4 c[kSplitU];
+    const int vk = v0 + nsm;  // slots below vk are kept
+    auto load_chunk = [&](int base, float4 (&c)[kSplitU]) {
 #pragma unroll
-        for (int u = 0; u < kSplitU; ++u) c[u] = ld_pol4(xb + 4 * (i + u * T), keep);
-        st = fold_chunk<OP, kSplitU>(st, c);
+        for (int u = 0; u < kSplitU; ++u) c[u] = ld_pol4(xb + 4 * (base + u * T), base + u * T < vk ? drop : keep);
+    };
+    int i = v0 + t;
+    bool have = i + (kSplitU - 1) * T < v1;
+    float4 cur[kSplitU];
+    if (have) load_chunk(i, cur);
+    while (have) {
+        const int inext = i + kSplitU * T;
+        const bool hnext = inext + (kSplitU - 1) * T < v1;
+        float4 nxt[kSplitU];
+        if (hnext) load_chunk(inext, nxt);
+#pragma unroll
+        for (int u = 0; u < kSplitU; ++u)
+            if (i + u * T < vk) cache[i + u * T - v0] = cur[u];
+        st = fold_chunk<OP, kSplitU>(st, cur);
+#pragma unroll
+        for (int u = 0; u < kSplitU; ++u) cur[u] = nxt[u];
+        i = inext;
+        have = hnext;
     }
     for (; i < v1; i += T) {
         float4 c[kSplitU];
-        c[0] = ld_pol4(xb + 4 * i, keep);
+        c[0] = ld_pol4(xb + 4 * i, i < vk ? drop : keep);
+        if (i < vk) cache[i - v0] = c[0];
         st = fold_chunk<OP, 1>(st, c);
     }
     float hv = 0.0f, tv = 0.0f;
@@ -271,15 +235,6 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
         tv = ld_stream1(xr + ti);
         st = fold_one<OP>(st, tv);
     }
-    // (testing: the copy wait of each row's first segment gives up, and the
-    // other segments must learn of it through the arrival word)
-    const bool copied =
-        mbar_wait_bounded(&bar, 0, a.wait_ns, a.err, (a.debug_flags & kDebugExpireCopies) && seg == 0);
-    if (!copied) s_abort = 1;
-    float ml = 0.0f;
-    // a segment whose copy has not landed is not read: its partial is marked
-    // aborted below and no CTA of the row merges it
-    if (copied) st = split_merge(st, fold_cached<OP>(cache, nsm, t, T, ml));
     RowPos p;
     p.w = t;
     p.W = T;
@@ -291,26 +246,18 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     st = cta_row_merge<Stat, 32>(st, p, part, buf);  // every thread holds the CTA's partial
 
     // ---- 2. publish the partial; warp 0 waits for the row's C partials and
-    // merges them in lane order (the same in every CTA of the row). The row's
-    // arrival word counts arrivals in its low 16 bits and aborted segments
-    // (whose copy wait gave up) from bit 16: one aborted segment makes every
-    // CTA of the row stop waiting and skip the epilogue.
+    // merges them in lane order (the same in every CTA of the row)
     __shared__ float4 s_row;
     if (t == 0) {
         a.sp_part[blockIdx.x] = pack(st);
-        red_add_release(a.sp_arrive + row, s_abort ? 1u + kSplitAbortUnit : 1u);
+        red_add_release(a.sp_arrive + row, 1u);
     }
     if (t < 32) {
         const unsigned long long t0 = global_ns();
         // (testing: every CTA's wait gives up before it looks)
-        bool late = a.debug_flags & kDebugExpirePeers, aborted = false;
+        bool late = a.debug_flags & kDebugExpirePeers;
         while (!late) {
-            const unsigned v = ld_acquire(a.sp_arrive + row);
-            if (v >= kSplitAbortUnit) {
-                aborted = true;
-                break;
-            }
-            if (v >= static_cast<unsigned>(C)) break;
+            if (ld_acquire(a.sp_arrive + row) >= static_cast<unsigned>(C)) break;
             if (static_cast<long long>(global_ns() - t0) > a.wait_ns) {
                 late = true;
                 break;
@@ -318,9 +265,10 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
             __nanosleep(20);
         }
         late = __any_sync(kFull, late);
-        aborted = __any_sync(kFull, aborted);
-        if (late && t == 0) atomicOr(a.err, kErrWaitTimeout);
-        if ((late || aborted) && t == 0) s_abort = 1;
+        if (late && t == 0) {
+            atomicOr(a.err, kErrWaitTimeout);
+            s_abort = 1;
+        }
         const Stat v = warp_merge<Stat, 32>(p.lane < C ? unpack<Stat>(ld_relaxed4(a.sp_part + row * C + p.lane))
                                                        : identity_of<Stat>());
         if (t == 0) s_row = pack(v);
@@ -338,19 +286,14 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     };
     if (s_abort) {
         depart();
-        if (t == 0 && !copied) mbar_wait_bounded(&bar, 0, a.wait_ns, nullptr);  // drain the copy
         return;
     }
 
     // ---- 4. epilogue: the overflow re-read first (most recently in L2), then the cached part
-    float scale, shift = 0.0f, mb = 0.0f, cscale = 0.0f;
+    float scale, shift = 0.0f, mb = 0.0f;
     if constexpr (OP == OP_SOFTMAX) {
         mb = mb_of(rs.m);
         scale = 1.0f / rs.s;
-        // cached values are 2^(x*log2e - off(ml)); ml = -inf caches only zeros
-        // (or NaN), and a row whose maximum is -inf gives NaN as in every plan
-        cscale = ex2((ml == MaxOp::id() ? 0.0f : mb_of(ml)) - mb) * scale;
-        if (ml == MaxOp::id() && rs.m != MaxOp::id()) cscale = 0.0f;
     } else if constexpr (OP == OP_RMSNORM) {
         scale = rsqrtf(fmaf(rs, a.inv_cols, a.eps));
     } else {
@@ -442,10 +385,7 @@ __global__ void __launch_bounds__(1024) split_kernel(const RowArgs a) {
     }
     for (; i < v1; i += T) st_out_pol(yb + 4 * i, params(out4(ld_pol4(xb + 4 * i, drop)), i), a.y_vec, drop);
     if constexpr (OP == OP_SOFTMAX) {
-        for (int j = t; j < nsm; j += T) {
-            const float4 c = cache[j];
-            st_out_pol(yb + 4 * (v0 + j), make_float4(c.x * cscale, c.y * cscale, c.z * cscale, c.w * cscale), a.y_vec, drop);
-        }
+        for (int j = t; j < nsm; j += T) st_out_pol(yb + 4 * (v0 + j), out4(cache[j]), a.y_vec, drop);
     } else {
         // kSplitU slots at a time, so that their weight/bias loads are in flight
         // together; whole blocks of T slots from the per-row rotation, as above
