@@ -29,7 +29,7 @@ EXTRA = {"k_ordered.cu": _EXACT, "k_wave_ordered.cu": _EXACT}
 SOURCES = ["tr_api.cu", "tr_plan.cpp", "k_softmax.cu", "k_rmsnorm.cu", "k_layernorm.cu", "k_xent.cu",
            "k_ordered.cu", "tr_noalloc.cu", "k_add_rmsnorm.cu", "k_add_layernorm.cu",
            "k_reduce.cu", "k_axis.cu", "k_backward.cu", "k_fold.cu", "k_ot_cluster.cu", "k_xent_bwd.cu",
-           "k_wave.cu", "k_wave_ordered.cu", "k_segments.cu"]
+           "k_wave.cu", "k_wave_ordered.cu", "k_segments.cu", "k_bwd_wave.cu"]
 HEADERS = ["tr_device.cuh", "tr_row_kernels.cuh", "tr_split_kernels.cuh", "tr_dispatch.cuh", "tr_internal.h",
            "tr_plan.h", "tr_ot.cuh", "tr_wave_kernels.cuh", "tr_segments_kernels.cuh"]
 

@@ -21,6 +21,7 @@
 // per-element terms, recomputed from x, dy and those statistics, finishes them
 // (ordered: OT-1024 over each column's terms, as every ordered column sum).
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <stdint.h>
 
 #include "tr_device.cuh"
@@ -389,11 +390,26 @@ __global__ void __launch_bounds__(kOrderedThreads) bw_kernel(const BwArgs a) {
 template <int OP, int K, bool O>
 cudaError_t launch_k(const BwArgs& a, int ctas, cudaStream_t stream) {
     const size_t smem = K * bw_smem_per_slot<OP>();
-    if (smem > 40 * 1024) {  // beyond the default 48 KB once the static shared memory is added
-        const cudaError_t e = cudaFuncSetAttribute(bw_kernel<OP, K, O>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(smem));
+    // (once per instantiation) the shared-memory opt-in and the CTAs the device
+    // holds at once: a grid of more rows than that would run a partial second
+    // wave, while resident CTAs that loop over their rows stage each next row
+    // during the current one's passes
+    static int resident = 0;
+    if (resident == 0) {
+        if (smem > 40 * 1024) {  // beyond the default 48 KB once the static shared memory is added
+            const cudaError_t e = cudaFuncSetAttribute(bw_kernel<OP, K, O>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+        }
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bw_kernel<OP, K, O>, kOrderedThreads, smem);
         if (e != cudaSuccess) return e;
+        resident = std::max(1, per_sm * sms);
     }
+    if (K > 0) ctas = std::min(ctas, resident);
     bw_kernel<OP, K, O><<<dim3(static_cast<unsigned>(ctas)), kOrderedThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }

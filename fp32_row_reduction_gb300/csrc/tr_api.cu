@@ -743,7 +743,11 @@ tr_status tr_norm_backward_workspace_bytes(int64_t rows, int64_t cols, size_t* b
     if (!bytes) return fail(TR_ERR_INVALID_ARG, "bytes must not be null");
     tr_status s = validate_common(rows, cols, TR_ORDER_UNORDERED_TREE);
     if (s != TR_OK) return s;
-    *bytes = static_cast<size_t>(rows) * 2 * sizeof(float);  // two statistics per row
+    // two statistics per row, or the one-pass kernel's column partials: two
+    // vectors of ceil(rows / 4) x cols floats
+    const size_t stats = static_cast<size_t>(rows) * 2 * sizeof(float);
+    const size_t quads = bwn_slots(cols) > 0 ? static_cast<size_t>((rows + 3) / 4) * static_cast<size_t>(cols) * 2 * sizeof(float) : 0;
+    *bytes = std::max(stats, quads);
     return TR_OK;
 }
 
@@ -760,6 +764,25 @@ static tr_status term_sum(int term, const BwArgs& b, float* out, float* out2, tr
 static tr_status bw_run(int op, BwArgs a, tr_order order, float* dw, float* db, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
     if (a.rows == 0) return TR_OK;
+    // the norms' one-pass kernel: aligned rows of 1024 .. 8192 columns (and, for
+    // the ordered column sums, at most 1024 rows: one row per tree leaf)
+    const bool one_pass = (op == BW_RMSNORM || op == BW_LAYERNORM) && bwn_slots(a.cols) > 0 &&
+                          !(order == TR_ORDER_ORDERED_TREE && a.rows > 1024) && !misaligned(a.x, 16) &&
+                          !misaligned(a.dy, 16) && !misaligned(a.dx, 16) && !misaligned(a.w, 16);
+    if (one_pass) {
+        float* partials = nullptr;
+        if (dw || db) {
+            size_t need = 0;  // the contract: at least tr_norm_backward_workspace_bytes
+            tr_norm_backward_workspace_bytes(a.rows, a.cols, &need);
+            if (!ws || ws_bytes < need)
+                return fail(TR_ERR_INVALID_ARG,
+                            "the workspace is missing or smaller than tr_norm_backward_workspace_bytes");
+            partials = static_cast<float*>(ws);
+        }
+        const cudaError_t e = launch_backward_wave(op, order == TR_ORDER_ORDERED_TREE, a, dw, db, partials, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+        return TR_OK;
+    }
     if (dw || db) {
         const size_t need = static_cast<size_t>(a.rows) * 2 * sizeof(float);
         if (!ws || ws_bytes < need)

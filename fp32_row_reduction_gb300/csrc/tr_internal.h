@@ -232,6 +232,8 @@ struct BwArgs {
     int cols;
     float eps;
     unsigned* err;           // device error word (kernels that check their own accesses record here)
+    int sms;                 // one-pass norm backward: the SM count (launch rank = blockIdx / sms)
+    int stagger_ns;          // one-pass norm backward: a CTA of launch rank k starts k x this late
 };
 
 // Device error word bit: a kernel's own access check skipped a bad access
@@ -240,6 +242,14 @@ constexpr unsigned kErrAccessCheck = 2u;
 
 // Launch backward op `op` (BwOp) with K cached quads per thread (0: re-read) on G CTAs.
 cudaError_t launch_backward(int op, bool ordered, int slots, const BwArgs& a, int ctas, cudaStream_t stream);
+// The one-pass norm backward (RMSNorm, LayerNorm) of aligned rows of 1024 .. 8192
+// columns: quads per thread (2, 4, 6, 8), 0 where it does not apply.
+int bwn_slots(int64_t cols);
+// dx, and the column gradients asked for (dw: dw or dgamma; db: dbeta) through
+// `partials`, ceil(rows / 4) x cols floats per gradient vector (both blocks for
+// LayerNorm). The ordered policy needs rows <= 1024.
+cudaError_t launch_backward_wave(int op, bool ordered, const BwArgs& a, float* dw, float* db, float* partials,
+                                 cudaStream_t stream);
 // Unordered cross-entropy backward of rows longer than the cached kernels take
 // (more than 8192 columns): a 1024-thread CTA per row, the row read twice.
 cudaError_t launch_xent_backward_stream(const BwArgs& a, cudaStream_t stream);

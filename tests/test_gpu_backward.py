@@ -29,7 +29,11 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 U = 2.0 ** -24
 SHAPES = [(1, 1), (5, 3), (4, 127), (17, 257), (3, 1024), (7, 1025), (37, 1537), (2, 4096), (9, 6144),
-          (3, 8193), (2, 20000), (2, 60000), (1100, 64)]
+          (3, 8193), (2, 20000), (2, 60000), (1100, 64),
+          # the norms' one-pass kernel (aligned rows of 1024 .. 8192 columns): row counts
+          # 1, 2, 3 past a leaf quad, the ordered limit of 1024 rows, and 1030 rows (the
+          # ordered policy then takes the two-pass kernels; the unordered one more than 256 quads)
+          (5, 2048), (6, 3000), (13, 8192), (1024, 1028), (1030, 1024)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -195,7 +199,8 @@ def test_dx_only_and_workspace_errors():
     DX, DW = torch.empty_like(X), torch.empty(3000, device=DEV)
     s = torch.cuda.current_stream().cuda_stream
     need = tr.norm_backward_workspace_bytes(6, 3000)
-    assert need == 6 * 2 * 4                                                        # two statistics per row
+    assert need == 2 * 3000 * 2 * 4            # the one-pass kernel's partials: 2 leaf quads x 3000 columns x 2
+    assert tr.norm_backward_workspace_bytes(6, 3001) == 6 * 2 * 4                 # two statistics per row
     small = torch.empty(need, dtype=torch.uint8, device=DEV)
     assert lib.tr_rmsnorm_backward_f32(X.data_ptr(), W.data_ptr(), DY.data_ptr(), DX.data_ptr(), DW.data_ptr(), 6, 3000,
                                        1e-5, 0, small.data_ptr(), need - 4, s) == tr.TR_ERR_INVALID_ARG
