@@ -248,8 +248,12 @@ tr_status tr_row_minmax_f32(const float* x, float* out_min, float* out_max, int6
  * written above, bit-identical to the CPU emulation; unordered results meet a
  * rounding bound. The column gradients need a caller-owned, 16-byte-aligned
  * device workspace of at least tr_norm_backward_workspace_bytes(rows, cols)
- * bytes (two statistics per row; none when dw, dgamma and dbeta are NULL);
- * they are column sums over the rows of their per-element terms, which may
+ * bytes (none when dw, dgamma and dbeta are NULL): two statistics per row, or,
+ * for rows of 1024 .. 8192 columns with cols % 4 == 0, the one-pass kernel's
+ * column partials, two vectors of ceil(rows / 4) x cols floats, whichever is
+ * larger. The norms take that one-pass kernel when x, dy, dx and the weight
+ * are 16-byte aligned (and, ordered, rows <= 1024); otherwise the column
+ * gradients are column sums over the rows of their per-element terms, which may
  * use the stream's library workspace, allocated on the first such call on the
  * stream, which therefore must not be captured. */
 tr_status tr_softmax_backward_f32(const float* y, const float* dy, float* dx, int64_t rows, int64_t cols,
