@@ -402,12 +402,34 @@ __global__ void __launch_bounds__(max_threads_res<OP, K, RES>(), min_blocks_res<
             if (a.has_b) bulk_g2s(sparams + (a.has_w ? a.cols : 0), a.b, bytes, &pbar);
         }
     }
+    // Packed rows of short stripes (G < 32 lanes, K <= 4): the norms' weight
+    // (and bias) quads are requested before the row. Requested after it, they
+    // would return behind the row loads that the SM's other CTAs still have
+    // in flight, even as L1 hits, and hold up the epilogue.
+    constexpr bool kParamsFirst = G < 32 && K <= 4 && !SP && !RES && OP != OP_SOFTMAX;
+    float4 wr[K], br[K];
+    if constexpr (kParamsFirst) {
+        const bool wv = a.has_w && aligned16(a.w + g.head);
+        const bool bv = a.has_b && aligned16(a.b + g.head);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const bool here = active && map.ok(j);
+            const int e = 4 * map.idx(j);
+            wr[j] = (a.has_w && here) ? ld_param(a.w + g.head + e, wv) : f4(1.0f);
+            br[j] = (OP == OP_LAYERNORM && a.has_b && here) ? ld_param(a.b + g.head + e, bv) : f4(0.0f);
+        }
+    }
     load_stripe<OP, K>(xr, g, map, active, p.w, own_h, own_t, v, hv, tv);
     if constexpr (RES) add_residual<K>(a, rr, g, map, active, p.w, own_h, own_t, v, hv, tv);
     RowsReducer<G> red{p, part, 0};
-    float4 none[K];
-    cached_epilogue<OP, K, false, SP>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red, none,
-                                      none, sp);
+    if constexpr (kParamsFirst) {
+        cached_epilogue<OP, K, true, false>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red,
+                                            wr, br, sp);
+    } else {
+        float4 none[K];
+        cached_epilogue<OP, K, false, SP>(a, a.y + rr * a.cols, g, v, hv, tv, own_h, own_t, active, p.w, map, red,
+                                          none, none, sp);
+    }
     // the weight copy has landed unless the epilogue's wait gave up: then wait
     // for it once more before the CTA's shared memory goes away
     if constexpr (SP)
