@@ -94,11 +94,11 @@ int reductions_of(int op) {
 // Fitted by coordinate descent (calibration/fit_cost_model.py) on GB300 plan
 // sweeps of calibration shapes DISJOINT from the benchmark workloads (the
 // shape lists are in calibration/sweep.py, the sweeps beside it), minimising
-// the mean time regret of the chosen plan (with the tie-break below): 6.1%
-// mean, 24.8% max over 69 cases. The benchmark shapes were then scored as a
-// held-out set with the constants frozen (the page's frozen held-out
-// protocol): 3.8% mean, 21.5% max over 27 cases. The clock is the datasheet
-// value.
+// the mean time regret of the chosen plan (with the tie-break below). On the
+// current sweeps (the kernels as they are now): 6.2% mean, 25.5% max over 69
+// calibration cases; the benchmark shapes, scored as a held-out set with the
+// constants frozen (the page's frozen held-out protocol): 4.7% mean, 20.5%
+// max over 27 cases. The clock is the datasheet value.
 const CostConstants kCostDefaults = {
     0.375,   // launch: launch and grid ramp beyond what the other terms cover
     3.3,     // latency: loaded DRAM round trip as seen by a CTA
