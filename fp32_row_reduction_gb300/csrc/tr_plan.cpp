@@ -389,6 +389,12 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
     if (p->kind == TR_PLAN_SPLIT && p->grid_ctas > res)
         return fail(TR_ERR_UNSUPPORTED, "a split plan's CTAs must all be resident at once (cooperative launch)");
     if (p->kind == TR_PLAN_STAGED || p->kind == TR_PLAN_ORDERED_STAGED) p->grid_ctas = std::min<int64_t>(rows, res);
+    // two-row wave plans whose rows outnumber the resident CTAs, but not twice
+    // over: every resident CTA, rows - res of them with two rows and the rest
+    // with one (the kernel maps them so), which spreads the rows evenly over
+    // the SMs (768 rows on 456 slots: 144 SMs of five rows and 8 of six,
+    // instead of 80 of six and 72 of four)
+    if (p->kind == TR_PLAN_WAVE && p->rows_per_cta == 2 && res < rows && 2 * res > rows) p->grid_ctas = res;
     if (p->kind == TR_PLAN_SEGMENTS) {
         // every resident CTA, at most one per SM; each owns a segment of every row
         p->grid_ctas = std::min<int64_t>(res, d.sm_count);

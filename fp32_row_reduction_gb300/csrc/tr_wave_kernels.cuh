@@ -164,11 +164,12 @@ __device__ __forceinline__ float2 sq_acc(float2 acc, float4 v) {
     return __ffma2_rn(hi2(v), hi2(v), acc);
 }
 
-// One group of R rows starting at row0. `part` holds two [R][8] slot blocks;
+// One group of nr <= R rows starting at row0 (rows r >= nr repeat row0 and
+// are not stored). `part` holds two [R][8] slot blocks;
 // the group's trees use part[tb], part[tb ^ 1], ... alternately, continuing
 // from the previous group (the caller passes the next block index in tb).
 template <int OP, bool ORD, int K, int R>
-__device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float (*part)[R][8], const float4* psm,
+__device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, int nr, float (*part)[R][8], const float4* psm,
                                            int& tb) {
     using Add = typename std::conditional<ORD, AddO, AddU>::type;
     const int t = threadIdx.x;
@@ -182,7 +183,7 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
     float4 v[R][K];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const int64_t row = min(row0 + r, a.rows - 1);  // rows past the end repeat the last (not stored)
+        const int64_t row = r < nr ? row0 + r : row0;  // (a repeated row is served by L2, not stored)
         const float* xr = a.x + row * a.cols + 4 * t;
 #pragma unroll
         for (int j = 0; j < K; ++j) v[r][j] = okj[j] ? ld_stream4(xr + 4 * kThreads * j) : make_float4(kId, kId, kId, kId);
@@ -282,7 +283,7 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
         tb ^= 1;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            if (row0 + r >= a.rows) break;
+            if (r >= nr) break;
             const float inv = ORD ? __fdiv_rn(1.0f, s[r]) : 1.0f / s[r];
             float* yr = a.y + (row0 + r) * a.cols + 4 * t;
 #pragma unroll
@@ -320,7 +321,7 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
             const float4 w = a.has_w ? param4(a.w + c, wv) : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                if (row0 + r >= a.rows) break;
+                if (r >= nr) break;
                 float4 o = mul4s(v[r][j], sc[r]);
                 if (ORD) {
                     if (a.has_w) o = mul4(o, w);
@@ -380,7 +381,7 @@ __device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, float
             const float4 b = a.has_b ? psm[K * kThreads + t + kThreads * j] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                if (row0 + r >= a.rows) break;
+                if (r >= nr) break;
                 float4 o = mul4s(sub4s(v[r][j], mu[r]), sc[r]);
                 if (ORD) {
                     if (a.has_w) o = a.has_b ? prod4_rn(o, w) : mul4(o, w);
@@ -455,7 +456,20 @@ __global__ void __launch_bounds__(kThreads, min_blocks<K, R>()) wave_kernel(cons
             __syncthreads();
         }
     }
-    for (int64_t g = blockIdx.x; g * R < a.rows; g += gridDim.x) wave_group<OP, ORD, K, R>(a, g * R, part, psm, tb);
+    if constexpr (R == 2) {
+        // One wave of every resident CTA (the selector's choice when the rows
+        // outnumber the CTAs the device holds but not twice over): CTAs
+        // 0 .. rows - G - 1 take two rows, the others one, so that an SM holds
+        // five or six rows rather than four or six.
+        const int64_t G = gridDim.x;
+        if (G < a.rows && 2 * G > a.rows) {
+            const int64_t pairs = a.rows - G, g = blockIdx.x;
+            wave_group<OP, ORD, K, R>(a, g < pairs ? 2 * g : pairs + g, g < pairs ? 2 : 1, part, psm, tb);
+            return;
+        }
+    }
+    for (int64_t g = blockIdx.x; g * R < a.rows; g += gridDim.x)
+        wave_group<OP, ORD, K, R>(a, g * R, a.rows - g * R < R ? static_cast<int>(a.rows - g * R) : R, part, psm, tb);
 }
 
 }  // namespace wave

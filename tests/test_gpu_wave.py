@@ -242,3 +242,32 @@ def test_wave_ordered_softmax_dense_exp_range(rows_per_cta):
     d = {"x": torch.from_numpy(x).to(DEV)}
     y = run_with(wave_plan("softmax", "ordered", cols, rows_per_cta), "softmax", d, "ordered").cpu().numpy()
     assert_bits(y, oracle.ot_softmax(x), "dense exp range")
+
+
+@pytest.mark.parametrize("order", ["unordered", "ordered"])
+@pytest.mark.parametrize("op", OPS)
+def test_wave_two_rows_balanced_over_every_resident_cta(op, order):
+    # rows between the resident CTAs (res) and twice as many: the grid is every
+    # resident CTA, rows - res of them with two rows and the rest with one
+    cols = 6000
+    p = wave_plan(op, order, cols, 2)
+    for extra in (1, 77, 1 << 20):
+        assert tr.tr_plan_override(p) == tr.TR_OK
+        try:
+            res = tr.tr_plan_describe(tr.OPS[op], 10, cols, 1 if order == "ordered" else 0).resident_ctas
+        finally:
+            tr.tr_plan_override(None)
+        rows = min(2 * res - 1, res + extra)
+        d = make(op, rows, cols, seed=rows)
+        y = run_with(p, op, d, order).cpu().numpy()
+        assert tr.tr_plan_override(p) == tr.TR_OK
+        try:
+            assert tr.tr_plan_describe(tr.OPS[op], rows, cols, 1 if order == "ordered" else 0).grid_ctas == res
+        finally:
+            tr.tr_plan_override(None)
+        h = host(d)
+        if order == "ordered":
+            assert_bits(y, emulated(op, h), f"{op} {rows}x{cols} balanced")
+        else:
+            assert_close(y, reference(op, h), f"{op} {rows}x{cols} balanced")
+

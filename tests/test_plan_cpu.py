@@ -46,12 +46,16 @@ def covers(p, cols):
 
 def check_wave(p, rows, cols, op):
     """A wave plan: 256 threads (8 warps) per CTA on 1 or 2 aligned rows of >= 1024
-    columns, vec_slots the smallest of 2/4/6/8 that covers the row, one CTA per rows_per_cta rows."""
+    columns, vec_slots the smallest of 2/4/6/8 that covers the row, one CTA per rows_per_cta rows
+    (two-row plans whose rows outnumber the resident CTAs, not twice over: every resident CTA)."""
     assert op in (0, 1, 2) and cols % 4 == 0 and cols >= 1024
     assert p.block_threads == 256 and p.warps_per_row == 8 and p.lanes_per_row == 32 and p.cluster_ctas == 1
     assert p.rows_per_cta in (1, 2) and p.flags == 0
     assert p.vec_slots == min(k for k in (2, 4, 6, 8) if 1024 * k >= cols)
-    assert p.grid_ctas == math.ceil(rows / p.rows_per_cta)
+    if p.rows_per_cta == 2 and p.resident_ctas < rows < 2 * p.resident_ctas:
+        assert p.grid_ctas == p.resident_ctas   # every resident CTA, rows - res of them with two rows
+    else:
+        assert p.grid_ctas == math.ceil(rows / p.rows_per_cta)
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
