@@ -156,7 +156,9 @@ int model_occupancy(const tr_device_desc& d, const tr_plan& p, size_t smem) {
             regs = (p.kind == TR_PLAN_ROWS && k == 6) ? 40 : 28 + 4 * k + (base_op(p.op) == TR_OP_LAYERNORM ? 4 : 0);
             break;
         case TR_PLAN_ORDERED_STAGED: regs = 40 + 4 * k; break;
-        case TR_PLAN_WAVE: regs = p.rows_per_cta == 1 ? std::max(32, 16 + 4 * k) : 30 + 8 * k; break;
+        case TR_PLAN_WAVE:
+            regs = p.rows_per_cta == 1 ? (k <= 2 ? 32 : std::max(40, 16 + 4 * k)) : (k <= 2 ? 40 : 30 + 8 * k);
+            break;
         case TR_PLAN_SEGMENTS: regs = 48 + 8 * k; break;
         case TR_PLAN_STREAM: regs = 64; break;
         case TR_PLAN_SPLIT: regs = 64; break;

@@ -38,9 +38,11 @@ constexpr int kThreads = 256;
 // Resident CTAs per SM each instantiation is compiled for (register budget of
 // 4 K R cached floats plus addresses and statistics): K = 6 gives 6, 3 and 2
 // CTAs for R = 1, 2, 3, i.e. 912 rows resident on 152 SMs in every case.
+// Smaller stripes also stop at six (40 registers): at eight (32) the norms'
+// epilogues spilled.
 template <int K, int R>
 constexpr int min_blocks() {
-    return K * R <= 4 ? 8 : K * R <= 6 ? 6 : K * R <= 8 ? 4 : K * R <= 12 ? 3 : K * R <= 18 ? 2 : 1;
+    return K * R <= 6 ? 6 : K * R <= 8 ? 4 : K * R <= 12 ? 3 : K * R <= 18 ? 2 : 1;
 }
 
 // Reducers. The ordered ones round every step; max is the hardware maxNum in
@@ -169,9 +171,10 @@ __device__ __forceinline__ float2 sq_acc(float2 acc, float4 v) {
 // the group's trees use part[tb], part[tb ^ 1], ... alternately, continuing
 // from the previous group (the caller passes the next block index in tb).
 template <int OP, bool ORD, int K, int R>
-__device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, int nr, float (*part)[R][8], const float4* psm,
-                                           int& tb) {
+__device__ __forceinline__ void wave_group(const RowArgs& a, int64_t row0, int nr_in, float (*part)[R][8],
+                                           const float4* psm, int& tb) {
     using Add = typename std::conditional<ORD, AddO, AddU>::type;
+    const int nr = R == 1 ? 1 : nr_in;  // (a constant for one-row groups)
     const int t = threadIdx.x;
     const int nvec = a.cols >> 2;
     // slots past the end of the row hold the reducer's identity (folded last,
