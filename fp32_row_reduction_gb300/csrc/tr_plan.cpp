@@ -767,12 +767,15 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
             // is slower than the split and cluster plans on most long-row shapes;
             // it runs only when a caller forces it)
             // few long rows: C co-resident CTAs per row, each caching its segment in
-            // shared memory (one CTA per SM with the whole budget, or two with half)
+            // shared memory (one CTA or two per SM, sharing the SM's shared memory
+            // less 32 KB, which stays L1: at 16 x 1048576
+            // two 106 KB caches ran 41.8 / 29.2 us (LayerNorm / softmax) against
+            // 39.9 / 27.1 us for two 88 KB ones)
             for (int C = 2; C <= kSplitMaxCtas && rows <= kSplitMaxRows && rows * C <= kSplitMaxParts; ++C)
                 for (int T : {256, 512, 1024}) {
                     const int64_t cover = ceil_div(ceil_div(n4, C), T);
-                    const int kfull = kStagedSmemBudget / (16 * T);
-                    const int khalf = (d.smem_per_sm / 2 - 1024 - kSplitStaticSmem) / (16 * T);
+                    const int kfull = std::min(kStagedSmemBudget, d.smem_per_sm - 32 * 1024 - 1024 - kSplitStaticSmem) / (16 * T);
+                    const int khalf = ((d.smem_per_sm - 32 * 1024) / 2 - 1024 - kSplitStaticSmem) / (16 * T);
                     int last = -1;
                     for (int kcap : {kfull, khalf}) {
                         const int k = static_cast<int>(std::min<int64_t>(cover, kcap));
