@@ -66,16 +66,17 @@ constexpr long long kWaitNs = 2000000000LL;  // a bounded device wait gives up a
 
 // The start delay per launch rank of a wave plan (see the wave kernel): the
 // time the device's HBM takes to deliver one rank's rows (SMs x rows_per_cta
-// rows), scaled by kWaveStagger (measured at 768 x 6144: 0.8-1.0 of it gave
-// 0.2-0.4 us per launch, 1.3 and more lost), for grids of more than one rank
-// that are resident in one wave; 0 (no delay) otherwise.
-constexpr double kWaveStagger = 0.95;
+// rows), scaled per operator (against 6800 GB/s: 0.92, and 1.0 for RMSNorm,
+// which an A/B at 768 x 6144 preferred by 0.05 us; 1.6 lost everywhere), for
+// grids of more than one rank that are resident in one wave; 0 (no delay)
+// otherwise.
 int wave_stagger_ns(const tr_device_desc& d, const tr_plan& p, int64_t cols) {
     if (p.kind != TR_PLAN_WAVE || d.sm_count < 1 || d.hbm_gbs <= 0.0) return 0;
     const int64_t resident = p.resident_ctas > 0 ? p.resident_ctas : static_cast<int64_t>(p.ctas_per_sm) * d.sm_count;
     if (p.grid_ctas <= d.sm_count || p.grid_ctas > resident) return 0;
+    const double scale = p.op == TR_OP_RMSNORM ? 1.0 : 0.92;
     const double rank_bytes = static_cast<double>(d.sm_count) * p.rows_per_cta * static_cast<double>(cols) * 4.0;
-    return static_cast<int>(std::min(4000.0, kWaveStagger * rank_bytes / d.hbm_gbs));  // GB/s = bytes per ns
+    return static_cast<int>(std::min(4000.0, scale * rank_bytes / 6800.0));  // 6800 GB/s = bytes per ns
 }
 
 // Allow a kernel the full dynamic shared memory budget (once per kernel and
