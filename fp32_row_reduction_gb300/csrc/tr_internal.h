@@ -46,7 +46,7 @@ struct RowArgs {
 
 // Testing modes (tr_debug_force_wait_timeout), a bit mask in RowArgs::debug_flags:
 constexpr int kDebugForceTimeout = 1;  // one extra wait on a barrier nothing completes (1 ms limit)
-constexpr int kDebugExpireCopies = 2;  // waits for bulk copies (staged rings, segments plan) give up at once
+constexpr int kDebugExpireCopies = 2;  // waits for bulk copies (staged rings) give up at once
 constexpr int kDebugExpirePeers = 4;   // a split CTA's wait for the other CTAs of its row gives up at once
 constexpr int kDebugModes = kDebugForceTimeout | kDebugExpireCopies | kDebugExpirePeers;
 // The testing modes in force now (for launches that build their own arguments).

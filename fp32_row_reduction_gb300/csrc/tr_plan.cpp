@@ -404,6 +404,7 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
         if (sq > static_cast<int64_t>(k) * T) return fail(TR_ERR_UNSUPPORTED, "a segment exceeds vec_slots quads per thread");
         if (sq < T / 2) return fail(TR_ERR_UNSUPPORTED, "segments plans are for rows of at least 512 quads per CTA");
         if (rows * p->grid_ctas > kSplitMaxParts) return fail(TR_ERR_UNSUPPORTED, "rows x CTAs partials exceed the workspace");
+        if (p->grid_ctas > 160) return fail(TR_ERR_UNSUPPORTED, "segments plans merge at most 160 partials per row");
     }
     if (why) *why = "";
     return TR_OK;

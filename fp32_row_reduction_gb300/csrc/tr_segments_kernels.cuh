@@ -12,13 +12,16 @@
 // once per launch. The statistics of all rows meet in ONE exchange through
 // the stream's workspace ("TIRx Metal reduction lowering" §4.2, the combine of
 // cooperating workers one level above a CTA):
-//   1. the first nbuf rows' segments are copied into shared memory by bulk
-//      asynchronous copies issued at entry; the other rows' segments are
-//      streamed (L2 evict-last: they are read again) while those land; each
-//      warp folds every row's quads into per-row partials;
+//   1. every row's segment streams through registers once, several rows'
+//      loads in flight while the oldest is folded into per-row warp partials
+//      (two passes over the lanes, not a merge per shuffle level);
+//      the first nbuf rows are also kept, raw, in shared memory (the others
+//      are read again in the epilogue: L2 evict-last until then);
 //   2. the CTA publishes one partial per row, arrives once on the launch's
 //      arrival word, and waits for all G CTAs (bounded); warp w then merges
-//      rows w, w + 32, ... over the G partials, in CTA order;
+//      rows w, w + 32, ... over the G partials in CTA order (row-major
+//      partials, coalesced weak loads; approximate division in the moments
+//      merges: the policy is unordered);
 //   3. the epilogue writes every row's segment: cached rows from shared
 //      memory, the others read again (evict-first), outputs evict-first.
 // Requirements (checked by the plan selector): cols % 4 == 0, x, w and b
@@ -31,19 +34,31 @@
 namespace tr {
 namespace segments {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxRows = 32;
 
-// Fold this thread's valid quads (the first `n` of c) into a statistic.
+// One thread's fold of its valid quads (the first `n` of c) of one row, kept
+// small so that the quads' registers take the next row's loads at once.
+//   softmax: (m, s) about the thread's own maximum;
+//   RMSNorm: the sum of squares;
+//   LayerNorm: (n, mean, M2) about the thread's own mean (two passes over its
+//   registers; n = 4 or 8 or ..., the mean by the reciprocal of n).
+template <int OP>
+struct ThreadFold;
+template <>
+struct ThreadFold<OP_SOFTMAX> { float m, s; };
+template <>
+struct ThreadFold<OP_RMSNORM> { float ss; };
+template <>
+struct ThreadFold<OP_LAYERNORM> { float n, mean, m2, sum; };
+
 template <int OP, int I>
-__device__ __forceinline__ SplitStat<OP> fold_quads(const float4 (&c)[I], int n) {
+__device__ __forceinline__ ThreadFold<OP> fold_thread(const float4 (&c)[I], int n) {
     if constexpr (OP == OP_SOFTMAX) {
         float cm = MaxOp::id();
 #pragma unroll
         for (int i = 0; i < I; ++i)
             if (i < n) cm = fmaxf(cm, max4(c[i]));
-        if (cm == MaxOp::id()) return MaxSum{cm, 0.0f};
+        if (cm == MaxOp::id()) return {cm, 0.0f};
         const float mb = mb_of(cm);
         float s = 0.0f;
 #pragma unroll
@@ -51,21 +66,21 @@ __device__ __forceinline__ SplitStat<OP> fold_quads(const float4 (&c)[I], int n)
             if (i < n)
                 s += (ex2(fmaf(c[i].x, kL2E, -mb)) + ex2(fmaf(c[i].y, kL2E, -mb))) +
                      (ex2(fmaf(c[i].z, kL2E, -mb)) + ex2(fmaf(c[i].w, kL2E, -mb)));
-        return MaxSum{cm, s};
+        return {cm, s};
     } else if constexpr (OP == OP_RMSNORM) {
         float ss = 0.0f;
 #pragma unroll
         for (int i = 0; i < I; ++i)
             if (i < n) ss = fmaf(c[i].x, c[i].x, fmaf(c[i].y, c[i].y, fmaf(c[i].z, c[i].z, fmaf(c[i].w, c[i].w, ss))));
-        return ss;
+        return {ss};
     } else {
-        if (n <= 0) return Moments{0.0f, 0.0f, 0.0f};
+        if (n <= 0) return {0.0f, 0.0f, 0.0f, 0.0f};
         float sm = 0.0f;
 #pragma unroll
         for (int i = 0; i < I; ++i)
             if (i < n) sm += sum4(c[i]);
         const float cnt = 4.0f * n;
-        const float mu = __fdiv_rn(sm, cnt);
+        const float mu = sm * __frcp_rn(cnt);
         float m2 = 0.0f;
 #pragma unroll
         for (int i = 0; i < I; ++i)
@@ -73,15 +88,70 @@ __device__ __forceinline__ SplitStat<OP> fold_quads(const float4 (&c)[I], int n)
                 const float dx = c[i].x - mu, dy = c[i].y - mu, dz = c[i].z - mu, dw = c[i].w - mu;
                 m2 = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, fmaf(dw, dw, m2))));
             }
-        return Moments{cnt, mu, m2};
+        return {cnt, mu, m2, sm};
     }
 }
 
-template <int OP, int I>
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+// The warp's statistic from its lanes' folds, in two passes over the lanes
+// instead of a merge per shuffle level: softmax takes the warp maximum first
+// and rescales each lane's sum to it once (one exponential per lane rather
+// than two per level); LayerNorm sums first, divides once by the warp's count
+// `nw`, and adds each lane's M2 to its squared offset from that mean times its
+// count (the parallel-axis identity, exact in real arithmetic). Special
+// values come out as from the pairwise merges: no finite element gives the
+// identity, an infinite maximum a NaN sum.
+template <int OP>
+__device__ __forceinline__ SplitStat<OP> fold_warp(ThreadFold<OP> f, float nw) {
+    if constexpr (OP == OP_SOFTMAX) {
+        const float m = warp_max(f.m);
+        if (m == MaxOp::id()) return MaxSum{m, 0.0f};
+        return MaxSum{m, warp_sum(f.s * ex2(mb_of(f.m) - mb_of(m)))};
+    } else if constexpr (OP == OP_RMSNORM) {
+        return warp_sum(f.ss);
+    } else {
+        if (nw == 0.0f) return Moments{0.0f, 0.0f, 0.0f};
+        const float mean = __fdiv_rn(warp_sum(f.sum), nw);
+        const float d = f.mean - mean;
+        return Moments{nw, mean, warp_sum(fmaf(f.n * d, d, f.m2))};
+    }
+}
+
+// Merges of the unordered policy with the approximate division (Chan's
+// moments): the exchange merges G partials per row, and the IEEE division of
+// mo_merge would dominate it.
+__device__ __forceinline__ float seg_merge(float a, float b) { return a + b; }
+__device__ __forceinline__ MaxSum seg_merge(MaxSum a, MaxSum b) { return ms_merge(a, b); }
+__device__ __forceinline__ Moments seg_merge(Moments a, Moments b) {
+    const float n = a.n + b.n;
+    if (n == 0.0f) return Moments{0.0f, 0.0f, 0.0f};
+    const float d = b.mean - a.mean;
+    const float fb = __fdividef(b.n, n);
+    return Moments{n, fmaf(d, fb, a.mean), fmaf(d * d, a.n * fb, a.m2 + b.m2)};
+}
+template <class Stat>
+__device__ __forceinline__ Stat seg_warp_merge(Stat v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = seg_merge(v, shfl_xor(v, o));
+    return v;
+}
+
+// kThreads threads per CTA, I quads per thread and row, D rows in flight per thread.
+template <int OP, int I, int kThreads = 1024, int D = 2>
 __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) {
     using Stat = SplitStat<OP>;
-    extern __shared__ __align__(16) float4 cache[];  // nbuf rows x sq quads
-    __shared__ __align__(8) uint64_t bar;
+    constexpr int kWarps = kThreads / 32;
+    extern __shared__ __align__(16) float4 cache[];  // nbuf rows x sq quads (raw x)
     __shared__ float4 wpart[kWarps][kMaxRows];  // per warp, per row
     __shared__ float4 srow[kMaxRows];           // the rows' merged statistics
     __shared__ volatile int s_abort;
@@ -92,30 +162,68 @@ __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) 
     const int q0 = static_cast<int>(static_cast<int64_t>(g) * nq / G);
     const int q1 = static_cast<int>(static_cast<int64_t>(g + 1) * nq / G);
     const int sq = q1 - q0;
-    const int rc = min(R, a.nbuf);                  // rows cached in shared memory
+    const int rc = min(R, a.nbuf);                  // rows kept in shared memory
     // this thread's quads q0 + t + kThreads * i, the first `mine` of them valid
     const int mine = t < sq ? (sq - 1 - t) / kThreads + 1 : 0;
-    if (t == 0) {
-        mbar_init(&bar, 1);
-        s_abort = 0;
-        fence_barrier_init();
-    }
+    // the elements this warp holds of every row (for LayerNorm's warp mean)
+    float nw = 0.0f;
+#pragma unroll
+    for (int i = 0; i < I; ++i) nw += 4.0f * static_cast<float>(min(32, max(0, sq - 32 * warp - kThreads * i)));
+    if (t == 0) s_abort = 0;
     __syncthreads();
     pdl_enter();
     uint64_t keep, drop;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(drop));
-    if (t == 0) {
-        if (rc > 0 && sq > 0) {
-            mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(rc) * static_cast<uint32_t>(sq) * 16u);
-            for (int r = 0; r < rc; ++r)
-                bulk_g2s_pol(cache + static_cast<int64_t>(r) * sq, a.x + static_cast<int64_t>(r) * cols + 4 * q0,
-                             static_cast<uint32_t>(sq) * 16u, &bar, drop);
-        } else {
-            mbar_arrive(&bar);
+    auto row_ptr = [&](int r, int i) { return a.x + static_cast<int64_t>(r) * cols + 4 * (q0 + t + kThreads * i); };
+    const float id = first_identity<OP>();
+    auto load_row = [&](int r, float4 (&c)[I], uint64_t pol) {
+#pragma unroll
+        for (int i = 0; i < I; ++i) c[i] = i < mine ? ld_pol4(row_ptr(r, i), pol) : f4(id);
+    };
+    float4 buf[D][I];
+
+    // ---- 1. every row streams through registers once, D rows in flight per
+    // thread: a thread folds the oldest, reloads its registers with the row D
+    // ahead, then its warp combines the folds; the first rc rows are also kept,
+    // raw, in shared memory for the epilogue (the others are read again, L2
+    // evict-last until then)
+#pragma unroll
+    for (int j = 0; j < D; ++j)
+        if (j < R) load_row(j, buf[j], j < rc ? drop : keep);
+    for (int r0 = 0; r0 < R; r0 += D) {
+#pragma unroll
+        for (int j = 0; j < D; ++j) {
+            const int r = r0 + j;
+            if (r < R) {
+                if (r < rc)
+#pragma unroll
+                    for (int i = 0; i < I; ++i)
+                        if (i < mine) cache[static_cast<int64_t>(r) * sq + t + kThreads * i] = buf[j][i];
+                const ThreadFold<OP> f = fold_thread<OP, I>(buf[j], mine);
+                if (r + D < R) load_row(r + D, buf[j], r + D < rc ? drop : keep);
+                const Stat st = fold_warp<OP>(f, nw);
+                if (lane == 0) wpart[warp][r] = pack(st);
+            }
         }
     }
-    // the weight (and bias) quads of this thread's columns, for every row
+    __syncthreads();
+    // the CTA's partial of each row (warp w merges rows w, w + kWarps, ...),
+    // stored row-major: row r's G partials are contiguous
+    for (int r = warp; r < R; r += kWarps) {
+        const Stat v = seg_warp_merge(lane < kWarps ? unpack<Stat>(wpart[lane][r]) : identity_of<Stat>());
+        if (lane == 0) a.sp_part[static_cast<int64_t>(r) * G + g] = pack(v);
+    }
+    // every partial of the CTA is stored before thread 0's release (cumulative
+    // over the barrier) makes them visible with its arrival
+    __syncthreads();
+
+    // ---- 2. one arrival per CTA; wait for all G (bounded), then merge each row
+    // over its G partials (CTA order, one fixed tree), warp w taking rows w,
+    // w + kWarps, ...: a lane loads its partials (coalesced, weak L2 loads
+    // ordered after the acquire by the barrier) before it merges them
+    if (t == 0) red_add_release(a.sp_arrive, 1u);
+    // the weight (and bias) quads of this thread's columns: in flight during the exchange
     float4 wq[I], bq[I];
 #pragma unroll
     for (int i = 0; i < I; ++i) {
@@ -123,59 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) 
         wq[i] = (OP != OP_SOFTMAX && a.has_w && i < mine) ? ld_param4(a.w + c) : f4(1.0f);
         bq[i] = (OP == OP_LAYERNORM && a.has_b && i < mine) ? ld_param4(a.b + c) : f4(0.0f);
     }
-    auto row_ptr = [&](int r, int i) { return a.x + static_cast<int64_t>(r) * cols + 4 * (q0 + t + kThreads * i); };
-    auto publish = [&](int r, Stat st) {  // warp partial of row r into shared memory
-        st = warp_merge<Stat, 32>(st);
-        if (lane == 0) wpart[warp][r] = pack(st);
-    };
-
-    // ---- 1. the streamed rows (two rows' loads in flight), then the cached rows
-    float4 cur[I], nxt[I];
-    const float id = first_identity<OP>();
-    auto load_row = [&](int r, float4 (&c)[I], uint64_t pol) {
-#pragma unroll
-        for (int i = 0; i < I; ++i) c[i] = i < mine ? ld_pol4(row_ptr(r, i), pol) : f4(id);
-    };
-    if (rc < R) load_row(rc, cur, keep);
-    for (int r = rc; r < R; ++r) {
-        if (r + 1 < R) load_row(r + 1, nxt, keep);
-        publish(r, fold_quads<OP, I>(cur, mine));
-#pragma unroll
-        for (int i = 0; i < I; ++i) cur[i] = nxt[i];
-    }
-    if (!mbar_wait_bounded(&bar, 0, a.wait_ns, a.err, a.debug_flags & kDebugExpireCopies)) s_abort = 1;
-    __syncthreads();  // s_abort as every thread saw it
-    const bool copied = !s_abort;
-    for (int r = 0; r < rc; ++r) {
-        float4 c[I];
-#pragma unroll
-        for (int i = 0; i < I; ++i)
-            c[i] = (copied && i < mine) ? cache[static_cast<int64_t>(r) * sq + t + kThreads * i] : f4(id);
-        publish(r, fold_quads<OP, I>(c, copied ? mine : 0));
-    }
-    __syncthreads();
-    // the CTA's partial of each row: warp w merges rows w, w + kWarps, ...
-    for (int r = warp; r < R; r += kWarps) {
-        const Stat v = warp_merge<Stat, 32>(lane < kWarps ? unpack<Stat>(wpart[lane][r]) : identity_of<Stat>());
-        if (lane == 0) {
-            a.sp_part[static_cast<int64_t>(g) * R + r] = pack(v);
-            __threadfence();  // visible at device scope before the CTA's arrival below
-        }
-    }
-    __syncthreads();  // every partial of the CTA is stored before thread 0's release
-
-    // ---- 2. one arrival per CTA; wait for all G (bounded), then merge each row over the G partials
-    if (t == 0) red_add_release(a.sp_arrive, s_abort ? 1u + kSplitAbortUnit : 1u);
     if (t < 32) {
         const unsigned long long t0 = global_ns();
-        bool late = a.debug_flags & kDebugExpirePeers, aborted = false;
+        bool late = a.debug_flags & kDebugExpirePeers;  // (testing: gives up before it looks)
         while (!late) {
-            const unsigned v = ld_acquire(a.sp_arrive);
-            if (v >= kSplitAbortUnit) {
-                aborted = true;
-                break;
-            }
-            if (v >= static_cast<unsigned>(G)) break;
+            if (ld_acquire(a.sp_arrive) >= static_cast<unsigned>(G)) break;
             if (static_cast<long long>(global_ns() - t0) > a.wait_ns) {
                 late = true;
                 break;
@@ -183,18 +243,26 @@ __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) 
             __nanosleep(32);
         }
         late = __any_sync(kFull, late);
-        aborted = __any_sync(kFull, aborted);
-        if (late && t == 0) atomicOr(a.err, kErrWaitTimeout);
-        if ((late || aborted) && t == 0) s_abort = 1;
+        if (late && t == 0) {
+            atomicOr(a.err, kErrWaitTimeout);
+            s_abort = 1;
+        }
     }
     __syncthreads();
     if (!s_abort) {
-        (void)ld_acquire(a.sp_arrive);  // each reading thread acquires the arrivals itself
+        constexpr int kPer = 5;  // partials per lane: G <= 160
         for (int r = warp; r < R; r += kWarps) {
-            Stat v = identity_of<Stat>();
-            for (int k = lane; k < G; k += 32)
-                v = split_merge(v, unpack<Stat>(ld_relaxed4(a.sp_part + static_cast<int64_t>(k) * R + r)));
-            v = warp_merge<Stat, 32>(v);
+            const float4* pr = a.sp_part + static_cast<int64_t>(r) * G;
+            float4 pv[kPer];
+#pragma unroll
+            for (int m = 0; m < kPer; ++m) {
+                const int k = lane + 32 * m;
+                pv[m] = k < G ? __ldcg(pr + k) : pack(identity_of<Stat>());
+            }
+            Stat v = unpack<Stat>(pv[0]);
+#pragma unroll
+            for (int m = 1; m < kPer; ++m) v = seg_merge(v, unpack<Stat>(pv[m]));
+            v = seg_warp_merge(v);
             if (lane == 0) srow[r] = pack(v);
         }
     }
@@ -205,10 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) 
         *a.sp_depart = 0u;
         __threadfence();
     }
-    if (s_abort) {
-        if (t == 0 && !copied) mbar_wait_bounded(&bar, 0, a.wait_ns, nullptr);  // drain the copies
-        return;
-    }
+    if (s_abort) return;
 
     // ---- 3. the epilogue of every row
     auto out_row = [&](int r, const float4 (&c)[I]) {
@@ -239,12 +304,18 @@ __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) 
         }
     };
     // the streamed rows first (their second read was kept in L2 most recently)
-    if (rc < R) load_row(rc, cur, drop);
-    for (int r = rc; r < R; ++r) {
-        if (r + 1 < R) load_row(r + 1, nxt, drop);
-        out_row(r, cur);
 #pragma unroll
-        for (int i = 0; i < I; ++i) cur[i] = nxt[i];
+    for (int j = 0; j < D; ++j)
+        if (rc + j < R) load_row(rc + j, buf[j], drop);
+    for (int r0 = rc; r0 < R; r0 += D) {
+#pragma unroll
+        for (int j = 0; j < D; ++j) {
+            const int r = r0 + j;
+            if (r < R) {
+                out_row(r, buf[j]);
+                if (r + D < R) load_row(r + D, buf[j], drop);
+            }
+        }
     }
     for (int r = 0; r < rc; ++r) {
         float4 c[I];

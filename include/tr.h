@@ -409,11 +409,10 @@ const char* tr_last_error_message(void);
  *   1  every launch of a plan with bounded waits (staged plans) also waits on
  *      a barrier that nothing completes, with a 1 ms limit; results stay correct;
  *   2  waits for bulk asynchronous copies give up at once: in the staged
- *      plans every ring slot (that row's outputs are undefined), in the
- *      segments plan every CTA's copy (the other CTAs learn of it through the
- *      arrival word, and no output is written); a CTA still waits for its
- *      copies, with the normal limit, before it exits. The split plan streams
- *      its segments through registers and has no such wait;
+ *      plans every ring slot (that row's outputs are undefined); a CTA still
+ *      waits for its copies, with the normal limit, before it exits. The split
+ *      and segments plans stream their segments through registers and have no
+ *      such wait;
  *   4  every split (and segments) CTA's wait for the other CTAs of its row
  *      gives up at once: no CTA of the row writes outputs.
  * Applies to the launches made while it is set, including

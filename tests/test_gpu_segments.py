@@ -9,7 +9,7 @@ CTA). Unordered policy: |gpu - oracle| <= 1e-6 + 2e-6 |oracle| element by
 element. Covered: rows with cached and streamed segments, 1 and 32 rows,
 ragged segment boundaries, outputs at another 16-byte phase, guard bands,
 repeated launches on one workspace (the arrival word is reset by the last CTA),
-the give-up paths of its waits, and the refusals.
+the give-up path of its wait for the other CTAs, and the refusals.
 """
 import numpy as np
 import pytest
@@ -130,7 +130,19 @@ def test_segments_repeated_launches_and_norms_without_affine():
         assert_close(y.cpu().numpy(), reference(op, dd), f"{op} without {drop}")
 
 
-@pytest.mark.parametrize("mode", [2, 4])
+def test_segments_plan_has_no_copy_wait():
+    # its segments stream through registers: the copy give-up mode changes nothing
+    rows, cols = 16, 400000
+    d = make("layernorm", rows, cols, seed=21)
+    assert tr.tr_debug_force_wait_timeout(2) == tr.TR_OK
+    try:
+        y = run_with(seg_plan("layernorm", rows, cols), "layernorm", d)
+    finally:
+        tr.tr_debug_force_wait_timeout(0)
+    assert_close(y.cpu().numpy(), reference("layernorm", d), "copy give-up mode")
+
+
+@pytest.mark.parametrize("mode", [4, 6])
 def test_segments_give_up_and_recover(mode):
     # a wait that gives up: the timeout is reported, no output is written, and
     # the next launch on the same workspace matches the oracle (nothing reset)
