@@ -47,7 +47,7 @@ TR_PLAN_STAGED = 5
 TR_PLAN_ORDERED_STAGED = 6
 TR_PLAN_SPLIT = 7
 TR_PLAN_FOLD = 8
-COST_CONSTANTS = 15  # TR_COST_CONSTANTS
+COST_CONSTANTS = 16  # TR_COST_CONSTANTS
 TR_PLAN_WAVE = 9
 TR_PLAN_SEGMENTS = 10
 TR_OP_ADD_RMSNORM = 4

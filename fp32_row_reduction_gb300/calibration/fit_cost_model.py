@@ -22,7 +22,8 @@ import math
 import fp32_row_reduction_gb300 as tr
 
 NAMES = ["launch", "latency", "cta_barrier", "cluster_barrier", "l2_over_hbm", "staged_row", "one_wave_alu", "wave",
-         "slot_pass", "param_trip", "clock_ghz", "split_sync", "pair_overlap", "wave_slot_pass", "wave_row_share"]
+         "slot_pass", "param_trip", "clock_ghz", "split_sync", "pair_overlap", "wave_slot_pass", "wave_row_share",
+         "seg_row"]
 FIXED = {"clock_ghz"}
 PLAN_KEYS = ["op", "order", "kind", "lanes_per_row", "warps_per_row", "rows_per_cta", "cluster_ctas", "vec_slots",
              "block_threads", "ctas_per_sm", "grid_ctas", "flags", "resident_ctas"]

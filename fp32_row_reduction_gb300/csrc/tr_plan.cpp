@@ -115,6 +115,7 @@ const CostConstants kCostDefaults = {
     0.6,     // pair_overlap: share of the write phase hidden by two rows per group
     0.015,   // wave_slot_pass: a wave thread's serial work per cached slot and pass
     4.0,     // wave_row_share: share of that work each further row of a wave thread adds
+    0.5,     // seg_row: a segments CTA's fixed step per row (fold, warp merges, epilogue)
 };
 
 tr_device_desc gb300_desc() {
@@ -417,7 +418,7 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
                  kOneWaveAluFactor = c.one_wave_alu, kWaveUs = c.wave, kSlotPassUs = c.slot_pass,
                  kParamTripUs = c.param_trip, kClockGhz = c.clock_ghz, kSplitSyncUs = c.split_sync,
                  kPairOverlap = c.pair_overlap, kWaveSlotPass = c.wave_slot_pass,
-                 kWaveRowShare = c.wave_row_share;
+                 kWaveRowShare = c.wave_row_share, kSegRowUs = c.seg_row;
     (void)align16;
     const double E = static_cast<double>(rows) * static_cast<double>(cols);
     const double bw = d.hbm_gbs * 1e3;  // bytes per microsecond
@@ -526,18 +527,19 @@ double estimate_us(const tr_device_desc& d, const tr_plan& p, int64_t rows, int6
     }
 
     if (p.kind == TR_PLAN_SEGMENTS) {
-        // one wave of co-resident CTAs: the cached rows land by bulk copies while
-        // the others stream, one exchange of all rows' partials, then the writes;
-        // the streamed rows are read again (from L2 when the input fits), the
-        // weights and biases cross L2 once
+        // one wave of co-resident CTAs, one per SM, each holding a segment of
+        // every row: the rows stream through registers (several in flight per
+        // thread), one exchange of all rows' partials, then the writes; each
+        // row adds a fixed step of folds, warp merges and epilogue per CTA; the
+        // rows not kept in shared memory are read again (L2, evict-last until
+        // then); the weights and biases cross L2 once
         const int nbuf = seg_cached_rows(rows, cols, p.grid_ctas);
-        const double cached = static_cast<double>(nbuf) * static_cast<double>(ceil_div(cols / 4, p.grid_ctas)) * 16.0 *
-                              static_cast<double>(p.grid_ctas);
-        const double over = std::max(0.0, read_bytes - cached);
-        const double t_over = over / ((l2_fits ? kL2OverHbm : 1.0) * bw);
+        const double over = static_cast<double>(rows - nbuf) * 4.0 * static_cast<double>(cols);
+        const double t_over = over / (kL2OverHbm * bw);
         const double t_par = param_bytes / (kL2OverHbm * bw);
-        return kLaunchUs + kLatencyUs + read_bytes / bw + kSplitSyncUs + kOneWaveAluFactor * t_alu + kchain +
-               write_bytes / bw + t_over + t_par;
+        return kLaunchUs + kLatencyUs + kSplitSyncUs + kchain +
+               std::max((read_bytes + write_bytes) / bw, kOneWaveAluFactor * t_alu) +
+               static_cast<double>(rows) * kSegRowUs + t_over + t_par;
     }
     if (p.kind == TR_PLAN_SPLIT) {
         // one wave of co-resident CTAs in lockstep: read (the bulk copy of the
@@ -764,9 +766,23 @@ void enumerate_plans(const tr_device_desc& d, const OccupancyFn& occ, int32_t op
                     s.vec_slots = 0;
                     cands.push_back(s);
                 }
-            // (the segments plan, TR_PLAN_SEGMENTS, is not enumerated: measured, it
-            // is slower than the split and cluster plans on most long-row shapes;
-            // it runs only when a caller forces it)
+            // few long rows, every SM holding a segment of every row: for the norms
+            // (their weights and biases cross L2 once instead of once per row), and
+            // for softmax only where the split plans leave SMs idle (fewer rows than
+            // SMs / kSplitMaxCtas; with more, its split plans measured faster)
+            if ((op == TR_OP_RMSNORM || op == TR_OP_LAYERNORM ||
+                 (op == TR_OP_SOFTMAX && rows * kSplitMaxCtas < d.sm_count)) &&
+                rows <= kSegMaxRows && cols % 4 == 0)
+                for (int k : kSegSlots) {
+                    tr_plan q = base(TR_PLAN_SEGMENTS);
+                    q.lanes_per_row = 32;
+                    q.warps_per_row = kSegThreads / 32;
+                    q.rows_per_cta = static_cast<int>(rows);
+                    q.block_threads = kSegThreads;
+                    q.cluster_ctas = 1;
+                    q.vec_slots = k;
+                    cands.push_back(q);
+                }
             // few long rows: C co-resident CTAs per row, each caching its segment in
             // shared memory (one CTA or two per SM, sharing the SM's shared memory
             // less 32 KB, which stays L1: at 16 x 1048576

@@ -29,9 +29,9 @@ tr_status check_plan(const tr_device_desc& d, const OccupancyFn& occ, tr_plan* p
 // The cost model's constants (microseconds unless stated).
 struct CostConstants {
     double launch, latency, cta_barrier, cluster_barrier, l2_over_hbm, staged_row, one_wave_alu, wave, slot_pass,
-        param_trip, clock_ghz, split_sync, pair_overlap, wave_slot_pass, wave_row_share;
+        param_trip, clock_ghz, split_sync, pair_overlap, wave_slot_pass, wave_row_share, seg_row;
 };
-constexpr int kCostConstantCount = 15;
+constexpr int kCostConstantCount = 16;
 extern const CostConstants kCostDefaults;
 
 // Cost-model estimate in microseconds for a legal plan (grid_ctas and

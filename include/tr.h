@@ -360,12 +360,12 @@ tr_status tr_plan_check_for(const tr_device_desc* dev, tr_plan* plan, int64_t ro
 /* ---- cost-model calibration and audit (host side) ----------------------
  * The model's constants, in this order: launch, latency, cta_barrier,
  * cluster_barrier, l2_over_hbm, staged_row, one_wave_alu, wave, slot_pass,
- * param_trip, clock_ghz, split_sync, pair_overlap, wave_slot_pass, wave_row_share
- * (microseconds unless stated). They are
+ * param_trip, clock_ghz, split_sync, pair_overlap, wave_slot_pass, wave_row_share,
+ * seg_row (microseconds unless stated). They are
  * fixed in the library; these calls exist so that an offline calibration can
  * score the model on measured plan sweeps ("Whole-launch reduction cost
  * policy": measurement calibrates priors, never selects a plan). */
-#define TR_COST_CONSTANTS 15
+#define TR_COST_CONSTANTS 16
 
 /* Copy the library's constants into out[0 .. n-1] (n must be TR_COST_CONSTANTS). */
 tr_status tr_plan_cost_constants(double* out, int32_t n);

@@ -1,5 +1,6 @@
 """GPU parity of the segments plan (TR_PLAN_SEGMENTS) against the CPU oracle.
-The selector never picks it; these tests force it with the plan override.
+The selector picks it for the norms' long rows and for softmax's few long
+rows; these tests force it with the plan override wherever it is legal.
 
 Few long rows: every co-resident CTA (one per SM) owns one column segment of
 every row and keeps its columns' weight and bias in registers for all rows;
@@ -96,10 +97,18 @@ def test_segments_match_oracle(op, rows, cols):
 
 
 @pytest.mark.parametrize("op", OPS)
-def test_segments_is_only_run_when_forced(op):
-    # measured slower than the split plan at 16 x 1048576: the selector leaves it out
-    assert tr.tr_plan_describe(tr.OPS[op], 16, 1048576, 0).kind != tr.TR_PLAN_SEGMENTS
-    assert all(c.kind != tr.TR_PLAN_SEGMENTS for c in tr.plan_candidates(tr.OPS[op], 16, 1048576, 0, 1))
+def test_segments_selection_and_default_path(op):
+    # the norms' 16 x 1048576 and every op's two rows of 1048576 run it unforced;
+    # softmax's 16 rows keep the split plan (measured faster there)
+    norm = op != "softmax"
+    assert (tr.tr_plan_describe(tr.OPS[op], 16, 1048576, 0).kind == tr.TR_PLAN_SEGMENTS) == norm
+    assert tr.tr_plan_describe(tr.OPS[op], 2, 1048576, 0).kind == tr.TR_PLAN_SEGMENTS
+    assert any(c.kind == tr.TR_PLAN_SEGMENTS for c in tr.plan_candidates(tr.OPS[op], 2, 1048576, 0, 1))
+    d = make(op, 2, 1048576, seed=31)
+    y = tr.run_op(op, d)
+    torch.cuda.synchronize()
+    assert tr.tr_last_device_error() == tr.TR_OK
+    assert_close(y.cpu().numpy(), reference(op, d), f"{op} 2x1048576 unforced")
 
 
 @pytest.mark.parametrize("yoff", [1, 3])

@@ -41,6 +41,8 @@ def covers(p, cols):
         return p.block_threads * p.vec_slots >= n4 and ring <= 225 * 1024
     if p.kind == trlib.TR_PLAN_WAVE:
         return cols % 4 == 0 and 1024 * p.vec_slots >= cols
+    if p.kind == trlib.TR_PLAN_SEGMENTS:  # one segment of every row per CTA, one CTA per SM
+        return cols % 4 == 0 and p.block_threads * p.vec_slots * p.grid_ctas >= n4
     return True  # streaming plans cover any row
 
 
@@ -63,7 +65,7 @@ def check_wave(p, rows, cols, op):
 def test_unordered_plans_are_legal_and_cover(op, rows, cols):
     p = select(op, rows, cols)
     assert p.kind in (trlib.TR_PLAN_ROWS, trlib.TR_PLAN_CLUSTER, trlib.TR_PLAN_STREAM, trlib.TR_PLAN_STAGED,
-                      trlib.TR_PLAN_SPLIT, trlib.TR_PLAN_WAVE)
+                      trlib.TR_PLAN_SPLIT, trlib.TR_PLAN_WAVE, trlib.TR_PLAN_SEGMENTS)
     assert covers(p, cols)
     assert p.block_threads % 32 == 0 and 32 <= p.block_threads <= 1024
     assert p.candidates >= 1 and p.est_us > 0 and p.ctas_per_sm >= 1
@@ -77,6 +79,8 @@ def test_unordered_plans_are_legal_and_cover(op, rows, cols):
         assert 2 <= p.cluster_ctas <= 32 and p.vec_slots * p.block_threads * 16 <= 225 * 1024
     elif p.kind == trlib.TR_PLAN_WAVE:
         check_wave(p, rows, cols, op)
+    elif p.kind == trlib.TR_PLAN_SEGMENTS:
+        assert p.grid_ctas == DEV.sm_count and p.rows_per_cta == rows and p.block_threads == 1024
     else:
         assert p.grid_ctas == rows * p.cluster_ctas
     if p.flags == trlib.TR_PLAN_FLAG_PARAMS_IN_REGISTERS:
@@ -150,9 +154,11 @@ def test_params_in_registers_only_when_aligned():
 
 def test_long_rows_split_across_ctas():
     # 16 rows cannot fill 152 SMs one CTA per row: the rows must be split
-    for cols in (262144, 1048576):
-        p = select(0, 16, cols)
-        assert p.cluster_ctas >= 2, p.as_dict()
+    # (several CTAs per row, or every CTA holding a segment of every row)
+    for op in (0, 1, 2):
+        for cols in (262144, 1048576):
+            p = select(op, 16, cols)
+            assert p.cluster_ctas >= 2 or p.kind == trlib.TR_PLAN_SEGMENTS, p.as_dict()
 
 
 def test_short_rows_pack_several_per_cta():
@@ -215,7 +221,7 @@ def seg_plan(op, rows, cols, K=None):
                          rows_per_cta=rows, cluster_ctas=1, vec_slots=K, block_threads=1024)
 
 
-def test_segments_plan_limits_and_never_selected():
+def test_segments_plan_limits_and_selection():
     # legal when forced: aligned rows, one 1024-thread CTA per SM holding a
     # segment of every row (rows <= 32, rows x SMs partials), 512..2048 quads per CTA
     for op, rows, cols, K, ok in [(0, 16, 1048576, 2, True), (1, 4, 1245184, 2, True), (2, 26, 400000, 1, True),
@@ -231,10 +237,24 @@ def test_segments_plan_limits_and_never_selected():
     p = seg_plan(0, 16, 1048576)
     p.rows_per_cta = 8                                 # a CTA holds every row
     assert trlib.check_plan_for(DEV, p, 16, 1048576, 1)[0] == trlib.TR_ERR_UNSUPPORTED
-    # measured slower than the split and cluster plans on most long rows: never chosen
+    # chosen for the norms' long rows (measured at 16 x 1048576: LayerNorm 33.4 us
+    # against 40.0 for the best split plan; one row of 1048576: 9.5 against 18.1),
+    # for softmax only with fewer rows than SMs / 32 (the split plans fill the
+    # GPU from there and measured faster: 26.9 against 31.5 us at 16 x 1048576)
+    for op in (1, 2):
+        for rows, cols in [(16, 1048576), (1, 400000), (2, 1048576), (8, 1245184)]:
+            assert select(op, rows, cols).kind == trlib.TR_PLAN_SEGMENTS, (op, rows, cols)
+    assert select(0, 2, 1048576).kind == trlib.TR_PLAN_SEGMENTS
+    for rows in (5, 8, 16, 24):
+        assert select(0, rows, 1048576).kind != trlib.TR_PLAN_SEGMENTS
+    # never for rows too short for it, an unaligned row, the ordered policy or cross-entropy
     for op in (0, 1, 2):
-        for rows, cols in SHAPES + [(4, 1245184), (24, 1048576), (16, 400000)]:
-            assert select(op, rows, cols).kind != trlib.TR_PLAN_SEGMENTS
+        for rows, cols in SHAPES:
+            if cols < 4 * 512 * DEV.sm_count:
+                assert select(op, rows, cols).kind != trlib.TR_PLAN_SEGMENTS
+        assert select(op, 16, 1048576, align=0).kind != trlib.TR_PLAN_SEGMENTS
+        assert select(op, 16, 1048576, order=1).kind != trlib.TR_PLAN_SEGMENTS
+    assert select(3, 2, 1048576).kind != trlib.TR_PLAN_SEGMENTS
 
 
 @pytest.mark.parametrize("op", [trlib.TR_OP_ROW_SUM, trlib.TR_OP_ROW_MAX, trlib.TR_OP_ROW_MIN, trlib.TR_OP_ROW_MINMAX])
