@@ -113,9 +113,9 @@ typedef enum tr_plan_kind {
                              one column segment of EVERY row (rows_per_cta = rows, at most 32), vec_slots
                              16-byte slots per thread per row (1 or 2); a thread keeps its columns' weight and
                              bias in registers for all rows; the rows' partials meet once in the stream's
-                             workspace (allocated on first use, as for the split plan). The selector never
-                             picks it (it measured slower than the split plan on most long rows): it runs
-                             only under tr_plan_override */
+                             workspace (allocated on first use, as for the split plan). The selector
+                             considers it for RMSNorm and LayerNorm, and for softmax with fewer rows than
+                             SMs / 32 (beyond that the split plans fill the GPU) */
 } tr_plan_kind;
 
 typedef struct tr_plan {
