@@ -11,7 +11,8 @@ The model itself is the library's (tr_plan_estimate_with): this script only
 searches its constants. Regret of a case = time of the plan with the lowest
 estimate / time of the fastest measured plan - 1. The fit minimises the mean
 regret over the calibration cases by coordinate descent on multiplicative
-steps; the clock stays at its datasheet value.
+steps; the clock stays at its datasheet value and the segments plans' per-row
+step (fitted on its own comparison with the split plans) is left as it is.
 """
 import argparse
 import collections
@@ -24,7 +25,9 @@ import fp32_row_reduction_gb300 as tr
 NAMES = ["launch", "latency", "cta_barrier", "cluster_barrier", "l2_over_hbm", "staged_row", "one_wave_alu", "wave",
          "slot_pass", "param_trip", "clock_ghz", "split_sync", "pair_overlap", "wave_slot_pass", "wave_row_share",
          "seg_row"]
-FIXED = {"clock_ghz"}
+# the clock is the datasheet value; the segments plans' per-row step is fitted on
+# its own comparison with the split plans (the sweeps hold no segments plans)
+FIXED = {"clock_ghz", "seg_row"}
 PLAN_KEYS = ["op", "order", "kind", "lanes_per_row", "warps_per_row", "rows_per_cta", "cluster_ctas", "vec_slots",
              "block_threads", "ctas_per_sm", "grid_ctas", "flags", "resident_ctas"]
 
