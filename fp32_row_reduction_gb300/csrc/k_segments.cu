@@ -7,9 +7,8 @@ namespace tr {
 template <int OP>
 static const void* segments_table(int slots) {
     switch (slots) {
-        // rows in flight per thread: four of one quad, two of two (the registers of 1024 threads)
-        case 1: return reinterpret_cast<const void*>(segments::segments_kernel<OP, 1, kSegThreads, 4>);
-        case 2: return reinterpret_cast<const void*>(segments::segments_kernel<OP, 2, kSegThreads, 2>);
+        case 1: return reinterpret_cast<const void*>(segments::segments_kernel<OP, 1>);
+        case 2: return reinterpret_cast<const void*>(segments::segments_kernel<OP, 2>);
     }
     return nullptr;
 }

@@ -115,7 +115,7 @@ const CostConstants kCostDefaults = {
     0.6,     // pair_overlap: share of the write phase hidden by two rows per group
     0.015,   // wave_slot_pass: a wave thread's serial work per cached slot and pass
     4.0,     // wave_row_share: share of that work each further row of a wave thread adds
-    0.5,     // seg_row: a segments CTA's fixed step per row (fold, warp merges, epilogue)
+    0.3,     // seg_row: a segments CTA's fixed step per row (fold, warp merges, epilogue)
 };
 
 tr_device_desc gb300_desc() {

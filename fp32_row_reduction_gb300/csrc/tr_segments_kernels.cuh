@@ -19,8 +19,9 @@
 //      are read again in the epilogue: L2 evict-last until then);
 //   2. the CTA publishes one partial per row, arrives once on the launch's
 //      arrival word, and waits for all G CTAs (bounded); warp w then merges
-//      rows w, w + 32, ... over the G partials (row-major partials,
-//      coalesced weak loads, the same two passes over the lanes);
+//      rows w, w + 32, ... over the G partials in CTA order (row-major
+//      partials, coalesced weak loads; approximate division in the moments
+//      merges: the policy is unordered);
 //   3. the epilogue writes every row's segment: cached rows from shared
 //      memory, the others read again (evict-first), outputs evict-first.
 // Requirements (checked by the plan selector): cols % 4 == 0, x, w and b
@@ -126,48 +127,23 @@ __device__ __forceinline__ SplitStat<OP> fold_warp(ThreadFold<OP> f, float nw) {
     }
 }
 
-// The statistic of P partials per lane over the whole warp (identities where
-// a lane has fewer), in the same two passes: softmax rescales every partial
-// sum to the warp maximum once; LayerNorm sums n and n x mean first, then each
-// partial's M2 plus n times its squared offset from the merged mean.
-template <int P>
-__device__ __forceinline__ float merge_lanes(const float (&v)[P]) {
-    float s = 0.0f;
-#pragma unroll
-    for (int m = 0; m < P; ++m) s += v[m];
-    return warp_sum(s);
-}
-template <int P>
-__device__ __forceinline__ MaxSum merge_lanes(const MaxSum (&v)[P]) {
-    float mx = MaxOp::id();
-#pragma unroll
-    for (int m = 0; m < P; ++m) mx = fmaxf(mx, v[m].m);
-    mx = warp_max(mx);
-    if (mx == MaxOp::id()) return MaxSum{mx, 0.0f};
-    const float mb = mb_of(mx);
-    float s = 0.0f;
-#pragma unroll
-    for (int m = 0; m < P; ++m) s += v[m].s * ex2(mb_of(v[m].m) - mb);
-    return MaxSum{mx, warp_sum(s)};
-}
-template <int P>
-__device__ __forceinline__ Moments merge_lanes(const Moments (&v)[P]) {
-    float n = 0.0f, sx = 0.0f;
-#pragma unroll
-    for (int m = 0; m < P; ++m) {
-        n += v[m].n;
-        sx = fmaf(v[m].n, v[m].mean, sx);
-    }
-    n = warp_sum(n);
+// Merges of the unordered policy with the approximate division (Chan's
+// moments): the exchange merges G partials per row, and the IEEE division of
+// mo_merge would dominate it.
+__device__ __forceinline__ float seg_merge(float a, float b) { return a + b; }
+__device__ __forceinline__ MaxSum seg_merge(MaxSum a, MaxSum b) { return ms_merge(a, b); }
+__device__ __forceinline__ Moments seg_merge(Moments a, Moments b) {
+    const float n = a.n + b.n;
     if (n == 0.0f) return Moments{0.0f, 0.0f, 0.0f};
-    const float mean = __fdiv_rn(warp_sum(sx), n);
-    float m2 = 0.0f;
+    const float d = b.mean - a.mean;
+    const float fb = __fdividef(b.n, n);
+    return Moments{n, fmaf(d, fb, a.mean), fmaf(d * d, a.n * fb, a.m2 + b.m2)};
+}
+template <class Stat>
+__device__ __forceinline__ Stat seg_warp_merge(Stat v) {
 #pragma unroll
-    for (int m = 0; m < P; ++m) {
-        const float d = v[m].mean - mean;
-        m2 += fmaf(v[m].n * d, d, v[m].m2);
-    }
-    return Moments{n, mean, warp_sum(m2)};
+    for (int o = 16; o >= 1; o >>= 1) v = seg_merge(v, shfl_xor(v, o));
+    return v;
 }
 
 // kThreads threads per CTA, I quads per thread and row, D rows in flight per thread.
@@ -235,8 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) 
     // the CTA's partial of each row (warp w merges rows w, w + kWarps, ...),
     // stored row-major: row r's G partials are contiguous
     for (int r = warp; r < R; r += kWarps) {
-        const Stat pv[1] = {lane < kWarps ? unpack<Stat>(wpart[lane][r]) : identity_of<Stat>()};
-        const Stat v = merge_lanes<1>(pv);
+        const Stat v = seg_warp_merge(lane < kWarps ? unpack<Stat>(wpart[lane][r]) : identity_of<Stat>());
         if (lane == 0) a.sp_part[static_cast<int64_t>(r) * G + g] = pack(v);
     }
     // every partial of the CTA is stored before thread 0's release (cumulative
@@ -248,6 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) 
     // w + kWarps, ...: a lane loads its partials (coalesced, weak L2 loads
     // ordered after the acquire by the barrier) before it merges them
     if (t == 0) red_add_release(a.sp_arrive, 1u);
+    // the weight (and bias) quads of this thread's columns: in flight during the exchange
+    float4 wq[I], bq[I];
+#pragma unroll
+    for (int i = 0; i < I; ++i) {
+        const int c = 4 * (q0 + t + kThreads * i);
+        wq[i] = (OP != OP_SOFTMAX && a.has_w && i < mine) ? ld_param4(a.w + c) : f4(1.0f);
+        bq[i] = (OP == OP_LAYERNORM && a.has_b && i < mine) ? ld_param4(a.b + c) : f4(0.0f);
+    }
     if (t < 32) {
         const unsigned long long t0 = global_ns();
         bool late = a.debug_flags & kDebugExpirePeers;  // (testing: gives up before it looks)
@@ -270,28 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1) segments_kernel(const RowArgs a) 
         constexpr int kPer = 5;  // partials per lane: G <= 160
         for (int r = warp; r < R; r += kWarps) {
             const float4* pr = a.sp_part + static_cast<int64_t>(r) * G;
-            float4 raw[kPer];
+            float4 pv[kPer];
 #pragma unroll
             for (int m = 0; m < kPer; ++m) {
                 const int k = lane + 32 * m;
-                raw[m] = k < G ? __ldcg(pr + k) : pack(identity_of<Stat>());
+                pv[m] = k < G ? __ldcg(pr + k) : pack(identity_of<Stat>());
             }
-            Stat pv[kPer];
+            Stat v = unpack<Stat>(pv[0]);
 #pragma unroll
-            for (int m = 0; m < kPer; ++m) pv[m] = unpack<Stat>(raw[m]);
-            const Stat v = merge_lanes<kPer>(pv);
+            for (int m = 1; m < kPer; ++m) v = seg_merge(v, unpack<Stat>(pv[m]));
+            v = seg_warp_merge(v);
             if (lane == 0) srow[r] = pack(v);
         }
-    }
-    // the weight (and bias) quads of this thread's columns, in flight while the
-    // CTA gathers the row statistics (loaded before the merge, they held
-    // registers that the merge spilled)
-    float4 wq[I], bq[I];
-#pragma unroll
-    for (int i = 0; i < I; ++i) {
-        const int c = 4 * (q0 + t + kThreads * i);
-        wq[i] = (OP != OP_SOFTMAX && a.has_w && i < mine) ? ld_param4(a.w + c) : f4(1.0f);
-        bq[i] = (OP == OP_LAYERNORM && a.has_b && i < mine) ? ld_param4(a.b + c) : f4(0.0f);
     }
     __syncthreads();  // every warp has read the partials it needs
     // the last CTA to leave clears the arrival word for the next launch
